@@ -1,0 +1,25 @@
+"""fp64 CPU oracle for chunked causal linear attention (test infrastructure).
+
+Only the test-suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The CUDA library never calls it and
+shares no code with it.
+
+Every function takes numpy arrays shaped ``[B, H, T, d]`` (any float dtype; they
+are widened to float64) and per-head decays ``lam`` shaped ``[H]`` or
+``[B, H]`` (``None`` means lambda = 1), and returns float64 arrays.
+
+Parity pins: every function here is pinned in ``tests/test_oracle_pins.py``
+(exact rational examples, brute force, autograd, closed forms and invariants).
+"""
+from .oracle import (  # noqa: F401
+    build,
+    fwd_recurrent,
+    bwd_recurrent,
+    fwd_chunked,
+    bwd_chunked,
+    fwd_quadratic,
+    bwd_quadratic,
+    segment_states,
+    state_scan,
+    threads_used,
+)

@@ -1,4 +1,256 @@
 """Chunked causal linear attention for GB300 (sm_103a): Python binding of liblinattn.
 
-The binding is argument marshalling only; every step runs in the CUDA library.
+Argument marshalling only: every step of the computation runs in the CUDA
+library (``_lib/liblinattn.so``, built in-tree by ``build.py``).  PyTorch is
+used to allocate outputs and workspaces and to supply the current stream.
+There is no fallback: if the library is missing, every call raises.
+
+Low-level functions carry the C names (``linattn_fwd`` ...) and take raw
+pointers; the helpers ``fwd``, ``bwd``, ``chunk_states`` and ``state_scan``
+take torch tensors.
 """
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "liblinattn.so")
+
+OK = 0
+ERR_INVALID = -1
+ERR_UNSUPPORTED = -2
+ERR_ALIGN = -3
+ERR_WORKSPACE = -4
+ERR_CUDA = -5
+ERR_DEVICE_TIMEOUT = -6
+ERR_DEVICE = -7
+BF16, F32 = 0, 1
+OP_FWD, OP_BWD, OP_CHUNK_STATES = 1, 2, 3
+ABI_VERSION = 1
+
+
+class LinattnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: status {status} ({status_string(status)})")
+
+
+class Shape(ctypes.Structure):
+    """Mirror of ``linattn_shape`` in include/linattn.h."""
+    _fields_ = [
+        ("abi_version", ctypes.c_int32), ("B", ctypes.c_int32), ("H", ctypes.c_int32),
+        ("T", ctypes.c_int32), ("dk", ctypes.c_int32), ("dv", ctypes.c_int32),
+        ("chunk", ctypes.c_int32), ("dtype", ctypes.c_int32),
+        ("stride_b", ctypes.c_int64), ("stride_h", ctypes.c_int64), ("stride_t", ctypes.c_int64),
+        ("decay", ctypes.c_void_p),
+    ]
+
+
+_lock = threading.Lock()
+_lib = None
+_vp, _i32, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+_SIGS = {
+    "linattn_abi_version": ([], _i32),
+    "linattn_status_string": ([_i32], ctypes.c_char_p),
+    "linattn_workspace_size": ([ctypes.POINTER(Shape), _i32, _i32, ctypes.POINTER(_sz)], _i32),
+    "linattn_fwd": ([ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
+    "linattn_bwd": ([ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
+    "linattn_chunk_states": ([ctypes.POINTER(Shape), _i32, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
+    "linattn_state_scan_workspace_size": ([_i32, _i32, _i32, _i32, ctypes.POINTER(_sz)], _i32),
+    "linattn_state_scan": ([_i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
+    "linattn_device_status": ([_vp, _vp], _i32),
+    "linattn_diag_mma": ([_i32, _vp, _vp, _vp, _vp], _i32),
+}
+
+
+def lib():
+    """The loaded ctypes library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                                   "`python -m chunked_state_scan_causal_gb300.build`")
+            l = ctypes.CDLL(LIB_PATH)
+            for name, (args, res) in _SIGS.items():
+                f = getattr(l, name)
+                f.argtypes = args
+                f.restype = res
+            _lib = l
+    return _lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return lib().linattn_status_string(status).decode()
+    except RuntimeError:
+        return "?"
+
+
+# ------------------------------------------------------------------ C names (raw pointers)
+def linattn_status_string(status: int) -> str:
+    return lib().linattn_status_string(status).decode()
+
+
+def linattn_abi_version() -> int:
+    return lib().linattn_abi_version()
+
+
+def linattn_workspace_size(shape: Shape, op: int, seg_len: int = 0) -> tuple[int, int]:
+    n = _sz(0)
+    st = lib().linattn_workspace_size(ctypes.byref(shape), op, seg_len, ctypes.byref(n))
+    return st, n.value
+
+
+def linattn_fwd(shape, q, k, v, o, init_state, final_state, chunk_states, ws, ws_bytes, stream) -> int:
+    return lib().linattn_fwd(ctypes.byref(shape), q, k, v, o, init_state, final_state, chunk_states,
+                             ws, ws_bytes, stream)
+
+
+def linattn_bwd(shape, q, k, v, dO, init_state, dq, dk, dv, d_init, ws, ws_bytes, stream) -> int:
+    return lib().linattn_bwd(ctypes.byref(shape), q, k, v, dO, init_state, dq, dk, dv, d_init,
+                             ws, ws_bytes, stream)
+
+
+def linattn_chunk_states(shape, seg_len, k, v, out, ws, ws_bytes, stream) -> int:
+    return lib().linattn_chunk_states(ctypes.byref(shape), seg_len, k, v, out, ws, ws_bytes, stream)
+
+
+def linattn_state_scan_workspace_size(G, BH, dk, dv) -> tuple[int, int]:
+    n = _sz(0)
+    st = lib().linattn_state_scan_workspace_size(G, BH, dk, dv, ctypes.byref(n))
+    return st, n.value
+
+
+def linattn_state_scan(G, BH, dk, dv, seg_decay, local, init, out, total, ws, ws_bytes, stream) -> int:
+    return lib().linattn_state_scan(G, BH, dk, dv, seg_decay, local, init, out, total, ws, ws_bytes, stream)
+
+
+def linattn_device_status(ws, stream) -> int:
+    return lib().linattn_device_status(ws, stream)
+
+
+def linattn_diag_mma(mode, A, B, D, stream) -> int:
+    return lib().linattn_diag_mma(mode, A, B, D, stream)
+
+
+# ------------------------------------------------------------------ torch helpers
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(dev, stream=None):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    return s.cuda_stream
+
+
+def shape_of(q, decay=None, chunk: int = 64) -> Shape:
+    """linattn_shape for a [B, H, T, d] tensor (last dim contiguous)."""
+    import torch
+    if q.dim() != 4 or q.stride(-1) != 1:
+        raise ValueError("sequence tensors must be [B, H, T, d] with a contiguous last dimension")
+    B, H, T, d = q.shape
+    dt = {torch.bfloat16: BF16, torch.float32: F32}.get(q.dtype)
+    if dt is None:
+        raise ValueError(f"unsupported dtype {q.dtype}")
+    s = Shape()
+    s.abi_version, s.B, s.H, s.T, s.dk, s.dv, s.chunk, s.dtype = ABI_VERSION, B, H, T, d, d, chunk, dt
+    s.stride_b, s.stride_h, s.stride_t = q.stride(0), q.stride(1), q.stride(2)
+    s.decay = _ptr(decay)
+    return s
+
+
+def _same_layout(ref, *ts):
+    for t in ts:
+        if t is not None and (t.shape != ref.shape or t.stride() != ref.stride() or t.dtype != ref.dtype
+                              or t.device != ref.device):
+            raise ValueError("q, k, v (and dO, outputs) must share shape, strides, dtype and device")
+
+
+def _check(st, what):
+    if st != OK:
+        raise LinattnError(st, what)
+
+
+def workspace(q, op: int, decay=None, seg_len: int = 0):
+    import torch
+    st, n = linattn_workspace_size(shape_of(q, decay), op, seg_len)
+    _check(st, "linattn_workspace_size")
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=q.device)
+
+
+def fwd(q, k, v, decay=None, init_state=None, want_final=False, want_chunk_states=False,
+        out=None, ws=None, stream=None):
+    """o (, final_state) (, chunk_states) for q, k, v [B, H, T, d] (bf16 or fp32)."""
+    import torch
+    _same_layout(q, k, v, out)
+    B, H, T, d = q.shape
+    o = out if out is not None else torch.empty_strided(q.shape, q.stride(), dtype=q.dtype, device=q.device)
+    fin = torch.empty((B, H, d, d), dtype=torch.float32, device=q.device) if want_final else None
+    nch = (T + 63) // 64
+    cs = torch.empty((B, H, nch, d, d), dtype=torch.float32, device=q.device) if want_chunk_states else None
+    shape = shape_of(q, decay)
+    if ws is None:
+        ws = workspace(q, OP_FWD, decay)
+    st = linattn_fwd(shape, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(init_state), _ptr(fin), _ptr(cs),
+                     _ptr(ws), ws.numel(), _stream(q.device, stream))
+    _check(st, "linattn_fwd")
+    return o, fin, cs
+
+
+def bwd(q, k, v, dO, decay=None, init_state=None, want_dinit=False, outs=None, ws=None, stream=None):
+    """(dq, dk, dv, d_init or None) for the upstream gradient dO."""
+    import torch
+    _same_layout(q, k, v, dO)
+    B, H, T, d = q.shape
+    if outs is None:
+        outs = [torch.empty_strided(q.shape, q.stride(), dtype=q.dtype, device=q.device) for _ in range(3)]
+    dq, dk, dv = outs
+    dinit = torch.empty((B, H, d, d), dtype=torch.float32, device=q.device) if want_dinit else None
+    shape = shape_of(q, decay)
+    if ws is None:
+        ws = workspace(q, OP_BWD, decay)
+    st = linattn_bwd(shape, _ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(init_state), _ptr(dq), _ptr(dk),
+                     _ptr(dv), _ptr(dinit), _ptr(ws), ws.numel(), _stream(q.device, stream))
+    _check(st, "linattn_bwd")
+    return dq, dk, dv, dinit
+
+
+def chunk_states(k, v, seg_len: int, decay=None, out=None, ws=None, stream=None):
+    """Segment-local states [G, B, H, d, d] (fp32) for G = T / seg_len segments."""
+    import torch
+    _same_layout(k, v)
+    B, H, T, d = k.shape
+    G = T // seg_len if seg_len > 0 else 0
+    out = out if out is not None else torch.empty((G, B, H, d, d), dtype=torch.float32, device=k.device)
+    if ws is None:
+        ws = workspace(k, OP_CHUNK_STATES, decay, seg_len)
+    st = linattn_chunk_states(shape_of(k, decay), seg_len, _ptr(k), _ptr(v), _ptr(out), _ptr(ws), ws.numel(),
+                              _stream(k.device, stream))
+    _check(st, "linattn_chunk_states")
+    return out
+
+
+def state_scan(local, seg_decay=None, init=None, want_total=False, out=None, ws=None, stream=None):
+    """Exclusive scan over the leading axis of local [G, *BH, dk, dv] (fp32)."""
+    import torch
+    G, dk, dv = local.shape[0], local.shape[-2], local.shape[-1]
+    BH = local[0].numel() // (dk * dv)
+    if not local.is_contiguous() or local.dtype != torch.float32:
+        raise ValueError("local states must be contiguous fp32")
+    out = out if out is not None else torch.empty_like(local)
+    total = torch.empty(local.shape[1:], dtype=torch.float32, device=local.device) if want_total else None
+    if ws is None:
+        st, n = linattn_state_scan_workspace_size(G, BH, dk, dv)
+        _check(st, "linattn_state_scan_workspace_size")
+        ws = torch.empty(n, dtype=torch.uint8, device=local.device)
+    st = linattn_state_scan(G, BH, dk, dv, _ptr(seg_decay), _ptr(local), _ptr(init), _ptr(out), _ptr(total),
+                            _ptr(ws), ws.numel(), _stream(local.device, stream))
+    _check(st, "linattn_state_scan")
+    return out, total
+
+
+def device_status(ws, stream=None) -> int:
+    return linattn_device_status(_ptr(ws), _stream(ws.device, stream))

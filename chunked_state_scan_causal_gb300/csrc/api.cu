@@ -1,0 +1,331 @@
+// C-ABI entry points of liblinattn: argument validation, workspace layout,
+// TMA descriptor encoding and the choice between the tensor-core pipeline
+// (bf16, d = 128) and the CUDA-core kernels (fp32 inputs, d = 64, per-chunk
+// state outputs).  Every error is detected here before anything is enqueued.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "../../include/linattn.h"
+#include "internal.h"
+
+namespace linattn {
+
+// ------------------------------------------------------------------ device checks
+static int device_ok() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return LINATTN_ERR_CUDA;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return LINATTN_ERR_CUDA;
+  return (major == 10 && minor == 3) ? LINATTN_OK : LINATTN_ERR_DEVICE;
+}
+
+static int num_sms() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
+
+// ------------------------------------------------------------------ tensor maps
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool make_tmap_bf16(void *map, const void *base, const uint64_t dims[4], const uint64_t strides[3]) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t gd[4] = {dims[0], dims[1], dims[2], dims[3]};
+  cuuint64_t gs[3] = {strides[0], strides[1], strides[2]};
+  cuuint32_t box[4] = {64, 128, 1, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = fn(reinterpret_cast<CUtensorMap *>(map), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                  const_cast<void *>(base), gd, gs, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------------ validation
+static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static int validate(const linattn_shape *s, Problem *p) {
+  if (!s) return LINATTN_ERR_INVALID;
+  if (s->abi_version != LINATTN_ABI_VERSION) return LINATTN_ERR_INVALID;
+  if (s->B < 1 || s->H < 1 || s->T < 0 || s->dk < 1 || s->dv < 1 || s->chunk < 1)
+    return LINATTN_ERR_INVALID;
+  if (s->dtype != LINATTN_BF16 && s->dtype != LINATTN_F32) return LINATTN_ERR_INVALID;
+  // an empty sequence reads nothing, so its strides are not checked
+  if (s->T > 0 && (s->stride_b < 1 || s->stride_h < 1 || s->stride_t < s->dk)) return LINATTN_ERR_INVALID;
+  if (s->chunk != 64) return LINATTN_ERR_UNSUPPORTED;
+  if (s->dk != s->dv || (s->dk != 64 && s->dk != 128)) return LINATTN_ERR_UNSUPPORTED;
+  const int64_t esz = s->dtype == LINATTN_BF16 ? 2 : 4;
+  if (s->T > 0 && ((s->stride_t * esz) % 16 || (s->stride_h * esz) % 16 || (s->stride_b * esz) % 16))
+    return LINATTN_ERR_ALIGN;
+  if ((int64_t)s->B * s->H > (1 << 30)) return LINATTN_ERR_UNSUPPORTED;
+  p->B = s->B;
+  p->H = s->H;
+  p->T = s->T;
+  p->d = s->dk;
+  p->dtype = s->dtype == LINATTN_BF16 ? 0 : 1;
+  p->sb = s->stride_b;
+  p->sh = s->stride_h;
+  p->st = s->stride_t;
+  p->decay = s->decay;
+  p->num_sms = num_sms();
+  return LINATTN_OK;
+}
+
+static int check_ptrs(std::initializer_list<const void *> required, std::initializer_list<const void *> optional) {
+  for (const void *x : required) {
+    if (!x) return LINATTN_ERR_INVALID;
+    if (!aligned16(x)) return LINATTN_ERR_ALIGN;
+  }
+  for (const void *x : optional)
+    if (x && !aligned16(x)) return LINATTN_ERR_ALIGN;
+  return LINATTN_OK;
+}
+
+static int cuda_status(cudaError_t e) { return e == cudaSuccess ? LINATTN_OK : LINATTN_ERR_CUDA; }
+
+// ------------------------------------------------------------------ workspace layout
+constexpr size_t kHeader = 256;  // int32 status word at offset 0
+
+struct FwdLayout {
+  int G = 0, L = 0;
+  size_t agg = 0, states = 0, scan = 0, total = kHeader;
+};
+static FwdLayout fwd_layout(const Problem &p) {
+  FwdLayout w;
+  if (!tc_supported(p) || p.T == 0) return w;
+  w.L = tc_group_len(p);
+  w.G = (p.T + w.L - 1) / w.L;
+  const size_t st = (size_t)w.G * p.B * p.H * p.d * p.d * sizeof(float);
+  w.agg = kHeader;
+  w.states = w.agg + align256(st);
+  w.scan = w.states + align256(st);
+  w.total = w.scan + scan_workspace_bytes(w.G, (int64_t)p.B * p.H * p.d * p.d);
+  return w;
+}
+struct BwdLayout {
+  FwdLayout f;            // forward states (aggregate of k v^T, exclusive scan)
+  size_t wagg = 0, rbar = 0, total = kHeader;
+};
+static BwdLayout bwd_layout(const Problem &p) {
+  BwdLayout w;
+  w.f = fwd_layout(p);
+  if (w.f.G == 0) return w;
+  const size_t st = (size_t)w.f.G * p.B * p.H * p.d * p.d * sizeof(float);
+  w.wagg = w.f.total;
+  w.rbar = w.wagg + align256(st);
+  w.total = w.rbar + align256(st);
+  return w;
+}
+
+static int check_ws(void *ws, size_t bytes, size_t need) {
+  if (!ws) return LINATTN_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return LINATTN_ERR_WORKSPACE;
+  if (bytes < need) return LINATTN_ERR_WORKSPACE;
+  return LINATTN_OK;
+}
+
+}  // namespace linattn
+
+using namespace linattn;
+
+extern "C" {
+
+int32_t linattn_abi_version(void) { return LINATTN_ABI_VERSION; }
+
+const char *linattn_status_string(int32_t s) {
+  switch (s) {
+    case LINATTN_OK: return "ok";
+    case LINATTN_ERR_INVALID: return "invalid argument";
+    case LINATTN_ERR_UNSUPPORTED: return "unsupported shape or option";
+    case LINATTN_ERR_ALIGN: return "pointer or stride not 16-byte aligned";
+    case LINATTN_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+    case LINATTN_ERR_CUDA: return "CUDA call failed";
+    case LINATTN_ERR_DEVICE_TIMEOUT: return "device-side bounded wait timed out";
+    case LINATTN_ERR_DEVICE: return "current device is not sm_103";
+    default: return "unknown status";
+  }
+}
+
+int32_t linattn_workspace_size(const linattn_shape *shape, int32_t op, int32_t seg_len, size_t *bytes) {
+  if (!bytes) return LINATTN_ERR_INVALID;
+  Problem p;
+  int st = validate(shape, &p);
+  if (st) return st;
+  if (op == LINATTN_OP_FWD) {
+    *bytes = fwd_layout(p).total;
+  } else if (op == LINATTN_OP_BWD) {
+    *bytes = bwd_layout(p).total;
+  } else if (op == LINATTN_OP_CHUNK_STATES) {
+    if (seg_len < 1) return LINATTN_ERR_INVALID;
+    *bytes = kHeader;
+  } else {
+    return LINATTN_ERR_INVALID;
+  }
+  return LINATTN_OK;
+}
+
+int32_t linattn_fwd(const linattn_shape *shape, const void *q, const void *k, const void *v, void *o,
+                    const float *init_state, float *final_state, float *chunk_states, void *workspace,
+                    size_t workspace_bytes, void *stream) {
+  Problem p;
+  int st = validate(shape, &p);
+  if (st) return st;
+  if (p.T > 0 && (st = check_ptrs({q, k, v, o}, {}))) return st;
+  if ((st = check_ptrs({}, {init_state, final_state, chunk_states}))) return st;
+  const FwdLayout w = fwd_layout(p);
+  if ((st = check_ws(workspace, workspace_bytes, w.total))) return st;
+  if ((st = device_ok())) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char *ws = static_cast<char *>(workspace);
+  int *status = reinterpret_cast<int *>(ws);
+  if (cudaMemsetAsync(ws, 0, kHeader, s) != cudaSuccess) return LINATTN_ERR_CUDA;
+  const int64_t BH = (int64_t)p.B * p.H;
+  const size_t state_bytes = (size_t)BH * p.d * p.d * sizeof(float);
+  if (p.T == 0) {
+    if (final_state) {
+      cudaError_t e = init_state ? cudaMemcpyAsync(final_state, init_state, state_bytes,
+                                                   cudaMemcpyDeviceToDevice, s)
+                                 : cudaMemsetAsync(final_state, 0, state_bytes, s);
+      return cuda_status(e);
+    }
+    return LINATTN_OK;
+  }
+  if (chunk_states || !tc_supported(p))
+    return cuda_status(simt_fwd(p, q, k, v, o, init_state, final_state, chunk_states, s));
+  // tensor-core pipeline: group aggregates -> exclusive scan -> per-group forward
+  float *agg = reinterpret_cast<float *>(ws + w.agg);
+  float *states = reinterpret_cast<float *>(ws + w.states);
+  cudaError_t e = tc_segment_states(p, w.L, k, v, false, agg, status, s);
+  if (e == cudaSuccess)
+    e = state_scan(w.G, (int)BH, p.d * p.d, nullptr, p.decay, p.H, w.L, false, agg, init_state,
+                   states, nullptr, ws + w.scan, status, s);
+  if (e == cudaSuccess) e = tc_main(p, w.L, false, q, k, v, o, states, false, final_state, status, s);
+  return cuda_status(e);
+}
+
+int32_t linattn_bwd(const linattn_shape *shape, const void *q, const void *k, const void *v,
+                    const void *dO, const float *init_state, void *dq, void *dk, void *dv,
+                    float *d_init_state, void *workspace, size_t workspace_bytes, void *stream) {
+  Problem p;
+  int st = validate(shape, &p);
+  if (st) return st;
+  if (p.T > 0 && (st = check_ptrs({q, k, v, dO, dq, dk, dv}, {}))) return st;
+  if ((st = check_ptrs({}, {init_state, d_init_state}))) return st;
+  const BwdLayout w = bwd_layout(p);
+  if ((st = check_ws(workspace, workspace_bytes, w.total))) return st;
+  if ((st = device_ok())) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char *ws = static_cast<char *>(workspace);
+  int *status = reinterpret_cast<int *>(ws);
+  if (cudaMemsetAsync(ws, 0, kHeader, s) != cudaSuccess) return LINATTN_ERR_CUDA;
+  const int64_t BH = (int64_t)p.B * p.H;
+  const size_t state_bytes = (size_t)BH * p.d * p.d * sizeof(float);
+  if (p.T == 0) {
+    if (d_init_state) return cuda_status(cudaMemsetAsync(d_init_state, 0, state_bytes, s));
+    return LINATTN_OK;
+  }
+  if (!tc_supported(p))
+    return cuda_status(simt_bwd(p, q, k, v, dO, init_state, dq, dk, dv, d_init_state, s));
+  const int L = w.f.L, G = w.f.G;
+  float *agg = reinterpret_cast<float *>(ws + w.f.agg);
+  float *states = reinterpret_cast<float *>(ws + w.f.states);
+  float *wagg = reinterpret_cast<float *>(ws + w.wagg);
+  float *rbar = reinterpret_cast<float *>(ws + w.rbar);
+  // forward group states (recomputed from k, v and init)
+  cudaError_t e = tc_segment_states(p, L, k, v, false, agg, status, s);
+  if (e == cudaSuccess)
+    e = state_scan(G, (int)BH, p.d * p.d, nullptr, p.decay, p.H, L, false, agg, init_state, states,
+                   nullptr, ws + w.f.scan, status, s);
+  // dq: the forward kernel with (q, k, v) := (dO, v, k) and the transposed states
+  if (e == cudaSuccess) e = tc_main(p, L, false, dO, v, k, dq, states, true, nullptr, status, s);
+  // reverse group states Rbar = sum_{u > group end} lambda^{u-end} q_u dO_u^T, scanned from the
+  // end; the value one step before the start is d_init = sum_t lambda^{t+1} q_t dO_t^T
+  if (e == cudaSuccess) e = tc_segment_states(p, L, q, dO, true, wagg, status, s);
+  if (e == cudaSuccess)
+    e = state_scan(G, (int)BH, p.d * p.d, nullptr, p.decay, p.H, L, true, wagg, nullptr, rbar,
+                   d_init_state, ws + w.f.scan, status, s);
+  // dv: reverse-time kernel with (q, k, v) := (k, q, dO), state Rbar
+  if (e == cudaSuccess) e = tc_main(p, L, true, k, q, dO, dv, rbar, false, nullptr, status, s);
+  // dk: reverse-time kernel with (q, k, v) := (v, dO, q), state Rbar^T
+  if (e == cudaSuccess) e = tc_main(p, L, true, v, dO, q, dk, rbar, true, nullptr, status, s);
+  return cuda_status(e);
+}
+
+int32_t linattn_chunk_states(const linattn_shape *shape, int32_t seg_len, const void *k, const void *v,
+                             float *local_states, void *workspace, size_t workspace_bytes, void *stream) {
+  Problem p;
+  int st = validate(shape, &p);
+  if (st) return st;
+  if (seg_len < 1) return LINATTN_ERR_INVALID;
+  if (p.T < 1 || p.T % seg_len) return LINATTN_ERR_UNSUPPORTED;
+  if ((st = check_ptrs({k, v, local_states}, {}))) return st;
+  if ((st = check_ws(workspace, workspace_bytes, kHeader))) return st;
+  if ((st = device_ok())) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int *status = reinterpret_cast<int *>(workspace);
+  if (cudaMemsetAsync(workspace, 0, kHeader, s) != cudaSuccess) return LINATTN_ERR_CUDA;
+  if (tc_supported(p) && seg_len % 128 == 0)
+    return cuda_status(tc_segment_states(p, seg_len, k, v, false, local_states, status, s));
+  return cuda_status(simt_segment_states(p, seg_len, k, v, local_states, s));
+}
+
+int32_t linattn_state_scan_workspace_size(int32_t G, int32_t BH, int32_t dk, int32_t dv, size_t *bytes) {
+  if (!bytes || G < 1 || BH < 1 || dk < 1 || dv < 1) return LINATTN_ERR_INVALID;
+  if (((int64_t)dk * dv) % 8) return LINATTN_ERR_UNSUPPORTED;
+  *bytes = kHeader + scan_workspace_bytes(G, (int64_t)BH * dk * dv);
+  return LINATTN_OK;
+}
+
+int32_t linattn_state_scan(int32_t G, int32_t BH, int32_t dk, int32_t dv, const float *seg_decay,
+                           const float *local_states, const float *init, float *init_states,
+                           float *total, void *workspace, size_t workspace_bytes, void *stream) {
+  size_t need = 0;
+  int st = linattn_state_scan_workspace_size(G, BH, dk, dv, &need);
+  if (st) return st;
+  if ((st = check_ptrs({local_states, init_states}, {seg_decay, init, total}))) return st;
+  if ((st = check_ws(workspace, workspace_bytes, need))) return st;
+  if ((st = device_ok())) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char *ws = static_cast<char *>(workspace);
+  if (cudaMemsetAsync(ws, 0, kHeader, s) != cudaSuccess) return LINATTN_ERR_CUDA;
+  return cuda_status(state_scan(G, BH, dk * dv, seg_decay, nullptr, 1, 1, false, local_states, init,
+                                init_states, total, ws + kHeader, reinterpret_cast<int *>(ws), s));
+}
+
+int32_t linattn_device_status(const void *workspace, void *stream) {
+  if (!workspace) return LINATTN_ERR_INVALID;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int h = 0;
+  if (cudaMemcpyAsync(&h, workspace, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return LINATTN_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return LINATTN_ERR_CUDA;
+  return h;
+}
+
+int32_t linattn_diag_mma(int32_t mode, const void *A, const void *B, float *D, void *stream) {
+  if (mode < 0 || mode > 4) return LINATTN_ERR_INVALID;
+  int st = check_ptrs({A, B, D}, {});
+  if (st) return st;
+  if ((st = device_ok())) return st;
+  return cuda_status(diag_mma(mode, A, B, D, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,65 @@
+// Internal declarations shared by the host entry points and the kernel files.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace linattn {
+
+// A validated request.  Sequence tensors are [B, H, T, d] with element strides
+// (sb, sh, st); states are [B*H, d, d] fp32.
+struct Problem {
+  int B, H, T, d;
+  int dtype;            // 0 bf16, 1 fp32
+  int64_t sb, sh, st;   // element strides
+  const float *decay;   // [H] device, or nullptr (lambda = 1)
+  int num_sms;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// ---------------------------------------------------------------- SIMT path (simt.cu)
+cudaError_t simt_fwd(const Problem &p, const void *q, const void *k, const void *v, void *o,
+                     const float *init, float *final_state, float *chunk_states, cudaStream_t s);
+cudaError_t simt_bwd(const Problem &p, const void *q, const void *k, const void *v, const void *dO,
+                     const float *init, void *dq, void *dk, void *dv, float *dinit, cudaStream_t s);
+cudaError_t simt_segment_states(const Problem &p, int seg_len, const void *k, const void *v,
+                                float *out, cudaStream_t s);
+
+// ---------------------------------------------------------------- state scan (scan.cu)
+// Exclusive scan over G segments of E = BH * DD fp32 elements each ([G][BH][DD]).
+// Per-(bh) multiplier: seg_decay[bh] if given; else decay_h[bh % H]^seg_len if
+// decay_h is given; else 1.  reverse: scan from g = G-1 down to 0 (out[G-1] =
+// init, out[g] = a * out[g+1] + local[g+1]).  total (optional) is the value one
+// step past the end.
+size_t scan_workspace_bytes(int G, int64_t E);
+cudaError_t state_scan(int G, int BH, int DD, const float *seg_decay, const float *decay_h, int H,
+                       int seg_len, bool reverse, const float *local, const float *init, float *out,
+                       float *total, void *ws, int *status, cudaStream_t s);
+
+// ---------------------------------------------------------------- tensor-core path (tc.cu)
+bool tc_supported(const Problem &p);   // bf16, d = 128
+int tc_group_len(const Problem &p);    // tokens per chunk group (multiple of 128)
+// Segment aggregates sum_s w_s x_s y_s^T over groups of seg_len tokens (seg_len
+// a multiple of 128), written as [G][BH][d][d] fp32.
+//   reverse == false: w_s = lambda^{end - s};  reverse == true: w_s = lambda^{s - start + 1}.
+cudaError_t tc_segment_states(const Problem &p, int seg_len, const void *X, const void *Y, bool reverse,
+                              float *out, int *status, cudaStream_t s);
+// Per-group chunked attention from the given group states [G][BH][d][d] (read
+// transposed when init_transposed).  reverse == false: causal, state entering
+// the group, o_i += lambda^{i+1} S^T q_i.  reverse == true: anti-causal, blocks
+// walked from the end, state = sum_{s > group end} lambda^{s - end} k_s v_s^T.
+// final_state (optional, forward only) is the state after the last token.
+cudaError_t tc_main(const Problem &p, int group_len, bool reverse, const void *q, const void *k,
+                    const void *v, void *o, const float *group_init, bool init_transposed,
+                    float *final_state, int *status, cudaStream_t s);
+
+// ---------------------------------------------------------------- TMA descriptors (api.cu)
+// 4-D bf16 tiled tensor map, dims innermost first, strides in bytes for dims 1..3,
+// box {64, 128, 1, 1} with the 128-byte swizzle (the SW128 tile half).
+bool make_tmap_bf16(void *map, const void *base, const uint64_t dims[4], const uint64_t strides[3]);
+
+// ---------------------------------------------------------------- diagnostics (diag.cu)
+cudaError_t diag_mma(int mode, const void *A, const void *B, float *D, cudaStream_t s);
+
+}  // namespace linattn

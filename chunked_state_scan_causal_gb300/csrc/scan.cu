@@ -1,0 +1,226 @@
+// Exclusive prefix scan of fp32 segment states -- the single-GPU counterpart
+// of the All-Scan that hands every sequence-parallel rank exactly its initial
+// state ("ZeCO: Zero Communication Overhead Sequence Parallelism for Linear
+// Attention", abstract) and of LASP-2's one gather of length-independent
+// memory states followed by a local combine ("LASP-2", abstract).
+//
+//   out[0] = init,  out[g] = a * out[g-1] + U[g-1]     (a = lambda^L per sequence)
+//
+// The combine of two neighbouring pieces is affine: (a2, X2) o (a1, X1) =
+// (a1 a2, a2 X1 + X2), so the scan is associative and runs in parallel:
+//  * a tile is 32 consecutive segments x 8 consecutive state elements; one
+//    warp owns a tile, lane l holds segment l's 8 elements (one 32-byte
+//    sector per lane, so every warp load is sector-complete);
+//  * inside the tile: Kogge-Stone inclusive scan with warp shuffles;
+//  * across tiles: decoupled look-back.  Tiles are taken from an atomic
+//    ticket in segment-tile-major order, so every predecessor of a waiting
+//    tile is already running; each tile publishes its aggregate at once and
+//    its inclusive prefix after the look-back; waits are bounded.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace linattn {
+namespace {
+
+constexpr int kWarps = 8;
+constexpr int kVec = 8;  // fp32 elements per lane
+
+struct ScanArgs {
+  int G, BH, DD, H, seg_len, ntg, ncg, reverse;
+  const float *seg_decay, *decay_h, *local, *init;
+  float *out, *total;
+  unsigned *counter;  // ticket counter (zeroed before launch)
+  unsigned *flags;    // [ntg * ncg] 0 empty, 1 aggregate, 2 inclusive (zeroed before launch)
+  float *agg, *incl;  // [ntg * ncg][kVec]
+  int *status;
+};
+
+__device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release(unsigned *p, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__global__ void __launch_bounds__(kWarps * 32) scan_kernel(ScanArgs A) {
+  const int lane = threadIdx.x & 31;
+  const int64_t E = (int64_t)A.BH * A.DD;
+  const unsigned ntiles = (unsigned)A.ntg * (unsigned)A.ncg;
+  while (true) {
+    unsigned ticket = 0;
+    if (lane == 0) ticket = atomicAdd(A.counter, 1u);
+    ticket = __shfl_sync(0xffffffffu, ticket, 0);
+    if (ticket >= ntiles) break;
+    const int tg = (int)(ticket / A.ncg), cg = (int)(ticket % A.ncg);
+    const int64_t e0 = (int64_t)cg * kVec;
+    const int bh = (int)(e0 / A.DD);
+    float a = 1.f;
+    if (A.seg_decay) a = A.seg_decay[bh];
+    else if (A.decay_h) a = (float)pow((double)A.decay_h[bh % A.H], (double)A.seg_len);
+
+    // processing index p = tg*32 + lane; segment g = p (forward) or G-1-p (reverse)
+    const int pidx = tg * 32 + lane;
+    const bool valid = pidx < A.G;
+    const int g = A.reverse ? A.G - 1 - pidx : pidx;
+    float x[kVec];
+    if (valid) {
+      const float4 *src = reinterpret_cast<const float4 *>(A.local + (int64_t)g * E + e0);
+      const float4 u0 = __ldg(src), u1 = __ldg(src + 1);
+      x[0] = u0.x; x[1] = u0.y; x[2] = u0.z; x[3] = u0.w;
+      x[4] = u1.x; x[5] = u1.y; x[6] = u1.z; x[7] = u1.w;
+    } else {
+#pragma unroll
+      for (int i = 0; i < kVec; ++i) x[i] = 0.f;
+    }
+    // inclusive scan inside the tile: X_l = sum_{m<=l} a^{l-m} U_m
+    float ad = a;  // a^d
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+#pragma unroll
+      for (int i = 0; i < kVec; ++i) {
+        const float y = __shfl_up_sync(0xffffffffu, x[i], d);
+        if (lane >= d) x[i] = fmaf(ad, y, x[i]);
+      }
+      ad *= ad;
+    }
+    const float a32 = ad;  // a^32
+    // prefix entering the tile (state after all earlier segments, incl. init)
+    float pin[kVec];
+    if (tg == 0) {
+#pragma unroll
+      for (int i = 0; i < kVec; ++i) pin[i] = A.init ? __ldg(A.init + e0 + i) : 0.f;
+    } else {
+      // publish the aggregate, then look back
+      if (lane == 31) {
+        float4 *dst = reinterpret_cast<float4 *>(A.agg + (int64_t)ticket * kVec);
+        dst[0] = make_float4(x[0], x[1], x[2], x[3]);
+        dst[1] = make_float4(x[4], x[5], x[6], x[7]);
+        __threadfence();
+        st_release(A.flags + ticket, 1u);
+      }
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < kVec; ++i) pin[i] = 0.f;
+      float fac = 1.f;
+      int pred = tg - 1;
+      bool failed = false;
+      while (true) {
+        const unsigned pt = (unsigned)pred * A.ncg + cg;
+        unsigned f = 0;
+        if (lane == 0) {
+          f = ld_acquire(A.flags + pt);
+          if (f == 0) {
+            const uint64_t t0 = globaltimer_ns();
+            while ((f = ld_acquire(A.flags + pt)) == 0) {
+              if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                report_error(A.status, -6);
+                f = 3;  // give up: treat as an inclusive prefix of zeros
+                break;
+              }
+            }
+          }
+        }
+        f = __shfl_sync(0xffffffffu, f, 0);
+        if (f == 3) { failed = true; break; }
+        const float *src = (f == 2 ? A.incl : A.agg) + (int64_t)pt * kVec;
+#pragma unroll
+        for (int i = 0; i < kVec; ++i) pin[i] = fmaf(fac, __ldcg(src + i), pin[i]);
+        if (f == 2) break;
+        fac *= a32;
+        if (--pred < 0) {
+          // reached the first tile without an inclusive prefix: add the decayed init
+          if (A.init) {
+#pragma unroll
+            for (int i = 0; i < kVec; ++i) pin[i] = fmaf(fac, __ldg(A.init + e0 + i), pin[i]);
+          }
+          break;
+        }
+      }
+      (void)failed;
+    }
+    // publish the inclusive prefix of this tile
+    if (tg + 1 < A.ntg && lane == 31) {
+      float4 *dst = reinterpret_cast<float4 *>(A.incl + (int64_t)ticket * kVec);
+      float v[kVec];
+#pragma unroll
+      for (int i = 0; i < kVec; ++i) v[i] = fmaf(a32, pin[i], x[i]);
+      dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+      dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+      __threadfence();
+      st_release(A.flags + ticket, 2u);
+    }
+    // exclusive outputs: out[p] = X_{l-1} + a^l * pin
+    float al = 1.f;  // a^lane
+    {
+      float base = a;
+      int n = lane;
+#pragma unroll 1
+      while (n) {
+        if (n & 1) al *= base;
+        base *= base;
+        n >>= 1;
+      }
+    }
+    float ex[kVec];
+#pragma unroll
+    for (int i = 0; i < kVec; ++i) {
+      const float y = __shfl_up_sync(0xffffffffu, x[i], 1);
+      ex[i] = fmaf(al, pin[i], lane == 0 ? 0.f : y);
+    }
+    if (valid) {
+      float4 *dst = reinterpret_cast<float4 *>(A.out + (int64_t)g * E + e0);
+      dst[0] = make_float4(ex[0], ex[1], ex[2], ex[3]);
+      dst[1] = make_float4(ex[4], ex[5], ex[6], ex[7]);
+      if (A.total && pidx == A.G - 1) {
+        // value one step past the end: a * out[last] + U[last] = X_l + a^{l+1} pin
+        float4 *tt = reinterpret_cast<float4 *>(A.total + e0);
+        float v[kVec];
+#pragma unroll
+        for (int i = 0; i < kVec; ++i) v[i] = fmaf(al * a, pin[i], x[i]);
+        tt[0] = make_float4(v[0], v[1], v[2], v[3]);
+        tt[1] = make_float4(v[4], v[5], v[6], v[7]);
+      }
+    }
+  }
+}
+
+}  // namespace
+
+size_t scan_workspace_bytes(int G, int64_t E) {
+  const int64_t ntg = (G + 31) / 32, ncg = E / kVec;
+  const int64_t nt = ntg * ncg;
+  return align256(256 + nt * 4) + 2 * align256(nt * kVec * 4);
+}
+
+cudaError_t state_scan(int G, int BH, int DD, const float *seg_decay, const float *decay_h, int H,
+                       int seg_len, bool reverse, const float *local, const float *init, float *out,
+                       float *total, void *ws, int *status, cudaStream_t s) {
+  const int64_t E = (int64_t)BH * DD;
+  ScanArgs A;
+  A.G = G; A.BH = BH; A.DD = DD; A.H = H; A.seg_len = seg_len;
+  A.ntg = (G + 31) / 32;
+  A.ncg = (int)(E / kVec);
+  A.reverse = reverse ? 1 : 0;
+  A.seg_decay = seg_decay; A.decay_h = decay_h; A.local = local; A.init = init;
+  A.out = out; A.total = total; A.status = status;
+  const int64_t nt = (int64_t)A.ntg * A.ncg;
+  char *w = static_cast<char *>(ws);
+  A.counter = reinterpret_cast<unsigned *>(w);
+  A.flags = reinterpret_cast<unsigned *>(w + 256);
+  const size_t head = align256(256 + nt * 4);
+  A.agg = reinterpret_cast<float *>(w + head);
+  A.incl = reinterpret_cast<float *>(w + head + align256(nt * kVec * 4));
+  cudaError_t e = cudaMemsetAsync(w, 0, head, s);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t want = (nt + kWarps - 1) / kWarps;
+  const int grid = (int)(want < (int64_t)sms * 8 ? want : (int64_t)sms * 8);
+  scan_kernel<<<grid, kWarps * 32, 0, s>>>(A);
+  return cudaGetLastError();
+}
+
+}  // namespace linattn

@@ -1,0 +1,332 @@
+// CUDA-core (SIMT) kernels in fp32 arithmetic: the path for fp32 inputs, for
+// head dimension 64, and for requests of per-chunk states.  One CTA walks one
+// (batch, head) sequence chunk by chunk (chunk = 64 tokens), in the order the
+// chunked method states it: masked attention inside the chunk, query times the
+// running state across chunks, then the state update ("Lightning Attention-2"
+// entry and abstract of the LASP-2 page).  All tiles live in shared memory
+// with a padded row stride (d + 1) so that column walks are bank-conflict free.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+
+namespace linattn {
+namespace {
+
+constexpr int kC = 64;          // chunk length
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ float ld_elem(const float *p) { return *p; }
+__device__ __forceinline__ float ld_elem(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
+__device__ __forceinline__ void st_elem(float *p, float x) { *p = x; }
+__device__ __forceinline__ void st_elem(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
+
+// pw[k] = lambda^k for k = 0..kC, by repeated multiplication in double.
+__device__ void fill_powers(float *pw, float lam) {
+  if (threadIdx.x == 0) {
+    double x = 1.0;
+    for (int i = 0; i <= kC; ++i) {
+      pw[i] = (float)x;
+      x *= (double)lam;
+    }
+  }
+}
+
+// Load rows [c0, c0+n) of one head into a [kC][D+1] fp32 tile; rows >= n are zero.
+template <int D, typename TIn>
+__device__ void load_tile(float *tile, const TIn *base, int64_t st, int c0, int n) {
+  for (int e = threadIdx.x; e < kC * D; e += kThreads) {
+    const int r = e / D, c = e % D;
+    tile[r * (D + 1) + c] = r < n ? ld_elem(base + (int64_t)(c0 + r) * st + c) : 0.f;
+  }
+}
+
+// ------------------------------------------------------------------ forward
+template <int D, typename TIn>
+__global__ void __launch_bounds__(kThreads) simt_fwd_kernel(Problem p, const TIn *q, const TIn *k,
+                                                            const TIn *v, TIn *o, const float *init,
+                                                            float *final_state, float *chunk_states) {
+  extern __shared__ float sm[];
+  constexpr int LD = D + 1;
+  float *S = sm;                 // [D][LD]
+  float *Q = S + D * LD;         // [kC][LD]
+  float *K = Q + kC * LD;
+  float *V = K + kC * LD;
+  float *P = V + kC * LD;        // [kC][kC]
+  float *pw = P + kC * kC;       // [kC + 1]
+
+  const int bh = blockIdx.x, b = bh / p.H, h = bh % p.H;
+  const int64_t off = (int64_t)b * p.sb + (int64_t)h * p.sh;
+  const float lam = p.decay ? p.decay[h] : 1.f;
+  fill_powers(pw, lam);
+  for (int e = threadIdx.x; e < D * D; e += kThreads)
+    S[(e / D) * LD + e % D] = init ? init[(int64_t)bh * D * D + e] : 0.f;
+  __syncthreads();
+
+  const int nchunk = (p.T + kC - 1) / kC;
+  for (int c = 0; c < nchunk; ++c) {
+    const int c0 = c * kC, n = min(kC, p.T - c0);
+    if (chunk_states) {
+      float *cs = chunk_states + ((int64_t)bh * nchunk + c) * D * D;
+      for (int e = threadIdx.x; e < D * D; e += kThreads) cs[e] = S[(e / D) * LD + e % D];
+    }
+    load_tile<D>(Q, q + off, p.st, c0, n);
+    load_tile<D>(K, k + off, p.st, c0, n);
+    load_tile<D>(V, v + off, p.st, c0, n);
+    __syncthreads();
+    // intra-chunk scores with the causal decay mask
+    for (int e = threadIdx.x; e < kC * kC; e += kThreads) {
+      const int i = e / kC, j = e % kC;
+      float s = 0.f;
+      if (j <= i) {
+        for (int a = 0; a < D; ++a) s = fmaf(Q[i * LD + a], K[j * LD + a], s);
+        s *= pw[i - j];
+      }
+      P[e] = s;
+    }
+    __syncthreads();
+    // outputs: lambda^{i+1} S^T q_i + sum_j P_ij v_j
+    for (int e = threadIdx.x; e < kC * D; e += kThreads) {
+      const int i = e / D, bb = e % D;
+      if (i >= n) continue;
+      float inter = 0.f, intra = 0.f;
+      for (int a = 0; a < D; ++a) inter = fmaf(Q[i * LD + a], S[a * LD + bb], inter);
+      for (int j = 0; j <= i; ++j) intra = fmaf(P[i * kC + j], V[j * LD + bb], intra);
+      st_elem(o + off + (int64_t)(c0 + i) * p.st + bb, fmaf(pw[i + 1], inter, intra));
+    }
+    __syncthreads();
+    // state update: S <- lambda^n S + sum_j lambda^{n-1-j} k_j v_j^T
+    for (int e = threadIdx.x; e < D * D; e += kThreads) {
+      const int a = e / D, bb = e % D;
+      float acc = 0.f;
+      for (int j = 0; j < n; ++j) acc = fmaf(pw[n - 1 - j] * K[j * LD + a], V[j * LD + bb], acc);
+      S[a * LD + bb] = fmaf(pw[n], S[a * LD + bb], acc);
+    }
+    __syncthreads();
+  }
+  if (final_state)
+    for (int e = threadIdx.x; e < D * D; e += kThreads)
+      final_state[(int64_t)bh * D * D + e] = S[(e / D) * LD + e % D];
+}
+
+// ------------------------------------------------------------------ backward
+template <int D, typename TIn>
+__global__ void __launch_bounds__(kThreads) simt_bwd_kernel(Problem p, const TIn *q, const TIn *k,
+                                                            const TIn *v, const TIn *dO,
+                                                            const float *init, TIn *dq, TIn *dk,
+                                                            TIn *dv, float *dinit) {
+  extern __shared__ float sm[];
+  constexpr int LD = D + 1;
+  float *S = sm;                 // forward state, then the reverse state
+  float *Q = S + D * LD;
+  float *K = Q + kC * LD;
+  float *V = K + kC * LD;
+  float *G = V + kC * LD;        // dO tile
+  float *P = G + kC * LD;        // [kC][kC]
+  float *dP = P + kC * kC;       // [kC][kC]
+  float *pw = dP + kC * kC;
+
+  const int bh = blockIdx.x, b = bh / p.H, h = bh % p.H;
+  const int64_t off = (int64_t)b * p.sb + (int64_t)h * p.sh;
+  const float lam = p.decay ? p.decay[h] : 1.f;
+  fill_powers(pw, lam);
+  for (int e = threadIdx.x; e < D * D; e += kThreads)
+    S[(e / D) * LD + e % D] = init ? init[(int64_t)bh * D * D + e] : 0.f;
+  __syncthreads();
+  const int nchunk = (p.T + kC - 1) / kC;
+
+  // forward sweep: dq_i = sum_{j<=i} lambda^{i-j} (dO_i.v_j) k_j + lambda^{i+1} S_prev dO_i
+  for (int c = 0; c < nchunk; ++c) {
+    const int c0 = c * kC, n = min(kC, p.T - c0);
+    load_tile<D>(K, k + off, p.st, c0, n);
+    load_tile<D>(V, v + off, p.st, c0, n);
+    load_tile<D>(G, dO + off, p.st, c0, n);
+    __syncthreads();
+    for (int e = threadIdx.x; e < kC * kC; e += kThreads) {
+      const int i = e / kC, j = e % kC;
+      float s = 0.f;
+      if (j <= i) {
+        for (int a = 0; a < D; ++a) s = fmaf(G[i * LD + a], V[j * LD + a], s);
+        s *= pw[i - j];
+      }
+      dP[e] = s;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < kC * D; e += kThreads) {
+      const int i = e / D, a = e % D;
+      if (i >= n) continue;
+      float inter = 0.f, intra = 0.f;
+      for (int bb = 0; bb < D; ++bb) inter = fmaf(S[a * LD + bb], G[i * LD + bb], inter);
+      for (int j = 0; j <= i; ++j) intra = fmaf(dP[i * kC + j], K[j * LD + a], intra);
+      st_elem(dq + off + (int64_t)(c0 + i) * p.st + a, fmaf(pw[i + 1], inter, intra));
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < D * D; e += kThreads) {
+      const int a = e / D, bb = e % D;
+      float acc = 0.f;
+      for (int j = 0; j < n; ++j) acc = fmaf(pw[n - 1 - j] * K[j * LD + a], V[j * LD + bb], acc);
+      S[a * LD + bb] = fmaf(pw[n], S[a * LD + bb], acc);
+    }
+    __syncthreads();
+  }
+
+  // reverse sweep with Rbar = sum_{u > chunk end} lambda^{u-end} q_u dO_u^T
+  for (int e = threadIdx.x; e < D * D; e += kThreads) S[(e / D) * LD + e % D] = 0.f;
+  __syncthreads();
+  for (int c = nchunk - 1; c >= 0; --c) {
+    const int c0 = c * kC, n = min(kC, p.T - c0);
+    load_tile<D>(Q, q + off, p.st, c0, n);
+    load_tile<D>(K, k + off, p.st, c0, n);
+    load_tile<D>(V, v + off, p.st, c0, n);
+    load_tile<D>(G, dO + off, p.st, c0, n);
+    __syncthreads();
+    for (int e = threadIdx.x; e < kC * kC; e += kThreads) {
+      const int i = e / kC, j = e % kC;
+      float s = 0.f, g = 0.f;
+      if (j <= i) {
+        for (int a = 0; a < D; ++a) {
+          s = fmaf(Q[i * LD + a], K[j * LD + a], s);
+          g = fmaf(G[i * LD + a], V[j * LD + a], g);
+        }
+        s *= pw[i - j];
+        g *= pw[i - j];
+      }
+      P[e] = s;
+      dP[e] = g;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < kC * D; e += kThreads) {
+      const int j = e / D, a = e % D;
+      if (j >= n) continue;
+      // dk_j[a] = sum_i dP_ij q_i[a] + lambda^{n-1-j} (Rbar v_j)[a]
+      float intra = 0.f, inter = 0.f;
+      for (int i = j; i < n; ++i) intra = fmaf(dP[i * kC + j], Q[i * LD + a], intra);
+      for (int bb = 0; bb < D; ++bb) inter = fmaf(S[a * LD + bb], V[j * LD + bb], inter);
+      st_elem(dk + off + (int64_t)(c0 + j) * p.st + a, fmaf(pw[n - 1 - j], inter, intra));
+      // dv_j[a] = sum_i P_ij dO_i[a] + lambda^{n-1-j} (Rbar^T k_j)[a]
+      float intra2 = 0.f, inter2 = 0.f;
+      for (int i = j; i < n; ++i) intra2 = fmaf(P[i * kC + j], G[i * LD + a], intra2);
+      for (int aa = 0; aa < D; ++aa) inter2 = fmaf(S[aa * LD + a], K[j * LD + aa], inter2);
+      st_elem(dv + off + (int64_t)(c0 + j) * p.st + a, fmaf(pw[n - 1 - j], inter2, intra2));
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < D * D; e += kThreads) {
+      const int a = e / D, bb = e % D;
+      float acc = 0.f;
+      for (int i = 0; i < n; ++i) acc = fmaf(pw[i + 1] * Q[i * LD + a], G[i * LD + bb], acc);
+      S[a * LD + bb] = fmaf(pw[n], S[a * LD + bb], acc);
+    }
+    __syncthreads();
+  }
+  if (dinit)
+    for (int e = threadIdx.x; e < D * D; e += kThreads)
+      dinit[(int64_t)bh * D * D + e] = S[(e / D) * LD + e % D];
+}
+
+// ------------------------------------------------------------------ segment-local states
+template <int D, typename TIn>
+__global__ void __launch_bounds__(kThreads) simt_segment_kernel(Problem p, int seg_len, const TIn *k,
+                                                                const TIn *v, float *out) {
+  extern __shared__ float sm[];
+  constexpr int LD = D + 1;
+  constexpr int PER = D * D / kThreads;
+  float *K = sm;
+  float *V = K + kC * LD;
+  float *pw = V + kC * LD;
+  const int g = blockIdx.y, bh = blockIdx.x, b = bh / p.H, h = bh % p.H;
+  const int64_t off = (int64_t)b * p.sb + (int64_t)h * p.sh;
+  const float lam = p.decay ? p.decay[h] : 1.f;
+  fill_powers(pw, lam);
+  float acc[PER];
+#pragma unroll
+  for (int m = 0; m < PER; ++m) acc[m] = 0.f;
+  const int s0 = g * seg_len, s1 = min(p.T, s0 + seg_len);
+  for (int c0 = s0; c0 < s1; c0 += kC) {
+    const int n = min(kC, s1 - c0);
+    __syncthreads();
+    load_tile<D>(K, k + off, p.st, c0, n);
+    load_tile<D>(V, v + off, p.st, c0, n);
+    __syncthreads();
+#pragma unroll
+    for (int m = 0; m < PER; ++m) {
+      const int e = threadIdx.x + m * kThreads, a = e / D, bb = e % D;
+      float x = 0.f;
+      for (int j = 0; j < n; ++j) x = fmaf(pw[n - 1 - j] * K[j * LD + a], V[j * LD + bb], x);
+      acc[m] = fmaf(pw[n], acc[m], x);
+    }
+  }
+  float *U = out + ((int64_t)g * p.B * p.H + bh) * D * D;
+#pragma unroll
+  for (int m = 0; m < PER; ++m) U[threadIdx.x + m * kThreads] = acc[m];
+}
+
+template <int D>
+size_t fwd_smem() { return sizeof(float) * (D * (D + 1) + 3 * kC * (D + 1) + kC * kC + kC + 1); }
+template <int D>
+size_t bwd_smem() { return sizeof(float) * (D * (D + 1) + 4 * kC * (D + 1) + 2 * kC * kC + kC + 1); }
+template <int D>
+size_t seg_smem() { return sizeof(float) * (2 * kC * (D + 1) + kC + 1); }
+
+template <int D, typename TIn>
+cudaError_t launch_fwd(const Problem &p, const void *q, const void *k, const void *v, void *o,
+                       const float *init, float *fin, float *cs, cudaStream_t s) {
+  auto kern = simt_fwd_kernel<D, TIn>;
+  const size_t sm = fwd_smem<D>();
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  if (e != cudaSuccess) return e;
+  kern<<<p.B * p.H, kThreads, sm, s>>>(p, (const TIn *)q, (const TIn *)k, (const TIn *)v, (TIn *)o,
+                                        init, fin, cs);
+  return cudaGetLastError();
+}
+template <int D, typename TIn>
+cudaError_t launch_bwd(const Problem &p, const void *q, const void *k, const void *v, const void *dO,
+                       const float *init, void *dq, void *dk, void *dv, float *dinit, cudaStream_t s) {
+  auto kern = simt_bwd_kernel<D, TIn>;
+  const size_t sm = bwd_smem<D>();
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  if (e != cudaSuccess) return e;
+  kern<<<p.B * p.H, kThreads, sm, s>>>(p, (const TIn *)q, (const TIn *)k, (const TIn *)v,
+                                        (const TIn *)dO, init, (TIn *)dq, (TIn *)dk, (TIn *)dv, dinit);
+  return cudaGetLastError();
+}
+template <int D, typename TIn>
+cudaError_t launch_seg(const Problem &p, int seg_len, const void *k, const void *v, float *out,
+                       cudaStream_t s) {
+  auto kern = simt_segment_kernel<D, TIn>;
+  const size_t sm = seg_smem<D>();
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  if (e != cudaSuccess) return e;
+  const int G = (p.T + seg_len - 1) / seg_len;
+  kern<<<dim3(p.B * p.H, G), kThreads, sm, s>>>(p, seg_len, (const TIn *)k, (const TIn *)v, out);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t simt_fwd(const Problem &p, const void *q, const void *k, const void *v, void *o,
+                     const float *init, float *final_state, float *chunk_states, cudaStream_t s) {
+  if (p.d == 64)
+    return p.dtype == 1 ? launch_fwd<64, float>(p, q, k, v, o, init, final_state, chunk_states, s)
+                        : launch_fwd<64, __nv_bfloat16>(p, q, k, v, o, init, final_state, chunk_states, s);
+  return p.dtype == 1 ? launch_fwd<128, float>(p, q, k, v, o, init, final_state, chunk_states, s)
+                      : launch_fwd<128, __nv_bfloat16>(p, q, k, v, o, init, final_state, chunk_states, s);
+}
+
+cudaError_t simt_bwd(const Problem &p, const void *q, const void *k, const void *v, const void *dO,
+                     const float *init, void *dq, void *dk, void *dv, float *dinit, cudaStream_t s) {
+  if (p.d == 64)
+    return p.dtype == 1 ? launch_bwd<64, float>(p, q, k, v, dO, init, dq, dk, dv, dinit, s)
+                        : launch_bwd<64, __nv_bfloat16>(p, q, k, v, dO, init, dq, dk, dv, dinit, s);
+  return p.dtype == 1 ? launch_bwd<128, float>(p, q, k, v, dO, init, dq, dk, dv, dinit, s)
+                      : launch_bwd<128, __nv_bfloat16>(p, q, k, v, dO, init, dq, dk, dv, dinit, s);
+}
+
+cudaError_t simt_segment_states(const Problem &p, int seg_len, const void *k, const void *v,
+                                float *out, cudaStream_t s) {
+  if (p.d == 64)
+    return p.dtype == 1 ? launch_seg<64, float>(p, seg_len, k, v, out, s)
+                        : launch_seg<64, __nv_bfloat16>(p, seg_len, k, v, out, s);
+  return p.dtype == 1 ? launch_seg<128, float>(p, seg_len, k, v, out, s)
+                      : launch_seg<128, __nv_bfloat16>(p, seg_len, k, v, out, s);
+}
+
+}  // namespace linattn

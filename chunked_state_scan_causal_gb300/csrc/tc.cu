@@ -1,0 +1,625 @@
+// Tensor-core kernels (tcgen05 + TMEM + TMA) for bf16 sequences with d = 128.
+//
+// Both kernels are persistent (one CTA per SM, items taken round-robin) and
+// warp-specialised:
+//   warp 0        TMA producer (one thread)
+//   warp 1        TMEM allocator and MMA issuer (one thread)
+//   warps 4..7    epilogue group A (TMEM -> registers -> shared / global)
+//   warps 8..11   epilogue group B
+// Every wait is a bounded mbarrier wait (see ptx.cuh); a timeout records an
+// error in the status word and unwinds the kernel instead of hanging.
+//
+// A "block" is 128 tokens, i.e. two chunks of 64: the M = 128 tcgen05 MMA is
+// the natural tile, and chunking at 128 instead of 64 changes only the
+// rounding order (the chunked form equals the definition for any chunk
+// length).  All operands are SW128 tiles (ptx.cuh).
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace linattn {
+
+bool tc_supported(const Problem &p) { return p.dtype == 0 && p.d == 128 && p.T >= 1; }
+
+int tc_group_len(const Problem &p) {
+  // Enough (group, sequence) items for ~8 per SM, but groups of at least 512
+  // tokens so that the per-group fp32 state (64 KiB) stays small next to the
+  // group's own data (256 KiB of q, k, v per 512 tokens).
+  const int64_t BH = (int64_t)p.B * p.H;
+  const int64_t target = 8 * (int64_t)p.num_sms;
+  int64_t L = (p.T * BH + target - 1) / target;
+  L = (L + 127) / 128 * 128;
+  if (L < 512) L = 512;
+  const int64_t Tr = ((int64_t)p.T + 127) / 128 * 128;
+  if (L > Tr) L = Tr;
+  return (int)L;
+}
+
+namespace {
+
+constexpr int kThreads = 384;
+
+__device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
+  return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+// Multiply one 128-element bf16 row of an SW128 tile by w (rounded back to bf16).
+__device__ __forceinline__ void scale_tile_row(uint32_t tile, uint32_t row, float w) {
+#pragma unroll 4
+  for (uint32_t c = 0; c < 16; ++c) {
+    const uint32_t addr = tile + sw128_offset(row, c);
+    uint32_t x0, x1, x2, x3;
+    ld_shared_v4(addr, x0, x1, x2, x3);
+    x0 = pack_bf16(bf16lo(x0) * w, bf16hi(x0) * w);
+    x1 = pack_bf16(bf16lo(x1) * w, bf16hi(x1) * w);
+    x2 = pack_bf16(bf16lo(x2) * w, bf16hi(x2) * w);
+    x3 = pack_bf16(bf16lo(x3) * w, bf16hi(x3) * w);
+    st_shared_v4(addr, x0, x1, x2, x3);
+  }
+}
+
+// Store 32 fp32 values (columns 32c .. 32c+31 of `row`) as bf16 into an SW128 tile.
+__device__ __forceinline__ void store_row_chunk_bf16(uint32_t tile, uint32_t row, uint32_t c,
+                                                     const float (&x)[32]) {
+#pragma unroll
+  for (uint32_t q = 0; q < 4; ++q) {
+    st_shared_v4(tile + sw128_offset(row, 4 * c + q), pack_bf16(x[8 * q + 0], x[8 * q + 1]),
+                 pack_bf16(x[8 * q + 2], x[8 * q + 3]), pack_bf16(x[8 * q + 4], x[8 * q + 5]),
+                 pack_bf16(x[8 * q + 6], x[8 * q + 7]));
+  }
+}
+
+__device__ __forceinline__ void ld_chunk(uint32_t taddr, float (&x)[32]) {
+  uint32_t r[32];
+  tmem_ld32(taddr, r);
+  tmem_ld_wait();
+#pragma unroll
+  for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]);
+}
+
+// ============================================================================ segment aggregates
+struct AggParams {
+  int B, H, T, L, G, nitems, reverse;
+  const float *decay;
+  float *out;
+  int *status;
+};
+
+template <bool DECAY>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_agg_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__ CUtensorMap my,
+                  AggParams P) {
+  constexpr int NS = 3;              // stages of (X tile, Y tile)
+  constexpr uint32_t kStage = 2 * kTileBytes;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = align1024(smem_raw);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + NS * kStage);
+  uint64_t *full = bars, *scaled = bars + NS, *empty = bars + 2 * NS;
+  uint64_t *accf = bars + 3 * NS, *acce = accf + 2;
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(acce + 2);
+  __shared__ int abort_flag;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int BH = P.B * P.H;
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&scaled[s], 128);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&accf[a], 1);
+      mbar_init(&acce[a], 128);
+    }
+    fence_mbar_init();
+    prefetch_tensormap(&mx);
+    prefetch_tensormap(&my);
+  }
+  if (warp == 1) {
+    tmem_alloc(tslot, 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int it = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < P.nitems && ok; item += gridDim.x) {
+        const int g = item / BH, bh = item % BH, b = bh / P.H, h = bh % P.H;
+        const int s0 = g * P.L, s1 = min(P.T, s0 + P.L);
+        for (int t0 = s0; t0 < s1; t0 += 128, ++it) {
+          const int s = it % NS, u = it / NS;
+          if (u > 0 && !(ok = mbar_wait(&empty[s], (u - 1) & 1, &abort_flag, P.status))) break;
+          uint8_t *xs = smem + s * kStage;
+          mbar_arrive_expect_tx(&full[s], kStage);
+          tma_load_4d(&mx, &full[s], xs, 0, t0, h, b, kPolicyEvictFirst);
+          tma_load_4d(&mx, &full[s], xs + kTileHalfBytes, 64, t0, h, b, kPolicyEvictFirst);
+          tma_load_4d(&my, &full[s], xs + kTileBytes, 0, t0, h, b, kPolicyEvictFirst);
+          tma_load_4d(&my, &full[s], xs + kTileBytes + kTileHalfBytes, 64, t0, h, b, kPolicyEvictFirst);
+        }
+      }
+      // never leave with copies in flight: wait (time-bounded, even after an
+      // abort) for the last load of every stage
+      volatile int no_abort = 0;
+      for (int s = 0; s < NS; ++s) {
+        const int uses = it > s ? (it - 1 - s) / NS + 1 : 0;
+        if (uses > 0) mbar_wait(&full[s], (uses - 1) & 1, &no_abort, P.status);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int it = 0, ai = 0;
+      bool ok = true;
+      const uint32_t idesc = idesc_bf16(128, 128, true, true);
+      for (int item = blockIdx.x; item < P.nitems && ok; item += gridDim.x) {
+        const int g = item / BH;
+        const int s0 = g * P.L, s1 = min(P.T, s0 + P.L);
+        const int a = ai & 1, ua = ai >> 1;
+        if (ua > 0 && !(ok = mbar_wait(&acce[a], (ua - 1) & 1, &abort_flag, P.status))) break;
+        tc_fence_after();
+        const uint32_t dt = tmem + a * 128;
+        bool first = true;
+        for (int t0 = s0; t0 < s1; t0 += 128, ++it) {
+          const int s = it % NS, u = it / NS;
+          if (!(ok = mbar_wait(DECAY ? &scaled[s] : &full[s], u & 1, &abort_flag, P.status))) break;
+          tc_fence_after();
+          const uint32_t xs = smem_u32(smem + s * kStage), ys = xs + kTileBytes;
+#pragma unroll
+          for (uint32_t ks = 0; ks < 8; ++ks)
+            mma_ss(dt, desc_mnmajor(xs, ks), desc_mnmajor(ys, ks), idesc, (first && ks == 0) ? 0u : 1u);
+          first = false;
+          mma_commit(&empty[s]);
+        }
+        if (!ok) break;
+        mma_commit(&accf[a]);
+        ++ai;
+      }
+    }
+  } else if (warp >= 4 && warp < 8) {
+    if (DECAY) {
+      // scale X rows in place by the token weights before the MMA reads them
+      const uint32_t row = threadIdx.x - 128;
+      int it = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < P.nitems && ok; item += gridDim.x) {
+        const int g = item / BH, h = (item % BH) % P.H;
+        const int s0 = g * P.L, s1 = min(P.T, s0 + P.L);
+        const float l2 = log2f(P.decay[h]);
+        for (int t0 = s0; t0 < s1; t0 += 128, ++it) {
+          const int s = it % NS, u = it / NS;
+          if (!(ok = mbar_wait(&full[s], u & 1, &abort_flag, P.status))) break;
+          const int tok = t0 + (int)row;
+          float w = 0.f;
+          if (tok < s1) w = exp2f(l2 * (float)(P.reverse ? (tok - s0 + 1) : (s1 - 1 - tok)));
+          scale_tile_row(smem_u32(smem + s * kStage), row, w);
+          fence_proxy_async_smem();
+          mbar_arrive(&scaled[s]);
+        }
+      }
+    }
+  } else if (warp >= 8) {
+    const uint32_t quad = warp & 3, row = quad * 32 + lane;
+    int ai = 0;
+    for (int item = blockIdx.x; item < P.nitems; item += gridDim.x, ++ai) {
+      const int g = item / BH, bh = item % BH;
+      const int a = ai & 1, ua = ai >> 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&accf[a], ua & 1, &abort_flag, P.status))) break;
+      tc_fence_after();
+      float *dst = P.out + ((int64_t)g * BH + bh) * 16384 + row * 128;
+#pragma unroll 1
+      for (uint32_t c = 0; c < 4; ++c) {
+        float x[32];
+        ld_chunk(tmem + a * 128 + ((quad * 32) << 16) + c * 32, x);
+#pragma unroll
+        for (int j = 0; j < 32; j += 4)
+          *reinterpret_cast<float4 *>(dst + c * 32 + j) = make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
+      }
+      tc_fence_before();
+      mbar_arrive(&acce[a]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, 256);
+}
+
+// ============================================================================ per-group main kernel
+struct MainParams {
+  int B, H, T, L, G, nitems, init_t;
+  const float *decay;
+  const float *ginit;  // [G][BH][d][d]
+  float *final_state;  // [BH][d][d] or null
+  int *status;
+};
+
+constexpr int kSlots = 5;
+constexpr uint32_t kOffPs = kSlots * kTileBytes;          // P (then O staging) tile
+constexpr uint32_t kOffSh = kOffPs + kTileBytes;          // bf16 state tile
+constexpr uint32_t kOffBar = kOffSh + kTileBytes;
+constexpr size_t kMainSmem = kOffBar + 256 + 1024;
+
+// barrier indices
+enum { B_FULL = 0, B_EMPTY = kSlots, B_PFULL = 2 * kSlots, B_PEMPTY, B_OFULL, B_OEMPTY, B_SFULL, B_PRE,
+       B_PSFULL, B_COUNT };
+
+// Decay mask of one 32-column chunk of a score row: keep j <= i (causal) or
+// j >= i (anti-causal) and weight by lambda^{|i-j|}; walks j so that the
+// weight only ever shrinks (no overflow for any lambda in (0, 1]).
+template <bool DECAY, bool REV>
+__device__ __forceinline__ void mask_chunk(float (&x)[32], int i, int c, float lam, float l2) {
+  if (!DECAY) {
+#pragma unroll
+    for (int jj = 0; jj < 32; ++jj) {
+      const int j = c * 32 + jj;
+      x[jj] = (REV ? (j >= i) : (j <= i)) ? x[jj] : 0.f;
+    }
+    return;
+  }
+  if (!REV) {
+    const int e0 = i - (c * 32 + 31);  // exponent at jj = 31
+    float w = e0 >= 0 ? exp2f(l2 * (float)e0) : 0.f;
+#pragma unroll
+    for (int jj = 31; jj >= 0; --jj) {
+      const int j = c * 32 + jj;
+      if (j == i) w = 1.f;
+      x[jj] = (j <= i) ? x[jj] * w : 0.f;
+      w *= lam;
+    }
+  } else {
+    const int e0 = c * 32 - i;  // exponent at jj = 0
+    float w = e0 >= 0 ? exp2f(l2 * (float)e0) : 0.f;
+#pragma unroll
+    for (int jj = 0; jj < 32; ++jj) {
+      const int j = c * 32 + jj;
+      if (j == i) w = 1.f;
+      x[jj] = (j >= i) ? x[jj] * w : 0.f;
+      w *= lam;
+    }
+  }
+}
+
+template <bool DECAY, bool REV>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_main_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+                   const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mo,
+                   MainParams P) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = align1024(smem_raw);
+  uint64_t *bar = reinterpret_cast<uint64_t *>(smem + kOffBar);
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + B_COUNT);
+  __shared__ int abort_flag;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int BH = P.B * P.H;
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(&bar[B_FULL + s], 1);
+      mbar_init(&bar[B_EMPTY + s], 1);
+    }
+    mbar_init(&bar[B_PFULL], 1);
+    mbar_init(&bar[B_PEMPTY], 128);
+    mbar_init(&bar[B_OFULL], 1);
+    mbar_init(&bar[B_OEMPTY], 128);
+    mbar_init(&bar[B_SFULL], 1);
+    mbar_init(&bar[B_PRE], 128);
+    mbar_init(&bar[B_PSFULL], 128);
+    fence_mbar_init();
+    prefetch_tensormap(&mq);
+    prefetch_tensormap(&mk);
+    prefetch_tensormap(&mv);
+    prefetch_tensormap(&mo);
+  }
+  if (warp == 1) {
+    tmem_alloc(tslot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  const uint32_t tS = tmem, tP = tmem + 128, tO = tmem + 256;
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t sPs = sbase + kOffPs, sSh = sbase + kOffSh;
+  auto slot_addr = [&](int t) { return sbase + (uint32_t)(t % kSlots) * kTileBytes; };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int blk = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < P.nitems && ok; item += gridDim.x) {
+        const int g = item / BH, bh = item % BH, b = bh / P.H, h = bh % P.H;
+        const int s0 = g * P.L, s1 = min(P.T, s0 + P.L), nb = (s1 - s0 + 127) / 128;
+        for (int n = 0; n < nb && ok; ++n, ++blk) {
+          const int t0 = s0 + 128 * (REV ? nb - 1 - n : n);
+          for (int x = 0; x < 3; ++x) {
+            const int t = 3 * blk + x, s = t % kSlots, u = t / kSlots;
+            if (u > 0 && !(ok = mbar_wait(&bar[B_EMPTY + s], (u - 1) & 1, &abort_flag, P.status))) break;
+            const CUtensorMap *m = x == 0 ? &mq : (x == 1 ? &mk : &mv);
+            uint8_t *dst = smem + s * kTileBytes;
+            mbar_arrive_expect_tx(&bar[B_FULL + s], kTileBytes);
+            tma_load_4d(m, &bar[B_FULL + s], dst, 0, t0, h, b, kPolicyEvictFirst);
+            tma_load_4d(m, &bar[B_FULL + s], dst + kTileHalfBytes, 64, t0, h, b, kPolicyEvictFirst);
+          }
+        }
+      }
+      // time-bounded drain of the loads in flight (also after an abort)
+      const int ntile = 3 * blk;
+      volatile int no_abort = 0;
+      for (int s = 0; s < kSlots; ++s) {
+        const int uses = ntile > s ? (ntile - 1 - s) / kSlots + 1 : 0;
+        if (uses > 0) mbar_wait(&bar[B_FULL + s], (uses - 1) & 1, &no_abort, P.status);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t id_qk = idesc_bf16(128, 128, false, false);  // Q K^T
+      const uint32_t id_qs = idesc_bf16(128, 128, false, true);   // Q S,  P V
+      const uint32_t id_kv = idesc_bf16(128, 128, true, true);    // K^T V
+      int blk = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < P.nitems && ok; item += gridDim.x) {
+        const int g = item / BH;
+        const int s0 = g * P.L, s1 = min(P.T, s0 + P.L), nb = (s1 - s0 + 127) / 128;
+        for (int n = 0; n < nb; ++n, ++blk) {
+          const int tq = 3 * blk, tk = tq + 1, tv = tq + 2;
+          const uint32_t Q = slot_addr(tq), K = slot_addr(tk), V = slot_addr(tv);
+          // scores: P = Q K^T
+          ok = mbar_wait(&bar[B_FULL + tq % kSlots], (tq / kSlots) & 1, &abort_flag, P.status) &&
+               mbar_wait(&bar[B_FULL + tk % kSlots], (tk / kSlots) & 1, &abort_flag, P.status) &&
+               (blk == 0 || mbar_wait(&bar[B_PEMPTY], (blk - 1) & 1, &abort_flag, P.status));
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tP, desc_kmajor(Q, ks), desc_kmajor(K, ks), id_qk, ks > 0);
+          mma_commit(&bar[B_PFULL]);
+          // inter-block term: O = Q' S   (Q' = decay-weighted rows)
+          ok = mbar_wait(&bar[B_PRE], blk & 1, &abort_flag, P.status) &&
+               (blk == 0 || mbar_wait(&bar[B_OEMPTY], (blk - 1) & 1, &abort_flag, P.status));
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tO, desc_kmajor(Q, ks), desc_mnmajor(sSh, ks), id_qs, ks > 0);
+          mma_commit(&bar[B_EMPTY + tq % kSlots]);
+          // state update: S += K'^T V
+          if (!(ok = mbar_wait(&bar[B_FULL + tv % kSlots], (tv / kSlots) & 1, &abort_flag, P.status))) break;
+          tc_fence_after();
+#pragma unroll
+          for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tS, desc_mnmajor(K, ks), desc_mnmajor(V, ks), id_kv, 1u);
+          mma_commit(&bar[B_EMPTY + tk % kSlots]);
+          mma_commit(&bar[B_SFULL]);
+          // intra-block term: O += P V
+          if (!(ok = mbar_wait(&bar[B_PSFULL], blk & 1, &abort_flag, P.status))) break;
+          tc_fence_after();
+#pragma unroll
+          for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tO, desc_kmajor(sPs, ks), desc_mnmajor(V, ks), id_qs, 1u);
+          mma_commit(&bar[B_EMPTY + tv % kSlots]);
+          mma_commit(&bar[B_OFULL]);
+        }
+      }
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // ------------------------------------------------------------ group A: scores and outputs
+    const uint32_t quad = warp & 3, row = quad * 32 + lane, lb = (quad * 32) << 16;
+    const bool leader = threadIdx.x == 128;
+    int blk = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; item < P.nitems && ok; item += gridDim.x) {
+      const int g = item / BH, bh = item % BH, b = bh / P.H, h = bh % P.H;
+      const int s0 = g * P.L, s1 = min(P.T, s0 + P.L), nb = (s1 - s0 + 127) / 128;
+      const float lam = DECAY ? P.decay[h] : 1.f;
+      const float l2 = DECAY ? log2f(lam) : 0.f;
+      for (int n = 0; n < nb; ++n, ++blk) {
+        const int t0 = s0 + 128 * (REV ? nb - 1 - n : n);
+        ok = group_all(mbar_wait(&bar[B_PFULL], blk & 1, &abort_flag, P.status), 2, 128);
+        if (!ok) break;
+        tc_fence_after();
+        // the P tile buffer is free once the previous output store has read it
+        if (leader) bulk_wait_read_all();
+        named_bar_sync(1, 128);
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          float x[32];
+          ld_chunk(tP + lb + c * 32, x);
+          mask_chunk<DECAY, REV>(x, (int)row, c, lam, l2);
+          store_row_chunk_bf16(sPs, row, c, x);
+        }
+        tc_fence_before();
+        mbar_arrive(&bar[B_PEMPTY]);
+        fence_proxy_async_smem();
+        mbar_arrive(&bar[B_PSFULL]);
+        // outputs
+        ok = group_all(mbar_wait(&bar[B_OFULL], blk & 1, &abort_flag, P.status), 2, 128);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          float x[32];
+          ld_chunk(tO + lb + c * 32, x);
+          store_row_chunk_bf16(sPs, row, c, x);
+        }
+        tc_fence_before();
+        mbar_arrive(&bar[B_OEMPTY]);
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (leader) {
+          tma_store_4d(&mo, smem + kOffPs, 0, t0, h, b);
+          tma_store_4d(&mo, smem + kOffPs + kTileHalfBytes, 64, t0, h, b);
+          bulk_commit();
+        }
+      }
+    }
+    if (leader) bulk_wait_all();
+  } else if (warp >= 8) {
+    // ------------------------------------------------------------ group B: state tile (+ decay weights)
+    const uint32_t quad = warp & 3, row = quad * 32 + lane, lb = (quad * 32) << 16;
+    int blk = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; item < P.nitems && ok; item += gridDim.x) {
+      const int g = item / BH, bh = item % BH, h = bh % P.H;
+      const int s0 = g * P.L, s1 = min(P.T, s0 + P.L), nb = (s1 - s0 + 127) / 128;
+      const float lam = DECAY ? P.decay[h] : 1.f;
+      const float l2 = DECAY ? log2f(lam) : 0.f;
+      auto nvalid = [&](int n) {
+        const int t0 = s0 + 128 * (REV ? nb - 1 - n : n);
+        return min(128, s1 - t0);
+      };
+      // Decay weights of block `bb` (global block counter) with nv valid rows:
+      // forward q_i *= lambda^{i+1}, k_j *= lambda^{nv-1-j};
+      // reverse q_i *= lambda^{nv-1-i}, k_j *= lambda^{j+1}.
+      auto weigh = [&](int bb, int nv) -> bool {
+        if (!__all_sync(0xffffffffu, mbar_wait(&bar[B_PFULL], bb & 1, &abort_flag, P.status))) return false;
+        const int r = (int)row;
+        float wq = 0.f, wk = 0.f;
+        if (r < nv) {
+          wq = exp2f(l2 * (float)(REV ? nv - 1 - r : r + 1));
+          wk = exp2f(l2 * (float)(REV ? r + 1 : nv - 1 - r));
+        }
+        scale_tile_row(slot_addr(3 * bb), row, wq);
+        scale_tile_row(slot_addr(3 * bb + 1), row, wk);
+        return true;
+      };
+      // initial state of the group
+      {
+        const float *src = P.ginit + ((int64_t)g * BH + bh) * 16384;
+        const float dec = DECAY ? exp2f(l2 * (float)nvalid(0)) : 1.f;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          float x[32];
+          if (!P.init_t) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {
+              const float4 v4 = __ldg(reinterpret_cast<const float4 *>(src + row * 128 + c * 32 + j));
+              x[j] = v4.x; x[j + 1] = v4.y; x[j + 2] = v4.z; x[j + 3] = v4.w;
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) x[j] = __ldg(src + (c * 32 + j) * 128 + row);
+          }
+          store_row_chunk_bf16(sSh, row, c, x);
+          uint32_t r[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(x[j] * dec);
+          tmem_st32(tS + lb + c * 32, r);
+        }
+        tmem_st_wait();
+        if (DECAY && !(ok = weigh(blk, nvalid(0)))) break;
+        tc_fence_before();
+        fence_proxy_async_smem();
+        mbar_arrive(&bar[B_PRE]);
+      }
+      for (int n = 0; n < nb; ++n, ++blk) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_SFULL], blk & 1, &abort_flag, P.status));
+        if (!ok) break;
+        tc_fence_after();
+        if (n + 1 < nb) {
+          const int nv = nvalid(n + 1);
+          const float dec = DECAY ? exp2f(l2 * (float)nv) : 1.f;
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            float x[32];
+            ld_chunk(tS + lb + c * 32, x);
+            store_row_chunk_bf16(sSh, row, c, x);
+            if (DECAY) {
+              uint32_t r[32];
+#pragma unroll
+              for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(x[j] * dec);
+              tmem_st32(tS + lb + c * 32, r);
+            }
+          }
+          if (DECAY) tmem_st_wait();
+          if (DECAY && !(ok = weigh(blk + 1, nv))) break;
+          tc_fence_before();
+          fence_proxy_async_smem();
+          mbar_arrive(&bar[B_PRE]);
+        } else if (P.final_state && !REV && g == P.G - 1) {
+          float *dst = P.final_state + (int64_t)bh * 16384 + row * 128;
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            float x[32];
+            ld_chunk(tS + lb + c * 32, x);
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+              *reinterpret_cast<float4 *>(dst + c * 32 + j) = make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
+          }
+          tc_fence_before();
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+bool seq_tmap(const Problem &p, const void *base, CUtensorMap *m) {
+  const uint64_t dims[4] = {(uint64_t)p.d, (uint64_t)p.T, (uint64_t)p.H, (uint64_t)p.B};
+  const uint64_t strides[3] = {(uint64_t)p.st * 2, (uint64_t)p.sh * 2, (uint64_t)p.sb * 2};
+  return make_tmap_bf16(m, base, dims, strides);
+}
+
+template <typename K>
+cudaError_t set_smem(K kern, size_t bytes) {
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+}  // namespace
+
+cudaError_t tc_segment_states(const Problem &p, int seg_len, const void *X, const void *Y, bool reverse,
+                              float *out, int *status, cudaStream_t s) {
+  alignas(64) CUtensorMap mx, my;
+  if (!seq_tmap(p, X, &mx) || !seq_tmap(p, Y, &my)) return cudaErrorInvalidValue;
+  AggParams A;
+  A.B = p.B; A.H = p.H; A.T = p.T; A.L = seg_len;
+  A.G = (p.T + seg_len - 1) / seg_len;
+  A.nitems = A.G * p.B * p.H;
+  A.reverse = reverse ? 1 : 0;
+  A.decay = p.decay; A.out = out; A.status = status;
+  const size_t smem = 3 * 2 * kTileBytes + 1024 + 256;
+  const int grid = A.nitems < p.num_sms ? A.nitems : p.num_sms;
+  cudaError_t e;
+  if (p.decay) {
+    if ((e = set_smem(tc_agg_kernel<true>, smem)) != cudaSuccess) return e;
+    tc_agg_kernel<true><<<grid, kThreads, smem, s>>>(mx, my, A);
+  } else {
+    if ((e = set_smem(tc_agg_kernel<false>, smem)) != cudaSuccess) return e;
+    tc_agg_kernel<false><<<grid, kThreads, smem, s>>>(mx, my, A);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t tc_main(const Problem &p, int group_len, bool reverse, const void *q, const void *k,
+                    const void *v, void *o, const float *group_init, bool init_transposed,
+                    float *final_state, int *status, cudaStream_t s) {
+  alignas(64) CUtensorMap mq, mk, mv, mo;
+  if (!seq_tmap(p, q, &mq) || !seq_tmap(p, k, &mk) || !seq_tmap(p, v, &mv) || !seq_tmap(p, o, &mo))
+    return cudaErrorInvalidValue;
+  MainParams M;
+  M.B = p.B; M.H = p.H; M.T = p.T; M.L = group_len;
+  M.G = (p.T + group_len - 1) / group_len;
+  M.nitems = M.G * p.B * p.H;
+  M.init_t = init_transposed ? 1 : 0;
+  M.decay = p.decay; M.ginit = group_init; M.final_state = final_state; M.status = status;
+  const int grid = M.nitems < p.num_sms ? M.nitems : p.num_sms;
+  cudaError_t e;
+#define LINATTN_LAUNCH_MAIN(DEC, REV)                                              \
+  do {                                                                             \
+    if ((e = set_smem(tc_main_kernel<DEC, REV>, kMainSmem)) != cudaSuccess) return e; \
+    tc_main_kernel<DEC, REV><<<grid, kThreads, kMainSmem, s>>>(mq, mk, mv, mo, M);  \
+  } while (0)
+  if (p.decay) {
+    if (reverse) LINATTN_LAUNCH_MAIN(true, true); else LINATTN_LAUNCH_MAIN(true, false);
+  } else {
+    if (reverse) LINATTN_LAUNCH_MAIN(false, true); else LINATTN_LAUNCH_MAIN(false, false);
+  }
+#undef LINATTN_LAUNCH_MAIN
+  return cudaGetLastError();
+}
+
+}  // namespace linattn

@@ -1,0 +1,160 @@
+/*
+ * linattn -- chunked causal linear attention with a chunk-state prefix scan,
+ * for one NVIDIA GB300 (sm_103a).  C ABI: plain pointers, sizes and a stream.
+ *
+ * The operation (the recurrent definition; the chunked evaluation below
+ * reaches the same values up to rounding order):
+ *
+ *     S_t = lambda_h * S_{t-1} + k_t v_t^T        S_{-1} = init_state (or 0)
+ *     o_t = S_t^T q_t                             S is d_k x d_v, fp32
+ *
+ * computed right-product-first in chunks ("LASP-2: Rethinking Sequence
+ * Parallelism for Linear Attention and Its Hybrid", abstract): inside a chunk
+ * ordinary masked attention (Q K^T * M) V, across chunks the kernel trick
+ * Q . S_prev (related-paper entry "Lightning Attention-2" on the same page),
+ * with the chunk states combined by a prefix scan -- the single-GPU reading of
+ * the All-Scan that hands every rank its initial state ("ZeCO: Zero
+ * Communication Overhead Sequence Parallelism for Linear Attention",
+ * abstract) and of LASP-2's single gather of length-independent states.
+ *
+ * CONVENTIONS (every entry point)
+ *  - Every data pointer is CALLER-OWNED DEVICE memory on the current device.
+ *    The library never allocates, frees or synchronises (except
+ *    linattn_device_status, which synchronises the given stream).
+ *  - All work is enqueued on `stream` (a cudaStream_t passed as void*; NULL is
+ *    the legacy default stream) and the call returns without waiting.
+ *  - Host-side errors are returned BEFORE anything is enqueued.  A failed
+ *    launch returns LINATTN_ERR_CUDA.  Device-side errors (a bounded wait that
+ *    gave up) are written to the status word at the start of the workspace
+ *    and read back by linattn_device_status.  Every entry point that takes a
+ *    workspace clears that word first, so it reports the last call only.
+ *  - Re-entrant and stateless: concurrent calls need distinct workspaces.
+ *  - Sequence tensors q, k, v, o (and dO, dq, dk, dv) are [B, H, T, d] with the
+ *    last dimension contiguous and the element strides of linattn_shape.
+ *    Their base pointers and row strides must be 16-byte aligned.  With
+ *    T == 0 they are not read and may be NULL; the final state is then the
+ *    initial state (or zeros) and d_init_state is zero.
+ *  - States are fp32, row-major [.., d_k, d_v] (row index = key dimension).
+ */
+#ifndef LINATTN_H
+#define LINATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define LINATTN_ABI_VERSION 1
+
+/* Status codes (return values and device status word). */
+enum {
+  LINATTN_OK = 0,
+  LINATTN_ERR_INVALID = -1,        /* null pointer, negative size, bad op code       */
+  LINATTN_ERR_UNSUPPORTED = -2,    /* valid request outside what is implemented      */
+  LINATTN_ERR_ALIGN = -3,          /* pointer or stride not 16-byte aligned          */
+  LINATTN_ERR_WORKSPACE = -4,      /* workspace missing, too small or not 256-B aligned */
+  LINATTN_ERR_CUDA = -5,           /* a CUDA runtime / driver call failed            */
+  LINATTN_ERR_DEVICE_TIMEOUT = -6, /* device status: a bounded wait gave up          */
+  LINATTN_ERR_DEVICE = -7          /* current device is not an sm_103 GPU            */
+};
+
+/* Element type of the sequence tensors (states are always fp32). */
+enum { LINATTN_BF16 = 0, LINATTN_F32 = 1 };
+
+/* Workspace queries. */
+enum { LINATTN_OP_FWD = 1, LINATTN_OP_BWD = 2, LINATTN_OP_CHUNK_STATES = 3 };
+
+typedef struct {
+  int32_t abi_version;  /* must be LINATTN_ABI_VERSION                              */
+  int32_t B, H, T;      /* batch, heads, tokens; B, H >= 1, T >= 0                  */
+  int32_t dk, dv;       /* head dims; this version: dk == dv, both 64 or 128        */
+  int32_t chunk;        /* chunk length C of the chunk-state outputs; must be 64    */
+  int32_t dtype;        /* LINATTN_BF16 or LINATTN_F32 for every sequence tensor    */
+  int64_t stride_b;     /* element strides of every sequence tensor; > 0 (unchecked when T == 0) */
+  int64_t stride_h;
+  int64_t stride_t;     /* >= dk; the last dimension is contiguous                  */
+  const float *decay;   /* [H] device fp32 per-head lambda_h in (0, 1], or NULL for 1 */
+} linattn_shape;
+
+/* Library ABI version (LINATTN_ABI_VERSION of the build). */
+int32_t linattn_abi_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *linattn_status_string(int32_t status);
+
+/* Workspace bytes needed by linattn_fwd (op=LINATTN_OP_FWD), linattn_bwd
+ * (LINATTN_OP_BWD) or linattn_chunk_states (LINATTN_OP_CHUNK_STATES, with its
+ * seg_len; ignored otherwise) for this shape on the current device.  Writes
+ * *bytes and returns a status; the workspace must be 256-byte aligned. */
+int32_t linattn_workspace_size(const linattn_shape *shape, int32_t op, int32_t seg_len,
+                               size_t *bytes);
+
+/* Forward.  Computes o for every token (steps: intra-chunk masked attention,
+ * inter-chunk query-times-state, state update, prefix scan of chunk-group
+ * states; "Lightning Attention-2" entry and abstract of the LASP-2 page).
+ *   q, k  [B,H,T,dk], v, o [B,H,T,dv]  (dtype of the shape)
+ *   init_state   [B,H,dk,dv] fp32 state before token 0, or NULL (zeros)
+ *   final_state  [B,H,dk,dv] fp32 state after token T-1, or NULL
+ *   chunk_states [B,H,ceil(T/chunk),dk,dv] fp32 state ENTERING every chunk
+ *                (exclusive: entry 0 is init_state), or NULL
+ * Returns a status. */
+int32_t linattn_fwd(const linattn_shape *shape, const void *q, const void *k, const void *v,
+                    void *o, const float *init_state, float *final_state, float *chunk_states,
+                    void *workspace, size_t workspace_bytes, void *stream);
+
+/* Backward of linattn_fwd for an upstream gradient dO [B,H,T,dv]:
+ *   dq_t = S_t dO_t,   dk_t = R_t v_t,   dv_t = R_t^T k_t,
+ *   R_t = sum_{u>=t} lambda^{u-t} q_u dO_u^T (reverse state, scanned backwards),
+ *   d_init_state = sum_t lambda^{t+1} q_t dO_t^T   ([B,H,dk,dv] fp32, or NULL).
+ * dq, dk [B,H,T,dk] and dv [B,H,T,dv] are written in the shape's dtype.  The
+ * forward states are recomputed from k, v and init_state (no stored
+ * activations).  Returns a status. */
+int32_t linattn_bwd(const linattn_shape *shape, const void *q, const void *k, const void *v,
+                    const void *dO, const float *init_state, void *dq, void *dk, void *dv,
+                    float *d_init_state, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Segment-local states (what each sequence-parallel rank computes from its
+ * own contiguous segment before the exchange; LASP-2 page, abstract):
+ *   local_states[g,b,h] = sum_{s in segment g} lambda^{end_g - s} k_s v_s^T
+ * for G = T / seg_len segments of seg_len tokens (seg_len >= 1 and a divisor
+ * of T; T >= 1).  local_states is [G,B,H,dk,dv] fp32.  Returns a status. */
+int32_t linattn_chunk_states(const linattn_shape *shape, int32_t seg_len, const void *k,
+                             const void *v, float *local_states, void *workspace,
+                             size_t workspace_bytes, void *stream);
+
+/* Workspace bytes for linattn_state_scan. */
+int32_t linattn_state_scan_workspace_size(int32_t G, int32_t BH, int32_t dk, int32_t dv,
+                                          size_t *bytes);
+
+/* Exclusive prefix scan of segment states (ZeCO page, abstract: All-Scan
+ * hands every rank exactly its initial state):
+ *   init_states[0] = init (or 0),
+ *   init_states[g] = a_bh * init_states[g-1] + local_states[g-1],
+ *   total          = a_bh * init_states[G-1] + local_states[G-1]   (or NULL)
+ * local_states / init_states [G,BH,dk,dv] fp32 (they must not overlap),
+ * init / total [BH,dk,dv] fp32 or NULL, seg_decay [BH] fp32 (a_bh = lambda^L
+ * of the segment length) or NULL for 1.  G >= 1, BH >= 1, dk*dv % 8 == 0.
+ * Implemented as a warp-shuffle scan over 32 segments per warp with a
+ * decoupled look-back across 32-segment tiles.  Returns a status. */
+int32_t linattn_state_scan(int32_t G, int32_t BH, int32_t dk, int32_t dv, const float *seg_decay,
+                           const float *local_states, const float *init, float *init_states,
+                           float *total, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Synchronises `stream`, then returns the device status word of `workspace`
+ * (LINATTN_OK, or e.g. LINATTN_ERR_DEVICE_TIMEOUT) or LINATTN_ERR_CUDA. */
+int32_t linattn_device_status(const void *workspace, void *stream);
+
+/* Diagnostic (not part of the method): one 128x128x128 bf16 tensor-core
+ * product through the same shared-memory layouts the kernels use, written as
+ * fp32 D[128][128].  A and B are 128x128 bf16 row-major device arrays.
+ *   mode 0: D = A   B^T     mode 1: D = A^T B     mode 2: D = A B
+ *   mode 3: D = A^T B^T     mode 4: D = A B with A staged through tensor memory
+ * Returns a status (LINATTN_ERR_DEVICE off sm_103). */
+int32_t linattn_diag_mma(int32_t mode, const void *A, const void *B, float *D, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LINATTN_H */

@@ -1,0 +1,217 @@
+"""CUDA path vs the fp64 oracle, element by element, through the C ABI.
+
+Tolerance (max|gpu - ref| / max|ref| over each output tensor): 1e-2 for bf16
+inputs, 1e-4 for fp32 inputs, 1e-5 for the fp32-only state scan.  Cases span
+several 128-token tiles, several chunk groups, ragged tails (T not a multiple
+of 64 or 128), decays from 0.5 to 0.99986, initial states and T = 0.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import chunked_state_scan_causal_gb300 as la
+from chunked_state_scan_causal_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+TOL = {torch.bfloat16: 1e-2, torch.float32: 1e-4}
+
+
+def rel(got, ref):
+    got = got.detach().double().cpu().numpy() if torch.is_tensor(got) else got
+    den = max(float(np.max(np.abs(ref))), 1e-30)
+    return float(np.max(np.abs(got - ref))) / den
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from chunked_state_scan_causal_gb300 import build
+    build.build()
+    assert torch.cuda.is_available()
+
+
+def to_dev(a, dtype):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(dtype).cuda()
+
+
+def case(seed, B, H, T, d, dtype, sigma=0.125):
+    c = inputs.random_case(seed, B, H, T, d, dtype="bf16" if dtype == torch.bfloat16 else "f32", sigma=sigma)
+    dev = {k: to_dev(v, dtype) for k, v in c.items()}
+    return c, dev
+
+
+def decays(H, kind):
+    if kind is None:
+        return None
+    if kind == "cfg":
+        lam = inputs.decay_per_head(H)
+    else:
+        lam = np.linspace(kind, 0.999, H).astype(np.float32)
+    return lam
+
+
+# ------------------------------------------------------------------ diagnostics
+@pytest.mark.parametrize("mode", [0, 1, 2, 3, 4])
+def test_diag_tensor_core_product(mode):
+    """Every operand layout of the tensor-core MMA equals a plain fp32 matrix product."""
+    g = torch.Generator().manual_seed(mode)
+    A = torch.randn(128, 128, generator=g).to(torch.bfloat16).cuda()
+    B = torch.randn(128, 128, generator=g).to(torch.bfloat16).cuda()
+    D = torch.zeros(128, 128, dtype=torch.float32, device="cuda")
+    st = la.linattn_diag_mma(mode, A.data_ptr(), B.data_ptr(), D.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert st == la.OK
+    torch.cuda.synchronize()
+    a, b = A.double().cpu(), B.double().cpu()
+    ref = {0: a @ b.T, 1: a.T @ b, 2: a @ b, 3: a.T @ b.T, 4: a @ b}[mode].numpy()
+    assert rel(D, ref) < 1e-5
+
+
+# ------------------------------------------------------------------ state scan
+@pytest.mark.parametrize("G", [1, 5, 32, 33, 70])
+@pytest.mark.parametrize("with_decay,with_init", [(False, False), (True, True), (True, False)])
+def test_state_scan(G, with_decay, with_init):
+    r = np.random.default_rng(G)
+    BH, dk, dv = 3, 16, 24
+    U = r.standard_normal((G, BH, dk, dv)).astype(np.float32)
+    a = r.uniform(0.5, 1.0, BH).astype(np.float32) if with_decay else None
+    init = r.standard_normal((BH, dk, dv)).astype(np.float32) if with_init else None
+    ref, ref_tot = oracle.state_scan(U, seg_decay=a, init=init)
+    out, tot = la.state_scan(torch.from_numpy(U).cuda(), None if a is None else torch.from_numpy(a).cuda(),
+                             None if init is None else torch.from_numpy(init).cuda(), want_total=True)
+    torch.cuda.synchronize()
+    assert rel(out, ref) < 1e-5
+    assert rel(tot, ref_tot) < 1e-5
+
+
+# ------------------------------------------------------------------ chunk_states (segment-local states)
+@pytest.mark.parametrize("dtype,d,T,seg", [(torch.float32, 64, 512, 128), (torch.bfloat16, 128, 1024, 256),
+                                           (torch.bfloat16, 128, 768, 384), (torch.bfloat16, 64, 512, 64)])
+@pytest.mark.parametrize("dk", [None, 0.5, "cfg"])
+def test_chunk_states(dtype, d, T, seg, dk):
+    B, H = 2, 3
+    c, dev = case(3, B, H, T, d, dtype)
+    lam = decays(H, dk)
+    got = la.chunk_states(dev["k"], dev["v"], seg, decay=None if lam is None else torch.from_numpy(lam).cuda())
+    torch.cuda.synchronize()
+    ref = oracle.segment_states(c["k"], c["v"], seg, lam=lam)
+    assert rel(got, ref) < (1e-2 if dtype == torch.bfloat16 else 1e-4)
+
+
+# ------------------------------------------------------------------ forward
+def run_fwd(c, dev, dtype, lam, init, want_cs=False):
+    dec = None if lam is None else torch.from_numpy(lam).cuda()
+    init_d = None if init is None else torch.from_numpy(init.astype(np.float32)).cuda()
+    o, fin, cs = la.fwd(dev["q"], dev["k"], dev["v"], decay=dec, init_state=init_d, want_final=True,
+                        want_chunk_states=want_cs)
+    torch.cuda.synchronize()
+    return o, fin, cs
+
+
+def test_config1_fp32_forward_and_chunk_states():
+    """The tiny fp32 workload at full size: O [1,2,1024,64] and 16 exclusive chunk states."""
+    cfg = inputs.WORKLOADS[1]
+    q, k, v = (inputs.make(cfg, w).cuda() for w in ("q", "k", "v"))
+    o, fin, cs = la.fwd(q, k, v, want_final=True, want_chunk_states=True)
+    torch.cuda.synchronize()
+    ro, rcs, rfin = oracle.fwd_recurrent(q.double().cpu().numpy(), k.double().cpu().numpy(),
+                                         v.double().cpu().numpy(), chunk=64)
+    assert cs.shape == (1, 2, 16, 64, 64)
+    assert rel(o, ro) <= 1e-4
+    assert rel(cs, rcs) <= 1e-4
+    assert rel(fin, rfin) <= 1e-4
+    assert float(cs[:, :, 0].abs().max()) == 0.0  # exclusive: chunk 0 enters with the zero state
+
+
+@pytest.mark.parametrize("dtype,d", [(torch.bfloat16, 128), (torch.bfloat16, 64), (torch.float32, 128),
+                                     (torch.float32, 64)])
+@pytest.mark.parametrize("T", [64, 200, 1000, 2048])
+@pytest.mark.parametrize("dk", [None, 0.5, "cfg"])
+def test_forward(dtype, d, T, dk):
+    B, H = 1, 3
+    c, dev = case(5 + T, B, H, T, d, dtype)
+    lam = decays(H, dk)
+    init = np.random.default_rng(T).standard_normal((B, H, d, d)) * 0.1
+    init = init.astype(np.float32).astype(np.float64)
+    o, fin, _ = run_fwd(c, dev, dtype, lam, init)
+    ro, _, rfin = oracle.fwd_recurrent(c["q"], c["k"], c["v"], lam=lam, init=init)
+    assert rel(o, ro) < TOL[dtype]
+    assert rel(fin, rfin) < TOL[dtype]
+
+
+def test_forward_many_groups_bf16():
+    """T long enough for several chunk groups per sequence (group scan and group init exercised)."""
+    B, H, T, d = 2, 2, 8192 + 128, 128
+    c, dev = case(11, B, H, T, d, torch.bfloat16, sigma=1 / np.sqrt(128))
+    for lam in (None, decays(H, "cfg")):
+        o, fin, _ = run_fwd(c, dev, torch.bfloat16, lam, None)
+        ro, _, rfin = oracle.fwd_recurrent(c["q"], c["k"], c["v"], lam=lam)
+        assert rel(o, ro) < 1e-2
+        assert rel(fin, rfin) < 1e-2
+
+
+def test_forward_empty_sequence():
+    q = torch.zeros(1, 2, 0, 128, dtype=torch.bfloat16, device="cuda")
+    init = torch.randn(1, 2, 128, 128, device="cuda")
+    o, fin, _ = la.fwd(q, q, q, init_state=init, want_final=True)
+    torch.cuda.synchronize()
+    assert o.numel() == 0 and torch.equal(fin, init)
+
+
+def test_forward_strided_segments_view():
+    """Segments of one long sequence passed as a batch through strides (no copies)."""
+    H, T, d, S = 2, 2048, 128, 4
+    c, dev = case(13, 1, H, T, d, torch.bfloat16)
+    seg = T // S
+    view = lambda x: x[0].view(H, S, seg, d).permute(1, 0, 2, 3)   # [S, H, seg, d]
+    q, k, v = (view(dev[w]) for w in ("q", "k", "v"))
+    U = la.chunk_states(k, v, seg)                                   # [1, S, H, d, d]
+    init, _ = la.state_scan(U[0].contiguous())                       # [S, H, d, d]
+    o_seg, _, _ = la.fwd(q, k, v, init_state=init)
+    o_one, _, _ = la.fwd(dev["q"], dev["k"], dev["v"])
+    torch.cuda.synchronize()
+    ro, _, _ = oracle.fwd_recurrent(c["q"], c["k"], c["v"])
+    got = o_seg.permute(1, 0, 2, 3).reshape(1, H, T, d)
+    assert rel(got, ro) < 1e-2
+    assert rel(o_one, ro) < 1e-2
+
+
+# ------------------------------------------------------------------ backward
+@pytest.mark.parametrize("dtype,d", [(torch.bfloat16, 128), (torch.bfloat16, 64), (torch.float32, 64)])
+@pytest.mark.parametrize("T", [64, 200, 1000, 2048])
+@pytest.mark.parametrize("dk", [None, 0.5, "cfg"])
+def test_backward(dtype, d, T, dk):
+    B, H = 1, 3
+    c, dev = case(7 + T, B, H, T, d, dtype)
+    lam = decays(H, dk)
+    init = (np.random.default_rng(T + 1).standard_normal((B, H, d, d)) * 0.1).astype(np.float32).astype(np.float64)
+    dec = None if lam is None else torch.from_numpy(lam).cuda()
+    dq, dk_, dv, dinit = la.bwd(dev["q"], dev["k"], dev["v"], dev["dO"], decay=dec,
+                                init_state=torch.from_numpy(init.astype(np.float32)).cuda(), want_dinit=True)
+    torch.cuda.synchronize()
+    rq, rk, rv, rinit = oracle.bwd_recurrent(c["q"], c["k"], c["v"], c["dO"], lam=lam, init=init)
+    tol = TOL[dtype]
+    assert rel(dq, rq) < tol
+    assert rel(dk_, rk) < tol
+    assert rel(dv, rv) < tol
+    assert rel(dinit, rinit) < tol
+
+
+def test_backward_many_groups_bf16():
+    B, H, T, d = 1, 2, 8192 + 64, 128
+    c, dev = case(17, B, H, T, d, torch.bfloat16, sigma=1 / np.sqrt(128))
+    for lam in (None, decays(H, "cfg")):
+        dec = None if lam is None else torch.from_numpy(lam).cuda()
+        dq, dk_, dv, dinit = la.bwd(dev["q"], dev["k"], dev["v"], dev["dO"], decay=dec, want_dinit=True)
+        torch.cuda.synchronize()
+        rq, rk, rv, rinit = oracle.bwd_recurrent(c["q"], c["k"], c["v"], c["dO"], lam=lam)
+        for got, ref in ((dq, rq), (dk_, rk), (dv, rv), (dinit, rinit)):
+            assert rel(got, ref) < 1e-2
+
+
+def test_device_status_clean_after_calls():
+    B, H, T, d = 1, 2, 1024, 128
+    c, dev = case(19, B, H, T, d, torch.bfloat16)
+    ws = la.workspace(dev["q"], la.OP_BWD)
+    la.bwd(dev["q"], dev["k"], dev["v"], dev["dO"], ws=ws)
+    assert la.device_status(ws) == la.OK

@@ -61,7 +61,11 @@ _SIGS = {
     "linattn_state_scan": ([_i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "linattn_device_status": ([_vp, _vp], _i32),
     "linattn_diag_mma": ([_i32, _vp, _vp, _vp, _vp], _i32),
+    "linattn_timing_enable": ([_i32], _i32),
+    "linattn_timing_collect": ([_i32, ctypes.POINTER(_i32), ctypes.POINTER(ctypes.c_float)], _i32),
+    "linattn_kernel_name": ([_i32], ctypes.c_char_p),
 }
+KERNEL_KINDS = 8
 
 
 def lib():
@@ -133,6 +137,24 @@ def linattn_device_status(ws, stream) -> int:
 
 def linattn_diag_mma(mode, A, B, D, stream) -> int:
     return lib().linattn_diag_mma(mode, A, B, D, stream)
+
+
+def linattn_timing_enable(on: bool) -> int:
+    return lib().linattn_timing_enable(1 if on else 0)
+
+
+def linattn_timing_collect() -> dict:
+    """{kernel name: (launches, total ms)} of the launches recorded since the last collect."""
+    n = (_i32 * KERNEL_KINDS)()
+    ms = (ctypes.c_float * KERNEL_KINDS)()
+    st = lib().linattn_timing_collect(KERNEL_KINDS, n, ms)
+    if st < 0:
+        raise LinattnError(st, "linattn_timing_collect")
+    return {linattn_kernel_name(k): (n[k], ms[k]) for k in range(KERNEL_KINDS) if n[k]}
+
+
+def linattn_kernel_name(kind: int) -> str:
+    return lib().linattn_kernel_name(kind).decode()
 
 
 # ------------------------------------------------------------------ torch helpers

@@ -6,6 +6,7 @@
 #include <cudaTypedefs.h>
 
 #include <mutex>
+#include <vector>
 
 #include "../../include/linattn.h"
 #include "internal.h"
@@ -57,6 +58,44 @@ bool make_tmap_bf16(void *map, const void *base, const uint64_t dims[4], const u
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------------ per-kernel timing
+namespace {
+struct TimingState {
+  std::mutex mu;
+  bool on = false;
+  std::vector<cudaEvent_t> pool;  // pairs (start, stop), reused across collections
+  struct Rec { int kind; int slot; };
+  std::vector<Rec> recs;
+  int used = 0;
+};
+TimingState &timing() {
+  static TimingState t;
+  return t;
+}
+}  // namespace
+
+TimedLaunch::TimedLaunch(int k, cudaStream_t s) : kind(k), slot(-1), stream(s) {
+  TimingState &t = timing();
+  std::lock_guard<std::mutex> g(t.mu);
+  if (!t.on) return;
+  if (t.used * 2 + 2 > (int)t.pool.size()) {
+    cudaEvent_t a, b;
+    if (cudaEventCreate(&a) != cudaSuccess) return;
+    if (cudaEventCreate(&b) != cudaSuccess) { cudaEventDestroy(a); return; }
+    t.pool.push_back(a);
+    t.pool.push_back(b);
+  }
+  slot = t.used++;
+  cudaEventRecord(t.pool[2 * slot], s);
+}
+TimedLaunch::~TimedLaunch() {
+  if (slot < 0) return;
+  TimingState &t = timing();
+  std::lock_guard<std::mutex> g(t.mu);
+  cudaEventRecord(t.pool[2 * slot + 1], stream);
+  t.recs.push_back({kind, slot});
 }
 
 // ------------------------------------------------------------------ validation
@@ -318,6 +357,46 @@ int32_t linattn_device_status(const void *workspace, void *stream) {
     return LINATTN_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return LINATTN_ERR_CUDA;
   return h;
+}
+
+int32_t linattn_timing_enable(int32_t on) {
+  TimingState &t = timing();
+  std::lock_guard<std::mutex> g(t.mu);
+  t.on = on != 0;
+  return LINATTN_OK;
+}
+
+int32_t linattn_timing_collect(int32_t max_kinds, int32_t *launches, float *total_ms) {
+  if (max_kinds < 0 || (max_kinds > 0 && (!launches || !total_ms))) return LINATTN_ERR_INVALID;
+  TimingState &t = timing();
+  std::lock_guard<std::mutex> g(t.mu);
+  for (int k = 0; k < max_kinds; ++k) {
+    launches[k] = 0;
+    total_ms[k] = 0.f;
+  }
+  int status = LINATTN_OK;
+  for (const auto &r : t.recs) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(t.pool[2 * r.slot + 1]) != cudaSuccess ||
+        cudaEventElapsedTime(&ms, t.pool[2 * r.slot], t.pool[2 * r.slot + 1]) != cudaSuccess) {
+      status = LINATTN_ERR_CUDA;
+      continue;
+    }
+    if (r.kind < max_kinds) {
+      launches[r.kind] += 1;
+      total_ms[r.kind] += ms;
+    }
+  }
+  t.recs.clear();
+  t.used = 0;
+  return status == LINATTN_OK ? (int32_t)K_KINDS : status;
+}
+
+const char *linattn_kernel_name(int32_t kind) {
+  static const char *names[K_KINDS] = {"simt_fwd", "simt_bwd", "simt_segment_states", "state_scan",
+                                       "tc_segment_aggregate", "tc_chunked_fwd", "tc_chunked_rev",
+                                       "diag_mma"};
+  return (kind >= 0 && kind < K_KINDS) ? names[kind] : "?";
 }
 
 int32_t linattn_diag_mma(int32_t mode, const void *A, const void *B, float *D, void *stream) {

@@ -116,6 +116,7 @@ cudaError_t diag_mma(int mode, const void *A, const void *B, float *D, cudaStrea
   const size_t sm = 2 * kTileBytes + 1024 + 64;
   cudaError_t e = cudaFuncSetAttribute(diag_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return e;
+  TimedLaunch t(K_DIAG, s);
   diag_mma_kernel<<<1, 128, sm, s>>>(mA, mB, mode, D);
   return cudaGetLastError();
 }

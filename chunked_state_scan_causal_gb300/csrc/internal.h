@@ -18,6 +18,19 @@ struct Problem {
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// ---------------------------------------------------------------- per-kernel timing (api.cu)
+enum KernelKind {
+  K_SIMT_FWD = 0, K_SIMT_BWD, K_SIMT_SEGMENT, K_SCAN, K_TC_AGG, K_TC_MAIN_FWD, K_TC_MAIN_REV, K_DIAG,
+  K_KINDS
+};
+// Records timing events around one launch on `s` while timing is enabled.
+struct TimedLaunch {
+  TimedLaunch(int kind, cudaStream_t s);
+  ~TimedLaunch();
+  int kind, slot;
+  cudaStream_t stream;
+};
+
 // ---------------------------------------------------------------- SIMT path (simt.cu)
 cudaError_t simt_fwd(const Problem &p, const void *q, const void *k, const void *v, void *o,
                      const float *init, float *final_state, float *chunk_states, cudaStream_t s);

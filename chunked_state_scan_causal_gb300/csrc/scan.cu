@@ -219,6 +219,7 @@ cudaError_t state_scan(int G, int BH, int DD, const float *seg_decay, const floa
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int64_t want = (nt + kWarps - 1) / kWarps;
   const int grid = (int)(want < (int64_t)sms * 8 ? want : (int64_t)sms * 8);
+  TimedLaunch t(K_SCAN, s);
   scan_kernel<<<grid, kWarps * 32, 0, s>>>(A);
   return cudaGetLastError();
 }

@@ -273,6 +273,7 @@ cudaError_t launch_fwd(const Problem &p, const void *q, const void *k, const voi
   const size_t sm = fwd_smem<D>();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return e;
+  TimedLaunch t(K_SIMT_FWD, s);
   kern<<<p.B * p.H, kThreads, sm, s>>>(p, (const TIn *)q, (const TIn *)k, (const TIn *)v, (TIn *)o,
                                         init, fin, cs);
   return cudaGetLastError();
@@ -284,6 +285,7 @@ cudaError_t launch_bwd(const Problem &p, const void *q, const void *k, const voi
   const size_t sm = bwd_smem<D>();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return e;
+  TimedLaunch t(K_SIMT_BWD, s);
   kern<<<p.B * p.H, kThreads, sm, s>>>(p, (const TIn *)q, (const TIn *)k, (const TIn *)v,
                                         (const TIn *)dO, init, (TIn *)dq, (TIn *)dk, (TIn *)dv, dinit);
   return cudaGetLastError();
@@ -296,6 +298,7 @@ cudaError_t launch_seg(const Problem &p, int seg_len, const void *k, const void 
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return e;
   const int G = (p.T + seg_len - 1) / seg_len;
+  TimedLaunch t(K_SIMT_SEGMENT, s);
   kern<<<dim3(p.B * p.H, G), kThreads, sm, s>>>(p, seg_len, (const TIn *)k, (const TIn *)v, out);
   return cudaGetLastError();
 }

@@ -584,6 +584,7 @@ cudaError_t tc_segment_states(const Problem &p, int seg_len, const void *X, cons
   const size_t smem = 3 * 2 * kTileBytes + 1024 + 256;
   const int grid = A.nitems < p.num_sms ? A.nitems : p.num_sms;
   cudaError_t e;
+  TimedLaunch t(K_TC_AGG, s);
   if (p.decay) {
     if ((e = set_smem(tc_agg_kernel<true>, smem)) != cudaSuccess) return e;
     tc_agg_kernel<true><<<grid, kThreads, smem, s>>>(mx, my, A);
@@ -608,6 +609,7 @@ cudaError_t tc_main(const Problem &p, int group_len, bool reverse, const void *q
   M.decay = p.decay; M.ginit = group_init; M.final_state = final_state; M.status = status;
   const int grid = M.nitems < p.num_sms ? M.nitems : p.num_sms;
   cudaError_t e;
+  TimedLaunch t(reverse ? K_TC_MAIN_REV : K_TC_MAIN_FWD, s);
 #define LINATTN_LAUNCH_MAIN(DEC, REV)                                              \
   do {                                                                             \
     if ((e = set_smem(tc_main_kernel<DEC, REV>, kMainSmem)) != cudaSuccess) return e; \

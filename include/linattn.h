@@ -146,6 +146,20 @@ int32_t linattn_state_scan(int32_t G, int32_t BH, int32_t dk, int32_t dv, const 
  * (LINATTN_OK, or e.g. LINATTN_ERR_DEVICE_TIMEOUT) or LINATTN_ERR_CUDA. */
 int32_t linattn_device_status(const void *workspace, void *stream);
 
+/* Per-kernel timing (diagnostics for measurement, not part of the method).
+ * While enabled for the process, every kernel the library launches is
+ * bracketed by two CUDA timing events recorded on its launch stream (the
+ * events come from a pool created on first use; no device memory is
+ * allocated).  linattn_timing_collect synchronises the recorded events, writes
+ * for every kernel kind k < max_kinds its launch count and summed device time
+ * (ms), clears the record and returns the number of kinds
+ * (LINATTN_KERNEL_KINDS), or a negative status. */
+#define LINATTN_KERNEL_KINDS 8
+int32_t linattn_timing_enable(int32_t on);
+int32_t linattn_timing_collect(int32_t max_kinds, int32_t *launches, float *total_ms);
+/* Name of kernel kind k (static string; "?" when out of range). */
+const char *linattn_kernel_name(int32_t kind);
+
 /* Diagnostic (not part of the method): one 128x128x128 bf16 tensor-core
  * product through the same shared-memory layouts the kernels use, written as
  * fp32 D[128][128].  A and B are 128x128 bf16 row-major device arrays.

@@ -1,0 +1,367 @@
+"""Benchmark of chunked causal linear attention (forward + backward) on GB300.
+
+One step = the whole hot path over one batch: linattn_fwd (segment aggregates,
+state scan, chunked forward) then linattn_bwd (forward states recomputed,
+reverse states, dq / dv / dk passes) on the synthetic workload
+B=2, H=16, T=65536, d=128, bf16, lambda=1 (seeded; q, k, v ~ N(0, 0.125^2),
+dO ~ N(0, 1)).  Prints ONE JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload 3]
+
+--impl reference times the fp64 CPU oracle on a bounded sample of the same
+workload (the reference arm of this benchmark: there is no upstream code).
+Under torchrun each rank runs an independent replica (weak scaling); only
+rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "causal linear-attn fwd+bwd tokens/s & TFLOP/s @H16 d128 T16K–1M; % roofline"
+# algorithmic work per token per head at d = 128 (chunk 64): forward 4d(C+d) FLOP and
+# q,k,v read + o written; backward 8d(C+d) FLOP and q,k,v,dO read + dq,dk,dv written.
+FLOP_FWD, FLOP_BWD = 98304, 196608
+BYTES_FWD, BYTES_BWD = 1024, 1792
+# one launch of the chunked kernel reads three bf16 sequence tensors and writes one
+MAIN_BYTES_PER_TOKEN_HEAD = 1024
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def dist_max(x: float, device=None) -> float:
+    """Maximum of x over the ranks of the default process group (x itself when not distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_throughput(units_per_rank: float, ms_per_step_max: float, world: int) -> float:
+    """Units all ranks processed per second, timed by the slowest rank (weak scaling)."""
+    return units_per_rank * world / (ms_per_step_max * 1e-3)
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 6800.0, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _gpu_uuid(dev):
+    import torch
+    try:
+        u = torch.cuda.get_device_properties(dev).uuid
+        s = str(u)
+        return s if s.startswith("GPU-") else "GPU-" + s
+    except Exception:
+        return None
+
+
+def _profile_traffic():
+    """DRAM bytes per token-head of the chunked kernel from the committed ncu summary, if any."""
+    path = os.path.join(ROOT, "profiles", "tc_chunked_fwd_traffic.txt")
+    try:
+        with open(path) as f:
+            for ln in f:
+                if ln.startswith("dram_bytes_per_token_head"):
+                    return float(ln.split("=")[1])
+    except Exception:
+        pass
+    return None
+
+
+# ---------------------------------------------------------------------------------- reference arm
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    from chunked_state_scan_causal_gb300 import inputs
+    cfg = inputs.WORKLOADS[args.workload]
+    oracle.build()
+    T = cfg["T"]
+    heads = list(range(min(cfg["H"], args.ref_heads)))
+    lam = inputs.workload_decay(cfg)
+    lam_s = None if lam is None else lam[heads]
+    x = {w: np.stack([inputs.make_head64(cfg, w, 0, h) for h in heads])[None] for w in ("q", "k", "v", "dO")}
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle.fwd_recurrent(x["q"], x["k"], x["v"], lam=lam_s)
+        oracle.bwd_recurrent(x["q"], x["k"], x["v"], x["dO"], lam=lam_s)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    sec = sum(times) / len(times)
+    tokens = T * len(heads) / cfg["H"]  # token equivalents of the full-head workload
+    value = tokens / sec
+    sample = f"batch row 0, heads 0..{len(heads) - 1} of {cfg['H']}, T={T}: fwd+bwd fp64 recurrence"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": cfg["name"], "B": cfg["B"], "H": cfg["H"], "T": T, "d": cfg["d"]},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.threads_used(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------------- our arm
+def run_ours(args):
+    import torch
+    import chunked_state_scan_causal_gb300 as la
+    from chunked_state_scan_causal_gb300 import build, inputs
+
+    ws_n, rank, local = _dist()
+    if ws_n > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build.build()
+    cfg = inputs.WORKLOADS[args.workload]
+    B, H, T, d = cfg["B"], cfg["H"], cfg["T"], cfg["d"]
+    lam = inputs.workload_decay(cfg)
+
+    # inputs: seeded on the host, pinned, copied once (the device-resident leg)
+    host = {w: inputs.make(cfg, w).pin_memory() for w in ("q", "k", "v", "dO")}
+    x = {w: t.to(dev, non_blocking=True) for w, t in host.items()}
+    decay = None if lam is None else torch.from_numpy(lam).to(dev)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+    o = torch.empty_like(x["q"])
+    grads = [torch.empty_like(x["q"]) for _ in range(3)]
+    ws_f = la.workspace(x["q"], la.OP_FWD, decay)
+    ws_b = la.workspace(x["q"], la.OP_BWD, decay)
+
+    def step():
+        la.fwd(x["q"], x["k"], x["v"], decay=decay, out=o, ws=ws_f)
+        la.bwd(x["q"], x["k"], x["v"], x["dO"], decay=decay, outs=grads, ws=ws_b)
+
+    def barrier():
+        if ws_n > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if la.device_status(ws_b) != la.OK or la.device_status(ws_f) != la.OK:
+        raise RuntimeError("device-side error during warm-up")
+
+    # ---- timed region (inputs are 512 MiB per tensor, 4x larger than L2: no flush needed)
+    la.linattn_timing_enable(True)
+    la.linattn_timing_collect()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(_gpu_uuid(dev)) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    la.linattn_timing_enable(False)
+    kernels = la.linattn_timing_collect()
+    ms = dist_max(e0.elapsed_time(e1) / args.steps, dev)
+    tokens_step = B * T * ws_n
+    value = whole_job_throughput(B * T, ms, ws_n)
+    flops = (FLOP_FWD + FLOP_BWD) * B * H * T
+    bytes_ = (BYTES_FWD + BYTES_BWD) * B * H * T
+    hbm, tf, peak_src = _peaks()
+
+    # ---- dominant kernel roofline (chunked kernel, forward and reverse-time launches)
+    launches = sum(n for n, _ in kernels.values())
+    main = [kernels.get("tc_chunked_fwd", (0, 0.0)), kernels.get("tc_chunked_rev", (0, 0.0))]
+    n_main = sum(n for n, _ in main)
+    ms_main = sum(t for _, t in main)
+    per_launch_bytes = MAIN_BYTES_PER_TOKEN_HEAD * B * H * T
+    avg_ms = ms_main / max(n_main, 1)
+    achieved = per_launch_bytes / (avg_ms * 1e-3) / 1e9 if n_main else None
+    traffic_tok = _profile_traffic()
+    roofline = {
+        "kernel": "tc_chunked (fwd + reverse-time launches)",
+        "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+        "frac": (achieved / hbm) if achieved else None,
+        "traffic": None if traffic_tok is None else traffic_tok * B * H * T,
+        "peak_source": f"{peak_src} hbm_gbs",
+        "launches_per_step": n_main / args.steps,
+        "share_of_step": ms_main / (ms * args.steps) if ms else None,
+    }
+    breakdown = {k: {"launches_per_step": n / args.steps, "ms_per_step": t / args.steps}
+                 for k, (n, t) in kernels.items()}
+
+    # ---- end to end through the public API with host buffers (H2D inputs, D2H outputs)
+    h_out = [torch.empty(x["q"].shape, dtype=x["q"].dtype, pin_memory=True) for _ in range(4)]
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in h_out)
+
+    def e2e_step():
+        for w in x:
+            x[w].copy_(host[w], non_blocking=True)
+        step()
+        for h, t in zip(h_out, [o] + grads):
+            h.copy_(t, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    e2 = torch.cuda.Event(enable_timing=True)
+    e3 = torch.cuda.Event(enable_timing=True)
+    n_e2e = max(3, args.steps // 3)
+    e2.record(stream)
+    for _ in range(n_e2e):
+        e2e_step()
+    e3.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = dist_max(e2.elapsed_time(e3) / n_e2e, dev)
+
+    # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only)
+    cpu = None
+    if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
+        import numpy as np
+        import oracle
+        oracle.build()
+        heads = list(range(min(H, args.cpu_heads)))
+        xs = {w: np.stack([inputs.make_head64(cfg, w, 0, h) for h in heads])[None]
+              for w in ("q", "k", "v", "dO")}
+        lam_s = None if lam is None else lam[heads]
+        t0 = time.perf_counter()
+        oracle.fwd_recurrent(xs["q"], xs["k"], xs["v"], lam=lam_s)
+        oracle.bwd_recurrent(xs["q"], xs["k"], xs["v"], xs["dO"], lam=lam_s)
+        sec = time.perf_counter() - t0
+        cpu = {"value": T * len(heads) / H / sec, "unit": "tokens/s", "cores": oracle.threads_used(),
+               "kind": "oracle",
+               "sample": f"batch row 0, heads 0..{len(heads) - 1} of {H}, T={T}, fwd+bwd fp64 recurrence, "
+                         f"{sec:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws_n, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded normal; no dataset)",
+            "config": {"workload": cfg["name"], "B": B, "H": H, "T": T, "d": d, "chunk": 64,
+                       "decay": "per-head" if lam is not None else "none",
+                       "l2": "inputs 512 MiB per tensor > L2 (no flush)",
+                       "step": "linattn_fwd + linattn_bwd", "parallelism": f"replicas x{ws_n}"},
+            "tflops": flops / (ms * 1e-3) / 1e12,
+            "algorithmic_gbs": bytes_ / (ms * 1e-3) / 1e9,
+            "path_roofline_frac": max(flops / (tf * 1e12), bytes_ / (hbm * 1e9)) / (ms * 1e-3),
+            "roofline": roofline,
+            "kernels": breakdown,
+            "gpu_launches": launches,
+            "clocks": clk.summary(),
+            "e2e": {"value": whole_job_throughput(B * T, ms_e2e, ws_n), "unit": "tokens/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": ms_e2e},
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if ws_n > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=3)
+    ap.add_argument("--ref-heads", type=int, default=4, help="heads per step of the reference arm")
+    ap.add_argument("--cpu-heads", type=int, default=16, help="heads of the cpu_baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

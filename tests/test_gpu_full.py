@@ -1,0 +1,102 @@
+"""Full-size workloads through the C ABI, checked against the fp64 oracle on sampled heads.
+
+Each workload runs at its full shape in the launch configuration the benchmark
+times; the oracle recomputes whole sequences of a few sampled (batch, head)
+pairs (independent of the others), and properties that hold at any size
+(segmented == unsegmented, device status clean) are checked on everything.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import chunked_state_scan_causal_gb300 as la
+from chunked_state_scan_causal_gb300 import inputs
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+
+def rel(got, ref):
+    got = got.detach().double().cpu().numpy() if torch.is_tensor(got) else got
+    return float(np.max(np.abs(got - ref))) / max(float(np.max(np.abs(ref))), 1e-30)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from chunked_state_scan_causal_gb300 import build
+    build.build()
+
+
+def load(cfg, which=("q", "k", "v")):
+    return {w: inputs.make(cfg, w).cuda() for w in which}
+
+
+def heads64(cfg, pairs, which):
+    return {w: np.stack([inputs.make_head64(cfg, w, b, h) for b, h in pairs])[None] for w in which}
+
+
+def lam_of(cfg, pairs):
+    lam = inputs.workload_decay(cfg)
+    return None if lam is None else np.array([lam[h] for _, h in pairs], dtype=np.float32)
+
+
+def test_workload2_forward_full_size():
+    cfg = inputs.WORKLOADS[2]
+    x = load(cfg)
+    o, fin, _ = la.fwd(x["q"], x["k"], x["v"], want_final=True)
+    torch.cuda.synchronize()
+    pairs = [(0, 0), (1, 7), (3, 15)]
+    ref = heads64(cfg, pairs, ("q", "k", "v"))
+    ro, _, rfin = oracle.fwd_recurrent(ref["q"], ref["k"], ref["v"])
+    for i, (b, h) in enumerate(pairs):
+        assert rel(o[b, h], ro[0, i]) < 1e-2, (b, h)
+        assert rel(fin[b, h], rfin[0, i]) < 1e-2, (b, h)
+
+
+@pytest.mark.parametrize("wl", [3, 4])
+def test_forward_backward_full_size(wl):
+    cfg = inputs.WORKLOADS[wl]
+    x = load(cfg, ("q", "k", "v", "dO"))
+    lam = inputs.workload_decay(cfg)
+    dec = None if lam is None else torch.from_numpy(lam).cuda()
+    o, _, _ = la.fwd(x["q"], x["k"], x["v"], decay=dec)
+    dq, dk, dv, dinit = la.bwd(x["q"], x["k"], x["v"], x["dO"], decay=dec, want_dinit=True)
+    torch.cuda.synchronize()
+    H = cfg["H"]
+    pairs = [(0, 0), (cfg["B"] - 1, H - 1), (0, H // 2)]
+    ref = heads64(cfg, pairs, ("q", "k", "v", "dO"))
+    ls = lam_of(cfg, pairs)
+    ro, _, _ = oracle.fwd_recurrent(ref["q"], ref["k"], ref["v"], lam=ls)
+    rq, rk, rv, rinit = oracle.bwd_recurrent(ref["q"], ref["k"], ref["v"], ref["dO"], lam=ls)
+    for i, (b, h) in enumerate(pairs):
+        for name, got, r in (("o", o, ro), ("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv), ("dinit", dinit, rinit)):
+            assert rel(got[b, h], r[0, i]) < 1e-2, (name, b, h)
+
+
+def test_workload5_segmented_equals_single_and_oracle():
+    """64 segments x 16384: segment states -> exclusive scan -> per-segment forward == one forward."""
+    cfg = inputs.WORKLOADS[5]
+    H, T, d, L = cfg["H"], cfg["T"], cfg["d"], cfg["seg_len"]
+    S = T // L
+    x = load(cfg)
+    seg = lambda t: t[0].view(H, S, L, d).permute(1, 0, 2, 3)        # [64, 16, 16384, 128] view
+    U = la.chunk_states(x["k"], x["v"], L)                            # [64, 1, 16, 128, 128]
+    init, total = la.state_scan(U.view(S, H, d, d), want_total=True)  # [64, 16, 128, 128]
+    o_seg, _, _ = la.fwd(seg(x["q"]), seg(x["k"]), seg(x["v"]), init_state=init)
+    o_one, fin, _ = la.fwd(x["q"], x["k"], x["v"], want_final=True)
+    torch.cuda.synchronize()
+    # property at full size: every output of the segmented run equals the single run
+    diff = (o_seg.permute(1, 0, 2, 3).reshape(1, H, T, d).float() - o_one.float()).abs().max().item()
+    assert diff / o_one.float().abs().max().item() < 1e-2
+    assert rel(total, fin.double().cpu().numpy()) < 1e-2
+    # oracle on sampled heads: segment states, their scan, and the outputs
+    pairs = [(0, 0), (0, H - 1)]
+    ref = heads64(cfg, pairs, ("q", "k", "v"))
+    rU = oracle.segment_states(ref["k"], ref["v"], L)                 # [64, 1, 2, d, d]
+    rS, _ = oracle.state_scan(rU)
+    ro, _, _ = oracle.fwd_recurrent(ref["q"], ref["k"], ref["v"])
+    for i, (_, h) in enumerate(pairs):
+        assert rel(U[:, 0, h], rU[:, 0, i]) < 1e-2
+        assert rel(init[:, h], rS[:, 0, i]) < 1e-2
+        assert rel(o_one[0, h], ro[0, i]) < 1e-2
+        assert rel(o_seg[:, h].reshape(T, d), ro[0, i]) < 1e-2

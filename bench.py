@@ -200,7 +200,11 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     build.build()
-    cfg = inputs.WORKLOADS[args.workload]
+    cfg = dict(inputs.WORKLOADS[args.workload])
+    if args.B:
+        cfg["B"] = args.B
+    if args.T:
+        cfg["T"] = args.T
     B, H, T, d = cfg["B"], cfg["H"], cfg["T"], cfg["d"]
     lam = inputs.workload_decay(cfg)
 
@@ -274,7 +278,8 @@ def run_ours(args):
                  for k, (n, t) in kernels.items()}
 
     # ---- end to end through the public API with host buffers (H2D inputs, D2H outputs)
-    h_out = [torch.empty(x["q"].shape, dtype=x["q"].dtype, pin_memory=True) for _ in range(4)]
+    h_out = [torch.empty(x["q"].shape, dtype=x["q"].dtype, pin_memory=True) for _ in range(4)] \
+        if not args.no_e2e else []
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = sum(t.numel() * t.element_size() for t in h_out)
 
@@ -285,18 +290,20 @@ def run_ours(args):
         for h, t in zip(h_out, [o] + grads):
             h.copy_(t, non_blocking=True)
 
-    e2e_step()
-    torch.cuda.synchronize()
-    barrier()
-    e2 = torch.cuda.Event(enable_timing=True)
-    e3 = torch.cuda.Event(enable_timing=True)
-    n_e2e = max(3, args.steps // 3)
-    e2.record(stream)
-    for _ in range(n_e2e):
+    ms_e2e = None
+    if not args.no_e2e:
         e2e_step()
-    e3.record(stream)
-    torch.cuda.synchronize()
-    ms_e2e = dist_max(e2.elapsed_time(e3) / n_e2e, dev)
+        torch.cuda.synchronize()
+        barrier()
+        e2 = torch.cuda.Event(enable_timing=True)
+        e3 = torch.cuda.Event(enable_timing=True)
+        n_e2e = max(3, args.steps // 3)
+        e2.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e3.record(stream)
+        torch.cuda.synchronize()
+        ms_e2e = dist_max(e2.elapsed_time(e3) / n_e2e, dev)
 
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only)
     cpu = None
@@ -333,9 +340,9 @@ def run_ours(args):
             "kernels": breakdown,
             "gpu_launches": launches,
             "clocks": clk.summary(),
-            "e2e": {"value": whole_job_throughput(B * T, ms_e2e, ws_n), "unit": "tokens/s",
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "ms_per_step": ms_e2e},
+            "e2e": None if ms_e2e is None else {
+                "value": whole_job_throughput(B * T, ms_e2e, ws_n), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
@@ -354,6 +361,9 @@ def main():
     ap.add_argument("--ref-heads", type=int, default=4, help="heads per step of the reference arm")
     ap.add_argument("--cpu-heads", type=int, default=16, help="heads of the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--B", type=int, default=0, help="override the batch size (profiling cases)")
+    ap.add_argument("--T", type=int, default=0, help="override the sequence length (profiling cases)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -44,14 +44,32 @@ __device__ __forceinline__ void st_release(unsigned *p, unsigned v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+constexpr unsigned kBatch = 16;  // tickets taken per atomic (look-back case)
+
 __global__ void __launch_bounds__(kWarps * 32) scan_kernel(ScanArgs A) {
   const int lane = threadIdx.x & 31;
   const int64_t E = (int64_t)A.BH * A.DD;
   const unsigned ntiles = (unsigned)A.ntg * (unsigned)A.ncg;
+  // Without look-back (one segment tile) tiles are independent: plain grid
+  // stride.  With look-back, tickets come in order from an atomic counter, a
+  // batch of kBatch per warp; a warp works through its batch in order, so
+  // every tile a warp waits on belongs to a warp that is already running.
+  const unsigned gwarp = blockIdx.x * kWarps + threadIdx.x / 32, nwarp = gridDim.x * kWarps;
+  unsigned next = gwarp, end = 0;
   while (true) {
-    unsigned ticket = 0;
-    if (lane == 0) ticket = atomicAdd(A.counter, 1u);
-    ticket = __shfl_sync(0xffffffffu, ticket, 0);
+    unsigned ticket;
+    if (A.ntg == 1) {
+      ticket = next;
+      next += nwarp;
+    } else {
+      if (next >= end) {
+        unsigned base = 0;
+        if (lane == 0) base = atomicAdd(A.counter, kBatch);
+        next = __shfl_sync(0xffffffffu, base, 0);
+        end = next + kBatch;
+      }
+      ticket = next++;
+    }
     if (ticket >= ntiles) break;
     const int tg = (int)(ticket / A.ncg), cg = (int)(ticket % A.ncg);
     const int64_t e0 = (int64_t)cg * kVec;
@@ -105,7 +123,6 @@ __global__ void __launch_bounds__(kWarps * 32) scan_kernel(ScanArgs A) {
       for (int i = 0; i < kVec; ++i) pin[i] = 0.f;
       float fac = 1.f;
       int pred = tg - 1;
-      bool failed = false;
       while (true) {
         const unsigned pt = (unsigned)pred * A.ncg + cg;
         unsigned f = 0;
@@ -123,7 +140,7 @@ __global__ void __launch_bounds__(kWarps * 32) scan_kernel(ScanArgs A) {
           }
         }
         f = __shfl_sync(0xffffffffu, f, 0);
-        if (f == 3) { failed = true; break; }
+        if (f == 3) break;
         const float *src = (f == 2 ? A.incl : A.agg) + (int64_t)pt * kVec;
 #pragma unroll
         for (int i = 0; i < kVec; ++i) pin[i] = fmaf(fac, __ldcg(src + i), pin[i]);
@@ -138,7 +155,6 @@ __global__ void __launch_bounds__(kWarps * 32) scan_kernel(ScanArgs A) {
           break;
         }
       }
-      (void)failed;
     }
     // publish the inclusive prefix of this tile
     if (tg + 1 < A.ntg && lane == 31) {
@@ -212,8 +228,10 @@ cudaError_t state_scan(int G, int BH, int DD, const float *seg_decay, const floa
   const size_t head = align256(256 + nt * 4);
   A.agg = reinterpret_cast<float *>(w + head);
   A.incl = reinterpret_cast<float *>(w + head + align256(nt * kVec * 4));
-  cudaError_t e = cudaMemsetAsync(w, 0, head, s);
-  if (e != cudaSuccess) return e;
+  if (A.ntg > 1) {  // ticket counter and look-back flags start at zero
+    cudaError_t e = cudaMemsetAsync(w, 0, head, s);
+    if (e != cudaSuccess) return e;
+  }
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);

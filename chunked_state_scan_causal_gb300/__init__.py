@@ -25,6 +25,8 @@ ERR_WORKSPACE = -4
 ERR_CUDA = -5
 ERR_DEVICE_TIMEOUT = -6
 ERR_DEVICE = -7
+ERR_SCRATCH_LIMIT = -8
+NOALLOC_MAX_TILES = 65536
 BF16, F32 = 0, 1
 OP_FWD, OP_BWD, OP_CHUNK_STATES = 1, 2, 3
 ABI_VERSION = 1
@@ -60,6 +62,7 @@ _SIGS = {
     "linattn_state_scan_workspace_size": ([_i32, _i32, _i32, _i32, ctypes.POINTER(_sz)], _i32),
     "linattn_state_scan": ([_i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "linattn_device_status": ([_vp, _vp], _i32),
+    "linattn_state_scan_noalloc": ([_i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp], _i32),
     "linattn_diag_mma": ([_i32, _vp, _vp, _vp, _vp], _i32),
     "linattn_timing_enable": ([_i32], _i32),
     "linattn_timing_collect": ([_i32, ctypes.POINTER(_i32), ctypes.POINTER(ctypes.c_float)], _i32),
@@ -129,6 +132,12 @@ def linattn_state_scan_workspace_size(G, BH, dk, dv) -> tuple[int, int]:
 
 def linattn_state_scan(G, BH, dk, dv, seg_decay, local, init, out, total, ws, ws_bytes, stream) -> int:
     return lib().linattn_state_scan(G, BH, dk, dv, seg_decay, local, init, out, total, ws, ws_bytes, stream)
+
+
+def linattn_state_scan_noalloc(G, BH, dk, dv, seg_decay, local, init, out, total, device_status, stream) -> int:
+    """Allocation-free scan: no workspace; the library's fixed device scratch is used instead."""
+    return lib().linattn_state_scan_noalloc(G, BH, dk, dv, seg_decay, local, init, out, total, device_status,
+                                            stream)
 
 
 def linattn_device_status(ws, stream) -> int:

@@ -14,7 +14,7 @@
 namespace linattn {
 
 // ------------------------------------------------------------------ device checks
-static int device_ok() {
+int device_ok() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return LINATTN_ERR_CUDA;
   int major = 0, minor = 0;
@@ -199,6 +199,7 @@ const char *linattn_status_string(int32_t s) {
     case LINATTN_ERR_CUDA: return "CUDA call failed";
     case LINATTN_ERR_DEVICE_TIMEOUT: return "device-side bounded wait timed out";
     case LINATTN_ERR_DEVICE: return "current device is not sm_103";
+    case LINATTN_ERR_SCRATCH_LIMIT: return "request exceeds the fixed scratch of the allocation-free entry point";
     default: return "unknown status";
   }
 }

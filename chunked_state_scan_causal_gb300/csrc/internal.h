@@ -18,6 +18,9 @@ struct Problem {
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// LINATTN_OK when the current device is an sm_103 GPU (api.cu).
+int device_ok();
+
 // ---------------------------------------------------------------- per-kernel timing (api.cu)
 enum KernelKind {
   K_SIMT_FWD = 0, K_SIMT_BWD, K_SIMT_SEGMENT, K_SCAN, K_TC_AGG, K_TC_MAIN_FWD, K_TC_MAIN_REV, K_DIAG,

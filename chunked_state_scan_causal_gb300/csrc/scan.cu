@@ -16,6 +16,9 @@
 //    ticket in segment-tile-major order, so every predecessor of a waiting
 //    tile is already running; each tile publishes its aggregate at once and
 //    its inclusive prefix after the look-back; waits are bounded.
+#include <mutex>
+
+#include "../../include/linattn.h"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -243,3 +246,65 @@ cudaError_t state_scan(int G, int BH, int DD, const float *seg_decay, const floa
 }
 
 }  // namespace linattn
+
+// ============================================================================
+// Allocation-free entry point: the same scan with its scratch in a fixed
+// static device array (see linattn_state_scan_noalloc in linattn.h).
+namespace linattn {
+namespace {
+static_assert(LINATTN_NOALLOC_SCRATCH_BYTES == 256 + 4 * LINATTN_NOALLOC_MAX_TILES +
+                                                   2 * LINATTN_NOALLOC_MAX_TILES * kVec * 4,
+              "scratch size must cover the scan's workspace layout at the tile limit");
+static __device__ __align__(256) unsigned char g_noalloc_scratch[LINATTN_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void *g_noalloc_addr[kMaxDevices] = {};
+
+// Device address of the scratch for the current device, looked up once per
+// device (with that device current).  In host code the symbol itself is only a
+// host-side stand-in, never a device address.
+cudaError_t noalloc_scratch(void **ptr) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> g(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    g_noalloc_addr[dev] = p;
+  }
+  *ptr = g_noalloc_addr[dev];
+  return cudaSuccess;
+}
+}  // namespace
+}  // namespace linattn
+
+extern "C" int32_t linattn_state_scan_noalloc(int32_t G, int32_t BH, int32_t dk, int32_t dv,
+                                              const float *seg_decay, const float *local_states,
+                                              const float *init, float *init_states, float *total,
+                                              int32_t *device_status, void *stream) {
+  using namespace linattn;
+  if (G < 1 || BH < 1 || dk < 1 || dv < 1) return LINATTN_ERR_INVALID;
+  const int64_t DD = (int64_t)dk * dv;
+  if (DD % kVec) return LINATTN_ERR_UNSUPPORTED;
+  if (!local_states || !init_states) return LINATTN_ERR_INVALID;
+  for (const void *x : {(const void *)seg_decay, (const void *)local_states, (const void *)init,
+                        (const void *)init_states, (const void *)total, (const void *)device_status})
+    if (reinterpret_cast<uintptr_t>(x) & 15u) return LINATTN_ERR_ALIGN;
+  const int64_t ntiles = (int64_t)((G + 31) / 32) * ((int64_t)BH * DD / kVec);
+  if (ntiles > LINATTN_NOALLOC_MAX_TILES) return LINATTN_ERR_SCRATCH_LIMIT;
+  int st = device_ok();
+  if (st != LINATTN_OK) return st;
+  void *scratch = nullptr;
+  if (noalloc_scratch(&scratch) != cudaSuccess) return LINATTN_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (device_status && cudaMemsetAsync(device_status, 0, sizeof(int32_t), s) != cudaSuccess)
+    return LINATTN_ERR_CUDA;
+  // state_scan clears the ticket counter and the look-back flags itself
+  cudaError_t e = state_scan(G, BH, (int)DD, seg_decay, nullptr, 1, 1, false, local_states, init,
+                             init_states, total, scratch, reinterpret_cast<int *>(device_status), s);
+  return e == cudaSuccess ? LINATTN_OK : LINATTN_ERR_CUDA;
+}

@@ -57,7 +57,8 @@ enum {
   LINATTN_ERR_WORKSPACE = -4,      /* workspace missing, too small or not 256-B aligned */
   LINATTN_ERR_CUDA = -5,           /* a CUDA runtime / driver call failed            */
   LINATTN_ERR_DEVICE_TIMEOUT = -6, /* device status: a bounded wait gave up          */
-  LINATTN_ERR_DEVICE = -7          /* current device is not an sm_103 GPU            */
+  LINATTN_ERR_DEVICE = -7,         /* current device is not an sm_103 GPU            */
+  LINATTN_ERR_SCRATCH_LIMIT = -8   /* request exceeds the fixed scratch of linattn_state_scan_noalloc */
 };
 
 /* Element type of the sequence tensors (states are always fp32). */
@@ -141,6 +142,37 @@ int32_t linattn_state_scan_workspace_size(int32_t G, int32_t BH, int32_t dk, int
 int32_t linattn_state_scan(int32_t G, int32_t BH, int32_t dk, int32_t dv, const float *seg_decay,
                            const float *local_states, const float *init, float *init_states,
                            float *total, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Allocation-free variant of linattn_state_scan (the pages have no
+ * counterpart; this is a deployment convenience).  Some callers cannot call
+ * cudaMalloc at all: code embedded in a host application whose device memory
+ * is entirely owned by that application's own allocator or pool, and
+ * latency-critical paths where an allocation (which may synchronise the
+ * device) is not allowed.  Such callers cannot provide a workspace, so this
+ * entry point takes none: its scratch (ticket counter, look-back flags,
+ * per-tile aggregates and inclusive prefixes) is a fixed static device array
+ * of LINATTN_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that
+ * loads the library holds until the process exits.  Nothing is allocated:
+ * no cudaMalloc, cudaFree or allocating library routine is called.
+ *   - Same operands and results as linattn_state_scan.
+ *   - Limit: ceil(G/32) * (BH*dk*dv/8) <= LINATTN_NOALLOC_MAX_TILES (65536), e.g.
+ *     64 segments of 16 states of 128x128; larger requests return
+ *     LINATTN_ERR_SCRATCH_LIMIT before anything is enqueued.
+ *   - device_status: optional device int32 (NULL allowed) that is zeroed and
+ *     then receives LINATTN_ERR_DEVICE_TIMEOUT if a bounded look-back wait
+ *     gives up; there is no workspace status word in this variant.
+ *   - The first call on a device looks up the scratch's device address once
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - Every call uses the same scratch and leaves the last call's contents in
+ *     it; the call clears what must start at zero (counter, flags) on
+ *     `stream`.  Calls that overlap on the GPU (other streams, other host
+ *     threads) race on the scratch: serialise them.  Returns a status. */
+#define LINATTN_NOALLOC_MAX_TILES 65536
+#define LINATTN_NOALLOC_SCRATCH_BYTES (256 + 4 * LINATTN_NOALLOC_MAX_TILES + 64 * LINATTN_NOALLOC_MAX_TILES)
+int32_t linattn_state_scan_noalloc(int32_t G, int32_t BH, int32_t dk, int32_t dv, const float *seg_decay,
+                                   const float *local_states, const float *init, float *init_states,
+                                   float *total, int32_t *device_status, void *stream);
 
 /* Synchronises `stream`, then returns the device status word of `workspace`
  * (LINATTN_OK, or e.g. LINATTN_ERR_DEVICE_TIMEOUT) or LINATTN_ERR_CUDA. */

@@ -59,6 +59,7 @@ _SIGS = {
     "linattn_fwd": ([ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "linattn_bwd": ([ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "linattn_chunk_states": ([ctypes.POINTER(Shape), _i32, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
+    "linattn_decode": ([ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp], _i32),
     "linattn_state_scan_workspace_size": ([_i32, _i32, _i32, _i32, ctypes.POINTER(_sz)], _i32),
     "linattn_state_scan": ([_i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "linattn_device_status": ([_vp, _vp], _i32),
@@ -68,7 +69,7 @@ _SIGS = {
     "linattn_timing_collect": ([_i32, ctypes.POINTER(_i32), ctypes.POINTER(ctypes.c_float)], _i32),
     "linattn_kernel_name": ([_i32], ctypes.c_char_p),
 }
-KERNEL_KINDS = 8
+KERNEL_KINDS = 11
 
 
 def lib():
@@ -118,6 +119,10 @@ def linattn_fwd(shape, q, k, v, o, init_state, final_state, chunk_states, ws, ws
 def linattn_bwd(shape, q, k, v, dO, init_state, dq, dk, dv, d_init, ws, ws_bytes, stream) -> int:
     return lib().linattn_bwd(ctypes.byref(shape), q, k, v, dO, init_state, dq, dk, dv, d_init,
                              ws, ws_bytes, stream)
+
+
+def linattn_decode(shape, q, k, v, o, state, stream) -> int:
+    return lib().linattn_decode(ctypes.byref(shape), q, k, v, o, state, stream)
 
 
 def linattn_chunk_states(shape, seg_len, k, v, out, ws, ws_bytes, stream) -> int:
@@ -247,6 +252,19 @@ def bwd(q, k, v, dO, decay=None, init_state=None, want_dinit=False, outs=None, w
                      _ptr(dv), _ptr(dinit), _ptr(ws), ws.numel(), _stream(q.device, stream))
     _check(st, "linattn_bwd")
     return dq, dk, dv, dinit
+
+
+def decode(q, k, v, state, decay=None, out=None, stream=None):
+    """o for T new tokens [B, H, T, d]; `state` [B, H, d, d] fp32 is updated in place."""
+    import torch
+    _same_layout(q, k, v, out)
+    if state.dtype != torch.float32 or not state.is_contiguous():
+        raise ValueError("state must be contiguous fp32 [B, H, d, d]")
+    o = out if out is not None else torch.empty_strided(q.shape, q.stride(), dtype=q.dtype, device=q.device)
+    st = linattn_decode(shape_of(q, decay), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(state),
+                        _stream(q.device, stream))
+    _check(st, "linattn_decode")
+    return o
 
 
 def chunk_states(k, v, seg_len: int, decay=None, out=None, ws=None, stream=None):

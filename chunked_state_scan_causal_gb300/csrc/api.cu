@@ -145,31 +145,27 @@ constexpr size_t kHeader = 256;  // int32 status word at offset 0
 
 struct FwdLayout {
   int G = 0, L = 0;
-  size_t agg = 0, states = 0, scan = 0, total = kHeader;
+  size_t scratch = 0, total = kHeader;  // fused look-back scratch (flags, aggregates, prefixes)
 };
 static FwdLayout fwd_layout(const Problem &p) {
   FwdLayout w;
   if (!tc_supported(p) || p.T == 0) return w;
-  w.L = tc_group_len(p);
+  w.L = tc_fused_group_len(p);
   w.G = (p.T + w.L - 1) / w.L;
-  const size_t st = (size_t)w.G * p.B * p.H * p.d * p.d * sizeof(float);
-  w.agg = kHeader;
-  w.states = w.agg + align256(st);
-  w.scan = w.states + align256(st);
-  w.total = w.scan + scan_workspace_bytes(w.G, (int64_t)p.B * p.H * p.d * p.d);
+  w.scratch = kHeader;
+  w.total = w.scratch + tc_fused_scratch_bytes(p, w.L);
   return w;
 }
 struct BwdLayout {
-  FwdLayout f;            // forward states (aggregate of k v^T, exclusive scan)
-  size_t wagg = 0, rbar = 0, total = kHeader;
+  FwdLayout f;            // look-back scratch, reused by the dq and dv passes in turn
+  size_t rbar = 0, total = kHeader;
 };
 static BwdLayout bwd_layout(const Problem &p) {
   BwdLayout w;
   w.f = fwd_layout(p);
   if (w.f.G == 0) return w;
   const size_t st = (size_t)w.f.G * p.B * p.H * p.d * p.d * sizeof(float);
-  w.wagg = w.f.total;
-  w.rbar = w.wagg + align256(st);
+  w.rbar = w.f.total;
   w.total = w.rbar + align256(st);
   return w;
 }
@@ -250,15 +246,9 @@ int32_t linattn_fwd(const linattn_shape *shape, const void *q, const void *k, co
   }
   if (chunk_states || !tc_supported(p))
     return cuda_status(simt_fwd(p, q, k, v, o, init_state, final_state, chunk_states, s));
-  // tensor-core pipeline: group aggregates -> exclusive scan -> per-group forward
-  float *agg = reinterpret_cast<float *>(ws + w.agg);
-  float *states = reinterpret_cast<float *>(ws + w.states);
-  cudaError_t e = tc_segment_states(p, w.L, k, v, false, agg, status, s);
-  if (e == cudaSuccess)
-    e = state_scan(w.G, (int)BH, p.d * p.d, nullptr, p.decay, p.H, w.L, false, agg, init_state,
-                   states, nullptr, ws + w.scan, status, s);
-  if (e == cudaSuccess) e = tc_main(p, w.L, false, q, k, v, o, states, false, final_state, status, s);
-  return cuda_status(e);
+  // tensor-core path: one fused launch (group aggregates, look-back, chunked forward)
+  return cuda_status(tc_fused(p, w.L, false, q, k, v, o, init_state, false, final_state, nullptr, nullptr,
+                              ws + w.scratch, status, s));
 }
 
 int32_t linattn_bwd(const linattn_shape *shape, const void *q, const void *k, const void *v,
@@ -284,29 +274,32 @@ int32_t linattn_bwd(const linattn_shape *shape, const void *q, const void *k, co
   }
   if (!tc_supported(p))
     return cuda_status(simt_bwd(p, q, k, v, dO, init_state, dq, dk, dv, d_init_state, s));
-  const int L = w.f.L, G = w.f.G;
-  float *agg = reinterpret_cast<float *>(ws + w.f.agg);
-  float *states = reinterpret_cast<float *>(ws + w.f.states);
-  float *wagg = reinterpret_cast<float *>(ws + w.wagg);
+  const int L = w.f.L;
+  char *scratch = ws + w.f.scratch;
   float *rbar = reinterpret_cast<float *>(ws + w.rbar);
-  // forward group states (recomputed from k, v and init)
-  cudaError_t e = tc_segment_states(p, L, k, v, false, agg, status, s);
+  // dq: the forward-time kernel with (q, k, v) := (dO, v, k); its states are the
+  // transposed forward states, recomputed by its own aggregates and look-back
+  cudaError_t e = tc_fused(p, L, false, dO, v, k, dq, init_state, true, nullptr, nullptr, nullptr, scratch,
+                           status, s);
+  // dv: the reverse-time kernel with (q, k, v) := (k, q, dO); its states are
+  // Rbar_g = sum_{u > group end} lambda^{u-end} q_u dO_u^T, kept for the dk pass;
+  // the prefix one step before token 0 is d_init = sum_t lambda^{t+1} q_t dO_t^T
   if (e == cudaSuccess)
-    e = state_scan(G, (int)BH, p.d * p.d, nullptr, p.decay, p.H, L, false, agg, init_state, states,
-                   nullptr, ws + w.f.scan, status, s);
-  // dq: the forward kernel with (q, k, v) := (dO, v, k) and the transposed states
-  if (e == cudaSuccess) e = tc_main(p, L, false, dO, v, k, dq, states, true, nullptr, status, s);
-  // reverse group states Rbar = sum_{u > group end} lambda^{u-end} q_u dO_u^T, scanned from the
-  // end; the value one step before the start is d_init = sum_t lambda^{t+1} q_t dO_t^T
-  if (e == cudaSuccess) e = tc_segment_states(p, L, q, dO, true, wagg, status, s);
-  if (e == cudaSuccess)
-    e = state_scan(G, (int)BH, p.d * p.d, nullptr, p.decay, p.H, L, true, wagg, nullptr, rbar,
-                   d_init_state, ws + w.f.scan, status, s);
-  // dv: reverse-time kernel with (q, k, v) := (k, q, dO), state Rbar
-  if (e == cudaSuccess) e = tc_main(p, L, true, k, q, dO, dv, rbar, false, nullptr, status, s);
-  // dk: reverse-time kernel with (q, k, v) := (v, dO, q), state Rbar^T
+    e = tc_fused(p, L, true, k, q, dO, dv, nullptr, false, nullptr, d_init_state, rbar, scratch, status, s);
+  // dk: the reverse-time kernel with (q, k, v) := (v, dO, q) and the states Rbar^T
   if (e == cudaSuccess) e = tc_main(p, L, true, v, dO, q, dk, rbar, true, nullptr, status, s);
   return cuda_status(e);
+}
+
+int32_t linattn_decode(const linattn_shape *shape, const void *q, const void *k, const void *v, void *o,
+                       float *state, void *stream) {
+  Problem p;
+  int st = validate(shape, &p);
+  if (st) return st;
+  if (p.T == 0) return LINATTN_OK;
+  if ((st = check_ptrs({q, k, v, o, state}, {}))) return st;
+  if ((st = device_ok())) return st;
+  return cuda_status(decode(p, q, k, v, o, state, static_cast<cudaStream_t>(stream)));
 }
 
 int32_t linattn_chunk_states(const linattn_shape *shape, int32_t seg_len, const void *k, const void *v,
@@ -396,7 +389,7 @@ int32_t linattn_timing_collect(int32_t max_kinds, int32_t *launches, float *tota
 const char *linattn_kernel_name(int32_t kind) {
   static const char *names[K_KINDS] = {"simt_fwd", "simt_bwd", "simt_segment_states", "state_scan",
                                        "tc_segment_aggregate", "tc_chunked_fwd", "tc_chunked_rev",
-                                       "diag_mma"};
+                                       "diag_mma", "tc_fused_fwd", "tc_fused_rev", "decode"};
   return (kind >= 0 && kind < K_KINDS) ? names[kind] : "?";
 }
 

@@ -72,8 +72,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 // the CTA-wide abort flag is raised or after kWaitLimitNs; then records
 // LINATTN_ERR_DEVICE_TIMEOUT (-6) in the status word, raises the abort flag and
 // returns false.  Callers then unwind their role without further waits.
+// `detail` (optional) receives, for the first wait that gives up, which one:
+// (warp << 24) | (parity << 23) | shared-memory address of the barrier.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                          int *status) {
+                                          int *status, int *detail = nullptr) {
 #pragma unroll 1
   for (int i = 0; i < 256; ++i)
     if (mbar_try_wait(bar, parity)) return true;
@@ -84,10 +86,43 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
     if (*abort_flag) return false;
     if (globaltimer_ns() - t0 > kWaitLimitNs) {
       report_error(status, -6);
+      if (detail)
+        atomicCAS(detail, 0, (int)(((threadIdx.x / 32) << 24) | ((parity & 1) << 23) | (smem_u32(bar) & 0x7FFFFF)));
       *abort_flag = 1;
       return false;
     }
   }
+}
+
+// ----------------------------------------------------------------------------- global flags
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(unsigned *p, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Bounded spin until *flag != 0; returns the value, or 0 after kWaitLimitNs
+// (then LINATTN_ERR_DEVICE_TIMEOUT is recorded and the abort flag raised) or
+// once the abort flag is up.
+// `detail` (optional) receives (1 << 30) | flag index for the first flag wait that gives up.
+__device__ __forceinline__ unsigned wait_flag(const unsigned *flag, volatile int *abort_flag, int *status,
+                                              int *detail = nullptr, unsigned index = 0) {
+  unsigned v = ld_acquire_gpu(flag);
+  if (v) return v;
+  const uint64_t t0 = globaltimer_ns();
+#pragma unroll 1
+  while ((v = ld_acquire_gpu(flag)) == 0) {
+    if (*abort_flag) return 0;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      report_error(status, -6);
+      if (detail) atomicCAS(detail, 0, (int)((1u << 30) | (index & 0x3FFFFFFFu)));
+      *abort_flag = 1;
+      return 0;
+    }
+  }
+  return v;
 }
 
 // ----------------------------------------------------------------------------- named barriers
@@ -125,6 +160,14 @@ __device__ __forceinline__ void tma_load_4d(const CUtensorMap *map, uint64_t *ba
       " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar)),
       "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void tma_store_4d_hint(const CUtensorMap *map, const void *src, int c0, int c1,
+                                                  int c2, int c3, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3, %4, %5}], [%1], %6;" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "l"(policy)
       : "memory");
 }
 __device__ __forceinline__ void tma_store_4d(const CUtensorMap *map, const void *src, int c0, int c1,

@@ -16,6 +16,12 @@
 //    ticket in segment-tile-major order, so every predecessor of a waiting
 //    tile is already running; each tile publishes its aggregate at once and
 //    its inclusive prefix after the look-back; waits are bounded.
+// Up to kColumnMaxG segments a second, column-parallel form is used instead:
+// every thread owns 4 consecutive state elements and walks the segments in
+// order with several loads in flight, so every warp access is one contiguous
+// 512-byte piece (the segment-per-lane tiles above touch 32 scattered sectors
+// per warp access, which DRAM serves far less efficiently).  The look-back
+// form remains for long scans, where it supplies the parallelism.
 #include <mutex>
 
 #include "../../include/linattn.h"
@@ -205,6 +211,39 @@ __global__ void __launch_bounds__(kWarps * 32) scan_kernel(ScanArgs A) {
   }
 }
 
+constexpr int kColumnMaxG = 256;
+constexpr int kColumnDepth = 4;  // loads in flight per thread
+
+__global__ void __launch_bounds__(256) scan_columns_kernel(ScanArgs A) {
+  const int64_t E = (int64_t)A.BH * A.DD, n4 = E / 4;
+  for (int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c < n4; c += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t e0 = c * 4;
+    const int bh = (int)(e0 / A.DD);
+    float a = 1.f;
+    if (A.seg_decay) a = A.seg_decay[bh];
+    else if (A.decay_h) a = (float)pow((double)A.decay_h[bh % A.H], (double)A.seg_len);
+    float4 acc = A.init ? __ldg(reinterpret_cast<const float4 *>(A.init + e0)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = 0; i < A.G; i += kColumnDepth) {
+      float4 u[kColumnDepth];
+#pragma unroll
+      for (int j = 0; j < kColumnDepth; ++j) {
+        const int p = i + j, g = A.reverse ? A.G - 1 - p : p;
+        if (p < A.G) u[j] = __ldg(reinterpret_cast<const float4 *>(A.local + (int64_t)g * E + e0));
+      }
+#pragma unroll
+      for (int j = 0; j < kColumnDepth; ++j) {
+        const int p = i + j, g = A.reverse ? A.G - 1 - p : p;
+        if (p < A.G) {
+          *reinterpret_cast<float4 *>(A.out + (int64_t)g * E + e0) = acc;
+          acc = make_float4(fmaf(a, acc.x, u[j].x), fmaf(a, acc.y, u[j].y), fmaf(a, acc.z, u[j].z),
+                            fmaf(a, acc.w, u[j].w));
+        }
+      }
+    }
+    if (A.total) *reinterpret_cast<float4 *>(A.total + e0) = acc;
+  }
+}
+
 }  // namespace
 
 size_t scan_workspace_bytes(int G, int64_t E) {
@@ -224,6 +263,15 @@ cudaError_t state_scan(int G, int BH, int DD, const float *seg_decay, const floa
   A.reverse = reverse ? 1 : 0;
   A.seg_decay = seg_decay; A.decay_h = decay_h; A.local = local; A.init = init;
   A.out = out; A.total = total; A.status = status;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (G <= kColumnMaxG) {
+    const int64_t n4 = E / 4, want = (n4 + 255) / 256, cap = (int64_t)sms * 8;
+    TimedLaunch t(K_SCAN, s);
+    scan_columns_kernel<<<(int)(want < cap ? want : cap), 256, 0, s>>>(A);
+    return cudaGetLastError();
+  }
   const int64_t nt = (int64_t)A.ntg * A.ncg;
   char *w = static_cast<char *>(ws);
   A.counter = reinterpret_cast<unsigned *>(w);
@@ -235,9 +283,6 @@ cudaError_t state_scan(int G, int BH, int DD, const float *seg_decay, const floa
     cudaError_t e = cudaMemsetAsync(w, 0, head, s);
     if (e != cudaSuccess) return e;
   }
-  int dev = 0, sms = 148;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int64_t want = (nt + kWarps - 1) / kWarps;
   const int grid = (int)(want < (int64_t)sms * 8 ? want : (int64_t)sms * 8);
   TimedLaunch t(K_SCAN, s);

@@ -116,6 +116,17 @@ int32_t linattn_bwd(const linattn_shape *shape, const void *q, const void *k, co
                     const void *dO, const float *init_state, void *dq, void *dk, void *dv,
                     float *d_init_state, void *workspace, size_t workspace_bytes, void *stream);
 
+/* Recurrent decode of T new tokens per sequence (constant-memory inference:
+ * LASP-2 page, abstract): for t = 0..T-1
+ *   S <- lambda S + k_t v_t^T,   o_t = S^T q_t,
+ * with `state` ([B,H,dk,dv] fp32 device memory) read at the start and the
+ * updated state written back in place.  q, k, v, o follow the shape (T >= 0;
+ * meant for a few tokens per call -- the tokens of one call are processed in
+ * order by every CTA, so long T belongs to linattn_fwd with init/final
+ * states).  No workspace.  Returns a status. */
+int32_t linattn_decode(const linattn_shape *shape, const void *q, const void *k, const void *v, void *o,
+                       float *state, void *stream);
+
 /* Segment-local states (what each sequence-parallel rank computes from its
  * own contiguous segment before the exchange; LASP-2 page, abstract):
  *   local_states[g,b,h] = sum_{s in segment g} lambda^{end_g - s} k_s v_s^T
@@ -186,7 +197,7 @@ int32_t linattn_device_status(const void *workspace, void *stream);
  * for every kernel kind k < max_kinds its launch count and summed device time
  * (ms), clears the record and returns the number of kinds
  * (LINATTN_KERNEL_KINDS), or a negative status. */
-#define LINATTN_KERNEL_KINDS 8
+#define LINATTN_KERNEL_KINDS 11
 int32_t linattn_timing_enable(int32_t on);
 int32_t linattn_timing_collect(int32_t max_kinds, int32_t *launches, float *total_ms);
 /* Name of kernel kind k (static string; "?" when out of range). */

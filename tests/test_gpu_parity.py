@@ -68,9 +68,10 @@ def test_diag_tensor_core_product(mode):
 
 
 # ------------------------------------------------------------------ state scan
-@pytest.mark.parametrize("G", [1, 5, 32, 33, 70])
+@pytest.mark.parametrize("G", [1, 5, 32, 33, 70, 256, 257, 300, 1000])
 @pytest.mark.parametrize("with_decay,with_init", [(False, False), (True, True), (True, False)])
 def test_state_scan(G, with_decay, with_init):
+    """Column-parallel form (G <= 256) and shuffle + decoupled look-back form (G > 256)."""
     r = np.random.default_rng(G)
     BH, dk, dv = 3, 16, 24
     U = r.standard_normal((G, BH, dk, dv)).astype(np.float32)
@@ -215,3 +216,21 @@ def test_device_status_clean_after_calls():
     ws = la.workspace(dev["q"], la.OP_BWD)
     la.bwd(dev["q"], dev["k"], dev["v"], dev["dO"], ws=ws)
     assert la.device_status(ws) == la.OK
+
+
+# ------------------------------------------------------------------ recurrent decode
+@pytest.mark.parametrize("dtype,d", [(torch.bfloat16, 128), (torch.float32, 64), (torch.float32, 128)])
+@pytest.mark.parametrize("T", [1, 3, 16])
+@pytest.mark.parametrize("dk", [None, "cfg"])
+def test_decode_steps(dtype, d, T, dk):
+    """Decode of T tokens from a given state == the definition continued from that state."""
+    B, H = 2, 3
+    c, dev = case(23 + T, B, H, T, d, dtype)
+    lam = decays(H, dk)
+    init = (np.random.default_rng(T).standard_normal((B, H, d, d)) * 0.3).astype(np.float32)
+    state = torch.from_numpy(init).cuda()
+    o = la.decode(dev["q"], dev["k"], dev["v"], state, decay=None if lam is None else torch.from_numpy(lam).cuda())
+    torch.cuda.synchronize()
+    ro, _, rfin = oracle.fwd_recurrent(c["q"], c["k"], c["v"], lam=lam, init=init.astype(np.float64))
+    assert rel(o, ro) < TOL[dtype]
+    assert rel(state, rfin) < 1e-5

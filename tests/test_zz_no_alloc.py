@@ -5,8 +5,9 @@ Callers that cannot allocate device memory (their host application owns all
 of it, or their path must not allocate) use the allocation-free entry point,
 whose scratch is a fixed array inside the library.  Two calls in a row with
 different inputs check that the shared scratch is reset between calls; the
-case spans three 32-segment tiles so the decoupled look-back through that
-scratch is exercised.  This file is collected last on purpose.
+case has 300 segments (ten 32-segment tiles), long enough for the scan's
+decoupled look-back, which is what goes through that scratch.  This file is
+collected last on purpose.
 """
 import numpy as np
 import pytest
@@ -29,7 +30,7 @@ def _rel(a, b):
 
 
 def test_noalloc_scan_matches_workspace_scan_on_two_calls():
-    G, BH, dk, dv = 70, 3, 16, 24
+    G, BH, dk, dv = 300, 3, 16, 24
     stream = torch.cuda.current_stream().cuda_stream
     for call in range(2):
         g = torch.Generator().manual_seed(100 + call)

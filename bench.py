@@ -220,10 +220,12 @@ def run_ours(args):
     grads = [torch.empty_like(x["q"]) for _ in range(3)]
     ws_f = la.workspace(x["q"], la.OP_FWD, decay)
     ws_b = la.workspace(x["q"], la.OP_BWD, decay)
+    ck = la.checkpoint(x["q"], decay)
 
     def step():
-        la.fwd(x["q"], x["k"], x["v"], decay=decay, out=o, ws=ws_f)
-        la.bwd(x["q"], x["k"], x["v"], x["dO"], decay=decay, outs=grads, ws=ws_b)
+        # a training step of the layer: forward keeping its group states, then backward
+        la.fwd(x["q"], x["k"], x["v"], decay=decay, out=o, ws=ws_f, ckpt=ck)
+        la.bwd(x["q"], x["k"], x["v"], x["dO"], decay=decay, outs=grads, ws=ws_b, ckpt=ck)
 
     def barrier():
         if ws_n > 1:
@@ -260,7 +262,7 @@ def run_ours(args):
 
     # ---- dominant kernel roofline (chunked kernel, forward and reverse-time launches)
     launches = sum(n for n, _ in kernels.values())
-    main = [kernels.get(k, (0, 0.0)) for k in ("tc_fused_fwd", "tc_fused_rev", "tc_chunked_fwd", "tc_chunked_rev")]
+    main = [kernels.get(k, (0, 0.0)) for k in ("tc_chunked_fwd", "tc_chunked_rev")]
     n_main = sum(n for n, _ in main)
     ms_main = sum(t for _, t in main)
     per_launch_bytes = MAIN_BYTES_PER_TOKEN_HEAD * B * H * T
@@ -268,7 +270,7 @@ def run_ours(args):
     achieved = per_launch_bytes / (avg_ms * 1e-3) / 1e9 if n_main else None
     traffic_tok = _profile_traffic()
     roofline = {
-        "kernel": "tc_main_kernel (fused and plain, forward- and reverse-time launches)",
+        "kernel": "tc_main_kernel (chunked; forward- and reverse-time launches)",
         "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
         "frac": (achieved / hbm) if achieved else None,
         "traffic": None if traffic_tok is None else traffic_tok * B * H * T,
@@ -291,7 +293,7 @@ def run_ours(args):
             outs = [torch.empty_like(x["q"]) for _ in range(4)]
             hout = [torch.empty(x["q"].shape, dtype=x["q"].dtype, pin_memory=True) for _ in range(4)]
             ev = {n: torch.cuda.Event() for n in ("in", "comp", "out")}
-            slots.append(dict(x=xin, o=outs, h=hout, ev=ev, used=False,
+            slots.append(dict(x=xin, o=outs, h=hout, ev=ev, used=False, ck=la.checkpoint(x["q"], decay),
                               wsf=la.workspace(x["q"], la.OP_FWD, decay), wsb=la.workspace(x["q"], la.OP_BWD, decay)))
         s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
         h2d = sum(t.numel() * t.element_size() for t in host.values())
@@ -309,8 +311,8 @@ def run_ours(args):
             if sl["used"]:
                 stream.wait_event(sl["ev"]["out"])         # previous results of this slot copied out
             xs, (o_, dq_, dk_, dv_) = sl["x"], sl["o"]
-            la.fwd(xs["q"], xs["k"], xs["v"], decay=decay, out=o_, ws=sl["wsf"])
-            la.bwd(xs["q"], xs["k"], xs["v"], xs["dO"], decay=decay, outs=[dq_, dk_, dv_], ws=sl["wsb"])
+            la.fwd(xs["q"], xs["k"], xs["v"], decay=decay, out=o_, ws=sl["wsf"], ckpt=sl["ck"])
+            la.bwd(xs["q"], xs["k"], xs["v"], xs["dO"], decay=decay, outs=[dq_, dk_, dv_], ws=sl["wsb"], ckpt=sl["ck"])
             sl["ev"]["comp"].record(stream)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(sl["ev"]["comp"])
@@ -359,7 +361,7 @@ def run_ours(args):
             "config": {"workload": cfg["name"], "B": B, "H": H, "T": T, "d": d, "chunk": 64,
                        "decay": "per-head" if lam is not None else "none",
                        "l2": "inputs 512 MiB per tensor > L2 (no flush)",
-                       "step": "linattn_fwd + linattn_bwd", "parallelism": f"replicas x{ws_n}"},
+                       "step": "linattn_fwd_ckpt + linattn_bwd_ckpt", "parallelism": f"replicas x{ws_n}"},
             "tflops": flops / (ms * 1e-3) / 1e12,
             "algorithmic_gbs": bytes_ / (ms * 1e-3) / 1e9,
             "path_roofline_frac": max(flops / (tf * 1e12), bytes_ / (hbm * 1e9)) / (ms * 1e-3),

@@ -28,7 +28,7 @@ ERR_DEVICE = -7
 ERR_SCRATCH_LIMIT = -8
 NOALLOC_MAX_TILES = 65536
 BF16, F32 = 0, 1
-OP_FWD, OP_BWD, OP_CHUNK_STATES = 1, 2, 3
+OP_FWD, OP_BWD, OP_CHUNK_STATES, OP_CHECKPOINT = 1, 2, 3, 4
 ABI_VERSION = 1
 
 
@@ -58,6 +58,9 @@ _SIGS = {
     "linattn_workspace_size": ([ctypes.POINTER(Shape), _i32, _i32, ctypes.POINTER(_sz)], _i32),
     "linattn_fwd": ([ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "linattn_bwd": ([ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
+    "linattn_fwd_ckpt": ([ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _sz, _vp], _i32),
+    "linattn_bwd_ckpt": ([ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _vp, _vp, _vp, _vp, _sz,
+                          _vp], _i32),
     "linattn_chunk_states": ([ctypes.POINTER(Shape), _i32, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "linattn_decode": ([ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp], _i32),
     "linattn_state_scan_workspace_size": ([_i32, _i32, _i32, _i32, ctypes.POINTER(_sz)], _i32),
@@ -69,7 +72,7 @@ _SIGS = {
     "linattn_timing_collect": ([_i32, ctypes.POINTER(_i32), ctypes.POINTER(ctypes.c_float)], _i32),
     "linattn_kernel_name": ([_i32], ctypes.c_char_p),
 }
-KERNEL_KINDS = 11
+KERNEL_KINDS = 9
 
 
 def lib():
@@ -123,6 +126,17 @@ def linattn_bwd(shape, q, k, v, dO, init_state, dq, dk, dv, d_init, ws, ws_bytes
 
 def linattn_decode(shape, q, k, v, o, state, stream) -> int:
     return lib().linattn_decode(ctypes.byref(shape), q, k, v, o, state, stream)
+
+
+def linattn_fwd_ckpt(shape, q, k, v, o, init_state, final_state, ckpt, ckpt_bytes, ws, ws_bytes, stream) -> int:
+    return lib().linattn_fwd_ckpt(ctypes.byref(shape), q, k, v, o, init_state, final_state, ckpt, ckpt_bytes,
+                                  ws, ws_bytes, stream)
+
+
+def linattn_bwd_ckpt(shape, q, k, v, dO, init_state, ckpt, ckpt_bytes, dq, dk, dv, d_init, ws, ws_bytes,
+                     stream) -> int:
+    return lib().linattn_bwd_ckpt(ctypes.byref(shape), q, k, v, dO, init_state, ckpt, ckpt_bytes, dq, dk, dv, d_init,
+                                  ws, ws_bytes, stream)
 
 
 def linattn_chunk_states(shape, seg_len, k, v, out, ws, ws_bytes, stream) -> int:
@@ -217,9 +231,19 @@ def workspace(q, op: int, decay=None, seg_len: int = 0):
     return torch.empty(max(n, 256), dtype=torch.uint8, device=q.device)
 
 
+def checkpoint(q, decay=None):
+    """Buffer for the forward group states kept by fwd(..., ckpt=...) for bwd(..., ckpt=...)."""
+    import torch
+    st, n = linattn_workspace_size(shape_of(q, decay), OP_CHECKPOINT)
+    _check(st, "linattn_workspace_size")
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=q.device)
+
+
 def fwd(q, k, v, decay=None, init_state=None, want_final=False, want_chunk_states=False,
-        out=None, ws=None, stream=None):
-    """o (, final_state) (, chunk_states) for q, k, v [B, H, T, d] (bf16 or fp32)."""
+        out=None, ws=None, stream=None, ckpt=None):
+    """o (, final_state) (, chunk_states) for q, k, v [B, H, T, d] (bf16 or fp32).
+
+    With ``ckpt`` (from ``checkpoint``) the forward group states are also stored for ``bwd(..., ckpt=)``."""
     import torch
     _same_layout(q, k, v, out)
     B, H, T, d = q.shape
@@ -230,14 +254,21 @@ def fwd(q, k, v, decay=None, init_state=None, want_final=False, want_chunk_state
     shape = shape_of(q, decay)
     if ws is None:
         ws = workspace(q, OP_FWD, decay)
+    if ckpt is not None:
+        if cs is not None:
+            raise ValueError("per-chunk states are not offered together with a checkpoint")
+        st = linattn_fwd_ckpt(shape, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(init_state), _ptr(fin),
+                              _ptr(ckpt), ckpt.numel(), _ptr(ws), ws.numel(), _stream(q.device, stream))
+        _check(st, "linattn_fwd_ckpt")
+        return o, fin, cs
     st = linattn_fwd(shape, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(init_state), _ptr(fin), _ptr(cs),
                      _ptr(ws), ws.numel(), _stream(q.device, stream))
     _check(st, "linattn_fwd")
     return o, fin, cs
 
 
-def bwd(q, k, v, dO, decay=None, init_state=None, want_dinit=False, outs=None, ws=None, stream=None):
-    """(dq, dk, dv, d_init or None) for the upstream gradient dO."""
+def bwd(q, k, v, dO, decay=None, init_state=None, want_dinit=False, outs=None, ws=None, stream=None, ckpt=None):
+    """(dq, dk, dv, d_init or None) for the upstream gradient dO (forward states from ``ckpt`` if given)."""
     import torch
     _same_layout(q, k, v, dO)
     B, H, T, d = q.shape
@@ -248,6 +279,12 @@ def bwd(q, k, v, dO, decay=None, init_state=None, want_dinit=False, outs=None, w
     shape = shape_of(q, decay)
     if ws is None:
         ws = workspace(q, OP_BWD, decay)
+    if ckpt is not None:
+        st = linattn_bwd_ckpt(shape, _ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(init_state), _ptr(ckpt), ckpt.numel(),
+                              _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dinit), _ptr(ws), ws.numel(),
+                              _stream(q.device, stream))
+        _check(st, "linattn_bwd_ckpt")
+        return dq, dk, dv, dinit
     st = linattn_bwd(shape, _ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(init_state), _ptr(dq), _ptr(dk),
                      _ptr(dv), _ptr(dinit), _ptr(ws), ws.numel(), _stream(q.device, stream))
     _check(st, "linattn_bwd")

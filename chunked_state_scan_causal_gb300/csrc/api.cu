@@ -145,29 +145,39 @@ constexpr size_t kHeader = 256;  // int32 status word at offset 0
 
 struct FwdLayout {
   int G = 0, L = 0;
-  size_t scratch = 0, total = kHeader;  // fused look-back scratch (flags, aggregates, prefixes)
+  size_t agg = 0, states = 0, scan = 0, total = kHeader;
 };
 static FwdLayout fwd_layout(const Problem &p) {
   FwdLayout w;
   if (!tc_supported(p) || p.T == 0) return w;
-  w.L = tc_fused_group_len(p);
+  w.L = tc_group_len(p);
   w.G = (p.T + w.L - 1) / w.L;
-  w.scratch = kHeader;
-  w.total = w.scratch + tc_fused_scratch_bytes(p, w.L);
+  const size_t st = (size_t)w.G * p.B * p.H * p.d * p.d * sizeof(float);
+  w.agg = kHeader;
+  w.states = w.agg + align256(st);
+  w.scan = w.states + align256(st);
+  w.total = w.scan + scan_workspace_bytes(w.G, (int64_t)p.B * p.H * p.d * p.d);
   return w;
 }
 struct BwdLayout {
-  FwdLayout f;            // look-back scratch, reused by the dq and dv passes in turn
-  size_t rbar = 0, total = kHeader;
+  FwdLayout f;            // forward group aggregates / states (recomputed without a checkpoint)
+  size_t wagg = 0, rbar = 0, total = kHeader;
 };
 static BwdLayout bwd_layout(const Problem &p) {
   BwdLayout w;
   w.f = fwd_layout(p);
   if (w.f.G == 0) return w;
   const size_t st = (size_t)w.f.G * p.B * p.H * p.d * p.d * sizeof(float);
-  w.rbar = w.f.total;
+  w.wagg = w.f.total;
+  w.rbar = w.wagg + align256(st);
   w.total = w.rbar + align256(st);
   return w;
+}
+
+// Checkpoint of the forward group states: [G][BH][d][d] fp32 (tensor-core path only).
+static size_t ckpt_bytes(const Problem &p) {
+  const FwdLayout w = fwd_layout(p);
+  return w.G == 0 ? 0 : (size_t)w.G * p.B * p.H * p.d * p.d * sizeof(float);
 }
 
 static int check_ws(void *ws, size_t bytes, size_t need) {
@@ -212,15 +222,17 @@ int32_t linattn_workspace_size(const linattn_shape *shape, int32_t op, int32_t s
   } else if (op == LINATTN_OP_CHUNK_STATES) {
     if (seg_len < 1) return LINATTN_ERR_INVALID;
     *bytes = kHeader;
+  } else if (op == LINATTN_OP_CHECKPOINT) {
+    *bytes = ckpt_bytes(p);
   } else {
     return LINATTN_ERR_INVALID;
   }
   return LINATTN_OK;
 }
 
-int32_t linattn_fwd(const linattn_shape *shape, const void *q, const void *k, const void *v, void *o,
-                    const float *init_state, float *final_state, float *chunk_states, void *workspace,
-                    size_t workspace_bytes, void *stream) {
+static int32_t fwd_impl(const linattn_shape *shape, const void *q, const void *k, const void *v, void *o,
+                        const float *init_state, float *final_state, float *chunk_states, float *ckpt,
+                        size_t ckpt_size, bool want_ckpt, void *workspace, size_t workspace_bytes, void *stream) {
   Problem p;
   int st = validate(shape, &p);
   if (st) return st;
@@ -228,6 +240,9 @@ int32_t linattn_fwd(const linattn_shape *shape, const void *q, const void *k, co
   if ((st = check_ptrs({}, {init_state, final_state, chunk_states}))) return st;
   const FwdLayout w = fwd_layout(p);
   if ((st = check_ws(workspace, workspace_bytes, w.total))) return st;
+  const size_t need_ckpt = want_ckpt ? ckpt_bytes(p) : 0;
+  if (need_ckpt && (!ckpt || (reinterpret_cast<uintptr_t>(ckpt) & 255u) || ckpt_size < need_ckpt))
+    return LINATTN_ERR_INVALID;
   if ((st = device_ok())) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char *ws = static_cast<char *>(workspace);
@@ -246,14 +261,36 @@ int32_t linattn_fwd(const linattn_shape *shape, const void *q, const void *k, co
   }
   if (chunk_states || !tc_supported(p))
     return cuda_status(simt_fwd(p, q, k, v, o, init_state, final_state, chunk_states, s));
-  // tensor-core path: one fused launch (group aggregates, look-back, chunked forward)
-  return cuda_status(tc_fused(p, w.L, false, q, k, v, o, init_state, false, final_state, nullptr, nullptr,
-                              ws + w.scratch, status, s));
+  // tensor-core path: chunk-group aggregates -> exclusive scan of the group states
+  // -> chunked forward of every group from its entering state
+  float *agg = reinterpret_cast<float *>(ws + w.agg);
+  float *states = need_ckpt ? ckpt : reinterpret_cast<float *>(ws + w.states);
+  cudaError_t e = tc_segment_states(p, w.L, k, v, false, agg, status, s);
+  if (e == cudaSuccess)
+    e = state_scan(w.G, (int)BH, p.d * p.d, nullptr, p.decay, p.H, w.L, false, agg, init_state, states, nullptr,
+                   ws + w.scan, status, s);
+  if (e == cudaSuccess) e = tc_main(p, w.L, false, q, k, v, o, states, false, final_state, status, s);
+  return cuda_status(e);
 }
 
-int32_t linattn_bwd(const linattn_shape *shape, const void *q, const void *k, const void *v,
-                    const void *dO, const float *init_state, void *dq, void *dk, void *dv,
-                    float *d_init_state, void *workspace, size_t workspace_bytes, void *stream) {
+int32_t linattn_fwd(const linattn_shape *shape, const void *q, const void *k, const void *v, void *o,
+                    const float *init_state, float *final_state, float *chunk_states, void *workspace,
+                    size_t workspace_bytes, void *stream) {
+  return fwd_impl(shape, q, k, v, o, init_state, final_state, chunk_states, nullptr, 0, false, workspace,
+                  workspace_bytes, stream);
+}
+
+int32_t linattn_fwd_ckpt(const linattn_shape *shape, const void *q, const void *k, const void *v, void *o,
+                         const float *init_state, float *final_state, void *checkpoint,
+                         size_t checkpoint_bytes, void *workspace, size_t workspace_bytes, void *stream) {
+  return fwd_impl(shape, q, k, v, o, init_state, final_state, nullptr, static_cast<float *>(checkpoint),
+                  checkpoint_bytes, true, workspace, workspace_bytes, stream);
+}
+
+static int32_t bwd_impl(const linattn_shape *shape, const void *q, const void *k, const void *v,
+                        const void *dO, const float *init_state, const float *ckpt, size_t ckpt_size,
+                        bool use_ckpt, void *dq, void *dk, void *dv, float *d_init_state, void *workspace,
+                        size_t workspace_bytes, void *stream) {
   Problem p;
   int st = validate(shape, &p);
   if (st) return st;
@@ -261,6 +298,9 @@ int32_t linattn_bwd(const linattn_shape *shape, const void *q, const void *k, co
   if ((st = check_ptrs({}, {init_state, d_init_state}))) return st;
   const BwdLayout w = bwd_layout(p);
   if ((st = check_ws(workspace, workspace_bytes, w.total))) return st;
+  const size_t need_ckpt = use_ckpt ? ckpt_bytes(p) : 0;
+  if (need_ckpt && (!ckpt || (reinterpret_cast<uintptr_t>(ckpt) & 255u) || ckpt_size < need_ckpt))
+    return LINATTN_ERR_INVALID;
   if ((st = device_ok())) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char *ws = static_cast<char *>(workspace);
@@ -274,21 +314,51 @@ int32_t linattn_bwd(const linattn_shape *shape, const void *q, const void *k, co
   }
   if (!tc_supported(p))
     return cuda_status(simt_bwd(p, q, k, v, dO, init_state, dq, dk, dv, d_init_state, s));
-  const int L = w.f.L;
-  char *scratch = ws + w.f.scratch;
+  const int L = w.f.L, G = w.f.G;
+  float *agg = reinterpret_cast<float *>(ws + w.f.agg);
+  float *wagg = reinterpret_cast<float *>(ws + w.wagg);
   float *rbar = reinterpret_cast<float *>(ws + w.rbar);
-  // dq: the forward-time kernel with (q, k, v) := (dO, v, k); its states are the
-  // transposed forward states, recomputed by its own aggregates and look-back
-  cudaError_t e = tc_fused(p, L, false, dO, v, k, dq, init_state, true, nullptr, nullptr, nullptr, scratch,
-                           status, s);
-  // dv: the reverse-time kernel with (q, k, v) := (k, q, dO); its states are
-  // Rbar_g = sum_{u > group end} lambda^{u-end} q_u dO_u^T, kept for the dk pass;
-  // the prefix one step before token 0 is d_init = sum_t lambda^{t+1} q_t dO_t^T
+  cudaError_t e = cudaSuccess;
+  // forward group states: from the checkpoint, or recomputed from k, v and init_state
+  const float *states = ckpt;
+  if (!need_ckpt) {
+    float *st = reinterpret_cast<float *>(ws + w.f.states);
+    e = tc_segment_states(p, L, k, v, false, agg, status, s);
+    if (e == cudaSuccess)
+      e = state_scan(G, (int)BH, p.d * p.d, nullptr, p.decay, p.H, L, false, agg, init_state, st, nullptr,
+                     ws + w.f.scan, status, s);
+    states = st;
+  }
+  // dq: the forward-time kernel with (q, k, v) := (dO, v, k), reading every
+  // group's state transposed
+  if (e == cudaSuccess) e = tc_main(p, L, false, dO, v, k, dq, states, true, nullptr, status, s);
+  // reverse group states Rbar_g = sum_{u > group end} lambda^{u-end} q_u dO_u^T: group
+  // aggregates of q dO^T, scanned from the end; the value one step before token 0 is
+  // d_init = sum_t lambda^{t+1} q_t dO_t^T
+  if (e == cudaSuccess) e = tc_segment_states(p, L, q, dO, true, wagg, status, s);
   if (e == cudaSuccess)
-    e = tc_fused(p, L, true, k, q, dO, dv, nullptr, false, nullptr, d_init_state, rbar, scratch, status, s);
+    e = state_scan(G, (int)BH, p.d * p.d, nullptr, p.decay, p.H, L, true, wagg, nullptr, rbar, d_init_state,
+                   ws + w.f.scan, status, s);
+  // dv: the reverse-time kernel with (q, k, v) := (k, q, dO) and the states Rbar
+  if (e == cudaSuccess) e = tc_main(p, L, true, k, q, dO, dv, rbar, false, nullptr, status, s);
   // dk: the reverse-time kernel with (q, k, v) := (v, dO, q) and the states Rbar^T
   if (e == cudaSuccess) e = tc_main(p, L, true, v, dO, q, dk, rbar, true, nullptr, status, s);
   return cuda_status(e);
+}
+
+int32_t linattn_bwd(const linattn_shape *shape, const void *q, const void *k, const void *v,
+                    const void *dO, const float *init_state, void *dq, void *dk, void *dv,
+                    float *d_init_state, void *workspace, size_t workspace_bytes, void *stream) {
+  return bwd_impl(shape, q, k, v, dO, init_state, nullptr, 0, false, dq, dk, dv, d_init_state, workspace,
+                  workspace_bytes, stream);
+}
+
+int32_t linattn_bwd_ckpt(const linattn_shape *shape, const void *q, const void *k, const void *v,
+                         const void *dO, const float *init_state, const void *checkpoint, size_t checkpoint_bytes,
+                         void *dq, void *dk, void *dv, float *d_init_state, void *workspace,
+                         size_t workspace_bytes, void *stream) {
+  return bwd_impl(shape, q, k, v, dO, init_state, static_cast<const float *>(checkpoint), checkpoint_bytes, true,
+                  dq, dk, dv, d_init_state, workspace, workspace_bytes, stream);
 }
 
 int32_t linattn_decode(const linattn_shape *shape, const void *q, const void *k, const void *v, void *o,
@@ -389,7 +459,7 @@ int32_t linattn_timing_collect(int32_t max_kinds, int32_t *launches, float *tota
 const char *linattn_kernel_name(int32_t kind) {
   static const char *names[K_KINDS] = {"simt_fwd", "simt_bwd", "simt_segment_states", "state_scan",
                                        "tc_segment_aggregate", "tc_chunked_fwd", "tc_chunked_rev",
-                                       "diag_mma", "tc_fused_fwd", "tc_fused_rev", "decode"};
+                                       "diag_mma", "decode"};
   return (kind >= 0 && kind < K_KINDS) ? names[kind] : "?";
 }
 

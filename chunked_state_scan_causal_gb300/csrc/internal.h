@@ -24,7 +24,7 @@ int device_ok();
 // ---------------------------------------------------------------- per-kernel timing (api.cu)
 enum KernelKind {
   K_SIMT_FWD = 0, K_SIMT_BWD, K_SIMT_SEGMENT, K_SCAN, K_TC_AGG, K_TC_MAIN_FWD, K_TC_MAIN_REV, K_DIAG,
-  K_TC_FUSED_FWD, K_TC_FUSED_REV, K_DECODE, K_KINDS
+  K_DECODE, K_KINDS
 };
 // Records timing events around one launch on `s` while timing is enabled.
 struct TimedLaunch {
@@ -69,19 +69,6 @@ cudaError_t tc_segment_states(const Problem &p, int seg_len, const void *X, cons
 cudaError_t tc_main(const Problem &p, int group_len, bool reverse, const void *q, const void *k,
                     const void *v, void *o, const float *group_init, bool init_transposed,
                     float *final_state, int *status, cudaStream_t s);
-
-// Fused variant: every work item also computes its group's aggregate (pass 1)
-// and obtains its entering state by decoupled look-back over the groups before
-// it in walk order (forward: g - 1, g - 2, ...; reverse: g + 1, ...), so no
-// separate aggregate or scan launch is needed.  init (optional) is the state
-// before the first group of the walk; final_state (forward), dinit (reverse:
-// the state one step before token 0) and states_out ([G][BH][d][d] exclusive
-// group states) are optional outputs.  scratch holds tc_fused_scratch_bytes.
-int tc_fused_group_len(const Problem &p);
-size_t tc_fused_scratch_bytes(const Problem &p, int group_len);
-cudaError_t tc_fused(const Problem &p, int group_len, bool reverse, const void *q, const void *k,
-                     const void *v, void *o, const float *init, bool init_transposed, float *final_state,
-                     float *dinit, float *states_out, void *scratch, int *status, cudaStream_t s);
 
 // ---------------------------------------------------------------- TMA descriptors (api.cu)
 // 4-D bf16 tiled tensor map, dims innermost first, strides in bytes for dims 1..3,

@@ -103,27 +103,6 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p) {
 __device__ __forceinline__ void st_release_gpu(unsigned *p, unsigned v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
-// Bounded spin until *flag != 0; returns the value, or 0 after kWaitLimitNs
-// (then LINATTN_ERR_DEVICE_TIMEOUT is recorded and the abort flag raised) or
-// once the abort flag is up.
-// `detail` (optional) receives (1 << 30) | flag index for the first flag wait that gives up.
-__device__ __forceinline__ unsigned wait_flag(const unsigned *flag, volatile int *abort_flag, int *status,
-                                              int *detail = nullptr, unsigned index = 0) {
-  unsigned v = ld_acquire_gpu(flag);
-  if (v) return v;
-  const uint64_t t0 = globaltimer_ns();
-#pragma unroll 1
-  while ((v = ld_acquire_gpu(flag)) == 0) {
-    if (*abort_flag) return 0;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
-      report_error(status, -6);
-      if (detail) atomicCAS(detail, 0, (int)((1u << 30) | (index & 0x3FFFFFFFu)));
-      *abort_flag = 1;
-      return 0;
-    }
-  }
-  return v;
-}
 
 // ----------------------------------------------------------------------------- named barriers
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {

@@ -44,15 +44,6 @@ struct ScanArgs {
   int *status;
 };
 
-__device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void st_release(unsigned *p, unsigned v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
 constexpr unsigned kBatch = 16;  // tickets taken per atomic (look-back case)
 
 __global__ void __launch_bounds__(kWarps * 32) scan_kernel(ScanArgs A) {
@@ -125,7 +116,7 @@ __global__ void __launch_bounds__(kWarps * 32) scan_kernel(ScanArgs A) {
         dst[0] = make_float4(x[0], x[1], x[2], x[3]);
         dst[1] = make_float4(x[4], x[5], x[6], x[7]);
         __threadfence();
-        st_release(A.flags + ticket, 1u);
+        st_release_gpu(A.flags + ticket, 1u);
       }
       __syncwarp();
 #pragma unroll
@@ -136,10 +127,10 @@ __global__ void __launch_bounds__(kWarps * 32) scan_kernel(ScanArgs A) {
         const unsigned pt = (unsigned)pred * A.ncg + cg;
         unsigned f = 0;
         if (lane == 0) {
-          f = ld_acquire(A.flags + pt);
+          f = ld_acquire_gpu(A.flags + pt);
           if (f == 0) {
             const uint64_t t0 = globaltimer_ns();
-            while ((f = ld_acquire(A.flags + pt)) == 0) {
+            while ((f = ld_acquire_gpu(A.flags + pt)) == 0) {
               if (globaltimer_ns() - t0 > kWaitLimitNs) {
                 report_error(A.status, -6);
                 f = 3;  // give up: treat as an inclusive prefix of zeros
@@ -174,7 +165,7 @@ __global__ void __launch_bounds__(kWarps * 32) scan_kernel(ScanArgs A) {
       dst[0] = make_float4(v[0], v[1], v[2], v[3]);
       dst[1] = make_float4(v[4], v[5], v[6], v[7]);
       __threadfence();
-      st_release(A.flags + ticket, 2u);
+      st_release_gpu(A.flags + ticket, 2u);
     }
     // exclusive outputs: out[p] = X_{l-1} + a^l * pin
     float al = 1.f;  // a^lane

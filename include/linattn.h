@@ -64,8 +64,8 @@ enum {
 /* Element type of the sequence tensors (states are always fp32). */
 enum { LINATTN_BF16 = 0, LINATTN_F32 = 1 };
 
-/* Workspace queries. */
-enum { LINATTN_OP_FWD = 1, LINATTN_OP_BWD = 2, LINATTN_OP_CHUNK_STATES = 3 };
+/* Workspace / checkpoint queries. */
+enum { LINATTN_OP_FWD = 1, LINATTN_OP_BWD = 2, LINATTN_OP_CHUNK_STATES = 3, LINATTN_OP_CHECKPOINT = 4 };
 
 typedef struct {
   int32_t abi_version;  /* must be LINATTN_ABI_VERSION                              */
@@ -87,8 +87,10 @@ const char *linattn_status_string(int32_t status);
 
 /* Workspace bytes needed by linattn_fwd (op=LINATTN_OP_FWD), linattn_bwd
  * (LINATTN_OP_BWD) or linattn_chunk_states (LINATTN_OP_CHUNK_STATES, with its
- * seg_len; ignored otherwise) for this shape on the current device.  Writes
- * *bytes and returns a status; the workspace must be 256-byte aligned. */
+ * seg_len; ignored otherwise) for this shape on the current device.  With
+ * op=LINATTN_OP_CHECKPOINT: bytes of the checkpoint of linattn_fwd_ckpt (may
+ * be 0 when the shape takes the CUDA-core path, which recomputes instead).
+ * Writes *bytes and returns a status; the workspace must be 256-byte aligned. */
 int32_t linattn_workspace_size(const linattn_shape *shape, int32_t op, int32_t seg_len,
                                size_t *bytes);
 
@@ -115,6 +117,26 @@ int32_t linattn_fwd(const linattn_shape *shape, const void *q, const void *k, co
 int32_t linattn_bwd(const linattn_shape *shape, const void *q, const void *k, const void *v,
                     const void *dO, const float *init_state, void *dq, void *dk, void *dv,
                     float *d_init_state, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Forward that also stores a checkpoint for linattn_bwd_ckpt: the fp32 state
+ * entering every chunk group of every sequence (the group length is the
+ * library's choice; size from linattn_workspace_size(.., LINATTN_OP_CHECKPOINT,
+ * ..)).  Same results as linattn_fwd (per-chunk states are not offered here).
+ * `checkpoint` is caller-owned device memory, 256-byte aligned.  Returns a
+ * status. */
+int32_t linattn_fwd_ckpt(const linattn_shape *shape, const void *q, const void *k, const void *v, void *o,
+                         const float *init_state, float *final_state, void *checkpoint,
+                         size_t checkpoint_bytes, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Backward that takes the forward states from a checkpoint written by
+ * linattn_fwd_ckpt for the same shape, k, v and init_state, instead of
+ * recomputing them.  init_state is the same as given to the forward (only the
+ * CUDA-core path, whose checkpoint is empty, reads it).  Same outputs as
+ * linattn_bwd.  Returns a status. */
+int32_t linattn_bwd_ckpt(const linattn_shape *shape, const void *q, const void *k, const void *v,
+                         const void *dO, const float *init_state, const void *checkpoint, size_t checkpoint_bytes,
+                         void *dq, void *dk, void *dv, float *d_init_state, void *workspace,
+                         size_t workspace_bytes, void *stream);
 
 /* Recurrent decode of T new tokens per sequence (constant-memory inference:
  * LASP-2 page, abstract): for t = 0..T-1
@@ -197,7 +219,7 @@ int32_t linattn_device_status(const void *workspace, void *stream);
  * for every kernel kind k < max_kinds its launch count and summed device time
  * (ms), clears the record and returns the number of kinds
  * (LINATTN_KERNEL_KINDS), or a negative status. */
-#define LINATTN_KERNEL_KINDS 11
+#define LINATTN_KERNEL_KINDS 9
 int32_t linattn_timing_enable(int32_t on);
 int32_t linattn_timing_collect(int32_t max_kinds, int32_t *launches, float *total_ms);
 /* Name of kernel kind k (static string; "?" when out of range). */

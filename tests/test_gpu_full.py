@@ -40,10 +40,24 @@ def lam_of(cfg, pairs):
     return None if lam is None else np.array([lam[h] for _, h in pairs], dtype=np.float32)
 
 
+def fwd_checked(q, k, v, **kw):
+    ws = la.workspace(q, la.OP_FWD, kw.get("decay"))
+    out = la.fwd(q, k, v, ws=ws, **kw)
+    assert la.device_status(ws) == la.OK
+    return out
+
+
+def bwd_checked(q, k, v, dO, **kw):
+    ws = la.workspace(q, la.OP_BWD, kw.get("decay"))
+    out = la.bwd(q, k, v, dO, ws=ws, **kw)
+    assert la.device_status(ws) == la.OK
+    return out
+
+
 def test_workload2_forward_full_size():
     cfg = inputs.WORKLOADS[2]
     x = load(cfg)
-    o, fin, _ = la.fwd(x["q"], x["k"], x["v"], want_final=True)
+    o, fin, _ = fwd_checked(x["q"], x["k"], x["v"], want_final=True)
     torch.cuda.synchronize()
     pairs = [(0, 0), (1, 7), (3, 15)]
     ref = heads64(cfg, pairs, ("q", "k", "v"))
@@ -59,8 +73,9 @@ def test_forward_backward_full_size(wl):
     x = load(cfg, ("q", "k", "v", "dO"))
     lam = inputs.workload_decay(cfg)
     dec = None if lam is None else torch.from_numpy(lam).cuda()
-    o, _, _ = la.fwd(x["q"], x["k"], x["v"], decay=dec)
-    dq, dk, dv, dinit = la.bwd(x["q"], x["k"], x["v"], x["dO"], decay=dec, want_dinit=True)
+    ck = la.checkpoint(x["q"], dec)   # the benchmark's step: checkpointed forward, then backward
+    o, _, _ = fwd_checked(x["q"], x["k"], x["v"], decay=dec, ckpt=ck)
+    dq, dk, dv, dinit = bwd_checked(x["q"], x["k"], x["v"], x["dO"], decay=dec, want_dinit=True, ckpt=ck)
     torch.cuda.synchronize()
     H = cfg["H"]
     pairs = [(0, 0), (cfg["B"] - 1, H - 1), (0, H // 2)]
@@ -82,8 +97,8 @@ def test_workload5_segmented_equals_single_and_oracle():
     seg = lambda t: t[0].view(H, S, L, d).permute(1, 0, 2, 3)        # [64, 16, 16384, 128] view
     U = la.chunk_states(x["k"], x["v"], L)                            # [64, 1, 16, 128, 128]
     init, total = la.state_scan(U.view(S, H, d, d), want_total=True)  # [64, 16, 128, 128]
-    o_seg, _, _ = la.fwd(seg(x["q"]), seg(x["k"]), seg(x["v"]), init_state=init)
-    o_one, fin, _ = la.fwd(x["q"], x["k"], x["v"], want_final=True)
+    o_seg, _, _ = fwd_checked(seg(x["q"]), seg(x["k"]), seg(x["v"]), init_state=init)
+    o_one, fin, _ = fwd_checked(x["q"], x["k"], x["v"], want_final=True)
     torch.cuda.synchronize()
     # property at full size: every output of the segmented run equals the single run
     diff = (o_seg.permute(1, 0, 2, 3).reshape(1, H, T, d).float() - o_one.float()).abs().max().item()

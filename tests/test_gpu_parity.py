@@ -103,9 +103,10 @@ def test_chunk_states(dtype, d, T, seg, dk):
 def run_fwd(c, dev, dtype, lam, init, want_cs=False):
     dec = None if lam is None else torch.from_numpy(lam).cuda()
     init_d = None if init is None else torch.from_numpy(init.astype(np.float32)).cuda()
+    ws = la.workspace(dev["q"], la.OP_FWD, dec)
     o, fin, cs = la.fwd(dev["q"], dev["k"], dev["v"], decay=dec, init_state=init_d, want_final=True,
-                        want_chunk_states=want_cs)
-    torch.cuda.synchronize()
+                        want_chunk_states=want_cs, ws=ws)
+    assert la.device_status(ws) == la.OK
     return o, fin, cs
 
 
@@ -187,15 +188,40 @@ def test_backward(dtype, d, T, dk):
     lam = decays(H, dk)
     init = (np.random.default_rng(T + 1).standard_normal((B, H, d, d)) * 0.1).astype(np.float32).astype(np.float64)
     dec = None if lam is None else torch.from_numpy(lam).cuda()
+    ws = la.workspace(dev["q"], la.OP_BWD, dec)
     dq, dk_, dv, dinit = la.bwd(dev["q"], dev["k"], dev["v"], dev["dO"], decay=dec,
-                                init_state=torch.from_numpy(init.astype(np.float32)).cuda(), want_dinit=True)
-    torch.cuda.synchronize()
+                                init_state=torch.from_numpy(init.astype(np.float32)).cuda(), want_dinit=True, ws=ws)
+    assert la.device_status(ws) == la.OK
     rq, rk, rv, rinit = oracle.bwd_recurrent(c["q"], c["k"], c["v"], c["dO"], lam=lam, init=init)
     tol = TOL[dtype]
     assert rel(dq, rq) < tol
     assert rel(dk_, rk) < tol
     assert rel(dv, rv) < tol
     assert rel(dinit, rinit) < tol
+
+
+@pytest.mark.parametrize("dtype,d", [(torch.bfloat16, 128), (torch.float32, 64)])
+@pytest.mark.parametrize("T,dk", [(2048, None), (8192 + 64, "cfg"), (1000, 0.5)])
+def test_checkpointed_forward_backward(dtype, d, T, dk):
+    """fwd_ckpt + bwd_ckpt give the oracle's outputs (the backward reads the stored group states)."""
+    B, H = 2, 2
+    c, dev = case(29 + T, B, H, T, d, dtype, sigma=1 / np.sqrt(128))
+    lam = decays(H, dk)
+    dec = None if lam is None else torch.from_numpy(lam).cuda()
+    init = (np.random.default_rng(T + 3).standard_normal((B, H, d, d)) * 0.1).astype(np.float32)
+    init_d = torch.from_numpy(init).cuda()
+    ck = la.checkpoint(dev["q"], dec)
+    wsf, wsb = la.workspace(dev["q"], la.OP_FWD, dec), la.workspace(dev["q"], la.OP_BWD, dec)
+    o, fin, _ = la.fwd(dev["q"], dev["k"], dev["v"], decay=dec, init_state=init_d, want_final=True, ws=wsf, ckpt=ck)
+    dq, dk_, dv, dinit = la.bwd(dev["q"], dev["k"], dev["v"], dev["dO"], decay=dec, want_dinit=True, ws=wsb,
+                                ckpt=ck, init_state=init_d)
+    assert la.device_status(wsf) == la.OK and la.device_status(wsb) == la.OK
+    init64 = init.astype(np.float64)
+    ro, _, rfin = oracle.fwd_recurrent(c["q"], c["k"], c["v"], lam=lam, init=init64)
+    rq, rk, rv, rinit = oracle.bwd_recurrent(c["q"], c["k"], c["v"], c["dO"], lam=lam, init=init64)
+    tol = TOL[dtype]
+    for got, ref in ((o, ro), (fin, rfin), (dq, rq), (dk_, rk), (dv, rv), (dinit, rinit)):
+        assert rel(got, ref) < tol
 
 
 def test_backward_many_groups_bf16():

@@ -32,10 +32,14 @@ METRIC = "causal linear-attn fwd+bwd tokens/s & TFLOP/s @H16 d128 T16K–1M; % r
 # q,k,v read + o written; backward 8d(C+d) FLOP and q,k,v,dO read + dq,dk,dv written.
 FLOP_FWD, FLOP_BWD = 98304, 196608
 BYTES_FWD, BYTES_BWD = 1024, 1792
-# algorithmic bytes of one launch of the chunked kernel: three bf16 sequence tensors
-# read and one written per token-head (its own re-reads of k, v for the group
-# aggregates are overhead, not credited)
-MAIN_BYTES_PER_TOKEN_HEAD = 1024
+# algorithmic bytes per token-head of one launch of each tensor-core kernel kind:
+# the chunked kernel reads three bf16 sequence tensors and writes one (with the
+# fused group aggregates of the dq pass it reads a fourth); the dual reverse-time
+# kernel reads four (k, q, dO, v) and writes two (dk, dv); the aggregate kernel
+# reads two.  Group states are overhead, not credited.
+KIND_BYTES_PER_TOKEN_HEAD = {"tc_chunked_fwd": 1024, "tc_chunked_rev": 1024, "tc_chunked_fwd_agg": 1280,
+                             "tc_dual_rev": 1536, "tc_segment_aggregate": 512}
+CHUNKED_KINDS = ("tc_chunked_fwd", "tc_chunked_rev", "tc_chunked_fwd_agg", "tc_dual_rev")
 
 
 def _dist():
@@ -260,26 +264,32 @@ def run_ours(args):
     bytes_ = (BYTES_FWD + BYTES_BWD) * B * H * T
     hbm, tf, peak_src = _peaks()
 
-    # ---- dominant kernel roofline (chunked kernel, forward and reverse-time launches)
+    # ---- dominant kernels' roofline: the chunked tensor-core kernels (the forward-time
+    # chunked kernel for o and dq, the dual reverse-time kernel for dk and dv); achieved =
+    # their algorithmic bytes over their summed CUDA-event time on the launching stream
     launches = sum(n for n, _ in kernels.values())
-    main = [kernels.get(k, (0, 0.0)) for k in ("tc_chunked_fwd", "tc_chunked_rev")]
-    n_main = sum(n for n, _ in main)
-    ms_main = sum(t for _, t in main)
-    per_launch_bytes = MAIN_BYTES_PER_TOKEN_HEAD * B * H * T
-    avg_ms = ms_main / max(n_main, 1)
-    achieved = per_launch_bytes / (avg_ms * 1e-3) / 1e9 if n_main else None
+    tok_heads = B * H * T
+    main = {k: kernels[k] for k in CHUNKED_KINDS if k in kernels}
+    n_main = sum(n for n, _ in main.values())
+    ms_main = sum(t for _, t in main.values())
+    bytes_main = sum(KIND_BYTES_PER_TOKEN_HEAD[k] * tok_heads * n for k, (n, _) in main.items())
+    achieved = bytes_main / (ms_main * 1e-3) / 1e9 if n_main else None
     traffic_tok = _profile_traffic()
     roofline = {
-        "kernel": "tc_main_kernel (chunked; forward- and reverse-time launches)",
+        "kernel": "chunked tensor-core kernels: " + ", ".join(f"{k} x{n // args.steps}" for k, (n, _) in main.items()),
         "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
         "frac": (achieved / hbm) if achieved else None,
-        "traffic": None if traffic_tok is None else traffic_tok * B * H * T,
+        "traffic": None if traffic_tok is None else traffic_tok * tok_heads,
         "peak_source": f"{peak_src} hbm_gbs",
         "launches_per_step": n_main / args.steps,
         "share_of_step": ms_main / (ms * args.steps) if ms else None,
     }
-    breakdown = {k: {"launches_per_step": n / args.steps, "ms_per_step": t / args.steps}
-                 for k, (n, t) in kernels.items()}
+    breakdown = {}
+    for k, (n, t) in kernels.items():
+        e = {"launches_per_step": n / args.steps, "ms_per_step": t / args.steps}
+        if k in KIND_BYTES_PER_TOKEN_HEAD and t > 0:
+            e["algorithmic_gbs"] = KIND_BYTES_PER_TOKEN_HEAD[k] * tok_heads * n / (t * 1e-3) / 1e9
+        breakdown[k] = e
 
     # ---- end to end through the public API with host buffers: every step copies its
     # inputs host->device from pinned memory and its results (o, dq, dk, dv) device->host.

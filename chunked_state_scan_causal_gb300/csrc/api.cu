@@ -330,19 +330,21 @@ static int32_t bwd_impl(const linattn_shape *shape, const void *q, const void *k
     states = st;
   }
   // dq: the forward-time kernel with (q, k, v) := (dO, v, k), reading every
-  // group's state transposed
-  if (e == cudaSuccess) e = tc_main(p, L, false, dO, v, k, dq, states, true, nullptr, status, s);
-  // reverse group states Rbar_g = sum_{u > group end} lambda^{u-end} q_u dO_u^T: group
-  // aggregates of q dO^T, scanned from the end; the value one step before token 0 is
-  // d_init = sum_t lambda^{t+1} q_t dO_t^T
-  if (e == cudaSuccess) e = tc_segment_states(p, L, q, dO, true, wagg, status, s);
+  // group's state transposed.  Reverse group states Rbar_g = sum_{u > group end}
+  // lambda^{u-end} q_u dO_u^T come from group aggregates of q dO^T scanned from
+  // the end (the value one step before token 0 is d_init = sum_t lambda^{t+1}
+  // q_t dO_t^T); without a decay the dq pass accumulates those aggregates too.
+  if (!p.decay) {
+    if (e == cudaSuccess) e = tc_main(p, L, false, dO, v, k, dq, states, true, nullptr, status, s, q, wagg);
+  } else {
+    if (e == cudaSuccess) e = tc_main(p, L, false, dO, v, k, dq, states, true, nullptr, status, s);
+    if (e == cudaSuccess) e = tc_segment_states(p, L, q, dO, true, wagg, status, s);
+  }
   if (e == cudaSuccess)
     e = state_scan(G, (int)BH, p.d * p.d, nullptr, p.decay, p.H, L, true, wagg, nullptr, rbar, d_init_state,
                    ws + w.f.scan, status, s);
-  // dv: the reverse-time kernel with (q, k, v) := (k, q, dO) and the states Rbar
-  if (e == cudaSuccess) e = tc_main(p, L, true, k, q, dO, dv, rbar, false, nullptr, status, s);
-  // dk: the reverse-time kernel with (q, k, v) := (v, dO, q) and the states Rbar^T
-  if (e == cudaSuccess) e = tc_main(p, L, true, v, dO, q, dk, rbar, true, nullptr, status, s);
+  // dv and dk in one reverse-time pass from the states Rbar
+  if (e == cudaSuccess) e = tc_dual(p, L, q, k, v, dO, dk, dv, rbar, status, s);
   return cuda_status(e);
 }
 
@@ -459,7 +461,7 @@ int32_t linattn_timing_collect(int32_t max_kinds, int32_t *launches, float *tota
 const char *linattn_kernel_name(int32_t kind) {
   static const char *names[K_KINDS] = {"simt_fwd", "simt_bwd", "simt_segment_states", "state_scan",
                                        "tc_segment_aggregate", "tc_chunked_fwd", "tc_chunked_rev",
-                                       "diag_mma", "decode"};
+                                       "diag_mma", "decode", "tc_dual_rev", "tc_chunked_fwd_agg"};
   return (kind >= 0 && kind < K_KINDS) ? names[kind] : "?";
 }
 

@@ -24,7 +24,7 @@ int device_ok();
 // ---------------------------------------------------------------- per-kernel timing (api.cu)
 enum KernelKind {
   K_SIMT_FWD = 0, K_SIMT_BWD, K_SIMT_SEGMENT, K_SCAN, K_TC_AGG, K_TC_MAIN_FWD, K_TC_MAIN_REV, K_DIAG,
-  K_DECODE, K_KINDS
+  K_DECODE, K_TC_DUAL_REV, K_TC_MAIN_AGG, K_KINDS
 };
 // Records timing events around one launch on `s` while timing is enabled.
 struct TimedLaunch {
@@ -66,9 +66,19 @@ cudaError_t tc_segment_states(const Problem &p, int seg_len, const void *X, cons
 // the group, o_i += lambda^{i+1} S^T q_i.  reverse == true: anti-causal, blocks
 // walked from the end, state = sum_{s > group end} lambda^{s - end} k_s v_s^T.
 // final_state (optional, forward only) is the state after the last token.
+// x (optional; forward time without decay): also writes agg_out[g] =
+// sum_{s in group g} x_s q_s^T ([G][BH][d][d]) from the same pass.
 cudaError_t tc_main(const Problem &p, int group_len, bool reverse, const void *q, const void *k,
                     const void *v, void *o, const float *group_init, bool init_transposed,
-                    float *final_state, int *status, cudaStream_t s);
+                    float *final_state, int *status, cudaStream_t s, const void *x = nullptr,
+                    float *agg_out = nullptr);
+
+// The backward's dv and dk in one reverse-time pass over (k, q, dO, v) from the
+// reverse group states [G][BH][d][d] (sum over later tokens u of
+// lambda^{u - group end} q_u dO_u^T); equals tc_main(reverse) with roles
+// (k, q, dO) for dv and (v, dO, q) with the transposed states for dk.
+cudaError_t tc_dual(const Problem &p, int group_len, const void *q, const void *k, const void *v,
+                    const void *dO, void *dk, void *dv, const float *group_init, int *status, cudaStream_t s);
 
 // ---------------------------------------------------------------- TMA descriptors (api.cu)
 // 4-D bf16 tiled tensor map, dims innermost first, strides in bytes for dims 1..3,

@@ -13,6 +13,8 @@
 // the natural tile, and chunking at 128 instead of 64 changes only the
 // rounding order (the chunked form equals the definition for any chunk
 // length).  All operands are SW128 tiles (ptx.cuh).
+#include <cuda_bf16.h>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -234,6 +236,7 @@ struct MainParams {
   const float *decay;
   const float *ginit;  // [G][BH][d][d]
   float *final_state;  // [BH][d][d] or null
+  float *agg_out;      // [G][BH][d][d]: per group sum_s x_s q_s^T (AGG instances)
   int *status;
 };
 
@@ -245,7 +248,7 @@ constexpr size_t kMainSmem = kOffBar + 256 + 1024;
 
 // barrier indices
 enum { B_FULL = 0, B_EMPTY = kSlots, B_PFULL = 2 * kSlots, B_PEMPTY, B_OFULL, B_OEMPTY, B_SFULL, B_PRE,
-       B_PSFULL, B_COUNT };
+       B_PSFULL, B_WEMPTY, B_COUNT };
 
 // Decay mask of one 32-column chunk of a score row: keep j <= i (causal) or
 // j >= i (anti-causal) and weight by lambda^{|i-j|}; walks j so that the
@@ -283,11 +286,18 @@ __device__ __forceinline__ void mask_chunk(float (&x)[32], int i, int c, float l
   }
 }
 
-template <bool DECAY, bool REV>
+// AGG instances (forward time, no decay) also load a fourth tile x per block
+// and accumulate the group aggregate W = sum_s x_s q_s^T in the fourth TMEM
+// region, written per group to agg_out: for the dq launch (q := dO, x := q)
+// that is the reverse group aggregate sum_s q_s dO_s^T.  Tiles are loaded in
+// the order q, x, k, v and released in the same order.
+template <bool DECAY, bool REV, bool AGG = false>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_main_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                    const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mo,
-                   MainParams P) {
+                   const __grid_constant__ CUtensorMap mx, MainParams P) {
+  static_assert(!AGG || (!DECAY && !REV), "group aggregates are fused for the forward-time, decay-free kernel");
+  constexpr int NT = AGG ? 4 : 3;  // tiles per block
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
   uint64_t *bar = reinterpret_cast<uint64_t *>(smem + kOffBar);
@@ -310,11 +320,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bar[B_SFULL], 1);
     mbar_init(&bar[B_PRE], 128);
     mbar_init(&bar[B_PSFULL], 128);
+    mbar_init(&bar[B_WEMPTY], 128);
     fence_mbar_init();
     prefetch_tensormap(&mq);
     prefetch_tensormap(&mk);
     prefetch_tensormap(&mv);
     prefetch_tensormap(&mo);
+    if (AGG) prefetch_tensormap(&mx);
   }
   if (warp == 1) {
     tmem_alloc(tslot, 512);
@@ -324,10 +336,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
-  const uint32_t tS = tmem, tP = tmem + 128, tO = tmem + 256;
+  const uint32_t tS = tmem, tP = tmem + 128, tO = tmem + 256, tW = tmem + 384;
   const uint32_t sbase = smem_u32(smem);
   const uint32_t sPs = sbase + kOffPs, sSh = sbase + kOffSh;
   auto slot_addr = [&](int t) { return sbase + (uint32_t)(t % kSlots) * kTileBytes; };
+  // ring position of tile role r (0 q, 1 k, 2 v, 3 x) of block blk
+  auto tile_of = [&](int blk, int r) {
+    return NT * blk + (AGG ? (r == 0 ? 0 : (r == 3 ? 1 : r + 1)) : r);
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -339,10 +355,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s0 = g * P.L, s1 = min(P.T, s0 + P.L), nb = (s1 - s0 + 127) / 128;
         for (int n = 0; n < nb && ok; ++n, ++blk) {
           const int t0 = s0 + 128 * (REV ? nb - 1 - n : n);
-          for (int x = 0; x < 3; ++x) {
-            const int t = 3 * blk + x, s = t % kSlots, u = t / kSlots;
+          for (int x = 0; x < NT; ++x) {
+            const int t = NT * blk + x, s = t % kSlots, u = t / kSlots;
             if (u > 0 && !(ok = mbar_wait(&bar[B_EMPTY + s], (u - 1) & 1, &abort_flag, P.status, detail))) break;
-            const CUtensorMap *m = x == 0 ? &mq : (x == 1 ? &mk : &mv);
+            const CUtensorMap *m = AGG ? (x == 0 ? &mq : (x == 1 ? &mx : (x == 2 ? &mk : &mv)))
+                                       : (x == 0 ? &mq : (x == 1 ? &mk : &mv));
             uint8_t *dst = smem + s * kTileBytes;
             mbar_arrive_expect_tx(&bar[B_FULL + s], kTileBytes);
             tma_load_4d(m, &bar[B_FULL + s], dst, 0, t0, h, b, kPolicyEvictFirst);
@@ -351,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // time-bounded drain of the loads in flight (also after an abort)
-      const int ntile = 3 * blk;
+      const int ntile = NT * blk;
       volatile int no_abort = 0;
       for (int s = 0; s < kSlots; ++s) {
         const int uses = ntile > s ? (ntile - 1 - s) / kSlots + 1 : 0;
@@ -364,13 +381,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t id_qk = idesc_bf16(128, 128, false, false);  // Q K^T
       const uint32_t id_qs = idesc_bf16(128, 128, false, true);   // Q S,  P V
       const uint32_t id_kv = idesc_bf16(128, 128, true, true);    // K^T V
-      int blk = 0;
+      const uint32_t id_xq = idesc_bf16(128, 128, true, true);    // X^T Q
+      int blk = 0, it = 0;
       bool ok = true;
-      for (int item = blockIdx.x; item < P.nitems && ok; item += gridDim.x) {
+      for (int item = blockIdx.x; item < P.nitems && ok; item += gridDim.x, ++it) {
         const int g = item / BH;
         const int s0 = g * P.L, s1 = min(P.T, s0 + P.L), nb = (s1 - s0 + 127) / 128;
         for (int n = 0; n < nb; ++n, ++blk) {
-          const int tq = 3 * blk, tk = tq + 1, tv = tq + 2;
+          const int tq = tile_of(blk, 0), tk = tile_of(blk, 1), tv = tile_of(blk, 2), tx = tile_of(blk, 3);
           const uint32_t Q = slot_addr(tq), K = slot_addr(tk), V = slot_addr(tv);
           // scores: P = Q K^T
           ok = mbar_wait(&bar[B_FULL + tq % kSlots], (tq / kSlots) & 1, &abort_flag, P.status, detail) &&
@@ -388,7 +406,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
 #pragma unroll
           for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tO, desc_kmajor(Q, ks), desc_mnmajor(sSh, ks), id_qs, ks > 0);
+          if (AGG) {
+            // group aggregate: W += X^T Q (the previous group's W must have been read out)
+            ok = mbar_wait(&bar[B_FULL + tx % kSlots], (tx / kSlots) & 1, &abort_flag, P.status, detail) &&
+                 (n > 0 || it == 0 || mbar_wait(&bar[B_WEMPTY], (it - 1) & 1, &abort_flag, P.status, detail));
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t X = slot_addr(tx);
+#pragma unroll
+            for (uint32_t ks = 0; ks < 8; ++ks)
+              mma_ss(tW, desc_mnmajor(X, ks), desc_mnmajor(Q, ks), id_xq, (n > 0 || ks > 0) ? 1u : 0u);
+          }
           mma_commit(&bar[B_EMPTY + tq % kSlots]);
+          if (AGG) mma_commit(&bar[B_EMPTY + tx % kSlots]);
           // state update: S += K'^T V
           if (!(ok = mbar_wait(&bar[B_FULL + tv % kSlots], (tv / kSlots) & 1, &abort_flag, P.status, detail))) break;
           tc_fence_after();
@@ -483,8 +513,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           wq = exp2f(l2 * (float)(REV ? nv - 1 - r : r + 1));
           wk = exp2f(l2 * (float)(REV ? r + 1 : nv - 1 - r));
         }
-        scale_tile_row(slot_addr(3 * bb), row, wq);
-        scale_tile_row(slot_addr(3 * bb + 1), row, wk);
+        scale_tile_row(slot_addr(tile_of(bb, 0)), row, wq);
+        scale_tile_row(slot_addr(tile_of(bb, 1)), row, wk);
         return true;
       };
       // initial state of the group
@@ -540,6 +570,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_before();
           fence_proxy_async_smem();
           mbar_arrive(&bar[B_PRE]);
+        } else if (AGG) {
+          // the group's aggregate W (complete: its last product precedes the state update)
+          float *dst = P.agg_out + ((int64_t)g * BH + bh) * 16384 + row * 128;
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            float x[32];
+            ld_chunk(tW + lb + c * 32, x);
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+              *reinterpret_cast<float4 *>(dst + c * 32 + j) = make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
+          }
+          tc_fence_before();
+          mbar_arrive(&bar[B_WEMPTY]);
         } else if (P.final_state && !REV && g == P.G - 1) {
           float *dst = P.final_state + (int64_t)bh * 16384 + row * 128;
 #pragma unroll 1
@@ -551,6 +594,388 @@ __global__ void __launch_bounds__(kThreads, 1)
               *reinterpret_cast<float4 *>(dst + c * 32 + j) = make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
           }
           tc_fence_before();
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// ============================================================================ reverse-time dual kernel
+// dv and dk of the backward in one pass over (k, q, dO, v), walking every
+// group's blocks from its end.  With R the reverse state entering a block
+// (R = sum over later tokens u of lambda^{u - block end} q_u dO_u^T) and rows
+// i, j of the block (nv valid rows):
+//   dv = diag(lambda^{nv-1-i}) K R   + (K Q^T  (.) M) dO
+//   dk = diag(lambda^{nv-1-i}) V R^T + (V dO^T (.) M) Q
+//   R <- lambda^{nv} R + Q^T diag(lambda^{j+1}) dO
+// with the anti-causal decay mask M_ij = lambda^{j-i} [j >= i].  Both outputs
+// share one TMEM state; R^T is the same bf16 tile read through a K-major
+// descriptor.  Warps 12..15 (group C) write dv and dk straight from registers.
+struct DualParams {
+  int B, H, T, L, G, nitems;
+  const float *decay;
+  const float *ginit;  // [G][BH][d][d] reverse states entering each group
+  __nv_bfloat16 *dk, *dv;
+  int64_t sb, sh, st;  // element strides of dk and dv
+  int *status;
+};
+
+constexpr int kDualThreads = 512;
+enum { D_FULL = 0, D_EMPTY = kSlots, D_PFULL = 2 * kSlots, D_PEMPTY, D_PSFULL, D_PSEMPTY, D_O1FULL, D_O1EMPTY,
+       D_O2FULL, D_O2EMPTY, D_SFULL, D_PRE, D_KSC, D_VSC, D_DSC, D_COUNT };
+
+// Ring slot and earlier loads into that slot for tile x (0 K, 1 Q, 2 V, 3 dO)
+// of the blk-th block a CTA processes.  Tiles are loaded in the order K, Q, V,
+// dO and released in the order K, V, dO, Q (Q is read by the last product of
+// the block), and every tile takes the slot freed five releases earlier: V
+// and dO then keep slots 2 and 3, and K and Q rotate over slots 0, 1, 4
+// (K of block b reuses Q of block b-2, Q of block b reuses K of block b-1).
+__device__ __forceinline__ void dual_slot(int blk, int x, int &slot, int &cnt) {
+  const int r = blk % 3, q3 = blk / 3;
+  if (x == 0) {
+    slot = r == 0 ? 0 : (r == 1 ? 4 : 1);
+    cnt = 2 * q3 + (r == 2 ? 1 : 0);
+  } else if (x == 1) {
+    slot = r == 0 ? 1 : (r == 1 ? 0 : 4);
+    cnt = 2 * q3 + (r != 0 ? 1 : 0);
+  } else {
+    slot = x;
+    cnt = blk;
+  }
+}
+
+// 32 fp32 values -> 64 contiguous bytes of bf16 in global memory (streaming store).
+__device__ __forceinline__ void st_global_chunk_bf16(__nv_bfloat16 *dst, const float (&x)[32]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    asm volatile("st.global.cs.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(dst + 8 * q),
+                 "r"(pack_bf16(x[8 * q + 0], x[8 * q + 1])), "r"(pack_bf16(x[8 * q + 2], x[8 * q + 3])),
+                 "r"(pack_bf16(x[8 * q + 4], x[8 * q + 5])), "r"(pack_bf16(x[8 * q + 6], x[8 * q + 7]))
+                 : "memory");
+  }
+}
+
+template <bool DECAY>
+__global__ void __launch_bounds__(kDualThreads, 1)
+    tc_dual_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mq,
+                   const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
+                   DualParams P) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = align1024(smem_raw);
+  uint64_t *bar = reinterpret_cast<uint64_t *>(smem + kOffBar);
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + D_COUNT);
+  __shared__ int abort_flag;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int BH = P.B * P.H;
+  int *const detail = P.status ? P.status + 1 + warp : nullptr;
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(&bar[D_FULL + s], 1);
+      mbar_init(&bar[D_EMPTY + s], 1);
+    }
+    mbar_init(&bar[D_PFULL], 1);
+    mbar_init(&bar[D_PEMPTY], 128);
+    mbar_init(&bar[D_PSFULL], 128);
+    mbar_init(&bar[D_PSEMPTY], 1);
+    mbar_init(&bar[D_O1FULL], 1);
+    mbar_init(&bar[D_O1EMPTY], 128);
+    mbar_init(&bar[D_O2FULL], 1);
+    mbar_init(&bar[D_O2EMPTY], 128);
+    mbar_init(&bar[D_SFULL], 1);
+    mbar_init(&bar[D_PRE], 128);
+    mbar_init(&bar[D_KSC], 128);
+    mbar_init(&bar[D_VSC], 128);
+    mbar_init(&bar[D_DSC], 128);
+    fence_mbar_init();
+    prefetch_tensormap(&mk);
+    prefetch_tensormap(&mq);
+    prefetch_tensormap(&mv);
+    prefetch_tensormap(&mdo);
+  }
+  if (warp == 1) {
+    tmem_alloc(tslot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  const uint32_t tR = tmem, tP = tmem + 128, tO1 = tmem + 256, tO2 = tmem + 384;
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t sPs = sbase + kOffPs, sSh = sbase + kOffSh;
+  auto tile_addr = [&](int slot) { return sbase + (uint32_t)slot * kTileBytes; };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int blk = 0;
+      bool ok = true;
+      int loads[kSlots] = {0, 0, 0, 0, 0};
+      for (int item = blockIdx.x; item < P.nitems && ok; item += gridDim.x) {
+        const int g = item / BH, bh = item % BH, b = bh / P.H, h = bh % P.H;
+        const int s0 = g * P.L, s1 = min(P.T, s0 + P.L), nb = (s1 - s0 + 127) / 128;
+        for (int n = 0; n < nb && ok; ++n, ++blk) {
+          const int t0 = s0 + 128 * (nb - 1 - n);
+          for (int x = 0; x < 4; ++x) {
+            int s, c;
+            dual_slot(blk, x, s, c);
+            if (c > 0 && !(ok = mbar_wait(&bar[D_EMPTY + s], (c - 1) & 1, &abort_flag, P.status, detail))) break;
+            const CUtensorMap *m = x == 0 ? &mk : (x == 1 ? &mq : (x == 2 ? &mv : &mdo));
+            uint8_t *dst = smem + s * kTileBytes;
+            mbar_arrive_expect_tx(&bar[D_FULL + s], kTileBytes);
+            tma_load_4d(m, &bar[D_FULL + s], dst, 0, t0, h, b, kPolicyEvictFirst);
+            tma_load_4d(m, &bar[D_FULL + s], dst + kTileHalfBytes, 64, t0, h, b, kPolicyEvictFirst);
+            ++loads[s];
+          }
+        }
+      }
+      volatile int no_abort = 0;
+      for (int s = 0; s < kSlots; ++s)
+        if (loads[s] > 0) mbar_wait(&bar[D_FULL + s], (loads[s] - 1) & 1, &no_abort, P.status);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t id_kk = idesc_bf16(128, 128, false, false);  // A K-major, B K-major
+      const uint32_t id_km = idesc_bf16(128, 128, false, true);   // A K-major, B MN-major
+      const uint32_t id_mm = idesc_bf16(128, 128, true, true);    // A MN-major, B MN-major
+      int blk = 0;
+      bool ok = true;
+      auto wait = [&](int idx, int parity) {
+        return mbar_wait(&bar[idx], parity & 1, &abort_flag, P.status, detail);
+      };
+      for (int item = blockIdx.x; item < P.nitems && ok; item += gridDim.x) {
+        const int g = item / BH;
+        const int s0 = g * P.L, s1 = min(P.T, s0 + P.L), nb = (s1 - s0 + 127) / 128;
+        for (int n = 0; n < nb && ok; ++n, ++blk) {
+          int sk, ck, sq, cq;
+          dual_slot(blk, 0, sk, ck);
+          dual_slot(blk, 1, sq, cq);
+          const uint32_t K = tile_addr(sk), Q = tile_addr(sq), V = tile_addr(2), DO = tile_addr(3);
+          const int u1 = 2 * blk, u2 = u1 + 1;
+          // P1 = K Q^T
+          ok = wait(D_FULL + sk, ck) && wait(D_FULL + sq, cq) && (u1 == 0 || wait(D_PEMPTY, u1 - 1));
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tP, desc_kmajor(K, ks), desc_kmajor(Q, ks), id_kk, ks > 0);
+          mma_commit(&bar[D_PFULL]);
+          // dv  = K' R   (R from the bf16 state tile, MN-major)
+          ok = (!DECAY || wait(D_KSC, blk)) && wait(D_PRE, blk) && (blk == 0 || wait(D_O1EMPTY, blk - 1));
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tO1, desc_kmajor(K, ks), desc_mnmajor(sSh, ks), id_km, ks > 0);
+          mma_commit(&bar[D_EMPTY + sk]);
+          if (!DECAY) {
+            // dk  = V R^T  (the same tile, K-major)
+            ok = wait(D_FULL + 2, blk) && (blk == 0 || wait(D_O2EMPTY, blk - 1));
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tO2, desc_kmajor(V, ks), desc_kmajor(sSh, ks), id_kk, ks > 0);
+            // R += Q^T dO
+            if (!(ok = wait(D_FULL + 3, blk))) break;
+            tc_fence_after();
+#pragma unroll
+            for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tR, desc_mnmajor(Q, ks), desc_mnmajor(DO, ks), id_mm, 1u);
+            mma_commit(&bar[D_SFULL]);
+            // P2 = V dO^T once the masked P1 has left TMEM
+            ok = wait(D_PSFULL, u1) && wait(D_PEMPTY, u1);
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tP, desc_kmajor(V, ks), desc_kmajor(DO, ks), id_kk, ks > 0);
+            mma_commit(&bar[D_PFULL]);
+            mma_commit(&bar[D_EMPTY + 2]);
+            // dv += P1~ dO
+#pragma unroll
+            for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tO1, desc_kmajor(sPs, ks), desc_mnmajor(DO, ks), id_km, 1u);
+            mma_commit(&bar[D_PSEMPTY]);
+            mma_commit(&bar[D_O1FULL]);
+            mma_commit(&bar[D_EMPTY + 3]);
+          } else {
+            // P2 = V dO^T once the masked P1 has left TMEM
+            ok = wait(D_PSFULL, u1) && wait(D_PEMPTY, u1) && wait(D_FULL + 2, blk) && wait(D_FULL + 3, blk);
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tP, desc_kmajor(V, ks), desc_kmajor(DO, ks), id_kk, ks > 0);
+            mma_commit(&bar[D_PFULL]);
+            // dv += P1~ dO
+#pragma unroll
+            for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tO1, desc_kmajor(sPs, ks), desc_mnmajor(DO, ks), id_km, 1u);
+            mma_commit(&bar[D_PSEMPTY]);
+            mma_commit(&bar[D_O1FULL]);
+            // dk = V' R^T once V's rows are weighted
+            ok = wait(D_VSC, blk) && (blk == 0 || wait(D_O2EMPTY, blk - 1));
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tO2, desc_kmajor(V, ks), desc_kmajor(sSh, ks), id_kk, ks > 0);
+            mma_commit(&bar[D_EMPTY + 2]);
+            // R += Q^T dO' once dO's rows are weighted
+            if (!(ok = wait(D_DSC, blk))) break;
+            tc_fence_after();
+#pragma unroll
+            for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tR, desc_mnmajor(Q, ks), desc_mnmajor(DO, ks), id_mm, 1u);
+            mma_commit(&bar[D_SFULL]);
+            mma_commit(&bar[D_EMPTY + 3]);
+          }
+          // dk += P2~ Q
+          if (!(ok = wait(D_PSFULL, u2))) break;
+          tc_fence_after();
+#pragma unroll
+          for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tO2, desc_kmajor(sPs, ks), desc_mnmajor(Q, ks), id_km, 1u);
+          mma_commit(&bar[D_PSEMPTY]);
+          mma_commit(&bar[D_O2FULL]);
+          mma_commit(&bar[D_EMPTY + sq]);
+        }
+      }
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // ------------------------------------------------------------ group A: masked score tiles
+    const uint32_t quad = warp & 3, row = quad * 32 + lane, lb = (quad * 32) << 16;
+    int blk = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; item < P.nitems && ok; item += gridDim.x) {
+      const int g = item / BH, h = (item % BH) % P.H;
+      const int s0 = g * P.L, s1 = min(P.T, s0 + P.L), nb = (s1 - s0 + 127) / 128;
+      const float lam = DECAY ? P.decay[h] : 1.f;
+      const float l2 = DECAY ? log2f(lam) : 0.f;
+      for (int n = 0; n < nb && ok; ++n, ++blk) {
+        for (int half = 0; half < 2 && ok; ++half) {
+          const int u = 2 * blk + half;
+          ok = __all_sync(0xffffffffu, mbar_wait(&bar[D_PFULL], u & 1, &abort_flag, P.status, detail)) &&
+               __all_sync(0xffffffffu,
+                          u == 0 || mbar_wait(&bar[D_PSEMPTY], (u - 1) & 1, &abort_flag, P.status, detail));
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            float x[32];
+            ld_chunk(tP + lb + c * 32, x);
+            mask_chunk<DECAY, true>(x, (int)row, c, lam, l2);
+            store_row_chunk_bf16(sPs, row, c, x);
+          }
+          tc_fence_before();
+          mbar_arrive(&bar[D_PEMPTY]);
+          fence_proxy_async_smem();
+          mbar_arrive(&bar[D_PSFULL]);
+        }
+      }
+    }
+  } else if (warp >= 8 && warp < 12) {
+    // ------------------------------------------------------------ group B: state tile (+ decay weights)
+    const uint32_t quad = warp & 3, row = quad * 32 + lane, lb = (quad * 32) << 16;
+    int blk = 0;
+    bool ok = true;
+    auto wait = [&](int idx, int parity) {
+      return __all_sync(0xffffffffu, mbar_wait(&bar[idx], parity & 1, &abort_flag, P.status, detail));
+    };
+    for (int item = blockIdx.x; item < P.nitems && ok; item += gridDim.x) {
+      const int g = item / BH, bh = item % BH, h = bh % P.H;
+      const int s0 = g * P.L, s1 = min(P.T, s0 + P.L), nb = (s1 - s0 + 127) / 128;
+      const float lam = DECAY ? P.decay[h] : 1.f;
+      const float l2 = DECAY ? log2f(lam) : 0.f;
+      auto nvalid = [&](int n) { return min(128, s1 - (s0 + 128 * (nb - 1 - n))); };
+      {
+        const float *src = P.ginit + ((int64_t)g * BH + bh) * 16384;
+        const float dec = DECAY ? exp2f(l2 * (float)nvalid(0)) : 1.f;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          float x[32];
+#pragma unroll
+          for (int j = 0; j < 32; j += 4) {
+            const float4 v4 = __ldg(reinterpret_cast<const float4 *>(src + row * 128 + c * 32 + j));
+            x[j] = v4.x; x[j + 1] = v4.y; x[j + 2] = v4.z; x[j + 3] = v4.w;
+          }
+          store_row_chunk_bf16(sSh, row, c, x);
+          uint32_t r[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(x[j] * dec);
+          tmem_st32(tR + lb + c * 32, r);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        fence_proxy_async_smem();
+        mbar_arrive(&bar[D_PRE]);
+      }
+      for (int n = 0; n < nb && ok; ++n, ++blk) {
+        if (DECAY) {
+          const int nv = nvalid(n), r = (int)row;
+          const float wx = r < nv ? exp2f(l2 * (float)(nv - 1 - r)) : 0.f;  // rows of K and V
+          const float wy = r < nv ? exp2f(l2 * (float)(r + 1)) : 0.f;       // rows of dO
+          int sk, ck;
+          dual_slot(blk, 0, sk, ck);
+          if (!(ok = wait(D_PFULL, 2 * blk))) break;
+          scale_tile_row(tile_addr(sk), row, wx);
+          fence_proxy_async_smem();
+          mbar_arrive(&bar[D_KSC]);
+          if (!(ok = wait(D_PFULL, 2 * blk + 1))) break;
+          scale_tile_row(tile_addr(2), row, wx);
+          fence_proxy_async_smem();
+          mbar_arrive(&bar[D_VSC]);
+          if (!(ok = wait(D_O1FULL, blk))) break;
+          scale_tile_row(tile_addr(3), row, wy);
+          fence_proxy_async_smem();
+          mbar_arrive(&bar[D_DSC]);
+        }
+        if (!(ok = wait(D_SFULL, blk))) break;
+        tc_fence_after();
+        if (n + 1 < nb) {
+          const float dec = DECAY ? exp2f(l2 * (float)nvalid(n + 1)) : 1.f;
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            float x[32];
+            ld_chunk(tR + lb + c * 32, x);
+            store_row_chunk_bf16(sSh, row, c, x);
+            if (DECAY) {
+              uint32_t r[32];
+#pragma unroll
+              for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(x[j] * dec);
+              tmem_st32(tR + lb + c * 32, r);
+            }
+          }
+          if (DECAY) tmem_st_wait();
+          tc_fence_before();
+          fence_proxy_async_smem();
+          mbar_arrive(&bar[D_PRE]);
+        }
+      }
+    }
+  } else if (warp >= 12) {
+    // ------------------------------------------------------------ group C: dv and dk rows to global memory
+    const uint32_t quad = warp & 3, row = quad * 32 + lane, lb = (quad * 32) << 16;
+    int blk = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; item < P.nitems && ok; item += gridDim.x) {
+      const int g = item / BH, bh = item % BH, b = bh / P.H, h = bh % P.H;
+      const int s0 = g * P.L, s1 = min(P.T, s0 + P.L), nb = (s1 - s0 + 127) / 128;
+      for (int n = 0; n < nb && ok; ++n, ++blk) {
+        const int t0 = s0 + 128 * (nb - 1 - n);
+        const bool valid = t0 + (int)row < s1;
+        for (int half = 0; half < 2 && ok; ++half) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&bar[half ? D_O2FULL : D_O1FULL], blk & 1, &abort_flag,
+                                                 P.status, detail));
+          if (!ok) break;
+          tc_fence_after();
+          __nv_bfloat16 *dst = (half ? P.dk : P.dv) + (int64_t)b * P.sb + (int64_t)h * P.sh +
+                               (int64_t)(t0 + (int)row) * P.st;
+          const uint32_t tO = half ? tO2 : tO1;
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            float x[32];
+            ld_chunk(tO + lb + c * 32, x);
+            if (valid) st_global_chunk_bf16(dst + c * 32, x);
+          }
+          tc_fence_before();
+          mbar_arrive(&bar[half ? D_O2EMPTY : D_O1EMPTY]);
         }
       }
     }
@@ -597,11 +1022,38 @@ cudaError_t tc_segment_states(const Problem &p, int seg_len, const void *X, cons
   return cudaGetLastError();
 }
 
+cudaError_t tc_dual(const Problem &p, int group_len, const void *q, const void *k, const void *v,
+                    const void *dO, void *dk, void *dv, const float *group_init, int *status, cudaStream_t s) {
+  alignas(64) CUtensorMap mk, mq, mv, mdo;
+  if (!seq_tmap(p, k, &mk) || !seq_tmap(p, q, &mq) || !seq_tmap(p, v, &mv) || !seq_tmap(p, dO, &mdo))
+    return cudaErrorInvalidValue;
+  DualParams D;
+  D.B = p.B; D.H = p.H; D.T = p.T; D.L = group_len;
+  D.G = (p.T + group_len - 1) / group_len;
+  D.nitems = D.G * p.B * p.H;
+  D.decay = p.decay; D.ginit = group_init;
+  D.dk = static_cast<__nv_bfloat16 *>(dk); D.dv = static_cast<__nv_bfloat16 *>(dv);
+  D.sb = p.sb; D.sh = p.sh; D.st = p.st; D.status = status;
+  const int grid = D.nitems < p.num_sms ? D.nitems : p.num_sms;
+  cudaError_t e;
+  TimedLaunch t(K_TC_DUAL_REV, s);
+  if (p.decay) {
+    if ((e = set_smem(tc_dual_kernel<true>, kMainSmem)) != cudaSuccess) return e;
+    tc_dual_kernel<true><<<grid, kDualThreads, kMainSmem, s>>>(mk, mq, mv, mdo, D);
+  } else {
+    if ((e = set_smem(tc_dual_kernel<false>, kMainSmem)) != cudaSuccess) return e;
+    tc_dual_kernel<false><<<grid, kDualThreads, kMainSmem, s>>>(mk, mq, mv, mdo, D);
+  }
+  return cudaGetLastError();
+}
+
 cudaError_t tc_main(const Problem &p, int group_len, bool reverse, const void *q, const void *k,
                     const void *v, void *o, const float *group_init, bool init_transposed,
-                    float *final_state, int *status, cudaStream_t s) {
-  alignas(64) CUtensorMap mq, mk, mv, mo;
-  if (!seq_tmap(p, q, &mq) || !seq_tmap(p, k, &mk) || !seq_tmap(p, v, &mv) || !seq_tmap(p, o, &mo))
+                    float *final_state, int *status, cudaStream_t s, const void *x, float *agg_out) {
+  if (x && (reverse || p.decay || !agg_out)) return cudaErrorInvalidValue;
+  alignas(64) CUtensorMap mq, mk, mv, mo, mx;
+  if (!seq_tmap(p, q, &mq) || !seq_tmap(p, k, &mk) || !seq_tmap(p, v, &mv) || !seq_tmap(p, o, &mo) ||
+      !seq_tmap(p, x ? x : q, &mx))
     return cudaErrorInvalidValue;
   MainParams M;
   M.B = p.B; M.H = p.H; M.T = p.T; M.L = group_len;
@@ -609,18 +1061,21 @@ cudaError_t tc_main(const Problem &p, int group_len, bool reverse, const void *q
   M.nitems = M.G * p.B * p.H;
   M.init_t = init_transposed ? 1 : 0;
   M.decay = p.decay; M.ginit = group_init; M.final_state = final_state; M.status = status;
+  M.agg_out = agg_out;
   const int grid = M.nitems < p.num_sms ? M.nitems : p.num_sms;
   cudaError_t e;
-  TimedLaunch t(reverse ? K_TC_MAIN_REV : K_TC_MAIN_FWD, s);
-#define LINATTN_LAUNCH_MAIN(DEC, REV)                                              \
-  do {                                                                             \
-    if ((e = set_smem(tc_main_kernel<DEC, REV>, kMainSmem)) != cudaSuccess) return e; \
-    tc_main_kernel<DEC, REV><<<grid, kThreads, kMainSmem, s>>>(mq, mk, mv, mo, M);  \
+  TimedLaunch t(x ? K_TC_MAIN_AGG : (reverse ? K_TC_MAIN_REV : K_TC_MAIN_FWD), s);
+#define LINATTN_LAUNCH_MAIN(DEC, REV, AGG)                                                     \
+  do {                                                                                        \
+    if ((e = set_smem(tc_main_kernel<DEC, REV, AGG>, kMainSmem)) != cudaSuccess) return e;    \
+    tc_main_kernel<DEC, REV, AGG><<<grid, kThreads, kMainSmem, s>>>(mq, mk, mv, mo, mx, M);   \
   } while (0)
-  if (p.decay) {
-    if (reverse) LINATTN_LAUNCH_MAIN(true, true); else LINATTN_LAUNCH_MAIN(true, false);
+  if (x) {
+    LINATTN_LAUNCH_MAIN(false, false, true);
+  } else if (p.decay) {
+    if (reverse) LINATTN_LAUNCH_MAIN(true, true, false); else LINATTN_LAUNCH_MAIN(true, false, false);
   } else {
-    if (reverse) LINATTN_LAUNCH_MAIN(false, true); else LINATTN_LAUNCH_MAIN(false, false);
+    if (reverse) LINATTN_LAUNCH_MAIN(false, true, false); else LINATTN_LAUNCH_MAIN(false, false, false);
   }
 #undef LINATTN_LAUNCH_MAIN
   return cudaGetLastError();

@@ -613,7 +613,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 //   R <- lambda^{nv} R + Q^T diag(lambda^{j+1}) dO
 // with the anti-causal decay mask M_ij = lambda^{j-i} [j >= i].  Both outputs
 // share one TMEM state; R^T is the same bf16 tile read through a K-major
-// descriptor.  Warps 12..15 (group C) write dv and dk straight from registers.
+// descriptor.  The masked score tiles stay in TMEM: group A overwrites each
+// fp32 score tile with its bf16 pairs, which the next product reads as its A
+// operand (tcgen05 products issued by one thread run in issue order, so the
+// following score product may overwrite them).  That leaves shared memory for
+// six input tiles.  Warps 12..15 (group C) write dv and dk from registers.
 struct DualParams {
   int B, H, T, L, G, nitems;
   const float *decay;
@@ -624,27 +628,26 @@ struct DualParams {
 };
 
 constexpr int kDualThreads = 512;
-enum { D_FULL = 0, D_EMPTY = kSlots, D_PFULL = 2 * kSlots, D_PEMPTY, D_PSFULL, D_PSEMPTY, D_O1FULL, D_O1EMPTY,
-       D_O2FULL, D_O2EMPTY, D_SFULL, D_PRE, D_KSC, D_VSC, D_DSC, D_COUNT };
+constexpr int kDualSlots = 6;
+constexpr uint32_t kDualOffSh = kDualSlots * kTileBytes;  // bf16 state tile
+constexpr uint32_t kDualOffBar = kDualOffSh + kTileBytes;
+constexpr size_t kDualSmem = kDualOffBar + 256 + 1024;
+enum { D_FULL = 0, D_EMPTY = kDualSlots, D_PFULL = 2 * kDualSlots, D_PSFULL, D_O1FULL, D_O1EMPTY, D_O2FULL,
+       D_O2EMPTY, D_SFULL, D_PRE, D_KSC, D_VSC, D_COUNT };
 
-// Ring slot and earlier loads into that slot for tile x (0 K, 1 Q, 2 V, 3 dO)
-// of the blk-th block a CTA processes.  Tiles are loaded in the order K, Q, V,
-// dO and released in the order K, V, dO, Q (Q is read by the last product of
-// the block), and every tile takes the slot freed five releases earlier: V
-// and dO then keep slots 2 and 3, and K and Q rotate over slots 0, 1, 4
-// (K of block b reuses Q of block b-2, Q of block b reuses K of block b-1).
+// Ring slot of tile x (0 K, 1 Q, 2 dO, 3 V) of the blk-th block a CTA
+// processes, and how many loads that slot received before it.  Tiles are
+// loaded in that order and released in the order K, dO, V, Q; each takes the
+// slot freed six releases earlier, which repeats every four blocks:
+//   slots  [0 1 2 3] [4 5 0 2] [3 1 4 0] [2 5 3 4]
+// with 3, 2, 3, 3, 3, 2 loads of slots 0..5 per four blocks.
 __device__ __forceinline__ void dual_slot(int blk, int x, int &slot, int &cnt) {
-  const int r = blk % 3, q3 = blk / 3;
-  if (x == 0) {
-    slot = r == 0 ? 0 : (r == 1 ? 4 : 1);
-    cnt = 2 * q3 + (r == 2 ? 1 : 0);
-  } else if (x == 1) {
-    slot = r == 0 ? 1 : (r == 1 ? 0 : 4);
-    cnt = 2 * q3 + (r != 0 ? 1 : 0);
-  } else {
-    slot = x;
-    cnt = blk;
-  }
+  constexpr uint64_t kSlot = 0x4352041320543210ull;  // 4 bits per (blk % 4, x)
+  constexpr uint32_t kPrior = 0xa6955000u;           // 2 bits: loads of the slot earlier in the period
+  constexpr uint32_t kPerPeriod = 0xbfbu;            // 2 bits per slot: loads per period
+  const int i = 4 * (blk & 3) + x;
+  slot = (int)((kSlot >> (4 * i)) & 15u);
+  cnt = (blk >> 2) * (int)((kPerPeriod >> (2 * slot)) & 3u) + (int)((kPrior >> (2 * i)) & 3u);
 }
 
 // 32 fp32 values -> 64 contiguous bytes of bf16 in global memory (streaming store).
@@ -665,7 +668,7 @@ __global__ void __launch_bounds__(kDualThreads, 1)
                    DualParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
-  uint64_t *bar = reinterpret_cast<uint64_t *>(smem + kOffBar);
+  uint64_t *bar = reinterpret_cast<uint64_t *>(smem + kDualOffBar);
   uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + D_COUNT);
   __shared__ int abort_flag;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -674,14 +677,12 @@ __global__ void __launch_bounds__(kDualThreads, 1)
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    for (int s = 0; s < kSlots; ++s) {
+    for (int s = 0; s < kDualSlots; ++s) {
       mbar_init(&bar[D_FULL + s], 1);
       mbar_init(&bar[D_EMPTY + s], 1);
     }
     mbar_init(&bar[D_PFULL], 1);
-    mbar_init(&bar[D_PEMPTY], 128);
     mbar_init(&bar[D_PSFULL], 128);
-    mbar_init(&bar[D_PSEMPTY], 1);
     mbar_init(&bar[D_O1FULL], 1);
     mbar_init(&bar[D_O1EMPTY], 128);
     mbar_init(&bar[D_O2FULL], 1);
@@ -690,7 +691,6 @@ __global__ void __launch_bounds__(kDualThreads, 1)
     mbar_init(&bar[D_PRE], 128);
     mbar_init(&bar[D_KSC], 128);
     mbar_init(&bar[D_VSC], 128);
-    mbar_init(&bar[D_DSC], 128);
     fence_mbar_init();
     prefetch_tensormap(&mk);
     prefetch_tensormap(&mq);
@@ -707,7 +707,7 @@ __global__ void __launch_bounds__(kDualThreads, 1)
   const uint32_t tmem = *tslot;
   const uint32_t tR = tmem, tP = tmem + 128, tO1 = tmem + 256, tO2 = tmem + 384;
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t sPs = sbase + kOffPs, sSh = sbase + kOffSh;
+  const uint32_t sSh = sbase + kDualOffSh;
   auto tile_addr = [&](int slot) { return sbase + (uint32_t)slot * kTileBytes; };
 
   if (warp == 0) {
@@ -715,7 +715,7 @@ __global__ void __launch_bounds__(kDualThreads, 1)
     if (lane == 0) {
       int blk = 0;
       bool ok = true;
-      int loads[kSlots] = {0, 0, 0, 0, 0};
+      int loads[kDualSlots] = {0, 0, 0, 0, 0, 0};
       for (int item = blockIdx.x; item < P.nitems && ok; item += gridDim.x) {
         const int g = item / BH, bh = item % BH, b = bh / P.H, h = bh % P.H;
         const int s0 = g * P.L, s1 = min(P.T, s0 + P.L), nb = (s1 - s0 + 127) / 128;
@@ -725,7 +725,7 @@ __global__ void __launch_bounds__(kDualThreads, 1)
             int s, c;
             dual_slot(blk, x, s, c);
             if (c > 0 && !(ok = mbar_wait(&bar[D_EMPTY + s], (c - 1) & 1, &abort_flag, P.status, detail))) break;
-            const CUtensorMap *m = x == 0 ? &mk : (x == 1 ? &mq : (x == 2 ? &mv : &mdo));
+            const CUtensorMap *m = x == 0 ? &mk : (x == 1 ? &mq : (x == 2 ? &mdo : &mv));
             uint8_t *dst = smem + s * kTileBytes;
             mbar_arrive_expect_tx(&bar[D_FULL + s], kTileBytes);
             tma_load_4d(m, &bar[D_FULL + s], dst, 0, t0, h, b, kPolicyEvictFirst);
@@ -735,106 +735,95 @@ __global__ void __launch_bounds__(kDualThreads, 1)
         }
       }
       volatile int no_abort = 0;
-      for (int s = 0; s < kSlots; ++s)
+      for (int s = 0; s < kDualSlots; ++s)
         if (loads[s] > 0) mbar_wait(&bar[D_FULL + s], (loads[s] - 1) & 1, &no_abort, P.status);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t id_kk = idesc_bf16(128, 128, false, false);  // A K-major, B K-major
-      const uint32_t id_km = idesc_bf16(128, 128, false, true);   // A K-major, B MN-major
+      const uint32_t id_km = idesc_bf16(128, 128, false, true);   // A K-major (or TMEM), B MN-major
       const uint32_t id_mm = idesc_bf16(128, 128, true, true);    // A MN-major, B MN-major
       int blk = 0;
       bool ok = true;
       auto wait = [&](int idx, int parity) {
         return mbar_wait(&bar[idx], parity & 1, &abort_flag, P.status, detail);
       };
+      auto full = [&](int x) {
+        int s, c;
+        dual_slot(blk, x, s, c);
+        return wait(D_FULL + s, c);
+      };
+      auto release = [&](int x) {
+        int s, c;
+        dual_slot(blk, x, s, c);
+        mma_commit(&bar[D_EMPTY + s]);
+      };
+      auto addr = [&](int x) {
+        int s, c;
+        dual_slot(blk, x, s, c);
+        return tile_addr(s);
+      };
       for (int item = blockIdx.x; item < P.nitems && ok; item += gridDim.x) {
         const int g = item / BH;
         const int s0 = g * P.L, s1 = min(P.T, s0 + P.L), nb = (s1 - s0 + 127) / 128;
         for (int n = 0; n < nb && ok; ++n, ++blk) {
-          int sk, ck, sq, cq;
-          dual_slot(blk, 0, sk, ck);
-          dual_slot(blk, 1, sq, cq);
-          const uint32_t K = tile_addr(sk), Q = tile_addr(sq), V = tile_addr(2), DO = tile_addr(3);
+          const uint32_t K = addr(0), Q = addr(1), DO = addr(2), V = addr(3);
           const int u1 = 2 * blk, u2 = u1 + 1;
-          // P1 = K Q^T
-          ok = wait(D_FULL + sk, ck) && wait(D_FULL + sq, cq) && (u1 == 0 || wait(D_PEMPTY, u1 - 1));
-          if (!ok) break;
+          // P1 = K Q^T  (the previous block's P2~ has been consumed: issue order)
+          if (!(ok = full(0) && full(1))) break;
           tc_fence_after();
 #pragma unroll
           for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tP, desc_kmajor(K, ks), desc_kmajor(Q, ks), id_kk, ks > 0);
           mma_commit(&bar[D_PFULL]);
-          // dv  = K' R   (R from the bf16 state tile, MN-major)
+          // dv = K' R   (R from the bf16 state tile, MN-major)
           ok = (!DECAY || wait(D_KSC, blk)) && wait(D_PRE, blk) && (blk == 0 || wait(D_O1EMPTY, blk - 1));
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
           for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tO1, desc_kmajor(K, ks), desc_mnmajor(sSh, ks), id_km, ks > 0);
-          mma_commit(&bar[D_EMPTY + sk]);
+          release(0);
           if (!DECAY) {
-            // dk  = V R^T  (the same tile, K-major)
-            ok = wait(D_FULL + 2, blk) && (blk == 0 || wait(D_O2EMPTY, blk - 1));
-            if (!ok) break;
-            tc_fence_after();
-#pragma unroll
-            for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tO2, desc_kmajor(V, ks), desc_kmajor(sSh, ks), id_kk, ks > 0);
-            // R += Q^T dO
-            if (!(ok = wait(D_FULL + 3, blk))) break;
+            // R += Q^T dO (the state tile is rewritten only after SFULL, below)
+            if (!(ok = full(2))) break;
             tc_fence_after();
 #pragma unroll
             for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tR, desc_mnmajor(Q, ks), desc_mnmajor(DO, ks), id_mm, 1u);
-            mma_commit(&bar[D_SFULL]);
-            // P2 = V dO^T once the masked P1 has left TMEM
-            ok = wait(D_PSFULL, u1) && wait(D_PEMPTY, u1);
-            if (!ok) break;
-            tc_fence_after();
-#pragma unroll
-            for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tP, desc_kmajor(V, ks), desc_kmajor(DO, ks), id_kk, ks > 0);
-            mma_commit(&bar[D_PFULL]);
-            mma_commit(&bar[D_EMPTY + 2]);
-            // dv += P1~ dO
-#pragma unroll
-            for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tO1, desc_kmajor(sPs, ks), desc_mnmajor(DO, ks), id_km, 1u);
-            mma_commit(&bar[D_PSEMPTY]);
-            mma_commit(&bar[D_O1FULL]);
-            mma_commit(&bar[D_EMPTY + 3]);
-          } else {
-            // P2 = V dO^T once the masked P1 has left TMEM
-            ok = wait(D_PSFULL, u1) && wait(D_PEMPTY, u1) && wait(D_FULL + 2, blk) && wait(D_FULL + 3, blk);
-            if (!ok) break;
-            tc_fence_after();
-#pragma unroll
-            for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tP, desc_kmajor(V, ks), desc_kmajor(DO, ks), id_kk, ks > 0);
-            mma_commit(&bar[D_PFULL]);
-            // dv += P1~ dO
-#pragma unroll
-            for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tO1, desc_kmajor(sPs, ks), desc_mnmajor(DO, ks), id_km, 1u);
-            mma_commit(&bar[D_PSEMPTY]);
-            mma_commit(&bar[D_O1FULL]);
-            // dk = V' R^T once V's rows are weighted
-            ok = wait(D_VSC, blk) && (blk == 0 || wait(D_O2EMPTY, blk - 1));
-            if (!ok) break;
-            tc_fence_after();
-#pragma unroll
-            for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tO2, desc_kmajor(V, ks), desc_kmajor(sSh, ks), id_kk, ks > 0);
-            mma_commit(&bar[D_EMPTY + 2]);
-            // R += Q^T dO' once dO's rows are weighted
-            if (!(ok = wait(D_DSC, blk))) break;
-            tc_fence_after();
-#pragma unroll
-            for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tR, desc_mnmajor(Q, ks), desc_mnmajor(DO, ks), id_mm, 1u);
-            mma_commit(&bar[D_SFULL]);
-            mma_commit(&bar[D_EMPTY + 3]);
           }
+          // dv += P1~ dO   (P1~ in TMEM as bf16 pairs)
+          if (!(ok = (DECAY ? full(2) : true) && wait(D_PSFULL, u1))) break;
+          tc_fence_after();
+#pragma unroll
+          for (uint32_t ks = 0; ks < 8; ++ks) mma_ts(tO1, tP + ks * 8, desc_mnmajor(DO, ks), id_km, 1u);
+          mma_commit(&bar[D_O1FULL]);
+          // P2 = V dO^T
+          if (!(ok = full(3))) break;
+          tc_fence_after();
+#pragma unroll
+          for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tP, desc_kmajor(V, ks), desc_kmajor(DO, ks), id_kk, ks > 0);
+          mma_commit(&bar[D_PFULL]);
+          if (!DECAY) release(2);
+          // dk = V' R^T  (the state tile read K-major)
+          ok = (!DECAY || wait(D_VSC, blk)) && (blk == 0 || wait(D_O2EMPTY, blk - 1));
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tO2, desc_kmajor(V, ks), desc_kmajor(sSh, ks), id_kk, ks > 0);
+          release(3);
+          if (DECAY) {
+            // R += Q^T dO'  (dO rows weighted together with V's)
+#pragma unroll
+            for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tR, desc_mnmajor(Q, ks), desc_mnmajor(DO, ks), id_mm, 1u);
+            release(2);
+          }
+          mma_commit(&bar[D_SFULL]);
           // dk += P2~ Q
           if (!(ok = wait(D_PSFULL, u2))) break;
           tc_fence_after();
 #pragma unroll
-          for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tO2, desc_kmajor(sPs, ks), desc_mnmajor(Q, ks), id_km, 1u);
-          mma_commit(&bar[D_PSEMPTY]);
+          for (uint32_t ks = 0; ks < 8; ++ks) mma_ts(tO2, tP + ks * 8, desc_mnmajor(Q, ks), id_km, 1u);
           mma_commit(&bar[D_O2FULL]);
-          mma_commit(&bar[D_EMPTY + sq]);
+          release(1);
         }
       }
     }
@@ -851,21 +840,23 @@ __global__ void __launch_bounds__(kDualThreads, 1)
       for (int n = 0; n < nb && ok; ++n, ++blk) {
         for (int half = 0; half < 2 && ok; ++half) {
           const int u = 2 * blk + half;
-          ok = __all_sync(0xffffffffu, mbar_wait(&bar[D_PFULL], u & 1, &abort_flag, P.status, detail)) &&
-               __all_sync(0xffffffffu,
-                          u == 0 || mbar_wait(&bar[D_PSEMPTY], (u - 1) & 1, &abort_flag, P.status, detail));
-          if (!ok) break;
+          if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar[D_PFULL], u & 1, &abort_flag, P.status, detail))))
+            break;
           tc_fence_after();
+          // chunk c's 32 scores become 16 columns of bf16 pairs at 16c: only
+          // columns already read are overwritten
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
             float x[32];
             ld_chunk(tP + lb + c * 32, x);
             mask_chunk<DECAY, true>(x, (int)row, c, lam, l2);
-            store_row_chunk_bf16(sPs, row, c, x);
+            uint32_t r[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) r[j] = pack_bf16(x[2 * j], x[2 * j + 1]);
+            tmem_st16(tP + lb + c * 16, r);
           }
+          tmem_st_wait();
           tc_fence_before();
-          mbar_arrive(&bar[D_PEMPTY]);
-          fence_proxy_async_smem();
           mbar_arrive(&bar[D_PSFULL]);
         }
       }
@@ -911,20 +902,20 @@ __global__ void __launch_bounds__(kDualThreads, 1)
           const int nv = nvalid(n), r = (int)row;
           const float wx = r < nv ? exp2f(l2 * (float)(nv - 1 - r)) : 0.f;  // rows of K and V
           const float wy = r < nv ? exp2f(l2 * (float)(r + 1)) : 0.f;       // rows of dO
-          int sk, ck;
-          dual_slot(blk, 0, sk, ck);
+          int sk, sdo, sv, c;
+          dual_slot(blk, 0, sk, c);
+          dual_slot(blk, 2, sdo, c);
+          dual_slot(blk, 3, sv, c);
+          // K after P1; V and dO after P2 (which follows dv += P1~ dO)
           if (!(ok = wait(D_PFULL, 2 * blk))) break;
           scale_tile_row(tile_addr(sk), row, wx);
           fence_proxy_async_smem();
           mbar_arrive(&bar[D_KSC]);
           if (!(ok = wait(D_PFULL, 2 * blk + 1))) break;
-          scale_tile_row(tile_addr(2), row, wx);
+          scale_tile_row(tile_addr(sv), row, wx);
+          scale_tile_row(tile_addr(sdo), row, wy);
           fence_proxy_async_smem();
           mbar_arrive(&bar[D_VSC]);
-          if (!(ok = wait(D_O1FULL, blk))) break;
-          scale_tile_row(tile_addr(3), row, wy);
-          fence_proxy_async_smem();
-          mbar_arrive(&bar[D_DSC]);
         }
         if (!(ok = wait(D_SFULL, blk))) break;
         tc_fence_after();
@@ -1038,11 +1029,11 @@ cudaError_t tc_dual(const Problem &p, int group_len, const void *q, const void *
   cudaError_t e;
   TimedLaunch t(K_TC_DUAL_REV, s);
   if (p.decay) {
-    if ((e = set_smem(tc_dual_kernel<true>, kMainSmem)) != cudaSuccess) return e;
-    tc_dual_kernel<true><<<grid, kDualThreads, kMainSmem, s>>>(mk, mq, mv, mdo, D);
+    if ((e = set_smem(tc_dual_kernel<true>, kDualSmem)) != cudaSuccess) return e;
+    tc_dual_kernel<true><<<grid, kDualThreads, kDualSmem, s>>>(mk, mq, mv, mdo, D);
   } else {
-    if ((e = set_smem(tc_dual_kernel<false>, kMainSmem)) != cudaSuccess) return e;
-    tc_dual_kernel<false><<<grid, kDualThreads, kMainSmem, s>>>(mk, mq, mv, mdo, D);
+    if ((e = set_smem(tc_dual_kernel<false>, kDualSmem)) != cudaSuccess) return e;
+    tc_dual_kernel<false><<<grid, kDualThreads, kDualSmem, s>>>(mk, mq, mv, mdo, D);
   }
   return cudaGetLastError();
 }

@@ -37,9 +37,9 @@ BYTES_FWD, BYTES_BWD = 1024, 1792
 # fused group aggregates of the dq pass it reads a fourth); the dual reverse-time
 # kernel reads four (k, q, dO, v) and writes two (dk, dv); the aggregate kernel
 # reads two.  Group states are overhead, not credited.
-KIND_BYTES_PER_TOKEN_HEAD = {"tc_chunked_fwd": 1024, "tc_chunked_rev": 1024, "tc_chunked_fwd_agg": 1280,
+KIND_BYTES_PER_TOKEN_HEAD = {"tc_chunked_fwd": 1024, "tc_chunked_fwd_agg": 1280,
                              "tc_dual_rev": 1536, "tc_segment_aggregate": 512}
-CHUNKED_KINDS = ("tc_chunked_fwd", "tc_chunked_rev", "tc_chunked_fwd_agg", "tc_dual_rev")
+CHUNKED_KINDS = ("tc_chunked_fwd", "tc_chunked_fwd_agg", "tc_dual_rev")
 
 
 def _dist():

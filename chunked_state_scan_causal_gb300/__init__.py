@@ -72,7 +72,7 @@ _SIGS = {
     "linattn_timing_collect": ([_i32, ctypes.POINTER(_i32), ctypes.POINTER(ctypes.c_float)], _i32),
     "linattn_kernel_name": ([_i32], ctypes.c_char_p),
 }
-KERNEL_KINDS = 11
+KERNEL_KINDS = 10
 
 
 def lib():

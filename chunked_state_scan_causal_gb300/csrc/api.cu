@@ -269,7 +269,7 @@ static int32_t fwd_impl(const linattn_shape *shape, const void *q, const void *k
   if (e == cudaSuccess)
     e = state_scan(w.G, (int)BH, p.d * p.d, nullptr, p.decay, p.H, w.L, false, agg, init_state, states, nullptr,
                    ws + w.scan, status, s);
-  if (e == cudaSuccess) e = tc_main(p, w.L, false, q, k, v, o, states, false, final_state, status, s);
+  if (e == cudaSuccess) e = tc_main(p, w.L, q, k, v, o, states, false, final_state, status, s);
   return cuda_status(e);
 }
 
@@ -335,9 +335,9 @@ static int32_t bwd_impl(const linattn_shape *shape, const void *q, const void *k
   // the end (the value one step before token 0 is d_init = sum_t lambda^{t+1}
   // q_t dO_t^T); without a decay the dq pass accumulates those aggregates too.
   if (!p.decay) {
-    if (e == cudaSuccess) e = tc_main(p, L, false, dO, v, k, dq, states, true, nullptr, status, s, q, wagg);
+    if (e == cudaSuccess) e = tc_main(p, L, dO, v, k, dq, states, true, nullptr, status, s, q, wagg);
   } else {
-    if (e == cudaSuccess) e = tc_main(p, L, false, dO, v, k, dq, states, true, nullptr, status, s);
+    if (e == cudaSuccess) e = tc_main(p, L, dO, v, k, dq, states, true, nullptr, status, s);
     if (e == cudaSuccess) e = tc_segment_states(p, L, q, dO, true, wagg, status, s);
   }
   if (e == cudaSuccess)
@@ -460,7 +460,7 @@ int32_t linattn_timing_collect(int32_t max_kinds, int32_t *launches, float *tota
 
 const char *linattn_kernel_name(int32_t kind) {
   static const char *names[K_KINDS] = {"simt_fwd", "simt_bwd", "simt_segment_states", "state_scan",
-                                       "tc_segment_aggregate", "tc_chunked_fwd", "tc_chunked_rev",
+                                       "tc_segment_aggregate", "tc_chunked_fwd",
                                        "diag_mma", "decode", "tc_dual_rev", "tc_chunked_fwd_agg"};
   return (kind >= 0 && kind < K_KINDS) ? names[kind] : "?";
 }

@@ -23,7 +23,7 @@ int device_ok();
 
 // ---------------------------------------------------------------- per-kernel timing (api.cu)
 enum KernelKind {
-  K_SIMT_FWD = 0, K_SIMT_BWD, K_SIMT_SEGMENT, K_SCAN, K_TC_AGG, K_TC_MAIN_FWD, K_TC_MAIN_REV, K_DIAG,
+  K_SIMT_FWD = 0, K_SIMT_BWD, K_SIMT_SEGMENT, K_SCAN, K_TC_AGG, K_TC_MAIN_FWD, K_DIAG,
   K_DECODE, K_TC_DUAL_REV, K_TC_MAIN_AGG, K_KINDS
 };
 // Records timing events around one launch on `s` while timing is enabled.
@@ -61,17 +61,15 @@ int tc_group_len(const Problem &p);    // tokens per chunk group (multiple of 12
 //   reverse == false: w_s = lambda^{end - s};  reverse == true: w_s = lambda^{s - start + 1}.
 cudaError_t tc_segment_states(const Problem &p, int seg_len, const void *X, const void *Y, bool reverse,
                               float *out, int *status, cudaStream_t s);
-// Per-group chunked attention from the given group states [G][BH][d][d] (read
-// transposed when init_transposed).  reverse == false: causal, state entering
-// the group, o_i += lambda^{i+1} S^T q_i.  reverse == true: anti-causal, blocks
-// walked from the end, state = sum_{s > group end} lambda^{s - end} k_s v_s^T.
-// final_state (optional, forward only) is the state after the last token.
-// x (optional; forward time without decay): also writes agg_out[g] =
-// sum_{s in group g} x_s q_s^T ([G][BH][d][d]) from the same pass.
-cudaError_t tc_main(const Problem &p, int group_len, bool reverse, const void *q, const void *k,
-                    const void *v, void *o, const float *group_init, bool init_transposed,
-                    float *final_state, int *status, cudaStream_t s, const void *x = nullptr,
-                    float *agg_out = nullptr);
+// Per-group causal chunked attention from the given group states
+// [G][BH][d][d] (read transposed when init_transposed): o_i = lambda^{i+1}
+// S^T q_i + intra-block terms, S the state entering the block.  final_state
+// (optional) is the state after the last token.  x (optional, no decay): also
+// writes agg_out[g] = sum_{s in group g} x_s q_s^T ([G][BH][d][d]) from the
+// same pass.
+cudaError_t tc_main(const Problem &p, int group_len, const void *q, const void *k, const void *v, void *o,
+                    const float *group_init, bool init_transposed, float *final_state, int *status,
+                    cudaStream_t s, const void *x = nullptr, float *agg_out = nullptr);
 
 // The backward's dv and dk in one reverse-time pass over (k, q, dO, v) from the
 // reverse group states [G][BH][d][d] (sum over later tokens u of

@@ -248,7 +248,7 @@ constexpr size_t kMainSmem = kOffBar + 256 + 1024;
 
 // barrier indices
 enum { B_FULL = 0, B_EMPTY = kSlots, B_PFULL = 2 * kSlots, B_PEMPTY, B_OFULL, B_OEMPTY, B_SFULL, B_PRE,
-       B_PSFULL, B_WEMPTY, B_COUNT };
+       B_PSFULL, B_WEMPTY, B_KSC, B_COUNT };
 
 // Decay mask of one 32-column chunk of a score row: keep j <= i (causal) or
 // j >= i (anti-causal) and weight by lambda^{|i-j|}; walks j so that the
@@ -286,17 +286,22 @@ __device__ __forceinline__ void mask_chunk(float (&x)[32], int i, int c, float l
   }
 }
 
-// AGG instances (forward time, no decay) also load a fourth tile x per block
-// and accumulate the group aggregate W = sum_s x_s q_s^T in the fourth TMEM
-// region, written per group to agg_out: for the dq launch (q := dO, x := q)
-// that is the reverse group aggregate sum_s q_s dO_s^T.  Tiles are loaded in
-// the order q, x, k, v and released in the same order.
-template <bool DECAY, bool REV, bool AGG = false>
+// With a decay the inter-block term goes to the fourth TMEM region from the
+// unweighted q (O_inter = Q S) and the epilogue adds lambda^{i+1} O_inter to
+// the intra-block term, so only the key rows are weighted in shared memory
+// (k_j *= lambda^{nv-1-j}, for the state update), and that off the path from
+// the scores to the inter-block product.
+// AGG instances (no decay) also load a fourth tile x per block and accumulate
+// the group aggregate W = sum_s x_s q_s^T in the fourth TMEM region, written
+// per group to agg_out: for the dq launch (q := dO, x := q) that is the
+// reverse group aggregate sum_s q_s dO_s^T.  Tiles are loaded in the order
+// q, x, k, v and released in the same order.
+template <bool DECAY, bool AGG = false>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_main_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                    const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mo,
                    const __grid_constant__ CUtensorMap mx, MainParams P) {
-  static_assert(!AGG || (!DECAY && !REV), "group aggregates are fused for the forward-time, decay-free kernel");
+  static_assert(!AGG || !DECAY, "group aggregates are fused for the decay-free kernel");
   constexpr int NT = AGG ? 4 : 3;  // tiles per block
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
@@ -321,6 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bar[B_PRE], 128);
     mbar_init(&bar[B_PSFULL], 128);
     mbar_init(&bar[B_WEMPTY], 128);
+    mbar_init(&bar[B_KSC], 128);
     fence_mbar_init();
     prefetch_tensormap(&mq);
     prefetch_tensormap(&mk);
@@ -336,7 +342,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
-  const uint32_t tS = tmem, tP = tmem + 128, tO = tmem + 256, tW = tmem + 384;
+  const uint32_t tS = tmem, tP = tmem + 128, tO = tmem + 256;
+  const uint32_t tW = tmem + 384, tOi = tmem + 384;  // AGG: aggregate; DECAY: inter-block term
   const uint32_t sbase = smem_u32(smem);
   const uint32_t sPs = sbase + kOffPs, sSh = sbase + kOffSh;
   auto slot_addr = [&](int t) { return sbase + (uint32_t)(t % kSlots) * kTileBytes; };
@@ -354,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int g = item / BH, bh = item % BH, b = bh / P.H, h = bh % P.H;
         const int s0 = g * P.L, s1 = min(P.T, s0 + P.L), nb = (s1 - s0 + 127) / 128;
         for (int n = 0; n < nb && ok; ++n, ++blk) {
-          const int t0 = s0 + 128 * (REV ? nb - 1 - n : n);
+          const int t0 = s0 + 128 * n;
           for (int x = 0; x < NT; ++x) {
             const int t = NT * blk + x, s = t % kSlots, u = t / kSlots;
             if (u > 0 && !(ok = mbar_wait(&bar[B_EMPTY + s], (u - 1) & 1, &abort_flag, P.status, detail))) break;
@@ -399,13 +406,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tP, desc_kmajor(Q, ks), desc_kmajor(K, ks), id_qk, ks > 0);
           mma_commit(&bar[B_PFULL]);
-          // inter-block term: O = Q' S   (Q' = decay-weighted rows)
+          // inter-block term: O = Q S (its own accumulator with a decay)
           ok = mbar_wait(&bar[B_PRE], blk & 1, &abort_flag, P.status, detail) &&
                (blk == 0 || mbar_wait(&bar[B_OEMPTY], (blk - 1) & 1, &abort_flag, P.status, detail));
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
-          for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tO, desc_kmajor(Q, ks), desc_mnmajor(sSh, ks), id_qs, ks > 0);
+          for (uint32_t ks = 0; ks < 8; ++ks)
+            mma_ss(DECAY ? tOi : tO, desc_kmajor(Q, ks), desc_mnmajor(sSh, ks), id_qs, ks > 0);
           if (AGG) {
             // group aggregate: W += X^T Q (the previous group's W must have been read out)
             ok = mbar_wait(&bar[B_FULL + tx % kSlots], (tx / kSlots) & 1, &abort_flag, P.status, detail) &&
@@ -419,8 +427,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mma_commit(&bar[B_EMPTY + tq % kSlots]);
           if (AGG) mma_commit(&bar[B_EMPTY + tx % kSlots]);
-          // state update: S += K'^T V
-          if (!(ok = mbar_wait(&bar[B_FULL + tv % kSlots], (tv / kSlots) & 1, &abort_flag, P.status, detail))) break;
+          // state update: S += K'^T V  (K' = decay-weighted key rows)
+          ok = (!DECAY || mbar_wait(&bar[B_KSC], blk & 1, &abort_flag, P.status, detail)) &&
+               mbar_wait(&bar[B_FULL + tv % kSlots], (tv / kSlots) & 1, &abort_flag, P.status, detail);
+          if (!ok) break;
           tc_fence_after();
 #pragma unroll
           for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tS, desc_mnmajor(K, ks), desc_mnmajor(V, ks), id_kv, 1u);
@@ -430,7 +440,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = mbar_wait(&bar[B_PSFULL], blk & 1, &abort_flag, P.status, detail))) break;
           tc_fence_after();
 #pragma unroll
-          for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tO, desc_kmajor(sPs, ks), desc_mnmajor(V, ks), id_qs, 1u);
+          for (uint32_t ks = 0; ks < 8; ++ks)
+            mma_ss(tO, desc_kmajor(sPs, ks), desc_mnmajor(V, ks), id_qs, (!DECAY || ks > 0) ? 1u : 0u);
           mma_commit(&bar[B_EMPTY + tv % kSlots]);
           mma_commit(&bar[B_OFULL]);
         }
@@ -448,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float lam = DECAY ? P.decay[h] : 1.f;
       const float l2 = DECAY ? log2f(lam) : 0.f;
       for (int n = 0; n < nb; ++n, ++blk) {
-        const int t0 = s0 + 128 * (REV ? nb - 1 - n : n);
+        const int t0 = s0 + 128 * n;
         ok = group_all(mbar_wait(&bar[B_PFULL], blk & 1, &abort_flag, P.status, detail), 2, 128);
         if (!ok) break;
         tc_fence_after();
@@ -459,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 4; ++c) {
           float x[32];
           ld_chunk(tP + lb + c * 32, x);
-          mask_chunk<DECAY, REV>(x, (int)row, c, lam, l2);
+          mask_chunk<DECAY, false>(x, (int)row, c, lam, l2);
           store_row_chunk_bf16(sPs, row, c, x);
         }
         tc_fence_before();
@@ -470,10 +481,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = group_all(mbar_wait(&bar[B_OFULL], blk & 1, &abort_flag, P.status, detail), 2, 128);
         if (!ok) break;
         tc_fence_after();
+        const float wq = DECAY ? exp2f(l2 * (float)(row + 1)) : 0.f;
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           float x[32];
           ld_chunk(tO + lb + c * 32, x);
+          if (DECAY) {
+            float y[32];
+            ld_chunk(tOi + lb + c * 32, y);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) x[j] = fmaf(wq, y[j], x[j]);
+          }
           store_row_chunk_bf16(sPs, row, c, x);
         }
         tc_fence_before();
@@ -498,25 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int s0 = g * P.L, s1 = min(P.T, s0 + P.L), nb = (s1 - s0 + 127) / 128;
       const float lam = DECAY ? P.decay[h] : 1.f;
       const float l2 = DECAY ? log2f(lam) : 0.f;
-      auto nvalid = [&](int n) {
-        const int t0 = s0 + 128 * (REV ? nb - 1 - n : n);
-        return min(128, s1 - t0);
-      };
-      // Decay weights of block `bb` (global block counter) with nv valid rows:
-      // forward q_i *= lambda^{i+1}, k_j *= lambda^{nv-1-j};
-      // reverse q_i *= lambda^{nv-1-i}, k_j *= lambda^{j+1}.
-      auto weigh = [&](int bb, int nv) -> bool {
-        if (!__all_sync(0xffffffffu, mbar_wait(&bar[B_PFULL], bb & 1, &abort_flag, P.status, detail))) return false;
-        const int r = (int)row;
-        float wq = 0.f, wk = 0.f;
-        if (r < nv) {
-          wq = exp2f(l2 * (float)(REV ? nv - 1 - r : r + 1));
-          wk = exp2f(l2 * (float)(REV ? r + 1 : nv - 1 - r));
-        }
-        scale_tile_row(slot_addr(tile_of(bb, 0)), row, wq);
-        scale_tile_row(slot_addr(tile_of(bb, 1)), row, wk);
-        return true;
-      };
+      auto nvalid = [&](int n) { return min(128, s1 - (s0 + 128 * n)); };
       // initial state of the group
       {
         const float *src = P.ginit + ((int64_t)g * BH + bh) * 16384;
@@ -541,12 +541,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st32(tS + lb + c * 32, r);
         }
         tmem_st_wait();
-        if (DECAY && !(ok = weigh(blk, nvalid(0)))) break;
         tc_fence_before();
         fence_proxy_async_smem();
         mbar_arrive(&bar[B_PRE]);
       }
       for (int n = 0; n < nb; ++n, ++blk) {
+        if (DECAY) {
+          // key rows k_j *= lambda^{nv-1-j} once the scores have read them
+          const int nv = nvalid(n), r = (int)row;
+          const float wk = r < nv ? exp2f(l2 * (float)(nv - 1 - r)) : 0.f;
+          if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_PFULL], blk & 1, &abort_flag, P.status, detail))))
+            break;
+          scale_tile_row(slot_addr(tile_of(blk, 1)), row, wk);
+          fence_proxy_async_smem();
+          mbar_arrive(&bar[B_KSC]);
+        }
         ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_SFULL], blk & 1, &abort_flag, P.status, detail));
         if (!ok) break;
         tc_fence_after();
@@ -566,7 +575,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           if (DECAY) tmem_st_wait();
-          if (DECAY && !(ok = weigh(blk + 1, nv))) break;
           tc_fence_before();
           fence_proxy_async_smem();
           mbar_arrive(&bar[B_PRE]);
@@ -583,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_before();
           mbar_arrive(&bar[B_WEMPTY]);
-        } else if (P.final_state && !REV && g == P.G - 1) {
+        } else if (P.final_state && g == P.G - 1) {
           float *dst = P.final_state + (int64_t)bh * 16384 + row * 128;
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
@@ -1038,10 +1046,10 @@ cudaError_t tc_dual(const Problem &p, int group_len, const void *q, const void *
   return cudaGetLastError();
 }
 
-cudaError_t tc_main(const Problem &p, int group_len, bool reverse, const void *q, const void *k,
-                    const void *v, void *o, const float *group_init, bool init_transposed,
-                    float *final_state, int *status, cudaStream_t s, const void *x, float *agg_out) {
-  if (x && (reverse || p.decay || !agg_out)) return cudaErrorInvalidValue;
+cudaError_t tc_main(const Problem &p, int group_len, const void *q, const void *k, const void *v, void *o,
+                    const float *group_init, bool init_transposed, float *final_state, int *status,
+                    cudaStream_t s, const void *x, float *agg_out) {
+  if (x && (p.decay || !agg_out)) return cudaErrorInvalidValue;
   alignas(64) CUtensorMap mq, mk, mv, mo, mx;
   if (!seq_tmap(p, q, &mq) || !seq_tmap(p, k, &mk) || !seq_tmap(p, v, &mv) || !seq_tmap(p, o, &mo) ||
       !seq_tmap(p, x ? x : q, &mx))
@@ -1055,19 +1063,18 @@ cudaError_t tc_main(const Problem &p, int group_len, bool reverse, const void *q
   M.agg_out = agg_out;
   const int grid = M.nitems < p.num_sms ? M.nitems : p.num_sms;
   cudaError_t e;
-  TimedLaunch t(x ? K_TC_MAIN_AGG : (reverse ? K_TC_MAIN_REV : K_TC_MAIN_FWD), s);
-#define LINATTN_LAUNCH_MAIN(DEC, REV, AGG)                                                     \
+  TimedLaunch t(x ? K_TC_MAIN_AGG : K_TC_MAIN_FWD, s);
+#define LINATTN_LAUNCH_MAIN(DEC, AGG)                                                          \
   do {                                                                                        \
-    if ((e = set_smem(tc_main_kernel<DEC, REV, AGG>, kMainSmem)) != cudaSuccess) return e;    \
-    tc_main_kernel<DEC, REV, AGG><<<grid, kThreads, kMainSmem, s>>>(mq, mk, mv, mo, mx, M);   \
+    if ((e = set_smem(tc_main_kernel<DEC, AGG>, kMainSmem)) != cudaSuccess) return e;         \
+    tc_main_kernel<DEC, AGG><<<grid, kThreads, kMainSmem, s>>>(mq, mk, mv, mo, mx, M);        \
   } while (0)
-  if (x) {
-    LINATTN_LAUNCH_MAIN(false, false, true);
-  } else if (p.decay) {
-    if (reverse) LINATTN_LAUNCH_MAIN(true, true, false); else LINATTN_LAUNCH_MAIN(true, false, false);
-  } else {
-    if (reverse) LINATTN_LAUNCH_MAIN(false, true, false); else LINATTN_LAUNCH_MAIN(false, false, false);
-  }
+  if (x)
+    LINATTN_LAUNCH_MAIN(false, true);
+  else if (p.decay)
+    LINATTN_LAUNCH_MAIN(true, false);
+  else
+    LINATTN_LAUNCH_MAIN(false, false);
 #undef LINATTN_LAUNCH_MAIN
   return cudaGetLastError();
 }

@@ -20,6 +20,7 @@ from .oracle import (  # noqa: F401
     fwd_quadratic,
     bwd_quadratic,
     segment_states,
+    segment_grad_states,
     state_scan,
     threads_used,
 )

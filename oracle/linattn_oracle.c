@@ -93,8 +93,8 @@ void oracle_fwd_recurrent(i64 BH, i64 T, i64 dk, i64 dv, const double *lam,
 /* ---------------------------------------------------------------------- */
 void oracle_bwd_recurrent(i64 BH, i64 T, i64 dk, i64 dv, const double *lam,
                           const double *q, const double *k, const double *v,
-                          const double *dO, const double *init, double *dq,
-                          double *dkk, double *dvv, double *d_init) {
+                          const double *dO, const double *init, const double *d_final,
+                          double *dq, double *dkk, double *dvv, double *d_init) {
 #pragma omp parallel for schedule(dynamic, 1)
   for (i64 bh = 0; bh < BH; ++bh) {
     double *S = calloc((size_t)(dk * dv), sizeof(double));
@@ -114,8 +114,12 @@ void oracle_bwd_recurrent(i64 BH, i64 T, i64 dk, i64 dv, const double *lam,
         dqt[a] = acc;
       }
     }
+    /* R_t = dL/dS_t = q_t dO_t^T + lambda R_{t+1}, where the term after the
+     * last token is the gradient arriving at the final state (d_final, the
+     * state the next segment starts from), or 0. */
     double *R = S; /* reuse the buffer */
-    memset(R, 0, sizeof(double) * dk * dv);
+    if (d_final) memcpy(R, d_final + bh * dk * dv, sizeof(double) * dk * dv);
+    else memset(R, 0, sizeof(double) * dk * dv);
     for (i64 t = T - 1; t >= 0; --t) {
       const double *qt = q + (bh * T + t) * dk;
       const double *kt = k + (bh * T + t) * dk;
@@ -123,9 +127,10 @@ void oracle_bwd_recurrent(i64 BH, i64 T, i64 dk, i64 dv, const double *lam,
       const double *gt = dO + (bh * T + t) * dv;
       double *dkt = dkk + (bh * T + t) * dk;
       double *dvt = dvv + (bh * T + t) * dv;
+      const double carry = (t == T - 1) ? 1.0 : l; /* d_final enters undecayed at t = T-1 */
       for (i64 a = 0; a < dk; ++a)
         for (i64 b = 0; b < dv; ++b)
-          R[a * dv + b] = l * R[a * dv + b] + qt[a] * gt[b];
+          R[a * dv + b] = carry * R[a * dv + b] + qt[a] * gt[b];
       for (i64 a = 0; a < dk; ++a) {
         double acc = 0.0;
         for (i64 b = 0; b < dv; ++b) acc += R[a * dv + b] * vt[b];
@@ -137,8 +142,9 @@ void oracle_bwd_recurrent(i64 BH, i64 T, i64 dk, i64 dv, const double *lam,
         dvt[b] = acc;
       }
     }
+    /* dL/d(init) = lambda R_0; with no tokens the initial state is the final one */
     if (d_init)
-      for (i64 i = 0; i < dk * dv; ++i) d_init[bh * dk * dv + i] = l * R[i];
+      for (i64 i = 0; i < dk * dv; ++i) d_init[bh * dk * dv + i] = (T > 0 ? l : 1.0) * R[i];
     free(S);
   }
 }
@@ -328,6 +334,34 @@ void oracle_segment_states(i64 BH, i64 T, i64 dk, i64 dv, const double *lam, i64
         const double *vs = v + (bh * T + s0 + s) * dv;
         for (i64 a = 0; a < dk; ++a)
           for (i64 b = 0; b < dv; ++b) U[a * dv + b] = l * U[a * dv + b] + ks[a] * vs[b];
+      }
+    }
+  }
+}
+
+/* ---------------------------------------------------------------------- */
+/* Segment-local gradient states for the backward of a split sequence:     */
+/*   W_g = sum_{s in segment g} lambda^{s - start_g + 1} q_s dO_s^T,         */
+/* what segment g adds to the gradient arriving at the final state of the   */
+/* segment before it (the reverse counterpart of the All-Scan input).       */
+/* Horner order from the segment end: W <- lambda (W + q_s dO_s^T).         */
+/* ---------------------------------------------------------------------- */
+void oracle_segment_grad_states(i64 BH, i64 T, i64 dk, i64 dv, const double *lam, i64 L,
+                                const double *q, const double *dO, double *out) {
+  const i64 G = (T + L - 1) / L;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (i64 bh = 0; bh < BH; ++bh) {
+    const double l = lam_of(lam, bh);
+    for (i64 g = 0; g < G; ++g) {
+      double *W = out + (g * BH + bh) * dk * dv;
+      memset(W, 0, sizeof(double) * dk * dv);
+      const i64 s0 = g * L;
+      const i64 n = (T - s0) < L ? (T - s0) : L;
+      for (i64 s = n - 1; s >= 0; --s) {
+        const double *qs = q + (bh * T + s0 + s) * dk;
+        const double *gs = dO + (bh * T + s0 + s) * dv;
+        for (i64 a = 0; a < dk; ++a)
+          for (i64 b = 0; b < dv; ++b) W[a * dv + b] = l * (W[a * dv + b] + qs[a] * gs[b]);
       }
     }
   }

@@ -48,13 +48,15 @@ def _load():
             dp = ctypes.POINTER(ctypes.c_double)
             i64 = ctypes.c_int64
             lib.oracle_fwd_recurrent.argtypes = [i64, i64, i64, i64, dp, dp, dp, dp, dp, i64, dp, dp, dp]
-            lib.oracle_bwd_recurrent.argtypes = [i64, i64, i64, i64, dp, dp, dp, dp, dp, dp, dp, dp, dp, dp]
+            lib.oracle_bwd_recurrent.argtypes = [i64, i64, i64, i64, dp, dp, dp, dp, dp, dp, dp, dp, dp, dp, dp]
             lib.oracle_fwd_chunked.argtypes = [i64, i64, i64, i64, dp, i64, dp, dp, dp, dp, dp, dp, dp]
             lib.oracle_bwd_chunked.argtypes = [i64, i64, i64, i64, dp, i64, dp, dp, dp, dp, dp, dp, dp, dp, dp]
             lib.oracle_segment_states.argtypes = [i64, i64, i64, i64, dp, i64, dp, dp, dp]
+            lib.oracle_segment_grad_states.argtypes = [i64, i64, i64, i64, dp, i64, dp, dp, dp]
             lib.oracle_state_scan.argtypes = [i64, i64, i64, i64, dp, dp, dp, dp, dp]
             for f in ("oracle_fwd_recurrent", "oracle_bwd_recurrent", "oracle_fwd_chunked",
-                      "oracle_bwd_chunked", "oracle_segment_states", "oracle_state_scan"):
+                      "oracle_bwd_chunked", "oracle_segment_states", "oracle_segment_grad_states",
+                      "oracle_state_scan"):
                 getattr(lib, f).restype = None
             _lib = lib
     return _lib
@@ -115,15 +117,19 @@ def fwd_recurrent(q, k, v, lam=None, init=None, chunk=0):
     return o, cs, fin
 
 
-def bwd_recurrent(q, k, v, dO, lam=None, init=None):
-    """Returns (dq, dk, dv, d_init)."""
-    q, k, v, dO, init = _f64(q), _f64(k), _f64(v), _f64(dO), _f64(init)
+def bwd_recurrent(q, k, v, dO, lam=None, init=None, d_final=None):
+    """Returns (dq, dk, dv, d_init).
+
+    ``d_final`` [B, H, dk, dv] is the gradient arriving at the state after the
+    last token (from whatever continues the sequence), or None for zero.
+    """
+    q, k, v, dO, init, d_final = _f64(q), _f64(k), _f64(v), _f64(dO), _f64(init), _f64(d_final)
     B, H, T, dk, dv = _dims(q, k, v)
     dq, dkk, dvv = np.empty_like(q), np.empty_like(k), np.empty_like(v)
     dinit = np.empty((B, H, dk, dv))
     lam_bh = _lam_bh(lam, B, H)
     _load().oracle_bwd_recurrent(B * H, T, dk, dv, _ptr(lam_bh), _ptr(q), _ptr(k), _ptr(v), _ptr(dO),
-                                 _ptr(init), _ptr(dq), _ptr(dkk), _ptr(dvv), _ptr(dinit))
+                                 _ptr(init), _ptr(d_final), _ptr(dq), _ptr(dkk), _ptr(dvv), _ptr(dinit))
     return dq, dkk, dvv, dinit
 
 
@@ -164,6 +170,18 @@ def segment_states(k, v, seg_len, lam=None):
     out = np.empty((G, B, H, dk, dv))
     lam_bh = _lam_bh(lam, B, H)
     _load().oracle_segment_states(B * H, T, dk, dv, _ptr(lam_bh), seg_len, _ptr(k), _ptr(v), _ptr(out))
+    return out
+
+
+def segment_grad_states(q, dO, seg_len, lam=None):
+    """W[g, b, h] = sum over segment g of lambda^{s - start_g + 1} q_s dO_s^T; shape [G, B, H, dk, dv]."""
+    q, dO = _f64(q), _f64(dO)
+    B, H, T, dk = q.shape
+    dv = dO.shape[-1]
+    G = (T + seg_len - 1) // seg_len
+    out = np.empty((G, B, H, dk, dv))
+    lam_bh = _lam_bh(lam, B, H)
+    _load().oracle_segment_grad_states(B * H, T, dk, dv, _ptr(lam_bh), seg_len, _ptr(q), _ptr(dO), _ptr(out))
     return out
 
 

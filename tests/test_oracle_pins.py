@@ -164,6 +164,104 @@ def test_backward_central_finite_differences():
             assert abs(num - grads[which][idx]) < 1e-6 * max(1.0, abs(num)), (which, idx)
 
 
+def _torch_final_state(k, v, init, lam):
+    """S_{T-1} = lambda^T init + sum_s lambda^{T-1-s} k_s v_s^T, written out per token."""
+    T = k.shape[2]
+    lam_t = lam.view(1, -1, 1, 1)
+    w = lam_t[..., 0] ** (T - 1 - torch.arange(T, dtype=torch.float64))      # [1, H, T]
+    return torch.einsum("bht,bhta,bhtc->bhac", w.expand(k.shape[0], -1, -1), k, v) + (lam_t ** T) * init
+
+
+@pytest.mark.parametrize("lam", [1.0, 0.5, 0.96875])
+def test_backward_with_final_state_gradient_matches_autograd(lam):
+    """A gradient D arriving at the final state (from a later segment) adds <D, S_final>
+    to the loss: the recurrent backward with d_final equals torch fp64 autograd of it."""
+    B, H, T, dk, dv = 1, 2, 37, 4, 6
+    q, k, v, dO = _rand(21, B, H, T, dk, dv)
+    r = np.random.default_rng(22)
+    init, D = r.standard_normal((B, H, dk, dv)), r.standard_normal((B, H, dk, dv))
+    lam_h = np.array([lam, lam ** 0.25])
+    tq, tk, tv, ti = (torch.tensor(a, requires_grad=True) for a in (q, k, v, init))
+    lt = torch.tensor(lam_h)
+    loss = _torch_quadratic_loss(tq, tk, tv, ti, lt, torch.tensor(dO)) + \
+        (_torch_final_state(tk, tv, ti, lt) * torch.tensor(D)).sum()
+    loss.backward()
+    ref = [x.grad.numpy() for x in (tq, tk, tv, ti)]
+    got = oracle.bwd_recurrent(q, k, v, dO, lam=lam_h, init=init, d_final=D)
+    for g, e in zip(got, ref):
+        np.testing.assert_allclose(g, e, rtol=1e-10, atol=1e-10)
+    # the final state of the forward is the one the torch expression differentiates
+    _, _, fin = oracle.fwd_recurrent(q, k, v, lam=lam_h, init=init)
+    np.testing.assert_allclose(fin, _torch_final_state(*(torch.tensor(a) for a in (k, v, init)), lt).numpy(),
+                               rtol=1e-12, atol=1e-12)
+
+
+def test_final_state_gradient_finite_differences():
+    """d<S_final, D>/dx by central differences matches the backward with d_final (dO = 0)."""
+    B, H, T, dk, dv = 1, 1, 15, 3, 4
+    q, k, v, _ = _rand(31, B, H, T, dk, dv)
+    r = np.random.default_rng(32)
+    init, D = r.standard_normal((B, H, dk, dv)), r.standard_normal((B, H, dk, dv))
+    lam = np.array([0.85])
+    grads = oracle.bwd_recurrent(q, k, v, np.zeros_like(v), lam=lam, init=init, d_final=D)
+    assert np.abs(grads[0]).max() == 0.0                      # q does not reach the state
+    args, h = [q, k, v, init], 1e-6
+    for which in (1, 2, 3):
+        for _ in range(4):
+            idx = tuple(r.integers(0, n) for n in args[which].shape)
+            up, dn = [a.copy() for a in args], [a.copy() for a in args]
+            up[which][idx] += h
+            dn[which][idx] -= h
+            fu = np.sum(oracle.fwd_recurrent(*up[:3], lam=lam, init=up[3])[2] * D)
+            fd = np.sum(oracle.fwd_recurrent(*dn[:3], lam=lam, init=dn[3])[2] * D)
+            num = (fu - fd) / (2 * h)
+            assert abs(num - grads[which][idx]) < 1e-6 * max(1.0, abs(num)), (which, idx)
+
+
+def test_empty_sequence_passes_final_gradient_to_init():
+    """With no tokens the initial state is the final state: d_init == d_final."""
+    D = np.random.default_rng(41).standard_normal((1, 2, 3, 4))
+    z = np.zeros((1, 2, 0, 3))
+    _, _, _, dinit = oracle.bwd_recurrent(z, z, np.zeros((1, 2, 0, 4)), np.zeros((1, 2, 0, 4)),
+                                          lam=np.array([0.7, 0.9]), d_final=D)
+    np.testing.assert_array_equal(dinit, D)
+
+
+@pytest.mark.parametrize("lam", [None, 0.9])
+def test_segment_grad_states_one_segment_is_d_init(lam):
+    """Over one segment, sum_s lambda^{s+1} q_s dO_s^T is the pinned d_init of the backward."""
+    B, H, T, dk, dv = 2, 2, 29, 3, 5
+    q, k, v, dO = _rand(51, B, H, T, dk, dv)
+    lam_h = None if lam is None else np.array([lam, lam ** 0.5])
+    W = oracle.segment_grad_states(q, dO, T, lam=lam_h)
+    _, _, _, dinit = oracle.bwd_recurrent(q, k, v, dO, lam=lam_h)
+    np.testing.assert_allclose(W[0], dinit, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("lam", [None, 0.93])
+def test_split_sequence_backward_equals_whole(lam):
+    """Sequence split into N equal segments (ranks): each starts from the forward scan of
+    the segment states and receives d_final from the reverse scan of the segment gradient
+    states; the concatenated gradients equal the whole-sequence backward."""
+    B, H, N, L, dk, dv = 1, 2, 4, 11, 3, 4
+    T = N * L
+    q, k, v, dO = _rand(61, B, H, T, dk, dv)
+    init = np.random.default_rng(62).standard_normal((B, H, dk, dv))
+    lam_h = np.ones(H) if lam is None else np.array([lam, lam ** 0.5])
+    a = lam_h[None, :] ** L                                      # per-segment multiplier, [B, H]
+    U = oracle.segment_states(k, v, L, lam=lam_h)                # [N, B, H, dk, dv]
+    S_in, _ = oracle.state_scan(U, seg_decay=a, init=init)
+    W = oracle.segment_grad_states(q, dO, L, lam=lam_h)
+    Dr, _ = oracle.state_scan(W[::-1], seg_decay=a)              # reverse exclusive scan
+    D_fin = Dr[::-1]
+    ref = oracle.bwd_recurrent(q, k, v, dO, lam=lam_h, init=init)
+    parts = [oracle.bwd_recurrent(*(x[:, :, r * L:(r + 1) * L] for x in (q, k, v, dO)), lam=lam_h,
+                                  init=S_in[r], d_final=D_fin[r]) for r in range(N)]
+    for i in range(3):
+        np.testing.assert_allclose(np.concatenate([p[i] for p in parts], axis=2), ref[i], rtol=1e-10, atol=1e-10)
+    np.testing.assert_allclose(parts[0][3], ref[3], rtol=1e-10, atol=1e-10)
+
+
 # ------------------------------------------------------------------ chunked == recurrent == quadratic
 @pytest.mark.parametrize("lam", [None, 0.5, 0.96875])
 def test_chunked_equals_recurrent_every_chunk_length(lam):

@@ -170,17 +170,30 @@ def run_reference(args):
     lam = inputs.workload_decay(cfg)
     lam_s = None if lam is None else lam[heads]
     x = {w: np.stack([inputs.make_head64(cfg, w, 0, h) for h in heads])[None] for w in ("q", "k", "v", "dO")}
+
+    def run(n):
+        oracle.fwd_recurrent(x["q"][:, :, :n], x["k"][:, :, :n], x["v"][:, :, :n], lam=lam_s)
+        oracle.bwd_recurrent(x["q"][:, :, :n], x["k"][:, :, :n], x["v"][:, :, :n], x["dO"][:, :, :n], lam=lam_s)
+
+    # each step is the first T_s tokens of every sampled head, T_s sized so that the
+    # whole run (warm-up + timed steps) takes about --ref-budget seconds
+    n_cal = min(T, 2048)
+    t0 = time.perf_counter()
+    run(n_cal)
+    per_token = (time.perf_counter() - t0) / n_cal
+    T_s = int(args.ref_budget / (args.warmup + args.steps) / per_token) // 64 * 64
+    T_s = max(64, min(T, T_s))
     times = []
     for i in range(args.warmup + args.steps):
         t0 = time.perf_counter()
-        oracle.fwd_recurrent(x["q"], x["k"], x["v"], lam=lam_s)
-        oracle.bwd_recurrent(x["q"], x["k"], x["v"], x["dO"], lam=lam_s)
+        run(T_s)
         if i >= args.warmup:
             times.append(time.perf_counter() - t0)
     sec = sum(times) / len(times)
-    tokens = T * len(heads) / cfg["H"]  # token equivalents of the full-head workload
+    tokens = T_s * len(heads) / cfg["H"]  # token equivalents of the full-head workload
     value = tokens / sec
-    sample = f"batch row 0, heads 0..{len(heads) - 1} of {cfg['H']}, T={T}: fwd+bwd fp64 recurrence"
+    sample = (f"batch row 0, heads 0..{len(heads) - 1} of {cfg['H']}, first {T_s} of T={T} tokens: "
+              f"fwd+bwd fp64 recurrence")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
@@ -393,11 +406,12 @@ def run_ours(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=3)
-    ap.add_argument("--ref-heads", type=int, default=4, help="heads per step of the reference arm")
+    ap.add_argument("--ref-heads", type=int, default=16, help="heads per step of the reference arm")
+    ap.add_argument("--ref-budget", type=float, default=120.0, help="seconds for the whole reference arm")
     ap.add_argument("--cpu-heads", type=int, default=16, help="heads of the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")

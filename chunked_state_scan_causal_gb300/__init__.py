@@ -29,7 +29,7 @@ ERR_SCRATCH_LIMIT = -8
 NOALLOC_MAX_TILES = 65536
 BF16, F32 = 0, 1
 OP_FWD, OP_BWD, OP_CHUNK_STATES, OP_CHECKPOINT = 1, 2, 3, 4
-ABI_VERSION = 1
+ABI_VERSION = 2
 
 
 class LinattnError(RuntimeError):
@@ -57,11 +57,12 @@ _SIGS = {
     "linattn_status_string": ([_i32], ctypes.c_char_p),
     "linattn_workspace_size": ([ctypes.POINTER(Shape), _i32, _i32, ctypes.POINTER(_sz)], _i32),
     "linattn_fwd": ([ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
-    "linattn_bwd": ([ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
+    "linattn_bwd": ([ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "linattn_fwd_ckpt": ([ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _sz, _vp], _i32),
-    "linattn_bwd_ckpt": ([ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _vp, _vp, _vp, _vp, _sz,
-                          _vp], _i32),
+    "linattn_bwd_ckpt": ([ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _vp, _vp, _vp, _vp,
+                          _sz, _vp], _i32),
     "linattn_chunk_states": ([ctypes.POINTER(Shape), _i32, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
+    "linattn_chunk_states_rev": ([ctypes.POINTER(Shape), _i32, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "linattn_decode": ([ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp], _i32),
     "linattn_state_scan_workspace_size": ([_i32, _i32, _i32, _i32, ctypes.POINTER(_sz)], _i32),
     "linattn_state_scan": ([_i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
@@ -119,8 +120,8 @@ def linattn_fwd(shape, q, k, v, o, init_state, final_state, chunk_states, ws, ws
                              ws, ws_bytes, stream)
 
 
-def linattn_bwd(shape, q, k, v, dO, init_state, dq, dk, dv, d_init, ws, ws_bytes, stream) -> int:
-    return lib().linattn_bwd(ctypes.byref(shape), q, k, v, dO, init_state, dq, dk, dv, d_init,
+def linattn_bwd(shape, q, k, v, dO, init_state, d_final, dq, dk, dv, d_init, ws, ws_bytes, stream) -> int:
+    return lib().linattn_bwd(ctypes.byref(shape), q, k, v, dO, init_state, d_final, dq, dk, dv, d_init,
                              ws, ws_bytes, stream)
 
 
@@ -133,14 +134,18 @@ def linattn_fwd_ckpt(shape, q, k, v, o, init_state, final_state, ckpt, ckpt_byte
                                   ws, ws_bytes, stream)
 
 
-def linattn_bwd_ckpt(shape, q, k, v, dO, init_state, ckpt, ckpt_bytes, dq, dk, dv, d_init, ws, ws_bytes,
+def linattn_bwd_ckpt(shape, q, k, v, dO, init_state, d_final, ckpt, ckpt_bytes, dq, dk, dv, d_init, ws, ws_bytes,
                      stream) -> int:
-    return lib().linattn_bwd_ckpt(ctypes.byref(shape), q, k, v, dO, init_state, ckpt, ckpt_bytes, dq, dk, dv, d_init,
-                                  ws, ws_bytes, stream)
+    return lib().linattn_bwd_ckpt(ctypes.byref(shape), q, k, v, dO, init_state, d_final, ckpt, ckpt_bytes, dq, dk,
+                                  dv, d_init, ws, ws_bytes, stream)
 
 
 def linattn_chunk_states(shape, seg_len, k, v, out, ws, ws_bytes, stream) -> int:
     return lib().linattn_chunk_states(ctypes.byref(shape), seg_len, k, v, out, ws, ws_bytes, stream)
+
+
+def linattn_chunk_states_rev(shape, seg_len, q, dO, out, ws, ws_bytes, stream) -> int:
+    return lib().linattn_chunk_states_rev(ctypes.byref(shape), seg_len, q, dO, out, ws, ws_bytes, stream)
 
 
 def linattn_state_scan_workspace_size(G, BH, dk, dv) -> tuple[int, int]:
@@ -267,8 +272,11 @@ def fwd(q, k, v, decay=None, init_state=None, want_final=False, want_chunk_state
     return o, fin, cs
 
 
-def bwd(q, k, v, dO, decay=None, init_state=None, want_dinit=False, outs=None, ws=None, stream=None, ckpt=None):
-    """(dq, dk, dv, d_init or None) for the upstream gradient dO (forward states from ``ckpt`` if given)."""
+def bwd(q, k, v, dO, decay=None, init_state=None, want_dinit=False, outs=None, ws=None, stream=None, ckpt=None,
+        d_final=None):
+    """(dq, dk, dv, d_init or None) for the upstream gradient dO (forward states from ``ckpt`` if given).
+
+    ``d_final`` [B, H, d, d] fp32: gradient arriving at the final state (None: zero)."""
     import torch
     _same_layout(q, k, v, dO)
     B, H, T, d = q.shape
@@ -280,12 +288,13 @@ def bwd(q, k, v, dO, decay=None, init_state=None, want_dinit=False, outs=None, w
     if ws is None:
         ws = workspace(q, OP_BWD, decay)
     if ckpt is not None:
-        st = linattn_bwd_ckpt(shape, _ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(init_state), _ptr(ckpt), ckpt.numel(),
+        st = linattn_bwd_ckpt(shape, _ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(init_state), _ptr(d_final),
+                              _ptr(ckpt), ckpt.numel(),
                               _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dinit), _ptr(ws), ws.numel(),
                               _stream(q.device, stream))
         _check(st, "linattn_bwd_ckpt")
         return dq, dk, dv, dinit
-    st = linattn_bwd(shape, _ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(init_state), _ptr(dq), _ptr(dk),
+    st = linattn_bwd(shape, _ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(init_state), _ptr(d_final), _ptr(dq), _ptr(dk),
                      _ptr(dv), _ptr(dinit), _ptr(ws), ws.numel(), _stream(q.device, stream))
     _check(st, "linattn_bwd")
     return dq, dk, dv, dinit
@@ -316,6 +325,21 @@ def chunk_states(k, v, seg_len: int, decay=None, out=None, ws=None, stream=None)
     st = linattn_chunk_states(shape_of(k, decay), seg_len, _ptr(k), _ptr(v), _ptr(out), _ptr(ws), ws.numel(),
                               _stream(k.device, stream))
     _check(st, "linattn_chunk_states")
+    return out
+
+
+def chunk_states_rev(q, dO, seg_len: int, decay=None, out=None, ws=None, stream=None):
+    """Segment-local gradient states [G, B, H, d, d] (fp32): sum_s lambda^{s - start + 1} q_s dO_s^T."""
+    import torch
+    _same_layout(q, dO)
+    B, H, T, d = q.shape
+    G = T // seg_len if seg_len > 0 else 0
+    out = out if out is not None else torch.empty((G, B, H, d, d), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = workspace(q, OP_CHUNK_STATES, decay, seg_len)
+    st = linattn_chunk_states_rev(shape_of(q, decay), seg_len, _ptr(q), _ptr(dO), _ptr(out), _ptr(ws), ws.numel(),
+                                  _stream(q.device, stream))
+    _check(st, "linattn_chunk_states_rev")
     return out
 
 

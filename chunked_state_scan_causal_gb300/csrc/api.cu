@@ -288,14 +288,14 @@ int32_t linattn_fwd_ckpt(const linattn_shape *shape, const void *q, const void *
 }
 
 static int32_t bwd_impl(const linattn_shape *shape, const void *q, const void *k, const void *v,
-                        const void *dO, const float *init_state, const float *ckpt, size_t ckpt_size,
-                        bool use_ckpt, void *dq, void *dk, void *dv, float *d_init_state, void *workspace,
-                        size_t workspace_bytes, void *stream) {
+                        const void *dO, const float *init_state, const float *d_final, const float *ckpt,
+                        size_t ckpt_size, bool use_ckpt, void *dq, void *dk, void *dv, float *d_init_state,
+                        void *workspace, size_t workspace_bytes, void *stream) {
   Problem p;
   int st = validate(shape, &p);
   if (st) return st;
   if (p.T > 0 && (st = check_ptrs({q, k, v, dO, dq, dk, dv}, {}))) return st;
-  if ((st = check_ptrs({}, {init_state, d_init_state}))) return st;
+  if ((st = check_ptrs({}, {init_state, d_final, d_init_state}))) return st;
   const BwdLayout w = bwd_layout(p);
   if ((st = check_ws(workspace, workspace_bytes, w.total))) return st;
   const size_t need_ckpt = use_ckpt ? ckpt_bytes(p) : 0;
@@ -309,11 +309,14 @@ static int32_t bwd_impl(const linattn_shape *shape, const void *q, const void *k
   const int64_t BH = (int64_t)p.B * p.H;
   const size_t state_bytes = (size_t)BH * p.d * p.d * sizeof(float);
   if (p.T == 0) {
-    if (d_init_state) return cuda_status(cudaMemsetAsync(d_init_state, 0, state_bytes, s));
+    // no tokens: the initial state is the final one
+    if (d_init_state)
+      return cuda_status(d_final ? cudaMemcpyAsync(d_init_state, d_final, state_bytes, cudaMemcpyDeviceToDevice, s)
+                                 : cudaMemsetAsync(d_init_state, 0, state_bytes, s));
     return LINATTN_OK;
   }
   if (!tc_supported(p))
-    return cuda_status(simt_bwd(p, q, k, v, dO, init_state, dq, dk, dv, d_init_state, s));
+    return cuda_status(simt_bwd(p, q, k, v, dO, init_state, d_final, dq, dk, dv, d_init_state, s));
   const int L = w.f.L, G = w.f.G;
   float *agg = reinterpret_cast<float *>(ws + w.f.agg);
   float *wagg = reinterpret_cast<float *>(ws + w.wagg);
@@ -340,27 +343,36 @@ static int32_t bwd_impl(const linattn_shape *shape, const void *q, const void *k
     if (e == cudaSuccess) e = tc_main(p, L, dO, v, k, dq, states, true, nullptr, status, s);
     if (e == cudaSuccess) e = tc_segment_states(p, L, q, dO, true, wagg, status, s);
   }
+  // A gradient D arriving at the final state enters the reverse scan across the
+  // last group, whose length may be short of L: fold lambda^{len} D into that
+  // group's aggregate, scan from zero, and give the last group D itself.
+  const int64_t E = BH * p.d * p.d;
+  if (e == cudaSuccess && d_final)
+    e = fold_state(wagg + (int64_t)(G - 1) * E, d_final, p.decay, p.H, p.d * p.d, p.T - (G - 1) * L, E, s);
   if (e == cudaSuccess)
     e = state_scan(G, (int)BH, p.d * p.d, nullptr, p.decay, p.H, L, true, wagg, nullptr, rbar, d_init_state,
                    ws + w.f.scan, status, s);
+  if (e == cudaSuccess && d_final)
+    e = cudaMemcpyAsync(rbar + (int64_t)(G - 1) * E, d_final, state_bytes, cudaMemcpyDeviceToDevice, s);
   // dv and dk in one reverse-time pass from the states Rbar
   if (e == cudaSuccess) e = tc_dual(p, L, q, k, v, dO, dk, dv, rbar, status, s);
   return cuda_status(e);
 }
 
 int32_t linattn_bwd(const linattn_shape *shape, const void *q, const void *k, const void *v,
-                    const void *dO, const float *init_state, void *dq, void *dk, void *dv,
-                    float *d_init_state, void *workspace, size_t workspace_bytes, void *stream) {
-  return bwd_impl(shape, q, k, v, dO, init_state, nullptr, 0, false, dq, dk, dv, d_init_state, workspace,
-                  workspace_bytes, stream);
+                    const void *dO, const float *init_state, const float *d_final_state, void *dq,
+                    void *dk, void *dv, float *d_init_state, void *workspace, size_t workspace_bytes,
+                    void *stream) {
+  return bwd_impl(shape, q, k, v, dO, init_state, d_final_state, nullptr, 0, false, dq, dk, dv, d_init_state,
+                  workspace, workspace_bytes, stream);
 }
 
 int32_t linattn_bwd_ckpt(const linattn_shape *shape, const void *q, const void *k, const void *v,
-                         const void *dO, const float *init_state, const void *checkpoint, size_t checkpoint_bytes,
-                         void *dq, void *dk, void *dv, float *d_init_state, void *workspace,
-                         size_t workspace_bytes, void *stream) {
-  return bwd_impl(shape, q, k, v, dO, init_state, static_cast<const float *>(checkpoint), checkpoint_bytes, true,
-                  dq, dk, dv, d_init_state, workspace, workspace_bytes, stream);
+                         const void *dO, const float *init_state, const float *d_final_state,
+                         const void *checkpoint, size_t checkpoint_bytes, void *dq, void *dk, void *dv,
+                         float *d_init_state, void *workspace, size_t workspace_bytes, void *stream) {
+  return bwd_impl(shape, q, k, v, dO, init_state, d_final_state, static_cast<const float *>(checkpoint),
+                  checkpoint_bytes, true, dq, dk, dv, d_init_state, workspace, workspace_bytes, stream);
 }
 
 int32_t linattn_decode(const linattn_shape *shape, const void *q, const void *k, const void *v, void *o,
@@ -374,22 +386,33 @@ int32_t linattn_decode(const linattn_shape *shape, const void *q, const void *k,
   return cuda_status(decode(p, q, k, v, o, state, static_cast<cudaStream_t>(stream)));
 }
 
-int32_t linattn_chunk_states(const linattn_shape *shape, int32_t seg_len, const void *k, const void *v,
-                             float *local_states, void *workspace, size_t workspace_bytes, void *stream) {
+static int32_t chunk_states_impl(const linattn_shape *shape, int32_t seg_len, const void *x, const void *y,
+                                 bool reverse, float *out, void *workspace, size_t workspace_bytes, void *stream) {
   Problem p;
   int st = validate(shape, &p);
   if (st) return st;
   if (seg_len < 1) return LINATTN_ERR_INVALID;
   if (p.T < 1 || p.T % seg_len) return LINATTN_ERR_UNSUPPORTED;
-  if ((st = check_ptrs({k, v, local_states}, {}))) return st;
+  if ((st = check_ptrs({x, y, out}, {}))) return st;
   if ((st = check_ws(workspace, workspace_bytes, kHeader))) return st;
   if ((st = device_ok())) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int *status = reinterpret_cast<int *>(workspace);
   if (cudaMemsetAsync(workspace, 0, kHeader, s) != cudaSuccess) return LINATTN_ERR_CUDA;
   if (tc_supported(p) && seg_len % 128 == 0)
-    return cuda_status(tc_segment_states(p, seg_len, k, v, false, local_states, status, s));
-  return cuda_status(simt_segment_states(p, seg_len, k, v, local_states, s));
+    return cuda_status(tc_segment_states(p, seg_len, x, y, reverse, out, status, s));
+  return cuda_status(simt_segment_states(p, seg_len, x, y, reverse, out, s));
+}
+
+int32_t linattn_chunk_states(const linattn_shape *shape, int32_t seg_len, const void *k, const void *v,
+                             float *local_states, void *workspace, size_t workspace_bytes, void *stream) {
+  return chunk_states_impl(shape, seg_len, k, v, false, local_states, workspace, workspace_bytes, stream);
+}
+
+int32_t linattn_chunk_states_rev(const linattn_shape *shape, int32_t seg_len, const void *q, const void *dO,
+                                 float *local_grad_states, void *workspace, size_t workspace_bytes,
+                                 void *stream) {
+  return chunk_states_impl(shape, seg_len, q, dO, true, local_grad_states, workspace, workspace_bytes, stream);
 }
 
 int32_t linattn_state_scan_workspace_size(int32_t G, int32_t BH, int32_t dk, int32_t dv, size_t *bytes) {

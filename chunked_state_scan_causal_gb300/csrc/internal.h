@@ -38,8 +38,10 @@ struct TimedLaunch {
 cudaError_t simt_fwd(const Problem &p, const void *q, const void *k, const void *v, void *o,
                      const float *init, float *final_state, float *chunk_states, cudaStream_t s);
 cudaError_t simt_bwd(const Problem &p, const void *q, const void *k, const void *v, const void *dO,
-                     const float *init, void *dq, void *dk, void *dv, float *dinit, cudaStream_t s);
-cudaError_t simt_segment_states(const Problem &p, int seg_len, const void *k, const void *v,
+                     const float *init, const float *d_final, void *dq, void *dk, void *dv, float *dinit,
+                     cudaStream_t s);
+// Segment sums of w_s x_s y_s^T: w_s = lambda^{end - s}, or lambda^{s - start + 1} when reverse.
+cudaError_t simt_segment_states(const Problem &p, int seg_len, const void *x, const void *y, bool reverse,
                                 float *out, cudaStream_t s);
 
 // ---------------------------------------------------------------- state scan (scan.cu)
@@ -52,6 +54,12 @@ size_t scan_workspace_bytes(int G, int64_t E);
 cudaError_t state_scan(int G, int BH, int DD, const float *seg_decay, const float *decay_h, int H,
                        int seg_len, bool reverse, const float *local, const float *init, float *out,
                        float *total, void *ws, int *status, cudaStream_t s);
+
+// w[i] += lambda_h^len d[i] over n = BH * DD elements (h = (i / DD) % H; lambda = 1
+// without decay_h): folds a state entering across a segment of len tokens into
+// that segment's aggregate.
+cudaError_t fold_state(float *w, const float *d, const float *decay_h, int H, int DD, int len, int64_t n,
+                       cudaStream_t s);
 
 // ---------------------------------------------------------------- tensor-core path (tc.cu)
 bool tc_supported(const Problem &p);   // bf16, d = 128

@@ -243,6 +243,23 @@ size_t scan_workspace_bytes(int G, int64_t E) {
   return align256(256 + nt * 4) + 2 * align256(nt * kVec * 4);
 }
 
+namespace {
+__global__ void fold_kernel(float *w, const float *d, const float *decay_h, int H, int DD, int len, int64_t n) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const float a = decay_h ? (float)pow((double)decay_h[(i / DD) % H], (double)len) : 1.f;
+    w[i] = fmaf(a, d[i], w[i]);
+  }
+}
+}  // namespace
+
+cudaError_t fold_state(float *w, const float *d, const float *decay_h, int H, int DD, int len, int64_t n,
+                       cudaStream_t s) {
+  const int64_t want = (n + 255) / 256;
+  TimedLaunch t(K_SCAN, s);
+  fold_kernel<<<(int)(want < 1024 ? want : 1024), 256, 0, s>>>(w, d, decay_h, H, DD, len, n);
+  return cudaGetLastError();
+}
+
 cudaError_t state_scan(int G, int BH, int DD, const float *seg_decay, const float *decay_h, int H,
                        int seg_len, bool reverse, const float *local, const float *init, float *out,
                        float *total, void *ws, int *status, cudaStream_t s) {

@@ -112,8 +112,8 @@ __global__ void __launch_bounds__(kThreads) simt_fwd_kernel(Problem p, const TIn
 template <int D, typename TIn>
 __global__ void __launch_bounds__(kThreads) simt_bwd_kernel(Problem p, const TIn *q, const TIn *k,
                                                             const TIn *v, const TIn *dO,
-                                                            const float *init, TIn *dq, TIn *dk,
-                                                            TIn *dv, float *dinit) {
+                                                            const float *init, const float *dfin,
+                                                            TIn *dq, TIn *dk, TIn *dv, float *dinit) {
   extern __shared__ float sm[];
   constexpr int LD = D + 1;
   float *S = sm;                 // forward state, then the reverse state
@@ -170,7 +170,9 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_kernel(Problem p, const TIn
   }
 
   // reverse sweep with Rbar = sum_{u > chunk end} lambda^{u-end} q_u dO_u^T
-  for (int e = threadIdx.x; e < D * D; e += kThreads) S[(e / D) * LD + e % D] = 0.f;
+  // (+ lambda^{T-1-end} d_final: the gradient arriving at the final state)
+  for (int e = threadIdx.x; e < D * D; e += kThreads)
+    S[(e / D) * LD + e % D] = dfin ? dfin[(int64_t)bh * D * D + e] : 0.f;
   __syncthreads();
   for (int c = nchunk - 1; c >= 0; --c) {
     const int c0 = c * kC, n = min(kC, p.T - c0);
@@ -225,7 +227,7 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_kernel(Problem p, const TIn
 // ------------------------------------------------------------------ segment-local states
 template <int D, typename TIn>
 __global__ void __launch_bounds__(kThreads) simt_segment_kernel(Problem p, int seg_len, const TIn *k,
-                                                                const TIn *v, float *out) {
+                                                                const TIn *v, bool reverse, float *out) {
   extern __shared__ float sm[];
   constexpr int LD = D + 1;
   constexpr int PER = D * D / kThreads;
@@ -239,8 +241,12 @@ __global__ void __launch_bounds__(kThreads) simt_segment_kernel(Problem p, int s
   float acc[PER];
 #pragma unroll
   for (int m = 0; m < PER; ++m) acc[m] = 0.f;
+  // forward weights lambda^{end - s}: chunks in order, acc <- lambda^n acc + sum_j lambda^{n-1-j} k_j v_j^T;
+  // reverse weights lambda^{s - start + 1}: chunks from the end, acc <- lambda^n acc + sum_j lambda^{j+1} ...
   const int s0 = g * seg_len, s1 = min(p.T, s0 + seg_len);
-  for (int c0 = s0; c0 < s1; c0 += kC) {
+  const int nck = (s1 - s0 + kC - 1) / kC;
+  for (int ci = 0; ci < nck; ++ci) {
+    const int c0 = s0 + kC * (reverse ? nck - 1 - ci : ci);
     const int n = min(kC, s1 - c0);
     __syncthreads();
     load_tile<D>(K, k + off, p.st, c0, n);
@@ -250,7 +256,7 @@ __global__ void __launch_bounds__(kThreads) simt_segment_kernel(Problem p, int s
     for (int m = 0; m < PER; ++m) {
       const int e = threadIdx.x + m * kThreads, a = e / D, bb = e % D;
       float x = 0.f;
-      for (int j = 0; j < n; ++j) x = fmaf(pw[n - 1 - j] * K[j * LD + a], V[j * LD + bb], x);
+      for (int j = 0; j < n; ++j) x = fmaf(pw[reverse ? j + 1 : n - 1 - j] * K[j * LD + a], V[j * LD + bb], x);
       acc[m] = fmaf(pw[n], acc[m], x);
     }
   }
@@ -280,18 +286,19 @@ cudaError_t launch_fwd(const Problem &p, const void *q, const void *k, const voi
 }
 template <int D, typename TIn>
 cudaError_t launch_bwd(const Problem &p, const void *q, const void *k, const void *v, const void *dO,
-                       const float *init, void *dq, void *dk, void *dv, float *dinit, cudaStream_t s) {
+                       const float *init, const float *dfin, void *dq, void *dk, void *dv, float *dinit,
+                       cudaStream_t s) {
   auto kern = simt_bwd_kernel<D, TIn>;
   const size_t sm = bwd_smem<D>();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return e;
   TimedLaunch t(K_SIMT_BWD, s);
   kern<<<p.B * p.H, kThreads, sm, s>>>(p, (const TIn *)q, (const TIn *)k, (const TIn *)v,
-                                        (const TIn *)dO, init, (TIn *)dq, (TIn *)dk, (TIn *)dv, dinit);
+                                        (const TIn *)dO, init, dfin, (TIn *)dq, (TIn *)dk, (TIn *)dv, dinit);
   return cudaGetLastError();
 }
 template <int D, typename TIn>
-cudaError_t launch_seg(const Problem &p, int seg_len, const void *k, const void *v, float *out,
+cudaError_t launch_seg(const Problem &p, int seg_len, const void *k, const void *v, bool reverse, float *out,
                        cudaStream_t s) {
   auto kern = simt_segment_kernel<D, TIn>;
   const size_t sm = seg_smem<D>();
@@ -299,7 +306,7 @@ cudaError_t launch_seg(const Problem &p, int seg_len, const void *k, const void 
   if (e != cudaSuccess) return e;
   const int G = (p.T + seg_len - 1) / seg_len;
   TimedLaunch t(K_SIMT_SEGMENT, s);
-  kern<<<dim3(p.B * p.H, G), kThreads, sm, s>>>(p, seg_len, (const TIn *)k, (const TIn *)v, out);
+  kern<<<dim3(p.B * p.H, G), kThreads, sm, s>>>(p, seg_len, (const TIn *)k, (const TIn *)v, reverse, out);
   return cudaGetLastError();
 }
 
@@ -315,21 +322,22 @@ cudaError_t simt_fwd(const Problem &p, const void *q, const void *k, const void 
 }
 
 cudaError_t simt_bwd(const Problem &p, const void *q, const void *k, const void *v, const void *dO,
-                     const float *init, void *dq, void *dk, void *dv, float *dinit, cudaStream_t s) {
+                     const float *init, const float *d_final, void *dq, void *dk, void *dv, float *dinit,
+                     cudaStream_t s) {
   if (p.d == 64)
-    return p.dtype == 1 ? launch_bwd<64, float>(p, q, k, v, dO, init, dq, dk, dv, dinit, s)
-                        : launch_bwd<64, __nv_bfloat16>(p, q, k, v, dO, init, dq, dk, dv, dinit, s);
-  return p.dtype == 1 ? launch_bwd<128, float>(p, q, k, v, dO, init, dq, dk, dv, dinit, s)
-                      : launch_bwd<128, __nv_bfloat16>(p, q, k, v, dO, init, dq, dk, dv, dinit, s);
+    return p.dtype == 1 ? launch_bwd<64, float>(p, q, k, v, dO, init, d_final, dq, dk, dv, dinit, s)
+                        : launch_bwd<64, __nv_bfloat16>(p, q, k, v, dO, init, d_final, dq, dk, dv, dinit, s);
+  return p.dtype == 1 ? launch_bwd<128, float>(p, q, k, v, dO, init, d_final, dq, dk, dv, dinit, s)
+                      : launch_bwd<128, __nv_bfloat16>(p, q, k, v, dO, init, d_final, dq, dk, dv, dinit, s);
 }
 
-cudaError_t simt_segment_states(const Problem &p, int seg_len, const void *k, const void *v,
+cudaError_t simt_segment_states(const Problem &p, int seg_len, const void *x, const void *y, bool reverse,
                                 float *out, cudaStream_t s) {
   if (p.d == 64)
-    return p.dtype == 1 ? launch_seg<64, float>(p, seg_len, k, v, out, s)
-                        : launch_seg<64, __nv_bfloat16>(p, seg_len, k, v, out, s);
-  return p.dtype == 1 ? launch_seg<128, float>(p, seg_len, k, v, out, s)
-                      : launch_seg<128, __nv_bfloat16>(p, seg_len, k, v, out, s);
+    return p.dtype == 1 ? launch_seg<64, float>(p, seg_len, x, y, reverse, out, s)
+                        : launch_seg<64, __nv_bfloat16>(p, seg_len, x, y, reverse, out, s);
+  return p.dtype == 1 ? launch_seg<128, float>(p, seg_len, x, y, reverse, out, s)
+                      : launch_seg<128, __nv_bfloat16>(p, seg_len, x, y, reverse, out, s);
 }
 
 }  // namespace linattn

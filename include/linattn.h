@@ -46,7 +46,7 @@
 extern "C" {
 #endif
 
-#define LINATTN_ABI_VERSION 1
+#define LINATTN_ABI_VERSION 2
 
 /* Status codes (return values and device status word). */
 enum {
@@ -86,8 +86,9 @@ int32_t linattn_abi_version(void);
 const char *linattn_status_string(int32_t status);
 
 /* Workspace bytes needed by linattn_fwd (op=LINATTN_OP_FWD), linattn_bwd
- * (LINATTN_OP_BWD) or linattn_chunk_states (LINATTN_OP_CHUNK_STATES, with its
- * seg_len; ignored otherwise) for this shape on the current device.  With
+ * (LINATTN_OP_BWD) or linattn_chunk_states / linattn_chunk_states_rev
+ * (LINATTN_OP_CHUNK_STATES, with its seg_len; ignored otherwise) for this
+ * shape on the current device.  With
  * op=LINATTN_OP_CHECKPOINT: bytes of the checkpoint of linattn_fwd_ckpt (may
  * be 0 when the shape takes the CUDA-core path, which recomputes instead).
  * Writes *bytes and returns a status; the workspace must be 256-byte aligned. */
@@ -109,14 +110,20 @@ int32_t linattn_fwd(const linattn_shape *shape, const void *q, const void *k, co
 
 /* Backward of linattn_fwd for an upstream gradient dO [B,H,T,dv]:
  *   dq_t = S_t dO_t,   dk_t = R_t v_t,   dv_t = R_t^T k_t,
- *   R_t = sum_{u>=t} lambda^{u-t} q_u dO_u^T (reverse state, scanned backwards),
- *   d_init_state = sum_t lambda^{t+1} q_t dO_t^T   ([B,H,dk,dv] fp32, or NULL).
- * dq, dk [B,H,T,dk] and dv [B,H,T,dv] are written in the shape's dtype.  The
- * forward states are recomputed from k, v and init_state (no stored
- * activations).  Returns a status. */
+ *   R_t = sum_{u>=t} lambda^{u-t} q_u dO_u^T + lambda^{T-1-t} D
+ *         (reverse state, scanned backwards),
+ *   d_init_state = lambda R_0 (= D when T = 0)   ([B,H,dk,dv] fp32, or NULL),
+ * where D = d_final_state ([B,H,dk,dv] fp32, or NULL for zero) is the gradient
+ * arriving at the state after token T-1 -- nonzero when the sequence goes on
+ * in a later segment that started from this final state (the sequence-parallel
+ * split of the ZeCO and LASP-2 pages: the backward passes it from rank r+1 to
+ * rank r, see linattn_chunk_states_rev).  dq, dk [B,H,T,dk] and dv [B,H,T,dv]
+ * are written in the shape's dtype.  The forward states are recomputed from k,
+ * v and init_state (no stored activations).  Returns a status. */
 int32_t linattn_bwd(const linattn_shape *shape, const void *q, const void *k, const void *v,
-                    const void *dO, const float *init_state, void *dq, void *dk, void *dv,
-                    float *d_init_state, void *workspace, size_t workspace_bytes, void *stream);
+                    const void *dO, const float *init_state, const float *d_final_state, void *dq,
+                    void *dk, void *dv, float *d_init_state, void *workspace, size_t workspace_bytes,
+                    void *stream);
 
 /* Forward that also stores a checkpoint for linattn_bwd_ckpt: the fp32 state
  * entering every chunk group of every sequence (the group length is the
@@ -134,9 +141,9 @@ int32_t linattn_fwd_ckpt(const linattn_shape *shape, const void *q, const void *
  * CUDA-core path, whose checkpoint is empty, reads it).  Same outputs as
  * linattn_bwd.  Returns a status. */
 int32_t linattn_bwd_ckpt(const linattn_shape *shape, const void *q, const void *k, const void *v,
-                         const void *dO, const float *init_state, const void *checkpoint, size_t checkpoint_bytes,
-                         void *dq, void *dk, void *dv, float *d_init_state, void *workspace,
-                         size_t workspace_bytes, void *stream);
+                         const void *dO, const float *init_state, const float *d_final_state,
+                         const void *checkpoint, size_t checkpoint_bytes, void *dq, void *dk, void *dv,
+                         float *d_init_state, void *workspace, size_t workspace_bytes, void *stream);
 
 /* Recurrent decode of T new tokens per sequence (constant-memory inference:
  * LASP-2 page, abstract): for t = 0..T-1
@@ -157,6 +164,21 @@ int32_t linattn_decode(const linattn_shape *shape, const void *q, const void *k,
 int32_t linattn_chunk_states(const linattn_shape *shape, int32_t seg_len, const void *k,
                              const void *v, float *local_states, void *workspace,
                              size_t workspace_bytes, void *stream);
+
+/* Segment-local gradient states, the backward's counterpart of
+ * linattn_chunk_states (what each sequence-parallel rank contributes to the
+ * reverse scan that hands every rank the gradient at its final state):
+ *   local_grad_states[g,b,h] = sum_{s in segment g} lambda^{s - start_g + 1} q_s dO_s^T
+ * for G = T / seg_len segments (seg_len >= 1 and a divisor of T; T >= 1),
+ * [G,B,H,dk,dv] fp32.  With every segment's value, the gradient arriving at
+ * the final state of segment g is D_g = sum_{g' > g} a^{g'-g-1} W_g' (a =
+ * lambda^seg_len; linattn_state_scan over the segments in reverse order), and
+ * linattn_bwd of segment g with d_final_state = D_g gives that segment's part
+ * of the whole sequence's gradients.  Workspace as for linattn_chunk_states.
+ * Returns a status. */
+int32_t linattn_chunk_states_rev(const linattn_shape *shape, int32_t seg_len, const void *q,
+                                 const void *dO, float *local_grad_states, void *workspace,
+                                 size_t workspace_bytes, void *stream);
 
 /* Workspace bytes for linattn_state_scan. */
 int32_t linattn_state_scan_workspace_size(int32_t G, int32_t BH, int32_t dk, int32_t dv,

@@ -45,7 +45,7 @@ def test_binding_covers_every_declared_symbol():
 
 
 def test_abi_version_and_status_strings(cdll):
-    assert la.linattn_abi_version() == la.ABI_VERSION == 1
+    assert la.linattn_abi_version() == la.ABI_VERSION == 2
     for code in (0, -1, -2, -3, -4, -5, -6, -7):
         assert la.status_string(code) not in ("", "unknown status")
     assert la.status_string(12345) == "unknown status"
@@ -53,7 +53,7 @@ def test_abi_version_and_status_strings(cdll):
 
 def _shape(**kw):
     s = la.Shape()
-    s.abi_version, s.B, s.H, s.T, s.dk, s.dv, s.chunk, s.dtype = 1, 1, 2, 256, 128, 128, 64, la.BF16
+    s.abi_version, s.B, s.H, s.T, s.dk, s.dv, s.chunk, s.dtype = la.ABI_VERSION, 1, 2, 256, 128, 128, 64, la.BF16
     s.stride_b, s.stride_h, s.stride_t = 2 * 256 * 128, 256 * 128, 128
     s.decay = None
     for k, v in kw.items():
@@ -87,8 +87,11 @@ def test_null_and_misaligned_pointers(cdll):
     s = _shape()
     assert la.linattn_fwd(s, None, FAKE, FAKE, FAKE, None, None, None, FAKE, 1 << 30, None) == la.ERR_INVALID
     assert la.linattn_fwd(s, FAKE + 2, FAKE, FAKE, FAKE, None, None, None, FAKE, 1 << 30, None) == la.ERR_ALIGN
-    assert la.linattn_bwd(s, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, None, None, FAKE, 1 << 30,
+    assert la.linattn_bwd(s, FAKE, FAKE, FAKE, FAKE, None, None, FAKE, FAKE, None, None, FAKE, 1 << 30,
                           None) == la.ERR_INVALID
+    # a misaligned d_final_state is rejected before anything is enqueued
+    assert la.linattn_bwd(s, FAKE, FAKE, FAKE, FAKE, None, FAKE + 4, FAKE, FAKE, FAKE, None, FAKE, 1 << 30,
+                          None) == la.ERR_ALIGN
     assert la.lib().linattn_fwd(None, FAKE, FAKE, FAKE, FAKE, None, None, None, FAKE, 1 << 30, None) \
         == la.ERR_INVALID
 
@@ -110,6 +113,9 @@ def test_chunk_states_and_scan_argument_checks(cdll):
     # seg_len must divide T
     assert la.linattn_chunk_states(s, 100, FAKE, FAKE, FAKE, FAKE, 1 << 20, None) == la.ERR_UNSUPPORTED
     assert la.linattn_chunk_states(s, 0, FAKE, FAKE, FAKE, FAKE, 1 << 20, None) == la.ERR_INVALID
+    assert la.linattn_chunk_states_rev(s, 100, FAKE, FAKE, FAKE, FAKE, 1 << 20, None) == la.ERR_UNSUPPORTED
+    assert la.linattn_chunk_states_rev(s, 0, FAKE, FAKE, FAKE, FAKE, 1 << 20, None) == la.ERR_INVALID
+    assert la.linattn_chunk_states_rev(s, 64, None, FAKE, FAKE, FAKE, 1 << 20, None) == la.ERR_INVALID
     assert la.linattn_state_scan_workspace_size(0, 1, 8, 8)[0] == la.ERR_INVALID
     assert la.linattn_state_scan_workspace_size(3, 2, 3, 3)[0] == la.ERR_UNSUPPORTED
     st, n = la.linattn_state_scan_workspace_size(64, 16, 128, 128)

@@ -143,16 +143,22 @@ def _gpu_uuid(dev):
 
 
 def _profile_traffic():
-    """DRAM bytes per token-head of the chunked kernel from the committed ncu summary, if any."""
-    path = os.path.join(ROOT, "profiles", "tc_chunked_fwd_traffic.txt")
+    """(DRAM bytes per token-head per step, launches per step) of the chunked kernels from the
+    committed ncu summary of the current kernels, if any."""
+    path = os.path.join(ROOT, "profiles", "chunked_kernels_traffic_B2H16T64K.md")
+    vals = {}
     try:
         with open(path) as f:
             for ln in f:
-                if ln.startswith("dram_bytes_per_token_head"):
-                    return float(ln.split("=")[1])
-    except Exception:
-        pass
-    return None
+                if "=" in ln and ln.split("=")[0].strip() in ("dram_bytes_per_token_head_per_step",
+                                                             "chunked_launches_per_step"):
+                    k, v = ln.split("=")
+                    vals[k.strip()] = float(v)
+    except OSError:
+        return None
+    if len(vals) != 2:
+        return None
+    return vals["dram_bytes_per_token_head_per_step"], vals["chunked_launches_per_step"]
 
 
 # ---------------------------------------------------------------------------------- reference arm
@@ -292,7 +298,9 @@ def run_ours(args):
         "kernel": "chunked tensor-core kernels: " + ", ".join(f"{k} x{n // args.steps}" for k, (n, _) in main.items()),
         "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
         "frac": (achieved / hbm) if achieved else None,
-        "traffic": None if traffic_tok is None else traffic_tok * tok_heads,
+        # measured for the benchmark workload with lambda = 1 (null for other workloads)
+        "traffic": (traffic_tok[0] * tok_heads / traffic_tok[1]) if (
+            traffic_tok and args.workload == 3 and not args.B and not args.T) else None,
         "peak_source": f"{peak_src} hbm_gbs",
         "launches_per_step": n_main / args.steps,
         "share_of_step": ms_main / (ms * args.steps) if ms else None,

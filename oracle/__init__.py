@@ -21,6 +21,8 @@ from .oracle import (  # noqa: F401
     bwd_quadratic,
     segment_states,
     segment_grad_states,
+    fwd_gated,
+    bwd_gated,
     state_scan,
     threads_used,
 )

@@ -33,6 +33,7 @@
  * States: [BH][d_k][d_v] row-major (row index = key dimension).
  * lam: [BH] decay per (batch, head) sequence, or NULL for lambda = 1.
  */
+#include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -389,5 +390,118 @@ void oracle_state_scan(i64 G, i64 BH, i64 dk, i64 dv, const double *seg_decay,
     }
     if (total) memcpy(total + bh * D, S, sizeof(double) * D);
     free(S);
+  }
+}
+
+/* ====================================================================== */
+/* Data-dependent gates: a decay per token per head (the gated variant the  */
+/* LASP-2 page names beside the plain one).  With g_t = log(alpha_t) <= 0:  */
+/*     S_t = alpha_t S_{t-1} + k_t v_t^T,     o_t = S_t^T q_t,                */
+/* the plain definition with lambda replaced by the token's own gate.        */
+/* log_gate: [BH][T].                                                       */
+/* ====================================================================== */
+void oracle_fwd_gated(i64 BH, i64 T, i64 dk, i64 dv, const double *log_gate, const double *q,
+                      const double *k, const double *v, const double *init, double *o,
+                      double *final_state) {
+#pragma omp parallel for schedule(dynamic, 1)
+  for (i64 bh = 0; bh < BH; ++bh) {
+    double *S = calloc((size_t)(dk * dv), sizeof(double));
+    if (init) memcpy(S, init + bh * dk * dv, sizeof(double) * dk * dv);
+    for (i64 t = 0; t < T; ++t) {
+      const double a = exp(log_gate[bh * T + t]);
+      const double *qt = q + (bh * T + t) * dk;
+      const double *kt = k + (bh * T + t) * dk;
+      const double *vt = v + (bh * T + t) * dv;
+      double *ot = o + (bh * T + t) * dv;
+      for (i64 i = 0; i < dk; ++i)
+        for (i64 j = 0; j < dv; ++j) S[i * dv + j] = a * S[i * dv + j] + kt[i] * vt[j];
+      for (i64 j = 0; j < dv; ++j) {
+        double acc = 0.0;
+        for (i64 i = 0; i < dk; ++i) acc += S[i * dv + j] * qt[i];
+        ot[j] = acc;
+      }
+    }
+    if (final_state) memcpy(final_state + bh * dk * dv, S, sizeof(double) * dk * dv);
+    free(S);
+  }
+}
+
+/* Backward of oracle_fwd_gated, by the chain rule on the recurrence:       */
+/*   R_t = dL/dS_t = q_t dO_t^T + alpha_{t+1} R_{t+1}   (R_T-ish = d_final)   */
+/*   dq_t = S_t dO_t,  dk_t = R_t v_t,  dv_t = R_t^T k_t,                    */
+/*   dL/dg_t = alpha_t <R_t, S_{t-1}>   (S_t depends on g_t only through      */
+/*             alpha_t S_{t-1}),        d_init = alpha_0 R_0.                  */
+/* S_{t-1} for the reverse sweep is recomputed per 64-token block from the   */
+/* states kept at block starts.                                              */
+void oracle_bwd_gated(i64 BH, i64 T, i64 dk, i64 dv, const double *log_gate, const double *q,
+                      const double *k, const double *v, const double *dO, const double *init,
+                      const double *d_final, double *dq, double *dkk, double *dvv, double *d_log_gate,
+                      double *d_init) {
+  const i64 D = dk * dv, NB = 64, nblk = (T + NB - 1) / NB;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (i64 bh = 0; bh < BH; ++bh) {
+    const double *lg = log_gate + bh * T;
+    double *S = calloc((size_t)D, sizeof(double));
+    double *keep = calloc((size_t)((nblk + 1) * D), sizeof(double)); /* state entering each block */
+    double *blk = calloc((size_t)((NB + 1) * D), sizeof(double));    /* S_{t-1} for the block's t */
+    double *R = calloc((size_t)D, sizeof(double));
+    if (init) memcpy(S, init + bh * D, sizeof(double) * D);
+    for (i64 t = 0; t < T; ++t) {
+      if (t % NB == 0) memcpy(keep + (t / NB) * D, S, sizeof(double) * D);
+      const double a = exp(lg[t]);
+      const double *kt = k + (bh * T + t) * dk, *vt = v + (bh * T + t) * dv, *gt = dO + (bh * T + t) * dv;
+      double *dqt = dq + (bh * T + t) * dk;
+      for (i64 i = 0; i < dk; ++i) {
+        double acc = 0.0;
+        for (i64 j = 0; j < dv; ++j) {
+          S[i * dv + j] = a * S[i * dv + j] + kt[i] * vt[j];
+          acc += S[i * dv + j] * gt[j];
+        }
+        dqt[i] = acc;
+      }
+    }
+    if (d_final) memcpy(R, d_final + bh * D, sizeof(double) * D);
+    for (i64 b = nblk - 1; b >= 0; --b) {
+      const i64 t0 = b * NB, t1 = (t0 + NB < T) ? t0 + NB : T;
+      /* blk[m] = S_{t0+m-1}: the state before token t0+m */
+      memcpy(blk, keep + b * D, sizeof(double) * D);
+      for (i64 t = t0; t < t1 - 1; ++t) {
+        const double a = exp(lg[t]);
+        const double *kt = k + (bh * T + t) * dk, *vt = v + (bh * T + t) * dv;
+        double *prev = blk + (t - t0) * D, *next = blk + (t - t0 + 1) * D;
+        for (i64 i = 0; i < dk; ++i)
+          for (i64 j = 0; j < dv; ++j) next[i * dv + j] = a * prev[i * dv + j] + kt[i] * vt[j];
+      }
+      for (i64 t = t1 - 1; t >= t0; --t) {
+        const double *qt = q + (bh * T + t) * dk, *kt = k + (bh * T + t) * dk;
+        const double *vt = v + (bh * T + t) * dv, *gt = dO + (bh * T + t) * dv;
+        const double carry = (t == T - 1) ? 1.0 : exp(lg[t + 1]);
+        for (i64 i = 0; i < dk; ++i)
+          for (i64 j = 0; j < dv; ++j) R[i * dv + j] = carry * R[i * dv + j] + qt[i] * gt[j];
+        double *dkt = dkk + (bh * T + t) * dk, *dvt = dvv + (bh * T + t) * dv;
+        for (i64 i = 0; i < dk; ++i) {
+          double acc = 0.0;
+          for (i64 j = 0; j < dv; ++j) acc += R[i * dv + j] * vt[j];
+          dkt[i] = acc;
+        }
+        for (i64 j = 0; j < dv; ++j) {
+          double acc = 0.0;
+          for (i64 i = 0; i < dk; ++i) acc += R[i * dv + j] * kt[i];
+          dvt[j] = acc;
+        }
+        if (d_log_gate) {
+          const double *sp = blk + (t - t0) * D;
+          double acc = 0.0;
+          for (i64 x = 0; x < D; ++x) acc += R[x] * sp[x];
+          d_log_gate[bh * T + t] = exp(lg[t]) * acc;
+        }
+      }
+    }
+    if (d_init)
+      for (i64 x = 0; x < D; ++x) d_init[bh * D + x] = (T > 0 ? exp(lg[0]) : 1.0) * R[x];
+    free(S);
+    free(keep);
+    free(blk);
+    free(R);
   }
 }

@@ -262,6 +262,76 @@ def test_split_sequence_backward_equals_whole(lam):
     np.testing.assert_allclose(parts[0][3], ref[3], rtol=1e-10, atol=1e-10)
 
 
+# ------------------------------------------------------------------ data-dependent gates
+def _gates(seed, B, H, T, lo=-0.3):
+    return np.random.default_rng(seed).uniform(lo, 0.0, (B, H, T))
+
+
+def test_constant_gates_reduce_to_the_scalar_decay():
+    """log_gate_t = log(lambda_h) for every t gives the (pinned) per-head decay path."""
+    B, H, T, dk, dv = 2, 2, 33, 3, 4
+    q, k, v, dO = _rand(71, B, H, T, dk, dv)
+    r = np.random.default_rng(72)
+    init, D = r.standard_normal((B, H, dk, dv)), r.standard_normal((B, H, dk, dv))
+    lam = np.array([0.9, 0.6])
+    lg = np.broadcast_to(np.log(lam)[None, :, None], (B, H, T)).copy()
+    o, fin = oracle.fwd_gated(q, k, v, lg, init=init)
+    ro, _, rfin = oracle.fwd_recurrent(q, k, v, lam=lam, init=init)
+    np.testing.assert_allclose(o, ro, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(fin, rfin, rtol=1e-12, atol=1e-12)
+    g = oracle.bwd_gated(q, k, v, dO, lg, init=init, d_final=D)
+    rg = oracle.bwd_recurrent(q, k, v, dO, lam=lam, init=init, d_final=D)
+    for a, b in zip((g[0], g[1], g[2], g[4]), rg):
+        np.testing.assert_allclose(a, b, rtol=1e-11, atol=1e-11)
+
+
+def _torch_gated_loss(q, k, v, init, lg, dO, D):
+    G = torch.cumsum(lg, dim=-1)                                            # [B, H, T]
+    T = q.shape[2]
+    causal = torch.tril(torch.ones(T, T, dtype=torch.bool))
+    diff = G[..., :, None] - G[..., None, :]
+    M = torch.where(causal, torch.exp(torch.where(causal, diff, torch.zeros_like(diff))), torch.zeros_like(diff))
+    O = ((q @ k.transpose(-1, -2)) * M) @ v + torch.exp(G)[..., None] * (q @ init)
+    Sfin = torch.einsum("bht,bhta,bhtc->bhac", torch.exp(G[..., -1:] - G), k, v) + torch.exp(G[..., -1])[..., None, None] * init
+    return (O * dO).sum() + (Sfin * D).sum()
+
+
+def test_gated_backward_matches_fp64_autograd():
+    """Gradients of <dO, o> + <D, S_final> w.r.t. q, k, v, init and every log-gate equal
+    torch fp64 autograd of the masked form with mask exp(G_t - G_s), G = cumsum(log_gate)."""
+    B, H, T, dk, dv = 1, 2, 41, 4, 3
+    q, k, v, dO = _rand(81, B, H, T, dk, dv)
+    r = np.random.default_rng(82)
+    init, D = r.standard_normal((B, H, dk, dv)), r.standard_normal((B, H, dk, dv))
+    lg = _gates(83, B, H, T)
+    t = [torch.tensor(a, requires_grad=True) for a in (q, k, v, init, lg)]
+    loss = _torch_gated_loss(*t[:4], t[4], torch.tensor(dO), torch.tensor(D))
+    loss.backward()
+    dq, dk_, dv_, dlg, dinit = oracle.bwd_gated(q, k, v, dO, lg, init=init, d_final=D)
+    for got, ref in zip((dq, dk_, dv_, dinit, dlg), (t[0].grad, t[1].grad, t[2].grad, t[3].grad, t[4].grad)):
+        np.testing.assert_allclose(got, ref.numpy(), rtol=1e-10, atol=1e-10)
+    o, fin = oracle.fwd_gated(q, k, v, lg, init=init)
+    assert abs(float(np.sum(o * dO) + np.sum(fin * D)) - loss.item()) < 1e-9 * max(1.0, abs(loss.item()))
+
+
+def test_gated_log_gate_gradient_finite_differences():
+    """d(<o, dO> + <S_final, D>)/d log_gate_t by central differences on the forward."""
+    B, H, T, dk, dv = 1, 1, 70, 3, 2        # more than one 64-token recompute block
+    q, k, v, dO = _rand(91, B, H, T, dk, dv)
+    r = np.random.default_rng(92)
+    init, D = r.standard_normal((B, H, dk, dv)), r.standard_normal((B, H, dk, dv))
+    lg = _gates(93, B, H, T, lo=-0.5)
+    dlg = oracle.bwd_gated(q, k, v, dO, lg, init=init, d_final=D)[3]
+    h = 1e-6
+    for t in (0, 1, 31, 63, 64, 65, 69):
+        up, dn = lg.copy(), lg.copy()
+        up[0, 0, t] += h
+        dn[0, 0, t] -= h
+        f = lambda g: (lambda o, fin: float(np.sum(o * dO) + np.sum(fin * D)))(*oracle.fwd_gated(q, k, v, g, init=init))
+        num = (f(up) - f(dn)) / (2 * h)
+        assert abs(num - dlg[0, 0, t]) < 1e-6 * max(1.0, abs(num)), t
+
+
 # ------------------------------------------------------------------ chunked == recurrent == quadratic
 @pytest.mark.parametrize("lam", [None, 0.5, 0.96875])
 def test_chunked_equals_recurrent_every_chunk_length(lam):

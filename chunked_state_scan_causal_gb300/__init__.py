@@ -29,6 +29,7 @@ ERR_SCRATCH_LIMIT = -8
 NOALLOC_MAX_TILES = 65536
 BF16, F32 = 0, 1
 OP_FWD, OP_BWD, OP_CHUNK_STATES, OP_CHECKPOINT = 1, 2, 3, 4
+OP_FWD_GATED, OP_BWD_GATED, OP_CHECKPOINT_GATED = 5, 6, 7
 ABI_VERSION = 2
 
 
@@ -63,6 +64,9 @@ _SIGS = {
                           _sz, _vp], _i32),
     "linattn_chunk_states": ([ctypes.POINTER(Shape), _i32, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "linattn_chunk_states_rev": ([ctypes.POINTER(Shape), _i32, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
+    "linattn_fwd_gated": ([ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _sz, _vp], _i32),
+    "linattn_bwd_gated": ([ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _vp, _vp, _vp,
+                           _vp, _vp, _sz, _vp], _i32),
     "linattn_decode": ([ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp], _i32),
     "linattn_state_scan_workspace_size": ([_i32, _i32, _i32, _i32, ctypes.POINTER(_sz)], _i32),
     "linattn_state_scan": ([_i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
@@ -73,7 +77,7 @@ _SIGS = {
     "linattn_timing_collect": ([_i32, ctypes.POINTER(_i32), ctypes.POINTER(ctypes.c_float)], _i32),
     "linattn_kernel_name": ([_i32], ctypes.c_char_p),
 }
-KERNEL_KINDS = 10
+KERNEL_KINDS = 11
 
 
 def lib():
@@ -142,6 +146,18 @@ def linattn_bwd_ckpt(shape, q, k, v, dO, init_state, d_final, ckpt, ckpt_bytes, 
 
 def linattn_chunk_states(shape, seg_len, k, v, out, ws, ws_bytes, stream) -> int:
     return lib().linattn_chunk_states(ctypes.byref(shape), seg_len, k, v, out, ws, ws_bytes, stream)
+
+
+def linattn_fwd_gated(shape, q, k, v, log_gate, o, init_state, final_state, ckpt, ckpt_bytes, ws, ws_bytes,
+                      stream) -> int:
+    return lib().linattn_fwd_gated(ctypes.byref(shape), q, k, v, log_gate, o, init_state, final_state, ckpt,
+                                   ckpt_bytes, ws, ws_bytes, stream)
+
+
+def linattn_bwd_gated(shape, q, k, v, dO, log_gate, init_state, d_final, ckpt, ckpt_bytes, dq, dk, dv, d_log_gate,
+                      d_init, ws, ws_bytes, stream) -> int:
+    return lib().linattn_bwd_gated(ctypes.byref(shape), q, k, v, dO, log_gate, init_state, d_final, ckpt,
+                                   ckpt_bytes, dq, dk, dv, d_log_gate, d_init, ws, ws_bytes, stream)
 
 
 def linattn_chunk_states_rev(shape, seg_len, q, dO, out, ws, ws_bytes, stream) -> int:
@@ -341,6 +357,62 @@ def chunk_states_rev(q, dO, seg_len: int, decay=None, out=None, ws=None, stream=
                                   _stream(q.device, stream))
     _check(st, "linattn_chunk_states_rev")
     return out
+
+
+def checkpoint_gated(q):
+    """Checkpoint buffer of fwd_gated for bwd_gated (group states and the final state)."""
+    import torch
+    st, n = linattn_workspace_size(shape_of(q, None), OP_CHECKPOINT_GATED)
+    _check(st, "linattn_workspace_size")
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=q.device)
+
+
+def _gate_tensor(log_gate, q):
+    import torch
+    B, H, T, _ = q.shape
+    if log_gate.dtype != torch.float32 or not log_gate.is_contiguous() or tuple(log_gate.shape) != (B, H, T):
+        raise ValueError("log_gate must be contiguous fp32 [B, H, T]")
+    return log_gate
+
+
+def fwd_gated(q, k, v, log_gate, ckpt, init_state=None, want_final=False, out=None, ws=None, stream=None):
+    """(o, final_state or None) with a gate per token: S_t = exp(log_gate_t) S_{t-1} + k_t v_t^T.
+    ``ckpt`` (from checkpoint_gated) receives what bwd_gated needs."""
+    import torch
+    _same_layout(q, k, v, out)
+    _gate_tensor(log_gate, q)
+    B, H, T, d = q.shape
+    o = out if out is not None else torch.empty_strided(q.shape, q.stride(), dtype=q.dtype, device=q.device)
+    fin = torch.empty((B, H, d, d), dtype=torch.float32, device=q.device) if want_final else None
+    shape = shape_of(q, None)
+    if ws is None:
+        ws = workspace(q, OP_FWD_GATED)
+    st = linattn_fwd_gated(shape, _ptr(q), _ptr(k), _ptr(v), _ptr(log_gate), _ptr(o), _ptr(init_state), _ptr(fin),
+                           _ptr(ckpt), ckpt.numel(), _ptr(ws), ws.numel(), _stream(q.device, stream))
+    _check(st, "linattn_fwd_gated")
+    return o, fin
+
+
+def bwd_gated(q, k, v, dO, log_gate, ckpt, init_state=None, d_final=None, want_dinit=False, outs=None, ws=None,
+              stream=None):
+    """(dq, dk, dv, d_log_gate, d_init or None) of fwd_gated for the upstream gradient dO."""
+    import torch
+    _same_layout(q, k, v, dO)
+    _gate_tensor(log_gate, q)
+    B, H, T, d = q.shape
+    if outs is None:
+        outs = [torch.empty_strided(q.shape, q.stride(), dtype=q.dtype, device=q.device) for _ in range(3)]
+    dq, dk, dv = outs
+    dlg = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
+    dinit = torch.empty((B, H, d, d), dtype=torch.float32, device=q.device) if want_dinit else None
+    shape = shape_of(q, None)
+    if ws is None:
+        ws = workspace(q, OP_BWD_GATED)
+    st = linattn_bwd_gated(shape, _ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(log_gate), _ptr(init_state),
+                           _ptr(d_final), _ptr(ckpt), ckpt.numel(), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dlg),
+                           _ptr(dinit), _ptr(ws), ws.numel(), _stream(q.device, stream))
+    _check(st, "linattn_bwd_gated")
+    return dq, dk, dv, dlg, dinit
 
 
 def state_scan(local, seg_decay=None, init=None, want_total=False, out=None, ws=None, stream=None):

@@ -180,6 +180,36 @@ static size_t ckpt_bytes(const Problem &p) {
   return w.G == 0 ? 0 : (size_t)w.G * p.B * p.H * p.d * p.d * sizeof(float);
 }
 
+// Gated layouts: the forward layout plus the gates' cumulative sums [BH][T] and
+// group totals [G][BH]; the backward adds the reverse aggregates, the reverse
+// group states and the gate-gradient scratch.  The gated checkpoint holds the
+// group states and then the final state.
+struct GatedLayout {
+  FwdLayout f;
+  size_t C = 0, tot = 0, wagg = 0, rbar = 0, gsum = 0, dot = 0, gx = 0, fwd_total = kHeader, bwd_total = kHeader;
+};
+static GatedLayout gated_layout(const Problem &p) {
+  GatedLayout w;
+  w.f = fwd_layout(p);
+  if (w.f.G == 0) return w;
+  const int64_t BH = (int64_t)p.B * p.H;
+  const size_t st = (size_t)w.f.G * BH * p.d * p.d * sizeof(float);
+  w.C = w.f.total;
+  w.tot = w.C + align256((size_t)BH * p.T * sizeof(float));
+  w.fwd_total = w.tot + align256((size_t)w.f.G * BH * sizeof(float));
+  w.wagg = w.fwd_total;
+  w.rbar = w.wagg + align256(st);
+  w.gsum = w.rbar + align256(st);
+  w.dot = w.gsum + align256((size_t)w.f.G * BH * sizeof(float));
+  w.gx = w.dot + align256((size_t)BH * sizeof(float));
+  w.bwd_total = w.gx + align256((size_t)BH * p.T * sizeof(float));
+  return w;
+}
+static size_t ckpt_bytes_gated(const Problem &p) {
+  const FwdLayout w = fwd_layout(p);
+  return w.G == 0 ? 0 : ((size_t)w.G + 1) * p.B * p.H * p.d * p.d * sizeof(float);
+}
+
 static int check_ws(void *ws, size_t bytes, size_t need) {
   if (!ws) return LINATTN_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return LINATTN_ERR_WORKSPACE;
@@ -224,6 +254,12 @@ int32_t linattn_workspace_size(const linattn_shape *shape, int32_t op, int32_t s
     *bytes = kHeader;
   } else if (op == LINATTN_OP_CHECKPOINT) {
     *bytes = ckpt_bytes(p);
+  } else if (op == LINATTN_OP_FWD_GATED) {
+    *bytes = gated_layout(p).fwd_total;
+  } else if (op == LINATTN_OP_BWD_GATED) {
+    *bytes = gated_layout(p).bwd_total;
+  } else if (op == LINATTN_OP_CHECKPOINT_GATED) {
+    *bytes = ckpt_bytes_gated(p);
   } else {
     return LINATTN_ERR_INVALID;
   }
@@ -375,6 +411,120 @@ int32_t linattn_bwd_ckpt(const linattn_shape *shape, const void *q, const void *
                   checkpoint_bytes, true, dq, dk, dv, d_init_state, workspace, workspace_bytes, stream);
 }
 
+// ------------------------------------------------------------------ data-dependent gates
+static int gated_checks(const linattn_shape *shape, Problem *p, const float *log_gate, const void *ckpt,
+                        size_t ckpt_size) {
+  int st = validate(shape, p);
+  if (st) return st;
+  if (p->decay) return LINATTN_ERR_INVALID;  // gates replace the per-head decay
+  if (p->T > 0 && !tc_supported(*p)) return LINATTN_ERR_UNSUPPORTED;
+  if (p->T > 0 && (st = check_ptrs({log_gate}, {}))) return st;
+  const size_t need = ckpt_bytes_gated(*p);
+  if (need && (!ckpt || (reinterpret_cast<uintptr_t>(ckpt) & 255u) || ckpt_size < need)) return LINATTN_ERR_INVALID;
+  return LINATTN_OK;
+}
+
+int32_t linattn_fwd_gated(const linattn_shape *shape, const void *q, const void *k, const void *v,
+                          const float *log_gate, void *o, const float *init_state, float *final_state,
+                          void *checkpoint, size_t checkpoint_bytes, void *workspace, size_t workspace_bytes,
+                          void *stream) {
+  Problem p;
+  int st = gated_checks(shape, &p, log_gate, checkpoint, checkpoint_bytes);
+  if (st) return st;
+  if (p.T > 0 && (st = check_ptrs({q, k, v, o}, {}))) return st;
+  if ((st = check_ptrs({}, {init_state, final_state}))) return st;
+  const GatedLayout w = gated_layout(p);
+  if ((st = check_ws(workspace, workspace_bytes, w.fwd_total))) return st;
+  if ((st = device_ok())) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char *ws = static_cast<char *>(workspace);
+  int *status = reinterpret_cast<int *>(ws);
+  if (cudaMemsetAsync(ws, 0, kHeader, s) != cudaSuccess) return LINATTN_ERR_CUDA;
+  const int64_t BH = (int64_t)p.B * p.H;
+  const size_t state_bytes = (size_t)BH * p.d * p.d * sizeof(float);
+  if (p.T == 0) {
+    if (final_state) {
+      cudaError_t e = init_state ? cudaMemcpyAsync(final_state, init_state, state_bytes,
+                                                   cudaMemcpyDeviceToDevice, s)
+                                 : cudaMemsetAsync(final_state, 0, state_bytes, s);
+      return cuda_status(e);
+    }
+    return LINATTN_OK;
+  }
+  const int L = w.f.L, G = w.f.G;
+  float *C = reinterpret_cast<float *>(ws + w.C), *tot = reinterpret_cast<float *>(ws + w.tot);
+  float *agg = reinterpret_cast<float *>(ws + w.f.agg);
+  float *states = static_cast<float *>(checkpoint);
+  float *fin = states + (size_t)G * BH * p.d * p.d;  // the checkpoint's final state
+  cudaError_t e = gate_prep(p, L, log_gate, C, tot, s);
+  p.gC = C;
+  p.gtot = tot;
+  if (e == cudaSuccess) e = tc_segment_states(p, L, k, v, false, agg, status, s);
+  if (e == cudaSuccess)
+    e = state_scan(G, (int)BH, p.d * p.d, nullptr, nullptr, p.H, L, false, agg, init_state, states, nullptr,
+                   ws + w.f.scan, status, s, tot);
+  if (e == cudaSuccess) e = tc_main(p, L, q, k, v, o, states, false, fin, status, s);
+  if (e == cudaSuccess && final_state)
+    e = cudaMemcpyAsync(final_state, fin, state_bytes, cudaMemcpyDeviceToDevice, s);
+  return cuda_status(e);
+}
+
+int32_t linattn_bwd_gated(const linattn_shape *shape, const void *q, const void *k, const void *v,
+                          const void *dO, const float *log_gate, const float *init_state,
+                          const float *d_final_state, const void *checkpoint, size_t checkpoint_bytes, void *dq,
+                          void *dk, void *dv, float *d_log_gate, float *d_init_state, void *workspace,
+                          size_t workspace_bytes, void *stream) {
+  Problem p;
+  int st = gated_checks(shape, &p, log_gate, checkpoint, checkpoint_bytes);
+  if (st) return st;
+  if (p.T > 0 && (st = check_ptrs({q, k, v, dO, dq, dk, dv, d_log_gate}, {}))) return st;
+  if ((st = check_ptrs({}, {init_state, d_final_state, d_init_state}))) return st;
+  const GatedLayout w = gated_layout(p);
+  if ((st = check_ws(workspace, workspace_bytes, w.bwd_total))) return st;
+  if ((st = device_ok())) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char *ws = static_cast<char *>(workspace);
+  int *status = reinterpret_cast<int *>(ws);
+  if (cudaMemsetAsync(ws, 0, kHeader, s) != cudaSuccess) return LINATTN_ERR_CUDA;
+  const int64_t BH = (int64_t)p.B * p.H, E = BH * p.d * p.d;
+  const size_t state_bytes = (size_t)E * sizeof(float);
+  if (p.T == 0) {
+    if (d_init_state)
+      return cuda_status(d_final_state ? cudaMemcpyAsync(d_init_state, d_final_state, state_bytes,
+                                                         cudaMemcpyDeviceToDevice, s)
+                                       : cudaMemsetAsync(d_init_state, 0, state_bytes, s));
+    return LINATTN_OK;
+  }
+  const int L = w.f.L, G = w.f.G;
+  float *C = reinterpret_cast<float *>(ws + w.C), *tot = reinterpret_cast<float *>(ws + w.tot);
+  float *wagg = reinterpret_cast<float *>(ws + w.wagg), *rbar = reinterpret_cast<float *>(ws + w.rbar);
+  const float *states = static_cast<const float *>(checkpoint);
+  const float *fin = states + (size_t)G * E;
+  cudaError_t e = gate_prep(p, L, log_gate, C, tot, s);
+  p.gC = C;
+  p.gtot = tot;
+  p.gq = q;
+  p.gk = k;
+  p.gx = reinterpret_cast<float *>(ws + w.gx);
+  // dq: forward-time kernel with (q, k, v) := (dO, v, k) from the group states (transposed)
+  if (e == cudaSuccess) e = tc_main(p, L, dO, v, k, dq, states, true, nullptr, status, s);
+  // reverse group aggregates sum_s exp2(C_s) q_s dO_s^T, the final-state gradient folded
+  // across the last group, and the reverse scan with every group's own multiplier
+  if (e == cudaSuccess) e = tc_segment_states(p, L, q, dO, true, wagg, status, s);
+  if (e == cudaSuccess && d_final_state)
+    e = fold_state_log2(wagg + (int64_t)(G - 1) * E, d_final_state, tot + (int64_t)(G - 1) * BH, p.d * p.d, E, s);
+  if (e == cudaSuccess)
+    e = state_scan(G, (int)BH, p.d * p.d, nullptr, nullptr, p.H, L, true, wagg, nullptr, rbar, d_init_state,
+                   ws + w.f.scan, status, s, tot);
+  if (e == cudaSuccess && d_final_state)
+    e = cudaMemcpyAsync(rbar + (int64_t)(G - 1) * E, d_final_state, state_bytes, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess) e = tc_dual(p, L, q, k, v, dO, dk, dv, rbar, status, s);
+  if (e == cudaSuccess)
+    e = gate_grad(p, L, p.gx, d_final_state, fin, reinterpret_cast<float *>(ws + w.gsum),
+                  reinterpret_cast<float *>(ws + w.dot), d_log_gate, s);
+  return cuda_status(e);
+}
+
 int32_t linattn_decode(const linattn_shape *shape, const void *q, const void *k, const void *v, void *o,
                        float *state, void *stream) {
   Problem p;
@@ -484,7 +634,8 @@ int32_t linattn_timing_collect(int32_t max_kinds, int32_t *launches, float *tota
 const char *linattn_kernel_name(int32_t kind) {
   static const char *names[K_KINDS] = {"simt_fwd", "simt_bwd", "simt_segment_states", "state_scan",
                                        "tc_segment_aggregate", "tc_chunked_fwd",
-                                       "diag_mma", "decode", "tc_dual_rev", "tc_chunked_fwd_agg"};
+                                       "diag_mma", "decode", "tc_dual_rev", "tc_chunked_fwd_agg",
+                                       "gate_prep_and_grad"};
   return (kind >= 0 && kind < K_KINDS) ? names[kind] : "?";
 }
 

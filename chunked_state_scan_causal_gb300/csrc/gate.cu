@@ -1,0 +1,151 @@
+// Data-dependent gates: a decay alpha_t = exp(g_t) per token per head
+// (S_t = alpha_t S_{t-1} + k_t v_t^T), the gated variant the LASP-2 page names
+// beside the plain one.  Every weight the chunked kernels need is a ratio of
+// products of gates inside one chunk group, so they work from group-local
+// cumulative sums of the gates in base 2,
+//     C[t] = log2(e) * sum_{u = group start .. t} g_u,
+// and a weight exp(sum_{u in (j, i]} g_u) is exp2(C[i] - C[j]).
+//
+// This file holds the small passes around the chunked kernels: the cumulative
+// sums (and each group's total, the scan multiplier of the group), and the
+// gradient of the gates, which follows from the other gradients:
+//     dL/dG_t = q_t . dq_t - k_t . dk_t  (+ <D, S_final> at t = T-1),
+//     dL/dg_u = sum_{t >= u} dL/dG_t      (G_t = sum_{u <= t} g_u),
+// with dq, dk the gradients of the backward (dk includes the part that reaches
+// the final state's gradient D).  The two dot products are taken by the dq
+// and dk/dv passes from their fp32 results before these are rounded to the
+// output dtype: summed over a long sequence, terms from rounded dq, dk would
+// carry the rounding of every token.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+
+namespace linattn {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// One warp per (sequence, group): inclusive prefix sums in steps of 32 tokens.
+__global__ void __launch_bounds__(256) gate_prep_kernel(const float *lg, int T, int L, int G, int BH, float *C,
+                                                        float *tot) {
+  const int w = (int)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) / 32), lane = threadIdx.x & 31;
+  if (w >= BH * G) return;  // warp-uniform
+  const int bh = w / G, g = w % G;
+  const int s0 = g * L, s1 = min(T, s0 + L);
+  const float *src = lg + (int64_t)bh * T;
+  float *dst = C + (int64_t)bh * T;
+  float carry = 0.f;
+  for (int t = s0; t < s1; t += 32) {
+    const int tt = t + lane;
+    float x = tt < s1 ? src[tt] * kLog2e : 0.f;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, x, d);
+      if (lane >= d) x += y;
+    }
+    x += carry;
+    if (tt < s1) dst[tt] = x;
+    carry = __shfl_sync(0xffffffffu, x, 31);
+  }
+  if (lane == 0) tot[(int64_t)g * BH + bh] = carry;
+}
+
+// w[i] += exp2(tot[bh]) d[i] over n = BH * DD elements.
+__global__ void fold_log2_kernel(float *w, const float *d, const float *tot, int DD, int64_t n) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+    w[i] = fmaf(exp2f(tot[i / DD]), d[i], w[i]);
+}
+
+// One block of 256 threads per (sequence, group): the reverse inclusive sums of
+// gx inside the group, walked from the end in tiles of 256 tokens;
+// gsum[g][bh] = the group's total.
+__global__ void __launch_bounds__(256) dgate_local_kernel(int T, int L, int G, int BH, const float *gx, float *dlg,
+                                                          float *gsum) {
+  __shared__ float wsum[8];
+  const int bh = blockIdx.x / G, g = blockIdx.x % G;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+  const int s0 = g * L, s1 = min(T, s0 + L);
+  float carry = 0.f;
+  for (int te = s1; te > s0; te -= 256) {
+    const int ts = max(s0, te - 256), n = te - ts;
+    float v = (int)threadIdx.x < n ? gx[(int64_t)bh * T + ts + threadIdx.x] : 0.f;
+    // reverse inclusive scan: thread i owns token ts + i
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const float y = __shfl_down_sync(0xffffffffu, v, d);
+      if (lane + d < 32) v += y;
+    }
+    if (lane == 0) wsum[warp] = v;  // lane 0 holds its warp's total
+    __syncthreads();
+    float later = 0.f, tile = 0.f;  // sums of the later warps of the tile, of the whole tile
+    for (int w2 = 0; w2 < 8; ++w2) {
+      tile += wsum[w2];
+      if (w2 > warp) later += wsum[w2];
+    }
+    if ((int)threadIdx.x < n) dlg[(int64_t)bh * T + ts + threadIdx.x] = v + later + carry;
+    carry += tile;
+    __syncthreads();  // wsum is rewritten by the next tile
+  }
+  if (threadIdx.x == 0) gsum[(int64_t)g * BH + bh] = carry;
+}
+
+// <D, S_final> per sequence (d^2 elements, one block per sequence).
+__global__ void __launch_bounds__(256) dot_state_kernel(const float *D, const float *S, int DD, float *out) {
+  __shared__ float red[8];
+  const int bh = blockIdx.x;
+  float acc = 0.f;
+  for (int i = threadIdx.x; i < DD; i += 256) acc = fmaf(D[(int64_t)bh * DD + i], S[(int64_t)bh * DD + i], acc);
+#pragma unroll
+  for (int m = 16; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x / 32] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float s = 0.f;
+    for (int w = 0; w < 8; ++w) s += red[w];
+    out[bh] = s;
+  }
+}
+
+// dlg[t] += sum of the totals of the later groups (+ <D, S_final>).
+__global__ void __launch_bounds__(256) dgate_fix_kernel(int T, int L, int G, int BH, const float *gsum,
+                                                        const float *dot, float *dlg) {
+  const int bh = blockIdx.x / G, g = blockIdx.x % G;
+  float off = dot ? dot[bh] : 0.f;
+  for (int g2 = g + 1; g2 < G; ++g2) off += gsum[(int64_t)g2 * BH + bh];
+  const int s0 = g * L, s1 = min(T, s0 + L);
+  for (int t = s0 + threadIdx.x; t < s1; t += 256) dlg[(int64_t)bh * T + t] += off;
+}
+
+}  // namespace
+
+cudaError_t gate_prep(const Problem &p, int L, const float *log_gate, float *C, float *tot, cudaStream_t s) {
+  const int G = (p.T + L - 1) / L, BH = p.B * p.H;
+  const int64_t warps = (int64_t)BH * G;
+  TimedLaunch t(K_GATE, s);
+  gate_prep_kernel<<<(int)((warps + 7) / 8), 256, 0, s>>>(log_gate, p.T, L, G, BH, C, tot);
+  return cudaGetLastError();
+}
+
+cudaError_t fold_state_log2(float *w, const float *d, const float *tot_last, int DD, int64_t n, cudaStream_t s) {
+  const int64_t want = (n + 255) / 256;
+  TimedLaunch t(K_SCAN, s);
+  fold_log2_kernel<<<(int)(want < 1024 ? want : 1024), 256, 0, s>>>(w, d, tot_last, DD, n);
+  return cudaGetLastError();
+}
+
+cudaError_t gate_grad(const Problem &p, int L, const float *gx, const float *d_final, const float *final_state,
+                      float *gsum, float *dot, float *dlg, cudaStream_t s) {
+  const int G = (p.T + L - 1) / L, BH = p.B * p.H;
+  TimedLaunch t(K_GATE, s);
+  dgate_local_kernel<<<BH * G, 256, 0, s>>>(p.T, L, G, BH, gx, dlg, gsum);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (d_final) {
+    dot_state_kernel<<<BH, 256, 0, s>>>(d_final, final_state, p.d * p.d, dot);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  dgate_fix_kernel<<<BH * G, 256, 0, s>>>(p.T, L, G, BH, gsum, d_final ? dot : nullptr, dlg);
+  return cudaGetLastError();
+}
+
+}  // namespace linattn

@@ -14,6 +14,13 @@ struct Problem {
   int64_t sb, sh, st;   // element strides
   const float *decay;   // [H] device, or nullptr (lambda = 1)
   int num_sms;
+  // data-dependent gates (tensor-core path): group-local log2 cumulative sums
+  // [B*H][T] and group totals [G][B*H] for the group length in use, or nullptr
+  const float *gC = nullptr, *gtot = nullptr;
+  // gates, backward: q and k (bf16, the request's strides) and gx [B*H][T] fp32,
+  // which the dq pass fills with q_t . dq_t and the dk/dv pass reduces by k_t . dk_t
+  const void *gq = nullptr, *gk = nullptr;
+  float *gx = nullptr;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -24,7 +31,7 @@ int device_ok();
 // ---------------------------------------------------------------- per-kernel timing (api.cu)
 enum KernelKind {
   K_SIMT_FWD = 0, K_SIMT_BWD, K_SIMT_SEGMENT, K_SCAN, K_TC_AGG, K_TC_MAIN_FWD, K_DIAG,
-  K_DECODE, K_TC_DUAL_REV, K_TC_MAIN_AGG, K_KINDS
+  K_DECODE, K_TC_DUAL_REV, K_TC_MAIN_AGG, K_GATE, K_KINDS
 };
 // Records timing events around one launch on `s` while timing is enabled.
 struct TimedLaunch {
@@ -51,15 +58,28 @@ cudaError_t simt_segment_states(const Problem &p, int seg_len, const void *x, co
 // init, out[g] = a * out[g+1] + local[g+1]).  total (optional) is the value one
 // step past the end.
 size_t scan_workspace_bytes(int G, int64_t E);
+// group_log2 (optional, [G][BH], G <= 256): log2 of every group's own multiplier,
+// replacing the uniform one (data-dependent gates).
 cudaError_t state_scan(int G, int BH, int DD, const float *seg_decay, const float *decay_h, int H,
                        int seg_len, bool reverse, const float *local, const float *init, float *out,
-                       float *total, void *ws, int *status, cudaStream_t s);
+                       float *total, void *ws, int *status, cudaStream_t s, const float *group_log2 = nullptr);
 
 // w[i] += lambda_h^len d[i] over n = BH * DD elements (h = (i / DD) % H; lambda = 1
 // without decay_h): folds a state entering across a segment of len tokens into
 // that segment's aggregate.
 cudaError_t fold_state(float *w, const float *d, const float *decay_h, int H, int DD, int len, int64_t n,
                        cudaStream_t s);
+
+// ---------------------------------------------------------------- data-dependent gates (gate.cu)
+// C[t] = log2(e) * sum of log_gate over the group of L tokens up to t ([B,H,T]);
+// tot[g][bh] = C at the group's last token.
+cudaError_t gate_prep(const Problem &p, int L, const float *log_gate, float *C, float *tot, cudaStream_t s);
+// w[i] += exp2(tot_last[i / DD]) d[i], n elements.
+cudaError_t fold_state_log2(float *w, const float *d, const float *tot_last, int DD, int64_t n, cudaStream_t s);
+// d_log_gate [B,H,T]: reverse sums over each sequence of gx [B*H][T] (q_t . dq_t - k_t . dk_t)
+// and, with d_final, <d_final, final_state>; gsum [G][BH] and dot [BH] are scratch.
+cudaError_t gate_grad(const Problem &p, int L, const float *gx, const float *d_final, const float *final_state,
+                      float *gsum, float *dot, float *dlg, cudaStream_t s);
 
 // ---------------------------------------------------------------- tensor-core path (tc.cu)
 bool tc_supported(const Problem &p);   // bf16, d = 128

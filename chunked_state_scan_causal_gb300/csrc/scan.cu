@@ -37,6 +37,7 @@ constexpr int kVec = 8;  // fp32 elements per lane
 struct ScanArgs {
   int G, BH, DD, H, seg_len, ntg, ncg, reverse;
   const float *seg_decay, *decay_h, *local, *init;
+  const float *glog2;  // [G][BH] log2 of each group's own multiplier (column form only), or null
   float *out, *total;
   unsigned *counter;  // ticket counter (zeroed before launch)
   unsigned *flags;    // [ntg * ncg] 0 empty, 1 aggregate, 2 inclusive (zeroed before launch)
@@ -226,8 +227,10 @@ __global__ void __launch_bounds__(256) scan_columns_kernel(ScanArgs A) {
         const int p = i + j, g = A.reverse ? A.G - 1 - p : p;
         if (p < A.G) {
           *reinterpret_cast<float4 *>(A.out + (int64_t)g * E + e0) = acc;
-          acc = make_float4(fmaf(a, acc.x, u[j].x), fmaf(a, acc.y, u[j].y), fmaf(a, acc.z, u[j].z),
-                            fmaf(a, acc.w, u[j].w));
+          // the combine across group g decays by that group's multiplier
+          const float ag = A.glog2 ? exp2f(A.glog2[(int64_t)g * A.BH + bh]) : a;
+          acc = make_float4(fmaf(ag, acc.x, u[j].x), fmaf(ag, acc.y, u[j].y), fmaf(ag, acc.z, u[j].z),
+                            fmaf(ag, acc.w, u[j].w));
         }
       }
     }
@@ -262,14 +265,15 @@ cudaError_t fold_state(float *w, const float *d, const float *decay_h, int H, in
 
 cudaError_t state_scan(int G, int BH, int DD, const float *seg_decay, const float *decay_h, int H,
                        int seg_len, bool reverse, const float *local, const float *init, float *out,
-                       float *total, void *ws, int *status, cudaStream_t s) {
+                       float *total, void *ws, int *status, cudaStream_t s, const float *group_log2) {
   const int64_t E = (int64_t)BH * DD;
+  if (group_log2 && G > kColumnMaxG) return cudaErrorInvalidValue;
   ScanArgs A;
   A.G = G; A.BH = BH; A.DD = DD; A.H = H; A.seg_len = seg_len;
   A.ntg = (G + 31) / 32;
   A.ncg = (int)(E / kVec);
   A.reverse = reverse ? 1 : 0;
-  A.seg_decay = seg_decay; A.decay_h = decay_h; A.local = local; A.init = init;
+  A.seg_decay = seg_decay; A.decay_h = decay_h; A.local = local; A.init = init; A.glog2 = group_log2;
   A.out = out; A.total = total; A.status = status;
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);

@@ -84,9 +84,12 @@ struct AggParams {
   const float *decay;
   float *out;
   int *status;
+  const float *gC, *gtot;  // gates: group-local log2 cumulative sums [BH][T], group totals [G][BH]
 };
 
-template <bool DECAY>
+// GATE (with DECAY): token weights from the gates' cumulative sums instead of
+// powers of lambda: exp2(tot_g - C_s) (forward), exp2(C_s) (reverse).
+template <bool DECAY, bool GATE = false>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_agg_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__ CUtensorMap my,
                   AggParams P) {
@@ -189,15 +192,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       int it = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < P.nitems && ok; item += gridDim.x) {
-        const int g = item / BH, h = (item % BH) % P.H;
+        const int g = item / BH, bh = item % BH, h = bh % P.H;
         const int s0 = g * P.L, s1 = min(P.T, s0 + P.L);
-        const float l2 = log2f(P.decay[h]);
+        const float l2 = GATE ? 0.f : log2f(P.decay[h]);
+        const float *gc = GATE ? P.gC + (int64_t)bh * P.T : nullptr;
+        const float gt = GATE ? P.gtot[(int64_t)g * BH + bh] : 0.f;
         for (int t0 = s0; t0 < s1; t0 += 128, ++it) {
           const int s = it % NS, u = it / NS;
-          if (!(ok = mbar_wait(&full[s], u & 1, &abort_flag, P.status, detail))) break;
           const int tok = t0 + (int)row;
+          const float ct = (GATE && tok < s1) ? gc[tok] : 0.f;  // load before the wait
+          if (!(ok = mbar_wait(&full[s], u & 1, &abort_flag, P.status, detail))) break;
           float w = 0.f;
-          if (tok < s1) w = exp2f(l2 * (float)(P.reverse ? (tok - s0 + 1) : (s1 - 1 - tok)));
+          if (tok < s1)
+            w = GATE ? exp2f(P.reverse ? ct : gt - ct)
+                     : exp2f(l2 * (float)(P.reverse ? (tok - s0 + 1) : (s1 - 1 - tok)));
           scale_tile_row(smem_u32(smem + s * kStage), row, w);
           fence_proxy_async_smem();
           mbar_arrive(&scaled[s]);
@@ -238,13 +246,18 @@ struct MainParams {
   float *final_state;  // [BH][d][d] or null
   float *agg_out;      // [G][BH][d][d]: per group sum_s x_s q_s^T (AGG instances)
   int *status;
+  const float *gC;     // GATE: group-local log2 cumulative sums of the gates [BH][T]
+  const __nv_bfloat16 *gq;  // GATE, dq pass: the true q (strides sb, sh, st) for gx = q . dq
+  float *gx;           // GATE, dq pass: [BH][T] fp32 q_t . dq_t from the unrounded dq, or null
+  int64_t sb, sh, st;
 };
 
 constexpr int kSlots = 5;
 constexpr uint32_t kOffPs = kSlots * kTileBytes;          // P (then O staging) tile
 constexpr uint32_t kOffSh = kOffPs + kTileBytes;          // bf16 state tile
 constexpr uint32_t kOffBar = kOffSh + kTileBytes;
-constexpr size_t kMainSmem = kOffBar + 256 + 1024;
+constexpr uint32_t kOffGate = kOffBar + 256;               // GATE: 2 x 128 cumulative sums of a block
+constexpr size_t kMainSmem = kOffGate + 1024 + 1024;
 
 // barrier indices
 enum { B_FULL = 0, B_EMPTY = kSlots, B_PFULL = 2 * kSlots, B_PEMPTY, B_OFULL, B_OEMPTY, B_SFULL, B_PRE,
@@ -286,6 +299,42 @@ __device__ __forceinline__ void mask_chunk(float (&x)[32], int i, int c, float l
   }
 }
 
+// Gated mask of one 32-column chunk of a score row i: keep j <= i (causal) or
+// j >= i (anti-causal) and weight by exp2(C_i - C_j) (exp2(C_j - C_i)), with cb
+// the block's 128 cumulative sums; the exponent is <= 0 for gates <= 1.
+template <bool REV>
+__device__ __forceinline__ void mask_chunk_gate(float (&x)[32], int i, int c, float ci, const float *cb) {
+#pragma unroll
+  for (int jj = 0; jj < 32; ++jj) {
+    const int j = c * 32 + jj;
+    const bool keep = REV ? (j >= i) : (j <= i);
+    x[jj] = keep ? x[jj] * exp2f(REV ? cb[j] - ci : ci - cb[j]) : 0.f;
+  }
+}
+
+// sum_j x[j] * y[j] for 32 fp32 x and 32 bf16 y at src (64 contiguous bytes).
+__device__ __forceinline__ float dot32_bf16(const float (&x)[32], const __nv_bfloat16 *src) {
+  const uint4 *p = reinterpret_cast<const uint4 *>(src);
+  float acc = 0.f;
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const uint4 u = __ldg(p + m);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      acc = fmaf(x[8 * m + 2 * e], bf16lo(w[e]), acc);
+      acc = fmaf(x[8 * m + 2 * e + 1], bf16hi(w[e]), acc);
+    }
+  }
+  return acc;
+}
+
+// Cumulative gate sums of token t0 + r of a block of nv valid tokens (rows past
+// the end take the last valid one: finite weights for zero rows).
+__device__ __forceinline__ float gate_c(const float *gc, int t0, int r, int nv) {
+  return gc[t0 + (r < nv ? r : nv - 1)];
+}
+
 // With a decay the inter-block term goes to the fourth TMEM region from the
 // unweighted q (O_inter = Q S) and the epilogue adds lambda^{i+1} O_inter to
 // the intra-block term, so only the key rows are weighted in shared memory
@@ -296,12 +345,17 @@ __device__ __forceinline__ void mask_chunk(float (&x)[32], int i, int c, float l
 // per group to agg_out: for the dq launch (q := dO, x := q) that is the
 // reverse group aggregate sum_s q_s dO_s^T.  Tiles are loaded in the order
 // q, x, k, v and released in the same order.
-template <bool DECAY, bool AGG = false>
+// GATE (with DECAY) takes every weight from the gates' group-local cumulative
+// sums C: o_i = exp2(C_i - C_prev) (Q S)_i + (P V)_i, mask exp2(C_i - C_j), key
+// rows exp2(C_last - C_j), state decay exp2(C_last - C_prev) per block (C_prev:
+// the token before the block, 0 at a group start).
+template <bool DECAY, bool AGG = false, bool GATE = false>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_main_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                    const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mo,
                    const __grid_constant__ CUtensorMap mx, MainParams P) {
   static_assert(!AGG || !DECAY, "group aggregates are fused for the decay-free kernel");
+  static_assert(!GATE || DECAY, "gates use the weighted code paths");
   constexpr int NT = AGG ? 4 : 3;  // tiles per block
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
@@ -456,10 +510,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int item = blockIdx.x; item < P.nitems && ok; item += gridDim.x) {
       const int g = item / BH, bh = item % BH, b = bh / P.H, h = bh % P.H;
       const int s0 = g * P.L, s1 = min(P.T, s0 + P.L), nb = (s1 - s0 + 127) / 128;
-      const float lam = DECAY ? P.decay[h] : 1.f;
-      const float l2 = DECAY ? log2f(lam) : 0.f;
+      const float lam = (DECAY && !GATE) ? P.decay[h] : 1.f;
+      const float l2 = (DECAY && !GATE) ? log2f(lam) : 0.f;
+      const float *gc = GATE ? P.gC + (int64_t)bh * P.T : nullptr;
       for (int n = 0; n < nb; ++n, ++blk) {
-        const int t0 = s0 + 128 * n;
+        const int t0 = s0 + 128 * n, nv = min(128, s1 - t0);
+        float ci = 0.f, cprev = 0.f;
+        float *cb = reinterpret_cast<float *>(smem + kOffGate) + 128 * (blk & 1);
+        if (GATE) {
+          ci = gate_c(gc, t0, (int)row, nv);
+          cprev = t0 > s0 ? gc[t0 - 1] : 0.f;
+          cb[row] = ci;  // read by the whole group after the barrier below
+        }
         ok = group_all(mbar_wait(&bar[B_PFULL], blk & 1, &abort_flag, P.status, detail), 2, 128);
         if (!ok) break;
         tc_fence_after();
@@ -470,7 +532,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 4; ++c) {
           float x[32];
           ld_chunk(tP + lb + c * 32, x);
-          mask_chunk<DECAY, false>(x, (int)row, c, lam, l2);
+          if (GATE)
+            mask_chunk_gate<false>(x, (int)row, c, ci, cb);
+          else
+            mask_chunk<DECAY, false>(x, (int)row, c, lam, l2);
           store_row_chunk_bf16(sPs, row, c, x);
         }
         tc_fence_before();
@@ -481,7 +546,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = group_all(mbar_wait(&bar[B_OFULL], blk & 1, &abort_flag, P.status, detail), 2, 128);
         if (!ok) break;
         tc_fence_after();
-        const float wq = DECAY ? exp2f(l2 * (float)(row + 1)) : 0.f;
+        const float wq = GATE ? exp2f(ci - cprev) : (DECAY ? exp2f(l2 * (float)(row + 1)) : 0.f);
+        const bool gx_row = GATE && P.gx && (int)row < nv;
+        const __nv_bfloat16 *qrow = gx_row ? P.gq + (int64_t)b * P.sb + (int64_t)h * P.sh +
+                                                  (int64_t)(t0 + (int)row) * P.st : nullptr;
+        float gxacc = 0.f;
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           float x[32];
@@ -492,8 +561,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int j = 0; j < 32; ++j) x[j] = fmaf(wq, y[j], x[j]);
           }
+          if (gx_row) gxacc += dot32_bf16(x, qrow + c * 32);  // q . dq before dq is rounded
           store_row_chunk_bf16(sPs, row, c, x);
         }
+        if (gx_row) P.gx[(int64_t)bh * P.T + t0 + row] = gxacc;
         tc_fence_before();
         mbar_arrive(&bar[B_OEMPTY]);
         fence_proxy_async_smem();
@@ -514,13 +585,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int item = blockIdx.x; item < P.nitems && ok; item += gridDim.x) {
       const int g = item / BH, bh = item % BH, h = bh % P.H;
       const int s0 = g * P.L, s1 = min(P.T, s0 + P.L), nb = (s1 - s0 + 127) / 128;
-      const float lam = DECAY ? P.decay[h] : 1.f;
-      const float l2 = DECAY ? log2f(lam) : 0.f;
+      const float lam = (DECAY && !GATE) ? P.decay[h] : 1.f;
+      const float l2 = (DECAY && !GATE) ? log2f(lam) : 0.f;
+      const float *gc = GATE ? P.gC + (int64_t)bh * P.T : nullptr;
       auto nvalid = [&](int n) { return min(128, s1 - (s0 + 128 * n)); };
+      // state decay across block n: lambda^{nv}, or the product of its gates
+      auto block_decay = [&](int n) {
+        const int t0 = s0 + 128 * n, nv = nvalid(n);
+        if (GATE) return exp2f(gc[t0 + nv - 1] - (t0 > s0 ? gc[t0 - 1] : 0.f));
+        return DECAY ? exp2f(l2 * (float)nv) : 1.f;
+      };
       // initial state of the group
       {
         const float *src = P.ginit + ((int64_t)g * BH + bh) * 16384;
-        const float dec = DECAY ? exp2f(l2 * (float)nvalid(0)) : 1.f;
+        const float dec = block_decay(0);
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           float x[32];
@@ -547,9 +625,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int n = 0; n < nb; ++n, ++blk) {
         if (DECAY) {
-          // key rows k_j *= lambda^{nv-1-j} once the scores have read them
-          const int nv = nvalid(n), r = (int)row;
-          const float wk = r < nv ? exp2f(l2 * (float)(nv - 1 - r)) : 0.f;
+          // key rows k_j *= lambda^{nv-1-j} (gates: exp2(C_last - C_j)) once the scores have read them
+          const int nv = nvalid(n), r = (int)row, t0 = s0 + 128 * n;
+          float wk = 0.f;
+          if (r < nv) wk = GATE ? exp2f(gc[t0 + nv - 1] - gc[t0 + r]) : exp2f(l2 * (float)(nv - 1 - r));
           if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_PFULL], blk & 1, &abort_flag, P.status, detail))))
             break;
           scale_tile_row(slot_addr(tile_of(blk, 1)), row, wk);
@@ -560,8 +639,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         tc_fence_after();
         if (n + 1 < nb) {
-          const int nv = nvalid(n + 1);
-          const float dec = DECAY ? exp2f(l2 * (float)nv) : 1.f;
+          const float dec = block_decay(n + 1);
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
             float x[32];
@@ -633,13 +711,17 @@ struct DualParams {
   __nv_bfloat16 *dk, *dv;
   int64_t sb, sh, st;  // element strides of dk and dv
   int *status;
+  const float *gC;     // GATE: group-local log2 cumulative sums of the gates [BH][T]
+  const __nv_bfloat16 *gk;  // GATE: k (strides sb, sh, st) for gx -= k . dk
+  float *gx;           // GATE: [BH][T] fp32, q . dq from the dq pass; k . dk (unrounded dk) subtracted
 };
 
 constexpr int kDualThreads = 512;
 constexpr int kDualSlots = 6;
 constexpr uint32_t kDualOffSh = kDualSlots * kTileBytes;  // bf16 state tile
 constexpr uint32_t kDualOffBar = kDualOffSh + kTileBytes;
-constexpr size_t kDualSmem = kDualOffBar + 256 + 1024;
+constexpr uint32_t kDualOffGate = kDualOffBar + 256;  // GATE: 2 x 128 cumulative sums of a block
+constexpr size_t kDualSmem = kDualOffGate + 1024 + 1024;
 enum { D_FULL = 0, D_EMPTY = kDualSlots, D_PFULL = 2 * kDualSlots, D_PSFULL, D_O1FULL, D_O1EMPTY, D_O2FULL,
        D_O2EMPTY, D_SFULL, D_PRE, D_KSC, D_VSC, D_COUNT };
 
@@ -669,7 +751,10 @@ __device__ __forceinline__ void st_global_chunk_bf16(__nv_bfloat16 *dst, const f
   }
 }
 
-template <bool DECAY>
+// GATE (with DECAY): weights from the gates' group-local cumulative sums C:
+// rows of K, V exp2(C_last - C_i), rows of dO exp2(C_j - C_prev), mask
+// exp2(C_j - C_i), state decay exp2(C_last - C_prev) per block.
+template <bool DECAY, bool GATE = false>
 __global__ void __launch_bounds__(kDualThreads, 1)
     tc_dual_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mq,
                    const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
@@ -841,15 +926,26 @@ __global__ void __launch_bounds__(kDualThreads, 1)
     int blk = 0;
     bool ok = true;
     for (int item = blockIdx.x; item < P.nitems && ok; item += gridDim.x) {
-      const int g = item / BH, h = (item % BH) % P.H;
+      const int g = item / BH, bh = item % BH, h = bh % P.H;
       const int s0 = g * P.L, s1 = min(P.T, s0 + P.L), nb = (s1 - s0 + 127) / 128;
-      const float lam = DECAY ? P.decay[h] : 1.f;
-      const float l2 = DECAY ? log2f(lam) : 0.f;
+      const float lam = (DECAY && !GATE) ? P.decay[h] : 1.f;
+      const float l2 = (DECAY && !GATE) ? log2f(lam) : 0.f;
+      const float *gc = GATE ? P.gC + (int64_t)bh * P.T : nullptr;
       for (int n = 0; n < nb && ok; ++n, ++blk) {
+        float ci = 0.f;
+        float *cb = reinterpret_cast<float *>(smem + kDualOffGate) + 128 * (blk & 1);
+        if (GATE) {
+          // the block's cumulative sums, shared by the group (two buffers: a
+          // buffer is rewritten two blocks later, after this barrier's successor)
+          const int t0 = s0 + 128 * (nb - 1 - n), nv = min(128, s1 - t0);
+          ci = gate_c(gc, t0, (int)row, nv);
+          cb[row] = ci;
+          named_bar_sync(3, 128);
+        }
         for (int half = 0; half < 2 && ok; ++half) {
           const int u = 2 * blk + half;
-          if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar[D_PFULL], u & 1, &abort_flag, P.status, detail))))
-            break;
+          // group-uniform decision: the group also meets at named barrier 3
+          if (!(ok = group_all(mbar_wait(&bar[D_PFULL], u & 1, &abort_flag, P.status, detail), 3, 128))) break;
           tc_fence_after();
           // chunk c's 32 scores become 16 columns of bf16 pairs at 16c: only
           // columns already read are overwritten
@@ -857,7 +953,10 @@ __global__ void __launch_bounds__(kDualThreads, 1)
           for (int c = 0; c < 4; ++c) {
             float x[32];
             ld_chunk(tP + lb + c * 32, x);
-            mask_chunk<DECAY, true>(x, (int)row, c, lam, l2);
+            if (GATE)
+              mask_chunk_gate<true>(x, (int)row, c, ci, cb);
+            else
+              mask_chunk<DECAY, true>(x, (int)row, c, lam, l2);
             uint32_t r[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) r[j] = pack_bf16(x[2 * j], x[2 * j + 1]);
@@ -880,12 +979,21 @@ __global__ void __launch_bounds__(kDualThreads, 1)
     for (int item = blockIdx.x; item < P.nitems && ok; item += gridDim.x) {
       const int g = item / BH, bh = item % BH, h = bh % P.H;
       const int s0 = g * P.L, s1 = min(P.T, s0 + P.L), nb = (s1 - s0 + 127) / 128;
-      const float lam = DECAY ? P.decay[h] : 1.f;
-      const float l2 = DECAY ? log2f(lam) : 0.f;
+      const float lam = (DECAY && !GATE) ? P.decay[h] : 1.f;
+      const float l2 = (DECAY && !GATE) ? log2f(lam) : 0.f;
+      const float *gc = GATE ? P.gC + (int64_t)bh * P.T : nullptr;
       auto nvalid = [&](int n) { return min(128, s1 - (s0 + 128 * (nb - 1 - n))); };
+      auto start = [&](int n) { return s0 + 128 * (nb - 1 - n); };
+      auto cprev = [&](int n) { return start(n) > s0 ? gc[start(n) - 1] : 0.f; };
+      auto clast = [&](int n) { return gc[start(n) + nvalid(n) - 1]; };
+      // state decay across walk block n: lambda^{nv}, or the product of its gates
+      auto block_decay = [&](int n) {
+        if (GATE) return exp2f(clast(n) - cprev(n));
+        return DECAY ? exp2f(l2 * (float)nvalid(n)) : 1.f;
+      };
       {
         const float *src = P.ginit + ((int64_t)g * BH + bh) * 16384;
-        const float dec = DECAY ? exp2f(l2 * (float)nvalid(0)) : 1.f;
+        const float dec = block_decay(0);
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           float x[32];
@@ -908,8 +1016,17 @@ __global__ void __launch_bounds__(kDualThreads, 1)
       for (int n = 0; n < nb && ok; ++n, ++blk) {
         if (DECAY) {
           const int nv = nvalid(n), r = (int)row;
-          const float wx = r < nv ? exp2f(l2 * (float)(nv - 1 - r)) : 0.f;  // rows of K and V
-          const float wy = r < nv ? exp2f(l2 * (float)(r + 1)) : 0.f;       // rows of dO
+          float wx = 0.f, wy = 0.f;  // rows of K and V; rows of dO
+          if (r < nv) {
+            if (GATE) {
+              const float cr = gc[start(n) + r];
+              wx = exp2f(clast(n) - cr);
+              wy = exp2f(cr - cprev(n));
+            } else {
+              wx = exp2f(l2 * (float)(nv - 1 - r));
+              wy = exp2f(l2 * (float)(r + 1));
+            }
+          }
           int sk, sdo, sv, c;
           dual_slot(blk, 0, sk, c);
           dual_slot(blk, 2, sdo, c);
@@ -928,7 +1045,7 @@ __global__ void __launch_bounds__(kDualThreads, 1)
         if (!(ok = wait(D_SFULL, blk))) break;
         tc_fence_after();
         if (n + 1 < nb) {
-          const float dec = DECAY ? exp2f(l2 * (float)nvalid(n + 1)) : 1.f;
+          const float dec = block_decay(n + 1);
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
             float x[32];
@@ -967,12 +1084,18 @@ __global__ void __launch_bounds__(kDualThreads, 1)
           __nv_bfloat16 *dst = (half ? P.dk : P.dv) + (int64_t)b * P.sb + (int64_t)h * P.sh +
                                (int64_t)(t0 + (int)row) * P.st;
           const uint32_t tO = half ? tO2 : tO1;
+          const bool gx_row = GATE && half == 1 && P.gx && valid;
+          const __nv_bfloat16 *krow = gx_row ? P.gk + (int64_t)b * P.sb + (int64_t)h * P.sh +
+                                                   (int64_t)(t0 + (int)row) * P.st : nullptr;
+          float gxacc = 0.f;
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
             float x[32];
             ld_chunk(tO + lb + c * 32, x);
+            if (gx_row) gxacc += dot32_bf16(x, krow + c * 32);  // k . dk before dk is rounded
             if (valid) st_global_chunk_bf16(dst + c * 32, x);
           }
+          if (gx_row) P.gx[(int64_t)bh * P.T + t0 + row] -= gxacc;
           tc_fence_before();
           mbar_arrive(&bar[half ? D_O2EMPTY : D_O1EMPTY]);
         }
@@ -1007,11 +1130,15 @@ cudaError_t tc_segment_states(const Problem &p, int seg_len, const void *X, cons
   A.nitems = A.G * p.B * p.H;
   A.reverse = reverse ? 1 : 0;
   A.decay = p.decay; A.out = out; A.status = status;
+  A.gC = p.gC; A.gtot = p.gtot;
   const size_t smem = 3 * 2 * kTileBytes + 1024 + 256;
   const int grid = A.nitems < p.num_sms ? A.nitems : p.num_sms;
   cudaError_t e;
   TimedLaunch t(K_TC_AGG, s);
-  if (p.decay) {
+  if (p.gC) {
+    if ((e = set_smem(tc_agg_kernel<true, true>, smem)) != cudaSuccess) return e;
+    tc_agg_kernel<true, true><<<grid, kThreads, smem, s>>>(mx, my, A);
+  } else if (p.decay) {
     if ((e = set_smem(tc_agg_kernel<true>, smem)) != cudaSuccess) return e;
     tc_agg_kernel<true><<<grid, kThreads, smem, s>>>(mx, my, A);
   } else {
@@ -1033,10 +1160,16 @@ cudaError_t tc_dual(const Problem &p, int group_len, const void *q, const void *
   D.decay = p.decay; D.ginit = group_init;
   D.dk = static_cast<__nv_bfloat16 *>(dk); D.dv = static_cast<__nv_bfloat16 *>(dv);
   D.sb = p.sb; D.sh = p.sh; D.st = p.st; D.status = status;
+  D.gC = p.gC;
+  D.gk = static_cast<const __nv_bfloat16 *>(p.gk);
+  D.gx = p.gx;
   const int grid = D.nitems < p.num_sms ? D.nitems : p.num_sms;
   cudaError_t e;
   TimedLaunch t(K_TC_DUAL_REV, s);
-  if (p.decay) {
+  if (p.gC) {
+    if ((e = set_smem(tc_dual_kernel<true, true>, kDualSmem)) != cudaSuccess) return e;
+    tc_dual_kernel<true, true><<<grid, kDualThreads, kDualSmem, s>>>(mk, mq, mv, mdo, D);
+  } else if (p.decay) {
     if ((e = set_smem(tc_dual_kernel<true>, kDualSmem)) != cudaSuccess) return e;
     tc_dual_kernel<true><<<grid, kDualThreads, kDualSmem, s>>>(mk, mq, mv, mdo, D);
   } else {
@@ -1049,7 +1182,7 @@ cudaError_t tc_dual(const Problem &p, int group_len, const void *q, const void *
 cudaError_t tc_main(const Problem &p, int group_len, const void *q, const void *k, const void *v, void *o,
                     const float *group_init, bool init_transposed, float *final_state, int *status,
                     cudaStream_t s, const void *x, float *agg_out) {
-  if (x && (p.decay || !agg_out)) return cudaErrorInvalidValue;
+  if (x && (p.decay || p.gC || !agg_out)) return cudaErrorInvalidValue;
   alignas(64) CUtensorMap mq, mk, mv, mo, mx;
   if (!seq_tmap(p, q, &mq) || !seq_tmap(p, k, &mk) || !seq_tmap(p, v, &mv) || !seq_tmap(p, o, &mo) ||
       !seq_tmap(p, x ? x : q, &mx))
@@ -1061,20 +1194,26 @@ cudaError_t tc_main(const Problem &p, int group_len, const void *q, const void *
   M.init_t = init_transposed ? 1 : 0;
   M.decay = p.decay; M.ginit = group_init; M.final_state = final_state; M.status = status;
   M.agg_out = agg_out;
+  M.gC = p.gC;
+  M.gq = static_cast<const __nv_bfloat16 *>(p.gq);
+  M.gx = p.gx;
+  M.sb = p.sb; M.sh = p.sh; M.st = p.st;
   const int grid = M.nitems < p.num_sms ? M.nitems : p.num_sms;
   cudaError_t e;
   TimedLaunch t(x ? K_TC_MAIN_AGG : K_TC_MAIN_FWD, s);
-#define LINATTN_LAUNCH_MAIN(DEC, AGG)                                                          \
+#define LINATTN_LAUNCH_MAIN(DEC, AGG, GATE)                                                    \
   do {                                                                                        \
-    if ((e = set_smem(tc_main_kernel<DEC, AGG>, kMainSmem)) != cudaSuccess) return e;         \
-    tc_main_kernel<DEC, AGG><<<grid, kThreads, kMainSmem, s>>>(mq, mk, mv, mo, mx, M);        \
+    if ((e = set_smem(tc_main_kernel<DEC, AGG, GATE>, kMainSmem)) != cudaSuccess) return e;   \
+    tc_main_kernel<DEC, AGG, GATE><<<grid, kThreads, kMainSmem, s>>>(mq, mk, mv, mo, mx, M);  \
   } while (0)
   if (x)
-    LINATTN_LAUNCH_MAIN(false, true);
+    LINATTN_LAUNCH_MAIN(false, true, false);
+  else if (p.gC)
+    LINATTN_LAUNCH_MAIN(true, false, true);
   else if (p.decay)
-    LINATTN_LAUNCH_MAIN(true, false);
+    LINATTN_LAUNCH_MAIN(true, false, false);
   else
-    LINATTN_LAUNCH_MAIN(false, false);
+    LINATTN_LAUNCH_MAIN(false, false, false);
 #undef LINATTN_LAUNCH_MAIN
   return cudaGetLastError();
 }

@@ -65,7 +65,8 @@ enum {
 enum { LINATTN_BF16 = 0, LINATTN_F32 = 1 };
 
 /* Workspace / checkpoint queries. */
-enum { LINATTN_OP_FWD = 1, LINATTN_OP_BWD = 2, LINATTN_OP_CHUNK_STATES = 3, LINATTN_OP_CHECKPOINT = 4 };
+enum { LINATTN_OP_FWD = 1, LINATTN_OP_BWD = 2, LINATTN_OP_CHUNK_STATES = 3, LINATTN_OP_CHECKPOINT = 4,
+       LINATTN_OP_FWD_GATED = 5, LINATTN_OP_BWD_GATED = 6, LINATTN_OP_CHECKPOINT_GATED = 7 };
 
 typedef struct {
   int32_t abi_version;  /* must be LINATTN_ABI_VERSION                              */
@@ -144,6 +145,36 @@ int32_t linattn_bwd_ckpt(const linattn_shape *shape, const void *q, const void *
                          const void *dO, const float *init_state, const float *d_final_state,
                          const void *checkpoint, size_t checkpoint_bytes, void *dq, void *dk, void *dv,
                          float *d_init_state, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Data-dependent gates (the gated variant the LASP-2 page names beside the
+ * plain one): a decay alpha_t = exp(log_gate_t) per token and head instead of
+ * the shape's per-head lambda,
+ *   S_t = alpha_t S_{t-1} + k_t v_t^T,   o_t = S_t^T q_t.
+ * log_gate is [B,H,T] fp32, contiguous, 16-byte aligned (log of gates in
+ * (0, 1]: values <= 0; positive values are taken as given but their weights may
+ * overflow).  The shape's decay must be NULL.  Tensor-core path only: bf16,
+ * d = 128 (otherwise LINATTN_ERR_UNSUPPORTED).  The checkpoint (size from
+ * LINATTN_OP_CHECKPOINT_GATED) is required: it keeps every chunk group's
+ * entering state and the final state for linattn_bwd_gated.  Workspace sizes:
+ * LINATTN_OP_FWD_GATED / LINATTN_OP_BWD_GATED.  Returns a status. */
+int32_t linattn_fwd_gated(const linattn_shape *shape, const void *q, const void *k, const void *v,
+                          const float *log_gate, void *o, const float *init_state, float *final_state,
+                          void *checkpoint, size_t checkpoint_bytes, void *workspace, size_t workspace_bytes,
+                          void *stream);
+
+/* Backward of linattn_fwd_gated (same shape, q, k, v, log_gate, init_state and
+ * its checkpoint), for an upstream gradient dO and the gradient d_final_state
+ * arriving at the final state (or NULL): dq, dk, dv as linattn_bwd with every
+ * lambda power replaced by the product of the gates between the two tokens,
+ * d_init_state = alpha_0 R_0, and the gradient of every log-gate
+ *   d_log_gate[t] = sum_{u >= t} (q_u . dq_u - k_u . dk_u)  + <d_final, S_final>
+ * ([B,H,T] fp32, contiguous; derived from dL/d(cumulative log-gate) of the
+ * chunked form).  Returns a status. */
+int32_t linattn_bwd_gated(const linattn_shape *shape, const void *q, const void *k, const void *v,
+                          const void *dO, const float *log_gate, const float *init_state,
+                          const float *d_final_state, const void *checkpoint, size_t checkpoint_bytes, void *dq,
+                          void *dk, void *dv, float *d_log_gate, float *d_init_state, void *workspace,
+                          size_t workspace_bytes, void *stream);
 
 /* Recurrent decode of T new tokens per sequence (constant-memory inference:
  * LASP-2 page, abstract): for t = 0..T-1
@@ -241,7 +272,7 @@ int32_t linattn_device_status(const void *workspace, void *stream);
  * for every kernel kind k < max_kinds its launch count and summed device time
  * (ms), clears the record and returns the number of kinds
  * (LINATTN_KERNEL_KINDS), or a negative status. */
-#define LINATTN_KERNEL_KINDS 10
+#define LINATTN_KERNEL_KINDS 11
 int32_t linattn_timing_enable(int32_t on);
 int32_t linattn_timing_collect(int32_t max_kinds, int32_t *launches, float *total_ms);
 /* Name of kernel kind k (static string; "?" when out of range). */

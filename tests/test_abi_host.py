@@ -128,3 +128,25 @@ def test_chunk_states_and_scan_argument_checks(cdll):
 
 def test_device_status_null(cdll):
     assert la.linattn_device_status(None, None) == la.ERR_INVALID
+
+
+def test_gated_entry_points_check_their_arguments(cdll):
+    s = _shape()
+    ck = 1 << 30  # large enough for any checkpoint size check
+    # fp32 inputs have no gated path
+    assert la.linattn_fwd_gated(_shape(dtype=la.F32), FAKE, FAKE, FAKE, FAKE, FAKE, None, None, FAKE, ck, FAKE,
+                                1 << 30, None) == la.ERR_UNSUPPORTED
+    # the per-head decay and gates exclude each other
+    lam = (ctypes.c_float * 2)(0.9, 0.9)
+    assert la.linattn_fwd_gated(_shape(decay=ctypes.cast(lam, ctypes.c_void_p)), FAKE, FAKE, FAKE,
+                                FAKE, FAKE, None, None, FAKE, ck, FAKE, 1 << 30, None) == la.ERR_INVALID
+    # a checkpoint is required, and the gates
+    assert la.linattn_fwd_gated(s, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None, 0, FAKE, 1 << 30,
+                                None) == la.ERR_INVALID
+    assert la.linattn_fwd_gated(s, FAKE, FAKE, FAKE, None, FAKE, None, None, FAKE, ck, FAKE, 1 << 30,
+                                None) == la.ERR_INVALID
+    assert la.linattn_bwd_gated(s, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, FAKE, ck, FAKE, FAKE, FAKE, None,
+                                None, FAKE, 1 << 30, None) == la.ERR_INVALID
+    for op in (la.OP_FWD_GATED, la.OP_BWD_GATED, la.OP_CHECKPOINT_GATED):
+        st, n = la.linattn_workspace_size(s, op)
+        assert st == la.OK and n >= 256

@@ -1,0 +1,85 @@
+"""Data-dependent gates (linattn_fwd_gated / linattn_bwd_gated) against the
+fp64 oracle, through the C ABI: several chunk groups, ragged tails, initial
+state and final-state gradient, mild and strong gates, and the reduction to
+the per-head decay when every gate of a head is the same.  Tolerance as in
+test_gpu_parity (1e-2 of max|ref| per tensor for bf16 inputs)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import chunked_state_scan_causal_gb300 as la
+from chunked_state_scan_causal_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-2
+
+
+def rel(got, ref):
+    got = got.detach().double().cpu().numpy() if torch.is_tensor(got) else got
+    return float(np.max(np.abs(got - ref))) / max(float(np.max(np.abs(ref))), 1e-30)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from chunked_state_scan_causal_gb300 import build
+    build.build()
+
+
+def case(seed, B, H, T, lo):
+    c = inputs.random_case(seed, B, H, T, 128, dtype="bf16", sigma=1 / np.sqrt(128))
+    dev = {k: torch.from_numpy(np.ascontiguousarray(v)).to(torch.bfloat16).cuda() for k, v in c.items()}
+    lg = np.random.default_rng(seed + 1).uniform(lo, 0.0, (B, H, T)).astype(np.float32)
+    return c, dev, lg
+
+
+def f32(a):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()
+
+
+@pytest.mark.parametrize("T,lo", [(200, -0.05), (2048 + 64, -0.05), (8192 + 100, -0.02), (1000, -1.0)])
+def test_gated_forward_and_backward(T, lo):
+    B, H = 1, 3
+    c, dev, lg = case(T, B, H, T, lo)
+    r = np.random.default_rng(T + 7)
+    init = (0.1 * r.standard_normal((B, H, 128, 128))).astype(np.float32).astype(np.float64)
+    D = (0.1 * r.standard_normal((B, H, 128, 128))).astype(np.float32).astype(np.float64)
+    ck = la.checkpoint_gated(dev["q"])
+    wsf, wsb = la.workspace(dev["q"], la.OP_FWD_GATED), la.workspace(dev["q"], la.OP_BWD_GATED)
+    o, fin = la.fwd_gated(dev["q"], dev["k"], dev["v"], f32(lg), ck, init_state=f32(init), want_final=True, ws=wsf)
+    dq, dk, dv, dlg, dinit = la.bwd_gated(dev["q"], dev["k"], dev["v"], dev["dO"], f32(lg), ck, init_state=f32(init),
+                                          d_final=f32(D), want_dinit=True, ws=wsb)
+    assert la.device_status(wsf) == la.OK and la.device_status(wsb) == la.OK
+    lg64 = lg.astype(np.float64)
+    ro, rfin = oracle.fwd_gated(c["q"], c["k"], c["v"], lg64, init=init)
+    rq, rk, rv, rlg, rinit = oracle.bwd_gated(c["q"], c["k"], c["v"], c["dO"], lg64, init=init, d_final=D)
+    for name, got, ref in (("o", o, ro), ("final", fin, rfin), ("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv),
+                           ("d_log_gate", dlg, rlg), ("d_init", dinit, rinit)):
+        assert rel(got, ref) < TOL, (name, rel(got, ref))
+
+
+def test_constant_gates_match_the_per_head_decay():
+    B, H, T = 1, 2, 3000
+    c, dev, _ = case(5, B, H, T, -0.1)
+    lam = inputs.decay_per_head(H)
+    lg = np.broadcast_to(np.log(lam.astype(np.float64))[None, :, None], (B, H, T)).astype(np.float32)
+    ck = la.checkpoint_gated(dev["q"])
+    o, _ = la.fwd_gated(dev["q"], dev["k"], dev["v"], f32(lg), ck)
+    o2, _, _ = la.fwd(dev["q"], dev["k"], dev["v"], decay=torch.from_numpy(lam).cuda())
+    dq, dk, dv, _, _ = la.bwd_gated(dev["q"], dev["k"], dev["v"], dev["dO"], f32(lg), ck)
+    dq2, dk2, dv2, _ = la.bwd(dev["q"], dev["k"], dev["v"], dev["dO"], decay=torch.from_numpy(lam).cuda())
+    torch.cuda.synchronize()
+    for a, b in ((o, o2), (dq, dq2), (dk, dk2), (dv, dv2)):
+        assert rel(a, b.double().cpu().numpy()) < TOL
+
+
+def test_gated_empty_sequence():
+    z = torch.empty((1, 2, 0, 128), dtype=torch.bfloat16, device="cuda")
+    lg = torch.empty((1, 2, 0), dtype=torch.float32, device="cuda")
+    D = torch.randn(1, 2, 128, 128, device="cuda")
+    init = torch.randn(1, 2, 128, 128, device="cuda")
+    ck = la.checkpoint_gated(z)
+    _, fin = la.fwd_gated(z, z, z, lg, ck, init_state=init, want_final=True)
+    _, _, _, _, dinit = la.bwd_gated(z, z, z, z, lg, ck, d_final=D, want_dinit=True)
+    torch.cuda.synchronize()
+    assert torch.equal(fin, init) and torch.equal(dinit, D)

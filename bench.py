@@ -176,10 +176,18 @@ def run_reference(args):
     lam = inputs.workload_decay(cfg)
     lam_s = None if lam is None else lam[heads]
     x = {w: np.stack([inputs.make_head64(cfg, w, 0, h) for h in heads])[None] for w in ("q", "k", "v", "dO")}
+    gates = None
+    if cfg.get("gates") is not None:
+        gates = np.stack([inputs.gate_head(cfg, 0, h) for h in heads])[None].astype(np.float64)
 
     def run(n):
-        oracle.fwd_recurrent(x["q"][:, :, :n], x["k"][:, :, :n], x["v"][:, :, :n], lam=lam_s)
-        oracle.bwd_recurrent(x["q"][:, :, :n], x["k"][:, :, :n], x["v"][:, :, :n], x["dO"][:, :, :n], lam=lam_s)
+        xs = [x[w][:, :, :n] for w in ("q", "k", "v", "dO")]
+        if gates is not None:
+            oracle.fwd_gated(*xs[:3], gates[:, :, :n])
+            oracle.bwd_gated(*xs, gates[:, :, :n])
+            return
+        oracle.fwd_recurrent(*xs[:3], lam=lam_s)
+        oracle.bwd_recurrent(*xs, lam=lam_s)
 
     # each step is the first T_s tokens of every sampled head, T_s sized so that the
     # whole run (warm-up + timed steps) takes about --ref-budget seconds
@@ -234,21 +242,40 @@ def run_ours(args):
     lam = inputs.workload_decay(cfg)
 
     # inputs: seeded on the host, pinned, copied once (the device-resident leg)
+    gated = cfg.get("gates") is not None
     host = {w: inputs.make(cfg, w).pin_memory() for w in ("q", "k", "v", "dO")}
+    if gated:
+        host["log_gate"] = inputs.make_gates(cfg).pin_memory()
     x = {w: t.to(dev, non_blocking=True) for w, t in host.items()}
     decay = None if lam is None else torch.from_numpy(lam).to(dev)
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream(dev)
-    o = torch.empty_like(x["q"])
-    grads = [torch.empty_like(x["q"]) for _ in range(3)]
-    ws_f = la.workspace(x["q"], la.OP_FWD, decay)
-    ws_b = la.workspace(x["q"], la.OP_BWD, decay)
-    ck = la.checkpoint(x["q"], decay)
+
+    def buffers():
+        """Outputs, workspaces and the forward's checkpoint of one step."""
+        b = dict(o=torch.empty_like(x["q"]), g=[torch.empty_like(x["q"]) for _ in range(3)])
+        if gated:
+            b.update(wsf=la.workspace(x["q"], la.OP_FWD_GATED), wsb=la.workspace(x["q"], la.OP_BWD_GATED),
+                     ck=la.checkpoint_gated(x["q"]), dlg=torch.empty_like(x["log_gate"]))
+        else:
+            b.update(wsf=la.workspace(x["q"], la.OP_FWD, decay), wsb=la.workspace(x["q"], la.OP_BWD, decay),
+                     ck=la.checkpoint(x["q"], decay))
+        return b
+
+    def layer(xs, b):
+        # a training step of the layer: forward keeping its group states, then backward
+        if gated:
+            la.fwd_gated(xs["q"], xs["k"], xs["v"], xs["log_gate"], b["ck"], out=b["o"], ws=b["wsf"])
+            la.bwd_gated(xs["q"], xs["k"], xs["v"], xs["dO"], xs["log_gate"], b["ck"], outs=b["g"], ws=b["wsb"],
+                         dlg_out=b["dlg"])
+        else:
+            la.fwd(xs["q"], xs["k"], xs["v"], decay=decay, out=b["o"], ws=b["wsf"], ckpt=b["ck"])
+            la.bwd(xs["q"], xs["k"], xs["v"], xs["dO"], decay=decay, outs=b["g"], ws=b["wsb"], ckpt=b["ck"])
+
+    main_buf = buffers()
 
     def step():
-        # a training step of the layer: forward keeping its group states, then backward
-        la.fwd(x["q"], x["k"], x["v"], decay=decay, out=o, ws=ws_f, ckpt=ck)
-        la.bwd(x["q"], x["k"], x["v"], x["dO"], decay=decay, outs=grads, ws=ws_b, ckpt=ck)
+        layer(x, main_buf)
 
     def barrier():
         if ws_n > 1:
@@ -258,7 +285,7 @@ def run_ours(args):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
-    if la.device_status(ws_b) != la.OK or la.device_status(ws_f) != la.OK:
+    if la.device_status(main_buf["wsb"]) != la.OK or la.device_status(main_buf["wsf"]) != la.OK:
         raise RuntimeError("device-side error during warm-up")
 
     # ---- timed region (inputs are 512 MiB per tensor, 4x larger than L2: no flush needed)
@@ -280,7 +307,8 @@ def run_ours(args):
     tokens_step = B * T * ws_n
     value = whole_job_throughput(B * T, ms, ws_n)
     flops = (FLOP_FWD + FLOP_BWD) * B * H * T
-    bytes_ = (BYTES_FWD + BYTES_BWD) * B * H * T
+    # gates add a 4-byte log-gate read to each pass and the 4-byte gate gradient written
+    bytes_ = (BYTES_FWD + BYTES_BWD + (12 if gated else 0)) * B * H * T
     hbm, tf, peak_src = _peaks()
 
     # ---- dominant kernels' roofline: the chunked tensor-core kernels (the forward-time
@@ -321,11 +349,11 @@ def run_ours(args):
         slots = []
         for _ in range(2):
             xin = {w: torch.empty_like(x[w]) for w in x}
-            outs = [torch.empty_like(x["q"]) for _ in range(4)]
-            hout = [torch.empty(x["q"].shape, dtype=x["q"].dtype, pin_memory=True) for _ in range(4)]
+            b = buffers()
+            outs = [b["o"]] + b["g"] + ([b["dlg"]] if gated else [])
+            hout = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
             ev = {n: torch.cuda.Event() for n in ("in", "comp", "out")}
-            slots.append(dict(x=xin, o=outs, h=hout, ev=ev, used=False, ck=la.checkpoint(x["q"], decay),
-                              wsf=la.workspace(x["q"], la.OP_FWD, decay), wsb=la.workspace(x["q"], la.OP_BWD, decay)))
+            slots.append(dict(x=xin, b=b, o=outs, h=hout, ev=ev, used=False))
         s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
         h2d = sum(t.numel() * t.element_size() for t in host.values())
         d2h = sum(t.numel() * t.element_size() for t in slots[0]["h"])
@@ -341,9 +369,7 @@ def run_ours(args):
             stream.wait_event(sl["ev"]["in"])
             if sl["used"]:
                 stream.wait_event(sl["ev"]["out"])         # previous results of this slot copied out
-            xs, (o_, dq_, dk_, dv_) = sl["x"], sl["o"]
-            la.fwd(xs["q"], xs["k"], xs["v"], decay=decay, out=o_, ws=sl["wsf"], ckpt=sl["ck"])
-            la.bwd(xs["q"], xs["k"], xs["v"], xs["dO"], decay=decay, outs=[dq_, dk_, dv_], ws=sl["wsb"], ckpt=sl["ck"])
+            layer(sl["x"], sl["b"])
             sl["ev"]["comp"].record(stream)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(sl["ev"]["comp"])
@@ -376,8 +402,13 @@ def run_ours(args):
               for w in ("q", "k", "v", "dO")}
         lam_s = None if lam is None else lam[heads]
         t0 = time.perf_counter()
-        oracle.fwd_recurrent(xs["q"], xs["k"], xs["v"], lam=lam_s)
-        oracle.bwd_recurrent(xs["q"], xs["k"], xs["v"], xs["dO"], lam=lam_s)
+        if gated:
+            gs = np.stack([inputs.gate_head(cfg, 0, h) for h in heads])[None].astype(np.float64)
+            oracle.fwd_gated(xs["q"], xs["k"], xs["v"], gs)
+            oracle.bwd_gated(xs["q"], xs["k"], xs["v"], xs["dO"], gs)
+        else:
+            oracle.fwd_recurrent(xs["q"], xs["k"], xs["v"], lam=lam_s)
+            oracle.bwd_recurrent(xs["q"], xs["k"], xs["v"], xs["dO"], lam=lam_s)
         sec = time.perf_counter() - t0
         cpu = {"value": T * len(heads) / H / sec, "unit": "tokens/s", "cores": oracle.threads_used(),
                "kind": "oracle",
@@ -390,7 +421,7 @@ def run_ours(args):
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded normal; no dataset)",
             "config": {"workload": cfg["name"], "B": B, "H": H, "T": T, "d": d, "chunk": 64,
-                       "decay": "per-head" if lam is not None else "none",
+                       "decay": "per-head" if lam is not None else ("per-token gates" if gated else "none"),
                        "l2": "inputs 512 MiB per tensor > L2 (no flush)",
                        "step": "linattn_fwd_ckpt + linattn_bwd_ckpt", "parallelism": f"replicas x{ws_n}"},
             "tflops": flops / (ms * 1e-3) / 1e12,

@@ -394,7 +394,7 @@ def fwd_gated(q, k, v, log_gate, ckpt, init_state=None, want_final=False, out=No
 
 
 def bwd_gated(q, k, v, dO, log_gate, ckpt, init_state=None, d_final=None, want_dinit=False, outs=None, ws=None,
-              stream=None):
+              stream=None, dlg_out=None):
     """(dq, dk, dv, d_log_gate, d_init or None) of fwd_gated for the upstream gradient dO."""
     import torch
     _same_layout(q, k, v, dO)
@@ -403,7 +403,7 @@ def bwd_gated(q, k, v, dO, log_gate, ckpt, init_state=None, d_final=None, want_d
     if outs is None:
         outs = [torch.empty_strided(q.shape, q.stride(), dtype=q.dtype, device=q.device) for _ in range(3)]
     dq, dk, dv = outs
-    dlg = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
+    dlg = dlg_out if dlg_out is not None else torch.empty((B, H, T), dtype=torch.float32, device=q.device)
     dinit = torch.empty((B, H, d, d), dtype=torch.float32, device=q.device) if want_dinit else None
     shape = shape_of(q, None)
     if ws is None:

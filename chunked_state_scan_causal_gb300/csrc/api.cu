@@ -182,11 +182,11 @@ static size_t ckpt_bytes(const Problem &p) {
 
 // Gated layouts: the forward layout plus the gates' cumulative sums [BH][T] and
 // group totals [G][BH]; the backward adds the reverse aggregates, the reverse
-// group states and the gate-gradient scratch.  The gated checkpoint holds the
+// group states and the per-token q . dq - k . dk of the gate gradient.  The gated checkpoint holds the
 // group states and then the final state.
 struct GatedLayout {
   FwdLayout f;
-  size_t C = 0, tot = 0, wagg = 0, rbar = 0, gsum = 0, dot = 0, gx = 0, fwd_total = kHeader, bwd_total = kHeader;
+  size_t C = 0, tot = 0, wagg = 0, rbar = 0, gx = 0, fwd_total = kHeader, bwd_total = kHeader;
 };
 static GatedLayout gated_layout(const Problem &p) {
   GatedLayout w;
@@ -199,9 +199,7 @@ static GatedLayout gated_layout(const Problem &p) {
   w.fwd_total = w.tot + align256((size_t)w.f.G * BH * sizeof(float));
   w.wagg = w.fwd_total;
   w.rbar = w.wagg + align256(st);
-  w.gsum = w.rbar + align256(st);
-  w.dot = w.gsum + align256((size_t)w.f.G * BH * sizeof(float));
-  w.gx = w.dot + align256((size_t)BH * sizeof(float));
+  w.gx = w.rbar + align256(st);
   w.bwd_total = w.gx + align256((size_t)BH * p.T * sizeof(float));
   return w;
 }
@@ -520,8 +518,7 @@ int32_t linattn_bwd_gated(const linattn_shape *shape, const void *q, const void 
     e = cudaMemcpyAsync(rbar + (int64_t)(G - 1) * E, d_final_state, state_bytes, cudaMemcpyDeviceToDevice, s);
   if (e == cudaSuccess) e = tc_dual(p, L, q, k, v, dO, dk, dv, rbar, status, s);
   if (e == cudaSuccess)
-    e = gate_grad(p, L, p.gx, d_final_state, fin, reinterpret_cast<float *>(ws + w.gsum),
-                  reinterpret_cast<float *>(ws + w.dot), d_log_gate, s);
+    e = gate_grad(p, L, p.gx, rbar, states, d_final_state, fin, d_log_gate, s);
   return cuda_status(e);
 }
 

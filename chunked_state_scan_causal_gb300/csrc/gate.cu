@@ -14,8 +14,8 @@
 // with dq, dk the gradients of the backward (dk includes the part that reaches
 // the final state's gradient D).  The two dot products are taken by the dq
 // and dk/dv passes from their fp32 results before these are rounded to the
-// output dtype: summed over a long sequence, terms from rounded dq, dk would
-// carry the rounding of every token.
+// output dtype, and the sums run inside one chunk group, each anchored at the
+// exact value at the next group's start (dgate_kernel).
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -57,15 +57,41 @@ __global__ void fold_log2_kernel(float *w, const float *d, const float *tot, int
 }
 
 // One block of 256 threads per (sequence, group): the reverse inclusive sums of
-// gx inside the group, walked from the end in tiles of 256 tokens;
-// gsum[g][bh] = the group's total.
-__global__ void __launch_bounds__(256) dgate_local_kernel(int T, int L, int G, int BH, const float *gx, float *dlg,
-                                                          float *gsum) {
+// gx inside the group, walked from the end in tiles of 256 tokens, plus the
+// exact value of the sum over everything after the group:
+//     sum_{t > group end} dL/dG_t = dL/dg at the next group's first token
+//       = alpha R at that token . S before it = <Rbar_g, S_{g+1}>,
+// Rbar_g the reverse state at the group's end (what the dk/dv pass starts
+// from) and S_{g+1} the forward state entering the next group (checkpoint);
+// for the last group it is <D, S_final> (or 0).  Anchoring each group at an
+// exact value keeps the sums short: a running sum over the whole sequence
+// would accumulate the errors of every later token.
+__global__ void __launch_bounds__(256) dgate_kernel(int T, int L, int G, int BH, int DD, const float *gx,
+                                                    const float *rbar, const float *states, const float *D,
+                                                    const float *Sfin, float *dlg) {
   __shared__ float wsum[8];
   const int bh = blockIdx.x / G, g = blockIdx.x % G;
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
-  const int s0 = g * L, s1 = min(T, s0 + L);
+  // the anchor: <Rbar_g, S_{g+1}> or <D, S_final>
+  const float *a = nullptr, *b = nullptr;
+  if (g + 1 < G) {
+    a = rbar + ((int64_t)g * BH + bh) * DD;
+    b = states + ((int64_t)(g + 1) * BH + bh) * DD;
+  } else if (D) {
+    a = D + (int64_t)bh * DD;
+    b = Sfin + (int64_t)bh * DD;
+  }
+  float acc = 0.f;
+  if (a)
+    for (int i = threadIdx.x; i < DD; i += 256) acc = fmaf(a[i], b[i], acc);
+#pragma unroll
+  for (int m = 16; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+  if (lane == 0) wsum[warp] = acc;
+  __syncthreads();
   float carry = 0.f;
+  for (int w2 = 0; w2 < 8; ++w2) carry += wsum[w2];
+  __syncthreads();
+  const int s0 = g * L, s1 = min(T, s0 + L);
   for (int te = s1; te > s0; te -= 256) {
     const int ts = max(s0, te - 256), n = te - ts;
     float v = (int)threadIdx.x < n ? gx[(int64_t)bh * T + ts + threadIdx.x] : 0.f;
@@ -86,34 +112,6 @@ __global__ void __launch_bounds__(256) dgate_local_kernel(int T, int L, int G, i
     carry += tile;
     __syncthreads();  // wsum is rewritten by the next tile
   }
-  if (threadIdx.x == 0) gsum[(int64_t)g * BH + bh] = carry;
-}
-
-// <D, S_final> per sequence (d^2 elements, one block per sequence).
-__global__ void __launch_bounds__(256) dot_state_kernel(const float *D, const float *S, int DD, float *out) {
-  __shared__ float red[8];
-  const int bh = blockIdx.x;
-  float acc = 0.f;
-  for (int i = threadIdx.x; i < DD; i += 256) acc = fmaf(D[(int64_t)bh * DD + i], S[(int64_t)bh * DD + i], acc);
-#pragma unroll
-  for (int m = 16; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x / 32] = acc;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float s = 0.f;
-    for (int w = 0; w < 8; ++w) s += red[w];
-    out[bh] = s;
-  }
-}
-
-// dlg[t] += sum of the totals of the later groups (+ <D, S_final>).
-__global__ void __launch_bounds__(256) dgate_fix_kernel(int T, int L, int G, int BH, const float *gsum,
-                                                        const float *dot, float *dlg) {
-  const int bh = blockIdx.x / G, g = blockIdx.x % G;
-  float off = dot ? dot[bh] : 0.f;
-  for (int g2 = g + 1; g2 < G; ++g2) off += gsum[(int64_t)g2 * BH + bh];
-  const int s0 = g * L, s1 = min(T, s0 + L);
-  for (int t = s0 + threadIdx.x; t < s1; t += 256) dlg[(int64_t)bh * T + t] += off;
 }
 
 }  // namespace
@@ -133,18 +131,11 @@ cudaError_t fold_state_log2(float *w, const float *d, const float *tot_last, int
   return cudaGetLastError();
 }
 
-cudaError_t gate_grad(const Problem &p, int L, const float *gx, const float *d_final, const float *final_state,
-                      float *gsum, float *dot, float *dlg, cudaStream_t s) {
+cudaError_t gate_grad(const Problem &p, int L, const float *gx, const float *rbar, const float *states,
+                      const float *d_final, const float *final_state, float *dlg, cudaStream_t s) {
   const int G = (p.T + L - 1) / L, BH = p.B * p.H;
   TimedLaunch t(K_GATE, s);
-  dgate_local_kernel<<<BH * G, 256, 0, s>>>(p.T, L, G, BH, gx, dlg, gsum);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  if (d_final) {
-    dot_state_kernel<<<BH, 256, 0, s>>>(d_final, final_state, p.d * p.d, dot);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
-  dgate_fix_kernel<<<BH * G, 256, 0, s>>>(p.T, L, G, BH, gsum, d_final ? dot : nullptr, dlg);
+  dgate_kernel<<<BH * G, 256, 0, s>>>(p.T, L, G, BH, p.d * p.d, gx, rbar, states, d_final, final_state, dlg);
   return cudaGetLastError();
 }
 

@@ -76,10 +76,10 @@ cudaError_t fold_state(float *w, const float *d, const float *decay_h, int H, in
 cudaError_t gate_prep(const Problem &p, int L, const float *log_gate, float *C, float *tot, cudaStream_t s);
 // w[i] += exp2(tot_last[i / DD]) d[i], n elements.
 cudaError_t fold_state_log2(float *w, const float *d, const float *tot_last, int DD, int64_t n, cudaStream_t s);
-// d_log_gate [B,H,T]: reverse sums over each sequence of gx [B*H][T] (q_t . dq_t - k_t . dk_t)
-// and, with d_final, <d_final, final_state>; gsum [G][BH] and dot [BH] are scratch.
-cudaError_t gate_grad(const Problem &p, int L, const float *gx, const float *d_final, const float *final_state,
-                      float *gsum, float *dot, float *dlg, cudaStream_t s);
+// d_log_gate [B,H,T]: reverse sums of gx [B*H][T] (q_t . dq_t - k_t . dk_t) inside each
+// group, plus <rbar[g], states[g+1]> (<d_final, final_state> for the last group).
+cudaError_t gate_grad(const Problem &p, int L, const float *gx, const float *rbar, const float *states,
+                      const float *d_final, const float *final_state, float *dlg, cudaStream_t s);
 
 // ---------------------------------------------------------------- tensor-core path (tc.cu)
 bool tc_supported(const Problem &p);   // bf16, d = 128

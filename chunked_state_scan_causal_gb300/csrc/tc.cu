@@ -624,6 +624,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&bar[B_PRE]);
       }
       for (int n = 0; n < nb; ++n, ++blk) {
+        if (n == (nb > 1 ? nb - 2 : 0) && item + (int)gridDim.x < P.nitems) {
+          // the next item's entering state: this thread's 512-byte row, into L2 ahead of its load
+          const int nx = item + (int)gridDim.x;
+          const float *nsrc = P.ginit + ((int64_t)(nx / BH) * BH + nx % BH) * 16384 + row * 128;
+#pragma unroll
+          for (int m = 0; m < 4; ++m) prefetch_l2(nsrc + 32 * m);
+        }
         if (DECAY) {
           // key rows k_j *= lambda^{nv-1-j} (gates: exp2(C_last - C_j)) once the scores have read them
           const int nv = nvalid(n), r = (int)row, t0 = s0 + 128 * n;
@@ -1014,6 +1021,13 @@ __global__ void __launch_bounds__(kDualThreads, 1)
         mbar_arrive(&bar[D_PRE]);
       }
       for (int n = 0; n < nb && ok; ++n, ++blk) {
+        if (n == (nb > 1 ? nb - 2 : 0) && item + (int)gridDim.x < P.nitems) {
+          // the next item's entering state: this thread's 512-byte row, into L2 ahead of its load
+          const int nx = item + (int)gridDim.x;
+          const float *nsrc = P.ginit + ((int64_t)(nx / BH) * BH + nx % BH) * 16384 + row * 128;
+#pragma unroll
+          for (int m = 0; m < 4; ++m) prefetch_l2(nsrc + 32 * m);
+        }
         if (DECAY) {
           const int nv = nvalid(n), r = (int)row;
           float wx = 0.f, wy = 0.f;  // rows of K and V; rows of dO

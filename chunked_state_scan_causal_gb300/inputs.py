@@ -20,7 +20,7 @@ from concurrent.futures import ThreadPoolExecutor
 import numpy as np
 import torch
 
-TENSOR_ID = {"q": 0, "k": 1, "v": 2, "dO": 3}
+TENSOR_ID = {"q": 0, "k": 1, "v": 2, "dO": 3}  # 4: the log-gates of a gated workload
 
 # The five workloads.  "sigma" is the std-dev of q, k, v; dO is always N(0, 1).
 WORKLOADS = {
@@ -35,6 +35,10 @@ WORKLOADS = {
     5: dict(name="segmented-B1H16T1M-d128-64x16K", B=1, H=16, T=1 << 20, d=128, dtype="bf16",
             decay=None, dist="normal", sigma=1.0 / math.sqrt(128), seed=4, passes="segments",
             seg_len=16384),
+    # data-dependent gates: log_gate ~ U(-1/16, 0) per token and head (gates in [0.94, 1])
+    6: dict(name="fwdbwd-gated-B1H32T128K-d128", B=1, H=32, T=131072, d=128, dtype="bf16",
+            decay=None, dist="normal", sigma=1.0 / math.sqrt(128), seed=5, passes="fwd+bwd",
+            gates=(-1.0 / 16, 0.0)),
 }
 
 
@@ -42,6 +46,26 @@ def decay_per_head(H: int) -> np.ndarray:
     """lambda_h = 1 - 2^-(5 + 8h/32) for h = 0..H-1 (float64 math, one rounding to float32)."""
     h = np.arange(H, dtype=np.float64)
     return (1.0 - np.power(2.0, -(5.0 + 8.0 * h / 32.0))).astype(np.float32)
+
+
+def gate_head(cfg: dict, b: int, h: int, T: int | None = None) -> np.ndarray:
+    """log-gates of one head, float32 [T] (uniform in cfg["gates"]), or None without gates."""
+    if cfg.get("gates") is None:
+        return None
+    T = cfg["T"] if T is None else T
+    lo, hi = cfg["gates"]
+    ss = np.random.SeedSequence([cfg["seed"], 4, b, h])
+    return np.random.Generator(np.random.PCG64(ss)).uniform(lo, hi, T).astype(np.float32)
+
+
+def make_gates(cfg: dict, T: int | None = None, B: int | None = None, H: int | None = None, device=None):
+    """log-gates [B, H, T] float32 of a gated workload (None without gates)."""
+    if cfg.get("gates") is None:
+        return None
+    B = cfg["B"] if B is None else B
+    H = cfg["H"] if H is None else H
+    g = np.stack([np.stack([gate_head(cfg, b, h, T) for h in range(H)]) for b in range(B)])
+    return torch.from_numpy(g).to(device) if device is not None else torch.from_numpy(g)
 
 
 def workload_decay(cfg: dict):

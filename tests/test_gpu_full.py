@@ -115,3 +115,26 @@ def test_workload5_segmented_equals_single_and_oracle():
         assert rel(init[:, h], rS[:, 0, i]) < 1e-2
         assert rel(o_one[0, h], ro[0, i]) < 1e-2
         assert rel(o_seg[:, h].reshape(T, d), ro[0, i]) < 1e-2
+
+
+def test_workload6_gated_forward_backward_full_size():
+    """Per-token gates at full size (B1 H32 T131072): checkpointed gated forward and
+    backward, three sampled heads against the fp64 oracle."""
+    cfg = inputs.WORKLOADS[6]
+    x = load(cfg, ("q", "k", "v", "dO"))
+    lg = inputs.make_gates(cfg).cuda()
+    ck = la.checkpoint_gated(x["q"])
+    wsf, wsb = la.workspace(x["q"], la.OP_FWD_GATED), la.workspace(x["q"], la.OP_BWD_GATED)
+    o, _ = la.fwd_gated(x["q"], x["k"], x["v"], lg, ck, ws=wsf)
+    dq, dk, dv, dlg, _ = la.bwd_gated(x["q"], x["k"], x["v"], x["dO"], lg, ck, ws=wsb)
+    assert la.device_status(wsf) == la.OK and la.device_status(wsb) == la.OK
+    H = cfg["H"]
+    pairs = [(0, 0), (0, H - 1), (0, H // 2)]
+    ref = heads64(cfg, pairs, ("q", "k", "v", "dO"))
+    g64 = np.stack([inputs.gate_head(cfg, b, h) for b, h in pairs])[None].astype(np.float64)
+    ro, _ = oracle.fwd_gated(ref["q"], ref["k"], ref["v"], g64)
+    rq, rk, rv, rlg, _ = oracle.bwd_gated(ref["q"], ref["k"], ref["v"], ref["dO"], g64)
+    for i, (b, h) in enumerate(pairs):
+        for name, got, r in (("o", o, ro), ("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
+            assert rel(got[b, h], r[0, i]) < 1e-2, (name, b, h)
+        assert rel(dlg[b, h], rlg[0, i]) < 1e-2, ("d_log_gate", b, h)

@@ -256,7 +256,7 @@ constexpr int kSlots = 5;
 constexpr uint32_t kOffPs = kSlots * kTileBytes;          // P (then O staging) tile
 constexpr uint32_t kOffSh = kOffPs + kTileBytes;          // bf16 state tile
 constexpr uint32_t kOffBar = kOffSh + kTileBytes;
-constexpr uint32_t kOffGate = kOffBar + 256;               // GATE: 2 x 128 cumulative sums of a block
+constexpr uint32_t kOffGate = kOffBar + 256;               // GATE: a block's 128 sums, 128 column factors
 constexpr size_t kMainSmem = kOffGate + 1024 + 1024;
 
 // barrier indices
@@ -299,17 +299,50 @@ __device__ __forceinline__ void mask_chunk(float (&x)[32], int i, int c, float l
   }
 }
 
+// Cumulative gate sums of token t0 + r of a block of nv valid tokens (rows past
+// the end take the last valid one: finite weights for zero rows).
+__device__ __forceinline__ float gate_c(const float *gc, int t0, int r, int nv) {
+  return gc[t0 + (r < nv ? r : nv - 1)];
+}
+
 // Gated mask of one 32-column chunk of a score row i: keep j <= i (causal) or
 // j >= i (anti-causal) and weight by exp2(C_i - C_j) (exp2(C_j - C_i)), with cb
-// the block's 128 cumulative sums; the exponent is <= 0 for gates <= 1.
+// the block's 128 cumulative sums.  The weight factors through the chunk's
+// middle column m: exp2(C_i - C_m) per row times the column factor
+// cw[j] = exp2(C_m - C_j) (anti-causal: exp2(C_m - C_i) and exp2(C_j - C_m)),
+// one exponential per row and chunk instead of one per element.  Both factors
+// stay within 2^+-100 when the chunk's sums span at most 100 (kept entries: the
+// product is the weight, <= 1); a wider span (very small gates) takes the
+// per-element form.  Entries outside the mask are set, never multiplied.
 template <bool REV>
-__device__ __forceinline__ void mask_chunk_gate(float (&x)[32], int i, int c, float ci, const float *cb) {
+__device__ __forceinline__ void mask_chunk_gate(float (&x)[32], int i, int c, float ci, const float *cb,
+                                                const float *cw) {
+  const int j0 = c * 32;
+  if (fabsf(cb[j0] - cb[j0 + 31]) <= 100.f) {
+    const float cm = cb[j0 + 16];
+    const float rf = exp2f(REV ? cm - ci : ci - cm);
 #pragma unroll
-  for (int jj = 0; jj < 32; ++jj) {
-    const int j = c * 32 + jj;
-    const bool keep = REV ? (j >= i) : (j <= i);
-    x[jj] = keep ? x[jj] * exp2f(REV ? cb[j] - ci : ci - cb[j]) : 0.f;
+    for (int jj = 0; jj < 32; ++jj) {
+      const int j = j0 + jj;
+      const bool keep = REV ? (j >= i) : (j <= i);
+      x[jj] = keep ? x[jj] * (rf * cw[j]) : 0.f;
+    }
+  } else {
+#pragma unroll
+    for (int jj = 0; jj < 32; ++jj) {
+      const int j = j0 + jj;
+      const bool keep = REV ? (j >= i) : (j <= i);
+      x[jj] = keep ? x[jj] * exp2f(REV ? cb[j] - ci : ci - cb[j]) : 0.f;
+    }
   }
+}
+
+// Column factor of token r of a block (see mask_chunk_gate): exp2(C_m - C_r),
+// or exp2(C_r - C_m) for the anti-causal mask, m the middle of r's chunk.
+template <bool REV>
+__device__ __forceinline__ float gate_colw(const float *gc, int t0, int r, int nv) {
+  const float cr = gate_c(gc, t0, r, nv), cm = gate_c(gc, t0, (r & ~31) + 16, nv);
+  return exp2f(REV ? cr - cm : cm - cr);
 }
 
 // sum_j x[j] * y[j] for 32 fp32 x and 32 bf16 y at src (64 contiguous bytes).
@@ -329,11 +362,6 @@ __device__ __forceinline__ float dot32_bf16(const float (&x)[32], const __nv_bfl
   return acc;
 }
 
-// Cumulative gate sums of token t0 + r of a block of nv valid tokens (rows past
-// the end take the last valid one: finite weights for zero rows).
-__device__ __forceinline__ float gate_c(const float *gc, int t0, int r, int nv) {
-  return gc[t0 + (r < nv ? r : nv - 1)];
-}
 
 // With a decay the inter-block term goes to the fourth TMEM region from the
 // unweighted q (O_inter = Q S) and the epilogue adds lambda^{i+1} O_inter to
@@ -516,11 +544,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int n = 0; n < nb; ++n, ++blk) {
         const int t0 = s0 + 128 * n, nv = min(128, s1 - t0);
         float ci = 0.f, cprev = 0.f;
-        float *cb = reinterpret_cast<float *>(smem + kOffGate) + 128 * (blk & 1);
+        // one buffer of sums and column factors: the previous block's readers passed
+        // the output-store barrier of that block before this write
+        float *cb = reinterpret_cast<float *>(smem + kOffGate), *cw = cb + 128;
         if (GATE) {
           ci = gate_c(gc, t0, (int)row, nv);
           cprev = t0 > s0 ? gc[t0 - 1] : 0.f;
           cb[row] = ci;  // read by the whole group after the barrier below
+          cw[row] = gate_colw<false>(gc, t0, (int)row, nv);
+        }
+        if (GATE && P.gx && (int)row < nv) {
+          // the q row for the epilogue's q . dq: two 128-byte lines into L1 now
+          const __nv_bfloat16 *qr = P.gq + (int64_t)b * P.sb + (int64_t)h * P.sh + (int64_t)(t0 + (int)row) * P.st;
+          prefetch_l1(qr);
+          prefetch_l1(qr + 64);
         }
         ok = group_all(mbar_wait(&bar[B_PFULL], blk & 1, &abort_flag, P.status, detail), 2, 128);
         if (!ok) break;
@@ -533,7 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           float x[32];
           ld_chunk(tP + lb + c * 32, x);
           if (GATE)
-            mask_chunk_gate<false>(x, (int)row, c, ci, cb);
+            mask_chunk_gate<false>(x, (int)row, c, ci, cb, cw);
           else
             mask_chunk<DECAY, false>(x, (int)row, c, lam, l2);
           store_row_chunk_bf16(sPs, row, c, x);
@@ -624,6 +661,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&bar[B_PRE]);
       }
       for (int n = 0; n < nb; ++n, ++blk) {
+        // the next block's state decay (gates: two loads), ahead of the waits below
+        const float dec_next = n + 1 < nb ? block_decay(n + 1) : 1.f;
         if (n == (nb > 1 ? nb - 2 : 0) && item + (int)gridDim.x < P.nitems) {
           // the next item's entering state: this thread's 512-byte row, into L2 ahead of its load
           const int nx = item + (int)gridDim.x;
@@ -646,7 +685,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         tc_fence_after();
         if (n + 1 < nb) {
-          const float dec = block_decay(n + 1);
+          const float dec = dec_next;
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
             float x[32];
@@ -727,7 +766,7 @@ constexpr int kDualThreads = 512;
 constexpr int kDualSlots = 6;
 constexpr uint32_t kDualOffSh = kDualSlots * kTileBytes;  // bf16 state tile
 constexpr uint32_t kDualOffBar = kDualOffSh + kTileBytes;
-constexpr uint32_t kDualOffGate = kDualOffBar + 256;  // GATE: 2 x 128 cumulative sums of a block
+constexpr uint32_t kDualOffGate = kDualOffBar + 256;  // GATE: a block's 128 sums, 128 column factors
 constexpr size_t kDualSmem = kDualOffGate + 1024 + 1024;
 enum { D_FULL = 0, D_EMPTY = kDualSlots, D_PFULL = 2 * kDualSlots, D_PSFULL, D_O1FULL, D_O1EMPTY, D_O2FULL,
        D_O2EMPTY, D_SFULL, D_PRE, D_KSC, D_VSC, D_COUNT };
@@ -940,13 +979,14 @@ __global__ void __launch_bounds__(kDualThreads, 1)
       const float *gc = GATE ? P.gC + (int64_t)bh * P.T : nullptr;
       for (int n = 0; n < nb && ok; ++n, ++blk) {
         float ci = 0.f;
-        float *cb = reinterpret_cast<float *>(smem + kDualOffGate) + 128 * (blk & 1);
+        float *cb = reinterpret_cast<float *>(smem + kDualOffGate), *cw = cb + 128;
         if (GATE) {
-          // the block's cumulative sums, shared by the group (two buffers: a
-          // buffer is rewritten two blocks later, after this barrier's successor)
+          // the block's cumulative sums and column factors, shared by the group
+          // (rewritten only after the barrier that ends the block below)
           const int t0 = s0 + 128 * (nb - 1 - n), nv = min(128, s1 - t0);
           ci = gate_c(gc, t0, (int)row, nv);
           cb[row] = ci;
+          cw[row] = gate_colw<true>(gc, t0, (int)row, nv);
           named_bar_sync(3, 128);
         }
         for (int half = 0; half < 2 && ok; ++half) {
@@ -961,7 +1001,7 @@ __global__ void __launch_bounds__(kDualThreads, 1)
             float x[32];
             ld_chunk(tP + lb + c * 32, x);
             if (GATE)
-              mask_chunk_gate<true>(x, (int)row, c, ci, cb);
+              mask_chunk_gate<true>(x, (int)row, c, ci, cb, cw);
             else
               mask_chunk<DECAY, true>(x, (int)row, c, lam, l2);
             uint32_t r[16];
@@ -973,6 +1013,7 @@ __global__ void __launch_bounds__(kDualThreads, 1)
           tc_fence_before();
           mbar_arrive(&bar[D_PSFULL]);
         }
+        if (GATE) named_bar_sync(3, 128);  // the block's sums are no longer read (ok is group-uniform)
       }
     }
   } else if (warp >= 8 && warp < 12) {
@@ -1021,6 +1062,8 @@ __global__ void __launch_bounds__(kDualThreads, 1)
         mbar_arrive(&bar[D_PRE]);
       }
       for (int n = 0; n < nb && ok; ++n, ++blk) {
+        // the next walk block's state decay (gates: two loads), ahead of the waits below
+        const float dec_next = n + 1 < nb ? block_decay(n + 1) : 1.f;
         if (n == (nb > 1 ? nb - 2 : 0) && item + (int)gridDim.x < P.nitems) {
           // the next item's entering state: this thread's 512-byte row, into L2 ahead of its load
           const int nx = item + (int)gridDim.x;
@@ -1059,7 +1102,7 @@ __global__ void __launch_bounds__(kDualThreads, 1)
         if (!(ok = wait(D_SFULL, blk))) break;
         tc_fence_after();
         if (n + 1 < nb) {
-          const float dec = block_decay(n + 1);
+          const float dec = dec_next;
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
             float x[32];
@@ -1090,6 +1133,12 @@ __global__ void __launch_bounds__(kDualThreads, 1)
       for (int n = 0; n < nb && ok; ++n, ++blk) {
         const int t0 = s0 + 128 * (nb - 1 - n);
         const bool valid = t0 + (int)row < s1;
+        if (GATE && P.gx && valid) {
+          // the k row for k . dk: two 128-byte lines into L1 while dv drains
+          const __nv_bfloat16 *kr = P.gk + (int64_t)b * P.sb + (int64_t)h * P.sh + (int64_t)(t0 + (int)row) * P.st;
+          prefetch_l1(kr);
+          prefetch_l1(kr + 64);
+        }
         for (int half = 0; half < 2 && ok; ++half) {
           ok = __all_sync(0xffffffffu, mbar_wait(&bar[half ? D_O2FULL : D_O1FULL], blk & 1, &abort_flag,
                                                  P.status, detail));

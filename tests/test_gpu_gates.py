@@ -37,7 +37,9 @@ def f32(a):
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()
 
 
-@pytest.mark.parametrize("T,lo", [(200, -0.05), (2048 + 64, -0.05), (8192 + 100, -0.02), (1000, -1.0)])
+# lo = -4: gates down to e^-4, so a 32-token chunk of cumulative sums can span more
+# than 100 (base 2) and the masks take their per-element form
+@pytest.mark.parametrize("T,lo", [(200, -0.05), (2048 + 64, -0.05), (8192 + 100, -0.02), (1000, -1.0), (300, -4.0)])
 def test_gated_forward_and_backward(T, lo):
     B, H = 1, 3
     c, dev, lg = case(T, B, H, T, lo)

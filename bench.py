@@ -442,6 +442,119 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+# ---------------------------------------------------------------------------------- decode
+def run_decode(args):
+    """Recurrent decode (constant-memory inference): one new token per sequence per call
+    for decode_batch x 16 heads at d = 128, the fp32 states resident on the device.  Bound
+    by the state traffic: 2 d^2 fp32 (read + write) per sequence per call."""
+    import torch
+    import chunked_state_scan_causal_gb300 as la
+    from chunked_state_scan_causal_gb300 import build
+    build.build()
+    dev = torch.device("cuda", 0)
+    B, H, d, T = args.decode_batch, 16, 128, 1
+    g = torch.Generator(device="cpu").manual_seed(9)
+    q, k, v = [(torch.randn(B, H, T, d, generator=g) / d ** 0.5).to(torch.bfloat16).to(dev) for _ in range(3)]
+    state = torch.zeros(B, H, d, d, dtype=torch.float32, device=dev)
+    o = torch.empty_like(q)
+    decay = torch.full((H,), 0.99, dtype=torch.float32, device=dev)
+    for _ in range(args.warmup):
+        la.decode(q, k, v, state, decay=decay, out=o)
+    torch.cuda.synchronize()
+    la.linattn_timing_enable(True)
+    la.linattn_timing_collect()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        la.decode(q, k, v, state, decay=decay, out=o)
+    e1.record()
+    torch.cuda.synchronize()
+    la.linattn_timing_enable(False)
+    kern = la.linattn_timing_collect().get("decode", (0, 0.0))
+    ms = e0.elapsed_time(e1) / args.steps
+    seq = B * H
+    bytes_call = seq * (2 * d * d * 4 + 4 * T * d * 2)  # states in and out, q, k, v read, o written
+    hbm, _, src = _peaks()
+    kms = kern[1] / max(kern[0], 1)
+    print(json.dumps({
+        "metric": "recurrent decode tokens/s (one token per sequence per call)", "value": B * T / (ms * 1e-3),
+        "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "dtype": "bf16 (fp32 state)", "data": "synthetic",
+        "config": {"workload": f"decode-B{B}H{H}-d{d}", "B": B, "H": H, "T_per_call": T, "d": d},
+        "roofline": {"kernel": "decode_kernel", "bound": "hbm", "achieved": bytes_call / (kms * 1e-3) / 1e9,
+                     "peak": hbm, "unit": "GB/s", "frac": bytes_call / (kms * 1e-3) / 1e9 / hbm,
+                     "peak_source": f"{src} hbm_gbs"},
+        "gpu_launches": kern[0]}), flush=True)
+
+
+# ---------------------------------------------------------------------------------- sequence split
+def run_sp(args):
+    """The sequence split across ranks (sp.forward + sp.backward) with N ranks as threads of
+    this process on one GPU, each holding T/N tokens of every sequence of the workload; the
+    ranks share the GPU, so this measures the split's total cost (its extra passes over the
+    segments and the exchanges) against the unsplit step, not scaling."""
+    import threading
+    import torch
+    import chunked_state_scan_causal_gb300 as la
+    from chunked_state_scan_causal_gb300 import build, inputs, sp
+    build.build()
+    dev = torch.device("cuda", 0)
+    cfg = dict(inputs.WORKLOADS[args.workload])
+    B, H, T = cfg["B"], cfg["H"], cfg["T"]
+    N = args.sp
+    L = T // N
+    x = {w: inputs.make(cfg, w).to(dev) for w in ("q", "k", "v", "dO")}
+    torch.cuda.synchronize()
+
+    def split_step():
+        group = sp.ThreadExchange.Group(N, timeout=60)
+        errs = []
+
+        def rank(r):
+            ex = group.rank(r)
+            try:
+                seg = {w: t[:, :, r * L:(r + 1) * L] for w, t in x.items()}
+                _, _, ctx = sp.forward(seg["q"], seg["k"], seg["v"], ex)
+                sp.backward(seg["q"], seg["k"], seg["v"], seg["dO"], ctx, ex)
+            except Exception as e:
+                errs.append(e)
+                ex.abort()
+
+        th = [threading.Thread(target=rank, args=(r,)) for r in range(N)]
+        for t in th:
+            t.start()
+        for t in th:
+            t.join()
+        if errs:
+            raise errs[0]
+
+    ck = la.checkpoint(x["q"])
+
+    def whole_step():
+        la.fwd(x["q"], x["k"], x["v"], ckpt=ck)
+        la.bwd(x["q"], x["k"], x["v"], x["dO"], ckpt=ck)
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / args.steps
+
+    ms_split, ms_whole = timed(split_step), timed(whole_step)
+    print(json.dumps({
+        "metric": f"sequence-split fwd+bwd tokens/s ({N} ranks as threads on one GPU)",
+        "value": B * T / (ms_split * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_split, "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": cfg["name"], "ranks": N, "segment": L},
+        "unsplit_ms_per_step": ms_whole, "split_over_unsplit": ms_split / ms_whole}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -456,10 +569,17 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--B", type=int, default=0, help="override the batch size (profiling cases)")
     ap.add_argument("--T", type=int, default=0, help="override the sequence length (profiling cases)")
+    ap.add_argument("--decode", action="store_true", help="measure the recurrent decode instead")
+    ap.add_argument("--decode-batch", type=int, default=512, help="sequences per head for --decode")
+    ap.add_argument("--sp", type=int, default=0, help="measure the sequence split with this many thread ranks")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.decode:
+        run_decode(args)
+    elif args.sp:
+        run_sp(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

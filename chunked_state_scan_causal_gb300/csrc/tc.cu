@@ -23,17 +23,31 @@ namespace linattn {
 bool tc_supported(const Problem &p) { return p.dtype == 0 && p.d == 128 && p.T >= 1; }
 
 int tc_group_len(const Problem &p) {
-  // Long groups keep the per-group fp32 states (64 KiB each, written and read
-  // a few times) small next to the group's data (1 MiB of q, k, v per 2048
-  // tokens); at most 256 groups per sequence keep the state scan in its
-  // column-parallel form; and there must be enough (group, sequence) items to
-  // fill the SMs twice over.
-  const int64_t BH = (int64_t)p.B * p.H;
-  int64_t L = 2048;
-  if ((p.T + L - 1) / L > 256) L = ((p.T + 255) / 256 + 127) / 128 * 128;
-  while (L > 256 && ((p.T + L - 1) / L) * BH < 2 * (int64_t)p.num_sms) L = (L / 2 + 127) / 128 * 128;
-  const int64_t Tr = ((int64_t)p.T + 127) / 128 * 128;
-  return (int)(L < Tr ? L : Tr);
+  // The persistent kernels give each CTA whole (group, sequence) items, so a
+  // launch lasts about ceil(items / SMs) waves of one item each.  Pick the
+  // group count G (at most 256 per sequence: the scan's column-parallel form)
+  // whose group length L (a multiple of 128 tokens, at least 256) minimises
+  //     waves(G) * (L / 128 + 1),
+  // the "+ 1" standing for an item's fixed cost (its entering state, its
+  // outputs at the end) in units of one 128-token block.  Ties go to longer
+  // groups (fewer states).
+  const int64_t BH = (int64_t)p.B * p.H, T = p.T, sms = p.num_sms > 0 ? p.num_sms : 1;
+  int64_t bestL = 0, bestCost = 0;
+  for (int64_t G = 1; G <= 256; ++G) {
+    int64_t L = ((T + G - 1) / G + 127) / 128 * 128;
+    if (L < 256) L = 256;
+    const int64_t Ge = (T + L - 1) / L;
+    if (Ge > 256) continue;
+    const int64_t waves = (BH * Ge + sms - 1) / sms;
+    const int64_t cost = waves * (L / 128 + 1);
+    if (bestL == 0 || cost < bestCost || (cost == bestCost && L > bestL)) {
+      bestL = L;
+      bestCost = cost;
+    }
+  }
+  // (G = 256 always qualifies, so bestL is set)
+  const int64_t Tr = (T + 127) / 128 * 128;
+  return (int)(bestL < Tr ? bestL : Tr);
 }
 
 namespace {

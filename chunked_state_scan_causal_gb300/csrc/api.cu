@@ -147,10 +147,10 @@ struct FwdLayout {
   int G = 0, L = 0;
   size_t agg = 0, states = 0, scan = 0, total = kHeader;
 };
-static FwdLayout fwd_layout(const Problem &p) {
+static FwdLayout fwd_layout(const Problem &p, int max_len = 0) {
   FwdLayout w;
   if (!tc_supported(p) || p.T == 0) return w;
-  w.L = tc_group_len(p);
+  w.L = tc_group_len(p, max_len);
   w.G = (p.T + w.L - 1) / w.L;
   const size_t st = (size_t)w.G * p.B * p.H * p.d * p.d * sizeof(float);
   w.agg = kHeader;
@@ -188,9 +188,13 @@ struct GatedLayout {
   FwdLayout f;
   size_t C = 0, tot = 0, wagg = 0, rbar = 0, gx = 0, fwd_total = kHeader, bwd_total = kHeader;
 };
+// With gates the groups are kept to at most 2048 tokens: the gate gradient sums
+// q.dq - k.dk inside a group (anchored exactly at the group ends), and those
+// sums gather the error of every token of the group.
+constexpr int kGatedMaxGroup = 2048;
 static GatedLayout gated_layout(const Problem &p) {
   GatedLayout w;
-  w.f = fwd_layout(p);
+  w.f = fwd_layout(p, kGatedMaxGroup);
   if (w.f.G == 0) return w;
   const int64_t BH = (int64_t)p.B * p.H;
   const size_t st = (size_t)w.f.G * BH * p.d * p.d * sizeof(float);
@@ -204,7 +208,7 @@ static GatedLayout gated_layout(const Problem &p) {
   return w;
 }
 static size_t ckpt_bytes_gated(const Problem &p) {
-  const FwdLayout w = fwd_layout(p);
+  const FwdLayout w = fwd_layout(p, kGatedMaxGroup);
   return w.G == 0 ? 0 : ((size_t)w.G + 1) * p.B * p.H * p.d * p.d * sizeof(float);
 }
 

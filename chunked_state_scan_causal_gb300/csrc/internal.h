@@ -83,7 +83,9 @@ cudaError_t gate_grad(const Problem &p, int L, const float *gx, const float *rba
 
 // ---------------------------------------------------------------- tensor-core path (tc.cu)
 bool tc_supported(const Problem &p);   // bf16, d = 128
-int tc_group_len(const Problem &p);    // tokens per chunk group (multiple of 128)
+// Tokens per chunk group (a multiple of 128); max_len > 0 caps it where possible
+// (at least ceil(T / 256) tokens per group remain).
+int tc_group_len(const Problem &p, int max_len = 0);
 // Segment aggregates sum_s w_s x_s y_s^T over groups of seg_len tokens (seg_len
 // a multiple of 128), written as [G][BH][d][d] fp32.
 //   reverse == false: w_s = lambda^{end - s};  reverse == true: w_s = lambda^{s - start + 1}.

@@ -13,6 +13,8 @@
 // the natural tile, and chunking at 128 instead of 64 changes only the
 // rounding order (the chunked form equals the definition for any chunk
 // length).  All operands are SW128 tiles (ptx.cuh).
+#include <algorithm>
+
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -22,7 +24,7 @@ namespace linattn {
 
 bool tc_supported(const Problem &p) { return p.dtype == 0 && p.d == 128 && p.T >= 1; }
 
-int tc_group_len(const Problem &p) {
+int tc_group_len(const Problem &p, int max_len) {
   // The persistent kernels give each CTA whole (group, sequence) items, so a
   // launch lasts about ceil(items / SMs) waves of one item each.  Pick the
   // group count G (at most 256 per sequence: the scan's column-parallel form)
@@ -32,12 +34,13 @@ int tc_group_len(const Problem &p) {
   // outputs at the end) in units of one 128-token block.  Ties go to longer
   // groups (fewer states).
   const int64_t BH = (int64_t)p.B * p.H, T = p.T, sms = p.num_sms > 0 ? p.num_sms : 1;
+  const int64_t cap = max_len > 0 ? std::max<int64_t>(max_len, ((T + 255) / 256 + 127) / 128 * 128) : 0;
   int64_t bestL = 0, bestCost = 0;
   for (int64_t G = 1; G <= 256; ++G) {
     int64_t L = ((T + G - 1) / G + 127) / 128 * 128;
     if (L < 256) L = 256;
     const int64_t Ge = (T + L - 1) / L;
-    if (Ge > 256) continue;
+    if (Ge > 256 || (cap && L > cap)) continue;
     const int64_t waves = (BH * Ge + sms - 1) / sms;
     const int64_t cost = waves * (L / 128 + 1);
     if (bestL == 0 || cost < bestCost || (cost == bestCost && L > bestL)) {

@@ -419,7 +419,6 @@ static int gated_checks(const linattn_shape *shape, Problem *p, const float *log
   int st = validate(shape, p);
   if (st) return st;
   if (p->decay) return LINATTN_ERR_INVALID;  // gates replace the per-head decay
-  if (p->T > 0 && !tc_supported(*p)) return LINATTN_ERR_UNSUPPORTED;
   if (p->T > 0 && (st = check_ptrs({log_gate}, {}))) return st;
   const size_t need = ckpt_bytes_gated(*p);
   if (need && (!ckpt || (reinterpret_cast<uintptr_t>(ckpt) & 255u) || ckpt_size < need)) return LINATTN_ERR_INVALID;
@@ -453,6 +452,8 @@ int32_t linattn_fwd_gated(const linattn_shape *shape, const void *q, const void 
     }
     return LINATTN_OK;
   }
+  // CUDA-core path (fp32 inputs, d = 64): one sequential walk, no checkpoint
+  if (!tc_supported(p)) return cuda_status(simt_fwd(p, q, k, v, o, init_state, final_state, nullptr, s, log_gate));
   const int L = w.f.L, G = w.f.G;
   float *C = reinterpret_cast<float *>(ws + w.C), *tot = reinterpret_cast<float *>(ws + w.tot);
   float *agg = reinterpret_cast<float *>(ws + w.f.agg);
@@ -497,6 +498,10 @@ int32_t linattn_bwd_gated(const linattn_shape *shape, const void *q, const void 
                                        : cudaMemsetAsync(d_init_state, 0, state_bytes, s));
     return LINATTN_OK;
   }
+  // CUDA-core path: recomputes the forward states from init_state (the checkpoint is empty)
+  if (!tc_supported(p))
+    return cuda_status(simt_bwd(p, q, k, v, dO, init_state, d_final_state, dq, dk, dv, d_init_state, s, log_gate,
+                                d_log_gate));
   const int L = w.f.L, G = w.f.G;
   float *C = reinterpret_cast<float *>(ws + w.C), *tot = reinterpret_cast<float *>(ws + w.tot);
   float *wagg = reinterpret_cast<float *>(ws + w.wagg), *rbar = reinterpret_cast<float *>(ws + w.rbar);

@@ -42,11 +42,14 @@ struct TimedLaunch {
 };
 
 // ---------------------------------------------------------------- SIMT path (simt.cu)
+// log_gate ([BH][T] fp32, natural log of the per-token gates) replaces the per-head
+// decay when non-null; the backward then also writes d_log_gate ([BH][T] fp32).
 cudaError_t simt_fwd(const Problem &p, const void *q, const void *k, const void *v, void *o,
-                     const float *init, float *final_state, float *chunk_states, cudaStream_t s);
+                     const float *init, float *final_state, float *chunk_states, cudaStream_t s,
+                     const float *log_gate = nullptr);
 cudaError_t simt_bwd(const Problem &p, const void *q, const void *k, const void *v, const void *dO,
                      const float *init, const float *d_final, void *dq, void *dk, void *dv, float *dinit,
-                     cudaStream_t s);
+                     cudaStream_t s, const float *log_gate = nullptr, float *d_log_gate = nullptr);
 // Segment sums of w_s x_s y_s^T: w_s = lambda^{end - s}, or lambda^{s - start + 1} when reverse.
 cudaError_t simt_segment_states(const Problem &p, int seg_len, const void *x, const void *y, bool reverse,
                                 float *out, cudaStream_t s);

@@ -152,10 +152,12 @@ int32_t linattn_bwd_ckpt(const linattn_shape *shape, const void *q, const void *
  *   S_t = alpha_t S_{t-1} + k_t v_t^T,   o_t = S_t^T q_t.
  * log_gate is [B,H,T] fp32, contiguous, 16-byte aligned (log of gates in
  * (0, 1]: values <= 0; positive values are taken as given but their weights may
- * overflow).  The shape's decay must be NULL.  Tensor-core path only: bf16,
- * d = 128 (otherwise LINATTN_ERR_UNSUPPORTED).  The checkpoint (size from
- * LINATTN_OP_CHECKPOINT_GATED) is required: it keeps every chunk group's
- * entering state and the final state for linattn_bwd_gated.  Workspace sizes:
+ * overflow).  The shape's decay must be NULL.  bf16 with d = 128 runs on the
+ * tensor-core kernels; fp32 inputs and d = 64 on the CUDA-core kernels.  The
+ * checkpoint (size from LINATTN_OP_CHECKPOINT_GATED) keeps every chunk group's
+ * entering state and the final state for linattn_bwd_gated; it is required
+ * when that size is nonzero (the CUDA-core path has none: its backward
+ * recomputes the states from init_state).  Workspace sizes:
  * LINATTN_OP_FWD_GATED / LINATTN_OP_BWD_GATED.  Returns a status. */
 int32_t linattn_fwd_gated(const linattn_shape *shape, const void *q, const void *k, const void *v,
                           const float *log_gate, void *o, const float *init_state, float *final_state,

@@ -133,9 +133,11 @@ def test_device_status_null(cdll):
 def test_gated_entry_points_check_their_arguments(cdll):
     s = _shape()
     ck = 1 << 30  # large enough for any checkpoint size check
-    # fp32 inputs have no gated path
-    assert la.linattn_fwd_gated(_shape(dtype=la.F32), FAKE, FAKE, FAKE, FAKE, FAKE, None, None, FAKE, ck, FAKE,
-                                1 << 30, None) == la.ERR_UNSUPPORTED
+    # fp32 inputs and d = 64 take the CUDA-core path: no checkpoint, no workspace past the status header
+    for sh in (_shape(dtype=la.F32), _shape(dk=64, dv=64, stride_b=2 * 256 * 64, stride_h=256 * 64, stride_t=64)):
+        for op in (la.OP_FWD_GATED, la.OP_BWD_GATED):
+            assert la.linattn_workspace_size(sh, op) == (la.OK, 256)
+        assert la.linattn_workspace_size(sh, la.OP_CHECKPOINT_GATED) == (la.OK, 0)
     # the per-head decay and gates exclude each other
     lam = (ctypes.c_float * 2)(0.9, 0.9)
     assert la.linattn_fwd_gated(_shape(decay=ctypes.cast(lam, ctypes.c_void_p)), FAKE, FAKE, FAKE,

@@ -2,7 +2,9 @@
 fp64 oracle, through the C ABI: several chunk groups, ragged tails, initial
 state and final-state gradient, mild and strong gates, and the reduction to
 the per-head decay when every gate of a head is the same.  Tolerance as in
-test_gpu_parity (1e-2 of max|ref| per tensor for bf16 inputs)."""
+test_gpu_parity (1e-2 of max|ref| per tensor for bf16 inputs, 1e-4 for fp32).
+bf16 with d = 128 runs on the tensor-core kernels; fp32 inputs and d = 64 on the
+CUDA-core kernels (one sequential walk per sequence)."""
 import numpy as np
 import pytest
 import torch
@@ -13,6 +15,7 @@ from chunked_state_scan_causal_gb300 import inputs
 
 pytestmark = pytest.mark.gpu
 TOL = 1e-2
+TOLS = {torch.bfloat16: 1e-2, torch.float32: 1e-4}
 
 
 def rel(got, ref):
@@ -26,9 +29,10 @@ def built():
     build.build()
 
 
-def case(seed, B, H, T, lo):
-    c = inputs.random_case(seed, B, H, T, 128, dtype="bf16", sigma=1 / np.sqrt(128))
-    dev = {k: torch.from_numpy(np.ascontiguousarray(v)).to(torch.bfloat16).cuda() for k, v in c.items()}
+def case(seed, B, H, T, lo, d=128, dtype=torch.bfloat16):
+    name = "bf16" if dtype == torch.bfloat16 else "f32"
+    c = inputs.random_case(seed, B, H, T, d, dtype=name, sigma=1 / np.sqrt(d))
+    dev = {k: torch.from_numpy(np.ascontiguousarray(v)).to(dtype).cuda() for k, v in c.items()}
     lg = np.random.default_rng(seed + 1).uniform(lo, 0.0, (B, H, T)).astype(np.float32)
     return c, dev, lg
 
@@ -60,9 +64,32 @@ def test_gated_forward_and_backward(T, lo):
         assert rel(got, ref) < TOL, (name, rel(got, ref))
 
 
-def test_constant_gates_match_the_per_head_decay():
+# the CUDA-core kernels: fp32 inputs (d = 128 and 64) and bf16 with d = 64
+@pytest.mark.parametrize("dtype,d,T,lo", [(torch.float32, 128, 200, -0.05), (torch.float32, 64, 1000, -1.0),
+                                          (torch.float32, 64, 130, -4.0), (torch.bfloat16, 64, 700, -0.05)])
+def test_gated_cuda_core_path(dtype, d, T, lo):
+    B, H = 1, 2
+    c, dev, lg = case(T + d, B, H, T, lo, d=d, dtype=dtype)
+    r = np.random.default_rng(T + 11)
+    init = (0.1 * r.standard_normal((B, H, d, d))).astype(np.float32).astype(np.float64)
+    D = (0.1 * r.standard_normal((B, H, d, d))).astype(np.float32).astype(np.float64)
+    ck = la.checkpoint_gated(dev["q"])
+    o, fin = la.fwd_gated(dev["q"], dev["k"], dev["v"], f32(lg), ck, init_state=f32(init), want_final=True)
+    dq, dk, dv, dlg, dinit = la.bwd_gated(dev["q"], dev["k"], dev["v"], dev["dO"], f32(lg), ck, init_state=f32(init),
+                                          d_final=f32(D), want_dinit=True)
+    torch.cuda.synchronize()
+    lg64 = lg.astype(np.float64)
+    ro, rfin = oracle.fwd_gated(c["q"], c["k"], c["v"], lg64, init=init)
+    rq, rk, rv, rlg, rinit = oracle.bwd_gated(c["q"], c["k"], c["v"], c["dO"], lg64, init=init, d_final=D)
+    for name, got, ref in (("o", o, ro), ("final", fin, rfin), ("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv),
+                           ("d_log_gate", dlg, rlg), ("d_init", dinit, rinit)):
+        assert rel(got, ref) < TOLS[dtype], (name, rel(got, ref))
+
+
+@pytest.mark.parametrize("dtype,d", [(torch.bfloat16, 128), (torch.float32, 64)])
+def test_constant_gates_match_the_per_head_decay(dtype, d):
     B, H, T = 1, 2, 3000
-    c, dev, _ = case(5, B, H, T, -0.1)
+    c, dev, _ = case(5, B, H, T, -0.1, d=d, dtype=dtype)
     lam = inputs.decay_per_head(H)
     lg = np.broadcast_to(np.log(lam.astype(np.float64))[None, :, None], (B, H, T)).astype(np.float32)
     ck = la.checkpoint_gated(dev["q"])
@@ -72,7 +99,7 @@ def test_constant_gates_match_the_per_head_decay():
     dq2, dk2, dv2, _ = la.bwd(dev["q"], dev["k"], dev["v"], dev["dO"], decay=torch.from_numpy(lam).cuda())
     torch.cuda.synchronize()
     for a, b in ((o, o2), (dq, dq2), (dk, dk2), (dv, dv2)):
-        assert rel(a, b.double().cpu().numpy()) < TOL
+        assert rel(a, b.double().cpu().numpy()) < TOLS[dtype]
 
 
 def test_gated_empty_sequence():

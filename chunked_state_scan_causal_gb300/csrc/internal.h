@@ -85,6 +85,12 @@ cudaError_t gate_grad(const Problem &p, int L, const float *gx, const float *rba
                       const float *d_final, const float *final_state, float *dlg, cudaStream_t s);
 
 // ---------------------------------------------------------------- tensor-core path (tc.cu)
+// The persistent kernels take `status`, the start of the workspace's 256-byte
+// header (zeroed by every entry point): int 0 is the status word, ints 1..16 a
+// per-warp record of a wait that gave up, and each kernel kind keeps the two
+// counters of its dynamic item order at these offsets (each launch leaves them
+// zero again, so one call may launch a kind more than once).
+constexpr int kCounterAgg = 32, kCounterMain = 34, kCounterDual = 36;
 bool tc_supported(const Problem &p);   // bf16, d = 128
 // Tokens per chunk group (a multiple of 128); max_len > 0 caps it where possible
 // (at least ceil(T / 256) tokens per group remain).

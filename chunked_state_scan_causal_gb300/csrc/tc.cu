@@ -61,6 +61,62 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
   return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
+// ---------------------------------------------------------------------------- item order
+// The (group, sequence) items of a persistent launch are handed out at run
+// time: the producer thread draws the CTA's next item from a counter in global
+// memory when it is ready to load it, and posts it in a small shared ring that
+// every warp role reads in the same order (-1: no items left).  CTAs on SMs
+// that get more memory bandwidth draw more items, instead of every CTA waiting
+// for the slowest one's fixed share.  The last CTA of a launch to finish sets
+// the counters back to zero for the next launch on the stream (items_done).
+constexpr int kRing = 4;
+struct ItemRing {
+  int *item;        // [kRing]
+  uint64_t *full;   // [kRing]: one arrival, the producer's
+  uint64_t *empty;  // [kRing]: one arrival per reading thread
+};
+
+__device__ __forceinline__ void ring_init(const ItemRing &r, int readers) {
+  for (int i = 0; i < kRing; ++i) {
+    mbar_init(&r.full[i], 1);
+    mbar_init(&r.empty[i], readers);
+  }
+}
+
+// Producer: draw and post this CTA's k-th item.  False if a wait gave up.
+__device__ __forceinline__ bool ring_post(const ItemRing &r, int k, int *counter, int nitems, int &item,
+                                          volatile int *abort_flag, int *status, int *detail) {
+  const int s = k % kRing;
+  if (k >= kRing && !mbar_wait(&r.empty[s], (k / kRing - 1) & 1, abort_flag, status, detail)) return false;
+  const int x = atomicAdd(counter, 1);
+  item = x < nitems ? x : -1;
+  *reinterpret_cast<volatile int *>(&r.item[s]) = item;
+  mbar_arrive(&r.full[s]);  // release: the item is visible to the readers of the phase
+  return true;
+}
+
+// Reader: this CTA's k-th item.  False if the wait gave up.
+__device__ __forceinline__ bool ring_take(const ItemRing &r, int k, int &item, volatile int *abort_flag,
+                                          int *status, int *detail) {
+  const int s = k % kRing;
+  if (!mbar_wait(&r.full[s], (k / kRing) & 1, abort_flag, status, detail)) return false;
+  item = *reinterpret_cast<volatile int *>(&r.item[s]);
+  mbar_arrive(&r.empty[s]);
+  return true;
+}
+
+// End of a CTA (after its last barrier): counter[0] counts items drawn,
+// counter[1] finished CTAs; the last CTA out zeroes both.
+__device__ __forceinline__ void items_done(int *counter) {
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(counter + 1, 1) == (int)gridDim.x - 1) {
+      atomicExch(counter, 0);
+      atomicExch(counter + 1, 0);
+    }
+  }
+}
+
 // Multiply one 128-element bf16 row of an SW128 tile by w (rounded back to bf16).
 __device__ __forceinline__ void scale_tile_row(uint32_t tile, uint32_t row, float w) {
 #pragma unroll 4
@@ -101,6 +157,7 @@ struct AggParams {
   const float *decay;
   float *out;
   int *status;
+  int *counter;  // [2] item counter and finished CTAs (zero at launch)
   const float *gC, *gtot;  // gates: group-local log2 cumulative sums [BH][T], group totals [G][BH]
 };
 
@@ -119,6 +176,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *accf = bars + 3 * NS, *acce = accf + 2;
   uint32_t *tslot = reinterpret_cast<uint32_t *>(acce + 2);
   __shared__ int abort_flag;
+  __shared__ int ring_item[kRing];
+  __shared__ uint64_t ring_bar[2 * kRing];
+  const ItemRing ring{ring_item, ring_bar, ring_bar + kRing};
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int BH = P.B * P.H;
   int *const detail = P.status ? P.status + 1 + warp : nullptr;  // which wait gave up, per warp role
@@ -134,6 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&accf[a], 1);
       mbar_init(&acce[a], 128);
     }
+    ring_init(ring, 1 + (DECAY ? 128 : 0) + 128);  // readers: MMA thread, scaling warps, store warps
     fence_mbar_init();
     prefetch_tensormap(&mx);
     prefetch_tensormap(&my);
@@ -151,7 +212,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int it = 0;
       bool ok = true;
-      for (int item = blockIdx.x; item < P.nitems && ok; item += gridDim.x) {
+      for (int k = 0, item; ok; ++k) {
+        if (!(ok = ring_post(ring, k, P.counter, P.nitems, item, &abort_flag, P.status, detail)) || item < 0) break;
         const int g = item / BH, bh = item % BH, b = bh / P.H, h = bh % P.H;
         const int s0 = g * P.L, s1 = min(P.T, s0 + P.L);
         for (int t0 = s0; t0 < s1; t0 += 128, ++it) {
@@ -178,7 +240,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int it = 0, ai = 0;
       bool ok = true;
       const uint32_t idesc = idesc_bf16(128, 128, true, true);
-      for (int item = blockIdx.x; item < P.nitems && ok; item += gridDim.x) {
+      for (int k = 0, item; ok; ++k) {
+        if (!(ok = ring_take(ring, k, item, &abort_flag, P.status, detail)) || item < 0) break;
         const int g = item / BH;
         const int s0 = g * P.L, s1 = min(P.T, s0 + P.L);
         const int a = ai & 1, ua = ai >> 1;
@@ -208,7 +271,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t row = threadIdx.x - 128;
       int it = 0;
       bool ok = true;
-      for (int item = blockIdx.x; item < P.nitems && ok; item += gridDim.x) {
+      for (int k = 0, item; ok; ++k) {
+        if (!(ok = __all_sync(0xffffffffu, ring_take(ring, k, item, &abort_flag, P.status, detail))) || item < 0)
+          break;
         const int g = item / BH, bh = item % BH, h = bh % P.H;
         const int s0 = g * P.L, s1 = min(P.T, s0 + P.L);
         const float l2 = GATE ? 0.f : log2f(P.decay[h]);
@@ -232,7 +297,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= 8) {
     const uint32_t quad = warp & 3, row = quad * 32 + lane;
     int ai = 0;
-    for (int item = blockIdx.x; item < P.nitems; item += gridDim.x, ++ai) {
+    for (int k = 0, item;; ++k, ++ai) {
+      if (!__all_sync(0xffffffffu, ring_take(ring, k, item, &abort_flag, P.status, detail)) || item < 0) break;
       const int g = item / BH, bh = item % BH;
       const int a = ai & 1, ua = ai >> 1;
       if (!__all_sync(0xffffffffu, mbar_wait(&accf[a], ua & 1, &abort_flag, P.status, detail))) break;
@@ -252,6 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  items_done(P.counter);
   if (warp == 1) tmem_dealloc(tmem, 256);
 }
 
@@ -263,6 +330,7 @@ struct MainParams {
   float *final_state;  // [BH][d][d] or null
   float *agg_out;      // [G][BH][d][d]: per group sum_s x_s q_s^T (AGG instances)
   int *status;
+  int *counter;        // [2] item counter and finished CTAs (zero at launch)
   const float *gC;     // GATE: group-local log2 cumulative sums of the gates [BH][T]
   const __nv_bfloat16 *gq;  // GATE, dq pass: the true q (strides sb, sh, st) for gx = q . dq
   float *gx;           // GATE, dq pass: [BH][T] fp32 q_t . dq_t from the unrounded dq, or null
@@ -407,6 +475,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *bar = reinterpret_cast<uint64_t *>(smem + kOffBar);
   uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + B_COUNT);
   __shared__ int abort_flag;
+  __shared__ int ring_item[kRing];
+  __shared__ uint64_t ring_bar[2 * kRing];
+  const ItemRing ring{ring_item, ring_bar, ring_bar + kRing};
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int BH = P.B * P.H;
   int *const detail = P.status ? P.status + 1 + warp : nullptr;  // which wait gave up, per warp role
@@ -426,6 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bar[B_PSFULL], 128);
     mbar_init(&bar[B_WEMPTY], 128);
     mbar_init(&bar[B_KSC], 128);
+    ring_init(ring, 1 + 128 + 128);  // readers: MMA thread, groups A and B
     fence_mbar_init();
     prefetch_tensormap(&mq);
     prefetch_tensormap(&mk);
@@ -456,9 +528,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int blk = 0;
       bool ok = true;
-      for (int item = blockIdx.x; item < P.nitems && ok; item += gridDim.x) {
+      for (int k = 0, item; ok; ++k) {
+        if (!(ok = ring_post(ring, k, P.counter, P.nitems, item, &abort_flag, P.status, detail)) || item < 0) break;
         const int g = item / BH, bh = item % BH, b = bh / P.H, h = bh % P.H;
         const int s0 = g * P.L, s1 = min(P.T, s0 + P.L), nb = (s1 - s0 + 127) / 128;
+        bulk_prefetch_l2(P.ginit + ((int64_t)g * BH + bh) * 16384, 16384 * 4);  // the entering state
         for (int n = 0; n < nb && ok; ++n, ++blk) {
           const int t0 = s0 + 128 * n;
           for (int x = 0; x < NT; ++x) {
@@ -490,7 +564,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t id_xq = idesc_bf16(128, 128, true, true);    // X^T Q
       int blk = 0, it = 0;
       bool ok = true;
-      for (int item = blockIdx.x; item < P.nitems && ok; item += gridDim.x, ++it) {
+      for (int k = 0, item; ok; ++k, ++it) {
+        if (!(ok = ring_take(ring, k, item, &abort_flag, P.status, detail)) || item < 0) break;
         const int g = item / BH;
         const int s0 = g * P.L, s1 = min(P.T, s0 + P.L), nb = (s1 - s0 + 127) / 128;
         for (int n = 0; n < nb; ++n, ++blk) {
@@ -552,7 +627,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool leader = threadIdx.x == 128;
     int blk = 0;
     bool ok = true;
-    for (int item = blockIdx.x; item < P.nitems && ok; item += gridDim.x) {
+    for (int k = 0, item; ok; ++k) {
+      if (!(ok = group_all(ring_take(ring, k, item, &abort_flag, P.status, detail), 2, 128)) || item < 0) break;
       const int g = item / BH, bh = item % BH, b = bh / P.H, h = bh % P.H;
       const int s0 = g * P.L, s1 = min(P.T, s0 + P.L), nb = (s1 - s0 + 127) / 128;
       const float lam = (DECAY && !GATE) ? P.decay[h] : 1.f;
@@ -636,7 +712,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t quad = warp & 3, row = quad * 32 + lane, lb = (quad * 32) << 16;
     int blk = 0;
     bool ok = true;
-    for (int item = blockIdx.x; item < P.nitems && ok; item += gridDim.x) {
+    for (int k = 0, item; ok; ++k) {
+      if (!(ok = __all_sync(0xffffffffu, ring_take(ring, k, item, &abort_flag, P.status, detail))) || item < 0)
+        break;
       const int g = item / BH, bh = item % BH, h = bh % P.H;
       const int s0 = g * P.L, s1 = min(P.T, s0 + P.L), nb = (s1 - s0 + 127) / 128;
       const float lam = (DECAY && !GATE) ? P.decay[h] : 1.f;
@@ -680,13 +758,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int n = 0; n < nb; ++n, ++blk) {
         // the next block's state decay (gates: two loads), ahead of the waits below
         const float dec_next = n + 1 < nb ? block_decay(n + 1) : 1.f;
-        if (n == (nb > 1 ? nb - 2 : 0) && item + (int)gridDim.x < P.nitems) {
-          // the next item's entering state: this thread's 512-byte row, into L2 ahead of its load
-          const int nx = item + (int)gridDim.x;
-          const float *nsrc = P.ginit + ((int64_t)(nx / BH) * BH + nx % BH) * 16384 + row * 128;
-#pragma unroll
-          for (int m = 0; m < 4; ++m) prefetch_l2(nsrc + 32 * m);
-        }
         if (DECAY) {
           // key rows k_j *= lambda^{nv-1-j} (gates: exp2(C_last - C_j)) once the scores have read them
           const int nv = nvalid(n), r = (int)row, t0 = s0 + 128 * n;
@@ -749,6 +820,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  items_done(P.counter);
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
@@ -774,6 +846,7 @@ struct DualParams {
   __nv_bfloat16 *dk, *dv;
   int64_t sb, sh, st;  // element strides of dk and dv
   int *status;
+  int *counter;        // [2] item counter and finished CTAs (zero at launch)
   const float *gC;     // GATE: group-local log2 cumulative sums of the gates [BH][T]
   const __nv_bfloat16 *gk;  // GATE: k (strides sb, sh, st) for gx -= k . dk
   float *gx;           // GATE: [BH][T] fp32, q . dq from the dq pass; k . dk (unrounded dk) subtracted
@@ -827,6 +900,9 @@ __global__ void __launch_bounds__(kDualThreads, 1)
   uint64_t *bar = reinterpret_cast<uint64_t *>(smem + kDualOffBar);
   uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + D_COUNT);
   __shared__ int abort_flag;
+  __shared__ int ring_item[kRing];
+  __shared__ uint64_t ring_bar[2 * kRing];
+  const ItemRing ring{ring_item, ring_bar, ring_bar + kRing};
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int BH = P.B * P.H;
   int *const detail = P.status ? P.status + 1 + warp : nullptr;
@@ -847,6 +923,7 @@ __global__ void __launch_bounds__(kDualThreads, 1)
     mbar_init(&bar[D_PRE], 128);
     mbar_init(&bar[D_KSC], 128);
     mbar_init(&bar[D_VSC], 128);
+    ring_init(ring, 1 + 3 * 128);  // readers: MMA thread, groups A, B and C
     fence_mbar_init();
     prefetch_tensormap(&mk);
     prefetch_tensormap(&mq);
@@ -872,9 +949,11 @@ __global__ void __launch_bounds__(kDualThreads, 1)
       int blk = 0;
       bool ok = true;
       int loads[kDualSlots] = {0, 0, 0, 0, 0, 0};
-      for (int item = blockIdx.x; item < P.nitems && ok; item += gridDim.x) {
+      for (int k = 0, item; ok; ++k) {
+        if (!(ok = ring_post(ring, k, P.counter, P.nitems, item, &abort_flag, P.status, detail)) || item < 0) break;
         const int g = item / BH, bh = item % BH, b = bh / P.H, h = bh % P.H;
         const int s0 = g * P.L, s1 = min(P.T, s0 + P.L), nb = (s1 - s0 + 127) / 128;
+        bulk_prefetch_l2(P.ginit + ((int64_t)g * BH + bh) * 16384, 16384 * 4);  // the entering state
         for (int n = 0; n < nb && ok; ++n, ++blk) {
           const int t0 = s0 + 128 * (nb - 1 - n);
           for (int x = 0; x < 4; ++x) {
@@ -920,7 +999,8 @@ __global__ void __launch_bounds__(kDualThreads, 1)
         dual_slot(blk, x, s, c);
         return tile_addr(s);
       };
-      for (int item = blockIdx.x; item < P.nitems && ok; item += gridDim.x) {
+      for (int k = 0, item; ok; ++k) {
+        if (!(ok = ring_take(ring, k, item, &abort_flag, P.status, detail)) || item < 0) break;
         const int g = item / BH;
         const int s0 = g * P.L, s1 = min(P.T, s0 + P.L), nb = (s1 - s0 + 127) / 128;
         for (int n = 0; n < nb && ok; ++n, ++blk) {
@@ -988,7 +1068,8 @@ __global__ void __launch_bounds__(kDualThreads, 1)
     const uint32_t quad = warp & 3, row = quad * 32 + lane, lb = (quad * 32) << 16;
     int blk = 0;
     bool ok = true;
-    for (int item = blockIdx.x; item < P.nitems && ok; item += gridDim.x) {
+    for (int k = 0, item; ok; ++k) {
+      if (!(ok = group_all(ring_take(ring, k, item, &abort_flag, P.status, detail), 3, 128)) || item < 0) break;
       const int g = item / BH, bh = item % BH, h = bh % P.H;
       const int s0 = g * P.L, s1 = min(P.T, s0 + P.L), nb = (s1 - s0 + 127) / 128;
       const float lam = (DECAY && !GATE) ? P.decay[h] : 1.f;
@@ -1041,7 +1122,9 @@ __global__ void __launch_bounds__(kDualThreads, 1)
     auto wait = [&](int idx, int parity) {
       return __all_sync(0xffffffffu, mbar_wait(&bar[idx], parity & 1, &abort_flag, P.status, detail));
     };
-    for (int item = blockIdx.x; item < P.nitems && ok; item += gridDim.x) {
+    for (int k = 0, item; ok; ++k) {
+      if (!(ok = __all_sync(0xffffffffu, ring_take(ring, k, item, &abort_flag, P.status, detail))) || item < 0)
+        break;
       const int g = item / BH, bh = item % BH, h = bh % P.H;
       const int s0 = g * P.L, s1 = min(P.T, s0 + P.L), nb = (s1 - s0 + 127) / 128;
       const float lam = (DECAY && !GATE) ? P.decay[h] : 1.f;
@@ -1081,13 +1164,6 @@ __global__ void __launch_bounds__(kDualThreads, 1)
       for (int n = 0; n < nb && ok; ++n, ++blk) {
         // the next walk block's state decay (gates: two loads), ahead of the waits below
         const float dec_next = n + 1 < nb ? block_decay(n + 1) : 1.f;
-        if (n == (nb > 1 ? nb - 2 : 0) && item + (int)gridDim.x < P.nitems) {
-          // the next item's entering state: this thread's 512-byte row, into L2 ahead of its load
-          const int nx = item + (int)gridDim.x;
-          const float *nsrc = P.ginit + ((int64_t)(nx / BH) * BH + nx % BH) * 16384 + row * 128;
-#pragma unroll
-          for (int m = 0; m < 4; ++m) prefetch_l2(nsrc + 32 * m);
-        }
         if (DECAY) {
           const int nv = nvalid(n), r = (int)row;
           float wx = 0.f, wy = 0.f;  // rows of K and V; rows of dO
@@ -1144,7 +1220,9 @@ __global__ void __launch_bounds__(kDualThreads, 1)
     const uint32_t quad = warp & 3, row = quad * 32 + lane, lb = (quad * 32) << 16;
     int blk = 0;
     bool ok = true;
-    for (int item = blockIdx.x; item < P.nitems && ok; item += gridDim.x) {
+    for (int k = 0, item; ok; ++k) {
+      if (!(ok = __all_sync(0xffffffffu, ring_take(ring, k, item, &abort_flag, P.status, detail))) || item < 0)
+        break;
       const int g = item / BH, bh = item % BH, b = bh / P.H, h = bh % P.H;
       const int s0 = g * P.L, s1 = min(P.T, s0 + P.L), nb = (s1 - s0 + 127) / 128;
       for (int n = 0; n < nb && ok; ++n, ++blk) {
@@ -1184,6 +1262,7 @@ __global__ void __launch_bounds__(kDualThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  items_done(P.counter);
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
@@ -1209,7 +1288,8 @@ cudaError_t tc_segment_states(const Problem &p, int seg_len, const void *X, cons
   A.G = (p.T + seg_len - 1) / seg_len;
   A.nitems = A.G * p.B * p.H;
   A.reverse = reverse ? 1 : 0;
-  A.decay = p.decay; A.out = out; A.status = status;
+  if (!status) return cudaErrorInvalidValue;
+  A.decay = p.decay; A.out = out; A.status = status; A.counter = status + kCounterAgg;
   A.gC = p.gC; A.gtot = p.gtot;
   const size_t smem = 3 * 2 * kTileBytes + 1024 + 256;
   const int grid = A.nitems < p.num_sms ? A.nitems : p.num_sms;
@@ -1239,7 +1319,8 @@ cudaError_t tc_dual(const Problem &p, int group_len, const void *q, const void *
   D.nitems = D.G * p.B * p.H;
   D.decay = p.decay; D.ginit = group_init;
   D.dk = static_cast<__nv_bfloat16 *>(dk); D.dv = static_cast<__nv_bfloat16 *>(dv);
-  D.sb = p.sb; D.sh = p.sh; D.st = p.st; D.status = status;
+  if (!status) return cudaErrorInvalidValue;
+  D.sb = p.sb; D.sh = p.sh; D.st = p.st; D.status = status; D.counter = status + kCounterDual;
   D.gC = p.gC;
   D.gk = static_cast<const __nv_bfloat16 *>(p.gk);
   D.gx = p.gx;
@@ -1272,7 +1353,9 @@ cudaError_t tc_main(const Problem &p, int group_len, const void *q, const void *
   M.G = (p.T + group_len - 1) / group_len;
   M.nitems = M.G * p.B * p.H;
   M.init_t = init_transposed ? 1 : 0;
+  if (!status) return cudaErrorInvalidValue;
   M.decay = p.decay; M.ginit = group_init; M.final_state = final_state; M.status = status;
+  M.counter = status + kCounterMain;
   M.agg_out = agg_out;
   M.gC = p.gC;
   M.gq = static_cast<const __nv_bfloat16 *>(p.gq);

@@ -144,14 +144,15 @@ static int cuda_status(cudaError_t e) { return e == cudaSuccess ? LINATTN_OK : L
 constexpr size_t kHeader = 256;  // int32 status word at offset 0
 
 struct FwdLayout {
-  int G = 0, L = 0;
+  GroupPlan gp;
+  int G = 0;
   size_t agg = 0, states = 0, scan = 0, total = kHeader;
 };
 static FwdLayout fwd_layout(const Problem &p, int max_len = 0) {
   FwdLayout w;
   if (!tc_supported(p) || p.T == 0) return w;
-  w.L = tc_group_len(p, max_len);
-  w.G = (p.T + w.L - 1) / w.L;
+  w.gp = tc_group_plan(p, max_len);
+  w.G = w.gp.G;
   const size_t st = (size_t)w.G * p.B * p.H * p.d * p.d * sizeof(float);
   w.agg = kHeader;
   w.states = w.agg + align256(st);
@@ -210,6 +211,15 @@ static GatedLayout gated_layout(const Problem &p) {
 static size_t ckpt_bytes_gated(const Problem &p) {
   const FwdLayout w = fwd_layout(p, kGatedMaxGroup);
   return w.G == 0 ? 0 : ((size_t)w.G + 1) * p.B * p.H * p.d * p.d * sizeof(float);
+}
+
+// Exclusive scan of group aggregates over the groups of a plan (per-head decay
+// across each group by its own length; gates by group_log2).
+static cudaError_t plan_scan(const Problem &p, const GroupPlan &gp, bool reverse, const float *local,
+                             const float *init, float *out, float *total, void *ws, int *status, cudaStream_t s,
+                             const float *group_log2 = nullptr) {
+  return state_scan(gp.G, p.B * p.H, p.d * p.d, nullptr, group_log2 ? nullptr : p.decay, p.H, gp.L, reverse, local,
+                    init, out, total, ws, status, s, group_log2, gp.kb, gp.Ls);
 }
 
 static int check_ws(void *ws, size_t bytes, size_t need) {
@@ -303,11 +313,9 @@ static int32_t fwd_impl(const linattn_shape *shape, const void *q, const void *k
   // -> chunked forward of every group from its entering state
   float *agg = reinterpret_cast<float *>(ws + w.agg);
   float *states = need_ckpt ? ckpt : reinterpret_cast<float *>(ws + w.states);
-  cudaError_t e = tc_segment_states(p, w.L, k, v, false, agg, status, s);
-  if (e == cudaSuccess)
-    e = state_scan(w.G, (int)BH, p.d * p.d, nullptr, p.decay, p.H, w.L, false, agg, init_state, states, nullptr,
-                   ws + w.scan, status, s);
-  if (e == cudaSuccess) e = tc_main(p, w.L, q, k, v, o, states, false, final_state, status, s);
+  cudaError_t e = tc_segment_states(p, w.gp, k, v, false, agg, status, s);
+  if (e == cudaSuccess) e = plan_scan(p, w.gp, false, agg, init_state, states, nullptr, ws + w.scan, status, s);
+  if (e == cudaSuccess) e = tc_main(p, w.gp, q, k, v, o, states, false, final_state, status, s);
   return cuda_status(e);
 }
 
@@ -355,7 +363,8 @@ static int32_t bwd_impl(const linattn_shape *shape, const void *q, const void *k
   }
   if (!tc_supported(p))
     return cuda_status(simt_bwd(p, q, k, v, dO, init_state, d_final, dq, dk, dv, d_init_state, s));
-  const int L = w.f.L, G = w.f.G;
+  const GroupPlan &gp = w.f.gp;
+  const int G = gp.G;
   float *agg = reinterpret_cast<float *>(ws + w.f.agg);
   float *wagg = reinterpret_cast<float *>(ws + w.wagg);
   float *rbar = reinterpret_cast<float *>(ws + w.rbar);
@@ -364,10 +373,8 @@ static int32_t bwd_impl(const linattn_shape *shape, const void *q, const void *k
   const float *states = ckpt;
   if (!need_ckpt) {
     float *st = reinterpret_cast<float *>(ws + w.f.states);
-    e = tc_segment_states(p, L, k, v, false, agg, status, s);
-    if (e == cudaSuccess)
-      e = state_scan(G, (int)BH, p.d * p.d, nullptr, p.decay, p.H, L, false, agg, init_state, st, nullptr,
-                     ws + w.f.scan, status, s);
+    e = tc_segment_states(p, gp, k, v, false, agg, status, s);
+    if (e == cudaSuccess) e = plan_scan(p, gp, false, agg, init_state, st, nullptr, ws + w.f.scan, status, s);
     states = st;
   }
   // dq: the forward-time kernel with (q, k, v) := (dO, v, k), reading every
@@ -376,24 +383,22 @@ static int32_t bwd_impl(const linattn_shape *shape, const void *q, const void *k
   // the end (the value one step before token 0 is d_init = sum_t lambda^{t+1}
   // q_t dO_t^T); without a decay the dq pass accumulates those aggregates too.
   if (!p.decay) {
-    if (e == cudaSuccess) e = tc_main(p, L, dO, v, k, dq, states, true, nullptr, status, s, q, wagg);
+    if (e == cudaSuccess) e = tc_main(p, gp, dO, v, k, dq, states, true, nullptr, status, s, q, wagg);
   } else {
-    if (e == cudaSuccess) e = tc_main(p, L, dO, v, k, dq, states, true, nullptr, status, s);
-    if (e == cudaSuccess) e = tc_segment_states(p, L, q, dO, true, wagg, status, s);
+    if (e == cudaSuccess) e = tc_main(p, gp, dO, v, k, dq, states, true, nullptr, status, s);
+    if (e == cudaSuccess) e = tc_segment_states(p, gp, q, dO, true, wagg, status, s);
   }
   // A gradient D arriving at the final state enters the reverse scan across the
   // last group, whose length may be short of L: fold lambda^{len} D into that
   // group's aggregate, scan from zero, and give the last group D itself.
   const int64_t E = BH * p.d * p.d;
   if (e == cudaSuccess && d_final)
-    e = fold_state(wagg + (int64_t)(G - 1) * E, d_final, p.decay, p.H, p.d * p.d, p.T - (G - 1) * L, E, s);
-  if (e == cudaSuccess)
-    e = state_scan(G, (int)BH, p.d * p.d, nullptr, p.decay, p.H, L, true, wagg, nullptr, rbar, d_init_state,
-                   ws + w.f.scan, status, s);
+    e = fold_state(wagg + (int64_t)(G - 1) * E, d_final, p.decay, p.H, p.d * p.d, gp.len(G - 1, p.T), E, s);
+  if (e == cudaSuccess) e = plan_scan(p, gp, true, wagg, nullptr, rbar, d_init_state, ws + w.f.scan, status, s);
   if (e == cudaSuccess && d_final)
     e = cudaMemcpyAsync(rbar + (int64_t)(G - 1) * E, d_final, state_bytes, cudaMemcpyDeviceToDevice, s);
   // dv and dk in one reverse-time pass from the states Rbar
-  if (e == cudaSuccess) e = tc_dual(p, L, q, k, v, dO, dk, dv, rbar, status, s);
+  if (e == cudaSuccess) e = tc_dual(p, gp, q, k, v, dO, dk, dv, rbar, status, s);
   return cuda_status(e);
 }
 
@@ -454,19 +459,18 @@ int32_t linattn_fwd_gated(const linattn_shape *shape, const void *q, const void 
   }
   // CUDA-core path (fp32 inputs, d = 64): one sequential walk, no checkpoint
   if (!tc_supported(p)) return cuda_status(simt_fwd(p, q, k, v, o, init_state, final_state, nullptr, s, log_gate));
-  const int L = w.f.L, G = w.f.G;
+  const GroupPlan &gp = w.f.gp;
+  const int G = gp.G;
   float *C = reinterpret_cast<float *>(ws + w.C), *tot = reinterpret_cast<float *>(ws + w.tot);
   float *agg = reinterpret_cast<float *>(ws + w.f.agg);
   float *states = static_cast<float *>(checkpoint);
   float *fin = states + (size_t)G * BH * p.d * p.d;  // the checkpoint's final state
-  cudaError_t e = gate_prep(p, L, log_gate, C, tot, s);
+  cudaError_t e = gate_prep(p, gp, log_gate, C, tot, s);
   p.gC = C;
   p.gtot = tot;
-  if (e == cudaSuccess) e = tc_segment_states(p, L, k, v, false, agg, status, s);
-  if (e == cudaSuccess)
-    e = state_scan(G, (int)BH, p.d * p.d, nullptr, nullptr, p.H, L, false, agg, init_state, states, nullptr,
-                   ws + w.f.scan, status, s, tot);
-  if (e == cudaSuccess) e = tc_main(p, L, q, k, v, o, states, false, fin, status, s);
+  if (e == cudaSuccess) e = tc_segment_states(p, gp, k, v, false, agg, status, s);
+  if (e == cudaSuccess) e = plan_scan(p, gp, false, agg, init_state, states, nullptr, ws + w.f.scan, status, s, tot);
+  if (e == cudaSuccess) e = tc_main(p, gp, q, k, v, o, states, false, fin, status, s);
   if (e == cudaSuccess && final_state)
     e = cudaMemcpyAsync(final_state, fin, state_bytes, cudaMemcpyDeviceToDevice, s);
   return cuda_status(e);
@@ -502,32 +506,30 @@ int32_t linattn_bwd_gated(const linattn_shape *shape, const void *q, const void 
   if (!tc_supported(p))
     return cuda_status(simt_bwd(p, q, k, v, dO, init_state, d_final_state, dq, dk, dv, d_init_state, s, log_gate,
                                 d_log_gate));
-  const int L = w.f.L, G = w.f.G;
+  const GroupPlan &gp = w.f.gp;
+  const int G = gp.G;
   float *C = reinterpret_cast<float *>(ws + w.C), *tot = reinterpret_cast<float *>(ws + w.tot);
   float *wagg = reinterpret_cast<float *>(ws + w.wagg), *rbar = reinterpret_cast<float *>(ws + w.rbar);
   const float *states = static_cast<const float *>(checkpoint);
   const float *fin = states + (size_t)G * E;
-  cudaError_t e = gate_prep(p, L, log_gate, C, tot, s);
+  cudaError_t e = gate_prep(p, gp, log_gate, C, tot, s);
   p.gC = C;
   p.gtot = tot;
   p.gq = q;
   p.gk = k;
   p.gx = reinterpret_cast<float *>(ws + w.gx);
   // dq: forward-time kernel with (q, k, v) := (dO, v, k) from the group states (transposed)
-  if (e == cudaSuccess) e = tc_main(p, L, dO, v, k, dq, states, true, nullptr, status, s);
+  if (e == cudaSuccess) e = tc_main(p, gp, dO, v, k, dq, states, true, nullptr, status, s);
   // reverse group aggregates sum_s exp2(C_s) q_s dO_s^T, the final-state gradient folded
   // across the last group, and the reverse scan with every group's own multiplier
-  if (e == cudaSuccess) e = tc_segment_states(p, L, q, dO, true, wagg, status, s);
+  if (e == cudaSuccess) e = tc_segment_states(p, gp, q, dO, true, wagg, status, s);
   if (e == cudaSuccess && d_final_state)
     e = fold_state_log2(wagg + (int64_t)(G - 1) * E, d_final_state, tot + (int64_t)(G - 1) * BH, p.d * p.d, E, s);
-  if (e == cudaSuccess)
-    e = state_scan(G, (int)BH, p.d * p.d, nullptr, nullptr, p.H, L, true, wagg, nullptr, rbar, d_init_state,
-                   ws + w.f.scan, status, s, tot);
+  if (e == cudaSuccess) e = plan_scan(p, gp, true, wagg, nullptr, rbar, d_init_state, ws + w.f.scan, status, s, tot);
   if (e == cudaSuccess && d_final_state)
     e = cudaMemcpyAsync(rbar + (int64_t)(G - 1) * E, d_final_state, state_bytes, cudaMemcpyDeviceToDevice, s);
-  if (e == cudaSuccess) e = tc_dual(p, L, q, k, v, dO, dk, dv, rbar, status, s);
-  if (e == cudaSuccess)
-    e = gate_grad(p, L, p.gx, rbar, states, d_final_state, fin, d_log_gate, s);
+  if (e == cudaSuccess) e = tc_dual(p, gp, q, k, v, dO, dk, dv, rbar, status, s);
+  if (e == cudaSuccess) e = gate_grad(p, gp, p.gx, rbar, states, d_final_state, fin, d_log_gate, s);
   return cuda_status(e);
 }
 
@@ -556,7 +558,7 @@ static int32_t chunk_states_impl(const linattn_shape *shape, int32_t seg_len, co
   int *status = reinterpret_cast<int *>(workspace);
   if (cudaMemsetAsync(workspace, 0, kHeader, s) != cudaSuccess) return LINATTN_ERR_CUDA;
   if (tc_supported(p) && seg_len % 128 == 0)
-    return cuda_status(tc_segment_states(p, seg_len, x, y, reverse, out, status, s));
+    return cuda_status(tc_segment_states(p, GroupPlan::uniform(p.T, seg_len), x, y, reverse, out, status, s));
   return cuda_status(simt_segment_states(p, seg_len, x, y, reverse, out, s));
 }
 

@@ -26,12 +26,13 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 
 // One warp per (sequence, group): inclusive prefix sums in steps of 32 tokens.
-__global__ void __launch_bounds__(256) gate_prep_kernel(const float *lg, int T, int L, int G, int BH, float *C,
+__global__ void __launch_bounds__(256) gate_prep_kernel(const float *lg, int T, GroupPlan gp, int BH, float *C,
                                                         float *tot) {
+  const int G = gp.G;
   const int w = (int)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) / 32), lane = threadIdx.x & 31;
   if (w >= BH * G) return;  // warp-uniform
   const int bh = w / G, g = w % G;
-  const int s0 = g * L, s1 = min(T, s0 + L);
+  const int s0 = gp.start(g), s1 = min(T, gp.start(g + 1));
   const float *src = lg + (int64_t)bh * T;
   float *dst = C + (int64_t)bh * T;
   float carry = 0.f;
@@ -66,10 +67,11 @@ __global__ void fold_log2_kernel(float *w, const float *d, const float *tot, int
 // for the last group it is <D, S_final> (or 0).  Anchoring each group at an
 // exact value keeps the sums short: a running sum over the whole sequence
 // would accumulate the errors of every later token.
-__global__ void __launch_bounds__(256) dgate_kernel(int T, int L, int G, int BH, int DD, const float *gx,
+__global__ void __launch_bounds__(256) dgate_kernel(int T, GroupPlan gp, int BH, int DD, const float *gx,
                                                     const float *rbar, const float *states, const float *D,
                                                     const float *Sfin, float *dlg) {
   __shared__ float wsum[8];
+  const int G = gp.G;
   const int bh = blockIdx.x / G, g = blockIdx.x % G;
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
   // the anchor: <Rbar_g, S_{g+1}> or <D, S_final>
@@ -91,7 +93,7 @@ __global__ void __launch_bounds__(256) dgate_kernel(int T, int L, int G, int BH,
   float carry = 0.f;
   for (int w2 = 0; w2 < 8; ++w2) carry += wsum[w2];
   __syncthreads();
-  const int s0 = g * L, s1 = min(T, s0 + L);
+  const int s0 = gp.start(g), s1 = min(T, gp.start(g + 1));
   for (int te = s1; te > s0; te -= 256) {
     const int ts = max(s0, te - 256), n = te - ts;
     float v = (int)threadIdx.x < n ? gx[(int64_t)bh * T + ts + threadIdx.x] : 0.f;
@@ -116,11 +118,12 @@ __global__ void __launch_bounds__(256) dgate_kernel(int T, int L, int G, int BH,
 
 }  // namespace
 
-cudaError_t gate_prep(const Problem &p, int L, const float *log_gate, float *C, float *tot, cudaStream_t s) {
-  const int G = (p.T + L - 1) / L, BH = p.B * p.H;
-  const int64_t warps = (int64_t)BH * G;
+cudaError_t gate_prep(const Problem &p, const GroupPlan &gp, const float *log_gate, float *C, float *tot,
+                      cudaStream_t s) {
+  const int BH = p.B * p.H;
+  const int64_t warps = (int64_t)BH * gp.G;
   TimedLaunch t(K_GATE, s);
-  gate_prep_kernel<<<(int)((warps + 7) / 8), 256, 0, s>>>(log_gate, p.T, L, G, BH, C, tot);
+  gate_prep_kernel<<<(int)((warps + 7) / 8), 256, 0, s>>>(log_gate, p.T, gp, BH, C, tot);
   return cudaGetLastError();
 }
 
@@ -131,11 +134,11 @@ cudaError_t fold_state_log2(float *w, const float *d, const float *tot_last, int
   return cudaGetLastError();
 }
 
-cudaError_t gate_grad(const Problem &p, int L, const float *gx, const float *rbar, const float *states,
+cudaError_t gate_grad(const Problem &p, const GroupPlan &gp, const float *gx, const float *rbar, const float *states,
                       const float *d_final, const float *final_state, float *dlg, cudaStream_t s) {
-  const int G = (p.T + L - 1) / L, BH = p.B * p.H;
+  const int BH = p.B * p.H;
   TimedLaunch t(K_GATE, s);
-  dgate_kernel<<<BH * G, 256, 0, s>>>(p.T, L, G, BH, p.d * p.d, gx, rbar, states, d_final, final_state, dlg);
+  dgate_kernel<<<BH * gp.G, 256, 0, s>>>(p.T, gp, BH, p.d * p.d, gx, rbar, states, d_final, final_state, dlg);
   return cudaGetLastError();
 }
 

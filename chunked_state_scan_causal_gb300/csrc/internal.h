@@ -25,6 +25,28 @@ struct Problem {
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// ---------------------------------------------------------------- chunk groups
+// How a sequence of T tokens is cut into chunk groups (the units of the state
+// scan and the items of the persistent kernels): kb groups of L tokens, then
+// groups of Ls <= L tokens, the last one possibly shorter.  The long groups
+// come first, so the items a launch hands out last are short ones.  A uniform
+// cut has kb >= G.
+struct GroupPlan {
+  int G = 0, L = 0, kb = 0, Ls = 0;
+  __host__ __device__ int start(int g) const { return g <= kb ? g * L : kb * L + (g - kb) * Ls; }
+  __host__ __device__ int len(int g, int T) const {
+    const int e = start(g + 1);
+    return (e < T ? e : T) - start(g);
+  }
+  static GroupPlan uniform(int T, int L) {
+    GroupPlan gp;
+    gp.G = (T + L - 1) / L;
+    gp.L = gp.Ls = L;
+    gp.kb = gp.G;
+    return gp;
+  }
+};
+
 // LINATTN_OK when the current device is an sm_103 GPU (api.cu).
 int device_ok();
 
@@ -62,10 +84,12 @@ cudaError_t simt_segment_states(const Problem &p, int seg_len, const void *x, co
 // step past the end.
 size_t scan_workspace_bytes(int G, int64_t E);
 // group_log2 (optional, [G][BH], G <= 256): log2 of every group's own multiplier,
-// replacing the uniform one (data-dependent gates).
+// replacing the uniform one (data-dependent gates).  With decay_h, groups from
+// index kb on (G <= 256) have seg_len2 tokens instead of seg_len (a GroupPlan).
 cudaError_t state_scan(int G, int BH, int DD, const float *seg_decay, const float *decay_h, int H,
                        int seg_len, bool reverse, const float *local, const float *init, float *out,
-                       float *total, void *ws, int *status, cudaStream_t s, const float *group_log2 = nullptr);
+                       float *total, void *ws, int *status, cudaStream_t s, const float *group_log2 = nullptr,
+                       int kb = 1 << 30, int seg_len2 = 0);
 
 // w[i] += lambda_h^len d[i] over n = BH * DD elements (h = (i / DD) % H; lambda = 1
 // without decay_h): folds a state entering across a segment of len tokens into
@@ -76,12 +100,12 @@ cudaError_t fold_state(float *w, const float *d, const float *decay_h, int H, in
 // ---------------------------------------------------------------- data-dependent gates (gate.cu)
 // C[t] = log2(e) * sum of log_gate over the group of L tokens up to t ([B,H,T]);
 // tot[g][bh] = C at the group's last token.
-cudaError_t gate_prep(const Problem &p, int L, const float *log_gate, float *C, float *tot, cudaStream_t s);
+cudaError_t gate_prep(const Problem &p, const GroupPlan &gp, const float *log_gate, float *C, float *tot, cudaStream_t s);
 // w[i] += exp2(tot_last[i / DD]) d[i], n elements.
 cudaError_t fold_state_log2(float *w, const float *d, const float *tot_last, int DD, int64_t n, cudaStream_t s);
 // d_log_gate [B,H,T]: reverse sums of gx [B*H][T] (q_t . dq_t - k_t . dk_t) inside each
 // group, plus <rbar[g], states[g+1]> (<d_final, final_state> for the last group).
-cudaError_t gate_grad(const Problem &p, int L, const float *gx, const float *rbar, const float *states,
+cudaError_t gate_grad(const Problem &p, const GroupPlan &gp, const float *gx, const float *rbar, const float *states,
                       const float *d_final, const float *final_state, float *dlg, cudaStream_t s);
 
 // ---------------------------------------------------------------- tensor-core path (tc.cu)
@@ -92,13 +116,13 @@ cudaError_t gate_grad(const Problem &p, int L, const float *gx, const float *rba
 // zero again, so one call may launch a kind more than once).
 constexpr int kCounterAgg = 32, kCounterMain = 34, kCounterDual = 36;
 bool tc_supported(const Problem &p);   // bf16, d = 128
-// Tokens per chunk group (a multiple of 128); max_len > 0 caps it where possible
-// (at least ceil(T / 256) tokens per group remain).
-int tc_group_len(const Problem &p, int max_len = 0);
+// The chunk groups of the tensor-core path (lengths multiples of 128, at most
+// 256 groups); max_len > 0 caps the lengths where possible.
+GroupPlan tc_group_plan(const Problem &p, int max_len = 0);
 // Segment aggregates sum_s w_s x_s y_s^T over groups of seg_len tokens (seg_len
 // a multiple of 128), written as [G][BH][d][d] fp32.
 //   reverse == false: w_s = lambda^{end - s};  reverse == true: w_s = lambda^{s - start + 1}.
-cudaError_t tc_segment_states(const Problem &p, int seg_len, const void *X, const void *Y, bool reverse,
+cudaError_t tc_segment_states(const Problem &p, const GroupPlan &gp, const void *X, const void *Y, bool reverse,
                               float *out, int *status, cudaStream_t s);
 // Per-group causal chunked attention from the given group states
 // [G][BH][d][d] (read transposed when init_transposed): o_i = lambda^{i+1}
@@ -106,7 +130,7 @@ cudaError_t tc_segment_states(const Problem &p, int seg_len, const void *X, cons
 // (optional) is the state after the last token.  x (optional, no decay): also
 // writes agg_out[g] = sum_{s in group g} x_s q_s^T ([G][BH][d][d]) from the
 // same pass.
-cudaError_t tc_main(const Problem &p, int group_len, const void *q, const void *k, const void *v, void *o,
+cudaError_t tc_main(const Problem &p, const GroupPlan &gp, const void *q, const void *k, const void *v, void *o,
                     const float *group_init, bool init_transposed, float *final_state, int *status,
                     cudaStream_t s, const void *x = nullptr, float *agg_out = nullptr);
 
@@ -114,7 +138,7 @@ cudaError_t tc_main(const Problem &p, int group_len, const void *q, const void *
 // reverse group states [G][BH][d][d] (sum over later tokens u of
 // lambda^{u - group end} q_u dO_u^T); equals tc_main(reverse) with roles
 // (k, q, dO) for dv and (v, dO, q) with the transposed states for dk.
-cudaError_t tc_dual(const Problem &p, int group_len, const void *q, const void *k, const void *v,
+cudaError_t tc_dual(const Problem &p, const GroupPlan &gp, const void *q, const void *k, const void *v,
                     const void *dO, void *dk, void *dv, const float *group_init, int *status, cudaStream_t s);
 
 // ---------------------------------------------------------------- TMA descriptors (api.cu)

@@ -34,8 +34,13 @@ namespace {
 constexpr int kWarps = 8;
 constexpr int kVec = 8;  // fp32 elements per lane
 
+// lambda^len: exp2(len * log2 lambda) in fp32 (relative error about 1e-7 * |len * log2 lambda|),
+// 1 for len = 0.  A double-precision pow per thread cost more than the scan's memory traffic.
+__device__ __forceinline__ float pow_len(float lam, int len) { return len == 0 ? 1.f : exp2f(log2f(lam) * (float)len); }
+
 struct ScanArgs {
   int G, BH, DD, H, seg_len, ntg, ncg, reverse;
+  int kb, seg_len2;    // with decay_h (column form): groups kb.. have seg_len2 tokens
   const float *seg_decay, *decay_h, *local, *init;
   const float *glog2;  // [G][BH] log2 of each group's own multiplier (column form only), or null
   float *out, *total;
@@ -77,7 +82,7 @@ __global__ void __launch_bounds__(kWarps * 32) scan_kernel(ScanArgs A) {
     const int bh = (int)(e0 / A.DD);
     float a = 1.f;
     if (A.seg_decay) a = A.seg_decay[bh];
-    else if (A.decay_h) a = (float)pow((double)A.decay_h[bh % A.H], (double)A.seg_len);
+    else if (A.decay_h) a = pow_len(A.decay_h[bh % A.H], A.seg_len);
 
     // processing index p = tg*32 + lane; segment g = p (forward) or G-1-p (reverse)
     const int pidx = tg * 32 + lane;
@@ -211,9 +216,13 @@ __global__ void __launch_bounds__(256) scan_columns_kernel(ScanArgs A) {
   for (int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c < n4; c += (int64_t)gridDim.x * blockDim.x) {
     const int64_t e0 = c * 4;
     const int bh = (int)(e0 / A.DD);
-    float a = 1.f;
-    if (A.seg_decay) a = A.seg_decay[bh];
-    else if (A.decay_h) a = (float)pow((double)A.decay_h[bh % A.H], (double)A.seg_len);
+    float a = 1.f, a2 = 1.f;  // multipliers across a group of seg_len, of seg_len2 tokens
+    if (A.seg_decay) {
+      a = a2 = A.seg_decay[bh];
+    } else if (A.decay_h) {
+      a = pow_len(A.decay_h[bh % A.H], A.seg_len);
+      a2 = A.kb < A.G ? pow_len(A.decay_h[bh % A.H], A.seg_len2) : a;
+    }
     float4 acc = A.init ? __ldg(reinterpret_cast<const float4 *>(A.init + e0)) : make_float4(0.f, 0.f, 0.f, 0.f);
     for (int i = 0; i < A.G; i += kColumnDepth) {
       float4 u[kColumnDepth];
@@ -228,7 +237,7 @@ __global__ void __launch_bounds__(256) scan_columns_kernel(ScanArgs A) {
         if (p < A.G) {
           *reinterpret_cast<float4 *>(A.out + (int64_t)g * E + e0) = acc;
           // the combine across group g decays by that group's multiplier
-          const float ag = A.glog2 ? exp2f(A.glog2[(int64_t)g * A.BH + bh]) : a;
+          const float ag = A.glog2 ? exp2f(A.glog2[(int64_t)g * A.BH + bh]) : (g < A.kb ? a : a2);
           acc = make_float4(fmaf(ag, acc.x, u[j].x), fmaf(ag, acc.y, u[j].y), fmaf(ag, acc.z, u[j].z),
                             fmaf(ag, acc.w, u[j].w));
         }
@@ -249,7 +258,7 @@ size_t scan_workspace_bytes(int G, int64_t E) {
 namespace {
 __global__ void fold_kernel(float *w, const float *d, const float *decay_h, int H, int DD, int len, int64_t n) {
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
-    const float a = decay_h ? (float)pow((double)decay_h[(i / DD) % H], (double)len) : 1.f;
+    const float a = decay_h ? pow_len(decay_h[(i / DD) % H], len) : 1.f;
     w[i] = fmaf(a, d[i], w[i]);
   }
 }
@@ -265,11 +274,13 @@ cudaError_t fold_state(float *w, const float *d, const float *decay_h, int H, in
 
 cudaError_t state_scan(int G, int BH, int DD, const float *seg_decay, const float *decay_h, int H,
                        int seg_len, bool reverse, const float *local, const float *init, float *out,
-                       float *total, void *ws, int *status, cudaStream_t s, const float *group_log2) {
+                       float *total, void *ws, int *status, cudaStream_t s, const float *group_log2, int kb,
+                       int seg_len2) {
   const int64_t E = (int64_t)BH * DD;
-  if (group_log2 && G > kColumnMaxG) return cudaErrorInvalidValue;
+  if ((group_log2 || kb < G) && G > kColumnMaxG) return cudaErrorInvalidValue;
   ScanArgs A;
   A.G = G; A.BH = BH; A.DD = DD; A.H = H; A.seg_len = seg_len;
+  A.kb = kb; A.seg_len2 = seg_len2;
   A.ntg = (G + 31) / 32;
   A.ncg = (int)(E / kVec);
   A.reverse = reverse ? 1 : 0;

@@ -24,11 +24,15 @@ namespace linattn {
 
 bool tc_supported(const Problem &p) { return p.dtype == 0 && p.d == 128 && p.T >= 1; }
 
-int tc_group_len(const Problem &p, int max_len) {
-  // The persistent kernels give each CTA whole (group, sequence) items, so a
-  // launch lasts about ceil(items / SMs) waves of one item each.  Pick the
-  // group count G (at most 256 per sequence: the scan's column-parallel form)
-  // whose group length L (a multiple of 128 tokens, at least 256) minimises
+// The tail of short groups (tc_group_plan): the last kTailNum / kTailDen of a
+// sequence in groups of L / kTailDiv tokens, from kTailMinWaves waves of items.
+constexpr int kTailNum = 1, kTailDen = 10, kTailDiv = 2, kTailMinWaves = 3;
+
+GroupPlan tc_group_plan(const Problem &p, int max_len) {
+  // The persistent kernels hand out whole (group, sequence) items, so a launch
+  // lasts about ceil(items / SMs) waves of one item each.  Pick the group count
+  // G (at most 256 per sequence: the scan's column-parallel form) whose group
+  // length L (a multiple of 128 tokens, at least 256) minimises
   //     waves(G) * (L / 128 + 1),
   // the "+ 1" standing for an item's fixed cost (its entering state, its
   // outputs at the end) in units of one 128-token block.  Ties go to longer
@@ -50,7 +54,24 @@ int tc_group_len(const Problem &p, int max_len) {
   }
   // (G = 256 always qualifies, so bestL is set)
   const int64_t Tr = (T + 127) / 128 * 128;
-  return (int)(bestL < Tr ? bestL : Tr);
+  const int L = (int)(bestL < Tr ? bestL : Tr);
+  GroupPlan gp = GroupPlan::uniform((int)T, L);
+  // CTAs do not all stream at the same rate (measured with a fixed share of
+  // items per CTA: the last CTA of a launch ended up to 15 % after the median
+  // one).  With items drawn at run time, cutting the last tenth of every
+  // sequence into groups of half the length lets the faster CTAs take the short
+  // items at the end.  Worth it only with several waves of items.
+  const int64_t waves = (BH * gp.G + sms - 1) / sms;
+  if (waves < kTailMinWaves) return gp;
+  const int Ls = std::max(256, (L / kTailDiv + 127) / 128 * 128);
+  const int kb = (int)(T * (kTailDen - kTailNum) / ((int64_t)kTailDen * L));
+  if (Ls >= L || kb < 1) return gp;
+  const int64_t rest = T - (int64_t)kb * L, Gs = (rest + Ls - 1) / Ls;
+  if (kb + Gs > 256) return gp;
+  gp.G = kb + (int)Gs;
+  gp.kb = kb;
+  gp.Ls = Ls;
+  return gp;
 }
 
 namespace {
@@ -153,7 +174,8 @@ __device__ __forceinline__ void ld_chunk(uint32_t taddr, float (&x)[32]) {
 
 // ============================================================================ segment aggregates
 struct AggParams {
-  int B, H, T, L, G, nitems, reverse;
+  int B, H, T, nitems, reverse;
+  GroupPlan gp;
   const float *decay;
   float *out;
   int *status;
@@ -215,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int k = 0, item; ok; ++k) {
         if (!(ok = ring_post(ring, k, P.counter, P.nitems, item, &abort_flag, P.status, detail)) || item < 0) break;
         const int g = item / BH, bh = item % BH, b = bh / P.H, h = bh % P.H;
-        const int s0 = g * P.L, s1 = min(P.T, s0 + P.L);
+        const int s0 = P.gp.start(g), s1 = min(P.T, P.gp.start(g + 1));
         for (int t0 = s0; t0 < s1; t0 += 128, ++it) {
           const int s = it % NS, u = it / NS;
           if (u > 0 && !(ok = mbar_wait(&empty[s], (u - 1) & 1, &abort_flag, P.status, detail))) break;
@@ -243,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int k = 0, item; ok; ++k) {
         if (!(ok = ring_take(ring, k, item, &abort_flag, P.status, detail)) || item < 0) break;
         const int g = item / BH;
-        const int s0 = g * P.L, s1 = min(P.T, s0 + P.L);
+        const int s0 = P.gp.start(g), s1 = min(P.T, P.gp.start(g + 1));
         const int a = ai & 1, ua = ai >> 1;
         if (ua > 0 && !(ok = mbar_wait(&acce[a], (ua - 1) & 1, &abort_flag, P.status, detail))) break;
         tc_fence_after();
@@ -275,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = __all_sync(0xffffffffu, ring_take(ring, k, item, &abort_flag, P.status, detail))) || item < 0)
           break;
         const int g = item / BH, bh = item % BH, h = bh % P.H;
-        const int s0 = g * P.L, s1 = min(P.T, s0 + P.L);
+        const int s0 = P.gp.start(g), s1 = min(P.T, P.gp.start(g + 1));
         const float l2 = GATE ? 0.f : log2f(P.decay[h]);
         const float *gc = GATE ? P.gC + (int64_t)bh * P.T : nullptr;
         const float gt = GATE ? P.gtot[(int64_t)g * BH + bh] : 0.f;
@@ -324,7 +346,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ============================================================================ per-group main kernel
 struct MainParams {
-  int B, H, T, L, G, nitems, init_t;
+  int B, H, T, nitems, init_t;
+  GroupPlan gp;
   const float *decay;
   const float *ginit;  // [G][BH][d][d]
   float *final_state;  // [BH][d][d] or null
@@ -531,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int k = 0, item; ok; ++k) {
         if (!(ok = ring_post(ring, k, P.counter, P.nitems, item, &abort_flag, P.status, detail)) || item < 0) break;
         const int g = item / BH, bh = item % BH, b = bh / P.H, h = bh % P.H;
-        const int s0 = g * P.L, s1 = min(P.T, s0 + P.L), nb = (s1 - s0 + 127) / 128;
+        const int s0 = P.gp.start(g), s1 = min(P.T, P.gp.start(g + 1)), nb = (s1 - s0 + 127) / 128;
         bulk_prefetch_l2(P.ginit + ((int64_t)g * BH + bh) * 16384, 16384 * 4);  // the entering state
         for (int n = 0; n < nb && ok; ++n, ++blk) {
           const int t0 = s0 + 128 * n;
@@ -567,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int k = 0, item; ok; ++k, ++it) {
         if (!(ok = ring_take(ring, k, item, &abort_flag, P.status, detail)) || item < 0) break;
         const int g = item / BH;
-        const int s0 = g * P.L, s1 = min(P.T, s0 + P.L), nb = (s1 - s0 + 127) / 128;
+        const int s0 = P.gp.start(g), s1 = min(P.T, P.gp.start(g + 1)), nb = (s1 - s0 + 127) / 128;
         for (int n = 0; n < nb; ++n, ++blk) {
           const int tq = tile_of(blk, 0), tk = tile_of(blk, 1), tv = tile_of(blk, 2), tx = tile_of(blk, 3);
           const uint32_t Q = slot_addr(tq), K = slot_addr(tk), V = slot_addr(tv);
@@ -630,7 +653,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int k = 0, item; ok; ++k) {
       if (!(ok = group_all(ring_take(ring, k, item, &abort_flag, P.status, detail), 2, 128)) || item < 0) break;
       const int g = item / BH, bh = item % BH, b = bh / P.H, h = bh % P.H;
-      const int s0 = g * P.L, s1 = min(P.T, s0 + P.L), nb = (s1 - s0 + 127) / 128;
+      const int s0 = P.gp.start(g), s1 = min(P.T, P.gp.start(g + 1)), nb = (s1 - s0 + 127) / 128;
       const float lam = (DECAY && !GATE) ? P.decay[h] : 1.f;
       const float l2 = (DECAY && !GATE) ? log2f(lam) : 0.f;
       const float *gc = GATE ? P.gC + (int64_t)bh * P.T : nullptr;
@@ -716,7 +739,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!(ok = __all_sync(0xffffffffu, ring_take(ring, k, item, &abort_flag, P.status, detail))) || item < 0)
         break;
       const int g = item / BH, bh = item % BH, h = bh % P.H;
-      const int s0 = g * P.L, s1 = min(P.T, s0 + P.L), nb = (s1 - s0 + 127) / 128;
+      const int s0 = P.gp.start(g), s1 = min(P.T, P.gp.start(g + 1)), nb = (s1 - s0 + 127) / 128;
       const float lam = (DECAY && !GATE) ? P.decay[h] : 1.f;
       const float l2 = (DECAY && !GATE) ? log2f(lam) : 0.f;
       const float *gc = GATE ? P.gC + (int64_t)bh * P.T : nullptr;
@@ -803,7 +826,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_before();
           mbar_arrive(&bar[B_WEMPTY]);
-        } else if (P.final_state && g == P.G - 1) {
+        } else if (P.final_state && g == P.gp.G - 1) {
           float *dst = P.final_state + (int64_t)bh * 16384 + row * 128;
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
@@ -840,7 +863,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // following score product may overwrite them).  That leaves shared memory for
 // six input tiles.  Warps 12..15 (group C) write dv and dk from registers.
 struct DualParams {
-  int B, H, T, L, G, nitems;
+  int B, H, T, nitems;
+  GroupPlan gp;
   const float *decay;
   const float *ginit;  // [G][BH][d][d] reverse states entering each group
   __nv_bfloat16 *dk, *dv;
@@ -952,7 +976,7 @@ __global__ void __launch_bounds__(kDualThreads, 1)
       for (int k = 0, item; ok; ++k) {
         if (!(ok = ring_post(ring, k, P.counter, P.nitems, item, &abort_flag, P.status, detail)) || item < 0) break;
         const int g = item / BH, bh = item % BH, b = bh / P.H, h = bh % P.H;
-        const int s0 = g * P.L, s1 = min(P.T, s0 + P.L), nb = (s1 - s0 + 127) / 128;
+        const int s0 = P.gp.start(g), s1 = min(P.T, P.gp.start(g + 1)), nb = (s1 - s0 + 127) / 128;
         bulk_prefetch_l2(P.ginit + ((int64_t)g * BH + bh) * 16384, 16384 * 4);  // the entering state
         for (int n = 0; n < nb && ok; ++n, ++blk) {
           const int t0 = s0 + 128 * (nb - 1 - n);
@@ -1002,7 +1026,7 @@ __global__ void __launch_bounds__(kDualThreads, 1)
       for (int k = 0, item; ok; ++k) {
         if (!(ok = ring_take(ring, k, item, &abort_flag, P.status, detail)) || item < 0) break;
         const int g = item / BH;
-        const int s0 = g * P.L, s1 = min(P.T, s0 + P.L), nb = (s1 - s0 + 127) / 128;
+        const int s0 = P.gp.start(g), s1 = min(P.T, P.gp.start(g + 1)), nb = (s1 - s0 + 127) / 128;
         for (int n = 0; n < nb && ok; ++n, ++blk) {
           const uint32_t K = addr(0), Q = addr(1), DO = addr(2), V = addr(3);
           const int u1 = 2 * blk, u2 = u1 + 1;
@@ -1071,7 +1095,7 @@ __global__ void __launch_bounds__(kDualThreads, 1)
     for (int k = 0, item; ok; ++k) {
       if (!(ok = group_all(ring_take(ring, k, item, &abort_flag, P.status, detail), 3, 128)) || item < 0) break;
       const int g = item / BH, bh = item % BH, h = bh % P.H;
-      const int s0 = g * P.L, s1 = min(P.T, s0 + P.L), nb = (s1 - s0 + 127) / 128;
+      const int s0 = P.gp.start(g), s1 = min(P.T, P.gp.start(g + 1)), nb = (s1 - s0 + 127) / 128;
       const float lam = (DECAY && !GATE) ? P.decay[h] : 1.f;
       const float l2 = (DECAY && !GATE) ? log2f(lam) : 0.f;
       const float *gc = GATE ? P.gC + (int64_t)bh * P.T : nullptr;
@@ -1126,7 +1150,7 @@ __global__ void __launch_bounds__(kDualThreads, 1)
       if (!(ok = __all_sync(0xffffffffu, ring_take(ring, k, item, &abort_flag, P.status, detail))) || item < 0)
         break;
       const int g = item / BH, bh = item % BH, h = bh % P.H;
-      const int s0 = g * P.L, s1 = min(P.T, s0 + P.L), nb = (s1 - s0 + 127) / 128;
+      const int s0 = P.gp.start(g), s1 = min(P.T, P.gp.start(g + 1)), nb = (s1 - s0 + 127) / 128;
       const float lam = (DECAY && !GATE) ? P.decay[h] : 1.f;
       const float l2 = (DECAY && !GATE) ? log2f(lam) : 0.f;
       const float *gc = GATE ? P.gC + (int64_t)bh * P.T : nullptr;
@@ -1224,7 +1248,7 @@ __global__ void __launch_bounds__(kDualThreads, 1)
       if (!(ok = __all_sync(0xffffffffu, ring_take(ring, k, item, &abort_flag, P.status, detail))) || item < 0)
         break;
       const int g = item / BH, bh = item % BH, b = bh / P.H, h = bh % P.H;
-      const int s0 = g * P.L, s1 = min(P.T, s0 + P.L), nb = (s1 - s0 + 127) / 128;
+      const int s0 = P.gp.start(g), s1 = min(P.T, P.gp.start(g + 1)), nb = (s1 - s0 + 127) / 128;
       for (int n = 0; n < nb && ok; ++n, ++blk) {
         const int t0 = s0 + 128 * (nb - 1 - n);
         const bool valid = t0 + (int)row < s1;
@@ -1279,14 +1303,13 @@ cudaError_t set_smem(K kern, size_t bytes) {
 
 }  // namespace
 
-cudaError_t tc_segment_states(const Problem &p, int seg_len, const void *X, const void *Y, bool reverse,
+cudaError_t tc_segment_states(const Problem &p, const GroupPlan &gp, const void *X, const void *Y, bool reverse,
                               float *out, int *status, cudaStream_t s) {
   alignas(64) CUtensorMap mx, my;
   if (!seq_tmap(p, X, &mx) || !seq_tmap(p, Y, &my)) return cudaErrorInvalidValue;
   AggParams A;
-  A.B = p.B; A.H = p.H; A.T = p.T; A.L = seg_len;
-  A.G = (p.T + seg_len - 1) / seg_len;
-  A.nitems = A.G * p.B * p.H;
+  A.B = p.B; A.H = p.H; A.T = p.T; A.gp = gp;
+  A.nitems = gp.G * p.B * p.H;
   A.reverse = reverse ? 1 : 0;
   if (!status) return cudaErrorInvalidValue;
   A.decay = p.decay; A.out = out; A.status = status; A.counter = status + kCounterAgg;
@@ -1308,15 +1331,14 @@ cudaError_t tc_segment_states(const Problem &p, int seg_len, const void *X, cons
   return cudaGetLastError();
 }
 
-cudaError_t tc_dual(const Problem &p, int group_len, const void *q, const void *k, const void *v,
+cudaError_t tc_dual(const Problem &p, const GroupPlan &gp, const void *q, const void *k, const void *v,
                     const void *dO, void *dk, void *dv, const float *group_init, int *status, cudaStream_t s) {
   alignas(64) CUtensorMap mk, mq, mv, mdo;
   if (!seq_tmap(p, k, &mk) || !seq_tmap(p, q, &mq) || !seq_tmap(p, v, &mv) || !seq_tmap(p, dO, &mdo))
     return cudaErrorInvalidValue;
   DualParams D;
-  D.B = p.B; D.H = p.H; D.T = p.T; D.L = group_len;
-  D.G = (p.T + group_len - 1) / group_len;
-  D.nitems = D.G * p.B * p.H;
+  D.B = p.B; D.H = p.H; D.T = p.T; D.gp = gp;
+  D.nitems = gp.G * p.B * p.H;
   D.decay = p.decay; D.ginit = group_init;
   D.dk = static_cast<__nv_bfloat16 *>(dk); D.dv = static_cast<__nv_bfloat16 *>(dv);
   if (!status) return cudaErrorInvalidValue;
@@ -1340,7 +1362,7 @@ cudaError_t tc_dual(const Problem &p, int group_len, const void *q, const void *
   return cudaGetLastError();
 }
 
-cudaError_t tc_main(const Problem &p, int group_len, const void *q, const void *k, const void *v, void *o,
+cudaError_t tc_main(const Problem &p, const GroupPlan &gp, const void *q, const void *k, const void *v, void *o,
                     const float *group_init, bool init_transposed, float *final_state, int *status,
                     cudaStream_t s, const void *x, float *agg_out) {
   if (x && (p.decay || p.gC || !agg_out)) return cudaErrorInvalidValue;
@@ -1349,9 +1371,8 @@ cudaError_t tc_main(const Problem &p, int group_len, const void *q, const void *
       !seq_tmap(p, x ? x : q, &mx))
     return cudaErrorInvalidValue;
   MainParams M;
-  M.B = p.B; M.H = p.H; M.T = p.T; M.L = group_len;
-  M.G = (p.T + group_len - 1) / group_len;
-  M.nitems = M.G * p.B * p.H;
+  M.B = p.B; M.H = p.H; M.T = p.T; M.gp = gp;
+  M.nitems = gp.G * p.B * p.H;
   M.init_t = init_transposed ? 1 : 0;
   if (!status) return cudaErrorInvalidValue;
   M.decay = p.decay; M.ginit = group_init; M.final_state = final_state; M.status = status;

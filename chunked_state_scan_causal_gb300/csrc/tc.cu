@@ -1,8 +1,8 @@
 // Tensor-core kernels (tcgen05 + TMEM + TMA) for bf16 sequences with d = 128.
 //
-// Both kernels are persistent (one CTA per SM, items taken round-robin) and
-// warp-specialised:
-//   warp 0        TMA producer (one thread)
+// The kernels are persistent (one CTA per SM; (group, sequence) items drawn
+// at run time, see ItemRing) and warp-specialised:
+//   warp 0        TMA producer and item drawer (one thread)
 //   warp 1        TMEM allocator and MMA issuer (one thread)
 //   warps 4..7    epilogue group A (TMEM -> registers -> shared / global)
 //   warps 8..11   epilogue group B

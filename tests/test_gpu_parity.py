@@ -178,6 +178,30 @@ def test_forward_strided_segments_view():
     assert rel(o_one, ro) < 1e-2
 
 
+@pytest.mark.parametrize("width,off", [(136, 0), (144, 8)])
+def test_backward_padded_rows(width, off):
+    """Rows padded in memory (strides of 272 or 288 bytes; the second view also
+    starts 16 bytes off a 32-byte boundary), for the inputs and the outputs: the
+    dk/dv pass writes whole 32-byte sectors only where every row starts on a
+    32-byte boundary, and 16-byte pieces otherwise."""
+    B, H, T, d = 1, 2, 1000, 128
+    c, dev = case(17, B, H, T, d, torch.bfloat16)
+
+    def padded(x):
+        buf = torch.zeros(B, H, T, width, dtype=x.dtype, device=x.device)
+        view = buf[..., off:off + d]
+        view.copy_(x)
+        return view
+
+    q, k, v, dO = (padded(dev[w]) for w in ("q", "k", "v", "dO"))
+    outs = [padded(torch.zeros_like(dev["q"])) for _ in range(3)]
+    dq, dk, dv, _ = la.bwd(q, k, v, dO, outs=outs)
+    torch.cuda.synchronize()
+    rq, rk, rv, _ = oracle.bwd_recurrent(c["q"], c["k"], c["v"], c["dO"])
+    for got, ref in ((dq, rq), (dk, rk), (dv, rv)):
+        assert rel(got, ref) < 1e-2
+
+
 # ------------------------------------------------------------------ backward
 @pytest.mark.parametrize("dtype,d", [(torch.bfloat16, 128), (torch.bfloat16, 64), (torch.float32, 64)])
 @pytest.mark.parametrize("T", [64, 200, 1000, 2048])

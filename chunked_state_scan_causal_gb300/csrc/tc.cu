@@ -883,8 +883,27 @@ constexpr uint32_t kDualOffSh = kDualSlots * kTileBytes;  // bf16 state tile
 constexpr uint32_t kDualOffBar = kDualOffSh + kTileBytes;
 constexpr uint32_t kDualOffGate = kDualOffBar + 256;  // GATE: a block's 128 sums, 128 column factors
 constexpr size_t kDualSmem = kDualOffGate + 1024 + 1024;
+// D_KS, D_DS, D_VS: the K, dO and V tiles of a block weighted in place (two
+// barriers each, by block parity, so that an arrival for block n + 2 can only
+// follow the MMA thread's wait for block n).
 enum { D_FULL = 0, D_EMPTY = kDualSlots, D_PFULL = 2 * kDualSlots, D_PSFULL, D_O1FULL, D_O1EMPTY, D_O2FULL,
-       D_O2EMPTY, D_SFULL, D_PRE, D_KSC, D_VSC, D_COUNT };
+       D_O2EMPTY, D_SFULL, D_PRE, D_KS, D_DS = D_KS + 2, D_VS = D_DS + 2, D_COUNT = D_VS + 2 };
+static_assert(D_COUNT * 8 + 4 <= 256, "dual kernel barriers and the TMEM slot fit their 256 bytes");
+
+// Per-head decays lambda >= kDualWeightedMin take the weighted-operand form of
+// the dk/dv pass: the rows of K and V are weighted by lambda^{nv-1-i} and those
+// of dO by lambda^{j+1} as soon as their tiles land, before any product reads
+// them, and both score tiles then need the 0/1 anti-causal mask times the one
+// scalar lambda^{-nv}:
+//   (K' Q^T)_ij = lambda^{nv-1-i} k_i.q_j, and dv += P^1 dO' with
+//       P^1 = lambda^{-nv} [j >= i] K' Q^T gives lambda^{j-i} (k_i.q_j) dO_j;
+//   (V' dO'^T)_ij = lambda^{nv+j-i} v_i.dO_j, and lambda^{-nv} [j >= i] of it
+//       is the masked P2 of dk.
+// The factors stay within lambda^{-128} .. lambda^{255}, i.e. 2^{+-83} for
+// lambda >= 0.8, far inside fp32 and bf16 range.  Smaller decays weight the
+// tiles between the products (score tiles from unweighted operands, masks
+// per element), which puts the weighting on the critical path of the block.
+constexpr float kDualWeightedMin = 0.8f;
 
 // Ring slot of tile x (0 K, 1 Q, 2 dO, 3 V) of the blk-th block a CTA
 // processes, and how many loads that slot received before it.  Tiles are
@@ -963,8 +982,11 @@ __global__ void __launch_bounds__(kDualThreads, 1)
     mbar_init(&bar[D_O2EMPTY], 128);
     mbar_init(&bar[D_SFULL], 1);
     mbar_init(&bar[D_PRE], 128);
-    mbar_init(&bar[D_KSC], 128);
-    mbar_init(&bar[D_VSC], 128);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar[D_KS + i], 128);
+      mbar_init(&bar[D_DS + i], 128);
+      mbar_init(&bar[D_VS + i], 128);
+    }
     ring_init(ring, 1 + 3 * 128);  // readers: MMA thread, groups A, B and C
     fence_mbar_init();
     prefetch_tensormap(&mk);
@@ -1045,50 +1067,54 @@ __global__ void __launch_bounds__(kDualThreads, 1)
         if (!(ok = ring_take(ring, k, item, &abort_flag, P.status, detail)) || item < 0) break;
         const int g = item / BH;
         const int s0 = P.gp.start(g), s1 = min(P.T, P.gp.start(g + 1)), nb = (s1 - s0 + 127) / 128;
+        // weighted-operand form: K, dO, V are weighted before their first product
+        const bool wtd = DECAY && !GATE && P.decay[(item % BH) % P.H] >= kDualWeightedMin;
+        // the decay-free order (R updated right after dv's state term)
+        const bool early_r = !DECAY || wtd;
         for (int n = 0; n < nb && ok; ++n, ++blk) {
           const uint32_t K = addr(0), Q = addr(1), DO = addr(2), V = addr(3);
-          const int u1 = 2 * blk, u2 = u1 + 1;
+          const int u1 = 2 * blk, u2 = u1 + 1, wb = blk & 1, wp = blk >> 1;
           // P1 = K Q^T  (the previous block's P2~ has been consumed: issue order)
-          if (!(ok = full(0) && full(1))) break;
+          if (!(ok = (wtd ? wait(D_KS + wb, wp) : full(0)) && full(1))) break;
           tc_fence_after();
 #pragma unroll
           for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tP, desc_kmajor(K, ks), desc_kmajor(Q, ks), id_kk, ks > 0);
           mma_commit(&bar[D_PFULL]);
           // dv = K' R   (R from the bf16 state tile, MN-major)
-          ok = (!DECAY || wait(D_KSC, blk)) && wait(D_PRE, blk) && (blk == 0 || wait(D_O1EMPTY, blk - 1));
+          ok = (!DECAY || wtd || wait(D_KS + wb, wp)) && wait(D_PRE, blk) && (blk == 0 || wait(D_O1EMPTY, blk - 1));
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
           for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tO1, desc_kmajor(K, ks), desc_mnmajor(sSh, ks), id_km, ks > 0);
           release(0);
-          if (!DECAY) {
-            // R += Q^T dO (the state tile is rewritten only after SFULL, below)
-            if (!(ok = full(2))) break;
+          if (early_r) {
+            // R += Q^T dO' (the state tile is rewritten only after SFULL, below)
+            if (!(ok = wtd ? wait(D_DS + wb, wp) : full(2))) break;
             tc_fence_after();
 #pragma unroll
             for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tR, desc_mnmajor(Q, ks), desc_mnmajor(DO, ks), id_mm, 1u);
           }
           // dv += P1~ dO   (P1~ in TMEM as bf16 pairs)
-          if (!(ok = (DECAY ? full(2) : true) && wait(D_PSFULL, u1))) break;
+          if (!(ok = (early_r ? true : full(2)) && wait(D_PSFULL, u1))) break;
           tc_fence_after();
 #pragma unroll
           for (uint32_t ks = 0; ks < 8; ++ks) mma_ts(tO1, tP + ks * 8, desc_mnmajor(DO, ks), id_km, 1u);
           mma_commit(&bar[D_O1FULL]);
           // P2 = V dO^T
-          if (!(ok = full(3))) break;
+          if (!(ok = wtd ? wait(D_VS + wb, wp) : full(3))) break;
           tc_fence_after();
 #pragma unroll
           for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tP, desc_kmajor(V, ks), desc_kmajor(DO, ks), id_kk, ks > 0);
           mma_commit(&bar[D_PFULL]);
-          if (!DECAY) release(2);
+          if (early_r) release(2);
           // dk = V' R^T  (the state tile read K-major)
-          ok = (!DECAY || wait(D_VSC, blk)) && (blk == 0 || wait(D_O2EMPTY, blk - 1));
+          ok = (early_r || wait(D_VS + wb, wp)) && (blk == 0 || wait(D_O2EMPTY, blk - 1));
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
           for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tO2, desc_kmajor(V, ks), desc_kmajor(sSh, ks), id_kk, ks > 0);
           release(3);
-          if (DECAY) {
+          if (!early_r) {
             // R += Q^T dO'  (dO rows weighted together with V's)
 #pragma unroll
             for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tR, desc_mnmajor(Q, ks), desc_mnmajor(DO, ks), id_mm, 1u);
@@ -1116,8 +1142,11 @@ __global__ void __launch_bounds__(kDualThreads, 1)
       const int s0 = P.gp.start(g), s1 = min(P.T, P.gp.start(g + 1)), nb = (s1 - s0 + 127) / 128;
       const float lam = (DECAY && !GATE) ? P.decay[h] : 1.f;
       const float l2 = (DECAY && !GATE) ? log2f(lam) : 0.f;
+      const bool wtd = DECAY && !GATE && lam >= kDualWeightedMin;
       const float *gc = GATE ? P.gC + (int64_t)bh * P.T : nullptr;
       for (int n = 0; n < nb && ok; ++n, ++blk) {
+        // weighted operands: both score tiles take lambda^{-nv} inside the mask
+        const float wsc = wtd ? exp2f(-l2 * (float)min(128, s1 - (s0 + 128 * (nb - 1 - n)))) : 1.f;
         float ci = 0.f;
         float *cb = reinterpret_cast<float *>(smem + kDualOffGate), *cw = cb + 128;
         if (GATE) {
@@ -1140,10 +1169,15 @@ __global__ void __launch_bounds__(kDualThreads, 1)
           for (int c = 0; c < 4; ++c) {
             float x[32];
             ld_chunk(tP + lb + c * 32, x);
-            if (GATE)
+            if (GATE) {
               mask_chunk_gate<true>(x, (int)row, c, ci, cb, cw);
-            else
+            } else if (wtd) {
+              mask_chunk<false, true>(x, (int)row, c, 1.f, 0.f);
+#pragma unroll
+              for (int j = 0; j < 32; ++j) x[j] *= wsc;
+            } else {
               mask_chunk<DECAY, true>(x, (int)row, c, lam, l2);
+            }
             uint32_t r[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) r[j] = pack_bf16(x[2 * j], x[2 * j + 1]);
@@ -1164,6 +1198,17 @@ __global__ void __launch_bounds__(kDualThreads, 1)
     auto wait = [&](int idx, int parity) {
       return __all_sync(0xffffffffu, mbar_wait(&bar[idx], parity & 1, &abort_flag, P.status, detail));
     };
+    // Weight this thread's row of tile x (0 K, 2 dO, 3 V) of CTA block b once it
+    // has landed, then arrive on the tile's barrier (bar_idx + block parity).
+    auto weigh = [&](int b, int x, float w, int bar_idx) {
+      int s, c;
+      dual_slot(b, x, s, c);
+      if (!wait(D_FULL + s, c)) return false;
+      scale_tile_row(tile_addr(s), row, w);
+      fence_proxy_async_smem();
+      mbar_arrive(&bar[bar_idx + (b & 1)]);
+      return true;
+    };
     for (int k = 0, item; ok; ++k) {
       if (!(ok = __all_sync(0xffffffffu, ring_take(ring, k, item, &abort_flag, P.status, detail))) || item < 0)
         break;
@@ -1171,6 +1216,7 @@ __global__ void __launch_bounds__(kDualThreads, 1)
       const int s0 = P.gp.start(g), s1 = min(P.T, P.gp.start(g + 1)), nb = (s1 - s0 + 127) / 128;
       const float lam = (DECAY && !GATE) ? P.decay[h] : 1.f;
       const float l2 = (DECAY && !GATE) ? log2f(lam) : 0.f;
+      const bool wtd = DECAY && !GATE && lam >= kDualWeightedMin;
       const float *gc = GATE ? P.gC + (int64_t)bh * P.T : nullptr;
       auto nvalid = [&](int n) { return min(128, s1 - (s0 + 128 * (nb - 1 - n))); };
       auto start = [&](int n) { return s0 + 128 * (nb - 1 - n); };
@@ -1181,6 +1227,17 @@ __global__ void __launch_bounds__(kDualThreads, 1)
         if (GATE) return exp2f(clast(n) - cprev(n));
         return DECAY ? exp2f(l2 * (float)nvalid(n)) : 1.f;
       };
+      // weights of this thread's row in walk block n: K and V rows, dO rows
+      auto wk = [&](int n) {
+        const int nv = nvalid(n), r = (int)row;
+        return r < nv ? exp2f(l2 * (float)(nv - 1 - r)) : 0.f;
+      };
+      auto wdo = [&](int n) {
+        const int r = (int)row;
+        return r < nvalid(n) ? exp2f(l2 * (float)(r + 1)) : 0.f;
+      };
+      // weighted form: K of the item's first block ahead of its entering state
+      if (wtd && !(ok = weigh(blk, 0, wk(0), D_KS))) break;
       {
         const float *src = P.ginit + ((int64_t)g * BH + bh) * 16384;
         const float dec = block_decay(0);
@@ -1203,10 +1260,14 @@ __global__ void __launch_bounds__(kDualThreads, 1)
         fence_proxy_async_smem();
         mbar_arrive(&bar[D_PRE]);
       }
+      if (wtd && !(ok = weigh(blk, 2, wdo(0), D_DS) && weigh(blk, 3, wk(0), D_VS))) break;
       for (int n = 0; n < nb && ok; ++n, ++blk) {
         // the next walk block's state decay (gates: two loads), ahead of the waits below
         const float dec_next = n + 1 < nb ? block_decay(n + 1) : 1.f;
-        if (DECAY) {
+        const bool more = n + 1 < nb;
+        if (DECAY && !wtd) {
+          // weights between the products: K after P1; V and dO after P2
+          // (which follows dv += P1~ dO)
           const int nv = nvalid(n), r = (int)row;
           float wx = 0.f, wy = 0.f;  // rows of K and V; rows of dO
           if (r < nv) {
@@ -1223,20 +1284,41 @@ __global__ void __launch_bounds__(kDualThreads, 1)
           dual_slot(blk, 0, sk, c);
           dual_slot(blk, 2, sdo, c);
           dual_slot(blk, 3, sv, c);
-          // K after P1; V and dO after P2 (which follows dv += P1~ dO)
           if (!(ok = wait(D_PFULL, 2 * blk))) break;
           scale_tile_row(tile_addr(sk), row, wx);
           fence_proxy_async_smem();
-          mbar_arrive(&bar[D_KSC]);
+          mbar_arrive(&bar[D_KS + (blk & 1)]);
           if (!(ok = wait(D_PFULL, 2 * blk + 1))) break;
           scale_tile_row(tile_addr(sv), row, wx);
           scale_tile_row(tile_addr(sdo), row, wy);
           fence_proxy_async_smem();
-          mbar_arrive(&bar[D_VSC]);
+          // every block completes one phase of each weighting barrier, whatever
+          // the form (a CTA's items may mix both)
+          mbar_arrive(&bar[D_DS + (blk & 1)]);
+          mbar_arrive(&bar[D_VS + (blk & 1)]);
+        }
+        // weighted form, next block: K (loaded a block ahead) now; dO as soon as
+        // it lands, unless this block's state is ready first (the state goes
+        // first then, being on the critical path); V after the state
+        bool do_done = false;
+        if (wtd && more) {
+          if (!(ok = weigh(blk + 1, 0, wk(n + 1), D_KS))) break;
+          int s, c;
+          dual_slot(blk + 1, 2, s, c);
+          // bounded poll of both events; the bounded waits below follow either way
+#pragma unroll 1
+          for (int i = 0; i < (1 << 20) && !abort_flag; ++i) {
+            if (__any_sync(0xffffffffu, mbar_test_wait(&bar[D_SFULL], blk & 1))) break;
+            if (__all_sync(0xffffffffu, mbar_test_wait(&bar[D_FULL + s], c & 1))) {
+              do_done = true;
+              break;
+            }
+          }
+          if (do_done && !(ok = weigh(blk + 1, 2, wdo(n + 1), D_DS))) break;
         }
         if (!(ok = wait(D_SFULL, blk))) break;
         tc_fence_after();
-        if (n + 1 < nb) {
+        if (more) {
           const float dec = dec_next;
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
@@ -1254,6 +1336,10 @@ __global__ void __launch_bounds__(kDualThreads, 1)
           tc_fence_before();
           fence_proxy_async_smem();
           mbar_arrive(&bar[D_PRE]);
+          if (wtd) {
+            if (!do_done && !(ok = weigh(blk + 1, 2, wdo(n + 1), D_DS))) break;
+            if (!(ok = weigh(blk + 1, 3, wk(n + 1), D_VS))) break;
+          }
         }
       }
     }

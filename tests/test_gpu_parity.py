@@ -224,6 +224,26 @@ def test_backward(dtype, d, T, dk):
     assert rel(dinit, rinit) < tol
 
 
+def test_backward_decay_forms_mixed_across_items():
+    """Per-head decays on both sides of 0.8 (above it the dk/dv pass weights its
+    operands before the products, below it between them) in one launch with
+    more (group, sequence) items than SMs, so CTAs take items of both forms in
+    turn; a ragged tail; a few heads of each form checked against the oracle."""
+    B, H, T, d = 2, 16, 32768 + 200, 128  # 9 groups of 3712 tokens: 288 items
+    c, dev = case(41, B, H, T, d, torch.bfloat16, sigma=1 / np.sqrt(128))
+    lam = np.array([0.55, 0.97, 0.7999, 0.8, 0.99986, 0.6, 0.9, 0.75] * 2, np.float32)
+    dec = torch.from_numpy(lam).cuda()
+    ws = la.workspace(dev["q"], la.OP_BWD, dec)
+    dq, dk_, dv, dinit = la.bwd(dev["q"], dev["k"], dev["v"], dev["dO"], decay=dec, want_dinit=True, ws=ws)
+    assert la.device_status(ws) == la.OK
+    for h in (0, 1, 2, 3):
+        sl = slice(h, h + 1)
+        rq, rk, rv, rinit = oracle.bwd_recurrent(c["q"][:, sl], c["k"][:, sl], c["v"][:, sl], c["dO"][:, sl],
+                                                 lam=lam[sl])
+        for got, ref in ((dq, rq), (dk_, rk), (dv, rv), (dinit, rinit)):
+            assert rel(got[:, sl], ref) < 1e-2, (h, float(lam[h]))
+
+
 @pytest.mark.parametrize("dtype,d", [(torch.bfloat16, 128), (torch.float32, 64)])
 @pytest.mark.parametrize("T,dk", [(2048, None), (8192 + 64, "cfg"), (1000, 0.5)])
 def test_checkpointed_forward_backward(dtype, d, T, dk):

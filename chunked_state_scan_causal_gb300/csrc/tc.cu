@@ -891,18 +891,19 @@ enum { D_FULL = 0, D_EMPTY = kDualSlots, D_PFULL = 2 * kDualSlots, D_PSFULL, D_O
 static_assert(D_COUNT * 8 + 4 <= 256, "dual kernel barriers and the TMEM slot fit their 256 bytes");
 
 // Per-head decays lambda >= kDualWeightedMin take the weighted-operand form of
-// the dk/dv pass: the rows of K and V are weighted by lambda^{nv-1-i} and those
-// of dO by lambda^{j+1} as soon as their tiles land, before any product reads
-// them, and both score tiles then need the 0/1 anti-causal mask times the one
-// scalar lambda^{-nv}:
-//   (K' Q^T)_ij = lambda^{nv-1-i} k_i.q_j, and dv += P^1 dO' with
-//       P^1 = lambda^{-nv} [j >= i] K' Q^T gives lambda^{j-i} (k_i.q_j) dO_j;
-//   (V' dO'^T)_ij = lambda^{nv+j-i} v_i.dO_j, and lambda^{-nv} [j >= i] of it
-//       is the masked P2 of dk.
-// The factors stay within lambda^{-128} .. lambda^{255}, i.e. 2^{+-83} for
+// the dk/dv pass: only the rows of dO are weighted, by lambda^{j+1}, as soon as
+// their tile lands (before any product reads it); the two accumulators hold
+// dv and dk divided by the row weight w_i = lambda^{nv-1-i}, which the store
+// multiplies back; and both score tiles need only the 0/1 anti-causal mask
+// times the one scalar lambda^{-nv}:
+//   dv_i = w_i [ (K R)_i + sum_j lambda^{-nv} [j >= i] (k_i.q_j) dO'_j ],
+//   dk_i = w_i [ (V R^T)_i + sum_j lambda^{-nv} [j >= i] (v_i.dO'_j) q_j ],
+// with dO'_j = lambda^{j+1} dO_j (expand: the products are lambda^{j-i}).
+// The factors stay within lambda^{-128} .. lambda^{128}, i.e. 2^{+-42} for
 // lambda >= 0.8, far inside fp32 and bf16 range.  Smaller decays weight the
-// tiles between the products (score tiles from unweighted operands, masks
-// per element), which puts the weighting on the critical path of the block.
+// rows of K, V and dO between the products (score tiles from unweighted
+// operands, masks per element), which puts the weighting on the critical path
+// of the block.
 constexpr float kDualWeightedMin = 0.8f;
 
 // Ring slot of tile x (0 K, 1 Q, 2 dO, 3 V) of the blk-th block a CTA
@@ -1067,7 +1068,7 @@ __global__ void __launch_bounds__(kDualThreads, 1)
         if (!(ok = ring_take(ring, k, item, &abort_flag, P.status, detail)) || item < 0) break;
         const int g = item / BH;
         const int s0 = P.gp.start(g), s1 = min(P.T, P.gp.start(g + 1)), nb = (s1 - s0 + 127) / 128;
-        // weighted-operand form: K, dO, V are weighted before their first product
+        // weighted-operand form: dO is weighted before its first product
         const bool wtd = DECAY && !GATE && P.decay[(item % BH) % P.H] >= kDualWeightedMin;
         // the decay-free order (R updated right after dv's state term)
         const bool early_r = !DECAY || wtd;
@@ -1075,7 +1076,7 @@ __global__ void __launch_bounds__(kDualThreads, 1)
           const uint32_t K = addr(0), Q = addr(1), DO = addr(2), V = addr(3);
           const int u1 = 2 * blk, u2 = u1 + 1, wb = blk & 1, wp = blk >> 1;
           // P1 = K Q^T  (the previous block's P2~ has been consumed: issue order)
-          if (!(ok = (wtd ? wait(D_KS + wb, wp) : full(0)) && full(1))) break;
+          if (!(ok = full(0) && full(1))) break;
           tc_fence_after();
 #pragma unroll
           for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tP, desc_kmajor(K, ks), desc_kmajor(Q, ks), id_kk, ks > 0);
@@ -1101,7 +1102,7 @@ __global__ void __launch_bounds__(kDualThreads, 1)
           for (uint32_t ks = 0; ks < 8; ++ks) mma_ts(tO1, tP + ks * 8, desc_mnmajor(DO, ks), id_km, 1u);
           mma_commit(&bar[D_O1FULL]);
           // P2 = V dO^T
-          if (!(ok = wtd ? wait(D_VS + wb, wp) : full(3))) break;
+          if (!(ok = full(3))) break;
           tc_fence_after();
 #pragma unroll
           for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tP, desc_kmajor(V, ks), desc_kmajor(DO, ks), id_kk, ks > 0);
@@ -1227,17 +1228,19 @@ __global__ void __launch_bounds__(kDualThreads, 1)
         if (GATE) return exp2f(clast(n) - cprev(n));
         return DECAY ? exp2f(l2 * (float)nvalid(n)) : 1.f;
       };
-      // weights of this thread's row in walk block n: K and V rows, dO rows
-      auto wk = [&](int n) {
-        const int nv = nvalid(n), r = (int)row;
-        return r < nv ? exp2f(l2 * (float)(nv - 1 - r)) : 0.f;
-      };
+      // weight of this thread's row of dO in walk block n
       auto wdo = [&](int n) {
         const int r = (int)row;
         return r < nvalid(n) ? exp2f(l2 * (float)(r + 1)) : 0.f;
       };
-      // weighted form: K of the item's first block ahead of its entering state
-      if (wtd && !(ok = weigh(blk, 0, wk(0), D_KS))) break;
+      // weighted form: dO of a block, plus one (empty) phase of the K and V
+      // weighting barriers, which every block completes whatever its form
+      auto weigh_do = [&](int b, int n) {
+        if (!weigh(b, 2, wdo(n), D_DS)) return false;
+        mbar_arrive(&bar[D_KS + (b & 1)]);
+        mbar_arrive(&bar[D_VS + (b & 1)]);
+        return true;
+      };
       {
         const float *src = P.ginit + ((int64_t)g * BH + bh) * 16384;
         const float dec = block_decay(0);
@@ -1260,7 +1263,7 @@ __global__ void __launch_bounds__(kDualThreads, 1)
         fence_proxy_async_smem();
         mbar_arrive(&bar[D_PRE]);
       }
-      if (wtd && !(ok = weigh(blk, 2, wdo(0), D_DS) && weigh(blk, 3, wk(0), D_VS))) break;
+      if (wtd && !(ok = weigh_do(blk, 0))) break;
       for (int n = 0; n < nb && ok; ++n, ++blk) {
         // the next walk block's state decay (gates: two loads), ahead of the waits below
         const float dec_next = n + 1 < nb ? block_decay(n + 1) : 1.f;
@@ -1297,12 +1300,11 @@ __global__ void __launch_bounds__(kDualThreads, 1)
           mbar_arrive(&bar[D_DS + (blk & 1)]);
           mbar_arrive(&bar[D_VS + (blk & 1)]);
         }
-        // weighted form, next block: K (loaded a block ahead) now; dO as soon as
-        // it lands, unless this block's state is ready first (the state goes
-        // first then, being on the critical path); V after the state
+        // weighted form, next block: dO as soon as it lands, unless this
+        // block's state is ready first (the state goes first then, being on the
+        // critical path)
         bool do_done = false;
         if (wtd && more) {
-          if (!(ok = weigh(blk + 1, 0, wk(n + 1), D_KS))) break;
           int s, c;
           dual_slot(blk + 1, 2, s, c);
           // bounded poll of both events; the bounded waits below follow either way
@@ -1314,7 +1316,7 @@ __global__ void __launch_bounds__(kDualThreads, 1)
               break;
             }
           }
-          if (do_done && !(ok = weigh(blk + 1, 2, wdo(n + 1), D_DS))) break;
+          if (do_done && !(ok = weigh_do(blk + 1, n + 1))) break;
         }
         if (!(ok = wait(D_SFULL, blk))) break;
         tc_fence_after();
@@ -1336,10 +1338,7 @@ __global__ void __launch_bounds__(kDualThreads, 1)
           tc_fence_before();
           fence_proxy_async_smem();
           mbar_arrive(&bar[D_PRE]);
-          if (wtd) {
-            if (!do_done && !(ok = weigh(blk + 1, 2, wdo(n + 1), D_DS))) break;
-            if (!(ok = weigh(blk + 1, 3, wk(n + 1), D_VS))) break;
-          }
+          if (wtd && !do_done && !(ok = weigh_do(blk + 1, n + 1))) break;
         }
       }
     }
@@ -1353,9 +1352,14 @@ __global__ void __launch_bounds__(kDualThreads, 1)
         break;
       const int g = item / BH, bh = item % BH, b = bh / P.H, h = bh % P.H;
       const int s0 = P.gp.start(g), s1 = min(P.T, P.gp.start(g + 1)), nb = (s1 - s0 + 127) / 128;
+      const float lam = (DECAY && !GATE) ? P.decay[h] : 1.f;
+      const bool wtd = DECAY && !GATE && lam >= kDualWeightedMin;
+      const float l2 = wtd ? log2f(lam) : 0.f;
       for (int n = 0; n < nb && ok; ++n, ++blk) {
         const int t0 = s0 + 128 * (nb - 1 - n);
         const bool valid = t0 + (int)row < s1;
+        // weighted form: the accumulators hold the rows divided by lambda^{nv-1-i}
+        const float wrow = (wtd && valid) ? exp2f(l2 * (float)(min(128, s1 - t0) - 1 - (int)row)) : 1.f;
         if (GATE && P.gx && valid) {
           // the k row for k . dk: two 128-byte lines into L1 while dv drains
           const __nv_bfloat16 *kr = P.gk + (int64_t)b * P.sb + (int64_t)h * P.sh + (int64_t)(t0 + (int)row) * P.st;
@@ -1378,6 +1382,10 @@ __global__ void __launch_bounds__(kDualThreads, 1)
           for (int c = 0; c < 4; ++c) {
             float x[32];
             ld_chunk(tO + lb + c * 32, x);
+            if (wtd) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) x[j] *= wrow;
+            }
             if (gx_row) gxacc += dot32_bf16(x, krow + c * 32);  // k . dk before dk is rounded
             if (valid) {
               if (P.wide)

@@ -65,6 +65,35 @@ def test_gated_forward_and_backward(T, lo):
 
 
 # the CUDA-core kernels: fp32 inputs (d = 128 and 64) and bf16 with d = 64
+def test_gated_heads_of_mixed_strength_across_items():
+    """32 heads of four gate kinds in one launch with more (group, sequence)
+    items than SMs, so CTAs take items of different kinds in turn: mild gates,
+    strong gates (cumulative log2 sums spanning about 92 over a 128-token
+    block), gates with positive values (sums that rise and fall), and blocks
+    spanning about 46; one head of each kind against the oracle."""
+    B, H, T = 1, 32, 16384 + 100
+    c = inputs.random_case(51, B, H, T, 128, dtype="bf16", sigma=1 / np.sqrt(128))
+    dev = {k: torch.from_numpy(np.ascontiguousarray(v)).to(torch.bfloat16).cuda() for k, v in c.items()}
+    kinds = [(-0.05, 0.0), (-1.0, 0.0), (-0.03, 0.02), (-0.5, 0.0)]
+    r = np.random.default_rng(52)
+    lg = np.stack([r.uniform(*kinds[h % 4], T) for h in range(H)])[None].astype(np.float32)
+    ck = la.checkpoint_gated(dev["q"])
+    wsf, wsb = la.workspace(dev["q"], la.OP_FWD_GATED), la.workspace(dev["q"], la.OP_BWD_GATED)
+    o, _ = la.fwd_gated(dev["q"], dev["k"], dev["v"], f32(lg), ck, ws=wsf)
+    dq, dk, dv, dlg, dinit = la.bwd_gated(dev["q"], dev["k"], dev["v"], dev["dO"], f32(lg), ck, want_dinit=True,
+                                          ws=wsb)
+    assert la.device_status(wsf) == la.OK and la.device_status(wsb) == la.OK
+    lg64 = lg.astype(np.float64)
+    for h in range(4):
+        sl = slice(h, h + 1)
+        ro, _ = oracle.fwd_gated(c["q"][:, sl], c["k"][:, sl], c["v"][:, sl], lg64[:, sl])
+        rq, rk, rv, rlg, rinit = oracle.bwd_gated(c["q"][:, sl], c["k"][:, sl], c["v"][:, sl], c["dO"][:, sl],
+                                                  lg64[:, sl])
+        for name, got, ref in (("o", o, ro), ("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv),
+                               ("d_log_gate", dlg, rlg), ("d_init", dinit, rinit)):
+            assert rel(got[:, sl], ref) < TOL, (name, h, rel(got[:, sl], ref))
+
+
 @pytest.mark.parametrize("dtype,d,T,lo", [(torch.float32, 128, 200, -0.05), (torch.float32, 64, 1000, -1.0),
                                           (torch.float32, 64, 130, -4.0), (torch.bfloat16, 64, 700, -0.05)])
 def test_gated_cuda_core_path(dtype, d, T, lo):

@@ -162,6 +162,17 @@ def _profile_traffic():
 
 
 # ---------------------------------------------------------------------------------- reference arm
+def workload_config(cfg, ws_n):
+    """The `config` object of the JSON line, the same for both arms."""
+    from chunked_state_scan_causal_gb300 import inputs
+    lam = inputs.workload_decay(cfg)
+    gated = cfg.get("gates") is not None
+    return {"workload": cfg["name"], "B": cfg["B"], "H": cfg["H"], "T": cfg["T"], "d": cfg["d"], "chunk": 64,
+            "decay": "per-head" if lam is not None else ("per-token gates" if gated else "none"),
+            "l2": "inputs 512 MiB per tensor > L2 (no flush)",
+            "step": "linattn_fwd_ckpt + linattn_bwd_ckpt", "parallelism": f"replicas x{ws_n}"}
+
+
 def run_reference(args):
     ws, rank, _ = _dist()
     if rank != 0:
@@ -212,7 +223,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": cfg["name"], "B": cfg["B"], "H": cfg["H"], "T": T, "d": cfg["d"]},
+        "config": workload_config(cfg, ws),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.threads_used(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -420,10 +431,7 @@ def run_ours(args):
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws_n, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded normal; no dataset)",
-            "config": {"workload": cfg["name"], "B": B, "H": H, "T": T, "d": d, "chunk": 64,
-                       "decay": "per-head" if lam is not None else ("per-token gates" if gated else "none"),
-                       "l2": "inputs 512 MiB per tensor > L2 (no flush)",
-                       "step": "linattn_fwd_ckpt + linattn_bwd_ckpt", "parallelism": f"replicas x{ws_n}"},
+            "config": workload_config(cfg, ws_n),
             "tflops": flops / (ms * 1e-3) / 1e12,
             "algorithmic_gbs": bytes_ / (ms * 1e-3) / 1e9,
             "path_roofline_frac": max(flops / (tf * 1e12), bytes_ / (hbm * 1e9)) / (ms * 1e-3),

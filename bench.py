@@ -344,11 +344,22 @@ def run_ours(args):
         "launches_per_step": n_main / args.steps,
         "share_of_step": ms_main / (ms * args.steps) if ms else None,
     }
+    # token-heads per step that the aggregate launches cover: the forward's, plus
+    # the backward's for the heads whose dq pass does not accumulate them itself
+    # (gates, or a per-head decay below 0.8, where the chunked kernels switch
+    # to their weighted-operand form)
+    if gated:
+        agg_units = 2 * tok_heads
+    elif lam is not None:
+        agg_units = tok_heads * (1 + float((lam < 0.8).mean()))
+    else:
+        agg_units = tok_heads
     breakdown = {}
     for k, (n, t) in kernels.items():
         e = {"launches_per_step": n / args.steps, "ms_per_step": t / args.steps}
         if k in KIND_BYTES_PER_TOKEN_HEAD and t > 0:
-            e["algorithmic_gbs"] = KIND_BYTES_PER_TOKEN_HEAD[k] * tok_heads * n / (t * 1e-3) / 1e9
+            units = agg_units * args.steps if k == "tc_segment_aggregate" else tok_heads * n
+            e["algorithmic_gbs"] = KIND_BYTES_PER_TOKEN_HEAD[k] * units / (t * 1e-3) / 1e9
         breakdown[k] = e
 
     # ---- end to end through the public API with host buffers: every step copies its

@@ -381,13 +381,11 @@ static int32_t bwd_impl(const linattn_shape *shape, const void *q, const void *k
   // group's state transposed.  Reverse group states Rbar_g = sum_{u > group end}
   // lambda^{u-end} q_u dO_u^T come from group aggregates of q dO^T scanned from
   // the end (the value one step before token 0 is d_init = sum_t lambda^{t+1}
-  // q_t dO_t^T); without a decay the dq pass accumulates those aggregates too.
-  if (!p.decay) {
-    if (e == cudaSuccess) e = tc_main(p, gp, dO, v, k, dq, states, true, nullptr, status, s, q, wagg);
-  } else {
-    if (e == cudaSuccess) e = tc_main(p, gp, dO, v, k, dq, states, true, nullptr, status, s);
-    if (e == cudaSuccess) e = tc_segment_states(p, gp, q, dO, true, wagg, status, s);
-  }
+  // q_t dO_t^T).  The dq pass accumulates those aggregates too, for every head
+  // without a decay or with one of at least 0.8; the aggregate pass computes
+  // them for the heads with smaller decays and passes over the others.
+  if (e == cudaSuccess) e = tc_main(p, gp, dO, v, k, dq, states, true, nullptr, status, s, q, wagg);
+  if (e == cudaSuccess && p.decay) e = tc_segment_states(p, gp, q, dO, true, wagg, status, s, true);
   // A gradient D arriving at the final state enters the reverse scan across the
   // last group, whose length may be short of L: fold lambda^{len} D into that
   // group's aggregate, scan from zero, and give the last group D itself.

@@ -122,14 +122,18 @@ GroupPlan tc_group_plan(const Problem &p, int max_len = 0);
 // Segment aggregates sum_s w_s x_s y_s^T over groups of seg_len tokens (seg_len
 // a multiple of 128), written as [G][BH][d][d] fp32.
 //   reverse == false: w_s = lambda^{end - s};  reverse == true: w_s = lambda^{s - start + 1}.
+// skip_weighted: leave out the groups of heads whose decay takes the weighted
+// form (lambda >= 0.8), whose aggregates the dq pass accumulates itself.
 cudaError_t tc_segment_states(const Problem &p, const GroupPlan &gp, const void *X, const void *Y, bool reverse,
-                              float *out, int *status, cudaStream_t s);
+                              float *out, int *status, cudaStream_t s, bool skip_weighted = false);
 // Per-group causal chunked attention from the given group states
 // [G][BH][d][d] (read transposed when init_transposed): o_i = lambda^{i+1}
 // S^T q_i + intra-block terms, S the state entering the block.  final_state
-// (optional) is the state after the last token.  x (optional, no decay): also
-// writes agg_out[g] = sum_{s in group g} x_s q_s^T ([G][BH][d][d]) from the
-// same pass.
+// (optional) is the state after the last token.  x (optional, no gates): also
+// writes agg_out[g] = sum_{s in group g} w_s x_s q_s^T ([G][BH][d][d]) from the
+// same pass, w_s = lambda^{s - start + 1} (1 without a decay), for the groups
+// of heads whose decay takes the weighted form (lambda >= 0.8, or none); the
+// other groups are left to tc_segment_states.
 cudaError_t tc_main(const Problem &p, const GroupPlan &gp, const void *q, const void *k, const void *v, void *o,
                     const float *group_init, bool init_transposed, float *final_state, int *status,
                     cudaStream_t s, const void *x = nullptr, float *agg_out = nullptr);

@@ -104,12 +104,20 @@ __device__ __forceinline__ void ring_init(const ItemRing &r, int readers) {
   }
 }
 
-// Producer: draw and post this CTA's k-th item.  False if a wait gave up.
+struct NoSkip {
+  __device__ bool operator()(int) const { return false; }
+};
+
+// Producer: draw and post this CTA's k-th item (items for which skip() holds
+// are drawn and passed over).  False if a wait gave up.
+template <class Skip = NoSkip>
 __device__ __forceinline__ bool ring_post(const ItemRing &r, int k, int *counter, int nitems, int &item,
-                                          volatile int *abort_flag, int *status, int *detail) {
+                                          volatile int *abort_flag, int *status, int *detail,
+                                          Skip skip = Skip()) {
   const int s = k % kRing;
   if (k >= kRing && !mbar_wait(&r.empty[s], (k / kRing - 1) & 1, abort_flag, status, detail)) return false;
-  const int x = atomicAdd(counter, 1);
+  int x = atomicAdd(counter, 1);
+  while (x < nitems && skip(x)) x = atomicAdd(counter, 1);
   item = x < nitems ? x : -1;
   *reinterpret_cast<volatile int *>(&r.item[s]) = item;
   mbar_arrive(&r.full[s]);  // release: the item is visible to the readers of the phase
@@ -137,6 +145,12 @@ __device__ __forceinline__ void items_done(int *counter) {
     }
   }
 }
+
+// Per-head decays lambda >= kWeightedMin take the weighted-operand forms of
+// the chunked kernels (rows weighted as their tiles land, masks that reduce to
+// a 0/1 pattern times one scalar per block, output rows weighted in the store):
+// every factor then stays within lambda^{+-256}, i.e. 2^{+-83} at 0.8.
+constexpr float kWeightedMin = 0.8f;
 
 // Multiply one 128-element bf16 row of an SW128 tile by w (rounded back to bf16).
 __device__ __forceinline__ void scale_tile_row(uint32_t tile, uint32_t row, float w) {
@@ -181,6 +195,7 @@ struct AggParams {
   int *status;
   int *counter;  // [2] item counter and finished CTAs (zero at launch)
   const float *gC, *gtot;  // gates: group-local log2 cumulative sums [BH][T], group totals [G][BH]
+  int skip_weighted;       // pass over the items of heads with lambda >= kWeightedMin (the dq pass has them)
 };
 
 // GATE (with DECAY): token weights from the gates' cumulative sums instead of
@@ -235,7 +250,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       int it = 0;
       bool ok = true;
       for (int k = 0, item; ok; ++k) {
-        if (!(ok = ring_post(ring, k, P.counter, P.nitems, item, &abort_flag, P.status, detail)) || item < 0) break;
+        auto skip = [&](int x) { return DECAY && !GATE && P.skip_weighted && P.decay[(x % BH) % P.H] >= kWeightedMin; };
+        if (!(ok = ring_post(ring, k, P.counter, P.nitems, item, &abort_flag, P.status, detail, skip)) || item < 0)
+          break;
         const int g = item / BH, bh = item % BH, b = bh / P.H, h = bh % P.H;
         const int s0 = P.gp.start(g), s1 = min(P.T, P.gp.start(g + 1));
         for (int t0 = s0; t0 < s1; t0 += 128, ++it) {
@@ -368,8 +385,12 @@ constexpr uint32_t kOffGate = kOffBar + 256;               // GATE: a block's 12
 constexpr size_t kMainSmem = kOffGate + 1024 + 1024;
 
 // barrier indices
+// B_KS / B_XS: the block's K (X) tile weighted in place, two barriers each by
+// block parity (an arrival for block n + 2 can only follow the MMA thread's
+// wait for block n).
 enum { B_FULL = 0, B_EMPTY = kSlots, B_PFULL = 2 * kSlots, B_PEMPTY, B_OFULL, B_OEMPTY, B_SFULL, B_PRE,
-       B_PSFULL, B_WEMPTY, B_KSC, B_COUNT };
+       B_PSFULL, B_WEMPTY, B_KS, B_XS = B_KS + 2, B_COUNT = B_XS + 2 };
+static_assert(B_COUNT * 8 + 4 <= 256, "chunked kernel barriers and the TMEM slot fit their 256 bytes");
 
 // Decay mask of one 32-column chunk of a score row: keep j <= i (causal) or
 // j >= i (anti-causal) and weight by lambda^{|i-j|}; walks j so that the
@@ -490,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_main_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                    const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mo,
                    const __grid_constant__ CUtensorMap mx, MainParams P) {
-  static_assert(!AGG || !DECAY, "group aggregates are fused for the decay-free kernel");
+  static_assert(!AGG || !GATE, "group aggregates are fused for per-head decays only");
   static_assert(!GATE || DECAY, "gates use the weighted code paths");
   constexpr int NT = AGG ? 4 : 3;  // tiles per block
   extern __shared__ uint8_t smem_raw[];
@@ -519,7 +540,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bar[B_PRE], 128);
     mbar_init(&bar[B_PSFULL], 128);
     mbar_init(&bar[B_WEMPTY], 128);
-    mbar_init(&bar[B_KSC], 128);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar[B_KS + i], 128);
+      mbar_init(&bar[B_XS + i], 128);
+    }
     ring_init(ring, 1 + 128 + 128);  // readers: MMA thread, groups A and B
     fence_mbar_init();
     prefetch_tensormap(&mq);
@@ -585,36 +609,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t id_qs = idesc_bf16(128, 128, false, true);   // Q S,  P V
       const uint32_t id_kv = idesc_bf16(128, 128, true, true);    // K^T V
       const uint32_t id_xq = idesc_bf16(128, 128, true, true);    // X^T Q
-      int blk = 0, it = 0;
+      int blk = 0, ia = 0;  // ia: items that accumulated their group aggregate (phases of B_WEMPTY)
       bool ok = true;
-      for (int k = 0, item; ok; ++k, ++it) {
+      for (int k = 0, item; ok; ++k) {
         if (!(ok = ring_take(ring, k, item, &abort_flag, P.status, detail)) || item < 0) break;
         const int g = item / BH;
         const int s0 = P.gp.start(g), s1 = min(P.T, P.gp.start(g + 1)), nb = (s1 - s0 + 127) / 128;
+        // weighted-operand form (K and X weighted as they land); the group
+        // aggregate is accumulated here unless a decay takes the other form
+        const bool wtd = DECAY && !GATE && P.decay[(item % BH) % P.H] >= kWeightedMin;
+        const bool aggw = AGG && (!DECAY || wtd);
         for (int n = 0; n < nb; ++n, ++blk) {
           const int tq = tile_of(blk, 0), tk = tile_of(blk, 1), tv = tile_of(blk, 2), tx = tile_of(blk, 3);
           const uint32_t Q = slot_addr(tq), K = slot_addr(tk), V = slot_addr(tv);
-          // scores: P = Q K^T
+          const int wb = blk & 1, wp = (blk >> 1) & 1;
+          // scores: P = Q K^T  (weighted form: K')
           ok = mbar_wait(&bar[B_FULL + tq % kSlots], (tq / kSlots) & 1, &abort_flag, P.status, detail) &&
-               mbar_wait(&bar[B_FULL + tk % kSlots], (tk / kSlots) & 1, &abort_flag, P.status, detail) &&
+               (wtd ? mbar_wait(&bar[B_KS + wb], wp, &abort_flag, P.status, detail)
+                    : mbar_wait(&bar[B_FULL + tk % kSlots], (tk / kSlots) & 1, &abort_flag, P.status, detail)) &&
                (blk == 0 || mbar_wait(&bar[B_PEMPTY], (blk - 1) & 1, &abort_flag, P.status, detail));
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
           for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tP, desc_kmajor(Q, ks), desc_kmajor(K, ks), id_qk, ks > 0);
           mma_commit(&bar[B_PFULL]);
-          // inter-block term: O = Q S (its own accumulator with a decay)
+          // inter-block term: O = Q S (its own accumulator with a decay, unless weighted)
           ok = mbar_wait(&bar[B_PRE], blk & 1, &abort_flag, P.status, detail) &&
                (blk == 0 || mbar_wait(&bar[B_OEMPTY], (blk - 1) & 1, &abort_flag, P.status, detail));
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
           for (uint32_t ks = 0; ks < 8; ++ks)
-            mma_ss(DECAY ? tOi : tO, desc_kmajor(Q, ks), desc_mnmajor(sSh, ks), id_qs, ks > 0);
-          if (AGG) {
-            // group aggregate: W += X^T Q (the previous group's W must have been read out)
-            ok = mbar_wait(&bar[B_FULL + tx % kSlots], (tx / kSlots) & 1, &abort_flag, P.status, detail) &&
-                 (n > 0 || it == 0 || mbar_wait(&bar[B_WEMPTY], (it - 1) & 1, &abort_flag, P.status, detail));
+            mma_ss((DECAY && !wtd) ? tOi : tO, desc_kmajor(Q, ks), desc_mnmajor(sSh, ks), id_qs, ks > 0);
+          if (aggw) {
+            // group aggregate: W += X'^T Q (the previous group's W must have been read out;
+            // with a decay X' has its rows weighted by lambda^{s - start + 1})
+            ok = (DECAY ? mbar_wait(&bar[B_XS + wb], wp, &abort_flag, P.status, detail)
+                        : mbar_wait(&bar[B_FULL + tx % kSlots], (tx / kSlots) & 1, &abort_flag, P.status, detail)) &&
+                 (n > 0 || ia == 0 || mbar_wait(&bar[B_WEMPTY], (ia - 1) & 1, &abort_flag, P.status, detail));
             if (!ok) break;
             tc_fence_after();
             const uint32_t X = slot_addr(tx);
@@ -622,10 +654,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (uint32_t ks = 0; ks < 8; ++ks)
               mma_ss(tW, desc_mnmajor(X, ks), desc_mnmajor(Q, ks), id_xq, (n > 0 || ks > 0) ? 1u : 0u);
           }
+          // an X tile that no product reads is still waited for before its slot is released
+          if (AGG && !aggw &&
+              !(ok = mbar_wait(&bar[B_FULL + tx % kSlots], (tx / kSlots) & 1, &abort_flag, P.status, detail)))
+            break;
           mma_commit(&bar[B_EMPTY + tq % kSlots]);
           if (AGG) mma_commit(&bar[B_EMPTY + tx % kSlots]);
           // state update: S += K'^T V  (K' = decay-weighted key rows)
-          ok = (!DECAY || mbar_wait(&bar[B_KSC], blk & 1, &abort_flag, P.status, detail)) &&
+          ok = (!DECAY || wtd || mbar_wait(&bar[B_KS + wb], wp, &abort_flag, P.status, detail)) &&
                mbar_wait(&bar[B_FULL + tv % kSlots], (tv / kSlots) & 1, &abort_flag, P.status, detail);
           if (!ok) break;
           tc_fence_after();
@@ -638,10 +674,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
 #pragma unroll
           for (uint32_t ks = 0; ks < 8; ++ks)
-            mma_ss(tO, desc_kmajor(sPs, ks), desc_mnmajor(V, ks), id_qs, (!DECAY || ks > 0) ? 1u : 0u);
+            mma_ss(tO, desc_kmajor(sPs, ks), desc_mnmajor(V, ks), id_qs, (!DECAY || wtd || ks > 0) ? 1u : 0u);
           mma_commit(&bar[B_EMPTY + tv % kSlots]);
           mma_commit(&bar[B_OFULL]);
         }
+        if (ok && aggw) ++ia;
       }
     }
   } else if (warp >= 4 && warp < 8) {
@@ -656,9 +693,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int s0 = P.gp.start(g), s1 = min(P.T, P.gp.start(g + 1)), nb = (s1 - s0 + 127) / 128;
       const float lam = (DECAY && !GATE) ? P.decay[h] : 1.f;
       const float l2 = (DECAY && !GATE) ? log2f(lam) : 0.f;
+      const bool wtd = DECAY && !GATE && lam >= kWeightedMin;
       const float *gc = GATE ? P.gC + (int64_t)bh * P.T : nullptr;
       for (int n = 0; n < nb; ++n, ++blk) {
         const int t0 = s0 + 128 * n, nv = min(128, s1 - t0);
+        // weighted form: the scores of K' take lambda^{-nv} inside the causal mask
+        const float wsc = wtd ? exp2f(-l2 * (float)nv) : 1.f;
         float ci = 0.f, cprev = 0.f;
         // one buffer of sums and column factors: the previous block's readers passed
         // the output-store barrier of that block before this write
@@ -685,10 +725,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 4; ++c) {
           float x[32];
           ld_chunk(tP + lb + c * 32, x);
-          if (GATE)
+          if (GATE) {
             mask_chunk_gate<false>(x, (int)row, c, ci, cb, cw);
-          else
+          } else if (wtd) {
+            mask_chunk<false, false>(x, (int)row, c, 1.f, 0.f);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) x[j] *= wsc;
+          } else {
             mask_chunk<DECAY, false>(x, (int)row, c, lam, l2);
+          }
           store_row_chunk_bf16(sPs, row, c, x);
         }
         tc_fence_before();
@@ -708,7 +753,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 4; ++c) {
           float x[32];
           ld_chunk(tO + lb + c * 32, x);
-          if (DECAY) {
+          if (wtd) {
+            // the accumulator holds o_i / lambda^{i+1}
+#pragma unroll
+            for (int j = 0; j < 32; ++j) x[j] *= wq;
+          } else if (DECAY) {
             float y[32];
             ld_chunk(tOi + lb + c * 32, y);
 #pragma unroll
@@ -742,8 +791,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int s0 = P.gp.start(g), s1 = min(P.T, P.gp.start(g + 1)), nb = (s1 - s0 + 127) / 128;
       const float lam = (DECAY && !GATE) ? P.decay[h] : 1.f;
       const float l2 = (DECAY && !GATE) ? log2f(lam) : 0.f;
+      const bool wtd = DECAY && !GATE && lam >= kWeightedMin;
+      const bool aggw = AGG && (!DECAY || wtd);
       const float *gc = GATE ? P.gC + (int64_t)bh * P.T : nullptr;
       auto nvalid = [&](int n) { return min(128, s1 - (s0 + 128 * n)); };
+      // weighted form: key rows lambda^{nv-1-j}; rows of X (the group aggregate's
+      // left factor) lambda^{s-start+1}
+      auto wk = [&](int n) {
+        const int nv = nvalid(n), r = (int)row;
+        return r < nv ? exp2f(l2 * (float)(nv - 1 - r)) : 0.f;
+      };
+      auto wx = [&](int n) { return (int)row < nvalid(n) ? exp2f(l2 * (float)(128 * n + (int)row + 1)) : 0.f; };
+      // weigh this thread's row of tile role r (1 K, 3 X) of CTA block b once it
+      // has landed, then arrive on the barrier bar_idx + block parity
+      auto weigh = [&](int b, int r, float w, int bar_idx) {
+        const int t = tile_of(b, r);
+        if (!__all_sync(0xffffffffu, mbar_wait(&bar[B_FULL + t % kSlots], (t / kSlots) & 1, &abort_flag, P.status,
+                                               detail)))
+          return false;
+        scale_tile_row(slot_addr(t), row, w);
+        fence_proxy_async_smem();
+        mbar_arrive(&bar[bar_idx + (b & 1)]);
+        return true;
+      };
+      // weighted form: the block's K (and X) ahead of its scores
+      auto weigh_block = [&](int b, int n) { return weigh(b, 1, wk(n), B_KS) && (!AGG || weigh(b, 3, wx(n), B_XS)); };
+      if (wtd && !(ok = weigh_block(blk, 0))) break;
       // state decay across block n: lambda^{nv}, or the product of its gates
       auto block_decay = [&](int n) {
         const int t0 = s0 + 128 * n, nv = nvalid(n);
@@ -781,21 +854,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int n = 0; n < nb; ++n, ++blk) {
         // the next block's state decay (gates: two loads), ahead of the waits below
         const float dec_next = n + 1 < nb ? block_decay(n + 1) : 1.f;
-        if (DECAY) {
+        const bool more = n + 1 < nb;
+        if (DECAY && !wtd) {
           // key rows k_j *= lambda^{nv-1-j} (gates: exp2(C_last - C_j)) once the scores have read them
           const int nv = nvalid(n), r = (int)row, t0 = s0 + 128 * n;
-          float wk = 0.f;
-          if (r < nv) wk = GATE ? exp2f(gc[t0 + nv - 1] - gc[t0 + r]) : exp2f(l2 * (float)(nv - 1 - r));
+          float w = 0.f;
+          if (r < nv) w = GATE ? exp2f(gc[t0 + nv - 1] - gc[t0 + r]) : exp2f(l2 * (float)(nv - 1 - r));
           if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_PFULL], blk & 1, &abort_flag, P.status, detail))))
             break;
-          scale_tile_row(slot_addr(tile_of(blk, 1)), row, wk);
+          scale_tile_row(slot_addr(tile_of(blk, 1)), row, w);
           fence_proxy_async_smem();
-          mbar_arrive(&bar[B_KSC]);
+          mbar_arrive(&bar[B_KS + (blk & 1)]);
+          if (AGG) mbar_arrive(&bar[B_XS + (blk & 1)]);  // one phase per block in either form
+        }
+        // weighted form, next block: K (and X) as soon as they land, unless this
+        // block's state is ready first (then after the state, which is on the
+        // critical path).  The next X takes the slot of this block's Q: this
+        // block's scores completing says that Q has landed, so its fill is the
+        // one before X's.
+        bool next_done = false;
+        if (wtd && more) {
+          if (AGG &&
+              !(ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_PFULL], blk & 1, &abort_flag, P.status, detail))))
+            break;
+          const int t = tile_of(blk + 1, 1);
+#pragma unroll 1
+          for (int i = 0; i < (1 << 20) && !abort_flag; ++i) {
+            if (__any_sync(0xffffffffu, mbar_test_wait(&bar[B_SFULL], blk & 1))) break;
+            if (__all_sync(0xffffffffu, mbar_test_wait(&bar[B_FULL + t % kSlots], (t / kSlots) & 1))) {
+              next_done = true;
+              break;
+            }
+          }
+          if (next_done && !(ok = weigh_block(blk + 1, n + 1))) break;
         }
         ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_SFULL], blk & 1, &abort_flag, P.status, detail));
         if (!ok) break;
         tc_fence_after();
-        if (n + 1 < nb) {
+        if (more) {
           const float dec = dec_next;
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
@@ -813,7 +909,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_before();
           fence_proxy_async_smem();
           mbar_arrive(&bar[B_PRE]);
-        } else if (AGG) {
+          if (wtd && !next_done && !(ok = weigh_block(blk + 1, n + 1))) break;
+        } else if (aggw) {
           // the group's aggregate W (complete: its last product precedes the state update)
           float *dst = P.agg_out + ((int64_t)g * BH + bh) * 16384 + row * 128;
 #pragma unroll 1
@@ -890,7 +987,7 @@ enum { D_FULL = 0, D_EMPTY = kDualSlots, D_PFULL = 2 * kDualSlots, D_PSFULL, D_O
        D_O2EMPTY, D_SFULL, D_PRE, D_KS, D_DS = D_KS + 2, D_VS = D_DS + 2, D_COUNT = D_VS + 2 };
 static_assert(D_COUNT * 8 + 4 <= 256, "dual kernel barriers and the TMEM slot fit their 256 bytes");
 
-// Per-head decays lambda >= kDualWeightedMin take the weighted-operand form of
+// Per-head decays lambda >= kWeightedMin take the weighted-operand form of
 // the dk/dv pass: only the rows of dO are weighted, by lambda^{j+1}, as soon as
 // their tile lands (before any product reads it); the two accumulators hold
 // dv and dk divided by the row weight w_i = lambda^{nv-1-i}, which the store
@@ -900,11 +997,10 @@ static_assert(D_COUNT * 8 + 4 <= 256, "dual kernel barriers and the TMEM slot fi
 //   dk_i = w_i [ (V R^T)_i + sum_j lambda^{-nv} [j >= i] (v_i.dO'_j) q_j ],
 // with dO'_j = lambda^{j+1} dO_j (expand: the products are lambda^{j-i}).
 // The factors stay within lambda^{-128} .. lambda^{128}, i.e. 2^{+-42} for
-// lambda >= 0.8, far inside fp32 and bf16 range.  Smaller decays weight the
+// lambda >= kWeightedMin, far inside fp32 and bf16 range.  Smaller decays weight the
 // rows of K, V and dO between the products (score tiles from unweighted
 // operands, masks per element), which puts the weighting on the critical path
 // of the block.
-constexpr float kDualWeightedMin = 0.8f;
 
 // Ring slot of tile x (0 K, 1 Q, 2 dO, 3 V) of the blk-th block a CTA
 // processes, and how many loads that slot received before it.  Tiles are
@@ -1069,7 +1165,7 @@ __global__ void __launch_bounds__(kDualThreads, 1)
         const int g = item / BH;
         const int s0 = P.gp.start(g), s1 = min(P.T, P.gp.start(g + 1)), nb = (s1 - s0 + 127) / 128;
         // weighted-operand form: dO is weighted before its first product
-        const bool wtd = DECAY && !GATE && P.decay[(item % BH) % P.H] >= kDualWeightedMin;
+        const bool wtd = DECAY && !GATE && P.decay[(item % BH) % P.H] >= kWeightedMin;
         // the decay-free order (R updated right after dv's state term)
         const bool early_r = !DECAY || wtd;
         for (int n = 0; n < nb && ok; ++n, ++blk) {
@@ -1143,7 +1239,7 @@ __global__ void __launch_bounds__(kDualThreads, 1)
       const int s0 = P.gp.start(g), s1 = min(P.T, P.gp.start(g + 1)), nb = (s1 - s0 + 127) / 128;
       const float lam = (DECAY && !GATE) ? P.decay[h] : 1.f;
       const float l2 = (DECAY && !GATE) ? log2f(lam) : 0.f;
-      const bool wtd = DECAY && !GATE && lam >= kDualWeightedMin;
+      const bool wtd = DECAY && !GATE && lam >= kWeightedMin;
       const float *gc = GATE ? P.gC + (int64_t)bh * P.T : nullptr;
       for (int n = 0; n < nb && ok; ++n, ++blk) {
         // weighted operands: both score tiles take lambda^{-nv} inside the mask
@@ -1217,7 +1313,7 @@ __global__ void __launch_bounds__(kDualThreads, 1)
       const int s0 = P.gp.start(g), s1 = min(P.T, P.gp.start(g + 1)), nb = (s1 - s0 + 127) / 128;
       const float lam = (DECAY && !GATE) ? P.decay[h] : 1.f;
       const float l2 = (DECAY && !GATE) ? log2f(lam) : 0.f;
-      const bool wtd = DECAY && !GATE && lam >= kDualWeightedMin;
+      const bool wtd = DECAY && !GATE && lam >= kWeightedMin;
       const float *gc = GATE ? P.gC + (int64_t)bh * P.T : nullptr;
       auto nvalid = [&](int n) { return min(128, s1 - (s0 + 128 * (nb - 1 - n))); };
       auto start = [&](int n) { return s0 + 128 * (nb - 1 - n); };
@@ -1353,7 +1449,7 @@ __global__ void __launch_bounds__(kDualThreads, 1)
       const int g = item / BH, bh = item % BH, b = bh / P.H, h = bh % P.H;
       const int s0 = P.gp.start(g), s1 = min(P.T, P.gp.start(g + 1)), nb = (s1 - s0 + 127) / 128;
       const float lam = (DECAY && !GATE) ? P.decay[h] : 1.f;
-      const bool wtd = DECAY && !GATE && lam >= kDualWeightedMin;
+      const bool wtd = DECAY && !GATE && lam >= kWeightedMin;
       const float l2 = wtd ? log2f(lam) : 0.f;
       for (int n = 0; n < nb && ok; ++n, ++blk) {
         const int t0 = s0 + 128 * (nb - 1 - n);
@@ -1421,7 +1517,7 @@ cudaError_t set_smem(K kern, size_t bytes) {
 }  // namespace
 
 cudaError_t tc_segment_states(const Problem &p, const GroupPlan &gp, const void *X, const void *Y, bool reverse,
-                              float *out, int *status, cudaStream_t s) {
+                              float *out, int *status, cudaStream_t s, bool skip_weighted) {
   alignas(64) CUtensorMap mx, my;
   if (!seq_tmap(p, X, &mx) || !seq_tmap(p, Y, &my)) return cudaErrorInvalidValue;
   AggParams A;
@@ -1431,6 +1527,7 @@ cudaError_t tc_segment_states(const Problem &p, const GroupPlan &gp, const void 
   if (!status) return cudaErrorInvalidValue;
   A.decay = p.decay; A.out = out; A.status = status; A.counter = status + kCounterAgg;
   A.gC = p.gC; A.gtot = p.gtot;
+  A.skip_weighted = skip_weighted ? 1 : 0;
   const size_t smem = 3 * 2 * kTileBytes + 1024 + 256;
   const int grid = A.nitems < p.num_sms ? A.nitems : p.num_sms;
   cudaError_t e;
@@ -1484,7 +1581,7 @@ cudaError_t tc_dual(const Problem &p, const GroupPlan &gp, const void *q, const 
 cudaError_t tc_main(const Problem &p, const GroupPlan &gp, const void *q, const void *k, const void *v, void *o,
                     const float *group_init, bool init_transposed, float *final_state, int *status,
                     cudaStream_t s, const void *x, float *agg_out) {
-  if (x && (p.decay || p.gC || !agg_out)) return cudaErrorInvalidValue;
+  if (x && (p.gC || !agg_out)) return cudaErrorInvalidValue;
   alignas(64) CUtensorMap mq, mk, mv, mo, mx;
   if (!seq_tmap(p, q, &mq) || !seq_tmap(p, k, &mk) || !seq_tmap(p, v, &mv) || !seq_tmap(p, o, &mo) ||
       !seq_tmap(p, x ? x : q, &mx))
@@ -1509,7 +1606,9 @@ cudaError_t tc_main(const Problem &p, const GroupPlan &gp, const void *q, const 
     if ((e = set_smem(tc_main_kernel<DEC, AGG, GATE>, kMainSmem)) != cudaSuccess) return e;   \
     tc_main_kernel<DEC, AGG, GATE><<<grid, kThreads, kMainSmem, s>>>(mq, mk, mv, mo, mx, M);  \
   } while (0)
-  if (x)
+  if (x && p.decay)
+    LINATTN_LAUNCH_MAIN(true, true, false);
+  else if (x)
     LINATTN_LAUNCH_MAIN(false, true, false);
   else if (p.gC)
     LINATTN_LAUNCH_MAIN(true, false, true);

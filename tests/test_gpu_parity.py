@@ -224,11 +224,13 @@ def test_backward(dtype, d, T, dk):
     assert rel(dinit, rinit) < tol
 
 
-def test_backward_decay_forms_mixed_across_items():
-    """Per-head decays on both sides of 0.8 (above it the dk/dv pass weights its
-    operands before the products, below it between them) in one launch with
-    more (group, sequence) items than SMs, so CTAs take items of both forms in
-    turn; a ragged tail; a few heads of each form checked against the oracle."""
+def test_forward_backward_decay_forms_mixed_across_items():
+    """Per-head decays on both sides of 0.8 (at or above it the chunked kernels
+    weight their operands as the tiles land and the dq pass accumulates the
+    reverse aggregates; below it they weight between the products and the
+    aggregate pass takes those heads) in one launch with more (group, sequence)
+    items than SMs, so CTAs take items of both forms in turn; a ragged tail; a
+    few heads of each form checked against the oracle."""
     B, H, T, d = 2, 16, 32768 + 200, 128  # 9 groups of 3712 tokens: 288 items
     c, dev = case(41, B, H, T, d, torch.bfloat16, sigma=1 / np.sqrt(128))
     lam = np.array([0.55, 0.97, 0.7999, 0.8, 0.99986, 0.6, 0.9, 0.75] * 2, np.float32)
@@ -236,11 +238,15 @@ def test_backward_decay_forms_mixed_across_items():
     ws = la.workspace(dev["q"], la.OP_BWD, dec)
     dq, dk_, dv, dinit = la.bwd(dev["q"], dev["k"], dev["v"], dev["dO"], decay=dec, want_dinit=True, ws=ws)
     assert la.device_status(ws) == la.OK
+    wsf = la.workspace(dev["q"], la.OP_FWD, dec)
+    o, fin, _ = la.fwd(dev["q"], dev["k"], dev["v"], decay=dec, want_final=True, ws=wsf)
+    assert la.device_status(wsf) == la.OK
     for h in (0, 1, 2, 3):
         sl = slice(h, h + 1)
+        ro, _, rfin = oracle.fwd_recurrent(c["q"][:, sl], c["k"][:, sl], c["v"][:, sl], lam=lam[sl])
         rq, rk, rv, rinit = oracle.bwd_recurrent(c["q"][:, sl], c["k"][:, sl], c["v"][:, sl], c["dO"][:, sl],
                                                  lam=lam[sl])
-        for got, ref in ((dq, rq), (dk_, rk), (dv, rv), (dinit, rinit)):
+        for got, ref in ((o, ro), (fin, rfin), (dq, rq), (dk_, rk), (dv, rv), (dinit, rinit)):
             assert rel(got[:, sl], ref) < 1e-2, (h, float(lam[h]))
 
 

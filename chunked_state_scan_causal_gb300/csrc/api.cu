@@ -181,13 +181,14 @@ static size_t ckpt_bytes(const Problem &p) {
   return w.G == 0 ? 0 : (size_t)w.G * p.B * p.H * p.d * p.d * sizeof(float);
 }
 
-// Gated layouts: the forward layout plus the gates' cumulative sums [BH][T] and
-// group totals [G][BH]; the backward adds the reverse aggregates, the reverse
+// Gated layouts: the forward layout plus the gates' cumulative sums [BH][T],
+// group totals [G][BH] and the forward's per-item weighting flags [G][BH]; the
+// backward adds the reverse aggregates, the reverse
 // group states and the per-token q . dq - k . dk of the gate gradient.  The gated checkpoint holds the
 // group states and then the final state.
 struct GatedLayout {
   FwdLayout f;
-  size_t C = 0, tot = 0, wagg = 0, rbar = 0, gx = 0, fwd_total = kHeader, bwd_total = kHeader;
+  size_t C = 0, tot = 0, wflag = 0, wagg = 0, rbar = 0, gx = 0, fwd_total = kHeader, bwd_total = kHeader;
 };
 // With gates the groups are kept to at most 2048 tokens: the gate gradient sums
 // q.dq - k.dk inside a group (anchored exactly at the group ends), and those
@@ -201,7 +202,8 @@ static GatedLayout gated_layout(const Problem &p) {
   const size_t st = (size_t)w.f.G * BH * p.d * p.d * sizeof(float);
   w.C = w.f.total;
   w.tot = w.C + align256((size_t)BH * p.T * sizeof(float));
-  w.fwd_total = w.tot + align256((size_t)w.f.G * BH * sizeof(float));
+  w.wflag = w.tot + align256((size_t)w.f.G * BH * sizeof(float));
+  w.fwd_total = w.wflag + align256((size_t)w.f.G * BH * sizeof(int));
   w.wagg = w.fwd_total;
   w.rbar = w.wagg + align256(st);
   w.gx = w.rbar + align256(st);
@@ -463,9 +465,11 @@ int32_t linattn_fwd_gated(const linattn_shape *shape, const void *q, const void 
   float *agg = reinterpret_cast<float *>(ws + w.f.agg);
   float *states = static_cast<float *>(checkpoint);
   float *fin = states + (size_t)G * BH * p.d * p.d;  // the checkpoint's final state
-  cudaError_t e = gate_prep(p, gp, log_gate, C, tot, s);
+  int *wflag = reinterpret_cast<int *>(ws + w.wflag);
+  cudaError_t e = gate_prep(p, gp, log_gate, C, tot, wflag, s);
   p.gC = C;
   p.gtot = tot;
+  p.gflag = wflag;  // the chunked forward may weight its operands
   if (e == cudaSuccess) e = tc_segment_states(p, gp, k, v, false, agg, status, s);
   if (e == cudaSuccess) e = plan_scan(p, gp, false, agg, init_state, states, nullptr, ws + w.f.scan, status, s, tot);
   if (e == cudaSuccess) e = tc_main(p, gp, q, k, v, o, states, false, fin, status, s);
@@ -510,7 +514,7 @@ int32_t linattn_bwd_gated(const linattn_shape *shape, const void *q, const void 
   float *wagg = reinterpret_cast<float *>(ws + w.wagg), *rbar = reinterpret_cast<float *>(ws + w.rbar);
   const float *states = static_cast<const float *>(checkpoint);
   const float *fin = states + (size_t)G * E;
-  cudaError_t e = gate_prep(p, gp, log_gate, C, tot, s);
+  cudaError_t e = gate_prep(p, gp, log_gate, C, tot, nullptr, s);
   p.gC = C;
   p.gtot = tot;
   p.gq = q;

@@ -25,9 +25,11 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
-// One warp per (sequence, group): inclusive prefix sums in steps of 32 tokens.
+// One warp per (sequence, group): inclusive prefix sums in steps of 32 tokens,
+// and the widest span (max - min) of the sums over any 128-token block of the
+// group together with the sum before the block.
 __global__ void __launch_bounds__(256) gate_prep_kernel(const float *lg, int T, GroupPlan gp, int BH, float *C,
-                                                        float *tot) {
+                                                        float *tot, int *wflag) {
   const int G = gp.G;
   const int w = (int)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) / 32), lane = threadIdx.x & 31;
   if (w >= BH * G) return;  // warp-uniform
@@ -36,6 +38,7 @@ __global__ void __launch_bounds__(256) gate_prep_kernel(const float *lg, int T, 
   const float *src = lg + (int64_t)bh * T;
   float *dst = C + (int64_t)bh * T;
   float carry = 0.f;
+  float bmin = 0.f, bmax = 0.f, span = 0.f;  // the current block's range (from the sum before it)
   for (int t = s0; t < s1; t += 32) {
     const int tt = t + lane;
     float x = tt < s1 ? src[tt] * kLog2e : 0.f;
@@ -46,9 +49,25 @@ __global__ void __launch_bounds__(256) gate_prep_kernel(const float *lg, int T, 
     }
     x += carry;
     if (tt < s1) dst[tt] = x;
+    // lanes past the end hold the last sum, so all 32 lanes take part
+    float mn = x, mx = x;
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) {
+      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, d));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, d));
+    }
+    bmin = fminf(bmin, mn);
+    bmax = fmaxf(bmax, mx);
     carry = __shfl_sync(0xffffffffu, x, 31);
+    if (((t - s0) & 127) == 96 || t + 32 >= s1) {  // a block ends (groups start on 128-token boundaries)
+      span = fmaxf(span, bmax - bmin);
+      bmin = bmax = carry;
+    }
   }
-  if (lane == 0) tot[(int64_t)g * BH + bh] = carry;
+  if (lane == 0) {
+    tot[(int64_t)g * BH + bh] = carry;
+    if (wflag) wflag[(int64_t)g * BH + bh] = span <= kGateWeightedSpan ? 1 : 0;  // an infinite span fails
+  }
 }
 
 // w[i] += exp2(tot[bh]) d[i] over n = BH * DD elements.
@@ -119,11 +138,11 @@ __global__ void __launch_bounds__(256) dgate_kernel(int T, GroupPlan gp, int BH,
 }  // namespace
 
 cudaError_t gate_prep(const Problem &p, const GroupPlan &gp, const float *log_gate, float *C, float *tot,
-                      cudaStream_t s) {
+                      int *wflag, cudaStream_t s) {
   const int BH = p.B * p.H;
   const int64_t warps = (int64_t)BH * gp.G;
   TimedLaunch t(K_GATE, s);
-  gate_prep_kernel<<<(int)((warps + 7) / 8), 256, 0, s>>>(log_gate, p.T, gp, BH, C, tot);
+  gate_prep_kernel<<<(int)((warps + 7) / 8), 256, 0, s>>>(log_gate, p.T, gp, BH, C, tot, wflag);
   return cudaGetLastError();
 }
 

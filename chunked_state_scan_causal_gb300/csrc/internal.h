@@ -17,6 +17,10 @@ struct Problem {
   // data-dependent gates (tensor-core path): group-local log2 cumulative sums
   // [B*H][T] and group totals [G][B*H] for the group length in use, or nullptr
   const float *gC = nullptr, *gtot = nullptr;
+  // gated forward: per (group, sequence) item [G][B*H], nonzero when every
+  // 128-token block of the group keeps its cumulative sums, and the one before
+  // it, within a span of kGateWeightedSpan (the weighted-operand form applies)
+  const int *gflag = nullptr;
   // gates, backward: q and k (bf16, the request's strides) and gx [B*H][T] fp32,
   // which the dq pass fills with q_t . dq_t and the dk/dv pass reduces by k_t . dk_t
   const void *gq = nullptr, *gk = nullptr;
@@ -99,8 +103,12 @@ cudaError_t fold_state(float *w, const float *d, const float *decay_h, int H, in
 
 // ---------------------------------------------------------------- data-dependent gates (gate.cu)
 // C[t] = log2(e) * sum of log_gate over the group of L tokens up to t ([B,H,T]);
-// tot[g][bh] = C at the group's last token.
-cudaError_t gate_prep(const Problem &p, const GroupPlan &gp, const float *log_gate, float *C, float *tot, cudaStream_t s);
+// tot[g][bh] = C at the group's last token; wflag[g][bh] (if not null) =
+// whether every 128-token block of the group, with the sum before it, spans
+// at most kGateWeightedSpan.
+constexpr float kGateWeightedSpan = 60.f;
+cudaError_t gate_prep(const Problem &p, const GroupPlan &gp, const float *log_gate, float *C, float *tot,
+                      int *wflag, cudaStream_t s);
 // w[i] += exp2(tot_last[i / DD]) d[i], n elements.
 cudaError_t fold_state_log2(float *w, const float *d, const float *tot_last, int DD, int64_t n, cudaStream_t s);
 // d_log_gate [B,H,T]: reverse sums of gx [B*H][T] (q_t . dq_t - k_t . dk_t) inside each

@@ -372,6 +372,7 @@ struct MainParams {
   int *status;
   int *counter;        // [2] item counter and finished CTAs (zero at launch)
   const float *gC;     // GATE: group-local log2 cumulative sums of the gates [BH][T]
+  const int *gflag;    // GATE, forward: per item [G][BH], nonzero: the weighted-operand form applies
   const __nv_bfloat16 *gq;  // GATE, dq pass: the true q (strides sb, sh, st) for gx = q . dq
   float *gx;           // GATE, dq pass: [BH][T] fp32 q_t . dq_t from the unrounded dq, or null
   int64_t sb, sh, st;
@@ -617,7 +618,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s0 = P.gp.start(g), s1 = min(P.T, P.gp.start(g + 1)), nb = (s1 - s0 + 127) / 128;
         // weighted-operand form (K and X weighted as they land); the group
         // aggregate is accumulated here unless a decay takes the other form
-        const bool wtd = DECAY && !GATE && P.decay[(item % BH) % P.H] >= kWeightedMin;
+        const bool wtd = DECAY && (GATE ? P.gflag && P.gflag[item] != 0
+                                        : P.decay[(item % BH) % P.H] >= kWeightedMin);
         const bool aggw = AGG && (!DECAY || wtd);
         for (int n = 0; n < nb; ++n, ++blk) {
           const int tq = tile_of(blk, 0), tk = tile_of(blk, 1), tv = tile_of(blk, 2), tx = tile_of(blk, 3);
@@ -693,12 +695,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int s0 = P.gp.start(g), s1 = min(P.T, P.gp.start(g + 1)), nb = (s1 - s0 + 127) / 128;
       const float lam = (DECAY && !GATE) ? P.decay[h] : 1.f;
       const float l2 = (DECAY && !GATE) ? log2f(lam) : 0.f;
-      const bool wtd = DECAY && !GATE && lam >= kWeightedMin;
+      const bool wtd = DECAY && (GATE ? P.gflag && P.gflag[item] != 0 : lam >= kWeightedMin);
       const float *gc = GATE ? P.gC + (int64_t)bh * P.T : nullptr;
       for (int n = 0; n < nb; ++n, ++blk) {
         const int t0 = s0 + 128 * n, nv = min(128, s1 - t0);
-        // weighted form: the scores of K' take lambda^{-nv} inside the causal mask
-        const float wsc = wtd ? exp2f(-l2 * (float)nv) : 1.f;
+        // weighted form: the scores of K' take lambda^{-nv} (gates: exp2(C_prev -
+        // C_last)) inside the causal mask
+        float wsc = 1.f;
+        if (wtd) wsc = GATE ? exp2f((t0 > s0 ? gc[t0 - 1] : 0.f) - gc[t0 + nv - 1]) : exp2f(-l2 * (float)nv);
         float ci = 0.f, cprev = 0.f;
         // one buffer of sums and column factors: the previous block's readers passed
         // the output-store barrier of that block before this write
@@ -706,8 +710,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (GATE) {
           ci = gate_c(gc, t0, (int)row, nv);
           cprev = t0 > s0 ? gc[t0 - 1] : 0.f;
-          cb[row] = ci;  // read by the whole group after the barrier below
-          cw[row] = gate_colw<false>(gc, t0, (int)row, nv);
+          if (!wtd) {  // the per-element mask's sums and column factors
+            cb[row] = ci;  // read by the whole group after the barrier below
+            cw[row] = gate_colw<false>(gc, t0, (int)row, nv);
+          }
         }
         if (GATE && P.gx && (int)row < nv) {
           // the q row for the epilogue's q . dq: two 128-byte lines into L1 now
@@ -725,7 +731,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 4; ++c) {
           float x[32];
           ld_chunk(tP + lb + c * 32, x);
-          if (GATE) {
+          if (GATE && !wtd) {
             mask_chunk_gate<false>(x, (int)row, c, ci, cb, cw);
           } else if (wtd) {
             mask_chunk<false, false>(x, (int)row, c, 1.f, 0.f);
@@ -754,7 +760,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           float x[32];
           ld_chunk(tO + lb + c * 32, x);
           if (wtd) {
-            // the accumulator holds o_i / lambda^{i+1}
+            // the accumulator holds o_i / lambda^{i+1} (gates: / exp2(C_i - C_prev))
 #pragma unroll
             for (int j = 0; j < 32; ++j) x[j] *= wq;
           } else if (DECAY) {
@@ -791,15 +797,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int s0 = P.gp.start(g), s1 = min(P.T, P.gp.start(g + 1)), nb = (s1 - s0 + 127) / 128;
       const float lam = (DECAY && !GATE) ? P.decay[h] : 1.f;
       const float l2 = (DECAY && !GATE) ? log2f(lam) : 0.f;
-      const bool wtd = DECAY && !GATE && lam >= kWeightedMin;
+      const bool wtd = DECAY && (GATE ? P.gflag && P.gflag[item] != 0 : lam >= kWeightedMin);
       const bool aggw = AGG && (!DECAY || wtd);
       const float *gc = GATE ? P.gC + (int64_t)bh * P.T : nullptr;
       auto nvalid = [&](int n) { return min(128, s1 - (s0 + 128 * n)); };
-      // weighted form: key rows lambda^{nv-1-j}; rows of X (the group aggregate's
-      // left factor) lambda^{s-start+1}
+      // weighted form: key rows lambda^{nv-1-j} (gates: exp2(C_last - C_j)); rows
+      // of X (the group aggregate's left factor) lambda^{s-start+1}
       auto wk = [&](int n) {
-        const int nv = nvalid(n), r = (int)row;
-        return r < nv ? exp2f(l2 * (float)(nv - 1 - r)) : 0.f;
+        const int nv = nvalid(n), r = (int)row, t0 = s0 + 128 * n;
+        if (r >= nv) return 0.f;
+        return GATE ? exp2f(gc[t0 + nv - 1] - gc[t0 + r]) : exp2f(l2 * (float)(nv - 1 - r));
       };
       auto wx = [&](int n) { return (int)row < nvalid(n) ? exp2f(l2 * (float)(128 * n + (int)row + 1)) : 0.f; };
       // weigh this thread's row of tile role r (1 K, 3 X) of CTA block b once it
@@ -814,9 +821,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&bar[bar_idx + (b & 1)]);
         return true;
       };
-      // weighted form: the block's K (and X) ahead of its scores
-      auto weigh_block = [&](int b, int n) { return weigh(b, 1, wk(n), B_KS) && (!AGG || weigh(b, 3, wx(n), B_XS)); };
-      if (wtd && !(ok = weigh_block(blk, 0))) break;
+      // weighted form: the block's K (and X) ahead of its scores, with the key
+      // row's weight wkn (loaded early: gates read it from global memory)
+      auto weigh_block = [&](int b, int n, float wkn) {
+        return weigh(b, 1, wkn, B_KS) && (!AGG || weigh(b, 3, wx(n), B_XS));
+      };
+      if (wtd && !(ok = weigh_block(blk, 0, wk(0)))) break;
       // state decay across block n: lambda^{nv}, or the product of its gates
       auto block_decay = [&](int n) {
         const int t0 = s0 + 128 * n, nv = nvalid(n);
@@ -855,6 +865,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the next block's state decay (gates: two loads), ahead of the waits below
         const float dec_next = n + 1 < nb ? block_decay(n + 1) : 1.f;
         const bool more = n + 1 < nb;
+        const float wk_next = (wtd && more) ? wk(n + 1) : 0.f;  // ahead of the waits below
         if (DECAY && !wtd) {
           // key rows k_j *= lambda^{nv-1-j} (gates: exp2(C_last - C_j)) once the scores have read them
           const int nv = nvalid(n), r = (int)row, t0 = s0 + 128 * n;
@@ -886,7 +897,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
           }
-          if (next_done && !(ok = weigh_block(blk + 1, n + 1))) break;
+          if (next_done && !(ok = weigh_block(blk + 1, n + 1, wk_next))) break;
         }
         ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_SFULL], blk & 1, &abort_flag, P.status, detail));
         if (!ok) break;
@@ -909,7 +920,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_before();
           fence_proxy_async_smem();
           mbar_arrive(&bar[B_PRE]);
-          if (wtd && !next_done && !(ok = weigh_block(blk + 1, n + 1))) break;
+          if (wtd && !next_done && !(ok = weigh_block(blk + 1, n + 1, wk_next))) break;
         } else if (aggw) {
           // the group's aggregate W (complete: its last product precedes the state update)
           float *dst = P.agg_out + ((int64_t)g * BH + bh) * 16384 + row * 128;
@@ -1595,6 +1606,7 @@ cudaError_t tc_main(const Problem &p, const GroupPlan &gp, const void *q, const 
   M.counter = status + kCounterMain;
   M.agg_out = agg_out;
   M.gC = p.gC;
+  M.gflag = p.gflag;
   M.gq = static_cast<const __nv_bfloat16 *>(p.gq);
   M.gx = p.gx;
   M.sb = p.sb; M.sh = p.sh; M.st = p.st;

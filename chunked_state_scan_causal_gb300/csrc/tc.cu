@@ -567,8 +567,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sPs = sbase + kOffPs, sSh = sbase + kOffSh;
   auto slot_addr = [&](int t) { return sbase + (uint32_t)(t % kSlots) * kTileBytes; };
   // ring position of tile role r (0 q, 1 k, 2 v, 3 x) of block blk
+  // Tiles are loaded in this order per block and the ring reuses, for tile t,
+  // the slot of tile t - 5: only a block's first tile takes a slot freed a
+  // whole block earlier.  AGG loads q, x, k, v; AGG with a decay loads k
+  // first, so the next block's key tile lands early enough to be weighted off
+  // the critical path (then q, x, v).
   auto tile_of = [&](int blk, int r) {
-    return NT * blk + (AGG ? (r == 0 ? 0 : (r == 3 ? 1 : r + 1)) : r);
+    if (!AGG) return NT * blk + r;
+    if (DECAY) return NT * blk + (r == 1 ? 0 : (r == 0 ? 1 : (r == 3 ? 2 : 3)));
+    return NT * blk + (r == 0 ? 0 : (r == 3 ? 1 : r + 1));
   };
 
   if (warp == 0) {
@@ -586,8 +593,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int x = 0; x < NT; ++x) {
             const int t = NT * blk + x, s = t % kSlots, u = t / kSlots;
             if (u > 0 && !(ok = mbar_wait(&bar[B_EMPTY + s], (u - 1) & 1, &abort_flag, P.status, detail))) break;
-            const CUtensorMap *m = AGG ? (x == 0 ? &mq : (x == 1 ? &mx : (x == 2 ? &mk : &mv)))
-                                       : (x == 0 ? &mq : (x == 1 ? &mk : &mv));
+            const CUtensorMap *m = (AGG && DECAY) ? (x == 0 ? &mk : (x == 1 ? &mq : (x == 2 ? &mx : &mv)))
+                                   : AGG          ? (x == 0 ? &mq : (x == 1 ? &mx : (x == 2 ? &mk : &mv)))
+                                                  : (x == 0 ? &mq : (x == 1 ? &mk : &mv));
             uint8_t *dst = smem + s * kTileBytes;
             mbar_arrive_expect_tx(&bar[B_FULL + s], kTileBytes);
             tma_load_4d(m, &bar[B_FULL + s], dst, 0, t0, h, b, kPolicyEvictFirst);
@@ -878,11 +886,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(&bar[B_KS + (blk & 1)]);
           if (AGG) mbar_arrive(&bar[B_XS + (blk & 1)]);  // one phase per block in either form
         }
-        // weighted form, next block: K (and X) as soon as they land, unless this
-        // block's state is ready first (then after the state, which is on the
-        // critical path).  The next X takes the slot of this block's Q: this
-        // block's scores completing says that Q has landed, so its fill is the
-        // one before X's.
+        // weighted form, next block: K as soon as it lands, unless this block's
+        // state is ready first (then after the state, which is on the critical
+        // path); X after the state (its product follows the next block's
+        // scores).  The next X takes the slot of this block's Q: this block's
+        // scores completing says that Q has landed, so its fill is the one
+        // before X's.
         bool next_done = false;
         if (wtd && more) {
           if (AGG &&
@@ -897,7 +906,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
           }
-          if (next_done && !(ok = weigh_block(blk + 1, n + 1, wk_next))) break;
+          if (next_done && !(ok = weigh(blk + 1, 1, wk_next, B_KS))) break;
         }
         ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_SFULL], blk & 1, &abort_flag, P.status, detail));
         if (!ok) break;
@@ -920,7 +929,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_before();
           fence_proxy_async_smem();
           mbar_arrive(&bar[B_PRE]);
-          if (wtd && !next_done && !(ok = weigh_block(blk + 1, n + 1, wk_next))) break;
+          if (wtd && !next_done && !(ok = weigh(blk + 1, 1, wk_next, B_KS))) break;
+          if (wtd && AGG && !(ok = weigh(blk + 1, 3, wx(n + 1), B_XS))) break;
         } else if (aggw) {
           // the group's aggregate W (complete: its last product precedes the state update)
           float *dst = P.agg_out + ((int64_t)g * BH + bh) * 16384 + row * 128;

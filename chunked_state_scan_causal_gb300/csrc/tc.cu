@@ -493,20 +493,30 @@ __device__ __forceinline__ float dot32_bf16(const float (&x)[32], const __nv_bfl
 }
 
 
-// With a decay the inter-block term goes to the fourth TMEM region from the
-// unweighted q (O_inter = Q S) and the epilogue adds lambda^{i+1} O_inter to
-// the intra-block term, so only the key rows are weighted in shared memory
-// (k_j *= lambda^{nv-1-j}, for the state update), and that off the path from
-// the scores to the inter-block product.
-// AGG instances (no decay) also load a fourth tile x per block and accumulate
-// the group aggregate W = sum_s x_s q_s^T in the fourth TMEM region, written
-// per group to agg_out: for the dq launch (q := dO, x := q) that is the
-// reverse group aggregate sum_s q_s dO_s^T.  Tiles are loaded in the order
-// q, x, k, v and released in the same order.
+// With a decay, each (group, sequence) item takes one of two forms:
+//  * weighted operands (lambda >= kWeightedMin; gated forward items that
+//    gate_prep flags): group B weights the key rows (k_j *= lambda^{nv-1-j})
+//    as their tile lands, the scores Q K'^T take the causal 0/1 mask times
+//    lambda^{-nv}, and the output accumulator takes Q S and then P V, holding
+//    o_i / lambda^{i+1}, which the store multiplies back;
+//  * otherwise the inter-block term goes to the fourth TMEM region from the
+//    unweighted q (O_inter = Q S), the mask is applied per element, the
+//    epilogue adds lambda^{i+1} O_inter to the intra-block term, and the key
+//    rows are weighted after the scores have read them, for the state update.
+// AGG instances also load a fourth tile x per block and accumulate the group
+// aggregate W = sum_s w_s x_s q_s^T in the fourth TMEM region (w_s =
+// lambda^{s-start+1}, 1 without a decay; x rows weighted as they land),
+// written per group to agg_out: for the dq launch (q := dO, x := q) that is
+// the reverse group aggregate sum_s w_s q_s dO_s^T.  With a decay only the
+// items of the weighted form do so (the fourth region holds O_inter in the
+// others).  Tiles are loaded in the order q, x, k, v (with a decay k, q, x, v,
+// see tile_of) and released as their last product completes.
 // GATE (with DECAY) takes every weight from the gates' group-local cumulative
 // sums C: o_i = exp2(C_i - C_prev) (Q S)_i + (P V)_i, mask exp2(C_i - C_j), key
 // rows exp2(C_last - C_j), state decay exp2(C_last - C_prev) per block (C_prev:
-// the token before the block, 0 at a group start).
+// the token before the block, 0 at a group start); in the weighted form the
+// mask scalar is exp2(C_prev - C_last) and the store's row weight
+// exp2(C_i - C_prev).
 template <bool DECAY, bool AGG = false, bool GATE = false>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_main_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,

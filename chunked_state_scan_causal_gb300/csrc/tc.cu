@@ -495,10 +495,12 @@ __device__ __forceinline__ float dot32_bf16(const float (&x)[32], const __nv_bfl
 
 // With a decay, each (group, sequence) item takes one of two forms:
 //  * weighted operands (lambda >= kWeightedMin; gated forward items that
-//    gate_prep flags): group B weights the key rows (k_j *= lambda^{nv-1-j})
-//    as their tile lands, the scores Q K'^T take the causal 0/1 mask times
-//    lambda^{-nv}, and the output accumulator takes Q S and then P V, holding
-//    o_i / lambda^{i+1}, which the store multiplies back;
+//    gate_prep flags): group B weights the value rows (v_j *= lambda^{nv-1-j},
+//    for the state update K^T V' and for P V'), so the scores Q K^T need no
+//    weighted tile and take the causal 0/1 mask times lambda^{-nv}
+//    (lambda^{-j-1} v_j = lambda^{-nv} v'_j), and the output accumulator takes
+//    Q S and then P V', holding o_i / lambda^{i+1}, which the store multiplies
+//    back;
 //  * otherwise the inter-block term goes to the fourth TMEM region from the
 //    unweighted q (O_inter = Q S), the mask is applied per element, the
 //    epilogue adds lambda^{i+1} O_inter to the intra-block term, and the key
@@ -509,8 +511,8 @@ __device__ __forceinline__ float dot32_bf16(const float (&x)[32], const __nv_bfl
 // written per group to agg_out: for the dq launch (q := dO, x := q) that is
 // the reverse group aggregate sum_s w_s q_s dO_s^T.  With a decay only the
 // items of the weighted form do so (the fourth region holds O_inter in the
-// others).  Tiles are loaded in the order q, x, k, v (with a decay k, q, x, v,
-// see tile_of) and released as their last product completes.
+// others).  Tiles are loaded in the order q, x, k, v and released as their
+// last product completes.
 // GATE (with DECAY) takes every weight from the gates' group-local cumulative
 // sums C: o_i = exp2(C_i - C_prev) (Q S)_i + (P V)_i, mask exp2(C_i - C_j), key
 // rows exp2(C_last - C_j), state decay exp2(C_last - C_prev) per block (C_prev:
@@ -577,15 +579,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sPs = sbase + kOffPs, sSh = sbase + kOffSh;
   auto slot_addr = [&](int t) { return sbase + (uint32_t)(t % kSlots) * kTileBytes; };
   // ring position of tile role r (0 q, 1 k, 2 v, 3 x) of block blk
-  // Tiles are loaded in this order per block and the ring reuses, for tile t,
-  // the slot of tile t - 5: only a block's first tile takes a slot freed a
-  // whole block earlier.  AGG loads q, x, k, v; AGG with a decay loads k
-  // first, so the next block's key tile lands early enough to be weighted off
-  // the critical path (then q, x, v).
   auto tile_of = [&](int blk, int r) {
-    if (!AGG) return NT * blk + r;
-    if (DECAY) return NT * blk + (r == 1 ? 0 : (r == 0 ? 1 : (r == 3 ? 2 : 3)));
-    return NT * blk + (r == 0 ? 0 : (r == 3 ? 1 : r + 1));
+    return NT * blk + (AGG ? (r == 0 ? 0 : (r == 3 ? 1 : r + 1)) : r);
   };
 
   if (warp == 0) {
@@ -603,9 +598,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int x = 0; x < NT; ++x) {
             const int t = NT * blk + x, s = t % kSlots, u = t / kSlots;
             if (u > 0 && !(ok = mbar_wait(&bar[B_EMPTY + s], (u - 1) & 1, &abort_flag, P.status, detail))) break;
-            const CUtensorMap *m = (AGG && DECAY) ? (x == 0 ? &mk : (x == 1 ? &mq : (x == 2 ? &mx : &mv)))
-                                   : AGG          ? (x == 0 ? &mq : (x == 1 ? &mx : (x == 2 ? &mk : &mv)))
-                                                  : (x == 0 ? &mq : (x == 1 ? &mk : &mv));
+            const CUtensorMap *m = AGG ? (x == 0 ? &mq : (x == 1 ? &mx : (x == 2 ? &mk : &mv)))
+                                       : (x == 0 ? &mq : (x == 1 ? &mk : &mv));
             uint8_t *dst = smem + s * kTileBytes;
             mbar_arrive_expect_tx(&bar[B_FULL + s], kTileBytes);
             tma_load_4d(m, &bar[B_FULL + s], dst, 0, t0, h, b, kPolicyEvictFirst);
@@ -643,10 +637,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int tq = tile_of(blk, 0), tk = tile_of(blk, 1), tv = tile_of(blk, 2), tx = tile_of(blk, 3);
           const uint32_t Q = slot_addr(tq), K = slot_addr(tk), V = slot_addr(tv);
           const int wb = blk & 1, wp = (blk >> 1) & 1;
-          // scores: P = Q K^T  (weighted form: K')
+          // scores: P = Q K^T
           ok = mbar_wait(&bar[B_FULL + tq % kSlots], (tq / kSlots) & 1, &abort_flag, P.status, detail) &&
-               (wtd ? mbar_wait(&bar[B_KS + wb], wp, &abort_flag, P.status, detail)
-                    : mbar_wait(&bar[B_FULL + tk % kSlots], (tk / kSlots) & 1, &abort_flag, P.status, detail)) &&
+               mbar_wait(&bar[B_FULL + tk % kSlots], (tk / kSlots) & 1, &abort_flag, P.status, detail) &&
                (blk == 0 || mbar_wait(&bar[B_PEMPTY], (blk - 1) & 1, &abort_flag, P.status, detail));
           if (!ok) break;
           tc_fence_after();
@@ -680,8 +673,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           mma_commit(&bar[B_EMPTY + tq % kSlots]);
           if (AGG) mma_commit(&bar[B_EMPTY + tx % kSlots]);
-          // state update: S += K'^T V  (K' = decay-weighted key rows)
-          ok = (!DECAY || wtd || mbar_wait(&bar[B_KS + wb], wp, &abort_flag, P.status, detail)) &&
+          // state update: S += K'^T V (decay-weighted key rows), or K^T V' in the
+          // weighted form (decay-weighted value rows, which P V reads too)
+          ok = (!DECAY || mbar_wait(&bar[B_KS + wb], wp, &abort_flag, P.status, detail)) &&
                mbar_wait(&bar[B_FULL + tv % kSlots], (tv / kSlots) & 1, &abort_flag, P.status, detail);
           if (!ok) break;
           tc_fence_after();
@@ -819,7 +813,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool aggw = AGG && (!DECAY || wtd);
       const float *gc = GATE ? P.gC + (int64_t)bh * P.T : nullptr;
       auto nvalid = [&](int n) { return min(128, s1 - (s0 + 128 * n)); };
-      // weighted form: key rows lambda^{nv-1-j} (gates: exp2(C_last - C_j)); rows
+      // weighted form: value rows lambda^{nv-1-j} (gates: exp2(C_last - C_j)); rows
       // of X (the group aggregate's left factor) lambda^{s-start+1}
       auto wk = [&](int n) {
         const int nv = nvalid(n), r = (int)row, t0 = s0 + 128 * n;
@@ -827,7 +821,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         return GATE ? exp2f(gc[t0 + nv - 1] - gc[t0 + r]) : exp2f(l2 * (float)(nv - 1 - r));
       };
       auto wx = [&](int n) { return (int)row < nvalid(n) ? exp2f(l2 * (float)(128 * n + (int)row + 1)) : 0.f; };
-      // weigh this thread's row of tile role r (1 K, 3 X) of CTA block b once it
+      // weigh this thread's row of tile role r (2 V, 3 X) of CTA block b once it
       // has landed, then arrive on the barrier bar_idx + block parity
       auto weigh = [&](int b, int r, float w, int bar_idx) {
         const int t = tile_of(b, r);
@@ -839,10 +833,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&bar[bar_idx + (b & 1)]);
         return true;
       };
-      // weighted form: the block's K (and X) ahead of its scores, with the key
-      // row's weight wkn (loaded early: gates read it from global memory)
+      // weighted form: the block's V (and X), with the value row's weight wkn
+      // (loaded early: gates read it from global memory).  A tile's slot was
+      // last filled by a tile of the block before (V: its k or, without AGG, its
+      // q; X: its q), which the MMA thread waited for before that block's state
+      // update, so the state barrier waited before this says the fill landed.
+      // X first: its product comes earlier, and its slot frees earlier than V's.
       auto weigh_block = [&](int b, int n, float wkn) {
-        return weigh(b, 1, wkn, B_KS) && (!AGG || weigh(b, 3, wx(n), B_XS));
+        return (!AGG || weigh(b, 3, wx(n), B_XS)) && weigh(b, 2, wkn, B_KS);
       };
       if (wtd && !(ok = weigh_block(blk, 0, wk(0)))) break;
       // state decay across block n: lambda^{nv}, or the product of its gates
@@ -896,28 +894,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(&bar[B_KS + (blk & 1)]);
           if (AGG) mbar_arrive(&bar[B_XS + (blk & 1)]);  // one phase per block in either form
         }
-        // weighted form, next block: K as soon as it lands, unless this block's
-        // state is ready first (then after the state, which is on the critical
-        // path); X after the state (its product follows the next block's
-        // scores).  The next X takes the slot of this block's Q: this block's
-        // scores completing says that Q has landed, so its fill is the one
-        // before X's.
-        bool next_done = false;
-        if (wtd && more) {
-          if (AGG &&
-              !(ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_PFULL], blk & 1, &abort_flag, P.status, detail))))
-            break;
-          const int t = tile_of(blk + 1, 1);
-#pragma unroll 1
-          for (int i = 0; i < (1 << 20) && !abort_flag; ++i) {
-            if (__any_sync(0xffffffffu, mbar_test_wait(&bar[B_SFULL], blk & 1))) break;
-            if (__all_sync(0xffffffffu, mbar_test_wait(&bar[B_FULL + t % kSlots], (t / kSlots) & 1))) {
-              next_done = true;
-              break;
-            }
-          }
-          if (next_done && !(ok = weigh(blk + 1, 1, wk_next, B_KS))) break;
-        }
         ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_SFULL], blk & 1, &abort_flag, P.status, detail));
         if (!ok) break;
         tc_fence_after();
@@ -939,8 +915,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_before();
           fence_proxy_async_smem();
           mbar_arrive(&bar[B_PRE]);
-          if (wtd && !next_done && !(ok = weigh(blk + 1, 1, wk_next, B_KS))) break;
-          if (wtd && AGG && !(ok = weigh(blk + 1, 3, wx(n + 1), B_XS))) break;
+          // weighted form: the next block's V (and X), off the path to its scores
+          if (wtd && !(ok = weigh_block(blk + 1, n + 1, wk_next))) break;
         } else if (aggw) {
           // the group's aggregate W (complete: its last product precedes the state update)
           float *dst = P.agg_out + ((int64_t)g * BH + bh) * 16384 + row * 128;

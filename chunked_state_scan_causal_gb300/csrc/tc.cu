@@ -147,9 +147,12 @@ __device__ __forceinline__ void items_done(int *counter) {
 }
 
 // Per-head decays lambda >= kWeightedMin take the weighted-operand forms of
-// the chunked kernels (rows weighted as their tiles land, masks that reduce to
-// a 0/1 pattern times one scalar per block, output rows weighted in the store):
-// every factor then stays within lambda^{+-256}, i.e. 2^{+-83} at 0.8.
+// the chunked kernels (rows weighted in shared memory, masks that reduce to a
+// 0/1 pattern times one scalar per block, output rows weighted in the store):
+// the mask scalars and the row weights then stay within lambda^{+-256}, i.e.
+// 2^{+-83} at 0.8.  (The reverse aggregates' token weights lambda^{s-start+1}
+// may underflow deep into a group, as they do in the aggregate kernel: those
+// terms are far below the fp32 resolution of the group's first ones.)
 constexpr float kWeightedMin = 0.8f;
 
 // Multiply one 128-element bf16 row of an SW128 tile by w (rounded back to bf16).

@@ -1,13 +1,24 @@
-"""Benchmark of chunked causal linear attention (forward + backward) on GB300.
+"""Benchmark of chunked causal linear attention on GB300.
 
-One step = the whole hot path over one batch: linattn_fwd (segment aggregates,
-state scan, chunked forward) then linattn_bwd (forward states recomputed,
-reverse states, dq / dv / dk passes) on the synthetic workload
-B=2, H=16, T=65536, d=128, bf16, lambda=1 (seeded; q, k, v ~ N(0, 0.125^2),
-dO ~ N(0, 1)).  Prints ONE JSON line.
+A "step" is one pass of the whole hot path over one batch of synthetic input:
+
+  workload 3 (default): B=2 H=16 T=65536 d=128 bf16, lambda=1; step = the
+      checkpointed forward (linattn_fwd_ckpt) then the backward
+      (linattn_bwd_ckpt); q, k, v ~ N(0, 0.125^2), dO ~ N(0, 1), seeded;
+  workload 2: B=4 H=16 T=16384 forward only (linattn_fwd);
+  workload 4: B=1 H=32 T=131072 with per-head decays, forward + backward;
+  workload 5: B=1 H=16 T=2^20 as 64 segments of 16384 tokens: segment states
+      (linattn_chunk_states) -> exclusive scan (linattn_state_scan) ->
+      per-segment forward from those states; the single unsegmented forward of
+      the same sequence is timed in the same run (`single_fwd`);
+  workload 6: B=1 H=32 T=131072 with per-token gates, forward + backward.
+
+Prints ONE JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload 3]
 
+The timed region runs with the library's per-kernel event timing off; the
+per-kernel breakdown (`kernels`) comes from a separate pass afterwards.
 --impl reference times the fp64 CPU oracle on a bounded sample of the same
 workload (the reference arm of this benchmark: there is no upstream code).
 Under torchrun each rank runs an independent replica (weak scaling); only
@@ -16,6 +27,7 @@ rank 0 prints.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import json
 import os
 import statistics
@@ -28,18 +40,23 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "causal linear-attn fwd+bwd tokens/s & TFLOP/s @H16 d128 T16K–1M; % roofline"
-# algorithmic work per token per head at d = 128 (chunk 64): forward 4d(C+d) FLOP and
-# q,k,v read + o written; backward 8d(C+d) FLOP and q,k,v,dO read + dq,dk,dv written.
+# Algorithmic work per token per head at d = 128 (chunk 64): forward 4d(C+d) FLOP,
+# q, k, v read once and o written once; backward 8d(C+d) FLOP, q, k, v, dO read
+# once and dq, dk, dv written once.  The segment pipeline reads k, v once more
+# for the segment states (1536 B).  Group states, recomputation and re-reads
+# are not credited.
 FLOP_FWD, FLOP_BWD = 98304, 196608
 BYTES_FWD, BYTES_BWD = 1024, 1792
-# algorithmic bytes per token-head of one launch of each tensor-core kernel kind:
-# the chunked kernel reads three bf16 sequence tensors and writes one (with the
-# fused group aggregates of the dq pass it reads a fourth); the dual reverse-time
-# kernel reads four (k, q, dO, v) and writes two (dk, dv); the aggregate kernel
-# reads two.  Group states are overhead, not credited.
-KIND_BYTES_PER_TOKEN_HEAD = {"tc_chunked_fwd": 1024, "tc_chunked_fwd_agg": 1280,
-                             "tc_dual_rev": 1536, "tc_segment_aggregate": 512}
-CHUNKED_KINDS = ("tc_chunked_fwd", "tc_chunked_fwd_agg", "tc_dual_rev")
+BYTES_SEGMENTS = 1536
+# Bytes each kernel kind moves per token-head and launch by its own inputs and
+# outputs (sequence tensors only): an I/O figure per kernel, not the method's
+# algorithmic bytes.
+KIND_IO_BYTES_PER_TOKEN_HEAD = {"tc_chunked_fwd": 1024, "tc_chunked_fwd_agg": 1280, "tc_fused_fwd": 1536,
+                                "tc_dual_rev": 1536, "tc_segment_aggregate": 512}
+# The tensor-core kernels run 128-token blocks (two chunks of 64): the chunked
+# form equals the definition for any chunk length, only the rounding order changes.
+BLOCK = 128
+TRAFFIC_JSON = os.path.join(ROOT, "profiles", "traffic.json")
 
 
 def _dist():
@@ -75,18 +92,64 @@ def _peaks():
         return 6800.0, 1700.0, "fallback"
 
 
+class _Nvml:
+    """Read-only NVML queries through ctypes (clocks and clock-event reasons)."""
+    SM = 1
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown"}
+
+    def __init__(self, uuid: str | None, index: int):
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        ok = False
+        if uuid:
+            ok = self.lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.h)) == 0
+        if not ok and self.lib.nvmlDeviceGetHandleByIndex_v2(index, ctypes.byref(self.h)) != 0:
+            raise OSError("no NVML device handle")
+        self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def sm_mhz(self):
+        v = ctypes.c_uint()
+        return v.value if self.lib.nvmlDeviceGetClockInfo(self.h, self.SM, ctypes.byref(v)) == 0 else None
+
+    def max_sm_mhz(self):
+        v = ctypes.c_uint()
+        return v.value if self.lib.nvmlDeviceGetMaxClockInfo(self.h, self.SM, ctypes.byref(v)) == 0 else None
+
+    def reasons(self):
+        v = ctypes.c_ulonglong()
+        if self.reasons_fn(self.h, ctypes.byref(v)) != 0:
+            return set()
+        return {n for bit, n in self.REASONS.items() if v.value & bit}
+
+
 class ClockSampler:
-    """nvidia-smi clock / throttle samples while the timed region runs."""
+    """SM clock and throttle-reason samples while the timed region runs: NVML every
+    2 ms (read-only queries), else nvidia-smi every 200 ms."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_id: str | None):
-        self.gpu_id = gpu_id
+    def __init__(self, gpu_id: str | None, index: int = 0):
+        self.gpu_id, self.index = gpu_id, index
         self.proc = None
+        self.nvml = None
         self.lines = []
+        self.samples = []   # (sm MHz, reasons)
+        self.max_mhz = None
+        self.stop = threading.Event()
 
     def __enter__(self):
+        try:
+            self.nvml = _Nvml(self.gpu_id, self.index)
+            self.max_mhz = self.nvml.max_sm_mhz()
+            self.t = threading.Thread(target=self._poll, daemon=True)
+            self.t.start()
+            return self
+        except Exception:
+            self.nvml = None
         cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
         if self.gpu_id:
             cmd += ["-i", self.gpu_id]
@@ -98,11 +161,21 @@ class ClockSampler:
             self.proc = None
         return self
 
+    def _poll(self):
+        while not self.stop.is_set():
+            mhz = self.nvml.sm_mhz()
+            if mhz is not None:
+                self.samples.append((float(mhz), self.nvml.reasons()))
+            self.stop.wait(0.002)
+
     def _read(self):
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
     def __exit__(self, *exc):
+        self.stop.set()
+        if self.nvml is not None:
+            self.t.join(timeout=2)
         if self.proc:
             self.proc.terminate()
             try:
@@ -112,7 +185,10 @@ class ClockSampler:
             self.t.join(timeout=2)
 
     def summary(self):
-        sm, mx, reasons = [], None, set()
+        sm, mx, reasons = [], self.max_mhz, set()
+        for mhz, rs in self.samples:
+            sm.append(mhz)
+            reasons |= rs
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
             f = [x.strip() for x in ln.split(",")]
@@ -129,7 +205,7 @@ class ClockSampler:
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "source": "nvml" if self.samples else "nvidia-smi"}
 
 
 def _gpu_uuid(dev):
@@ -142,35 +218,110 @@ def _gpu_uuid(dev):
         return None
 
 
-def _profile_traffic():
-    """(DRAM bytes per token-head per step, launches per step) of the chunked kernels from the
-    committed ncu summary of the current kernels, if any."""
-    path = os.path.join(ROOT, "profiles", "chunked_kernels_traffic_B2H16T64K.md")
-    vals = {}
+def _traffic(workload_name: str):
+    """DRAM bytes per token-head of one step of this workload, from profiles/traffic.json
+    (written by `bench.py --traffic-from` out of an ncu capture), or None."""
     try:
-        with open(path) as f:
-            for ln in f:
-                if "=" in ln and ln.split("=")[0].strip() in ("dram_bytes_per_token_head_per_step",
-                                                             "chunked_launches_per_step"):
-                    k, v = ln.split("=")
-                    vals[k.strip()] = float(v)
-    except OSError:
+        with open(TRAFFIC_JSON) as f:
+            t = json.load(f)
+        return t["workloads"][workload_name]
+    except (OSError, KeyError, ValueError):
         return None
-    if len(vals) != 2:
-        return None
-    return vals["dram_bytes_per_token_head_per_step"], vals["chunked_launches_per_step"]
 
 
-# ---------------------------------------------------------------------------------- reference arm
+def traffic_from_ncu(csv_path: str, workload_name: str, units: float, note: str) -> dict:
+    """Sum dram__bytes_read.sum + dram__bytes_write.sum over every captured launch of an
+    `ncu --csv --metrics dram__bytes_read.sum,dram__bytes_write.sum` capture of whole steps,
+    divide by the token-heads the captured steps processed (`units`) and store the result
+    under the workload's name in profiles/traffic.json."""
+    import csv
+    per_kernel = {}
+    with open(csv_path) as f:
+        rows = [r for r in csv.reader(ln for ln in f if not ln.startswith("=="))]
+    head = rows[0]
+    ik, im, iv, iu = head.index("Kernel Name"), head.index("Metric Name"), head.index("Metric Value"), \
+        head.index("Metric Unit")
+    scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "KB": 1e3, "MB": 1e6, "GB": 1e9}
+    for r in rows[1:]:
+        if len(r) <= max(ik, im, iv, iu) or r[im] not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            continue
+        name = r[ik].split("(")[0].split("<")[0].split("::")[-1].strip()
+        v = float(r[iv].replace(",", "")) * scale.get(r[iu], 1)
+        per_kernel[name] = per_kernel.get(name, 0.0) + v
+    total = sum(per_kernel.values())
+    try:
+        with open(TRAFFIC_JSON) as f:
+            doc = json.load(f)
+    except (OSError, ValueError):
+        doc = {}
+    doc.setdefault("workloads", {})[workload_name] = {
+        "dram_bytes_per_token_head_per_step": total / units,
+        "per_kernel": {k: v / units for k, v in sorted(per_kernel.items())},
+        "note": note}
+    with open(TRAFFIC_JSON, "w") as f:
+        json.dump(doc, f, indent=1)
+    return doc["workloads"][workload_name]
+
+
+# ---------------------------------------------------------------------------------- workloads
+def passes(cfg) -> str:
+    return cfg["passes"]
+
+
+def step_units(cfg):
+    """(algorithmic FLOP, algorithmic bytes) per token-head of one step of the workload."""
+    gated = cfg.get("gates") is not None
+    p = passes(cfg)
+    if p == "fwd":
+        return FLOP_FWD, BYTES_FWD
+    if p == "segments":
+        return FLOP_FWD, BYTES_SEGMENTS
+    # gates add a 4-byte log-gate read to each pass and the 4-byte gate gradient written
+    return FLOP_FWD + FLOP_BWD, BYTES_FWD + BYTES_BWD + (12 if gated else 0)
+
+
+def step_name(cfg) -> str:
+    p = passes(cfg)
+    if p == "fwd":
+        return "linattn_fwd"
+    if p == "segments":
+        return "linattn_chunk_states -> linattn_state_scan -> linattn_fwd(init) over 64 segments"
+    if cfg.get("gates") is not None:
+        return "linattn_fwd_gated + linattn_bwd_gated"
+    return "linattn_fwd_ckpt + linattn_bwd_ckpt"
+
+
 def workload_config(cfg, ws_n):
     """The `config` object of the JSON line, the same for both arms."""
     from chunked_state_scan_causal_gb300 import inputs
     lam = inputs.workload_decay(cfg)
     gated = cfg.get("gates") is not None
-    return {"workload": cfg["name"], "B": cfg["B"], "H": cfg["H"], "T": cfg["T"], "d": cfg["d"], "chunk": 64,
-            "decay": "per-head" if lam is not None else ("per-token gates" if gated else "none"),
-            "l2": "inputs 512 MiB per tensor > L2 (no flush)",
-            "step": "linattn_fwd_ckpt + linattn_bwd_ckpt", "parallelism": f"replicas x{ws_n}"}
+    c = {"workload": cfg["name"], "B": cfg["B"], "H": cfg["H"], "T": cfg["T"], "d": cfg["d"], "chunk": 64,
+         "block": BLOCK,
+         "decay": "per-head" if lam is not None else ("per-token gates" if gated else "none"),
+         "l2": f"inputs {cfg['B'] * cfg['H'] * cfg['T'] * cfg['d'] * 2 >> 20} MiB per tensor > L2 (no flush)",
+         "step": step_name(cfg), "parallelism": f"replicas x{ws_n}"}
+    if passes(cfg) == "segments":
+        c["segments"] = cfg["T"] // cfg["seg_len"]
+        c["seg_len"] = cfg["seg_len"]
+    return c
+
+
+# ---------------------------------------------------------------------------------- reference arm
+def _oracle_step(oracle, cfg, xs, lam_s, gates):
+    p = passes(cfg)
+    if gates is not None:
+        oracle.fwd_gated(*xs[:3], gates)
+        oracle.bwd_gated(*xs, gates)
+    elif p in ("fwd", "segments"):
+        oracle.fwd_recurrent(*xs[:3], lam=lam_s)
+    else:
+        oracle.fwd_recurrent(*xs[:3], lam=lam_s)
+        oracle.bwd_recurrent(*xs, lam=lam_s)
+
+
+def _oracle_label(cfg):
+    return "fwd fp64 recurrence" if passes(cfg) in ("fwd", "segments") else "fwd+bwd fp64 recurrence"
 
 
 def run_reference(args):
@@ -186,28 +337,26 @@ def run_reference(args):
     heads = list(range(min(cfg["H"], args.ref_heads)))
     lam = inputs.workload_decay(cfg)
     lam_s = None if lam is None else lam[heads]
-    x = {w: np.stack([inputs.make_head64(cfg, w, 0, h) for h in heads])[None] for w in ("q", "k", "v", "dO")}
+    # at most the first 2^18 tokens of every sampled head are drawn (bounded host memory)
+    T_max = min(T, 1 << 18)
+    x = {w: np.stack([inputs.make_head64(cfg, w, 0, h, T=T_max) for h in heads])[None]
+         for w in ("q", "k", "v", "dO")}
     gates = None
     if cfg.get("gates") is not None:
         gates = np.stack([inputs.gate_head(cfg, 0, h) for h in heads])[None].astype(np.float64)
 
     def run(n):
         xs = [x[w][:, :, :n] for w in ("q", "k", "v", "dO")]
-        if gates is not None:
-            oracle.fwd_gated(*xs[:3], gates[:, :, :n])
-            oracle.bwd_gated(*xs, gates[:, :, :n])
-            return
-        oracle.fwd_recurrent(*xs[:3], lam=lam_s)
-        oracle.bwd_recurrent(*xs, lam=lam_s)
+        _oracle_step(oracle, cfg, xs, lam_s, None if gates is None else gates[:, :, :n])
 
     # each step is the first T_s tokens of every sampled head, T_s sized so that the
     # whole run (warm-up + timed steps) takes about --ref-budget seconds
-    n_cal = min(T, 2048)
+    n_cal = min(T_max, 2048)
     t0 = time.perf_counter()
     run(n_cal)
     per_token = (time.perf_counter() - t0) / n_cal
     T_s = int(args.ref_budget / (args.warmup + args.steps) / per_token) // 64 * 64
-    T_s = max(64, min(T, T_s))
+    T_s = max(64, min(T_max, T_s))
     times = []
     for i in range(args.warmup + args.steps):
         t0 = time.perf_counter()
@@ -218,7 +367,7 @@ def run_reference(args):
     tokens = T_s * len(heads) / cfg["H"]  # token equivalents of the full-head workload
     value = tokens / sec
     sample = (f"batch row 0, heads 0..{len(heads) - 1} of {cfg['H']}, first {T_s} of T={T} tokens: "
-              f"fwd+bwd fp64 recurrence")
+              f"{_oracle_label(cfg)}")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
@@ -232,6 +381,49 @@ def run_reference(args):
 
 
 # ---------------------------------------------------------------------------------- our arm
+def _cpu_baseline(cfg, args, lam):
+    """The oracle, as it stands, on a bounded sample of the workload (rank 0, N = 1)."""
+    import numpy as np
+    import oracle
+    from chunked_state_scan_causal_gb300 import inputs
+    oracle.build()
+    H, T = cfg["H"], cfg["T"]
+    heads = list(range(min(H, args.cpu_heads)))
+    T_s = min(T, args.cpu_tokens)
+    xs = {w: np.stack([inputs.make_head64(cfg, w, 0, h, T=T_s) for h in heads])[None]
+          for w in ("q", "k", "v", "dO")}
+    lam_s = None if lam is None else lam[heads]
+    gs = None
+    if cfg.get("gates") is not None:
+        gs = np.stack([inputs.gate_head(cfg, 0, h, T=T_s) for h in heads])[None].astype(np.float64)
+    t0 = time.perf_counter()
+    _oracle_step(oracle, cfg, [xs[w] for w in ("q", "k", "v", "dO")], lam_s, gs)
+    sec = time.perf_counter() - t0
+    extra = "" if T_s == T else f", first {T_s} of T={T} tokens (extrapolated linearly in tokens)"
+    return {"value": T_s * len(heads) / H / sec, "unit": "tokens/s", "cores": oracle.threads_used(),
+            "kind": "oracle",
+            "sample": f"batch row 0, heads 0..{len(heads) - 1} of {H}{extra}, {_oracle_label(cfg)}, {sec:.1f} s"}
+
+
+def _link_rates(dev, nbytes=1 << 29):
+    """Host<->device copy rates (GB/s) of one pinned buffer, measured with CUDA events."""
+    import torch
+    h = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    rates = {}
+    for name, (dst, src) in (("h2d_gbs", (d, h)), ("d2h_gbs", (h, d))):
+        dst.copy_(src, non_blocking=True)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(3):
+            dst.copy_(src, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        rates[name] = 3 * nbytes / (e0.elapsed_time(e1) * 1e-3) / 1e9
+    return rates
+
+
 def run_ours(args):
     import torch
     import chunked_state_scan_causal_gb300 as la
@@ -251,10 +443,14 @@ def run_ours(args):
         cfg["T"] = args.T
     B, H, T, d = cfg["B"], cfg["H"], cfg["T"], cfg["d"]
     lam = inputs.workload_decay(cfg)
+    mode = passes(cfg)
+    if mode not in ("fwd", "fwd+bwd", "segments"):
+        raise SystemExit(f"workload {args.workload} ({mode}) is a parity case, not a bench workload")
+    gated = cfg.get("gates") is not None
 
     # inputs: seeded on the host, pinned, copied once (the device-resident leg)
-    gated = cfg.get("gates") is not None
-    host = {w: inputs.make(cfg, w).pin_memory() for w in ("q", "k", "v", "dO")}
+    names = ("q", "k", "v", "dO") if mode == "fwd+bwd" else ("q", "k", "v")
+    host = {w: inputs.make(cfg, w).pin_memory() for w in names}
     if gated:
         host["log_gate"] = inputs.make_gates(cfg).pin_memory()
     x = {w: t.to(dev, non_blocking=True) for w, t in host.items()}
@@ -262,26 +458,60 @@ def run_ours(args):
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream(dev)
 
+    if mode == "segments":
+        L = cfg["seg_len"]
+        S = T // L
+
+        def seg(t):  # [1, H, T, d] -> [S, H, L, d] view (segments as a batch, by strides)
+            return t[0].view(H, S, L, d).permute(1, 0, 2, 3)
+
     def buffers():
-        """Outputs, workspaces and the forward's checkpoint of one step."""
-        b = dict(o=torch.empty_like(x["q"]), g=[torch.empty_like(x["q"]) for _ in range(3)])
-        if gated:
-            b.update(wsf=la.workspace(x["q"], la.OP_FWD_GATED), wsb=la.workspace(x["q"], la.OP_BWD_GATED),
-                     ck=la.checkpoint_gated(x["q"]), dlg=torch.empty_like(x["log_gate"]))
+        """Outputs, workspaces and checkpoints of one step."""
+        b = dict(o=torch.empty_like(x["q"]))
+        if mode == "fwd+bwd":
+            b["g"] = [torch.empty_like(x["q"]) for _ in range(3)]
+            if gated:
+                b.update(wsf=la.workspace(x["q"], la.OP_FWD_GATED), wsb=la.workspace(x["q"], la.OP_BWD_GATED),
+                         ck=la.checkpoint_gated(x["q"]), dlg=torch.empty_like(x["log_gate"]))
+            else:
+                b.update(wsf=la.workspace(x["q"], la.OP_FWD, decay), wsb=la.workspace(x["q"], la.OP_BWD, decay),
+                         ck=la.checkpoint(x["q"], decay))
+        elif mode == "fwd":
+            b["wsf"] = la.workspace(x["q"], la.OP_FWD, decay)
         else:
-            b.update(wsf=la.workspace(x["q"], la.OP_FWD, decay), wsb=la.workspace(x["q"], la.OP_BWD, decay),
-                     ck=la.checkpoint(x["q"], decay))
+            qs = seg(x["q"])
+            b.update(U=torch.empty((S, 1, H, d, d), dtype=torch.float32, device=dev),
+                     init=torch.empty((S, H, d, d), dtype=torch.float32, device=dev),
+                     wsc=la.workspace(x["k"], la.OP_CHUNK_STATES, None, L),
+                     wsf=la.workspace(qs, la.OP_FWD))
+            st, n = la.linattn_state_scan_workspace_size(S, H, d, d)
+            b["wss"] = torch.empty(n, dtype=torch.uint8, device=dev)
         return b
 
     def layer(xs, b):
-        # a training step of the layer: forward keeping its group states, then backward
-        if gated:
+        if mode == "fwd+bwd" and gated:
             la.fwd_gated(xs["q"], xs["k"], xs["v"], xs["log_gate"], b["ck"], out=b["o"], ws=b["wsf"])
             la.bwd_gated(xs["q"], xs["k"], xs["v"], xs["dO"], xs["log_gate"], b["ck"], outs=b["g"], ws=b["wsb"],
                          dlg_out=b["dlg"])
-        else:
+        elif mode == "fwd+bwd":
+            # a training step of the layer: forward keeping its group states, then backward
             la.fwd(xs["q"], xs["k"], xs["v"], decay=decay, out=b["o"], ws=b["wsf"], ckpt=b["ck"])
             la.bwd(xs["q"], xs["k"], xs["v"], xs["dO"], decay=decay, outs=b["g"], ws=b["wsb"], ckpt=b["ck"])
+        elif mode == "fwd":
+            la.fwd(xs["q"], xs["k"], xs["v"], decay=decay, out=b["o"], ws=b["wsf"])
+        else:
+            la.chunk_states(xs["k"], xs["v"], L, out=b["U"], ws=b["wsc"])
+            la.state_scan(b["U"].view(S, H, d, d), out=b["init"], ws=b["wss"])
+            la.fwd(seg(xs["q"]), seg(xs["k"]), seg(xs["v"]), init_state=b["init"], out=seg(b["o"]), ws=b["wsf"])
+
+    def outputs_of(b):
+        outs = [b["o"]]
+        if mode == "fwd+bwd":
+            outs += b["g"] + ([b["dlg"]] if gated else [])
+        return outs
+
+    def status_ok(b):
+        return all(la.device_status(b[k]) == la.OK for k in ("wsf", "wsb", "wsc", "wss") if k in b)
 
     main_buf = buffers()
 
@@ -293,86 +523,99 @@ def run_ours(args):
             import torch.distributed as dist
             dist.barrier()
 
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    if la.device_status(main_buf["wsb"]) != la.OK or la.device_status(main_buf["wsf"]) != la.OK:
-        raise RuntimeError("device-side error during warm-up")
-
-    # ---- timed region (inputs are 512 MiB per tensor, 4x larger than L2: no flush needed)
-    la.linattn_timing_enable(True)
-    la.linattn_timing_collect()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(_gpu_uuid(dev)) as clk:
+    def timed(fn, n):
+        """ms per call of fn over n calls, CUDA events on the launching stream."""
         barrier()
         torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for _ in range(args.steps):
-            step()
+        for _ in range(n):
+            fn()
         e1.record(stream)
         torch.cuda.synchronize()
         barrier()
+        return e0.elapsed_time(e1) / n
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if not status_ok(main_buf):
+        raise RuntimeError("device-side error during warm-up")
+
+    # ---- timed region: per-kernel event timing off; inputs are larger than L2 (no flush)
+    la.linattn_timing_enable(False)
+    with ClockSampler(_gpu_uuid(dev), local) as clk:
+        ms_local = timed(step, args.steps)
+    ms = dist_max(ms_local, dev)
+    if not status_ok(main_buf):
+        raise RuntimeError("device-side error during the timed steps")
+
+    # ---- per-kernel breakdown: a separate pass with the library's event timing on
+    n_break = max(1, min(args.steps, 50))
+    la.linattn_timing_enable(True)
+    la.linattn_timing_collect()
+    timed(step, n_break)
     la.linattn_timing_enable(False)
     kernels = la.linattn_timing_collect()
-    ms = dist_max(e0.elapsed_time(e1) / args.steps, dev)
-    tokens_step = B * T * ws_n
-    value = whole_job_throughput(B * T, ms, ws_n)
-    flops = (FLOP_FWD + FLOP_BWD) * B * H * T
-    # gates add a 4-byte log-gate read to each pass and the 4-byte gate gradient written
-    bytes_ = (BYTES_FWD + BYTES_BWD + (12 if gated else 0)) * B * H * T
-    hbm, tf, peak_src = _peaks()
 
-    # ---- dominant kernels' roofline: the chunked tensor-core kernels (the forward-time
-    # chunked kernel for o and dq, the dual reverse-time kernel for dk and dv); achieved =
-    # their algorithmic bytes over their summed CUDA-event time on the launching stream
-    launches = sum(n for n, _ in kernels.values())
     tok_heads = B * H * T
-    main = {k: kernels[k] for k in CHUNKED_KINDS if k in kernels}
-    n_main = sum(n for n, _ in main.values())
-    ms_main = sum(t for _, t in main.values())
-    bytes_main = sum(KIND_BYTES_PER_TOKEN_HEAD[k] * tok_heads * n for k, (n, _) in main.items())
-    achieved = bytes_main / (ms_main * 1e-3) / 1e9 if n_main else None
-    traffic_tok = _profile_traffic()
-    roofline = {
-        "kernel": "chunked tensor-core kernels: " + ", ".join(f"{k} x{n // args.steps}" for k, (n, _) in main.items()),
-        "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-        "frac": (achieved / hbm) if achieved else None,
-        # measured for the benchmark workload with lambda = 1 (null for other workloads)
-        "traffic": (traffic_tok[0] * tok_heads / traffic_tok[1]) if (
-            traffic_tok and args.workload == 3 and not args.B and not args.T) else None,
-        "peak_source": f"{peak_src} hbm_gbs",
-        "launches_per_step": n_main / args.steps,
-        "share_of_step": ms_main / (ms * args.steps) if ms else None,
-    }
-    # token-heads per step that the aggregate launches cover: the forward's, plus
-    # the backward's for the heads whose dq pass does not accumulate them itself
-    # (gates, or a per-head decay below 0.8, where the chunked kernels switch
-    # to their weighted-operand form)
-    if gated:
-        agg_units = 2 * tok_heads
-    elif lam is not None:
-        agg_units = tok_heads * (1 + float((lam < 0.8).mean()))
-    else:
-        agg_units = tok_heads
+    flop_th, bytes_th = step_units(cfg)
+    flops, bytes_ = flop_th * tok_heads, bytes_th * tok_heads
+    hbm, tf, peak_src = _peaks()
+    value = whole_job_throughput(B * T, ms, ws_n)
+    launches = sum(n for n, _ in kernels.values())
     breakdown = {}
     for k, (n, t) in kernels.items():
-        e = {"launches_per_step": n / args.steps, "ms_per_step": t / args.steps}
-        if k in KIND_BYTES_PER_TOKEN_HEAD and t > 0:
-            units = agg_units * args.steps if k == "tc_segment_aggregate" else tok_heads * n
-            e["algorithmic_gbs"] = KIND_BYTES_PER_TOKEN_HEAD[k] * units / (t * 1e-3) / 1e9
+        e = {"launches_per_step": n / n_break, "ms_per_step": t / n_break}
+        if k in KIND_IO_BYTES_PER_TOKEN_HEAD and t > 0 and k != "tc_segment_aggregate":
+            # bytes the kernel's own sequence-tensor inputs and outputs take per token-head
+            e["io_bytes_per_token_head"] = KIND_IO_BYTES_PER_TOKEN_HEAD[k]
+            e["io_gbs"] = KIND_IO_BYTES_PER_TOKEN_HEAD[k] * tok_heads * n / (t * 1e-3) / 1e9
         breakdown[k] = e
+    ms_kernels = sum(t for _, t in kernels.values()) / n_break
+    traffic = _traffic(cfg["name"]) if not (args.B or args.T) else None
+    # The roofline unit is the whole step (every launch of the hot path): achieved =
+    # the step's algorithmic bytes / the step's device time; frac = achieved / peak.
+    roofline = {
+        "kernel": "whole step: " + ", ".join(f"{k} x{n / n_break:g}" for k, (n, _) in sorted(kernels.items())),
+        "bound": "hbm", "achieved": bytes_ / (ms * 1e-3) / 1e9, "peak": hbm, "unit": "GB/s",
+        "frac": bytes_ / (ms * 1e-3) / 1e9 / hbm,
+        "traffic": None if traffic is None else traffic["dram_bytes_per_token_head_per_step"] * tok_heads,
+        "algorithmic_bytes": bytes_,
+        "peak_source": f"{peak_src} hbm_gbs (of {peak_src})",
+        "kernel_time_share": ms_kernels / ms if ms else None,
+    }
+
+    # ---- single unsegmented forward of the segment workload (same sequence, same run)
+    single = None
+    if mode == "segments":
+        ob = torch.empty_like(x["q"])
+        wso = la.workspace(x["q"], la.OP_FWD)
+
+        def one():
+            la.fwd(x["q"], x["k"], x["v"], out=ob, ws=wso)
+
+        for _ in range(args.warmup):
+            one()
+        ms1 = dist_max(timed(one, args.steps), dev)
+        if la.device_status(wso) != la.OK:
+            raise RuntimeError("device-side error in the single forward")
+        single = {"ms_per_step": ms1, "tokens_per_s": whole_job_throughput(B * T, ms1, ws_n),
+                  "tflops": FLOP_FWD * tok_heads / (ms1 * 1e-3) / 1e12,
+                  "algorithmic_gbs": BYTES_FWD * tok_heads / (ms1 * 1e-3) / 1e9,
+                  "path_roofline_frac": BYTES_FWD * tok_heads / (ms1 * 1e-3) / 1e9 / hbm}
 
     # ---- end to end through the public API with host buffers: every step copies its
-    # inputs host->device from pinned memory and its results (o, dq, dk, dv) device->host.
-    # Steps are pipelined over two buffer sets on three streams (copy-in, compute,
-    # copy-out), so step i+1's inputs arrive while step i computes.
-    ms_e2e, h2d, d2h = None, 0, 0
+    # inputs host->device from pinned memory and its results device->host.  Steps are
+    # pipelined over two buffer sets on three streams (copy-in, compute, copy-out), so
+    # step i+1's inputs arrive while step i computes.
+    ms_e2e, h2d, d2h, link = None, 0, 0, None
     if not args.no_e2e:
         slots = []
         for _ in range(2):
             xin = {w: torch.empty_like(x[w]) for w in x}
             b = buffers()
-            outs = [b["o"]] + b["g"] + ([b["dlg"]] if gated else [])
+            outs = outputs_of(b)
             hout = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
             ev = {n: torch.cuda.Event() for n in ("in", "comp", "out")}
             slots.append(dict(x=xin, b=b, o=outs, h=hout, ev=ev, used=False))
@@ -412,30 +655,13 @@ def run_ours(args):
         ev1.record(s_out)                                  # after the last copy-out, which waits for all else
         torch.cuda.synchronize()
         ms_e2e = dist_max(ev0.elapsed_time(ev1) / n_e2e, dev)
+        del slots
+        link = _link_rates(dev)
 
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only)
     cpu = None
     if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
-        import numpy as np
-        import oracle
-        oracle.build()
-        heads = list(range(min(H, args.cpu_heads)))
-        xs = {w: np.stack([inputs.make_head64(cfg, w, 0, h) for h in heads])[None]
-              for w in ("q", "k", "v", "dO")}
-        lam_s = None if lam is None else lam[heads]
-        t0 = time.perf_counter()
-        if gated:
-            gs = np.stack([inputs.gate_head(cfg, 0, h) for h in heads])[None].astype(np.float64)
-            oracle.fwd_gated(xs["q"], xs["k"], xs["v"], gs)
-            oracle.bwd_gated(xs["q"], xs["k"], xs["v"], xs["dO"], gs)
-        else:
-            oracle.fwd_recurrent(xs["q"], xs["k"], xs["v"], lam=lam_s)
-            oracle.bwd_recurrent(xs["q"], xs["k"], xs["v"], xs["dO"], lam=lam_s)
-        sec = time.perf_counter() - t0
-        cpu = {"value": T * len(heads) / H / sec, "unit": "tokens/s", "cores": oracle.threads_used(),
-               "kind": "oracle",
-               "sample": f"batch row 0, heads 0..{len(heads) - 1} of {H}, T={T}, fwd+bwd fp64 recurrence, "
-                         f"{sec:.1f} s"}
+        cpu = _cpu_baseline(cfg, args, lam)
 
     if rank == 0:
         line = {
@@ -448,13 +674,18 @@ def run_ours(args):
             "path_roofline_frac": max(flops / (tf * 1e12), bytes_ / (hbm * 1e9)) / (ms * 1e-3),
             "roofline": roofline,
             "kernels": breakdown,
-            "gpu_launches": launches,
+            "gpu_launches": launches * args.steps // n_break,
             "clocks": clk.summary(),
             "e2e": None if ms_e2e is None else {
                 "value": whole_job_throughput(B * T, ms_e2e, ws_n), "unit": "tokens/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e,
+                "link": link,
+                # the host link alone, both directions overlapped at their one-way rates
+                "link_min_ms": max(h2d / (link["h2d_gbs"] * 1e9), d2h / (link["d2h_gbs"] * 1e9)) * 1e3},
             "cpu_baseline": cpu,
         }
+        if single is not None:
+            line["single_fwd"] = single
         print(json.dumps(line), flush=True)
     if ws_n > 1:
         import torch.distributed as dist
@@ -584,6 +815,7 @@ def main():
     ap.add_argument("--ref-heads", type=int, default=16, help="heads per step of the reference arm")
     ap.add_argument("--ref-budget", type=float, default=120.0, help="seconds for the whole reference arm")
     ap.add_argument("--cpu-heads", type=int, default=16, help="heads of the cpu_baseline sample")
+    ap.add_argument("--cpu-tokens", type=int, default=1 << 17, help="tokens per head of the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--B", type=int, default=0, help="override the batch size (profiling cases)")
@@ -591,10 +823,20 @@ def main():
     ap.add_argument("--decode", action="store_true", help="measure the recurrent decode instead")
     ap.add_argument("--decode-batch", type=int, default=512, help="sequences per head for --decode")
     ap.add_argument("--sp", type=int, default=0, help="measure the sequence split with this many thread ranks")
+    ap.add_argument("--traffic-from", default="", help="ncu CSV of whole steps (dram__bytes_read/write.sum): "
+                    "store DRAM bytes per token-head in profiles/traffic.json and exit")
+    ap.add_argument("--traffic-steps", type=int, default=1, help="steps the --traffic-from capture covers")
+    ap.add_argument("--traffic-note", default="", help="how the --traffic-from capture was taken")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.decode:
+    if args.traffic_from:
+        from chunked_state_scan_causal_gb300 import inputs
+        cfg = dict(inputs.WORKLOADS[args.workload])
+        B, T = args.B or cfg["B"], args.T or cfg["T"]
+        units = B * cfg["H"] * T * args.traffic_steps
+        print(json.dumps(traffic_from_ncu(args.traffic_from, cfg["name"], units, args.traffic_note)))
+    elif args.decode:
         run_decode(args)
     elif args.sp:
         run_sp(args)

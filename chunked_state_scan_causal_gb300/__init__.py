@@ -73,11 +73,14 @@ _SIGS = {
     "linattn_device_status": ([_vp, _vp], _i32),
     "linattn_state_scan_noalloc": ([_i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp], _i32),
     "linattn_diag_mma": ([_i32, _vp, _vp, _vp, _vp], _i32),
+    "linattn_segment_decay": ([_vp, _i32, _i32, _i32, _vp, _vp], _i32),
+    "linattn_diag_scan_withhold": ([_i32, _i32, _i32, _i32, _vp, _vp, _i32, ctypes.c_double, _vp, _sz, _vp],
+                                   _i32),
     "linattn_timing_enable": ([_i32], _i32),
     "linattn_timing_collect": ([_i32, ctypes.POINTER(_i32), ctypes.POINTER(ctypes.c_float)], _i32),
     "linattn_kernel_name": ([_i32], ctypes.c_char_p),
 }
-KERNEL_KINDS = 11
+KERNEL_KINDS = 13
 
 
 def lib():
@@ -182,6 +185,16 @@ def linattn_state_scan_noalloc(G, BH, dk, dv, seg_decay, local, init, out, total
 
 def linattn_device_status(ws, stream) -> int:
     return lib().linattn_device_status(ws, stream)
+
+
+def linattn_segment_decay(decay, B, H, seg_len, out, stream) -> int:
+    return lib().linattn_segment_decay(decay, B, H, seg_len, out, stream)
+
+
+def linattn_diag_scan_withhold(G, BH, dk, dv, local, out, withhold_tile, wait_limit_ms, ws, ws_bytes,
+                               stream) -> int:
+    return lib().linattn_diag_scan_withhold(G, BH, dk, dv, local, out, withhold_tile, wait_limit_ms, ws,
+                                            ws_bytes, stream)
 
 
 def linattn_diag_mma(mode, A, B, D, stream) -> int:
@@ -432,6 +445,18 @@ def state_scan(local, seg_decay=None, init=None, want_total=False, out=None, ws=
                             _ptr(ws), ws.numel(), _stream(local.device, stream))
     _check(st, "linattn_state_scan")
     return out, total
+
+
+def segment_decay(decay, B: int, seg_len: int, out=None, stream=None):
+    """Per-(b, h) scan multiplier decay[h]^seg_len, [B*H] fp32 (None for decay None)."""
+    import torch
+    if decay is None:
+        return None
+    H = decay.numel()
+    out = out if out is not None else torch.empty(B * H, dtype=torch.float32, device=decay.device)
+    st = linattn_segment_decay(_ptr(decay), B, H, seg_len, _ptr(out), _stream(decay.device, stream))
+    _check(st, "linattn_segment_decay")
+    return out
 
 
 def device_status(ws, stream=None) -> int:

@@ -57,7 +57,7 @@ int device_ok();
 // ---------------------------------------------------------------- per-kernel timing (api.cu)
 enum KernelKind {
   K_SIMT_FWD = 0, K_SIMT_BWD, K_SIMT_SEGMENT, K_SCAN, K_TC_AGG, K_TC_MAIN_FWD, K_DIAG,
-  K_DECODE, K_TC_DUAL_REV, K_TC_MAIN_AGG, K_GATE, K_KINDS
+  K_DECODE, K_TC_DUAL_REV, K_TC_MAIN_AGG, K_GATE, K_TC_FUSED_FWD, K_TC_CHUNK_STATES, K_KINDS
 };
 // Records timing events around one launch on `s` while timing is enabled.
 struct TimedLaunch {
@@ -90,10 +90,19 @@ size_t scan_workspace_bytes(int G, int64_t E);
 // group_log2 (optional, [G][BH], G <= 256): log2 of every group's own multiplier,
 // replacing the uniform one (data-dependent gates).  With decay_h, groups from
 // index kb on (G <= 256) have seg_len2 tokens instead of seg_len (a GroupPlan).
+// limit_ns bounds every look-back wait (0: LINATTN_LOOKBACK_LIMIT_MS from the
+// environment, else 2 s); withhold >= 0 (diagnostics) forces the look-back form
+// and keeps that tile from ever publishing, so its successors' waits give up.
 cudaError_t state_scan(int G, int BH, int DD, const float *seg_decay, const float *decay_h, int H,
                        int seg_len, bool reverse, const float *local, const float *init, float *out,
                        float *total, void *ws, int *status, cudaStream_t s, const float *group_log2 = nullptr,
-                       int kb = 1 << 30, int seg_len2 = 0);
+                       int kb = 1 << 30, int seg_len2 = 0, uint64_t limit_ns = 0, int withhold = -1);
+// Bound of the device-side waits on other CTAs' results (look-back, chained
+// group states): LINATTN_LOOKBACK_LIMIT_MS from the environment, else 2 s.
+uint64_t wait_limit_ns();
+
+// out[b * H + h] = decay_h[h]^len for b < B (the scan multiplier of a segment of len tokens).
+cudaError_t segment_decay(const float *decay_h, int B, int H, int len, float *out, cudaStream_t s);
 
 // w[i] += lambda_h^len d[i] over n = BH * DD elements (h = (i / DD) % H; lambda = 1
 // without decay_h): folds a state entering across a segment of len tokens into
@@ -142,9 +151,27 @@ cudaError_t tc_segment_states(const Problem &p, const GroupPlan &gp, const void 
 // same pass, w_s = lambda^{s - start + 1} (1 without a decay), for the groups
 // of heads whose decay takes the weighted form (lambda >= 0.8, or none); the
 // other groups are left to tc_segment_states.
+// ginit_len > 0: group_init holds one state per ginit_len tokens (a checkpoint of
+// the fused forward's plan); group g starts from entry start(g) / ginit_len.
 cudaError_t tc_main(const Problem &p, const GroupPlan &gp, const void *q, const void *k, const void *v, void *o,
                     const float *group_init, bool init_transposed, float *final_state, int *status,
-                    cudaStream_t s, const void *x = nullptr, float *agg_out = nullptr);
+                    cudaStream_t s, const void *x = nullptr, float *agg_out = nullptr, int ginit_len = 0);
+
+// The groups of the fused forward (uniform, at most 1024 tokens, any count) and
+// the coarser groups of a pass that reads its checkpoint (lengths multiples of
+// `unit`, at most 256 groups).
+GroupPlan tc_fused_plan(const Problem &p);
+GroupPlan tc_coarse_plan(const Problem &p, int unit);
+
+// lambda = 1 forward in one launch: every group's k, v aggregate (pass 1), the
+// group states found by a decoupled look-back across the groups of a sequence
+// (`states` [G][BH][d][d] written: entry 0 = init or zeros, entry g + 1 = the
+// state after group g; `agg` [G][BH][d][d] the aggregates a group publishes
+// when its predecessor is not ready; `chain` [G][BH] flags, cleared here), then
+// the chunked pass from each group's entering state; final_state (optional).
+cudaError_t tc_fused_fwd(const Problem &p, const GroupPlan &gp, const void *q, const void *k, const void *v,
+                         void *o, const float *init, float *states, float *agg, unsigned *chain, float *final_state,
+                         int *status, cudaStream_t s);
 
 // The backward's dv and dk in one reverse-time pass over (k, q, dO, v) from the
 // reverse group states [G][BH][d][d] (sum over later tokens u of

@@ -22,6 +22,7 @@
 // 512-byte piece (the segment-per-lane tiles above touch 32 scattered sectors
 // per warp access, which DRAM serves far less efficiently).  The look-back
 // form remains for long scans, where it supplies the parallelism.
+#include <cstdlib>
 #include <mutex>
 
 #include "../../include/linattn.h"
@@ -48,6 +49,8 @@ struct ScanArgs {
   unsigned *flags;    // [ntg * ncg] 0 empty, 1 aggregate, 2 inclusive (zeroed before launch)
   float *agg, *incl;  // [ntg * ncg][kVec]
   int *status;
+  uint64_t limit_ns;  // bound of every look-back wait
+  int withhold;       // diagnostics: this tile never publishes (-1: none)
 };
 
 constexpr unsigned kBatch = 16;  // tickets taken per atomic (look-back case)
@@ -117,7 +120,7 @@ __global__ void __launch_bounds__(kWarps * 32) scan_kernel(ScanArgs A) {
       for (int i = 0; i < kVec; ++i) pin[i] = A.init ? __ldg(A.init + e0 + i) : 0.f;
     } else {
       // publish the aggregate, then look back
-      if (lane == 31) {
+      if (lane == 31 && ticket != (unsigned)A.withhold) {
         float4 *dst = reinterpret_cast<float4 *>(A.agg + (int64_t)ticket * kVec);
         dst[0] = make_float4(x[0], x[1], x[2], x[3]);
         dst[1] = make_float4(x[4], x[5], x[6], x[7]);
@@ -137,7 +140,7 @@ __global__ void __launch_bounds__(kWarps * 32) scan_kernel(ScanArgs A) {
           if (f == 0) {
             const uint64_t t0 = globaltimer_ns();
             while ((f = ld_acquire_gpu(A.flags + pt)) == 0) {
-              if (globaltimer_ns() - t0 > kWaitLimitNs) {
+              if (globaltimer_ns() - t0 > A.limit_ns) {
                 report_error(A.status, -6);
                 f = 3;  // give up: treat as an inclusive prefix of zeros
                 break;
@@ -163,7 +166,7 @@ __global__ void __launch_bounds__(kWarps * 32) scan_kernel(ScanArgs A) {
       }
     }
     // publish the inclusive prefix of this tile
-    if (tg + 1 < A.ntg && lane == 31) {
+    if (tg + 1 < A.ntg && lane == 31 && ticket != (unsigned)A.withhold) {
       float4 *dst = reinterpret_cast<float4 *>(A.incl + (int64_t)ticket * kVec);
       float v[kVec];
 #pragma unroll
@@ -264,6 +267,19 @@ __global__ void fold_kernel(float *w, const float *d, const float *decay_h, int 
 }
 }  // namespace
 
+namespace {
+__global__ void seg_decay_kernel(const float *decay_h, int H, int n, int len, float *out) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
+    out[i] = pow_len(decay_h[i % H], len);
+}
+}  // namespace
+
+cudaError_t segment_decay(const float *decay_h, int B, int H, int len, float *out, cudaStream_t s) {
+  const int n = B * H;
+  seg_decay_kernel<<<(n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024, 256, 0, s>>>(decay_h, H, n, len, out);
+  return cudaGetLastError();
+}
+
 cudaError_t fold_state(float *w, const float *d, const float *decay_h, int H, int DD, int len, int64_t n,
                        cudaStream_t s) {
   const int64_t want = (n + 255) / 256;
@@ -272,10 +288,19 @@ cudaError_t fold_state(float *w, const float *d, const float *decay_h, int H, in
   return cudaGetLastError();
 }
 
+uint64_t wait_limit_ns() {
+  const char *e = getenv("LINATTN_LOOKBACK_LIMIT_MS");
+  if (e && *e) {
+    const double ms = strtod(e, nullptr);
+    if (ms > 0 && ms < 6e4) return (uint64_t)(ms * 1e6);
+  }
+  return kWaitLimitNs;
+}
+
 cudaError_t state_scan(int G, int BH, int DD, const float *seg_decay, const float *decay_h, int H,
                        int seg_len, bool reverse, const float *local, const float *init, float *out,
                        float *total, void *ws, int *status, cudaStream_t s, const float *group_log2, int kb,
-                       int seg_len2) {
+                       int seg_len2, uint64_t limit_ns, int withhold) {
   const int64_t E = (int64_t)BH * DD;
   if ((group_log2 || kb < G) && G > kColumnMaxG) return cudaErrorInvalidValue;
   ScanArgs A;
@@ -286,10 +311,12 @@ cudaError_t state_scan(int G, int BH, int DD, const float *seg_decay, const floa
   A.reverse = reverse ? 1 : 0;
   A.seg_decay = seg_decay; A.decay_h = decay_h; A.local = local; A.init = init; A.glog2 = group_log2;
   A.out = out; A.total = total; A.status = status;
+  A.limit_ns = limit_ns ? limit_ns : wait_limit_ns();
+  A.withhold = withhold;
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (G <= kColumnMaxG) {
+  if (G <= kColumnMaxG && withhold < 0) {
     const int64_t n4 = E / 4, want = (n4 + 255) / 256, cap = (int64_t)sms * 8;
     TimedLaunch t(K_SCAN, s);
     scan_columns_kernel<<<(int)(want < cap ? want : cap), 256, 0, s>>>(A);
@@ -360,10 +387,13 @@ extern "C" int32_t linattn_state_scan_noalloc(int32_t G, int32_t BH, int32_t dk,
   if (DD % kVec) return LINATTN_ERR_UNSUPPORTED;
   if (!local_states || !init_states) return LINATTN_ERR_INVALID;
   for (const void *x : {(const void *)seg_decay, (const void *)local_states, (const void *)init,
-                        (const void *)init_states, (const void *)total, (const void *)device_status})
+                        (const void *)init_states, (const void *)total})
     if (reinterpret_cast<uintptr_t>(x) & 15u) return LINATTN_ERR_ALIGN;
+  if (reinterpret_cast<uintptr_t>(device_status) & 3u) return LINATTN_ERR_ALIGN;
+  // Only the look-back form (more than kColumnMaxG segments) uses the scratch;
+  // the column-parallel form touches none of it, so it has no size limit here.
   const int64_t ntiles = (int64_t)((G + 31) / 32) * ((int64_t)BH * DD / kVec);
-  if (ntiles > LINATTN_NOALLOC_MAX_TILES) return LINATTN_ERR_SCRATCH_LIMIT;
+  if (G > kColumnMaxG && ntiles > LINATTN_NOALLOC_MAX_TILES) return LINATTN_ERR_SCRATCH_LIMIT;
   int st = device_ok();
   if (st != LINATTN_OK) return st;
   void *scratch = nullptr;

@@ -137,9 +137,7 @@ class KernelOps:
 
     def seg_decay(self, decay, B, seg_len):
         """Per-(b, h) multiplier lambda_h^seg_len for the scan, [B*H] fp32 (None for lambda = 1)."""
-        if decay is None:
-            return None
-        return decay.double().pow(seg_len).float().repeat(B).contiguous()
+        return self.la.segment_decay(decay, B, seg_len)
 
 
 @dataclass

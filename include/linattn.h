@@ -243,15 +243,19 @@ int32_t linattn_state_scan(int32_t G, int32_t BH, int32_t dk, int32_t dv, const 
  * loads the library holds until the process exits.  Nothing is allocated:
  * no cudaMalloc, cudaFree or allocating library routine is called.
  *   - Same operands and results as linattn_state_scan.
- *   - Limit: ceil(G/32) * (BH*dk*dv/8) <= LINATTN_NOALLOC_MAX_TILES (65536), e.g.
- *     64 segments of 16 states of 128x128; larger requests return
+ *   - Limit: up to 256 segments the scan runs column-parallel and uses none of
+ *     the scratch (no size limit beyond the operands); with more segments
+ *     ceil(G/32) * (BH*dk*dv/8) must be <= LINATTN_NOALLOC_MAX_TILES (65536),
+ *     e.g. 1024 segments of one 128x128 state (32 x 2048 tiles); larger requests return
  *     LINATTN_ERR_SCRATCH_LIMIT before anything is enqueued.
- *   - device_status: optional device int32 (NULL allowed) that is zeroed and
- *     then receives LINATTN_ERR_DEVICE_TIMEOUT if a bounded look-back wait
- *     gives up; there is no workspace status word in this variant.
+ *   - device_status: optional device int32 (NULL allowed; 4-byte aligned) that
+ *     is zeroed and then receives LINATTN_ERR_DEVICE_TIMEOUT if a bounded
+ *     look-back wait gives up; there is no workspace status word in this variant.
  *   - The first call on a device looks up the scratch's device address once
- *     (cudaGetSymbolAddress, with that device current); make that first call
- *     before any stream capture.
+ *     (cudaGetSymbolAddress, with that device current) and keeps it for the
+ *     life of the process; make that first call before any stream capture.  A
+ *     reset of the device's context (cudaDeviceReset) makes the kept address
+ *     stale: do not call this entry point again in that process after one.
  *   - Every call uses the same scratch and leaves the last call's contents in
  *     it; the call clears what must start at zero (counter, flags) on
  *     `stream`.  Calls that overlap on the GPU (other streams, other host
@@ -261,6 +265,14 @@ int32_t linattn_state_scan(int32_t G, int32_t BH, int32_t dk, int32_t dv, const 
 int32_t linattn_state_scan_noalloc(int32_t G, int32_t BH, int32_t dk, int32_t dv, const float *seg_decay,
                                    const float *local_states, const float *init, float *init_states,
                                    float *total, int32_t *device_status, void *stream);
+
+/* Scan multipliers of segments of seg_len tokens: out[b*H + h] = decay[h]^seg_len
+ * for b < B (the seg_decay operand of linattn_state_scan for a sequence split into
+ * segments of seg_len tokens; ZeCO page, abstract: All-Scan over the ranks'
+ * segments).  decay [H] and out [B*H] are device fp32, 16-byte aligned;
+ * seg_len >= 0 (0 gives 1).  Returns a status. */
+int32_t linattn_segment_decay(const float *decay, int32_t B, int32_t H, int32_t seg_len, float *out,
+                              void *stream);
 
 /* Synchronises `stream`, then returns the device status word of `workspace`
  * (LINATTN_OK, or e.g. LINATTN_ERR_DEVICE_TIMEOUT) or LINATTN_ERR_CUDA. */
@@ -274,11 +286,29 @@ int32_t linattn_device_status(const void *workspace, void *stream);
  * for every kernel kind k < max_kinds its launch count and summed device time
  * (ms), clears the record and returns the number of kinds
  * (LINATTN_KERNEL_KINDS), or a negative status. */
-#define LINATTN_KERNEL_KINDS 11
+#define LINATTN_KERNEL_KINDS 13
 int32_t linattn_timing_enable(int32_t on);
 int32_t linattn_timing_collect(int32_t max_kinds, int32_t *launches, float *total_ms);
 /* Name of kernel kind k (static string; "?" when out of range). */
 const char *linattn_kernel_name(int32_t kind);
+
+/* Bounded device waits.  Every device-side wait on another CTA's result (the
+ * scan's look-back, the chained group states of the forward) gives up after
+ * LINATTN_LOOKBACK_LIMIT_MS milliseconds (environment variable, read at every
+ * call; default 2000), records LINATTN_ERR_DEVICE_TIMEOUT in the status word
+ * and lets the kernel finish instead of hanging.
+ *
+ * Diagnostic for that path (not part of the method): linattn_state_scan in its
+ * look-back form, except that look-back tile `withhold_tile` (tile index =
+ * segment tile * (BH*dk*dv/8) + element group) never publishes its aggregate
+ * or prefix, so every successor that looks back to it waits wait_limit_ms
+ * (0 < wait_limit_ms <= 2000), gives up and reports LINATTN_ERR_DEVICE_TIMEOUT
+ * in the workspace status word (read it with linattn_device_status).  The
+ * outputs past the withheld tile are then wrong by design.  Workspace as for
+ * linattn_state_scan.  Returns a status. */
+int32_t linattn_diag_scan_withhold(int32_t G, int32_t BH, int32_t dk, int32_t dv, const float *local_states,
+                                   float *init_states, int32_t withhold_tile, double wait_limit_ms,
+                                   void *workspace, size_t workspace_bytes, void *stream);
 
 /* Diagnostic (not part of the method): one 128x128x128 bf16 tensor-core
  * product through the same shared-memory layouts the kernels use, written as

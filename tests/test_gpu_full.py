@@ -88,6 +88,28 @@ def test_forward_backward_full_size(wl):
             assert rel(got[b, h], r[0, i]) < 1e-2, (name, b, h)
 
 
+def test_workload3_other_distribution_reading_full_size():
+    """The fwd+bwd workload at full size (B2 H16 T65536) with the other reading of its
+    input distribution: q, k, v ~ N(0, 1)/sqrt(128) with unit-norm key rows (the
+    distribution of the forward-only workload), dO ~ N(0, 1); the benchmark's
+    checkpointed step; heads from both ends of the item order against the oracle."""
+    cfg = dict(inputs.WORKLOADS[3], dist="unit_k", sigma=1.0 / np.sqrt(128), name="fwdbwd-B2H16T64K-unitk")
+    x = load(cfg, ("q", "k", "v", "dO"))
+    ck = la.checkpoint(x["q"])
+    o, fin, _ = fwd_checked(x["q"], x["k"], x["v"], ckpt=ck, want_final=True)
+    dq, dk, dv, dinit = bwd_checked(x["q"], x["k"], x["v"], x["dO"], want_dinit=True, ckpt=ck)
+    torch.cuda.synchronize()
+    H = cfg["H"]
+    pairs = [(0, 0), (cfg["B"] - 1, H - 1), (1, 5)]
+    ref = heads64(cfg, pairs, ("q", "k", "v", "dO"))
+    ro, _, rfin = oracle.fwd_recurrent(ref["q"], ref["k"], ref["v"])
+    rq, rk, rv, rinit = oracle.bwd_recurrent(ref["q"], ref["k"], ref["v"], ref["dO"])
+    for i, (b, h) in enumerate(pairs):
+        for name, got, r in (("o", o, ro), ("final", fin, rfin), ("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv),
+                             ("dinit", dinit, rinit)):
+            assert rel(got[b, h], r[0, i]) < 1e-2, (name, b, h)
+
+
 def test_workload5_segmented_equals_single_and_oracle():
     """64 segments x 16384: segment states -> exclusive scan -> per-segment forward == one forward."""
     cfg = inputs.WORKLOADS[5]

@@ -125,6 +125,26 @@ def test_config1_fp32_forward_and_chunk_states():
     assert float(cs[:, :, 0].abs().max()) == 0.0  # exclusive: chunk 0 enters with the zero state
 
 
+@pytest.mark.parametrize("d", [128, 64])
+@pytest.mark.parametrize("T", [64, 1000, 4096 + 64 + 40])
+@pytest.mark.parametrize("dk", [None, 0.5, "cfg"])
+def test_forward_chunk_states_bf16(d, T, dk):
+    """bf16 inputs with the per-chunk (C = 64) exclusive states requested: the
+    states entering every chunk, the outputs and the final state against the
+    oracle's definition form (ragged last chunk included)."""
+    B, H = 2, 3
+    c, dev = case(31 + T, B, H, T, d, torch.bfloat16, sigma=1 / np.sqrt(128))
+    lam = decays(H, dk)
+    init = (np.random.default_rng(T + 5).standard_normal((B, H, d, d)) * 0.1).astype(np.float32).astype(np.float64)
+    o, fin, cs = run_fwd(c, dev, torch.bfloat16, lam, init, want_cs=True)
+    ro, rcs, rfin = oracle.fwd_recurrent(c["q"], c["k"], c["v"], lam=lam, init=init, chunk=64)
+    assert cs.shape == (B, H, (T + 63) // 64, d, d)
+    assert rel(cs, rcs) < 1e-2
+    assert rel(o, ro) < 1e-2
+    assert rel(fin, rfin) < 1e-2
+    assert rel(cs[:, :, 0], init) < 1e-6   # exclusive: chunk 0 enters with the initial state
+
+
 @pytest.mark.parametrize("dtype,d", [(torch.bfloat16, 128), (torch.bfloat16, 64), (torch.float32, 128),
                                      (torch.float32, 64)])
 @pytest.mark.parametrize("T", [64, 200, 1000, 2048])
@@ -150,6 +170,31 @@ def test_forward_many_groups_bf16():
         ro, _, rfin = oracle.fwd_recurrent(c["q"], c["k"], c["v"], lam=lam)
         assert rel(o, ro) < 1e-2
         assert rel(fin, rfin) < 1e-2
+
+
+def test_fused_forward_chained_groups_more_items_than_sms():
+    """lambda = 1: the one-launch forward chains the group states through global
+    memory (each group waits for its predecessor's published state).  More
+    (group, sequence) items than SMs (B2 H16, 9 groups per sequence), a ragged
+    last group, an initial state; the checkpoint it writes feeds the backward."""
+    B, H, T, d = 2, 16, 8192 + 200, 128
+    c, dev = case(43, B, H, T, d, torch.bfloat16, sigma=1 / np.sqrt(128))
+    init = (np.random.default_rng(44).standard_normal((B, H, d, d)) * 0.1).astype(np.float32)
+    init_d = torch.from_numpy(init).cuda()
+    ck = la.checkpoint(dev["q"])
+    wsf, wsb = la.workspace(dev["q"], la.OP_FWD), la.workspace(dev["q"], la.OP_BWD)
+    o, fin, _ = la.fwd(dev["q"], dev["k"], dev["v"], init_state=init_d, want_final=True, ws=wsf, ckpt=ck)
+    dq, dk_, dv, dinit = la.bwd(dev["q"], dev["k"], dev["v"], dev["dO"], want_dinit=True, ws=wsb, ckpt=ck,
+                                init_state=init_d)
+    assert la.device_status(wsf) == la.OK and la.device_status(wsb) == la.OK
+    for b, h in ((0, 0), (0, 7), (1, 8), (1, 15)):
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        i64 = init[sl].astype(np.float64)
+        ro, _, rfin = oracle.fwd_recurrent(c["q"][sl], c["k"][sl], c["v"][sl], init=i64)
+        rq, rk, rv, rinit = oracle.bwd_recurrent(c["q"][sl], c["k"][sl], c["v"][sl], c["dO"][sl], init=i64)
+        for name, got, ref in (("o", o, ro), ("final", fin, rfin), ("dq", dq, rq), ("dk", dk_, rk), ("dv", dv, rv),
+                               ("d_init", dinit, rinit)):
+            assert rel(got[sl], ref) < 1e-2, (name, b, h)
 
 
 def test_forward_empty_sequence():

@@ -51,7 +51,7 @@ BYTES_SEGMENTS = 1536
 # Bytes each kernel kind moves per token-head and launch by its own inputs and
 # outputs (sequence tensors only): an I/O figure per kernel, not the method's
 # algorithmic bytes.
-KIND_IO_BYTES_PER_TOKEN_HEAD = {"tc_chunked_fwd": 1024, "tc_chunked_fwd_agg": 1280, "tc_fused_fwd": 1536,
+KIND_IO_BYTES_PER_TOKEN_HEAD = {"tc_chunked_fwd": 1024, "tc_chunked_fwd_agg": 1280,
                                 "tc_dual_rev": 1536, "tc_segment_aggregate": 512}
 # The tensor-core kernels run 128-token blocks (two chunks of 64): the chunked
 # form equals the definition for any chunk length, only the rounding order changes.

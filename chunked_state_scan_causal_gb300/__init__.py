@@ -80,7 +80,7 @@ _SIGS = {
     "linattn_timing_collect": ([_i32, ctypes.POINTER(_i32), ctypes.POINTER(ctypes.c_float)], _i32),
     "linattn_kernel_name": ([_i32], ctypes.c_char_p),
 }
-KERNEL_KINDS = 13
+KERNEL_KINDS = 12
 
 
 def lib():

@@ -1,7 +1,7 @@
 // C-ABI entry points of liblinattn: argument validation, workspace layout,
 // TMA descriptor encoding and the choice between the tensor-core pipeline
-// (bf16, d = 128) and the CUDA-core kernels (fp32 inputs, d = 64, per-chunk
-// state outputs).  Every error is detected here before anything is enqueued.
+// (bf16, d = 128) and the CUDA-core kernels (fp32 inputs, d = 64).  Every
+// error is detected here before anything is enqueued.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -143,67 +143,39 @@ static int cuda_status(cudaError_t e) { return e == cudaSuccess ? LINATTN_OK : L
 // ------------------------------------------------------------------ workspace layout
 constexpr size_t kHeader = 256;  // int32 status word at offset 0
 
-// Forward (tensor-core path).  Without a decay the forward is one fused launch
-// (tc_fused_fwd: group states chained inside it; workspace: the states and the
-// chain flags).  With a per-head decay, and with gates (max_len > 0), it is
-// the split pipeline: group aggregates -> scan -> chunked pass.
-// The one-launch forward for lambda = 1 (tc_fused_fwd); off: the split pipeline.
-constexpr bool kFusedForward = false;
 struct FwdLayout {
   GroupPlan gp;
   int G = 0;
-  bool fused = false;
-  size_t agg = 0, states = 0, scan = 0, chain = 0, total = kHeader;
+  size_t agg = 0, states = 0, scan = 0, total = kHeader;
 };
 static FwdLayout fwd_layout(const Problem &p, int max_len = 0) {
   FwdLayout w;
   if (!tc_supported(p) || p.T == 0) return w;
-  w.fused = kFusedForward && p.decay == nullptr && max_len == 0;
-  w.gp = w.fused ? tc_fused_plan(p) : tc_group_plan(p, max_len);
+  w.gp = tc_group_plan(p, max_len);
   w.G = w.gp.G;
   const size_t st = (size_t)w.G * p.B * p.H * p.d * p.d * sizeof(float);
-  if (w.fused) {
-    w.states = kHeader;
-    w.agg = w.states + align256(st);
-    w.chain = w.agg + align256(st);
-    w.total = w.chain + align256((size_t)w.G * p.B * p.H * sizeof(unsigned));
-    return w;
-  }
   w.agg = kHeader;
   w.states = w.agg + align256(st);
   w.scan = w.states + align256(st);
   w.total = w.scan + scan_workspace_bytes(w.G, (int64_t)p.B * p.H * p.d * p.d);
   return w;
 }
-// Backward (tensor-core path): its own groups, at most 256 per sequence (the
-// column-parallel scan).  After the fused forward they are whole multiples of
-// the forward's groups, so every backward group starts at a checkpointed state
-// (ginit_len = the forward's group length).  Without a checkpoint the forward
-// states are recomputed (aggregates + scan) on the backward's groups.
 struct BwdLayout {
-  GroupPlan gp;
-  int G = 0, ginit_len = 0;
-  size_t agg = 0, states = 0, scan = 0, wagg = 0, rbar = 0, total = kHeader;
+  FwdLayout f;            // forward group aggregates / states (recomputed without a checkpoint)
+  size_t wagg = 0, rbar = 0, total = kHeader;
 };
 static BwdLayout bwd_layout(const Problem &p) {
   BwdLayout w;
-  const FwdLayout f = fwd_layout(p);
-  if (f.G == 0) return w;
-  w.gp = f.fused ? tc_coarse_plan(p, f.gp.L) : f.gp;
-  w.ginit_len = f.fused ? f.gp.L : 0;
-  w.G = w.gp.G;
-  const size_t st = (size_t)w.G * p.B * p.H * p.d * p.d * sizeof(float);
-  w.agg = kHeader;
-  w.states = w.agg + align256(st);
-  w.scan = w.states + align256(st);
-  w.wagg = w.scan + scan_workspace_bytes(w.G, (int64_t)p.B * p.H * p.d * p.d);
+  w.f = fwd_layout(p);
+  if (w.f.G == 0) return w;
+  const size_t st = (size_t)w.f.G * p.B * p.H * p.d * p.d * sizeof(float);
+  w.wagg = w.f.total;
   w.rbar = w.wagg + align256(st);
   w.total = w.rbar + align256(st);
   return w;
 }
 
-// Checkpoint of the forward group states: [G][BH][d][d] fp32 for the forward's
-// groups (tensor-core path only).
+// Checkpoint of the forward group states: [G][BH][d][d] fp32 (tensor-core path only).
 static size_t ckpt_bytes(const Problem &p) {
   const FwdLayout w = fwd_layout(p);
   return w.G == 0 ? 0 : (size_t)w.G * p.B * p.H * p.d * p.d * sizeof(float);
@@ -337,18 +309,18 @@ static int32_t fwd_impl(const linattn_shape *shape, const void *q, const void *k
     }
     return LINATTN_OK;
   }
-  if (chunk_states || !tc_supported(p))
+  if (!tc_supported(p))
     return cuda_status(simt_fwd(p, q, k, v, o, init_state, final_state, chunk_states, s));
-  float *states = need_ckpt ? ckpt : reinterpret_cast<float *>(ws + w.states);
-  if (w.fused)  // one launch: group aggregates, chained group states, chunked pass
-    return cuda_status(tc_fused_fwd(p, w.gp, q, k, v, o, init_state, states, reinterpret_cast<float *>(ws + w.agg),
-                                    reinterpret_cast<unsigned *>(ws + w.chain), final_state, status, s));
-  // split pipeline: chunk-group aggregates -> exclusive scan of the group states
+  // tensor-core path: chunk-group aggregates -> exclusive scan of the group states
   // -> chunked forward of every group from its entering state
   float *agg = reinterpret_cast<float *>(ws + w.agg);
+  float *states = need_ckpt ? ckpt : reinterpret_cast<float *>(ws + w.states);
   cudaError_t e = tc_segment_states(p, w.gp, k, v, false, agg, status, s);
   if (e == cudaSuccess) e = plan_scan(p, w.gp, false, agg, init_state, states, nullptr, ws + w.scan, status, s);
   if (e == cudaSuccess) e = tc_main(p, w.gp, q, k, v, o, states, false, final_state, status, s);
+  // per-chunk (C = 64) exclusive states, when asked for: every group walked again
+  // from its entering state, one state out per chunk
+  if (e == cudaSuccess && chunk_states) e = tc_chunk_states(p, w.gp, k, v, states, chunk_states, status, s);
   return cuda_status(e);
 }
 
@@ -396,21 +368,19 @@ static int32_t bwd_impl(const linattn_shape *shape, const void *q, const void *k
   }
   if (!tc_supported(p))
     return cuda_status(simt_bwd(p, q, k, v, dO, init_state, d_final, dq, dk, dv, d_init_state, s));
-  const GroupPlan &gp = w.gp;
+  const GroupPlan &gp = w.f.gp;
   const int G = gp.G;
-  float *agg = reinterpret_cast<float *>(ws + w.agg);
+  float *agg = reinterpret_cast<float *>(ws + w.f.agg);
   float *wagg = reinterpret_cast<float *>(ws + w.wagg);
   float *rbar = reinterpret_cast<float *>(ws + w.rbar);
   cudaError_t e = cudaSuccess;
   // forward group states: from the checkpoint, or recomputed from k, v and init_state
   const float *states = ckpt;
-  int ginit_len = w.ginit_len;
   if (!need_ckpt) {
-    float *st = reinterpret_cast<float *>(ws + w.states);
+    float *st = reinterpret_cast<float *>(ws + w.f.states);
     e = tc_segment_states(p, gp, k, v, false, agg, status, s);
-    if (e == cudaSuccess) e = plan_scan(p, gp, false, agg, init_state, st, nullptr, ws + w.scan, status, s);
+    if (e == cudaSuccess) e = plan_scan(p, gp, false, agg, init_state, st, nullptr, ws + w.f.scan, status, s);
     states = st;
-    ginit_len = 0;
   }
   // dq: the forward-time kernel with (q, k, v) := (dO, v, k), reading every
   // group's state transposed.  Reverse group states Rbar_g = sum_{u > group end}
@@ -419,7 +389,7 @@ static int32_t bwd_impl(const linattn_shape *shape, const void *q, const void *k
   // q_t dO_t^T).  The dq pass accumulates those aggregates too, for every head
   // without a decay or with one of at least 0.8; the aggregate pass computes
   // them for the heads with smaller decays and passes over the others.
-  if (e == cudaSuccess) e = tc_main(p, gp, dO, v, k, dq, states, true, nullptr, status, s, q, wagg, ginit_len);
+  if (e == cudaSuccess) e = tc_main(p, gp, dO, v, k, dq, states, true, nullptr, status, s, q, wagg);
   if (e == cudaSuccess && p.decay) e = tc_segment_states(p, gp, q, dO, true, wagg, status, s, true);
   // A gradient D arriving at the final state enters the reverse scan across the
   // last group, whose length may be short of L: fold lambda^{len} D into that
@@ -427,7 +397,7 @@ static int32_t bwd_impl(const linattn_shape *shape, const void *q, const void *k
   const int64_t E = BH * p.d * p.d;
   if (e == cudaSuccess && d_final)
     e = fold_state(wagg + (int64_t)(G - 1) * E, d_final, p.decay, p.H, p.d * p.d, gp.len(G - 1, p.T), E, s);
-  if (e == cudaSuccess) e = plan_scan(p, gp, true, wagg, nullptr, rbar, d_init_state, ws + w.scan, status, s);
+  if (e == cudaSuccess) e = plan_scan(p, gp, true, wagg, nullptr, rbar, d_init_state, ws + w.f.scan, status, s);
   if (e == cudaSuccess && d_final)
     e = cudaMemcpyAsync(rbar + (int64_t)(G - 1) * E, d_final, state_bytes, cudaMemcpyDeviceToDevice, s);
   // dv and dk in one reverse-time pass from the states Rbar
@@ -707,7 +677,7 @@ const char *linattn_kernel_name(int32_t kind) {
   static const char *names[K_KINDS] = {"simt_fwd", "simt_bwd", "simt_segment_states", "state_scan",
                                        "tc_segment_aggregate", "tc_chunked_fwd",
                                        "diag_mma", "decode", "tc_dual_rev", "tc_chunked_fwd_agg",
-                                       "gate_prep_and_grad", "tc_fused_fwd", "tc_chunk_states"};
+                                       "gate_prep_and_grad", "tc_chunk_states"};
   return (kind >= 0 && kind < K_KINDS) ? names[kind] : "?";
 }
 

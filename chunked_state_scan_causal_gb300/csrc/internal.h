@@ -57,7 +57,7 @@ int device_ok();
 // ---------------------------------------------------------------- per-kernel timing (api.cu)
 enum KernelKind {
   K_SIMT_FWD = 0, K_SIMT_BWD, K_SIMT_SEGMENT, K_SCAN, K_TC_AGG, K_TC_MAIN_FWD, K_DIAG,
-  K_DECODE, K_TC_DUAL_REV, K_TC_MAIN_AGG, K_GATE, K_TC_FUSED_FWD, K_TC_CHUNK_STATES, K_KINDS
+  K_DECODE, K_TC_DUAL_REV, K_TC_MAIN_AGG, K_GATE, K_TC_CHUNK_STATES, K_KINDS
 };
 // Records timing events around one launch on `s` while timing is enabled.
 struct TimedLaunch {
@@ -97,8 +97,8 @@ cudaError_t state_scan(int G, int BH, int DD, const float *seg_decay, const floa
                        int seg_len, bool reverse, const float *local, const float *init, float *out,
                        float *total, void *ws, int *status, cudaStream_t s, const float *group_log2 = nullptr,
                        int kb = 1 << 30, int seg_len2 = 0, uint64_t limit_ns = 0, int withhold = -1);
-// Bound of the device-side waits on other CTAs' results (look-back, chained
-// group states): LINATTN_LOOKBACK_LIMIT_MS from the environment, else 2 s.
+// Bound of the device-side waits on other CTAs' results (the scan's look-back):
+// LINATTN_LOOKBACK_LIMIT_MS from the environment, else 2 s.
 uint64_t wait_limit_ns();
 
 // out[b * H + h] = decay_h[h]^len for b < B (the scan multiplier of a segment of len tokens).
@@ -131,7 +131,7 @@ cudaError_t gate_grad(const Problem &p, const GroupPlan &gp, const float *gx, co
 // per-warp record of a wait that gave up, and each kernel kind keeps the two
 // counters of its dynamic item order at these offsets (each launch leaves them
 // zero again, so one call may launch a kind more than once).
-constexpr int kCounterAgg = 32, kCounterMain = 34, kCounterDual = 36;
+constexpr int kCounterAgg = 32, kCounterMain = 34, kCounterDual = 36, kCounterChunk = 38;
 bool tc_supported(const Problem &p);   // bf16, d = 128
 // The chunk groups of the tensor-core path (lengths multiples of 128, at most
 // 256 groups); max_len > 0 caps the lengths where possible.
@@ -151,27 +151,15 @@ cudaError_t tc_segment_states(const Problem &p, const GroupPlan &gp, const void 
 // same pass, w_s = lambda^{s - start + 1} (1 without a decay), for the groups
 // of heads whose decay takes the weighted form (lambda >= 0.8, or none); the
 // other groups are left to tc_segment_states.
-// ginit_len > 0: group_init holds one state per ginit_len tokens (a checkpoint of
-// the fused forward's plan); group g starts from entry start(g) / ginit_len.
 cudaError_t tc_main(const Problem &p, const GroupPlan &gp, const void *q, const void *k, const void *v, void *o,
                     const float *group_init, bool init_transposed, float *final_state, int *status,
-                    cudaStream_t s, const void *x = nullptr, float *agg_out = nullptr, int ginit_len = 0);
+                    cudaStream_t s, const void *x = nullptr, float *agg_out = nullptr);
 
-// The groups of the fused forward (uniform, at most 1024 tokens, any count) and
-// the coarser groups of a pass that reads its checkpoint (lengths multiples of
-// `unit`, at most 256 groups).
-GroupPlan tc_fused_plan(const Problem &p);
-GroupPlan tc_coarse_plan(const Problem &p, int unit);
-
-// lambda = 1 forward in one launch: every group's k, v aggregate (pass 1), the
-// group states found by a decoupled look-back across the groups of a sequence
-// (`states` [G][BH][d][d] written: entry 0 = init or zeros, entry g + 1 = the
-// state after group g; `agg` [G][BH][d][d] the aggregates a group publishes
-// when its predecessor is not ready; `chain` [G][BH] flags, cleared here), then
-// the chunked pass from each group's entering state; final_state (optional).
-cudaError_t tc_fused_fwd(const Problem &p, const GroupPlan &gp, const void *q, const void *k, const void *v,
-                         void *o, const float *init, float *states, float *agg, unsigned *chain, float *final_state,
-                         int *status, cudaStream_t s);
+// The exclusive state entering every chunk of 64 tokens, out [BH][ceil(T/64)][d][d]
+// fp32, walking each group of the plan from its entering state group_init
+// ([G][BH][d][d], the scan's output) with one half-tile K^T V product per chunk.
+cudaError_t tc_chunk_states(const Problem &p, const GroupPlan &gp, const void *k, const void *v,
+                            const float *group_init, float *out, int *status, cudaStream_t s);
 
 // The backward's dv and dk in one reverse-time pass over (k, q, dO, v) from the
 // reverse group states [G][BH][d][d] (sum over later tokens u of

@@ -74,59 +74,6 @@ GroupPlan tc_group_plan(const Problem &p, int max_len) {
   return gp;
 }
 
-// The fused forward keeps each group's k, v in L2 between its two passes: at
-// most kFusedMaxLen tokens per group, so that one group per SM (152 x 1152 x
-// 512 bytes = 90 MB) fits the 126 MB L2 beside the other streams.  The group
-// count is free (the states are chained, not scanned): the length minimises
-// waves * (L / 128 + 1) as in tc_group_plan, uniform groups.
-constexpr int kFusedMaxLen = 1152;
-
-GroupPlan tc_fused_plan(const Problem &p) {
-  const int64_t BH = (int64_t)p.B * p.H, T = p.T, sms = p.num_sms > 0 ? p.num_sms : 1;
-  int64_t bestL = 256, bestCost = -1;
-  for (int64_t L = 256; L <= kFusedMaxLen; L += 128) {
-    const int64_t G = (T + L - 1) / L, waves = (BH * G + sms - 1) / sms, cost = waves * (L / 128 + 1);
-    if (bestCost < 0 || cost < bestCost || (cost == bestCost && L > bestL)) {
-      bestL = L;
-      bestCost = cost;
-    }
-  }
-  const int64_t Tr = (T + 127) / 128 * 128;
-  return GroupPlan::uniform((int)T, (int)(bestL < Tr ? bestL : Tr));
-}
-
-GroupPlan tc_coarse_plan(const Problem &p, int unit) {
-  // As tc_group_plan, with every group length a multiple of `unit` tokens (the
-  // group length of a checkpoint written by the fused forward), so that every
-  // group starts where a checkpointed state is.
-  const int64_t BH = (int64_t)p.B * p.H, T = p.T, sms = p.num_sms > 0 ? p.num_sms : 1;
-  const int64_t Gu = (T + unit - 1) / unit;  // checkpointed groups
-  int64_t bestR = 0, bestCost = 0;
-  for (int64_t r = 1; r <= Gu; ++r) {
-    const int64_t L = r * unit, G = (T + L - 1) / L;
-    if (G > 256) continue;
-    const int64_t waves = (BH * G + sms - 1) / sms, cost = waves * (L / 128 + 1);
-    if (bestR == 0 || cost < bestCost || (cost == bestCost && r > bestR)) {
-      bestR = r;
-      bestCost = cost;
-    }
-  }
-  if (bestR == 0) bestR = (Gu + 255) / 256;
-  GroupPlan gp = GroupPlan::uniform((int)T, (int)(bestR * unit));
-  const int64_t waves = (BH * gp.G + sms - 1) / sms;
-  const int64_t rs = bestR / kTailDiv;  // the tail in groups of half the length, whole units
-  if (waves < kTailMinWaves || rs < 1) return gp;
-  const int L = gp.L, Ls = (int)(rs * unit);
-  const int kb = (int)(T * (kTailDen - kTailNum) / ((int64_t)kTailDen * L));
-  if (kb < 1) return gp;
-  const int64_t rest = T - (int64_t)kb * L, Gs = (rest + Ls - 1) / Ls;
-  if (kb + Gs > 256) return gp;
-  gp.G = kb + (int)Gs;
-  gp.kb = kb;
-  gp.Ls = Ls;
-  return gp;
-}
-
 namespace {
 
 constexpr int kThreads = 384;
@@ -417,6 +364,218 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, 256);
 }
 
+// ============================================================================ per-chunk states
+// The exclusive state entering every chunk of C = 64 tokens, [B][H][ceil(T/64)][d][d]
+// fp32: per (group, sequence) item, from the state entering the group (the scan's
+// output), walking the group's chunks in order:
+//   out[c] = S;   S <- lambda^64 S + (diag(lambda^{63-j}) K_c)^T V_c   (j: row in the chunk)
+// The state stays in TMEM; each chunk's product contracts over the 64 rows of its
+// half of the 128-token tile (four K = 16 steps).  The last chunk of a group needs
+// no product (the next group starts from its own scanned state).
+struct ChunkParams {
+  int B, H, T, nitems, nch;  // nch = ceil(T / 64) chunks per sequence
+  GroupPlan gp;
+  const float *decay;
+  const float *ginit;  // [G][BH][d][d] states entering the groups
+  float *out;          // [BH][nch][d][d]
+  int *status;
+  int *counter;        // [2] item counter and finished CTAs (zero at launch)
+};
+
+template <bool DECAY>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_chunk_states_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
+                           ChunkParams P) {
+  constexpr int NS = 3;  // stages of (K tile, V tile)
+  constexpr uint32_t kStage = 2 * kTileBytes;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = align1024(smem_raw);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + NS * kStage);
+  uint64_t *full = bars, *scaled = bars + NS, *empty = bars + 2 * NS;
+  uint64_t *crd = bars + 3 * NS, *cmma = crd + 1;  // chunk state read out; chunk product done
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(cmma + 1);
+  __shared__ int abort_flag;
+  __shared__ int ring_item[kRing];
+  __shared__ uint64_t ring_bar[2 * kRing];
+  const ItemRing ring{ring_item, ring_bar, ring_bar + kRing};
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int BH = P.B * P.H;
+  int *const detail = P.status ? P.status + 1 + warp : nullptr;
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&scaled[s], 128);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(crd, 128);
+    mbar_init(cmma, 1);
+    ring_init(ring, 1 + (DECAY ? 128 : 0) + 128);  // readers: MMA thread, weighting warps, state warps
+    fence_mbar_init();
+    prefetch_tensormap(&mk);
+    prefetch_tensormap(&mv);
+  }
+  if (warp == 1) {
+    tmem_alloc(tslot, 128);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tS = *tslot;
+  auto range = [&](int item, int &s0, int &s1) {
+    const int g = item / BH;
+    s0 = P.gp.start(g);
+    s1 = min(P.T, P.gp.start(g + 1));
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer: K, V tiles per block
+    if (lane == 0) {
+      int it = 0;
+      bool ok = true;
+      for (int k = 0, item; ok; ++k) {
+        if (!(ok = ring_post(ring, k, P.counter, P.nitems, item, &abort_flag, P.status, detail)) || item < 0) break;
+        const int bh = item % BH, b = bh / P.H, h = bh % P.H;
+        int s0, s1;
+        range(item, s0, s1);
+        for (int t0 = s0; t0 < s1; t0 += 128, ++it) {
+          const int s = it % NS, u = it / NS;
+          if (u > 0 && !(ok = mbar_wait(&empty[s], (u - 1) & 1, &abort_flag, P.status, detail))) break;
+          uint8_t *xs = smem + s * kStage;
+          mbar_arrive_expect_tx(&full[s], kStage);
+          tma_load_4d(&mk, &full[s], xs, 0, t0, h, b, kPolicyEvictFirst);
+          tma_load_4d(&mk, &full[s], xs + kTileHalfBytes, 64, t0, h, b, kPolicyEvictFirst);
+          tma_load_4d(&mv, &full[s], xs + kTileBytes, 0, t0, h, b, kPolicyEvictFirst);
+          tma_load_4d(&mv, &full[s], xs + kTileBytes + kTileHalfBytes, 64, t0, h, b, kPolicyEvictFirst);
+        }
+      }
+      volatile int no_abort = 0;
+      for (int s = 0; s < NS; ++s) {
+        const int uses = it > s ? (it - 1 - s) / NS + 1 : 0;
+        if (uses > 0) mbar_wait(&full[s], (uses - 1) & 1, &no_abort, P.status);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer: one half-tile product per chunk
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(128, 128, true, true);
+      int it = 0, ck = 0;  // blocks and chunks seen by this CTA
+      bool ok = true;
+      for (int k = 0, item; ok; ++k) {
+        if (!(ok = ring_take(ring, k, item, &abort_flag, P.status, detail)) || item < 0) break;
+        int s0, s1;
+        range(item, s0, s1);
+        const int nc = (s1 - s0 + 63) / 64;
+        for (int c = 0; c < nc && ok; ++c, ++ck) {
+          const int s = it % NS, u = it / NS;
+          // the chunk's entering state has been read out (and decayed) from TMEM
+          if (!(ok = mbar_wait(crd, ck & 1, &abort_flag, P.status, detail))) break;
+          if (c + 1 < nc) {
+            if ((c & 1) == 0 &&
+                !(ok = mbar_wait(DECAY ? &scaled[s] : &full[s], u & 1, &abort_flag, P.status, detail)))
+              break;
+            tc_fence_after();
+            const uint32_t xs = smem_u32(smem + s * kStage), ys = xs + kTileBytes;
+#pragma unroll
+            for (uint32_t j = 0; j < 4; ++j) {
+              const uint32_t ks = 4 * (c & 1) + j;  // the chunk's 64 rows of the tile
+              mma_ss(tS, desc_mnmajor(xs, ks), desc_mnmajor(ys, ks), idesc, 1u);
+            }
+            mma_commit(cmma);
+          }
+          // a block's stage is released after its second chunk, or the group's last
+          if ((c & 1) == 1 || c + 1 == nc) {
+            if (c + 1 == nc && (c & 1) == 0 &&
+                !(ok = mbar_wait(DECAY ? &scaled[s] : &full[s], u & 1, &abort_flag, P.status, detail)))
+              break;
+            mma_commit(&empty[s]);
+            ++it;
+          }
+        }
+      }
+    }
+  } else if (warp >= 4 && warp < 8) {
+    if (DECAY) {
+      // key rows weighted in place: lambda^{63 - (row mod 64)}, before the products read them
+      const uint32_t row = threadIdx.x - 128;
+      int it = 0;
+      bool ok = true;
+      for (int k = 0, item; ok; ++k) {
+        if (!(ok = __all_sync(0xffffffffu, ring_take(ring, k, item, &abort_flag, P.status, detail))) || item < 0)
+          break;
+        const float l2 = log2f(P.decay[(item % BH) % P.H]);
+        const float w = exp2f(l2 * (float)(63 - (int)(row & 63)));
+        int s0, s1;
+        range(item, s0, s1);
+        for (int t0 = s0; t0 < s1; t0 += 128, ++it) {
+          const int s = it % NS, u = it / NS;
+          if (!(ok = mbar_wait(&full[s], u & 1, &abort_flag, P.status, detail))) break;
+          scale_tile_row(smem_u32(smem + s * kStage), row, w);
+          fence_proxy_async_smem();
+          mbar_arrive(&scaled[s]);
+        }
+      }
+    }
+  } else if (warp >= 8) {
+    // ------------------------------------------------------------ state warps: read out every chunk's state
+    const uint32_t quad = warp & 3, row = quad * 32 + lane, lb = (quad * 32) << 16;
+    int ck = 0;
+    bool ok = true;
+    for (int k = 0, item; ok; ++k) {
+      if (!(ok = __all_sync(0xffffffffu, ring_take(ring, k, item, &abort_flag, P.status, detail))) || item < 0)
+        break;
+      const int g = item / BH, bh = item % BH;
+      int s0, s1;
+      range(item, s0, s1);
+      const int nc = (s1 - s0 + 63) / 64;
+      const float dec = DECAY ? exp2f(log2f(P.decay[bh % P.H]) * 64.f) : 1.f;
+      float *dst0 = P.out + ((int64_t)bh * P.nch + s0 / 64) * 16384 + row * 128;
+      const float *src = P.ginit + ((int64_t)g * BH + bh) * 16384 + row * 128;
+      for (int c = 0; c < nc && ok; ++c, ++ck) {
+        float *dst = dst0 + (int64_t)c * 16384;
+        if (c > 0) {
+          // chunk c-1's product is done: its result is chunk c's entering state
+          if (!(ok = __all_sync(0xffffffffu, mbar_wait(cmma, (ck - 1 - k) & 1, &abort_flag, P.status, detail))))
+            break;
+          tc_fence_after();
+        }
+#pragma unroll 1
+        for (int q = 0; q < 4; ++q) {
+          float x[32];
+          if (c == 0) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {
+              const float4 v4 = __ldg(reinterpret_cast<const float4 *>(src + q * 32 + j));
+              x[j] = v4.x; x[j + 1] = v4.y; x[j + 2] = v4.z; x[j + 3] = v4.w;
+            }
+          } else {
+            ld_chunk(tS + lb + q * 32, x);
+          }
+#pragma unroll
+          for (int j = 0; j < 32; j += 4)
+            __stcs(reinterpret_cast<float4 *>(dst + q * 32 + j), make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]));
+          if ((c == 0 || DECAY) && c + 1 < nc) {
+            // the state the chunk's product accumulates into: lambda^64 S
+            uint32_t r[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(x[j] * dec);
+            tmem_st32(tS + lb + q * 32, r);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(crd);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  items_done(P.counter);
+  if (warp == 1) tmem_dealloc(tS, 128);
+}
+
 // ============================================================================ per-group main kernel
 struct MainParams {
   int B, H, T, nitems, init_t;
@@ -424,7 +583,7 @@ struct MainParams {
   const float *decay;
   const float *ginit;  // [G][BH][d][d]
   float *final_state;  // [BH][d][d] or null
-  float *agg_out;      // [G][BH][d][d]: per group sum_s x_s q_s^T (AGG); FUSED: group aggregates K^T V
+  float *agg_out;      // [G][BH][d][d]: per group sum_s x_s q_s^T (AGG instances)
   int *status;
   int *counter;        // [2] item counter and finished CTAs (zero at launch)
   const float *gC;     // GATE: group-local log2 cumulative sums of the gates [BH][T]
@@ -432,12 +591,6 @@ struct MainParams {
   const __nv_bfloat16 *gq;  // GATE, dq pass: the true q (strides sb, sh, st) for gx = q . dq
   float *gx;           // GATE, dq pass: [BH][T] fp32 q_t . dq_t from the unrounded dq, or null
   int64_t sb, sh, st;
-  int ginit_len;       // > 0: ginit holds one state per ginit_len tokens (group g reads start(g) / ginit_len)
-  // FUSED: the group states are chained inside the launch (see tc_main_kernel)
-  float *states;       // [G][BH][d][d] written: the state entering every group
-  const float *init;   // [BH][d][d] state before token 0, or null (zeros)
-  unsigned *chain;     // [G][BH] look-back flags: 1 aggregate in agg_out, 2 inclusive in states (zero at launch)
-  uint64_t limit_ns;   // bound of the wait for a group's entering state
 };
 
 constexpr int kSlots = 5;
@@ -452,7 +605,7 @@ constexpr size_t kMainSmem = kOffGate + 1024 + 1024;
 // block parity (an arrival for block n + 2 can only follow the MMA thread's
 // wait for block n).
 enum { B_FULL = 0, B_EMPTY = kSlots, B_PFULL = 2 * kSlots, B_PEMPTY, B_OFULL, B_OEMPTY, B_SFULL, B_PRE,
-       B_PSFULL, B_WEMPTY, B_KS, B_XS = B_KS + 2, B_UFULL = B_XS + 2, B_COUNT };
+       B_PSFULL, B_WEMPTY, B_KS, B_XS = B_KS + 2, B_COUNT = B_XS + 2 };
 static_assert(B_COUNT * 8 + 4 <= 256, "chunked kernel barriers and the TMEM slot fit their 256 bytes");
 
 // Decay mask of one 32-column chunk of a score row: keep j <= i (causal) or
@@ -581,24 +734,13 @@ __device__ __forceinline__ float dot32_bf16(const float (&x)[32], const __nv_bfl
 // the token before the block, 0 at a group start); in the weighted form the
 // mask scalar is exp2(C_prev - C_last) and the store's row weight
 // exp2(C_i - C_prev).
-//
-// FUSED (lambda = 1): the group states are not scanned beforehand but found
-// inside the launch.  Every item first streams its group's k, v once (pass 1,
-// L2 evict-last) into U = K^T V, accumulated in the state region of TMEM;
-// group B then finds the state S entering the group by a decoupled look-back
-// over the earlier groups of the same sequence (items are drawn group-major,
-// so those were drawn earlier by running CTAs; waits are bounded), publishes
-// the state entering the next group, S + U, and starts pass 2 from S.  Pass 2
-// is the chunked pass above; its k, v reads meet the lines pass 1 left in L2,
-// so HBM sees k and v once.
-template <bool DECAY, bool AGG = false, bool GATE = false, bool FUSED = false>
+template <bool DECAY, bool AGG = false, bool GATE = false>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_main_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                    const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mo,
                    const __grid_constant__ CUtensorMap mx, MainParams P) {
   static_assert(!AGG || !GATE, "group aggregates are fused for per-head decays only");
   static_assert(!GATE || DECAY, "gates use the weighted code paths");
-  static_assert(!FUSED || (!DECAY && !AGG && !GATE), "the chained group states are built for lambda = 1");
   constexpr int NT = AGG ? 4 : 3;  // tiles per block
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
@@ -626,7 +768,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bar[B_PRE], 128);
     mbar_init(&bar[B_PSFULL], 128);
     mbar_init(&bar[B_WEMPTY], 128);
-    mbar_init(&bar[B_UFULL], 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar[B_KS + i], 128);
       mbar_init(&bar[B_XS + i], 128);
@@ -652,11 +793,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sbase = smem_u32(smem);
   const uint32_t sPs = sbase + kOffPs, sSh = sbase + kOffSh;
   auto slot_addr = [&](int t) { return sbase + (uint32_t)(t % kSlots) * kTileBytes; };
-  // ring position of tile role r (0 q, 1 k, 2 v, 3 x) of block blk; p1 counts the
-  // pass-1 tiles (FUSED) that came through the ring before it
-  int p1 = 0;
+  // ring position of tile role r (0 q, 1 k, 2 v, 3 x) of block blk
   auto tile_of = [&](int blk, int r) {
-    return NT * blk + p1 + (AGG ? (r == 0 ? 0 : (r == 3 ? 1 : r + 1)) : r);
+    return NT * blk + (AGG ? (r == 0 ? 0 : (r == 3 ? 1 : r + 1)) : r);
   };
 
   if (warp == 0) {
@@ -668,29 +807,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = ring_post(ring, k, P.counter, P.nitems, item, &abort_flag, P.status, detail)) || item < 0) break;
         const int g = item / BH, bh = item % BH, b = bh / P.H, h = bh % P.H;
         const int s0 = P.gp.start(g), s1 = min(P.T, P.gp.start(g + 1)), nb = (s1 - s0 + 127) / 128;
-        if (!FUSED) {
-          const int gi = P.ginit_len > 0 ? s0 / P.ginit_len : g;
-          bulk_prefetch_l2(P.ginit + ((int64_t)gi * BH + bh) * 16384, 16384 * 4);  // the entering state
-        } else {
-          // pass 1: the group's k, v tiles from its last block back to its first,
-          // so that pass 2 starts on the most recently loaded lines
-          for (int i = 0; i < nb && ok; ++i) {
-            const int t0 = s0 + 128 * (nb - 1 - i);
-            for (int x = 0; x < 2; ++x) {
-              const int t = NT * blk + p1, s = t % kSlots, u = t / kSlots;
-              if (u > 0 && !(ok = mbar_wait(&bar[B_EMPTY + s], (u - 1) & 1, &abort_flag, P.status, detail))) break;
-              uint8_t *dst = smem + s * kTileBytes;
-              mbar_arrive_expect_tx(&bar[B_FULL + s], kTileBytes);
-              tma_load_4d(x ? &mv : &mk, &bar[B_FULL + s], dst, 0, t0, h, b, kPolicyEvictLast);
-              tma_load_4d(x ? &mv : &mk, &bar[B_FULL + s], dst + kTileHalfBytes, 64, t0, h, b, kPolicyEvictLast);
-              ++p1;
-            }
-          }
-        }
+        bulk_prefetch_l2(P.ginit + ((int64_t)g * BH + bh) * 16384, 16384 * 4);  // the entering state
         for (int n = 0; n < nb && ok; ++n, ++blk) {
           const int t0 = s0 + 128 * n;
           for (int x = 0; x < NT; ++x) {
-            const int t = NT * blk + p1 + x, s = t % kSlots, u = t / kSlots;  // load order = ring order
+            const int t = NT * blk + x, s = t % kSlots, u = t / kSlots;
             if (u > 0 && !(ok = mbar_wait(&bar[B_EMPTY + s], (u - 1) & 1, &abort_flag, P.status, detail))) break;
             const CUtensorMap *m = AGG ? (x == 0 ? &mq : (x == 1 ? &mx : (x == 2 ? &mk : &mv)))
                                        : (x == 0 ? &mq : (x == 1 ? &mk : &mv));
@@ -702,7 +823,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // time-bounded drain of the loads in flight (also after an abort)
-      const int ntile = NT * blk + p1;
+      const int ntile = NT * blk;
       volatile int no_abort = 0;
       for (int s = 0; s < kSlots; ++s) {
         const int uses = ntile > s ? (ntile - 1 - s) / kSlots + 1 : 0;
@@ -727,27 +848,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool wtd = DECAY && (GATE ? P.gflag && P.gflag[item] != 0
                                         : P.decay[(item % BH) % P.H] >= kWeightedMin);
         const bool aggw = AGG && (!DECAY || wtd);
-        if (FUSED) {
-          // pass 1: U = K^T V over the group into the state region (free: every
-          // product of the previous item precedes these in issue order, and its
-          // state was last read before its final block's Q S)
-          for (int i = 0; i < nb && ok; ++i) {
-            const int tk = NT * blk + p1, tv = tk + 1;
-            ok = mbar_wait(&bar[B_FULL + tk % kSlots], (tk / kSlots) & 1, &abort_flag, P.status, detail) &&
-                 mbar_wait(&bar[B_FULL + tv % kSlots], (tv / kSlots) & 1, &abort_flag, P.status, detail);
-            if (!ok) break;
-            tc_fence_after();
-            const uint32_t K = slot_addr(tk), V = slot_addr(tv);
-#pragma unroll
-            for (uint32_t ks = 0; ks < 8; ++ks)
-              mma_ss(tS, desc_mnmajor(K, ks), desc_mnmajor(V, ks), id_kv, (i > 0 || ks > 0) ? 1u : 0u);
-            mma_commit(&bar[B_EMPTY + tk % kSlots]);
-            mma_commit(&bar[B_EMPTY + tv % kSlots]);
-            p1 += 2;
-          }
-          if (!ok) break;
-          mma_commit(&bar[B_UFULL]);
-        }
         for (int n = 0; n < nb; ++n, ++blk) {
           const int tq = tile_of(blk, 0), tk = tile_of(blk, 1), tv = tile_of(blk, 2), tx = tile_of(blk, 3);
           const uint32_t Q = slot_addr(tq), K = slot_addr(tk), V = slot_addr(tv);
@@ -915,7 +1015,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= 8) {
     // ------------------------------------------------------------ group B: state tile (+ decay weights)
     const uint32_t quad = warp & 3, row = quad * 32 + lane, lb = (quad * 32) << 16;
-    int blk = 0, ui = 0;  // ui: items (phases of B_UFULL, FUSED)
+    int blk = 0;
     bool ok = true;
     for (int k = 0, item; ok; ++k) {
       if (!(ok = __all_sync(0xffffffffu, ring_take(ring, k, item, &abort_flag, P.status, detail))) || item < 0)
@@ -964,149 +1064,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (GATE) return exp2f(gc[t0 + nv - 1] - (t0 > s0 ? gc[t0 - 1] : 0.f));
         return DECAY ? exp2f(l2 * (float)nv) : 1.f;
       };
-      if (FUSED) {
-        // The state entering this group, by decoupled look-back over the groups
-        // before it in this sequence.  flag[g] (per sequence) is 1 once group g's
-        // aggregate U_g is in agg_out[g], 2 once its inclusive state (the state
-        // entering group g + 1) is in states[g + 1].  A group whose predecessor
-        // is not yet inclusive publishes its own aggregate first, so that no
-        // group ever waits for more than the pass 1 of the groups before it;
-        // in steady state the predecessor is inclusive and no aggregate is
-        // written.  Every wait is bounded.
-        bool okc = __all_sync(0xffffffffu, mbar_wait(&bar[B_UFULL], ui & 1, &abort_flag, P.status, detail));
-        ++ui;
-        if (!(ok = group_all(okc, 4, 128))) break;
-        tc_fence_after();
-        unsigned *const flags = P.chain + bh;  // flags[j * BH]: group j of this sequence
-        bool fast = true;
-        if (g > 0) {
-          unsigned f = 0;
-          if (lane == 0) f = ld_acquire_gpu(flags + (int64_t)(g - 1) * BH);
-          fast = __shfl_sync(0xffffffffu, f, 0) == 2u;
-        }
-        fast = group_all(fast, 4, 128);
-        if (!fast) {
-          float *dst = P.agg_out + ((int64_t)g * BH + bh) * 16384 + row * 128;
-#pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            float u[32];
-            ld_chunk(tS + lb + c * 32, u);
-#pragma unroll
-            for (int j = 0; j < 32; j += 4)
-              __stcg(reinterpret_cast<float4 *>(dst + c * 32 + j), make_float4(u[j], u[j + 1], u[j + 2], u[j + 3]));
-          }
-          __threadfence();
-          named_bar_sync(4, 128);
-          if (row == 0) st_release_gpu(flags + (int64_t)g * BH, 1u);
-        }
-        // the look-back path: aggregates of groups g-1 .. g-nagg, then the inclusive
-        // state of group g-1-nagg (= states[g - nagg]) or, past group 0, the initial state
-        int nagg = 0;
-        bool from_init = g == 0;
-        if (g > 0) {
-          unsigned code = 0;
-          if (lane == 0) {
-            int j = g - 1, n = 0;
-            bool hit_init = false, good = true;
-#pragma unroll 1
-            while (true) {
-              const unsigned *fp = flags + (int64_t)j * BH;
-              unsigned f = ld_acquire_gpu(fp);
-              if (!f) {
-                const uint64_t t0 = globaltimer_ns();
-                while (!(f = ld_acquire_gpu(fp))) {
-                  if (*reinterpret_cast<volatile int *>(&abort_flag) || globaltimer_ns() - t0 > P.limit_ns) break;
-                }
-                if (!f) {
-                  if (!*reinterpret_cast<volatile int *>(&abort_flag)) {
-                    report_error(P.status, -6);
-                    if (detail) atomicCAS(detail, 0, (int)((warp << 24) | 0x400000u));
-                    *reinterpret_cast<volatile int *>(&abort_flag) = 1;
-                  }
-                  good = false;
-                  break;
-                }
-              }
-              if (f == 2u) break;
-              ++n;
-              if (--j < 0) {
-                hit_init = true;
-                break;
-              }
-            }
-            code = good ? ((unsigned)n | (hit_init ? 0x40000000u : 0u)) : 0xFFFFFFFFu;
-          }
-          code = __shfl_sync(0xffffffffu, code, 0);
-          okc = code != 0xFFFFFFFFu;
-          nagg = (int)(code & 0x3FFFFFFFu);
-          from_init = (code >> 30) & 1u;
-          __threadfence();  // the loads below come after the flags seen
-        }
-        if (!(ok = group_all(okc, 4, 128))) break;
-        const float *base = from_init ? (P.init ? P.init + (int64_t)bh * 16384 : nullptr)
-                                      : P.states + ((int64_t)(g - nagg) * BH + bh) * 16384;
-        float *dst0 = g == 0 ? P.states + (int64_t)bh * 16384 : nullptr;  // the first entry: the initial state
-        float *dst = g + 1 < P.gp.G ? P.states + ((int64_t)(g + 1) * BH + bh) * 16384
-                                    : (P.final_state ? P.final_state + (int64_t)bh * 16384 : nullptr);
-#pragma unroll 1
-        for (int c2 = 0; c2 < 4; c2 += 2) {
-          // two chunks of the entering state in flight at once
-          float x[64];
-#pragma unroll
-          for (int j = 0; j < 64; j += 4) {
-            float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (base) v4 = __ldcg(reinterpret_cast<const float4 *>(base + row * 128 + c2 * 32 + j));
-            x[j] = v4.x; x[j + 1] = v4.y; x[j + 2] = v4.z; x[j + 3] = v4.w;
-          }
-#pragma unroll 1
-          for (int i = 0; i < nagg; ++i) {
-            const float *a = P.agg_out + ((int64_t)(g - 1 - i) * BH + bh) * 16384 + row * 128 + c2 * 32;
-#pragma unroll
-            for (int j = 0; j < 64; j += 4) {
-              const float4 v4 = __ldcg(reinterpret_cast<const float4 *>(a + j));
-              x[j] += v4.x; x[j + 1] += v4.y; x[j + 2] += v4.z; x[j + 3] += v4.w;
-            }
-          }
-#pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) {
-            const int c = c2 + h2;
-            float u[32];
-            ld_chunk(tS + lb + c * 32, u);
-            float *xs = x + 32 * h2;
-            if (dst0) {
-#pragma unroll
-              for (int j = 0; j < 32; j += 4)
-                *reinterpret_cast<float4 *>(dst0 + row * 128 + c * 32 + j) = make_float4(xs[j], xs[j + 1], xs[j + 2], xs[j + 3]);
-            }
-            if (dst) {
-#pragma unroll
-              for (int j = 0; j < 32; j += 4)
-                __stcg(reinterpret_cast<float4 *>(dst + row * 128 + c * 32 + j),
-                       make_float4(xs[j] + u[j], xs[j + 1] + u[j + 1], xs[j + 2] + u[j + 2], xs[j + 3] + u[j + 3]));
-            }
-            float xc[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) xc[j] = xs[j];
-            store_row_chunk_bf16(sSh, row, c, xc);
-            uint32_t r[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(xs[j]);
-            tmem_st32(tS + lb + c * 32, r);
-          }
-        }
-        tmem_st_wait();
-        if (g + 1 < P.gp.G) {
-          __threadfence();
-          named_bar_sync(4, 128);
-          if (row == 0) st_release_gpu(flags + (int64_t)g * BH, 2u);
-        }
-        tc_fence_before();
-        fence_proxy_async_smem();
-        mbar_arrive(&bar[B_PRE]);
-      } else {
-        // initial state of the group
-        const int gi = P.ginit_len > 0 ? s0 / P.ginit_len : g;
-        const float *src = P.ginit + ((int64_t)gi * BH + bh) * 16384;
+      // initial state of the group
+      {
+        const float *src = P.ginit + ((int64_t)g * BH + bh) * 16384;
         const float dec = block_decay(0);
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
@@ -1185,7 +1145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_before();
           mbar_arrive(&bar[B_WEMPTY]);
-        } else if (!FUSED && P.final_state && g == P.gp.G - 1) {
+        } else if (P.final_state && g == P.gp.G - 1) {
           float *dst = P.final_state + (int64_t)bh * 16384 + row * 128;
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
@@ -1807,6 +1767,29 @@ cudaError_t tc_segment_states(const Problem &p, const GroupPlan &gp, const void 
   return cudaGetLastError();
 }
 
+cudaError_t tc_chunk_states(const Problem &p, const GroupPlan &gp, const void *k, const void *v,
+                            const float *group_init, float *out, int *status, cudaStream_t s) {
+  alignas(64) CUtensorMap mk, mv;
+  if (!status || !seq_tmap(p, k, &mk) || !seq_tmap(p, v, &mv)) return cudaErrorInvalidValue;
+  ChunkParams C;
+  C.B = p.B; C.H = p.H; C.T = p.T; C.gp = gp;
+  C.nitems = gp.G * p.B * p.H;
+  C.nch = (p.T + 63) / 64;
+  C.decay = p.decay; C.ginit = group_init; C.out = out; C.status = status; C.counter = status + kCounterChunk;
+  const size_t smem = 3 * 2 * kTileBytes + 1024 + 256;
+  const int grid = C.nitems < p.num_sms ? C.nitems : p.num_sms;
+  cudaError_t e;
+  TimedLaunch t(K_TC_CHUNK_STATES, s);
+  if (p.decay) {
+    if ((e = set_smem(tc_chunk_states_kernel<true>, smem)) != cudaSuccess) return e;
+    tc_chunk_states_kernel<true><<<grid, kThreads, smem, s>>>(mk, mv, C);
+  } else {
+    if ((e = set_smem(tc_chunk_states_kernel<false>, smem)) != cudaSuccess) return e;
+    tc_chunk_states_kernel<false><<<grid, kThreads, smem, s>>>(mk, mv, C);
+  }
+  return cudaGetLastError();
+}
+
 cudaError_t tc_dual(const Problem &p, const GroupPlan &gp, const void *q, const void *k, const void *v,
                     const void *dO, void *dk, void *dv, const float *group_init, int *status, cudaStream_t s) {
   alignas(64) CUtensorMap mk, mq, mv, mdo;
@@ -1840,44 +1823,18 @@ cudaError_t tc_dual(const Problem &p, const GroupPlan &gp, const void *q, const 
   return cudaGetLastError();
 }
 
-cudaError_t tc_fused_fwd(const Problem &p, const GroupPlan &gp, const void *q, const void *k, const void *v,
-                         void *o, const float *init, float *states, float *agg, unsigned *chain, float *final_state,
-                         int *status, cudaStream_t s) {
-  if (p.decay || p.gC || !status || !states || !chain || !agg) return cudaErrorInvalidValue;
-  alignas(64) CUtensorMap mq, mk, mv, mo;
-  if (!seq_tmap(p, q, &mq) || !seq_tmap(p, k, &mk) || !seq_tmap(p, v, &mv) || !seq_tmap(p, o, &mo))
-    return cudaErrorInvalidValue;
-  MainParams M{};
-  M.B = p.B; M.H = p.H; M.T = p.T; M.gp = gp;
-  M.nitems = gp.G * p.B * p.H;
-  M.final_state = final_state; M.status = status;
-  M.counter = status + kCounterMain;
-  M.sb = p.sb; M.sh = p.sh; M.st = p.st;
-  M.states = states; M.init = init; M.chain = chain; M.limit_ns = wait_limit_ns();
-  M.agg_out = agg;
-  M.ginit = states;
-  const int grid = M.nitems < p.num_sms ? M.nitems : p.num_sms;
-  cudaError_t e = cudaMemsetAsync(chain, 0, (size_t)gp.G * p.B * p.H * sizeof(unsigned), s);
-  if (e != cudaSuccess) return e;
-  TimedLaunch t(K_TC_FUSED_FWD, s);
-  if ((e = set_smem(tc_main_kernel<false, false, false, true>, kMainSmem)) != cudaSuccess) return e;
-  tc_main_kernel<false, false, false, true><<<grid, kThreads, kMainSmem, s>>>(mq, mk, mv, mo, mq, M);
-  return cudaGetLastError();
-}
-
 cudaError_t tc_main(const Problem &p, const GroupPlan &gp, const void *q, const void *k, const void *v, void *o,
                     const float *group_init, bool init_transposed, float *final_state, int *status,
-                    cudaStream_t s, const void *x, float *agg_out, int ginit_len) {
+                    cudaStream_t s, const void *x, float *agg_out) {
   if (x && (p.gC || !agg_out)) return cudaErrorInvalidValue;
   alignas(64) CUtensorMap mq, mk, mv, mo, mx;
   if (!seq_tmap(p, q, &mq) || !seq_tmap(p, k, &mk) || !seq_tmap(p, v, &mv) || !seq_tmap(p, o, &mo) ||
       !seq_tmap(p, x ? x : q, &mx))
     return cudaErrorInvalidValue;
-  MainParams M{};
+  MainParams M;
   M.B = p.B; M.H = p.H; M.T = p.T; M.gp = gp;
   M.nitems = gp.G * p.B * p.H;
   M.init_t = init_transposed ? 1 : 0;
-  M.ginit_len = ginit_len;
   if (!status) return cudaErrorInvalidValue;
   M.decay = p.decay; M.ginit = group_init; M.final_state = final_state; M.status = status;
   M.counter = status + kCounterMain;

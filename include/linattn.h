@@ -35,6 +35,11 @@
  *    T == 0 they are not read and may be NULL; the final state is then the
  *    initial state (or zeros) and d_init_state is zero.
  *  - States are fp32, row-major [.., d_k, d_v] (row index = key dimension).
+ *  - Paths: bf16 with d = 128 runs on the tensor-core kernels (chunk groups
+ *    processed in parallel, states joined by the scan).  fp32 inputs and
+ *    d = 64 run on CUDA-core kernels that walk every sequence serially, one
+ *    CTA per (batch, head): correct for any length but far slower on long
+ *    sequences (meant for fp32 checks and small heads).
  */
 #ifndef LINATTN_H
 #define LINATTN_H
@@ -103,7 +108,9 @@ int32_t linattn_workspace_size(const linattn_shape *shape, int32_t op, int32_t s
  *   init_state   [B,H,dk,dv] fp32 state before token 0, or NULL (zeros)
  *   final_state  [B,H,dk,dv] fp32 state after token T-1, or NULL
  *   chunk_states [B,H,ceil(T/chunk),dk,dv] fp32 state ENTERING every chunk
- *                (exclusive: entry 0 is init_state), or NULL
+ *                (exclusive: entry 0 is init_state), or NULL; on the
+ *                tensor-core path they cost one more pass over k, v
+ *                (every chunk group walked again from its scanned state)
  * Returns a status. */
 int32_t linattn_fwd(const linattn_shape *shape, const void *q, const void *k, const void *v,
                     void *o, const float *init_state, float *final_state, float *chunk_states,
@@ -286,7 +293,7 @@ int32_t linattn_device_status(const void *workspace, void *stream);
  * for every kernel kind k < max_kinds its launch count and summed device time
  * (ms), clears the record and returns the number of kinds
  * (LINATTN_KERNEL_KINDS), or a negative status. */
-#define LINATTN_KERNEL_KINDS 13
+#define LINATTN_KERNEL_KINDS 12
 int32_t linattn_timing_enable(int32_t on);
 int32_t linattn_timing_collect(int32_t max_kinds, int32_t *launches, float *total_ms);
 /* Name of kernel kind k (static string; "?" when out of range). */

@@ -145,6 +145,25 @@ def test_forward_chunk_states_bf16(d, T, dk):
     assert rel(cs[:, :, 0], init) < 1e-6   # exclusive: chunk 0 enters with the initial state
 
 
+@pytest.mark.parametrize("dk", [None, "cfg"])
+def test_forward_chunk_states_bf16_many_groups(dk):
+    """Per-chunk states on the tensor-core path with several chunk groups per
+    sequence and more (group, sequence) items than SMs (B2 H16), a ragged last
+    chunk; sampled heads from both ends of the item order against the oracle."""
+    B, H, T, d = 2, 16, 8192 + 200, 128
+    c, dev = case(47, B, H, T, d, torch.bfloat16, sigma=1 / np.sqrt(128))
+    lam = decays(H, dk)
+    o, fin, cs = run_fwd(c, dev, torch.bfloat16, lam, None, want_cs=True)
+    assert cs.shape == (B, H, (T + 63) // 64, d, d)
+    for b, h in ((0, 0), (0, 9), (1, 15)):
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        ro, rcs, rfin = oracle.fwd_recurrent(c["q"][sl], c["k"][sl], c["v"][sl],
+                                             lam=None if lam is None else lam[h:h + 1], chunk=64)
+        assert rel(cs[sl], rcs) < 1e-2, (b, h)
+        assert rel(o[sl], ro) < 1e-2, (b, h)
+        assert rel(fin[sl], rfin) < 1e-2, (b, h)
+
+
 @pytest.mark.parametrize("dtype,d", [(torch.bfloat16, 128), (torch.bfloat16, 64), (torch.float32, 128),
                                      (torch.float32, 64)])
 @pytest.mark.parametrize("T", [64, 200, 1000, 2048])
@@ -172,11 +191,10 @@ def test_forward_many_groups_bf16():
         assert rel(fin, rfin) < 1e-2
 
 
-def test_fused_forward_chained_groups_more_items_than_sms():
-    """lambda = 1: the one-launch forward chains the group states through global
-    memory (each group waits for its predecessor's published state).  More
-    (group, sequence) items than SMs (B2 H16, 9 groups per sequence), a ragged
-    last group, an initial state; the checkpoint it writes feeds the backward."""
+def test_forward_backward_lambda1_more_items_than_sms():
+    """lambda = 1 with more (group, sequence) items than SMs (B2 H16, several
+    groups per sequence drawn at run time), a ragged last group and an initial
+    state; the checkpoint the forward writes feeds the backward."""
     B, H, T, d = 2, 16, 8192 + 200, 128
     c, dev = case(43, B, H, T, d, torch.bfloat16, sigma=1 / np.sqrt(128))
     init = (np.random.default_rng(44).standard_normal((B, H, d, d)) * 0.1).astype(np.float32)

@@ -245,7 +245,7 @@ def traffic_from_ncu(csv_path: str, workload_name: str, units: float, note: str)
     for r in rows[1:]:
         if len(r) <= max(ik, im, iv, iu) or r[im] not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
             continue
-        name = r[ik].split("(")[0].split("<")[0].split("::")[-1].strip()
+        name = r[ik].split("(")[0].split("::")[-1].strip()
         v = float(r[iv].replace(",", "")) * scale.get(r[iu], 1)
         per_kernel[name] = per_kernel.get(name, 0.0) + v
     total = sum(per_kernel.values())

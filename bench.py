@@ -737,6 +737,71 @@ def run_decode(args):
         "gpu_launches": kern[0]}), flush=True)
 
 
+# ---------------------------------------------------------------------------------- softmax segment
+def run_softmax_segment(args):
+    """The softmax-attention segment of the hybrid variant: the last Tq = 16384 positions
+    (one rank's segment of four) of a B1 H16 prefix of Tk = 65536 tokens attend causally
+    over the gathered prefix, d = 128, bf16.  Tensor-bound: algorithmic FLOPs are
+    4 d per (query, visible key) pair (Q K^T and P V)."""
+    import numpy as np
+    import torch
+    import chunked_state_scan_causal_gb300 as la
+    from chunked_state_scan_causal_gb300 import build
+    build.build()
+    dev = torch.device("cuda", 0)
+    B, H, Tk, Tq, d = 1, 16, args.sm_tk, args.sm_tq, 128
+    g = torch.Generator(device="cpu").manual_seed(11)
+    q = torch.randn(B, H, Tq, d, generator=g).to(torch.bfloat16).to(dev)
+    k = torch.randn(B, H, Tk, d, generator=g).to(torch.bfloat16).to(dev)
+    v = torch.randn(B, H, Tk, d, generator=g).to(torch.bfloat16).to(dev)
+    o = torch.empty_like(q)
+    ws = la.workspace(q, la.OP_SOFTMAX_SEGMENT)
+    for _ in range(args.warmup):
+        la.softmax_segment_fwd(q, k, v, out=o, ws=ws)
+    torch.cuda.synchronize()
+    if la.device_status(ws) != la.OK:
+        raise RuntimeError("device-side error during warm-up")
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(_gpu_uuid(dev), 0) as clk:
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(args.steps):
+            la.softmax_segment_fwd(q, k, v, out=o, ws=ws)
+        e1.record()
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    off = Tk - Tq
+    pairs = Tq * off + Tq * (Tq + 1) // 2
+    flops = 4 * d * pairs * B * H
+    bytes_ = (2 * Tq + 2 * Tk) * d * 2 * B * H  # q, o; k, v once
+    p = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
+        os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+    peak = float(p.get("bf16_tflops", 1900.0))
+    src = "measured bf16_tflops (burst, of measured)" if "bf16_tflops" in p else "fallback 1900 TFLOP/s"
+    tf = flops / (ms * 1e-3) / 1e12
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+        rows = list(range(0, Tq, max(1, Tq // 16)))[:16]
+        qn, kn, vn = (x[0:1, 0:4].double().cpu().numpy() for x in (q, k, v))
+        t0 = time.perf_counter()
+        oracle.softmax_segment_fwd(qn, kn, vn, rows=rows)
+        sec = time.perf_counter() - t0
+        rp = sum(off + r + 1 for r in rows) * 4
+        cpu = {"value": 4 * d * rp / sec / 1e12, "unit": "TFLOP/s", "cores": oracle.threads_used(), "kind": "oracle",
+               "sample": f"heads 0..3, {len(rows)} query rows spread over the segment, fp64 numpy, {sec:.2f} s"}
+    print(json.dumps({
+        "metric": "causal softmax-attention segment TFLOP/s (hybrid layers, prefix gathered)", "value": tf,
+        "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "dtype": "bf16", "data": "synthetic (seeded normal)",
+        "config": {"workload": f"softmax-segment-B{B}H{H}-Tq{Tq}-Tk{Tk}-d{d}", "B": B, "H": H, "Tq": Tq, "Tk": Tk,
+                   "d": d, "causal": True, "scale": "1/sqrt(d)"},
+        "tokens_per_s": B * Tq / (ms * 1e-3), "algorithmic_gbs": bytes_ / (ms * 1e-3) / 1e9,
+        "roofline": {"kernel": "softmax_segment_kernel", "bound": "tensor", "achieved": tf, "peak": peak,
+                     "unit": "TFLOP/s", "frac": tf / peak, "traffic": None, "peak_source": src},
+        "gpu_launches": args.steps, "clocks": clk.summary(), "cpu_baseline": cpu}), flush=True)
+
+
 # ---------------------------------------------------------------------------------- sequence split
 def run_sp(args):
     """The sequence split across ranks (sp.forward + sp.backward) with N ranks as threads of
@@ -823,6 +888,9 @@ def main():
     ap.add_argument("--decode", action="store_true", help="measure the recurrent decode instead")
     ap.add_argument("--decode-batch", type=int, default=512, help="sequences per head for --decode")
     ap.add_argument("--sp", type=int, default=0, help="measure the sequence split with this many thread ranks")
+    ap.add_argument("--softmax-segment", action="store_true", help="measure the softmax-attention segment instead")
+    ap.add_argument("--sm-tq", type=int, default=16384, help="queries of the softmax segment")
+    ap.add_argument("--sm-tk", type=int, default=65536, help="gathered prefix length of the softmax segment")
     ap.add_argument("--traffic-from", default="", help="ncu CSV of whole steps (dram__bytes_read/write.sum): "
                     "store DRAM bytes per token-head in profiles/traffic.json and exit")
     ap.add_argument("--traffic-steps", type=int, default=1, help="steps the --traffic-from capture covers")
@@ -838,6 +906,8 @@ def main():
         print(json.dumps(traffic_from_ncu(args.traffic_from, cfg["name"], units, args.traffic_note)))
     elif args.decode:
         run_decode(args)
+    elif args.softmax_segment:
+        run_softmax_segment(args)
     elif args.sp:
         run_sp(args)
     elif args.impl == "reference":

@@ -30,6 +30,7 @@ NOALLOC_MAX_TILES = 65536
 BF16, F32 = 0, 1
 OP_FWD, OP_BWD, OP_CHUNK_STATES, OP_CHECKPOINT = 1, 2, 3, 4
 OP_FWD_GATED, OP_BWD_GATED, OP_CHECKPOINT_GATED = 5, 6, 7
+OP_SOFTMAX_SEGMENT = 8
 ABI_VERSION = 2
 
 
@@ -74,13 +75,15 @@ _SIGS = {
     "linattn_state_scan_noalloc": ([_i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp], _i32),
     "linattn_diag_mma": ([_i32, _vp, _vp, _vp, _vp], _i32),
     "linattn_segment_decay": ([_vp, _i32, _i32, _i32, _vp, _vp], _i32),
+    "linattn_softmax_segment_fwd": ([ctypes.POINTER(Shape), ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp,
+                                     ctypes.c_float, _vp, _sz, _vp], _i32),
     "linattn_diag_scan_withhold": ([_i32, _i32, _i32, _i32, _vp, _vp, _i32, ctypes.c_double, _vp, _sz, _vp],
                                    _i32),
     "linattn_timing_enable": ([_i32], _i32),
     "linattn_timing_collect": ([_i32, ctypes.POINTER(_i32), ctypes.POINTER(ctypes.c_float)], _i32),
     "linattn_kernel_name": ([_i32], ctypes.c_char_p),
 }
-KERNEL_KINDS = 12
+KERNEL_KINDS = 13
 
 
 def lib():
@@ -185,6 +188,11 @@ def linattn_state_scan_noalloc(G, BH, dk, dv, seg_decay, local, init, out, total
 
 def linattn_device_status(ws, stream) -> int:
     return lib().linattn_device_status(ws, stream)
+
+
+def linattn_softmax_segment_fwd(q_shape, kv_shape, q, k, v, o, lse, softmax_scale, ws, ws_bytes, stream) -> int:
+    return lib().linattn_softmax_segment_fwd(ctypes.byref(q_shape), ctypes.byref(kv_shape), q, k, v, o, lse,
+                                             softmax_scale, ws, ws_bytes, stream)
 
 
 def linattn_segment_decay(decay, B, H, seg_len, out, stream) -> int:
@@ -457,6 +465,23 @@ def segment_decay(decay, B: int, seg_len: int, out=None, stream=None):
     st = linattn_segment_decay(_ptr(decay), B, H, seg_len, _ptr(out), _stream(decay.device, stream))
     _check(st, "linattn_segment_decay")
     return out
+
+
+def softmax_segment_fwd(q, k, v, scale: float = 0.0, want_lse: bool = False, out=None, ws=None, stream=None):
+    """(o, lse or None): causal softmax attention of q [B,H,Tq,128] (the last Tq positions)
+    over the prefix k, v [B,H,Tk,128] (bf16; scale 0 means 1/sqrt(128))."""
+    import torch
+    _same_layout(q, out)
+    _same_layout(k, v)
+    B, H, Tq, d = q.shape
+    o = out if out is not None else torch.empty_strided(q.shape, q.stride(), dtype=q.dtype, device=q.device)
+    lse = torch.empty((B, H, Tq), dtype=torch.float32, device=q.device) if want_lse else None
+    if ws is None:
+        ws = workspace(q, OP_SOFTMAX_SEGMENT)
+    st = linattn_softmax_segment_fwd(shape_of(q), shape_of(k), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), scale,
+                                     _ptr(ws), ws.numel(), _stream(q.device, stream))
+    _check(st, "linattn_softmax_segment_fwd")
+    return o, lse
 
 
 def device_status(ws, stream=None) -> int:

@@ -5,6 +5,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cmath>
 #include <mutex>
 #include <vector>
 
@@ -274,6 +275,8 @@ int32_t linattn_workspace_size(const linattn_shape *shape, int32_t op, int32_t s
     *bytes = gated_layout(p).bwd_total;
   } else if (op == LINATTN_OP_CHECKPOINT_GATED) {
     *bytes = ckpt_bytes_gated(p);
+  } else if (op == LINATTN_OP_SOFTMAX_SEGMENT) {
+    *bytes = kHeader;
   } else {
     return LINATTN_ERR_INVALID;
   }
@@ -601,6 +604,32 @@ int32_t linattn_state_scan(int32_t G, int32_t BH, int32_t dk, int32_t dv, const 
                                 init_states, total, ws + kHeader, reinterpret_cast<int *>(ws), s));
 }
 
+int32_t linattn_softmax_segment_fwd(const linattn_shape *q_shape, const linattn_shape *kv_shape, const void *q,
+                                    const void *k, const void *v, void *o, float *lse, float softmax_scale,
+                                    void *workspace, size_t workspace_bytes, void *stream) {
+  Problem pq, pk;
+  int st = validate(q_shape, &pq);
+  if (st) return st;
+  if ((st = validate(kv_shape, &pk))) return st;
+  if (pq.B != pk.B || pq.H != pk.H || pq.d != pk.d || pq.dtype != pk.dtype || pk.T < pq.T) return LINATTN_ERR_INVALID;
+  if (pq.decay || pk.decay) return LINATTN_ERR_INVALID;
+  if (pq.dtype != 0 || pq.d != 128) return LINATTN_ERR_UNSUPPORTED;
+  if (!(softmax_scale > 0.f) && softmax_scale != 0.f) return LINATTN_ERR_INVALID;
+  if (pq.T > 0 && (st = check_ptrs({q, k, v, o}, {lse}))) return st;
+  if ((st = check_ws(workspace, workspace_bytes, kHeader))) return st;
+  if ((st = device_ok())) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(workspace, 0, kHeader, s) != cudaSuccess) return LINATTN_ERR_CUDA;
+  if (pq.T == 0) return LINATTN_OK;
+  SoftmaxProblem sp;
+  sp.B = pq.B; sp.H = pq.H; sp.Tq = pq.T; sp.Tk = pk.T;
+  sp.qsb = pq.sb; sp.qsh = pq.sh; sp.qst = pq.st;
+  sp.ksb = pk.sb; sp.ksh = pk.sh; sp.kst = pk.st;
+  sp.scale = softmax_scale > 0.f ? softmax_scale : 1.f / sqrtf((float)pq.d);
+  sp.num_sms = pq.num_sms;
+  return cuda_status(softmax_segment(sp, q, k, v, o, lse, static_cast<int *>(workspace), s));
+}
+
 int32_t linattn_segment_decay(const float *decay, int32_t B, int32_t H, int32_t seg_len, float *out,
                               void *stream) {
   if (B < 1 || H < 1 || seg_len < 0 || (int64_t)B * H > (1 << 30)) return LINATTN_ERR_INVALID;
@@ -677,7 +706,7 @@ const char *linattn_kernel_name(int32_t kind) {
   static const char *names[K_KINDS] = {"simt_fwd", "simt_bwd", "simt_segment_states", "state_scan",
                                        "tc_segment_aggregate", "tc_chunked_fwd",
                                        "diag_mma", "decode", "tc_dual_rev", "tc_chunked_fwd_agg",
-                                       "gate_prep_and_grad", "tc_chunk_states"};
+                                       "gate_prep_and_grad", "tc_chunk_states", "softmax_segment"};
   return (kind >= 0 && kind < K_KINDS) ? names[kind] : "?";
 }
 

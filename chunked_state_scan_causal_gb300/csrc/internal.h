@@ -57,7 +57,7 @@ int device_ok();
 // ---------------------------------------------------------------- per-kernel timing (api.cu)
 enum KernelKind {
   K_SIMT_FWD = 0, K_SIMT_BWD, K_SIMT_SEGMENT, K_SCAN, K_TC_AGG, K_TC_MAIN_FWD, K_DIAG,
-  K_DECODE, K_TC_DUAL_REV, K_TC_MAIN_AGG, K_GATE, K_TC_CHUNK_STATES, K_KINDS
+  K_DECODE, K_TC_DUAL_REV, K_TC_MAIN_AGG, K_GATE, K_TC_CHUNK_STATES, K_SOFTMAX_SEGMENT, K_KINDS
 };
 // Records timing events around one launch on `s` while timing is enabled.
 struct TimedLaunch {
@@ -131,7 +131,7 @@ cudaError_t gate_grad(const Problem &p, const GroupPlan &gp, const float *gx, co
 // per-warp record of a wait that gave up, and each kernel kind keeps the two
 // counters of its dynamic item order at these offsets (each launch leaves them
 // zero again, so one call may launch a kind more than once).
-constexpr int kCounterAgg = 32, kCounterMain = 34, kCounterDual = 36, kCounterChunk = 38;
+constexpr int kCounterAgg = 32, kCounterMain = 34, kCounterDual = 36, kCounterChunk = 38, kCounterSoftmax = 40;
 bool tc_supported(const Problem &p);   // bf16, d = 128
 // The chunk groups of the tensor-core path (lengths multiples of 128, at most
 // 256 groups); max_len > 0 caps the lengths where possible.
@@ -167,6 +167,19 @@ cudaError_t tc_chunk_states(const Problem &p, const GroupPlan &gp, const void *k
 // (k, q, dO) for dv and (v, dO, q) with the transposed states for dk.
 cudaError_t tc_dual(const Problem &p, const GroupPlan &gp, const void *q, const void *k, const void *v,
                     const void *dO, void *dk, void *dv, const float *group_init, int *status, cudaStream_t s);
+
+// ---------------------------------------------------------------- softmax segment (softmax.cu)
+// Causal softmax attention of the last Tq positions of a prefix of Tk tokens over
+// that prefix (bf16, d = 128): q and o [B,H,Tq,128] with strides (qsb, qsh, qst),
+// k and v [B,H,Tk,128] with strides (ksb, ksh, kst); lse [B,H,Tq] fp32 optional.
+struct SoftmaxProblem {
+  int B, H, Tq, Tk;
+  int64_t qsb, qsh, qst, ksb, ksh, kst;
+  float scale;
+  int num_sms;
+};
+cudaError_t softmax_segment(const SoftmaxProblem &p, const void *q, const void *k, const void *v, void *o, float *lse,
+                            int *status, cudaStream_t s);
 
 // ---------------------------------------------------------------- TMA descriptors (api.cu)
 // 4-D bf16 tiled tensor map, dims innermost first, strides in bytes for dims 1..3,

@@ -71,7 +71,8 @@ enum { LINATTN_BF16 = 0, LINATTN_F32 = 1 };
 
 /* Workspace / checkpoint queries. */
 enum { LINATTN_OP_FWD = 1, LINATTN_OP_BWD = 2, LINATTN_OP_CHUNK_STATES = 3, LINATTN_OP_CHECKPOINT = 4,
-       LINATTN_OP_FWD_GATED = 5, LINATTN_OP_BWD_GATED = 6, LINATTN_OP_CHECKPOINT_GATED = 7 };
+       LINATTN_OP_FWD_GATED = 5, LINATTN_OP_BWD_GATED = 6, LINATTN_OP_CHECKPOINT_GATED = 7,
+       LINATTN_OP_SOFTMAX_SEGMENT = 8 };
 
 typedef struct {
   int32_t abi_version;  /* must be LINATTN_ABI_VERSION                              */
@@ -220,6 +221,27 @@ int32_t linattn_chunk_states_rev(const linattn_shape *shape, int32_t seg_len, co
                                  const void *dO, float *local_grad_states, void *workspace,
                                  size_t workspace_bytes, void *stream);
 
+/* Softmax-attention segment of a hybrid model (LASP-2 page, abstract: LASP-2H
+ * applies the same communication redesign to standard attention modules: one
+ * gather hands every sequence-parallel rank the keys and values of every
+ * position up to the end of its segment).  The queries are the LAST Tq
+ * positions of a prefix of Tk >= Tq tokens (offset = Tk - Tq), attending
+ * causally over the prefix with standard scaled dot-product softmax attention:
+ *   o_i   = sum_{j <= offset+i} softmax_j(scale q_i . k_j) v_j
+ *   lse_i = log sum_{j <= offset+i} exp(scale q_i . k_j)
+ * (blockwise with a running maximum and sum per row; the full row softmax is
+ * never formed).  Forward only.
+ *   q_shape:  B, H, T = Tq and the element strides of q and o
+ *   kv_shape: B, H, T = Tk and the element strides of k and v
+ *   both: bf16, dk = dv = 128, chunk = 64, decay NULL (else INVALID/UNSUPPORTED)
+ *   q, o [B,H,Tq,128]; k, v [B,H,Tk,128]; lse [B,H,Tq] fp32 contiguous or NULL
+ *   softmax_scale > 0, or 0 for 1/sqrt(128)
+ *   workspace: LINATTN_OP_SOFTMAX_SEGMENT bytes (status word and item counters)
+ * Returns a status. */
+int32_t linattn_softmax_segment_fwd(const linattn_shape *q_shape, const linattn_shape *kv_shape, const void *q,
+                                    const void *k, const void *v, void *o, float *lse, float softmax_scale,
+                                    void *workspace, size_t workspace_bytes, void *stream);
+
 /* Workspace bytes for linattn_state_scan. */
 int32_t linattn_state_scan_workspace_size(int32_t G, int32_t BH, int32_t dk, int32_t dv,
                                           size_t *bytes);
@@ -293,7 +315,7 @@ int32_t linattn_device_status(const void *workspace, void *stream);
  * for every kernel kind k < max_kinds its launch count and summed device time
  * (ms), clears the record and returns the number of kinds
  * (LINATTN_KERNEL_KINDS), or a negative status. */
-#define LINATTN_KERNEL_KINDS 12
+#define LINATTN_KERNEL_KINDS 13
 int32_t linattn_timing_enable(int32_t on);
 int32_t linattn_timing_collect(int32_t max_kinds, int32_t *launches, float *total_ms);
 /* Name of kernel kind k (static string; "?" when out of range). */

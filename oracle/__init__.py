@@ -4,7 +4,11 @@ Only the test-suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import this package.  The CUDA library never calls it and
 shares no code with it.
 
-Every function takes numpy arrays shaped ``[B, H, T, d]`` (any float dtype; they
+It also holds the causal softmax attention of a query segment over its
+gathered key/value prefix (``softmax_segment_fwd``: the standard-attention
+layers of the hybrid variant).
+
+Every linear-attention function takes numpy arrays shaped ``[B, H, T, d]`` (any float dtype; they
 are widened to float64) and per-head decays ``lam`` shaped ``[H]`` or
 ``[B, H]`` (``None`` means lambda = 1), and returns float64 arrays.
 
@@ -26,3 +30,4 @@ from .oracle import (  # noqa: F401
     state_scan,
     threads_used,
 )
+from .softmax_oracle import softmax_segment_fwd  # noqa: F401

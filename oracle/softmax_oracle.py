@@ -1,0 +1,48 @@
+"""fp64 reference for causal softmax attention over a gathered key/value prefix.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring).
+
+The hybrid variant on the LASP-2 page ("LASP-2: Rethinking Sequence
+Parallelism for Linear Attention and Its Hybrid", abstract: LASP-2H applies
+the same communication redesign to standard attention modules) gives each
+sequence-parallel rank the keys and values of every earlier position by one
+gather, and the rank's queries attend causally over that prefix.  The
+standard attention module is taken in its plainest form: scaled dot-product
+softmax attention with scale 1/sqrt(d) and a causal mask.  For queries that
+are the last Tq positions of a prefix of Tk tokens (offset = Tk - Tq):
+
+    o_i   = sum_{j <= offset + i} softmax_j(scale * q_i . k_j) v_j
+    lse_i = log sum_{j <= offset + i} exp(scale * q_i . k_j)
+
+written row by row with numpy as the library primitive (max subtraction only
+keeps exp in range; it cancels exactly in the ratio).
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+
+def softmax_segment_fwd(q, k, v, scale=None, rows=None):
+    """(o [B,H,Tq,dv], lse [B,H,Tq]) in float64; q [B,H,Tq,d], k [B,H,Tk,d], v [B,H,Tk,dv], Tk >= Tq.
+
+    ``rows`` (optional list of query indices) limits the work to those rows;
+    the other rows of the outputs are NaN."""
+    q, k, v = (np.asarray(x, dtype=np.float64) for x in (q, k, v))
+    B, H, Tq, d = q.shape
+    Tk = k.shape[2]
+    assert k.shape[:2] == (B, H) and v.shape[:3] == (B, H, Tk) and Tk >= Tq
+    off = Tk - Tq
+    sc = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = np.full((B, H, Tq, v.shape[3]), np.nan)
+    lse = np.full((B, H, Tq), np.nan)
+    for i in (range(Tq) if rows is None else rows):
+        n = off + i + 1                                         # keys 0 .. off + i
+        s = sc * np.einsum("bhjd,bhd->bhj", k[:, :, :n], q[:, :, i])
+        m = s.max(axis=2, keepdims=True)
+        p = np.exp(s - m)
+        l = p.sum(axis=2)
+        o[:, :, i] = np.einsum("bhj,bhje->bhe", p, v[:, :, :n]) / l[..., None]
+        lse[:, :, i] = m[..., 0] + np.log(l)
+    return o, lse

@@ -2,9 +2,9 @@
 // prefix, on the tensor cores (tcgen05 + TMEM + TMA), bf16 with d = 128.
 //
 // The hybrid variant on the LASP-2 page ("LASP-2: Rethinking Sequence
-// Parallelism for Linear Attention and Its Hybrid", abstract: LASP-2H applies
-// the same communication redesign to standard attention modules) gives each
-// sequence-parallel rank, by one gather, the keys and values of every
+// Parallelism for Linear Attention and Its Hybrid", abstract: LASP-2H carries
+// the one-gather exchange over to the softmax attention layers of hybrid
+// models) gives each sequence-parallel rank, by one gather, the keys and values of every
 // position up to the end of its own segment; the rank's queries then attend
 // causally over that prefix.  Here the queries are the last Tq positions of
 // a prefix of Tk tokens (offset = Tk - Tq):

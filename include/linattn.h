@@ -222,7 +222,7 @@ int32_t linattn_chunk_states_rev(const linattn_shape *shape, int32_t seg_len, co
                                  size_t workspace_bytes, void *stream);
 
 /* Softmax-attention segment of a hybrid model (LASP-2 page, abstract: LASP-2H
- * applies the same communication redesign to standard attention modules: one
+ * carries the one-gather exchange over to the softmax attention layers: one
  * gather hands every sequence-parallel rank the keys and values of every
  * position up to the end of its segment).  The queries are the LAST Tq
  * positions of a prefix of Tk >= Tq tokens (offset = Tk - Tq), attending

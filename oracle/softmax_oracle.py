@@ -3,8 +3,9 @@
 TEST INFRASTRUCTURE ONLY (see the package docstring).
 
 The hybrid variant on the LASP-2 page ("LASP-2: Rethinking Sequence
-Parallelism for Linear Attention and Its Hybrid", abstract: LASP-2H applies
-the same communication redesign to standard attention modules) gives each
+Parallelism for Linear Attention and Its Hybrid", abstract: LASP-2H carries
+the one-gather exchange over to the softmax attention layers of hybrid
+models) gives each
 sequence-parallel rank the keys and values of every earlier position by one
 gather, and the rank's queries attend causally over that prefix.  The
 standard attention module is taken in its plainest form: scaled dot-product

@@ -21,15 +21,20 @@
 // maximum by more than 8 (in log2 units): p then stays below 2^8, and O and
 // the row sum are rescaled only on those rare tiles.
 //
-// Persistent CTAs draw (query tile, sequence) items at run time, longest
-// (most key tiles) first.  Warp roles:
-//   warp 0      TMA producer (one thread): the item's Q tile, then K and V tiles
-//   warp 1      TMEM allocator and MMA issuer (one thread)
-//   warps 4..7  softmax (one thread per query row)
-//   warps 8..11 output: O / rowsum to bf16, log-sum-exp
-// Two score buffers let the product of the next key tile run while the
-// softmax of the current one is formed; two output regions let an item's
-// output be written while the next item accumulates.  Every wait is bounded.
+// Persistent CTAs draw items of two adjacent query tiles of one sequence at
+// run time, sequence by sequence (so that the keys and values of the sequences
+// in flight stay in L2) and, within a sequence, longest (most key tiles) first.
+// The two query tiles share every K and V tile and keep a score buffer and an
+// output region each, so the tensor pipe alternates between them: while the
+// softmax of one tile is formed, the other tile's products run.  Warp roles:
+//   warp 0       TMA producer (one thread): the item's two Q tiles, then K and V
+//                tiles through one ring of 32 KiB slots (K of a tile frees after
+//                both score products, V after both output products)
+//   warp 1       TMEM allocator and MMA issuer (one thread)
+//   warps 2..5   softmax and output of the first query tile, one thread per row
+//   warps 6..9   the same for the second query tile
+// (a warp reaches the TMEM lanes 32 (warp mod 4) .. +31, so each group of four
+// consecutive warps covers the 128 rows).  Every wait is bounded.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -38,17 +43,15 @@
 namespace linattn {
 namespace {
 
-constexpr int kSmThreads = 384;
-constexpr int kKvStages = 3;                               // stages of (K tile, V tile)
-constexpr uint32_t kSmOffKv = kTileBytes;                  // after the Q tile
-constexpr uint32_t kSmOffBar = kSmOffKv + kKvStages * 2 * kTileBytes;
-constexpr uint32_t kSmOffStats = kSmOffBar + 256;          // [128] row maxima, [128] row sums
-constexpr size_t kSmSmem = kSmOffStats + 1024 + 1024;      // (+ 1024: alignment of the tiles)
-static_assert(kSmSmem + 128 <= 232448, "tiles, barriers, row statistics and static shared memory fit 227 KB");
+constexpr int kSmThreads = 320;
+constexpr int kKvSlots = 5;                                // ring of K and V tiles (32 KiB each)
+constexpr uint32_t kSmOffKv = 2 * kTileBytes;              // after the two Q tiles
+constexpr uint32_t kSmOffBar = kSmOffKv + kKvSlots * kTileBytes;
+constexpr size_t kSmSmem = kSmOffBar + 256 + 1024;         // (+ 1024: alignment of the tiles)
+static_assert(kSmSmem + 128 <= 232448, "tiles, barriers and static shared memory fit 227 KB");
 
-enum { S_QFULL = 0, S_QEMPTY, S_KFULL, S_KEMPTY = S_KFULL + kKvStages, S_SFULL = S_KEMPTY + kKvStages,
-       S_PREADY = S_SFULL + 2, S_PVC = S_PREADY + 2, S_OFULL, S_OEMPTY = S_OFULL + 2, S_LFULL = S_OEMPTY + 2,
-       S_LEMPTY, S_COUNT };
+enum { S_QFULL = 0, S_QEMPTY, S_FULL, S_EMPTY = S_FULL + kKvSlots, S_SFULL = S_EMPTY + kKvSlots,
+       S_PREADY = S_SFULL + 2, S_OFULL = S_PREADY + 2, S_OEMPTY = S_OFULL + 2, S_COUNT = S_OEMPTY + 2 };
 static_assert(S_COUNT * 8 + 4 <= 256, "softmax kernel barriers and the TMEM slot fit their 256 bytes");
 
 constexpr int kRingS = 4;
@@ -75,12 +78,63 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// item -> (query tile, sequence): the query tiles with the most key tiles first
+// pairs of fp32 values in one 64-bit register: the packed FMA and add of sm_100 and later
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float &lo, float &hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// the maximum of three fp32 values in one instruction
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Whether the phases of the given parities of four mbarriers have all completed
+// (never blocks): the four tests issue back to back, so their latencies overlap.
+__device__ __forceinline__ bool mbar_test4(uint64_t *b0, int p0, uint64_t *b1, int p1, uint64_t *b2, int p2,
+                                           uint64_t *b3, int p3) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred q0, q1, q2, q3;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q0, [%1], %2;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q1, [%3], %4;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q2, [%5], %6;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q3, [%7], %8;\n\t"
+      "and.pred q0, q0, q1;\n\tand.pred q2, q2, q3;\n\tand.pred q0, q0, q2;\n\t"
+      "selp.u32 %0, 1, 0, q0;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(b0)), "r"(p0 & 1), "r"(smem_u32(b1)), "r"(p1 & 1), "r"(smem_u32(b2)), "r"(p2 & 1),
+        "r"(smem_u32(b3)), "r"(p3 & 1)
+      : "memory");
+  return ok != 0;
+}
+
+// item -> (pair of query tiles, sequence), sequence-major: the items that run at the
+// same time share one or two sequences' keys and values, which then stay in L2 (every
+// query tile of a sequence reads its whole key prefix); inside a sequence the pairs
+// with the most key tiles come first.  qt = the pair's first query tile (the second
+// is qt + 1, possibly past the end: its rows are then not stored); nt = key tiles up
+// to the second tile's diagonal (the first tile masks the extra one)
 __device__ __forceinline__ void sm_item(const SoftmaxParams &P, int item, int &qt, int &bh, int &nt) {
-  const int BH = P.B * P.H;
-  qt = P.nqt - 1 - item / BH;
-  bh = item % BH;
-  const int kend = min(P.Tk, P.off + 128 * qt + 128);  // keys up to the tile's last query
+  const int npair = (P.nqt + 1) / 2;
+  qt = 2 * (npair - 1 - item % npair);
+  bh = item / npair;
+  const int kend = min(P.Tk, P.off + 128 * qt + 256);  // keys up to the pair's last query
   nt = (kend + 127) / 128;
 }
 
@@ -113,13 +167,10 @@ __global__ void __launch_bounds__(kSmThreads, 1)
   uint8_t *smem = align1024(smem_raw);
   uint64_t *bar = reinterpret_cast<uint64_t *>(smem + kSmOffBar);
   uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + S_COUNT);
-  float *stat_m = reinterpret_cast<float *>(smem + kSmOffStats);  // [128]
-  float *stat_l = stat_m + 128;                                  // [128]
   __shared__ int abort_flag;
   __shared__ int ring_item[kRingS];
   __shared__ uint64_t ring_bar[2 * kRingS];
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int BH = P.B * P.H;
   int *const detail = P.status ? P.status + 1 + warp : nullptr;
   uint64_t *ring_full = ring_bar, *ring_empty = ring_bar + kRingS;
 
@@ -127,22 +178,19 @@ __global__ void __launch_bounds__(kSmThreads, 1)
     abort_flag = 0;
     mbar_init(&bar[S_QFULL], 1);
     mbar_init(&bar[S_QEMPTY], 1);
-    for (int s = 0; s < kKvStages; ++s) {
-      mbar_init(&bar[S_KFULL + s], 1);
-      mbar_init(&bar[S_KEMPTY + s], 1);
+    for (int s = 0; s < kKvSlots; ++s) {
+      mbar_init(&bar[S_FULL + s], 1);
+      mbar_init(&bar[S_EMPTY + s], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bar[S_SFULL + i], 1);
-      mbar_init(&bar[S_PREADY + i], 128);
-      mbar_init(&bar[S_OFULL + i], 1);
-      mbar_init(&bar[S_OEMPTY + i], 128);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&bar[S_SFULL + x], 1);
+      mbar_init(&bar[S_PREADY + x], 128);
+      mbar_init(&bar[S_OFULL + x], 1);
+      mbar_init(&bar[S_OEMPTY + x], 128);
     }
-    mbar_init(&bar[S_LFULL], 128);
-    mbar_init(&bar[S_LEMPTY], 128);
-    mbar_init(&bar[S_PVC], 1);
     for (int i = 0; i < kRingS; ++i) {
       mbar_init(&ring_full[i], 1);
-      mbar_init(&ring_empty[i], 1 + 128 + 128);  // readers: MMA thread, softmax and output groups
+      mbar_init(&ring_empty[i], 1 + 2 * 128);  // readers: MMA thread, the two softmax groups
     }
     fence_mbar_init();
     prefetch_tensormap(&mq);
@@ -157,10 +205,12 @@ __global__ void __launch_bounds__(kSmThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
-  auto tS = [&](int u) { return tmem + (uint32_t)(u & 1) * 128u; };          // score buffer of tile u
-  auto tOut = [&](int it) { return tmem + 256u + (uint32_t)(it & 1) * 128u; };  // output region of item it
-  const uint32_t sQ = smem_u32(smem);
-  auto kv_addr = [&](int kt) { return smem_u32(smem + kSmOffKv) + (uint32_t)(kt % kKvStages) * 2u * kTileBytes; };
+  // query tile x (0, 1) of an item: score buffer and output region
+  auto tS = [&](int x) { return tmem + (uint32_t)x * 128u; };
+  auto tO = [&](int x) { return tmem + 256u + (uint32_t)x * 128u; };
+  auto sQ = [&](int x) { return smem_u32(smem) + (uint32_t)x * kTileBytes; };
+  // ring slot of the i-th K/V tile loaded (K of key tile t and V of key tile t in turn)
+  auto slot_addr = [&](int i) { return smem_u32(smem + kSmOffKv) + (uint32_t)(i % kKvSlots) * kTileBytes; };
   auto wait = [&](int idx, int parity) { return mbar_wait(&bar[idx], parity & 1, &abort_flag, P.status, detail); };
   // the shared item ring: the producer draws, every other role reads in the same order
   auto take = [&](int k, int &item) {
@@ -174,8 +224,17 @@ __global__ void __launch_bounds__(kSmThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      int kt = 0, nq = 0;  // K/V tiles and Q tiles loaded
+      int li = 0, nq = 0;  // K/V tiles and Q tile pairs loaded
       bool ok = true;
+      auto load = [&](const CUtensorMap *m, int row, int h, int b) {
+        const int s = li % kKvSlots, u = li / kKvSlots;
+        if (u > 0 && !(ok = wait(S_EMPTY + s, u - 1))) return;
+        uint8_t *dst = smem + kSmOffKv + s * kTileBytes;
+        mbar_arrive_expect_tx(&bar[S_FULL + s], kTileBytes);
+        tma_load_4d(m, &bar[S_FULL + s], dst, 0, row, h, b, kPolicyEvictLast);
+        tma_load_4d(m, &bar[S_FULL + s], dst + kTileHalfBytes, 64, row, h, b, kPolicyEvictLast);
+        ++li;
+      };
       for (int k = 0;; ++k) {
         const int s = k % kRingS;
         if (k >= kRingS && !(ok = mbar_wait(&ring_empty[s], (k / kRingS - 1) & 1, &abort_flag, P.status, detail)))
@@ -188,74 +247,92 @@ __global__ void __launch_bounds__(kSmThreads, 1)
         sm_item(P, item, qt, bh, nt);
         const int b = bh / P.H, h = bh % P.H;
         if (k > 0 && !(ok = wait(S_QEMPTY, k - 1))) break;  // the previous item's products read Q
-        mbar_arrive_expect_tx(&bar[S_QFULL], kTileBytes);
-        tma_load_4d(&mq, &bar[S_QFULL], smem, 0, 128 * qt, h, b, kPolicyEvictFirst);
-        tma_load_4d(&mq, &bar[S_QFULL], smem + kTileHalfBytes, 64, 128 * qt, h, b, kPolicyEvictFirst);
+        mbar_arrive_expect_tx(&bar[S_QFULL], 2 * kTileBytes);
+        for (int q = 0; q < 2; ++q) {
+          uint8_t *dst = smem + q * kTileBytes;
+          tma_load_4d(&mq, &bar[S_QFULL], dst, 0, 128 * (qt + q), h, b, kPolicyEvictFirst);
+          tma_load_4d(&mq, &bar[S_QFULL], dst + kTileHalfBytes, 64, 128 * (qt + q), h, b, kPolicyEvictFirst);
+        }
         ++nq;
-        for (int t = 0; t < nt && ok; ++t, ++kt) {
-          const int st = kt % kKvStages, u = kt / kKvStages;
-          if (u > 0 && !(ok = wait(S_KEMPTY + st, u - 1))) break;
-          uint8_t *dst = smem + kSmOffKv + st * 2 * kTileBytes;
-          mbar_arrive_expect_tx(&bar[S_KFULL + st], 2 * kTileBytes);
-          tma_load_4d(&mk, &bar[S_KFULL + st], dst, 0, 128 * t, h, b, kPolicyEvictLast);
-          tma_load_4d(&mk, &bar[S_KFULL + st], dst + kTileHalfBytes, 64, 128 * t, h, b, kPolicyEvictLast);
-          tma_load_4d(&mv, &bar[S_KFULL + st], dst + kTileBytes, 0, 128 * t, h, b, kPolicyEvictLast);
-          tma_load_4d(&mv, &bar[S_KFULL + st], dst + kTileBytes + kTileHalfBytes, 64, 128 * t, h, b,
-                      kPolicyEvictLast);
+        for (int t = 0; t < nt && ok; ++t) {
+          load(&mk, 128 * t, h, b);
+          if (ok) load(&mv, 128 * t, h, b);
         }
         if (!ok) break;
       }
       // time-bounded drain of the loads in flight (also after an abort)
       volatile int no_abort = 0;
       if (nq > 0) mbar_wait(&bar[S_QFULL], (nq - 1) & 1, &no_abort, P.status);
-      for (int st = 0; st < kKvStages; ++st) {
-        const int uses = kt > st ? (kt - 1 - st) / kKvStages + 1 : 0;
-        if (uses > 0) mbar_wait(&bar[S_KFULL + st], (uses - 1) & 1, &no_abort, P.status);
+      for (int s = 0; s < kKvSlots; ++s) {
+        const int uses = li > s ? (li - 1 - s) / kKvSlots + 1 : 0;
+        if (uses > 0) mbar_wait(&bar[S_FULL + s], (uses - 1) & 1, &no_abort, P.status);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // Per key tile t, for the item's two query tiles in turn: O_x += P_x V_t (once the
+    // softmax of x is done), then S_x = Q_x K_{t+1}^T -- so each tile's next scores are
+    // issued right behind its output product, while the other tile's softmax runs.
     if (lane == 0) {
       const uint32_t id_qk = idesc_bf16(128, 128, false, false);  // Q K^T
       const uint32_t id_pv = idesc_bf16(128, 128, false, true);   // P V (P from TMEM)
-      int kt = 0, u = 0;
+      int li = 0, u = 0;  // K/V tiles consumed in load order; key tiles (both query tiles in step)
       bool ok = true;
+      auto qk = [&](int x, int ik) {
+        const uint32_t K = slot_addr(ik);
+#pragma unroll
+        for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tS(x), desc_kmajor(sQ(x), ks), desc_kmajor(K, ks), id_qk, ks > 0);
+        mma_commit(&bar[S_SFULL + x]);
+      };
       for (int k = 0, item; ok; ++k) {
         if (!(ok = take(k, item)) || item < 0) break;
         int qt, bh, nt;
         sm_item(P, item, qt, bh, nt);
-        const uint32_t tO = tOut(k);
-        // O += P V for the tile at counters (u0, kt0), the item's t0-th
-        auto pv = [&](int u0, int kt0, int t0) {
-          if (!(ok = wait(S_PREADY + (u0 & 1), u0 >> 1))) return;
-          if (t0 == 0 && k >= 2 && !(ok = wait(S_OEMPTY + (k & 1), (k >> 1) - 1))) return;
-          tc_fence_after();
-          const uint32_t V = kv_addr(kt0) + kTileBytes;
+        if (!(ok = wait(S_QFULL, k) && wait(S_FULL + li % kKvSlots, li / kKvSlots))) break;
+        tc_fence_after();
+        qk(0, li);
+        qk(1, li);
+        mma_commit(&bar[S_EMPTY + li % kKvSlots]);
+        if (nt == 1) mma_commit(&bar[S_QEMPTY]);
+        for (int t = 0; t < nt && ok; ++t, ++u, li += 2) {
+          const int iv = li + 1, ik1 = li + 2;  // V of this tile, K of the next
+          for (int x = 0; x < 2 && ok; ++x) {
+            // everything the two products of tile x need: its probabilities, its output region
+            // (first key tile of an item), V of this key tile, K of the next; tested together,
+            // then waited for one by one only when one of them is not yet there
+            const bool first = t == 0 && k > 0, more = t + 1 < nt;
+            const bool ready = mbar_test4(&bar[S_PREADY + x], u, &bar[first ? S_OEMPTY + x : S_PREADY + x],
+                                          first ? k - 1 : u, &bar[S_FULL + iv % kKvSlots], iv / kKvSlots,
+                                          &bar[S_FULL + (more ? ik1 : iv) % kKvSlots], (more ? ik1 : iv) / kKvSlots);
+            if (!ready && !(ok = wait(S_PREADY + x, u) && (!first || wait(S_OEMPTY + x, k - 1)) &&
+                                 wait(S_FULL + iv % kKvSlots, iv / kKvSlots)))
+              break;
+            tc_fence_after();
+            const uint32_t V = slot_addr(iv);
 #pragma unroll
-          for (uint32_t ks = 0; ks < 8; ++ks)
-            mma_ts(tO, tS(u0) + ks * 8, desc_mnmajor(V, ks), id_pv, (t0 > 0 || ks > 0) ? 1u : 0u);
-          mma_commit(&bar[S_KEMPTY + kt0 % kKvStages]);
-          mma_commit(&bar[S_PVC]);
-        };
-        if (!(ok = wait(S_QFULL, k))) break;
-        for (int t = 0; t < nt && ok; ++t, ++kt, ++u) {
-          if (!(ok = wait(S_KFULL + kt % kKvStages, kt / kKvStages))) break;
-          tc_fence_after();
-          const uint32_t K = kv_addr(kt);
-#pragma unroll
-          for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tS(u), desc_kmajor(sQ, ks), desc_kmajor(K, ks), id_qk, ks > 0);
-          mma_commit(&bar[S_SFULL + (u & 1)]);
-          if (t + 1 == nt) mma_commit(&bar[S_QEMPTY]);
-          if (t > 0) pv(u - 1, kt - 1, t - 1);  // the previous tile's softmax overlapped this product
+            for (uint32_t ks = 0; ks < 8; ++ks)
+              mma_ts(tO(x), tS(x) + ks * 8, desc_mnmajor(V, ks), id_pv, (t > 0 || ks > 0) ? 1u : 0u);
+            if (t + 1 == nt) mma_commit(&bar[S_OFULL + x]);
+            if (x == 1) mma_commit(&bar[S_EMPTY + iv % kKvSlots]);
+            if (more) {
+              if (!ready) {
+                if (!(ok = wait(S_FULL + ik1 % kKvSlots, ik1 / kKvSlots))) break;
+                tc_fence_after();
+              }
+              qk(x, ik1);
+              if (x == 1) {
+                mma_commit(&bar[S_EMPTY + ik1 % kKvSlots]);
+                if (t + 2 == nt) mma_commit(&bar[S_QEMPTY]);
+              }
+            }
+          }
         }
-        if (!ok) break;
-        pv(u - 1, kt - 1, nt - 1);
-        if (!ok) break;
-        mma_commit(&bar[S_OFULL + (k & 1)]);
       }
     }
-  } else if (warp >= 4 && warp < 8) {
-    // ------------------------------------------------------------ softmax: one query row per thread
+  } else if (warp >= 2 && warp < 10) {
+    // ------------------------------------------------------------ softmax and output of query tile x:
+    // one query row per thread
+    const int x = (warp - 2) >> 2;
     const uint32_t quad = warp & 3, row = quad * 32 + lane, lb = (quad * 32) << 16;
     int u = 0;
     bool ok = true;
@@ -263,21 +340,33 @@ __global__ void __launch_bounds__(kSmThreads, 1)
       if (!(ok = __all_sync(0xffffffffu, take(k, item))) || item < 0) break;
       int qt, bh, nt;
       sm_item(P, item, qt, bh, nt);
-      const int qabs = P.off + 128 * qt + (int)row;  // this row's query position in the prefix
-      const uint32_t tO = tOut(k);
+      const int qtile = qt + x;
+      const int qabs = P.off + 128 * qtile + (int)row;  // this row's query position in the prefix
       float m_ref = -INFINITY, l = 0.f;
       for (int t = 0; t < nt; ++t, ++u) {
-        if (!(ok = __all_sync(0xffffffffu, wait(S_SFULL + (u & 1), u >> 1)))) break;
+        if (!(ok = __all_sync(0xffffffffu, wait(S_SFULL + x, u)))) break;
         tc_fence_after();
-        // the tile's scaled, masked row maximum (all four loads in flight at once; the
-        // scores are read again below)
-        float mt = -INFINITY;
-        const int kmax = qabs - 128 * t;  // the last key column this row may see
-        {
-          uint32_t r[4][32];
+        // the row's 128 scores (all four loads in flight) and their masked maximum
+        uint32_t r[4][32];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) tmem_ld32(tS(u) + lb + c * 32, r[c]);
-          tmem_ld_wait();
+        for (int c = 0; c < 4; ++c) tmem_ld32(tS(x) + lb + 32 * c, r[c]);
+        tmem_ld_wait();
+        const int kmax = qabs - 128 * t;  // the last key column this row may see
+        // every column is visible to every row of the warp (the warp's first row sees them all)
+        const bool full = __shfl_sync(0xffffffffu, kmax, 0) >= 127;
+        float mt;
+        if (full) {
+          float mc[4];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            mc[c] = __uint_as_float(r[c][0]);
+#pragma unroll
+            for (int j = 1; j < 31; j += 2) mc[c] = max3(mc[c], __uint_as_float(r[c][j]), __uint_as_float(r[c][j + 1]));
+            mc[c] = fmaxf(mc[c], __uint_as_float(r[c][31]));
+          }
+          mt = max3(fmaxf(mc[0], mc[1]), mc[2], mc[3]);
+        } else {
+          mt = -INFINITY;
 #pragma unroll
           for (int c = 0; c < 4; ++c)
 #pragma unroll
@@ -285,90 +374,80 @@ __global__ void __launch_bounds__(kSmThreads, 1)
               if (32 * c + j <= kmax) mt = fmaxf(mt, __uint_as_float(r[c][j]));
         }
         mt *= P.scale_log2;
-        // move the reference maximum only when this tile raises the row's maximum by more than 8
+        // move the reference maximum only when this tile raises the row's maximum by more
+        // than 8; O and the row sum are then scaled by f
         const bool move = t == 0 || mt > m_ref + 8.f;
+        const float f = t > 0 && move ? ex2(m_ref - mt) : 1.f;
+        if (move) m_ref = mt;
+        l *= f;
+        // p = exp2(scale log2(e) s - m_ref), 0 past the diagonal, as bf16 pairs: chunk c goes
+        // to columns 16c .. 16c+15 (every score already in registers).  Pairs of scores go
+        // through the packed fp32 FMA and add; the row sum keeps two packed partial sums.
+        const uint64_t sc2 = f2_pack(P.scale_log2, P.scale_log2), nm2 = f2_pack(-m_ref, -m_ref);
+        uint64_t l2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t w[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            float p0, p1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(r[c][2 * j]), __uint_as_float(r[c][2 * j + 1])), sc2, nm2), p0, p1);
+            p0 = ex2(p0);
+            p1 = ex2(p1);
+            if (!full) {
+              const int j0 = 32 * c + 2 * j;
+              p0 = j0 <= kmax ? p0 : 0.f;
+              p1 = j0 + 1 <= kmax ? p1 : 0.f;
+            }
+            l2[j & 1] = f2_add(l2[j & 1], f2_pack(p0, p1));
+            w[j] = pack_bf16(p0, p1);
+          }
+          tmem_st16(tS(x) + lb + 16 * c, w);
+        }
+        {
+          float a0, a1, b0, b1;
+          f2_unpack(l2[0], a0, a1);
+          f2_unpack(l2[1], b0, b1);
+          l += (a0 + a1) + (b0 + b1);
+        }
+        // the rescale of O: the output product of the previous key tile is complete (it
+        // was issued before this tile's score product), this tile's is not yet issued
         if (t > 0 && __any_sync(0xffffffffu, move)) {
-          // rescale this warp's rows of O (the previous tile's product must be done)
-          if (!(ok = __all_sync(0xffffffffu, wait(S_PVC, u - 1)))) break;
-          tc_fence_after();
-          const float f = move ? ex2(m_ref - mt) : 1.f;
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
-            uint32_t r[32];
-            tmem_ld32(tO + lb + c * 32, r);
+            uint32_t o[32];
+            tmem_ld32(tO(x) + lb + 32 * c, o);
             tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * f);
-            tmem_st32(tO + lb + c * 32, r);
-          }
-          tmem_st_wait();
-          l *= f;
-        }
-        if (move) m_ref = mt;
-        // p = exp2(scale log2(e) s - m_ref), 0 past the diagonal, as bf16 pairs: chunk c goes to
-        // columns 16c..16c+15, which hold scores this pass has already read
-#pragma unroll 1
-        for (int c2 = 0; c2 < 4; c2 += 2) {
-          uint32_t r[2][32];
-          tmem_ld32(tS(u) + lb + c2 * 32, r[0]);
-          tmem_ld32(tS(u) + lb + c2 * 32 + 32, r[1]);
-          tmem_ld_wait();
-#pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) {
-            const int c = c2 + h2;
-            uint32_t w[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int j0 = 32 * c + 2 * j;
-              const float p0 = j0 <= kmax ? ex2(fmaf(__uint_as_float(r[h2][2 * j]), P.scale_log2, -m_ref)) : 0.f;
-              const float p1 = j0 + 1 <= kmax ? ex2(fmaf(__uint_as_float(r[h2][2 * j + 1]), P.scale_log2, -m_ref)) : 0.f;
-              l += p0 + p1;
-              w[j] = pack_bf16(p0, p1);
-            }
-            tmem_st16(tS(u) + lb + c * 16, w);
+            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * f);
+            tmem_st32(tO(x) + lb + 32 * c, o);
           }
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&bar[S_PREADY + (u & 1)]);
+        mbar_arrive(&bar[S_PREADY + x]);
       }
       if (!ok) break;
-      // hand the row's maximum and sum to the output group (which has read the previous item's)
-      if (k >= 1 && !(ok = __all_sync(0xffffffffu, wait(S_LEMPTY, k - 1)))) break;
-      stat_m[row] = m_ref;
-      stat_l[row] = l;
-      mbar_arrive(&bar[S_LFULL]);
-    }
-  } else if (warp >= 8) {
-    // ------------------------------------------------------------ output: O / rowsum, log-sum-exp
-    const uint32_t quad = warp & 3, row = quad * 32 + lane, lb = (quad * 32) << 16;
-    bool ok = true;
-    for (int k = 0, item; ok; ++k) {
-      if (!(ok = __all_sync(0xffffffffu, take(k, item))) || item < 0) break;
-      int qt, bh, nt;
-      sm_item(P, item, qt, bh, nt);
-      const int b = bh / P.H, h = bh % P.H, qrow = 128 * qt + (int)row;
-      const uint32_t tO = tOut(k);
-      if (!(ok = __all_sync(0xffffffffu, wait(S_OFULL + (k & 1), k >> 1) && wait(S_LFULL, k)))) break;
+      // output: O / rowsum as bf16, the log-sum-exp; then the region is free for the next item
+      if (!(ok = __all_sync(0xffffffffu, wait(S_OFULL + x, k)))) break;
       tc_fence_after();
-      const float m = stat_m[row], l = stat_l[row];
-      mbar_arrive(&bar[S_LEMPTY]);
+      const int b = bh / P.H, h = bh % P.H;
       const float inv = 1.f / l;
-      const bool valid = qrow < P.Tq;
-      __nv_bfloat16 *dst = P.o + (int64_t)b * P.osb + (int64_t)h * P.osh + (int64_t)qrow * P.ost;
+      const bool valid = qtile * 128 + (int)row < P.Tq;
+      __nv_bfloat16 *dst = P.o + (int64_t)b * P.osb + (int64_t)h * P.osh + (int64_t)(qtile * 128 + (int)row) * P.ost;
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
-        float x[32];
-        uint32_t r[32];
-        tmem_ld32(tO + lb + c * 32, r);
+        float y[32];
+        uint32_t o[32];
+        tmem_ld32(tO(x) + lb + c * 32, o);
         tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]) * inv;
-        if (valid) st_row_chunk(dst + 32 * c, x, P.wide != 0);
+        for (int j = 0; j < 32; ++j) y[j] = __uint_as_float(o[j]) * inv;
+        if (valid) st_row_chunk(dst + 32 * c, y, P.wide != 0);
       }
-      if (valid && P.lse) P.lse[(int64_t)bh * P.Tq + qrow] = (m + log2f(l)) * 0.6931471805599453f;
+      if (valid && P.lse) P.lse[(int64_t)bh * P.Tq + qtile * 128 + row] = (m_ref + log2f(l)) * 0.6931471805599453f;
       tc_fence_before();
-      mbar_arrive(&bar[S_OEMPTY + (k & 1)]);
+      mbar_arrive(&bar[S_OEMPTY + x]);
     }
   }
   tc_fence_before();
@@ -400,7 +479,7 @@ cudaError_t softmax_segment(const SoftmaxProblem &p, const void *q, const void *
   SoftmaxParams S;
   S.B = p.B; S.H = p.H; S.Tq = p.Tq; S.Tk = p.Tk; S.off = p.Tk - p.Tq;
   S.nqt = (p.Tq + 127) / 128;
-  S.nitems = S.nqt * p.B * p.H;
+  S.nitems = (S.nqt + 1) / 2 * p.B * p.H;
   S.scale_log2 = p.scale * 1.4426950408889634f;
   S.o = static_cast<__nv_bfloat16 *>(o);
   S.osb = p.qsb; S.osh = p.qsh; S.ost = p.qst;

@@ -30,7 +30,8 @@
 //   warp 0       TMA producer (one thread): the item's two Q tiles, then K and V
 //                tiles through one ring of 32 KiB slots (K of a tile frees after
 //                both score products, V after both output products)
-//   warp 1       TMEM allocator and MMA issuer (one thread)
+//   warp 1       TMEM allocator and MMA issuer (the whole warp; one elected lane
+//                issues each product)
 //   warps 2..5   softmax and output of the first query tile, one thread per row
 //   warps 6..9   the same for the second query tile
 // (a warp reaches the TMEM lanes 32 (warp mod 4) .. +31, so each group of four
@@ -190,7 +191,7 @@ __global__ void __launch_bounds__(kSmThreads, 1)
     }
     for (int i = 0; i < kRingS; ++i) {
       mbar_init(&ring_full[i], 1);
-      mbar_init(&ring_empty[i], 1 + 2 * 128);  // readers: MMA thread, the two softmax groups
+      mbar_init(&ring_empty[i], 32 + 2 * 128);  // readers: the MMA warp, the two softmax groups
     }
     fence_mbar_init();
     prefetch_tensormap(&mq);
@@ -273,27 +274,30 @@ __global__ void __launch_bounds__(kSmThreads, 1)
     // Per key tile t, for the item's two query tiles in turn: O_x += P_x V_t (once the
     // softmax of x is done), then S_x = Q_x K_{t+1}^T -- so each tile's next scores are
     // issued right behind its output product, while the other tile's softmax runs.
-    if (lane == 0) {
+    // The whole warp runs this loop (one elected lane issues each product).
+    {
       const uint32_t id_qk = idesc_bf16(128, 128, false, false);  // Q K^T
       const uint32_t id_pv = idesc_bf16(128, 128, false, true);   // P V (P from TMEM)
       int li = 0, u = 0;  // K/V tiles consumed in load order; key tiles (both query tiles in step)
       bool ok = true;
+      auto wait_all = [&](int idx, int parity) { return __all_sync(0xffffffffu, wait(idx, parity)); };
       auto qk = [&](int x, int ik) {
         const uint32_t K = slot_addr(ik);
 #pragma unroll
-        for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tS(x), desc_kmajor(sQ(x), ks), desc_kmajor(K, ks), id_qk, ks > 0);
-        mma_commit(&bar[S_SFULL + x]);
+        for (uint32_t ks = 0; ks < 8; ++ks)
+          mma_ss_warp(tS(x), desc_kmajor(sQ(x), ks), desc_kmajor(K, ks), id_qk, ks > 0);
+        mma_commit_warp(&bar[S_SFULL + x]);
       };
       for (int k = 0, item; ok; ++k) {
-        if (!(ok = take(k, item)) || item < 0) break;
+        if (!(ok = __all_sync(0xffffffffu, take(k, item))) || item < 0) break;
         int qt, bh, nt;
         sm_item(P, item, qt, bh, nt);
-        if (!(ok = wait(S_QFULL, k) && wait(S_FULL + li % kKvSlots, li / kKvSlots))) break;
+        if (!(ok = wait_all(S_QFULL, k) && wait_all(S_FULL + li % kKvSlots, li / kKvSlots))) break;
         tc_fence_after();
         qk(0, li);
         qk(1, li);
-        mma_commit(&bar[S_EMPTY + li % kKvSlots]);
-        if (nt == 1) mma_commit(&bar[S_QEMPTY]);
+        mma_commit_warp(&bar[S_EMPTY + li % kKvSlots]);
+        if (nt == 1) mma_commit_warp(&bar[S_QEMPTY]);
         for (int t = 0; t < nt && ok; ++t, ++u, li += 2) {
           const int iv = li + 1, ik1 = li + 2;  // V of this tile, K of the next
           for (int x = 0; x < 2 && ok; ++x) {
@@ -301,28 +305,29 @@ __global__ void __launch_bounds__(kSmThreads, 1)
             // (first key tile of an item), V of this key tile, K of the next; tested together,
             // then waited for one by one only when one of them is not yet there
             const bool first = t == 0 && k > 0, more = t + 1 < nt;
-            const bool ready = mbar_test4(&bar[S_PREADY + x], u, &bar[first ? S_OEMPTY + x : S_PREADY + x],
-                                          first ? k - 1 : u, &bar[S_FULL + iv % kKvSlots], iv / kKvSlots,
-                                          &bar[S_FULL + (more ? ik1 : iv) % kKvSlots], (more ? ik1 : iv) / kKvSlots);
-            if (!ready && !(ok = wait(S_PREADY + x, u) && (!first || wait(S_OEMPTY + x, k - 1)) &&
-                                 wait(S_FULL + iv % kKvSlots, iv / kKvSlots)))
+            const bool ready = __all_sync(
+                0xffffffffu, mbar_test4(&bar[S_PREADY + x], u, &bar[first ? S_OEMPTY + x : S_PREADY + x],
+                                        first ? k - 1 : u, &bar[S_FULL + iv % kKvSlots], iv / kKvSlots,
+                                        &bar[S_FULL + (more ? ik1 : iv) % kKvSlots], (more ? ik1 : iv) / kKvSlots));
+            if (!ready && !(ok = wait_all(S_PREADY + x, u) && (!first || wait_all(S_OEMPTY + x, k - 1)) &&
+                                 wait_all(S_FULL + iv % kKvSlots, iv / kKvSlots)))
               break;
             tc_fence_after();
             const uint32_t V = slot_addr(iv);
 #pragma unroll
             for (uint32_t ks = 0; ks < 8; ++ks)
-              mma_ts(tO(x), tS(x) + ks * 8, desc_mnmajor(V, ks), id_pv, (t > 0 || ks > 0) ? 1u : 0u);
-            if (t + 1 == nt) mma_commit(&bar[S_OFULL + x]);
-            if (x == 1) mma_commit(&bar[S_EMPTY + iv % kKvSlots]);
+              mma_ts_warp(tO(x), tS(x) + ks * 8, desc_mnmajor(V, ks), id_pv, (t > 0 || ks > 0) ? 1u : 0u);
+            if (t + 1 == nt) mma_commit_warp(&bar[S_OFULL + x]);
+            if (x == 1) mma_commit_warp(&bar[S_EMPTY + iv % kKvSlots]);
             if (more) {
               if (!ready) {
-                if (!(ok = wait(S_FULL + ik1 % kKvSlots, ik1 / kKvSlots))) break;
+                if (!(ok = wait_all(S_FULL + ik1 % kKvSlots, ik1 / kKvSlots))) break;
                 tc_fence_after();
               }
               qk(x, ik1);
               if (x == 1) {
-                mma_commit(&bar[S_EMPTY + ik1 % kKvSlots]);
-                if (t + 2 == nt) mma_commit(&bar[S_QEMPTY]);
+                mma_commit_warp(&bar[S_EMPTY + ik1 % kKvSlots]);
+                if (t + 2 == nt) mma_commit_warp(&bar[S_QEMPTY]);
               }
             }
           }

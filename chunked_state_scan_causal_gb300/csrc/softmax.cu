@@ -125,6 +125,63 @@ __device__ __forceinline__ bool mbar_test4(uint64_t *b0, int p0, uint64_t *b1, i
   return ok != 0;
 }
 
+// The row's maximum over the 128 scores of a tile (all visible), and over the
+// columns up to kmax.
+__device__ __forceinline__ float row_max(const uint32_t (&r)[4][32]) {
+  float mc[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    mc[c] = __uint_as_float(r[c][0]);
+#pragma unroll
+    for (int j = 1; j < 31; j += 2) mc[c] = max3(mc[c], __uint_as_float(r[c][j]), __uint_as_float(r[c][j + 1]));
+    mc[c] = fmaxf(mc[c], __uint_as_float(r[c][31]));
+  }
+  return max3(fmaxf(mc[0], mc[1]), mc[2], mc[3]);
+}
+__device__ __forceinline__ float row_max_masked(const uint32_t (&r)[4][32], int kmax) {
+  float m = -INFINITY;
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (32 * c + j <= kmax) m = fmaxf(m, __uint_as_float(r[c][j]));
+  return m;
+}
+
+// p = exp2(cs - m) of the row's 128 scores s (0 past column kmax when MASKED), written
+// as bf16 pairs into the first 64 columns of the score buffer at taddr (chunk c of 32
+// scores to columns 16c .. 16c+15); returns the row's sum of p.  Pairs of scores go
+// through the packed fp32 FMA and add; the sum keeps two packed partial sums.
+template <bool MASKED>
+__device__ __forceinline__ float probs_to_tmem(const uint32_t (&r)[4][32], float c, float m, int kmax,
+                                               uint32_t taddr) {
+  const uint64_t c2 = f2_pack(c, c), nm2 = f2_pack(-m, -m);
+  uint64_t l2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t w[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      float p0, p1;
+      f2_unpack(f2_fma(f2_pack(__uint_as_float(r[q][2 * j]), __uint_as_float(r[q][2 * j + 1])), c2, nm2), p0, p1);
+      p0 = ex2(p0);
+      p1 = ex2(p1);
+      if (MASKED) {
+        const int j0 = 32 * q + 2 * j;
+        p0 = j0 <= kmax ? p0 : 0.f;
+        p1 = j0 + 1 <= kmax ? p1 : 0.f;
+      }
+      l2[j & 1] = f2_add(l2[j & 1], f2_pack(p0, p1));
+      w[j] = pack_bf16(p0, p1);
+    }
+    tmem_st16(taddr + 16 * q, w);
+  }
+  float a0, a1, b0, b1;
+  f2_unpack(l2[0], a0, a1);
+  f2_unpack(l2[1], b0, b1);
+  return (a0 + a1) + (b0 + b1);
+}
+
 // item -> (pair of query tiles, sequence), sequence-major: the items that run at the
 // same time share one or two sequences' keys and values, which then stay in L2 (every
 // query tile of a sequence reads its whole key prefix); inside a sequence the pairs
@@ -359,62 +416,28 @@ __global__ void __launch_bounds__(kSmThreads, 1)
         const int kmax = qabs - 128 * t;  // the last key column this row may see
         // every column is visible to every row of the warp (the warp's first row sees them all)
         const bool full = __shfl_sync(0xffffffffu, kmax, 0) >= 127;
-        float mt;
-        if (full) {
-          float mc[4];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            mc[c] = __uint_as_float(r[c][0]);
-#pragma unroll
-            for (int j = 1; j < 31; j += 2) mc[c] = max3(mc[c], __uint_as_float(r[c][j]), __uint_as_float(r[c][j + 1]));
-            mc[c] = fmaxf(mc[c], __uint_as_float(r[c][31]));
-          }
-          mt = max3(fmaxf(mc[0], mc[1]), mc[2], mc[3]);
-        } else {
-          mt = -INFINITY;
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (32 * c + j <= kmax) mt = fmaxf(mt, __uint_as_float(r[c][j]));
+        // Past the first key tile, the probabilities are formed with the current reference
+        // maximum first: every p of the tile is at most the tile's sum, so a sum of at most
+        // 2^8 shows that the tile does not raise the row's maximum by more than 8, and the
+        // reference stays.  Only otherwise is the tile's maximum taken and the tile redone.
+        bool fast = t > 0 && full, move = false;
+        float f = 1.f, s_tile = 0.f;
+        if (fast) {
+          s_tile = probs_to_tmem<false>(r, P.scale_log2, m_ref, kmax, tS(x) + lb);
+          fast = !__any_sync(0xffffffffu, s_tile > 256.f);
+          if (!fast) tmem_st_wait();  // overwritten below
         }
-        mt *= P.scale_log2;
-        // move the reference maximum only when this tile raises the row's maximum by more
-        // than 8; O and the row sum are then scaled by f
-        const bool move = t == 0 || mt > m_ref + 8.f;
-        const float f = t > 0 && move ? ex2(m_ref - mt) : 1.f;
-        if (move) m_ref = mt;
-        l *= f;
-        // p = exp2(scale log2(e) s - m_ref), 0 past the diagonal, as bf16 pairs: chunk c goes
-        // to columns 16c .. 16c+15 (every score already in registers).  Pairs of scores go
-        // through the packed fp32 FMA and add; the row sum keeps two packed partial sums.
-        const uint64_t sc2 = f2_pack(P.scale_log2, P.scale_log2), nm2 = f2_pack(-m_ref, -m_ref);
-        uint64_t l2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t w[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            float p0, p1;
-            f2_unpack(f2_fma(f2_pack(__uint_as_float(r[c][2 * j]), __uint_as_float(r[c][2 * j + 1])), sc2, nm2), p0, p1);
-            p0 = ex2(p0);
-            p1 = ex2(p1);
-            if (!full) {
-              const int j0 = 32 * c + 2 * j;
-              p0 = j0 <= kmax ? p0 : 0.f;
-              p1 = j0 + 1 <= kmax ? p1 : 0.f;
-            }
-            l2[j & 1] = f2_add(l2[j & 1], f2_pack(p0, p1));
-            w[j] = pack_bf16(p0, p1);
-          }
-          tmem_st16(tS(x) + lb + 16 * c, w);
+        if (!fast) {
+          const float mt = (full ? row_max(r) : row_max_masked(r, kmax)) * P.scale_log2;
+          // move the reference maximum only when this tile raises the row's maximum by more
+          // than 8; O and the row sum are then scaled by f
+          move = t == 0 || mt > m_ref + 8.f;
+          f = t > 0 && move ? ex2(m_ref - mt) : 1.f;
+          if (move) m_ref = mt;
+          s_tile = full ? probs_to_tmem<false>(r, P.scale_log2, m_ref, kmax, tS(x) + lb)
+                        : probs_to_tmem<true>(r, P.scale_log2, m_ref, kmax, tS(x) + lb);
         }
-        {
-          float a0, a1, b0, b1;
-          f2_unpack(l2[0], a0, a1);
-          f2_unpack(l2[1], b0, b1);
-          l += (a0 + a1) + (b0 + b1);
-        }
+        l = l * f + s_tile;
         // the rescale of O: the output product of the previous key tile is complete (it
         // was issued before this tile's score product), this tile's is not yet issued
         if (t > 0 && __any_sync(0xffffffffu, move)) {

@@ -93,3 +93,20 @@ def test_softmax_segment_empty_queries():
     o, lse = la.softmax_segment_fwd(q, k, k, want_lse=True)
     torch.cuda.synchronize()
     assert o.numel() == 0 and lse.numel() == 0
+
+
+def test_softmax_segment_tile_sums_above_256_with_and_without_a_new_maximum():
+    """Scores built along one direction: the first key tile scores near 0, the next
+    tiles 3 log2-units higher (each tile's probabilities sum to ~2^10 > 2^8 while its
+    maximum stays within 8 of the reference), then tiles 11 units higher (the
+    reference maximum moves)."""
+    g = torch.Generator().manual_seed(11)
+    Tq, Tk = 256, 1024
+    c = 3.0 * math.sqrt(128) / math.log2(math.e)          # score 3 (log2 units) at scale 1/sqrt(128)
+    q = torch.randn(1, 1, Tq, 128, generator=g) * 0.01
+    q[..., 0] = 1.0
+    k = torch.randn(1, 1, Tk, 128, generator=g) * 0.01
+    k[..., 128:640, 0] = c
+    k[..., 640:, 0] = c * 11.0 / 3.0
+    v = torch.randn(1, 1, Tk, 128, generator=g)
+    check(*(x.to(torch.bfloat16) for x in (q, k, v)))

@@ -107,6 +107,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
   }
 }
 
+// mbar_wait by every lane of a warp, with one verdict for the whole warp.
+__device__ __forceinline__ bool mbar_wait_w(uint64_t *bar, uint32_t parity, volatile int *abort_flag, int *status,
+                                            int *detail = nullptr) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, status, detail));
+}
+
 // ----------------------------------------------------------------------------- global flags
 __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p) {
   unsigned v;

@@ -3,7 +3,8 @@
 // The kernels are persistent (one CTA per SM; (group, sequence) items drawn
 // at run time, see ItemRing) and warp-specialised:
 //   warp 0        TMA producer and item drawer (one thread)
-//   warp 1        TMEM allocator and MMA issuer (one thread)
+//   warp 1        TMEM allocator and MMA issuer (the whole warp runs the issue
+//                 loop, one elected lane issues each product; see mma_ss_warp)
 //   warps 4..7    epilogue group A (TMEM -> registers -> shared / global)
 //   warps 8..11   epilogue group B
 // Every wait is a bounded mbarrier wait (see ptx.cuh); a timeout records an
@@ -234,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&accf[a], 1);
       mbar_init(&acce[a], 128);
     }
-    ring_init(ring, 1 + (DECAY ? 128 : 0) + 128);  // readers: MMA thread, scaling warps, store warps
+    ring_init(ring, 32 + (DECAY ? 128 : 0) + 128);  // readers: MMA warp, scaling warps, store warps
     fence_mbar_init();
     prefetch_tensormap(&mx);
     prefetch_tensormap(&my);
@@ -278,32 +279,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    {  // the whole warp: one elected lane issues each product
       int it = 0, ai = 0;
       bool ok = true;
       const uint32_t idesc = idesc_bf16(128, 128, true, true);
       for (int k = 0, item; ok; ++k) {
-        if (!(ok = ring_take(ring, k, item, &abort_flag, P.status, detail)) || item < 0) break;
+        if (!(ok = __all_sync(0xffffffffu, ring_take(ring, k, item, &abort_flag, P.status, detail))) || item < 0) break;
         const int g = item / BH;
         const int s0 = P.gp.start(g), s1 = min(P.T, P.gp.start(g + 1));
         const int a = ai & 1, ua = ai >> 1;
-        if (ua > 0 && !(ok = mbar_wait(&acce[a], (ua - 1) & 1, &abort_flag, P.status, detail))) break;
+        if (ua > 0 && !(ok = mbar_wait_w(&acce[a], (ua - 1) & 1, &abort_flag, P.status, detail))) break;
         tc_fence_after();
         const uint32_t dt = tmem + a * 128;
         bool first = true;
         for (int t0 = s0; t0 < s1; t0 += 128, ++it) {
           const int s = it % NS, u = it / NS;
-          if (!(ok = mbar_wait(DECAY ? &scaled[s] : &full[s], u & 1, &abort_flag, P.status, detail))) break;
+          if (!(ok = mbar_wait_w(DECAY ? &scaled[s] : &full[s], u & 1, &abort_flag, P.status, detail))) break;
           tc_fence_after();
           const uint32_t xs = smem_u32(smem + s * kStage), ys = xs + kTileBytes;
 #pragma unroll
           for (uint32_t ks = 0; ks < 8; ++ks)
-            mma_ss(dt, desc_mnmajor(xs, ks), desc_mnmajor(ys, ks), idesc, (first && ks == 0) ? 0u : 1u);
+            mma_ss_warp(dt, desc_mnmajor(xs, ks), desc_mnmajor(ys, ks), idesc, (first && ks == 0) ? 0u : 1u);
           first = false;
-          mma_commit(&empty[s]);
+          mma_commit_warp(&empty[s]);
         }
         if (!ok) break;
-        mma_commit(&accf[a]);
+        mma_commit_warp(&accf[a]);
         ++ai;
       }
     }
@@ -411,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(crd, 128);
     mbar_init(cmma, 1);
-    ring_init(ring, 1 + (DECAY ? 128 : 0) + 128);  // readers: MMA thread, weighting warps, state warps
+    ring_init(ring, 32 + (DECAY ? 128 : 0) + 128);  // readers: MMA warp, weighting warps, state warps
     fence_mbar_init();
     prefetch_tensormap(&mk);
     prefetch_tensormap(&mv);
@@ -459,38 +460,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer: one half-tile product per chunk
-    if (lane == 0) {
+    {  // the whole warp: one elected lane issues each product
       const uint32_t idesc = idesc_bf16(128, 128, true, true);
       int it = 0, ck = 0;  // blocks and chunks seen by this CTA
       bool ok = true;
       for (int k = 0, item; ok; ++k) {
-        if (!(ok = ring_take(ring, k, item, &abort_flag, P.status, detail)) || item < 0) break;
+        if (!(ok = __all_sync(0xffffffffu, ring_take(ring, k, item, &abort_flag, P.status, detail))) || item < 0) break;
         int s0, s1;
         range(item, s0, s1);
         const int nc = (s1 - s0 + 63) / 64;
         for (int c = 0; c < nc && ok; ++c, ++ck) {
           const int s = it % NS, u = it / NS;
           // the chunk's entering state has been read out (and decayed) from TMEM
-          if (!(ok = mbar_wait(crd, ck & 1, &abort_flag, P.status, detail))) break;
+          if (!(ok = mbar_wait_w(crd, ck & 1, &abort_flag, P.status, detail))) break;
           if (c + 1 < nc) {
             if ((c & 1) == 0 &&
-                !(ok = mbar_wait(DECAY ? &scaled[s] : &full[s], u & 1, &abort_flag, P.status, detail)))
+                !(ok = mbar_wait_w(DECAY ? &scaled[s] : &full[s], u & 1, &abort_flag, P.status, detail)))
               break;
             tc_fence_after();
             const uint32_t xs = smem_u32(smem + s * kStage), ys = xs + kTileBytes;
 #pragma unroll
             for (uint32_t j = 0; j < 4; ++j) {
               const uint32_t ks = 4 * (c & 1) + j;  // the chunk's 64 rows of the tile
-              mma_ss(tS, desc_mnmajor(xs, ks), desc_mnmajor(ys, ks), idesc, 1u);
+              mma_ss_warp(tS, desc_mnmajor(xs, ks), desc_mnmajor(ys, ks), idesc, 1u);
             }
-            mma_commit(cmma);
+            mma_commit_warp(cmma);
           }
           // a block's stage is released after its second chunk, or the group's last
           if ((c & 1) == 1 || c + 1 == nc) {
             if (c + 1 == nc && (c & 1) == 0 &&
-                !(ok = mbar_wait(DECAY ? &scaled[s] : &full[s], u & 1, &abort_flag, P.status, detail)))
+                !(ok = mbar_wait_w(DECAY ? &scaled[s] : &full[s], u & 1, &abort_flag, P.status, detail)))
               break;
-            mma_commit(&empty[s]);
+            mma_commit_warp(&empty[s]);
             ++it;
           }
         }
@@ -772,7 +773,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar[B_KS + i], 128);
       mbar_init(&bar[B_XS + i], 128);
     }
-    ring_init(ring, 1 + 128 + 128);  // readers: MMA thread, groups A and B
+    ring_init(ring, 32 + 128 + 128);  // readers: MMA warp, groups A and B
     fence_mbar_init();
     prefetch_tensormap(&mq);
     prefetch_tensormap(&mk);
@@ -832,7 +833,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    {  // the whole warp: one elected lane issues each product
       const uint32_t id_qk = idesc_bf16(128, 128, false, false);  // Q K^T
       const uint32_t id_qs = idesc_bf16(128, 128, false, true);   // Q S,  P V
       const uint32_t id_kv = idesc_bf16(128, 128, true, true);    // K^T V
@@ -840,7 +841,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int blk = 0, ia = 0;  // ia: items that accumulated their group aggregate (phases of B_WEMPTY)
       bool ok = true;
       for (int k = 0, item; ok; ++k) {
-        if (!(ok = ring_take(ring, k, item, &abort_flag, P.status, detail)) || item < 0) break;
+        if (!(ok = __all_sync(0xffffffffu, ring_take(ring, k, item, &abort_flag, P.status, detail))) || item < 0) break;
         const int g = item / BH;
         const int s0 = P.gp.start(g), s1 = min(P.T, P.gp.start(g + 1)), nb = (s1 - s0 + 127) / 128;
         // weighted-operand form (K and X weighted as they land); the group
@@ -853,59 +854,59 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t Q = slot_addr(tq), K = slot_addr(tk), V = slot_addr(tv);
           const int wb = blk & 1, wp = (blk >> 1) & 1;
           // scores: P = Q K^T
-          ok = mbar_wait(&bar[B_FULL + tq % kSlots], (tq / kSlots) & 1, &abort_flag, P.status, detail) &&
-               mbar_wait(&bar[B_FULL + tk % kSlots], (tk / kSlots) & 1, &abort_flag, P.status, detail) &&
-               (blk == 0 || mbar_wait(&bar[B_PEMPTY], (blk - 1) & 1, &abort_flag, P.status, detail));
+          ok = mbar_wait_w(&bar[B_FULL + tq % kSlots], (tq / kSlots) & 1, &abort_flag, P.status, detail) &&
+               mbar_wait_w(&bar[B_FULL + tk % kSlots], (tk / kSlots) & 1, &abort_flag, P.status, detail) &&
+               (blk == 0 || mbar_wait_w(&bar[B_PEMPTY], (blk - 1) & 1, &abort_flag, P.status, detail));
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
-          for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tP, desc_kmajor(Q, ks), desc_kmajor(K, ks), id_qk, ks > 0);
-          mma_commit(&bar[B_PFULL]);
+          for (uint32_t ks = 0; ks < 8; ++ks) mma_ss_warp(tP, desc_kmajor(Q, ks), desc_kmajor(K, ks), id_qk, ks > 0);
+          mma_commit_warp(&bar[B_PFULL]);
           // inter-block term: O = Q S (its own accumulator with a decay, unless weighted)
-          ok = mbar_wait(&bar[B_PRE], blk & 1, &abort_flag, P.status, detail) &&
-               (blk == 0 || mbar_wait(&bar[B_OEMPTY], (blk - 1) & 1, &abort_flag, P.status, detail));
+          ok = mbar_wait_w(&bar[B_PRE], blk & 1, &abort_flag, P.status, detail) &&
+               (blk == 0 || mbar_wait_w(&bar[B_OEMPTY], (blk - 1) & 1, &abort_flag, P.status, detail));
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
           for (uint32_t ks = 0; ks < 8; ++ks)
-            mma_ss((DECAY && !wtd) ? tOi : tO, desc_kmajor(Q, ks), desc_mnmajor(sSh, ks), id_qs, ks > 0);
+            mma_ss_warp((DECAY && !wtd) ? tOi : tO, desc_kmajor(Q, ks), desc_mnmajor(sSh, ks), id_qs, ks > 0);
           if (aggw) {
             // group aggregate: W += X'^T Q (the previous group's W must have been read out;
             // with a decay X' has its rows weighted by lambda^{s - start + 1})
-            ok = (DECAY ? mbar_wait(&bar[B_XS + wb], wp, &abort_flag, P.status, detail)
-                        : mbar_wait(&bar[B_FULL + tx % kSlots], (tx / kSlots) & 1, &abort_flag, P.status, detail)) &&
-                 (n > 0 || ia == 0 || mbar_wait(&bar[B_WEMPTY], (ia - 1) & 1, &abort_flag, P.status, detail));
+            ok = (DECAY ? mbar_wait_w(&bar[B_XS + wb], wp, &abort_flag, P.status, detail)
+                        : mbar_wait_w(&bar[B_FULL + tx % kSlots], (tx / kSlots) & 1, &abort_flag, P.status, detail)) &&
+                 (n > 0 || ia == 0 || mbar_wait_w(&bar[B_WEMPTY], (ia - 1) & 1, &abort_flag, P.status, detail));
             if (!ok) break;
             tc_fence_after();
             const uint32_t X = slot_addr(tx);
 #pragma unroll
             for (uint32_t ks = 0; ks < 8; ++ks)
-              mma_ss(tW, desc_mnmajor(X, ks), desc_mnmajor(Q, ks), id_xq, (n > 0 || ks > 0) ? 1u : 0u);
+              mma_ss_warp(tW, desc_mnmajor(X, ks), desc_mnmajor(Q, ks), id_xq, (n > 0 || ks > 0) ? 1u : 0u);
           }
           // an X tile that no product reads is still waited for before its slot is released
           if (AGG && !aggw &&
-              !(ok = mbar_wait(&bar[B_FULL + tx % kSlots], (tx / kSlots) & 1, &abort_flag, P.status, detail)))
+              !(ok = mbar_wait_w(&bar[B_FULL + tx % kSlots], (tx / kSlots) & 1, &abort_flag, P.status, detail)))
             break;
-          mma_commit(&bar[B_EMPTY + tq % kSlots]);
-          if (AGG) mma_commit(&bar[B_EMPTY + tx % kSlots]);
+          mma_commit_warp(&bar[B_EMPTY + tq % kSlots]);
+          if (AGG) mma_commit_warp(&bar[B_EMPTY + tx % kSlots]);
           // state update: S += K'^T V (decay-weighted key rows), or K^T V' in the
           // weighted form (decay-weighted value rows, which P V reads too)
-          ok = (!DECAY || mbar_wait(&bar[B_KS + wb], wp, &abort_flag, P.status, detail)) &&
-               mbar_wait(&bar[B_FULL + tv % kSlots], (tv / kSlots) & 1, &abort_flag, P.status, detail);
+          ok = (!DECAY || mbar_wait_w(&bar[B_KS + wb], wp, &abort_flag, P.status, detail)) &&
+               mbar_wait_w(&bar[B_FULL + tv % kSlots], (tv / kSlots) & 1, &abort_flag, P.status, detail);
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
-          for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tS, desc_mnmajor(K, ks), desc_mnmajor(V, ks), id_kv, 1u);
-          mma_commit(&bar[B_EMPTY + tk % kSlots]);
-          mma_commit(&bar[B_SFULL]);
+          for (uint32_t ks = 0; ks < 8; ++ks) mma_ss_warp(tS, desc_mnmajor(K, ks), desc_mnmajor(V, ks), id_kv, 1u);
+          mma_commit_warp(&bar[B_EMPTY + tk % kSlots]);
+          mma_commit_warp(&bar[B_SFULL]);
           // intra-block term: O += P V
-          if (!(ok = mbar_wait(&bar[B_PSFULL], blk & 1, &abort_flag, P.status, detail))) break;
+          if (!(ok = mbar_wait_w(&bar[B_PSFULL], blk & 1, &abort_flag, P.status, detail))) break;
           tc_fence_after();
 #pragma unroll
           for (uint32_t ks = 0; ks < 8; ++ks)
-            mma_ss(tO, desc_kmajor(sPs, ks), desc_mnmajor(V, ks), id_qs, (!DECAY || wtd || ks > 0) ? 1u : 0u);
-          mma_commit(&bar[B_EMPTY + tv % kSlots]);
-          mma_commit(&bar[B_OFULL]);
+            mma_ss_warp(tO, desc_kmajor(sPs, ks), desc_mnmajor(V, ks), id_qs, (!DECAY || wtd || ks > 0) ? 1u : 0u);
+          mma_commit_warp(&bar[B_EMPTY + tv % kSlots]);
+          mma_commit_warp(&bar[B_OFULL]);
         }
         if (ok && aggw) ++ia;
       }
@@ -1306,7 +1307,7 @@ __global__ void __launch_bounds__(kDualThreads, 1)
       mbar_init(&bar[D_DS + i], 128);
       mbar_init(&bar[D_VS + i], 128);
     }
-    ring_init(ring, 1 + 3 * 128);  // readers: MMA thread, groups A, B and C
+    ring_init(ring, 32 + 3 * 128);  // readers: MMA warp, groups A, B and C
     fence_mbar_init();
     prefetch_tensormap(&mk);
     prefetch_tensormap(&mq);
@@ -1358,14 +1359,14 @@ __global__ void __launch_bounds__(kDualThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    {  // the whole warp: one elected lane issues each product
       const uint32_t id_kk = idesc_bf16(128, 128, false, false);  // A K-major, B K-major
       const uint32_t id_km = idesc_bf16(128, 128, false, true);   // A K-major (or TMEM), B MN-major
       const uint32_t id_mm = idesc_bf16(128, 128, true, true);    // A MN-major, B MN-major
       int blk = 0;
       bool ok = true;
       auto wait = [&](int idx, int parity) {
-        return mbar_wait(&bar[idx], parity & 1, &abort_flag, P.status, detail);
+        return mbar_wait_w(&bar[idx], parity & 1, &abort_flag, P.status, detail);
       };
       auto full = [&](int x) {
         int s, c;
@@ -1375,7 +1376,7 @@ __global__ void __launch_bounds__(kDualThreads, 1)
       auto release = [&](int x) {
         int s, c;
         dual_slot(blk, x, s, c);
-        mma_commit(&bar[D_EMPTY + s]);
+        mma_commit_warp(&bar[D_EMPTY + s]);
       };
       auto addr = [&](int x) {
         int s, c;
@@ -1383,7 +1384,7 @@ __global__ void __launch_bounds__(kDualThreads, 1)
         return tile_addr(s);
       };
       for (int k = 0, item; ok; ++k) {
-        if (!(ok = ring_take(ring, k, item, &abort_flag, P.status, detail)) || item < 0) break;
+        if (!(ok = __all_sync(0xffffffffu, ring_take(ring, k, item, &abort_flag, P.status, detail))) || item < 0) break;
         const int g = item / BH;
         const int s0 = P.gp.start(g), s1 = min(P.T, P.gp.start(g + 1)), nb = (s1 - s0 + 127) / 128;
         // weighted-operand form: dO is weighted before its first product
@@ -1397,55 +1398,55 @@ __global__ void __launch_bounds__(kDualThreads, 1)
           if (!(ok = full(0) && full(1))) break;
           tc_fence_after();
 #pragma unroll
-          for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tP, desc_kmajor(K, ks), desc_kmajor(Q, ks), id_kk, ks > 0);
-          mma_commit(&bar[D_PFULL]);
+          for (uint32_t ks = 0; ks < 8; ++ks) mma_ss_warp(tP, desc_kmajor(K, ks), desc_kmajor(Q, ks), id_kk, ks > 0);
+          mma_commit_warp(&bar[D_PFULL]);
           // dv = K' R   (R from the bf16 state tile, MN-major)
           ok = (!DECAY || wtd || wait(D_KS + wb, wp)) && wait(D_PRE, blk) && (blk == 0 || wait(D_O1EMPTY, blk - 1));
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
-          for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tO1, desc_kmajor(K, ks), desc_mnmajor(sSh, ks), id_km, ks > 0);
+          for (uint32_t ks = 0; ks < 8; ++ks) mma_ss_warp(tO1, desc_kmajor(K, ks), desc_mnmajor(sSh, ks), id_km, ks > 0);
           release(0);
           if (early_r) {
             // R += Q^T dO' (the state tile is rewritten only after SFULL, below)
             if (!(ok = wtd ? wait(D_DS + wb, wp) : full(2))) break;
             tc_fence_after();
 #pragma unroll
-            for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tR, desc_mnmajor(Q, ks), desc_mnmajor(DO, ks), id_mm, 1u);
+            for (uint32_t ks = 0; ks < 8; ++ks) mma_ss_warp(tR, desc_mnmajor(Q, ks), desc_mnmajor(DO, ks), id_mm, 1u);
           }
           // dv += P1~ dO   (P1~ in TMEM as bf16 pairs)
           if (!(ok = (early_r ? true : full(2)) && wait(D_PSFULL, u1))) break;
           tc_fence_after();
 #pragma unroll
-          for (uint32_t ks = 0; ks < 8; ++ks) mma_ts(tO1, tP + ks * 8, desc_mnmajor(DO, ks), id_km, 1u);
-          mma_commit(&bar[D_O1FULL]);
+          for (uint32_t ks = 0; ks < 8; ++ks) mma_ts_warp(tO1, tP + ks * 8, desc_mnmajor(DO, ks), id_km, 1u);
+          mma_commit_warp(&bar[D_O1FULL]);
           // P2 = V dO^T
           if (!(ok = full(3))) break;
           tc_fence_after();
 #pragma unroll
-          for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tP, desc_kmajor(V, ks), desc_kmajor(DO, ks), id_kk, ks > 0);
-          mma_commit(&bar[D_PFULL]);
+          for (uint32_t ks = 0; ks < 8; ++ks) mma_ss_warp(tP, desc_kmajor(V, ks), desc_kmajor(DO, ks), id_kk, ks > 0);
+          mma_commit_warp(&bar[D_PFULL]);
           if (early_r) release(2);
           // dk = V' R^T  (the state tile read K-major)
           ok = (early_r || wait(D_VS + wb, wp)) && (blk == 0 || wait(D_O2EMPTY, blk - 1));
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
-          for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tO2, desc_kmajor(V, ks), desc_kmajor(sSh, ks), id_kk, ks > 0);
+          for (uint32_t ks = 0; ks < 8; ++ks) mma_ss_warp(tO2, desc_kmajor(V, ks), desc_kmajor(sSh, ks), id_kk, ks > 0);
           release(3);
           if (!early_r) {
             // R += Q^T dO'  (dO rows weighted together with V's)
 #pragma unroll
-            for (uint32_t ks = 0; ks < 8; ++ks) mma_ss(tR, desc_mnmajor(Q, ks), desc_mnmajor(DO, ks), id_mm, 1u);
+            for (uint32_t ks = 0; ks < 8; ++ks) mma_ss_warp(tR, desc_mnmajor(Q, ks), desc_mnmajor(DO, ks), id_mm, 1u);
             release(2);
           }
-          mma_commit(&bar[D_SFULL]);
+          mma_commit_warp(&bar[D_SFULL]);
           // dk += P2~ Q
           if (!(ok = wait(D_PSFULL, u2))) break;
           tc_fence_after();
 #pragma unroll
-          for (uint32_t ks = 0; ks < 8; ++ks) mma_ts(tO2, tP + ks * 8, desc_mnmajor(Q, ks), id_km, 1u);
-          mma_commit(&bar[D_O2FULL]);
+          for (uint32_t ks = 0; ks < 8; ++ks) mma_ts_warp(tO2, tP + ks * 8, desc_mnmajor(Q, ks), id_km, 1u);
+          mma_commit_warp(&bar[D_O2FULL]);
           release(1);
         }
       }

@@ -520,9 +520,12 @@ int32_t linattn_bwd_gated(const linattn_shape *shape, const void *q, const void 
   float *wagg = reinterpret_cast<float *>(ws + w.wagg), *rbar = reinterpret_cast<float *>(ws + w.rbar);
   const float *states = static_cast<const float *>(checkpoint);
   const float *fin = states + (size_t)G * E;
-  cudaError_t e = gate_prep(p, gp, log_gate, C, tot, nullptr, s);
+  // per-item flags: the dq and dk/dv passes take the weighted-operand form together
+  int *wflag = reinterpret_cast<int *>(ws + w.wflag);
+  cudaError_t e = gate_prep(p, gp, log_gate, C, tot, wflag, s);
   p.gC = C;
   p.gtot = tot;
+  p.gflag = wflag;
   p.gq = q;
   p.gk = k;
   p.gx = reinterpret_cast<float *>(ws + w.gx);

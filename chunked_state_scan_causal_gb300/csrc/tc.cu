@@ -691,6 +691,25 @@ __device__ __forceinline__ float gate_colw(const float *gc, int t0, int r, int n
   return exp2f(REV ? cr - cm : cm - cr);
 }
 
+// sum_j x[j] * bf16(y[j] w) for 32 fp32 x and 32 bf16 y at src (64 contiguous
+// bytes): the row y weighted and rounded as scale_tile_row weights a tile row.
+__device__ __forceinline__ float dot32_bf16_w(const float (&x)[32], const __nv_bfloat16 *src, float w) {
+  const uint4 *p = reinterpret_cast<const uint4 *>(src);
+  float acc = 0.f;
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const uint4 u = __ldg(p + m);
+    const uint32_t v[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t y = pack_bf16(bf16lo(v[e]) * w, bf16hi(v[e]) * w);
+      acc = fmaf(x[8 * m + 2 * e], bf16lo(y), acc);
+      acc = fmaf(x[8 * m + 2 * e + 1], bf16hi(y), acc);
+    }
+  }
+  return acc;
+}
+
 // sum_j x[j] * y[j] for 32 fp32 x and 32 bf16 y at src (64 contiguous bytes).
 __device__ __forceinline__ float dot32_bf16(const float (&x)[32], const __nv_bfloat16 *src) {
   const uint4 *p = reinterpret_cast<const uint4 *>(src);
@@ -987,6 +1006,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 4; ++c) {
           float x[32];
           ld_chunk(tO + lb + c * 32, x);
+          // the gate-gradient term q . dq: in the weighted form, the q row as the dk/dv
+          // pass's products see it (bf16(q exp2(C_i - C_prev))) with the accumulator
+          // (dq / exp2(C_i - C_prev))
+          if (gx_row && wtd) gxacc += dot32_bf16_w(x, qrow + c * 32, wq);
           if (wtd) {
             // the accumulator holds o_i / lambda^{i+1} (gates: / exp2(C_i - C_prev))
 #pragma unroll
@@ -997,7 +1020,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int j = 0; j < 32; ++j) x[j] = fmaf(wq, y[j], x[j]);
           }
-          if (gx_row) gxacc += dot32_bf16(x, qrow + c * 32);  // q . dq before dq is rounded
+          if (gx_row && !wtd) gxacc += dot32_bf16(x, qrow + c * 32);  // q . dq before dq is rounded
           store_row_chunk_bf16(sPs, row, c, x);
         }
         if (gx_row) P.gx[(int64_t)bh * P.T + t0 + row] = gxacc;
@@ -1195,6 +1218,7 @@ struct DualParams {
   const float *gC;     // GATE: group-local log2 cumulative sums of the gates [BH][T]
   const __nv_bfloat16 *gk;  // GATE: k (strides sb, sh, st) for gx -= k . dk
   float *gx;           // GATE: [BH][T] fp32, q . dq from the dq pass; k . dk (unrounded dk) subtracted
+  const int *gflag;    // GATE: per item [G][BH], nonzero: the weighted-operand form (as in the dq pass)
 };
 
 constexpr int kDualThreads = 512;
@@ -1388,14 +1412,17 @@ __global__ void __launch_bounds__(kDualThreads, 1)
         const int g = item / BH;
         const int s0 = P.gp.start(g), s1 = min(P.T, P.gp.start(g + 1)), nb = (s1 - s0 + 127) / 128;
         // weighted-operand form: dO is weighted before its first product
-        const bool wtd = DECAY && !GATE && P.decay[(item % BH) % P.H] >= kWeightedMin;
+        // weighted-operand form: dO (gates: Q) is weighted before its first product
+        const bool wtd = DECAY && (GATE ? P.gflag && P.gflag[item] != 0
+                                        : P.decay[(item % BH) % P.H] >= kWeightedMin);
+        const bool wq = GATE && wtd;  // the weighted tile is Q, read by P1 already
         // the decay-free order (R updated right after dv's state term)
         const bool early_r = !DECAY || wtd;
         for (int n = 0; n < nb && ok; ++n, ++blk) {
           const uint32_t K = addr(0), Q = addr(1), DO = addr(2), V = addr(3);
           const int u1 = 2 * blk, u2 = u1 + 1, wb = blk & 1, wp = blk >> 1;
           // P1 = K Q^T  (the previous block's P2~ has been consumed: issue order)
-          if (!(ok = full(0) && full(1))) break;
+          if (!(ok = full(0) && (wq ? wait(D_DS + wb, wp) : full(1)))) break;
           tc_fence_after();
 #pragma unroll
           for (uint32_t ks = 0; ks < 8; ++ks) mma_ss_warp(tP, desc_kmajor(K, ks), desc_kmajor(Q, ks), id_kk, ks > 0);
@@ -1409,7 +1436,7 @@ __global__ void __launch_bounds__(kDualThreads, 1)
           release(0);
           if (early_r) {
             // R += Q^T dO' (the state tile is rewritten only after SFULL, below)
-            if (!(ok = wtd ? wait(D_DS + wb, wp) : full(2))) break;
+            if (!(ok = (wtd && !wq) ? wait(D_DS + wb, wp) : full(2))) break;
             tc_fence_after();
 #pragma unroll
             for (uint32_t ks = 0; ks < 8; ++ks) mma_ss_warp(tR, desc_mnmajor(Q, ks), desc_mnmajor(DO, ks), id_mm, 1u);
@@ -1462,14 +1489,19 @@ __global__ void __launch_bounds__(kDualThreads, 1)
       const int s0 = P.gp.start(g), s1 = min(P.T, P.gp.start(g + 1)), nb = (s1 - s0 + 127) / 128;
       const float lam = (DECAY && !GATE) ? P.decay[h] : 1.f;
       const float l2 = (DECAY && !GATE) ? log2f(lam) : 0.f;
-      const bool wtd = DECAY && !GATE && lam >= kWeightedMin;
+      const bool wtd = DECAY && (GATE ? P.gflag && P.gflag[item] != 0 : lam >= kWeightedMin);
       const float *gc = GATE ? P.gC + (int64_t)bh * P.T : nullptr;
       for (int n = 0; n < nb && ok; ++n, ++blk) {
-        // weighted operands: both score tiles take lambda^{-nv} inside the mask
-        const float wsc = wtd ? exp2f(-l2 * (float)min(128, s1 - (s0 + 128 * (nb - 1 - n)))) : 1.f;
+        // weighted operands: both score tiles take lambda^{-nv} (gates: exp2(C_prev -
+        // C_last), the factor of the dq pass's transposed tile) inside the mask
+        float wsc = 1.f;
+        if (wtd) {
+          const int t0 = s0 + 128 * (nb - 1 - n), nv = min(128, s1 - t0);
+          wsc = GATE ? exp2f((t0 > s0 ? gc[t0 - 1] : 0.f) - gc[t0 + nv - 1]) : exp2f(-l2 * (float)nv);
+        }
         float ci = 0.f;
         float *cb = reinterpret_cast<float *>(smem + kDualOffGate), *cw = cb + 128;
-        if (GATE) {
+        if (GATE && !wtd) {
           // the block's cumulative sums and column factors, shared by the group
           // (rewritten only after the barrier that ends the block below)
           const int t0 = s0 + 128 * (nb - 1 - n), nv = min(128, s1 - t0);
@@ -1489,7 +1521,7 @@ __global__ void __launch_bounds__(kDualThreads, 1)
           for (int c = 0; c < 4; ++c) {
             float x[32];
             ld_chunk(tP + lb + c * 32, x);
-            if (GATE) {
+            if (GATE && !wtd) {
               mask_chunk_gate<true>(x, (int)row, c, ci, cb, cw);
             } else if (wtd) {
               mask_chunk<false, true>(x, (int)row, c, 1.f, 0.f);
@@ -1507,7 +1539,7 @@ __global__ void __launch_bounds__(kDualThreads, 1)
           tc_fence_before();
           mbar_arrive(&bar[D_PSFULL]);
         }
-        if (GATE) named_bar_sync(3, 128);  // the block's sums are no longer read (ok is group-uniform)
+        if (GATE && !wtd) named_bar_sync(3, 128);  // the block's sums are no longer read (ok, wtd group-uniform)
       }
     }
   } else if (warp >= 8 && warp < 12) {
@@ -1536,7 +1568,7 @@ __global__ void __launch_bounds__(kDualThreads, 1)
       const int s0 = P.gp.start(g), s1 = min(P.T, P.gp.start(g + 1)), nb = (s1 - s0 + 127) / 128;
       const float lam = (DECAY && !GATE) ? P.decay[h] : 1.f;
       const float l2 = (DECAY && !GATE) ? log2f(lam) : 0.f;
-      const bool wtd = DECAY && !GATE && lam >= kWeightedMin;
+      const bool wtd = DECAY && (GATE ? P.gflag && P.gflag[item] != 0 : lam >= kWeightedMin);
       const float *gc = GATE ? P.gC + (int64_t)bh * P.T : nullptr;
       auto nvalid = [&](int n) { return min(128, s1 - (s0 + 128 * (nb - 1 - n))); };
       auto start = [&](int n) { return s0 + 128 * (nb - 1 - n); };
@@ -1547,15 +1579,19 @@ __global__ void __launch_bounds__(kDualThreads, 1)
         if (GATE) return exp2f(clast(n) - cprev(n));
         return DECAY ? exp2f(l2 * (float)nvalid(n)) : 1.f;
       };
-      // weight of this thread's row of dO in walk block n
+      // weighted form: the weighted tile (dO; gates: Q) and this thread's row weight
+      // in walk block n: lambda^{r+1}, or exp2(C_r - C_prev), the weight of the q row
+      // in the dq pass's gate-gradient term (the same fp32 expression)
+      const int wtile = GATE ? 1 : 2;
       auto wdo = [&](int n) {
         const int r = (int)row;
-        return r < nvalid(n) ? exp2f(l2 * (float)(r + 1)) : 0.f;
+        if (r >= nvalid(n)) return 0.f;
+        return GATE ? exp2f(gate_c(gc, start(n), r, nvalid(n)) - cprev(n)) : exp2f(l2 * (float)(r + 1));
       };
-      // weighted form: dO of a block, plus one (empty) phase of the K and V
+      // weighted form: that tile of a block, plus one (empty) phase of the K and V
       // weighting barriers, which every block completes whatever its form
       auto weigh_do = [&](int b, int n) {
-        if (!weigh(b, 2, wdo(n), D_DS)) return false;
+        if (!weigh(b, wtile, wdo(n), D_DS)) return false;
         mbar_arrive(&bar[D_KS + (b & 1)]);
         mbar_arrive(&bar[D_VS + (b & 1)]);
         return true;
@@ -1625,7 +1661,7 @@ __global__ void __launch_bounds__(kDualThreads, 1)
         bool do_done = false;
         if (wtd && more) {
           int s, c;
-          dual_slot(blk + 1, 2, s, c);
+          dual_slot(blk + 1, wtile, s, c);
           // bounded poll of both events; the bounded waits below follow either way
 #pragma unroll 1
           for (int i = 0; i < (1 << 20) && !abort_flag; ++i) {
@@ -1672,13 +1708,19 @@ __global__ void __launch_bounds__(kDualThreads, 1)
       const int g = item / BH, bh = item % BH, b = bh / P.H, h = bh % P.H;
       const int s0 = P.gp.start(g), s1 = min(P.T, P.gp.start(g + 1)), nb = (s1 - s0 + 127) / 128;
       const float lam = (DECAY && !GATE) ? P.decay[h] : 1.f;
-      const bool wtd = DECAY && !GATE && lam >= kWeightedMin;
-      const float l2 = wtd ? log2f(lam) : 0.f;
+      const bool wtd = DECAY && (GATE ? P.gflag && P.gflag[item] != 0 : lam >= kWeightedMin);
+      const float l2 = (wtd && !GATE) ? log2f(lam) : 0.f;
+      const float *gc = GATE ? P.gC + (int64_t)bh * P.T : nullptr;
       for (int n = 0; n < nb && ok; ++n, ++blk) {
         const int t0 = s0 + 128 * (nb - 1 - n);
         const bool valid = t0 + (int)row < s1;
         // weighted form: the accumulators hold the rows divided by lambda^{nv-1-i}
-        const float wrow = (wtd && valid) ? exp2f(l2 * (float)(min(128, s1 - t0) - 1 - (int)row)) : 1.f;
+        // (gates: exp2(C_last - C_i), the weight of the k row in the dq pass)
+        float wrow = 1.f;
+        if (wtd && valid) {
+          const int nv = min(128, s1 - t0);
+          wrow = GATE ? exp2f(gc[t0 + nv - 1] - gc[t0 + (int)row]) : exp2f(l2 * (float)(nv - 1 - (int)row));
+        }
         if (GATE && P.gx && valid) {
           // the k row for k . dk: two 128-byte lines into L1 while dv drains
           const __nv_bfloat16 *kr = P.gk + (int64_t)b * P.sb + (int64_t)h * P.sh + (int64_t)(t0 + (int)row) * P.st;
@@ -1701,11 +1743,16 @@ __global__ void __launch_bounds__(kDualThreads, 1)
           for (int c = 0; c < 4; ++c) {
             float x[32];
             ld_chunk(tO + lb + c * 32, x);
+            // the gate-gradient term k . dk: in the weighted form, the k row as the dq
+            // pass's products saw it (bf16(k exp2(C_last - C_i))) with the accumulator
+            // (dk / exp2(C_last - C_i)), so that the intra-block terms of q . dq and
+            // k . dk are the same products
+            if (gx_row && wtd) gxacc += dot32_bf16_w(x, krow + c * 32, wrow);
             if (wtd) {
 #pragma unroll
               for (int j = 0; j < 32; ++j) x[j] *= wrow;
             }
-            if (gx_row) gxacc += dot32_bf16(x, krow + c * 32);  // k . dk before dk is rounded
+            if (gx_row && !wtd) gxacc += dot32_bf16(x, krow + c * 32);  // k . dk before dk is rounded
             if (valid) {
               if (P.wide)
                 st_global_chunk_bf16<true>(dst + c * 32, x);
@@ -1808,6 +1855,7 @@ cudaError_t tc_dual(const Problem &p, const GroupPlan &gp, const void *q, const 
   D.gC = p.gC;
   D.gk = static_cast<const __nv_bfloat16 *>(p.gk);
   D.gx = p.gx;
+  D.gflag = p.gflag;
   const int grid = D.nitems < p.num_sms ? D.nitems : p.num_sms;
   cudaError_t e;
   TimedLaunch t(K_TC_DUAL_REV, s);

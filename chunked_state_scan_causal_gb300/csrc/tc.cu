@@ -1540,6 +1540,32 @@ __global__ void __launch_bounds__(kDualThreads, 1)
           mbar_arrive(&bar[D_PSFULL]);
         }
         if (GATE && !wtd) named_bar_sync(3, 128);  // the block's sums are no longer read (ok, wtd group-uniform)
+        if (GATE && wtd && ok) {
+          // Gated items in the weighted form store their dv rows here, in fp32 times
+          // the row weight exp2(C_last - C_i): the store warps keep the block for the dk
+          // rows and the gate gradient's k . dk term.
+          const int t0 = s0 + 128 * (nb - 1 - n), nv = min(128, s1 - t0);
+          const bool valid = (int)row < nv;
+          const float wrow = valid ? exp2f(gc[t0 + nv - 1] - gc[t0 + (int)row]) : 1.f;
+          if (!(ok = group_all(mbar_wait(&bar[D_O1FULL], blk & 1, &abort_flag, P.status, detail), 3, 128))) break;
+          tc_fence_after();
+          __nv_bfloat16 *dst = P.dv + (int64_t)(bh / P.H) * P.sb + (int64_t)h * P.sh + (int64_t)(t0 + (int)row) * P.st;
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            float x[32];
+            ld_chunk(tO1 + lb + c * 32, x);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) x[j] *= wrow;
+            if (valid) {
+              if (P.wide)
+                st_global_chunk_bf16<true>(dst + c * 32, x);
+              else
+                st_global_chunk_bf16<false>(dst + c * 32, x);
+            }
+          }
+          tc_fence_before();
+          mbar_arrive(&bar[D_O1EMPTY]);
+        }
       }
     }
   } else if (warp >= 8 && warp < 12) {
@@ -1727,7 +1753,8 @@ __global__ void __launch_bounds__(kDualThreads, 1)
           prefetch_l1(kr);
           prefetch_l1(kr + 64);
         }
-        for (int half = 0; half < 2 && ok; ++half) {
+        // (gated items in the weighted form: the dv rows are stored by the score warps)
+        for (int half = (GATE && wtd) ? 1 : 0; half < 2 && ok; ++half) {
           ok = __all_sync(0xffffffffu, mbar_wait(&bar[half ? D_O2FULL : D_O1FULL], blk & 1, &abort_flag,
                                                  P.status, detail));
           if (!ok) break;

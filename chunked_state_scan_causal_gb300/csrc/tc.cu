@@ -1685,7 +1685,12 @@ __global__ void __launch_bounds__(kDualThreads, 1)
         // block's state is ready first (the state goes first then, being on the
         // critical path)
         bool do_done = false;
-        if (wtd && more) {
+        if (GATE && wtd && more) {
+          // gates: the weighted tile is Q, which the next block's first product reads;
+          // it lands a block or more ahead, so it goes first
+          if (!(ok = weigh_do(blk + 1, n + 1))) break;
+          do_done = true;
+        } else if (wtd && more) {
           int s, c;
           dual_slot(blk + 1, wtile, s, c);
           // bounded poll of both events; the bounded waits below follow either way

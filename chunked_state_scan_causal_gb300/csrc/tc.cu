@@ -691,6 +691,24 @@ __device__ __forceinline__ float gate_colw(const float *gc, int t0, int r, int n
   return exp2f(REV ? cr - cm : cm - cr);
 }
 
+// sum_j x[j] * bf16(y[j] w) over columns 32c .. 32c+31 of a row of 128 bf16 y held
+// in registers (16 x 8 bf16), rounded as dot32_bf16_w rounds them.
+__device__ __forceinline__ float dot32_regs_w(const float (&x)[32], const uint4 (&y)[16], int c, float w) {
+  float acc = 0.f;
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const uint4 u = y[4 * c + m];
+    const uint32_t v[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t z = pack_bf16(bf16lo(v[e]) * w, bf16hi(v[e]) * w);
+      acc = fmaf(x[8 * m + 2 * e], bf16lo(z), acc);
+      acc = fmaf(x[8 * m + 2 * e + 1], bf16hi(z), acc);
+    }
+  }
+  return acc;
+}
+
 // sum_j x[j] * bf16(y[j] w) for 32 fp32 x and 32 bf16 y at src (64 contiguous
 // bytes): the row y weighted and rounded as scale_tile_row weights a tile row.
 __device__ __forceinline__ float dot32_bf16_w(const float (&x)[32], const __nv_bfloat16 *src, float w) {
@@ -962,11 +980,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             cw[row] = gate_colw<false>(gc, t0, (int)row, nv);
           }
         }
+        // the q row for the epilogue's q . dq: in the weighted form loaded whole into
+        // registers now (a thread's own row: a warp's loads touch 32 lines; their
+        // latency passes while the block's products run), else two lines into L1
+        uint4 qv[16];
+        const bool qreg = GATE && wtd && P.gx && (int)row < nv;
         if (GATE && P.gx && (int)row < nv) {
-          // the q row for the epilogue's q . dq: two 128-byte lines into L1 now
           const __nv_bfloat16 *qr = P.gq + (int64_t)b * P.sb + (int64_t)h * P.sh + (int64_t)(t0 + (int)row) * P.st;
-          prefetch_l1(qr);
-          prefetch_l1(qr + 64);
+          if (qreg) {
+#pragma unroll
+            for (int m = 0; m < 16; ++m) qv[m] = __ldg(reinterpret_cast<const uint4 *>(qr) + m);
+          } else {
+            prefetch_l1(qr);
+            prefetch_l1(qr + 64);
+          }
         }
         ok = group_all(mbar_wait(&bar[B_PFULL], blk & 1, &abort_flag, P.status, detail), 2, 128);
         if (!ok) break;
@@ -1002,14 +1029,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         const __nv_bfloat16 *qrow = gx_row ? P.gq + (int64_t)b * P.sb + (int64_t)h * P.sh +
                                                   (int64_t)(t0 + (int)row) * P.st : nullptr;
         float gxacc = 0.f;
+        if (GATE && wtd) {
+          // gated, weighted form: the gate-gradient term q . dq takes the q row as the
+          // dk/dv pass's products see it (bf16(q exp2(C_i - C_prev))) with the
+          // accumulator (dq / exp2(C_i - C_prev)); then dq = accumulator x weight
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            float x[32];
+            ld_chunk(tO + lb + c * 32, x);
+            if (qreg) gxacc += dot32_regs_w(x, qv, c, wq);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) x[j] *= wq;
+            store_row_chunk_bf16(sPs, row, c, x);
+          }
+        } else {
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           float x[32];
           ld_chunk(tO + lb + c * 32, x);
-          // the gate-gradient term q . dq: in the weighted form, the q row as the dk/dv
-          // pass's products see it (bf16(q exp2(C_i - C_prev))) with the accumulator
-          // (dq / exp2(C_i - C_prev))
-          if (gx_row && wtd) gxacc += dot32_bf16_w(x, qrow + c * 32, wq);
           if (wtd) {
             // the accumulator holds o_i / lambda^{i+1} (gates: / exp2(C_i - C_prev))
 #pragma unroll
@@ -1022,6 +1059,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (gx_row && !wtd) gxacc += dot32_bf16(x, qrow + c * 32);  // q . dq before dq is rounded
           store_row_chunk_bf16(sPs, row, c, x);
+        }
         }
         if (gx_row) P.gx[(int64_t)bh * P.T + t0 + row] = gxacc;
         tc_fence_before();

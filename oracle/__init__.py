@@ -27,6 +27,8 @@ from .oracle import (  # noqa: F401
     segment_grad_states,
     fwd_gated,
     bwd_gated,
+    fwd_gated_vec,
+    bwd_gated_vec,
     state_scan,
     threads_used,
 )

@@ -505,3 +505,122 @@ void oracle_bwd_gated(i64 BH, i64 T, i64 dk, i64 dv, const double *log_gate, con
     free(R);
   }
 }
+
+/* ====================================================================== */
+/* Per-dimension gates (the vector form of the data-dependent gate, as in   */
+/* "Gated Linear Attention ..." on the LASP-2 page's related list): one      */
+/* decay per token, head and key dimension, g_t[i] = log(alpha_t[i]) <= 0:  */
+/*     S_t = diag(alpha_t) S_{t-1} + k_t v_t^T,     o_t = S_t^T q_t.        */
+/* log_gate: [BH][T][dk].                                                   */
+/* ====================================================================== */
+void oracle_fwd_gated_vec(i64 BH, i64 T, i64 dk, i64 dv, const double *log_gate, const double *q,
+                          const double *k, const double *v, const double *init, double *o,
+                          double *final_state) {
+#pragma omp parallel for schedule(dynamic, 1)
+  for (i64 bh = 0; bh < BH; ++bh) {
+    double *S = calloc((size_t)(dk * dv), sizeof(double));
+    if (init) memcpy(S, init + bh * dk * dv, sizeof(double) * dk * dv);
+    for (i64 t = 0; t < T; ++t) {
+      const double *g = log_gate + (bh * T + t) * dk;
+      const double *qt = q + (bh * T + t) * dk;
+      const double *kt = k + (bh * T + t) * dk;
+      const double *vt = v + (bh * T + t) * dv;
+      double *ot = o + (bh * T + t) * dv;
+      for (i64 i = 0; i < dk; ++i) {
+        const double a = exp(g[i]);
+        for (i64 j = 0; j < dv; ++j) S[i * dv + j] = a * S[i * dv + j] + kt[i] * vt[j];
+      }
+      for (i64 j = 0; j < dv; ++j) {
+        double acc = 0.0;
+        for (i64 i = 0; i < dk; ++i) acc += S[i * dv + j] * qt[i];
+        ot[j] = acc;
+      }
+    }
+    if (final_state) memcpy(final_state + bh * dk * dv, S, sizeof(double) * dk * dv);
+    free(S);
+  }
+}
+
+/* Backward of oracle_fwd_gated_vec, the chain rule on the recurrence row by */
+/* row:  R_t = q_t dO_t^T + diag(alpha_{t+1}) R_{t+1}   (starting at d_final) */
+/*   dq_t = S_t dO_t,  dk_t = R_t v_t,  dv_t = R_t^T k_t,                    */
+/*   dL/dg_t[i] = alpha_t[i] sum_j R_t[i][j] S_{t-1}[i][j],                   */
+/*   d_init = diag(alpha_0) R_0.   S_{t-1} recomputed per 64-token block.      */
+void oracle_bwd_gated_vec(i64 BH, i64 T, i64 dk, i64 dv, const double *log_gate, const double *q,
+                          const double *k, const double *v, const double *dO, const double *init,
+                          const double *d_final, double *dq, double *dkk, double *dvv, double *d_log_gate,
+                          double *d_init) {
+  const i64 D = dk * dv, NB = 64, nblk = (T + NB - 1) / NB;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (i64 bh = 0; bh < BH; ++bh) {
+    const double *lg = log_gate + bh * T * dk;
+    double *S = calloc((size_t)D, sizeof(double));
+    double *keep = calloc((size_t)((nblk + 1) * D), sizeof(double));
+    double *blk = calloc((size_t)((NB + 1) * D), sizeof(double));
+    double *R = calloc((size_t)D, sizeof(double));
+    if (init) memcpy(S, init + bh * D, sizeof(double) * D);
+    for (i64 t = 0; t < T; ++t) {
+      if (t % NB == 0) memcpy(keep + (t / NB) * D, S, sizeof(double) * D);
+      const double *kt = k + (bh * T + t) * dk, *vt = v + (bh * T + t) * dv, *gt = dO + (bh * T + t) * dv;
+      double *dqt = dq + (bh * T + t) * dk;
+      for (i64 i = 0; i < dk; ++i) {
+        const double a = exp(lg[t * dk + i]);
+        double acc = 0.0;
+        for (i64 j = 0; j < dv; ++j) {
+          S[i * dv + j] = a * S[i * dv + j] + kt[i] * vt[j];
+          acc += S[i * dv + j] * gt[j];
+        }
+        dqt[i] = acc;
+      }
+    }
+    if (d_final) memcpy(R, d_final + bh * D, sizeof(double) * D);
+    for (i64 b = nblk - 1; b >= 0; --b) {
+      const i64 t0 = b * NB, t1 = (t0 + NB < T) ? t0 + NB : T;
+      memcpy(blk, keep + b * D, sizeof(double) * D);
+      for (i64 t = t0; t < t1 - 1; ++t) {
+        const double *kt = k + (bh * T + t) * dk, *vt = v + (bh * T + t) * dv;
+        double *prev = blk + (t - t0) * D, *next = blk + (t - t0 + 1) * D;
+        for (i64 i = 0; i < dk; ++i) {
+          const double a = exp(lg[t * dk + i]);
+          for (i64 j = 0; j < dv; ++j) next[i * dv + j] = a * prev[i * dv + j] + kt[i] * vt[j];
+        }
+      }
+      for (i64 t = t1 - 1; t >= t0; --t) {
+        const double *qt = q + (bh * T + t) * dk, *kt = k + (bh * T + t) * dk;
+        const double *vt = v + (bh * T + t) * dv, *gt = dO + (bh * T + t) * dv;
+        for (i64 i = 0; i < dk; ++i) {
+          const double carry = (t == T - 1) ? 1.0 : exp(lg[(t + 1) * dk + i]);
+          for (i64 j = 0; j < dv; ++j) R[i * dv + j] = carry * R[i * dv + j] + qt[i] * gt[j];
+        }
+        double *dkt = dkk + (bh * T + t) * dk, *dvt = dvv + (bh * T + t) * dv;
+        for (i64 i = 0; i < dk; ++i) {
+          double acc = 0.0;
+          for (i64 j = 0; j < dv; ++j) acc += R[i * dv + j] * vt[j];
+          dkt[i] = acc;
+        }
+        for (i64 j = 0; j < dv; ++j) {
+          double acc = 0.0;
+          for (i64 i = 0; i < dk; ++i) acc += R[i * dv + j] * kt[i];
+          dvt[j] = acc;
+        }
+        if (d_log_gate) {
+          const double *sp = blk + (t - t0) * D;
+          for (i64 i = 0; i < dk; ++i) {
+            double acc = 0.0;
+            for (i64 j = 0; j < dv; ++j) acc += R[i * dv + j] * sp[i * dv + j];
+            d_log_gate[(bh * T + t) * dk + i] = exp(lg[t * dk + i]) * acc;
+          }
+        }
+      }
+    }
+    if (d_init)
+      for (i64 i = 0; i < dk; ++i) {
+        const double a0 = T > 0 ? exp(lg[i]) : 1.0;
+        for (i64 j = 0; j < dv; ++j) d_init[bh * D + i * dv + j] = a0 * R[i * dv + j];
+      }
+    free(S);
+    free(keep);
+    free(blk);
+    free(R);
+  }
+}

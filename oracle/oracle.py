@@ -55,10 +55,13 @@ def _load():
             lib.oracle_segment_grad_states.argtypes = [i64, i64, i64, i64, dp, i64, dp, dp, dp]
             lib.oracle_fwd_gated.argtypes = [i64, i64, i64, i64, dp, dp, dp, dp, dp, dp, dp]
             lib.oracle_bwd_gated.argtypes = [i64, i64, i64, i64, dp, dp, dp, dp, dp, dp, dp, dp, dp, dp, dp, dp]
+            lib.oracle_fwd_gated_vec.argtypes = [i64, i64, i64, i64, dp, dp, dp, dp, dp, dp, dp]
+            lib.oracle_bwd_gated_vec.argtypes = [i64, i64, i64, i64, dp, dp, dp, dp, dp, dp, dp, dp, dp, dp, dp, dp]
             lib.oracle_state_scan.argtypes = [i64, i64, i64, i64, dp, dp, dp, dp, dp]
             for f in ("oracle_fwd_recurrent", "oracle_bwd_recurrent", "oracle_fwd_chunked",
                       "oracle_bwd_chunked", "oracle_segment_states", "oracle_segment_grad_states",
-                      "oracle_state_scan", "oracle_fwd_gated", "oracle_bwd_gated"):
+                      "oracle_state_scan", "oracle_fwd_gated", "oracle_bwd_gated", "oracle_fwd_gated_vec",
+                      "oracle_bwd_gated_vec"):
                 getattr(lib, f).restype = None
             _lib = lib
     return _lib
@@ -278,4 +281,31 @@ def bwd_gated(q, k, v, dO, log_gate, init=None, d_final=None):
     dinit = np.empty((B, H, dk, dv))
     _load().oracle_bwd_gated(B * H, T, dk, dv, _ptr(lg), _ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(init),
                              _ptr(d_final), _ptr(dq), _ptr(dkk), _ptr(dvv), _ptr(dlg), _ptr(dinit))
+    return dq, dkk, dvv, dlg, dinit
+
+
+# ----------------------------------------------------------------------------- per-dimension gates
+def fwd_gated_vec(q, k, v, log_gate, init=None):
+    """S_t = diag(exp(log_gate_t)) S_{t-1} + k_t v_t^T, o_t = S_t^T q_t: one gate per token,
+    head and key dimension, log_gate [B, H, T, dk].  Returns (o, final_state)."""
+    q, k, v, init, lg = _f64(q), _f64(k), _f64(v), _f64(init), _f64(log_gate)
+    B, H, T, dk, dv = _dims(q, k, v)
+    assert lg.shape == (B, H, T, dk)
+    o = np.empty((B, H, T, dv))
+    fin = np.empty((B, H, dk, dv))
+    _load().oracle_fwd_gated_vec(B * H, T, dk, dv, _ptr(lg), _ptr(q), _ptr(k), _ptr(v), _ptr(init), _ptr(o),
+                                 _ptr(fin))
+    return o, fin
+
+
+def bwd_gated_vec(q, k, v, dO, log_gate, init=None, d_final=None):
+    """Returns (dq, dk, dv, d_log_gate [B, H, T, dk], d_init) of <dO, o> (+ <d_final, final_state>)."""
+    q, k, v, dO, init, d_final, lg = (_f64(x) for x in (q, k, v, dO, init, d_final, log_gate))
+    B, H, T, dk, dv = _dims(q, k, v)
+    assert lg.shape == (B, H, T, dk)
+    dq, dkk, dvv = np.empty_like(q), np.empty_like(k), np.empty_like(v)
+    dlg = np.empty((B, H, T, dk))
+    dinit = np.empty((B, H, dk, dv))
+    _load().oracle_bwd_gated_vec(B * H, T, dk, dv, _ptr(lg), _ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(init),
+                                 _ptr(d_final), _ptr(dq), _ptr(dkk), _ptr(dvv), _ptr(dlg), _ptr(dinit))
     return dq, dkk, dvv, dlg, dinit

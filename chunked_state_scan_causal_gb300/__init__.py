@@ -68,6 +68,9 @@ _SIGS = {
     "linattn_fwd_gated": ([ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _sz, _vp], _i32),
     "linattn_bwd_gated": ([ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _vp, _vp, _vp,
                            _vp, _vp, _sz, _vp], _i32),
+    "linattn_fwd_gated_vec": ([ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp], _i32),
+    "linattn_bwd_gated_vec": ([ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                               _vp], _i32),
     "linattn_decode": ([ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp], _i32),
     "linattn_state_scan_workspace_size": ([_i32, _i32, _i32, _i32, ctypes.POINTER(_sz)], _i32),
     "linattn_state_scan": ([_i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
@@ -83,7 +86,7 @@ _SIGS = {
     "linattn_timing_collect": ([_i32, ctypes.POINTER(_i32), ctypes.POINTER(ctypes.c_float)], _i32),
     "linattn_kernel_name": ([_i32], ctypes.c_char_p),
 }
-KERNEL_KINDS = 13
+KERNEL_KINDS = 15
 
 
 def lib():
@@ -164,6 +167,16 @@ def linattn_bwd_gated(shape, q, k, v, dO, log_gate, init_state, d_final, ckpt, c
                       d_init, ws, ws_bytes, stream) -> int:
     return lib().linattn_bwd_gated(ctypes.byref(shape), q, k, v, dO, log_gate, init_state, d_final, ckpt,
                                    ckpt_bytes, dq, dk, dv, d_log_gate, d_init, ws, ws_bytes, stream)
+
+
+def linattn_fwd_gated_vec(shape, q, k, v, log_gate, o, init_state, final_state, stream) -> int:
+    return lib().linattn_fwd_gated_vec(ctypes.byref(shape), q, k, v, log_gate, o, init_state, final_state, stream)
+
+
+def linattn_bwd_gated_vec(shape, q, k, v, dO, log_gate, init_state, d_final, dq, dk, dv, d_log_gate, d_init,
+                          stream) -> int:
+    return lib().linattn_bwd_gated_vec(ctypes.byref(shape), q, k, v, dO, log_gate, init_state, d_final, dq, dk, dv,
+                                       d_log_gate, d_init, stream)
 
 
 def linattn_chunk_states_rev(shape, seg_len, q, dO, out, ws, ws_bytes, stream) -> int:
@@ -433,6 +446,47 @@ def bwd_gated(q, k, v, dO, log_gate, ckpt, init_state=None, d_final=None, want_d
                            _ptr(d_final), _ptr(ckpt), ckpt.numel(), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dlg),
                            _ptr(dinit), _ptr(ws), ws.numel(), _stream(q.device, stream))
     _check(st, "linattn_bwd_gated")
+    return dq, dk, dv, dlg, dinit
+
+
+def _gate_tensor_vec(log_gate, q):
+    import torch
+    B, H, T, d = q.shape
+    if log_gate.dtype != torch.float32 or not log_gate.is_contiguous() or tuple(log_gate.shape) != (B, H, T, d):
+        raise ValueError("log_gate must be contiguous fp32 [B, H, T, d]")
+    return log_gate
+
+
+def fwd_gated_vec(q, k, v, log_gate, init_state=None, want_final=False, out=None, stream=None):
+    """(o, final_state or None) with a gate per token and key dimension:
+    S_t = diag(exp(log_gate_t)) S_{t-1} + k_t v_t^T (log_gate [B, H, T, d] fp32)."""
+    import torch
+    _same_layout(q, k, v, out)
+    _gate_tensor_vec(log_gate, q)
+    B, H, T, d = q.shape
+    o = out if out is not None else torch.empty_strided(q.shape, q.stride(), dtype=q.dtype, device=q.device)
+    fin = torch.empty((B, H, d, d), dtype=torch.float32, device=q.device) if want_final else None
+    st = linattn_fwd_gated_vec(shape_of(q, None), _ptr(q), _ptr(k), _ptr(v), _ptr(log_gate), _ptr(o),
+                               _ptr(init_state), _ptr(fin), _stream(q.device, stream))
+    _check(st, "linattn_fwd_gated_vec")
+    return o, fin
+
+
+def bwd_gated_vec(q, k, v, dO, log_gate, init_state=None, d_final=None, want_dinit=False, outs=None, stream=None):
+    """(dq, dk, dv, d_log_gate [B, H, T, d], d_init or None) of fwd_gated_vec for the upstream gradient dO."""
+    import torch
+    _same_layout(q, k, v, dO)
+    _gate_tensor_vec(log_gate, q)
+    B, H, T, d = q.shape
+    if outs is None:
+        outs = [torch.empty_strided(q.shape, q.stride(), dtype=q.dtype, device=q.device) for _ in range(3)]
+    dq, dk, dv = outs
+    dlg = torch.empty((B, H, T, d), dtype=torch.float32, device=q.device)
+    dinit = torch.empty((B, H, d, d), dtype=torch.float32, device=q.device) if want_dinit else None
+    st = linattn_bwd_gated_vec(shape_of(q, None), _ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(log_gate),
+                               _ptr(init_state), _ptr(d_final), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dlg), _ptr(dinit),
+                               _stream(q.device, stream))
+    _check(st, "linattn_bwd_gated_vec")
     return dq, dk, dv, dlg, dinit
 
 

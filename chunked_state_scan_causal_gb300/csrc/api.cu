@@ -544,6 +544,49 @@ int32_t linattn_bwd_gated(const linattn_shape *shape, const void *q, const void 
   return cuda_status(e);
 }
 
+int32_t linattn_fwd_gated_vec(const linattn_shape *shape, const void *q, const void *k, const void *v,
+                              const float *log_gate, void *o, const float *init_state, float *final_state,
+                              void *stream) {
+  Problem p;
+  int st = validate(shape, &p);
+  if (st) return st;
+  if (p.decay) return LINATTN_ERR_INVALID;  // the gates replace the per-head decay
+  if ((st = check_ptrs({}, {init_state, final_state}))) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (p.T == 0) {
+    if (!final_state) return LINATTN_OK;
+    const size_t bytes = (size_t)p.B * p.H * p.d * p.d * sizeof(float);
+    return cuda_status(init_state ? cudaMemcpyAsync(final_state, init_state, bytes, cudaMemcpyDeviceToDevice, s)
+                                  : cudaMemsetAsync(final_state, 0, bytes, s));
+  }
+  if ((st = check_ptrs({q, k, v, o, log_gate}, {}))) return st;
+  if ((st = device_ok())) return st;
+  return cuda_status(gated_vec_fwd(p, q, k, v, log_gate, o, init_state, final_state, s));
+}
+
+int32_t linattn_bwd_gated_vec(const linattn_shape *shape, const void *q, const void *k, const void *v,
+                              const void *dO, const float *log_gate, const float *init_state,
+                              const float *d_final_state, void *dq, void *dk, void *dv, float *d_log_gate,
+                              float *d_init_state, void *stream) {
+  Problem p;
+  int st = validate(shape, &p);
+  if (st) return st;
+  if (p.decay) return LINATTN_ERR_INVALID;
+  if ((st = check_ptrs({}, {init_state, d_final_state, d_init_state}))) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (p.T == 0) {
+    if (!d_init_state) return LINATTN_OK;
+    const size_t bytes = (size_t)p.B * p.H * p.d * p.d * sizeof(float);
+    return cuda_status(d_final_state
+                           ? cudaMemcpyAsync(d_init_state, d_final_state, bytes, cudaMemcpyDeviceToDevice, s)
+                           : cudaMemsetAsync(d_init_state, 0, bytes, s));
+  }
+  if ((st = check_ptrs({q, k, v, dO, log_gate, dq, dk, dv, d_log_gate}, {}))) return st;
+  if ((st = device_ok())) return st;
+  return cuda_status(gated_vec_bwd(p, q, k, v, dO, log_gate, init_state, d_final_state, dq, dk, dv, d_log_gate,
+                                   d_init_state, s));
+}
+
 int32_t linattn_decode(const linattn_shape *shape, const void *q, const void *k, const void *v, void *o,
                        float *state, void *stream) {
   Problem p;
@@ -709,7 +752,8 @@ const char *linattn_kernel_name(int32_t kind) {
   static const char *names[K_KINDS] = {"simt_fwd", "simt_bwd", "simt_segment_states", "state_scan",
                                        "tc_segment_aggregate", "tc_chunked_fwd",
                                        "diag_mma", "decode", "tc_dual_rev", "tc_chunked_fwd_agg",
-                                       "gate_prep_and_grad", "tc_chunk_states", "softmax_segment"};
+                                       "gate_prep_and_grad", "tc_chunk_states", "softmax_segment",
+                                       "gated_vec_fwd", "gated_vec_bwd"};
   return (kind >= 0 && kind < K_KINDS) ? names[kind] : "?";
 }
 

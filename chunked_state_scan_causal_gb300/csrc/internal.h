@@ -57,7 +57,8 @@ int device_ok();
 // ---------------------------------------------------------------- per-kernel timing (api.cu)
 enum KernelKind {
   K_SIMT_FWD = 0, K_SIMT_BWD, K_SIMT_SEGMENT, K_SCAN, K_TC_AGG, K_TC_MAIN_FWD, K_DIAG,
-  K_DECODE, K_TC_DUAL_REV, K_TC_MAIN_AGG, K_GATE, K_TC_CHUNK_STATES, K_SOFTMAX_SEGMENT, K_KINDS
+  K_DECODE, K_TC_DUAL_REV, K_TC_MAIN_AGG, K_GATE, K_TC_CHUNK_STATES, K_SOFTMAX_SEGMENT, K_GATED_VEC_FWD,
+  K_GATED_VEC_BWD, K_KINDS
 };
 // Records timing events around one launch on `s` while timing is enabled.
 struct TimedLaunch {
@@ -178,6 +179,13 @@ struct SoftmaxProblem {
   float scale;
   int num_sms;
 };
+// Per-dimension gates (gate_vec.cu): one CTA per (batch, head) walks the sequence;
+// log_gate and d_log_gate are [B*H][T][d] fp32.
+cudaError_t gated_vec_fwd(const Problem &p, const void *q, const void *k, const void *v, const float *log_gate,
+                          void *o, const float *init, float *final_state, cudaStream_t s);
+cudaError_t gated_vec_bwd(const Problem &p, const void *q, const void *k, const void *v, const void *dO,
+                          const float *log_gate, const float *init, const float *d_final, void *dq, void *dk,
+                          void *dv, float *d_log_gate, float *d_init, cudaStream_t s);
 cudaError_t softmax_segment(const SoftmaxProblem &p, const void *q, const void *k, const void *v, void *o, float *lse,
                             int *status, cudaStream_t s);
 

@@ -186,6 +186,31 @@ int32_t linattn_bwd_gated(const linattn_shape *shape, const void *q, const void 
                           void *dk, void *dv, float *d_log_gate, float *d_init_state, void *workspace,
                           size_t workspace_bytes, void *stream);
 
+/* Per-dimension gates (the vector form of the data-dependent gate: "Gated
+ * Linear Attention ..." on the LASP-2 page's related list): a decay per token,
+ * head and KEY dimension, alpha_t[i] = exp(log_gate_t[i]),
+ *   S_t = diag(alpha_t) S_{t-1} + k_t v_t^T,   o_t = S_t^T q_t
+ * (row i of the state decays by the gate of key dimension i).  log_gate is
+ * [B,H,T,d] fp32, contiguous, 16-byte aligned; the shape's decay must be NULL.
+ * Runs on CUDA-core kernels that walk every sequence token by token, one CTA
+ * per (batch, head), fp32 state in shared memory: correct for any length,
+ * meant for moderate T (the per-token gates above have the tensor-core path).
+ * No workspace and no device-side waits.  Returns a status. */
+int32_t linattn_fwd_gated_vec(const linattn_shape *shape, const void *q, const void *k, const void *v,
+                              const float *log_gate, void *o, const float *init_state, float *final_state,
+                              void *stream);
+
+/* Backward of linattn_fwd_gated_vec for an upstream gradient dO and the
+ * gradient d_final_state arriving at the final state (or NULL): dq, dk, dv,
+ * d_init_state = diag(alpha_0) R_0 (R the state gradient), and the gradient of
+ * every log-gate ([B,H,T,d] fp32, contiguous)
+ *   d_log_gate[t][i] = sum_{u >= t} (q_u[i] dq_u[i] - k_u[i] dk_u[i]) + sum_j D[i][j] S_final[i][j].
+ * The forward states are recomputed from init_state.  Returns a status. */
+int32_t linattn_bwd_gated_vec(const linattn_shape *shape, const void *q, const void *k, const void *v,
+                              const void *dO, const float *log_gate, const float *init_state,
+                              const float *d_final_state, void *dq, void *dk, void *dv, float *d_log_gate,
+                              float *d_init_state, void *stream);
+
 /* Recurrent decode of T new tokens per sequence (constant-memory inference:
  * LASP-2 page, abstract): for t = 0..T-1
  *   S <- lambda S + k_t v_t^T,   o_t = S^T q_t,
@@ -315,7 +340,7 @@ int32_t linattn_device_status(const void *workspace, void *stream);
  * for every kernel kind k < max_kinds its launch count and summed device time
  * (ms), clears the record and returns the number of kinds
  * (LINATTN_KERNEL_KINDS), or a negative status. */
-#define LINATTN_KERNEL_KINDS 13
+#define LINATTN_KERNEL_KINDS 15
 int32_t linattn_timing_enable(int32_t on);
 int32_t linattn_timing_collect(int32_t max_kinds, int32_t *launches, float *total_ms);
 /* Name of kernel kind k (static string; "?" when out of range). */

@@ -86,7 +86,7 @@ _SIGS = {
     "linattn_timing_collect": ([_i32, ctypes.POINTER(_i32), ctypes.POINTER(ctypes.c_float)], _i32),
     "linattn_kernel_name": ([_i32], ctypes.c_char_p),
 }
-KERNEL_KINDS = 15
+KERNEL_KINDS = 16
 
 
 def lib():

@@ -14,7 +14,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(OUT_DIR, "liblinattn.so")
-SOURCES = ["api.cu", "simt.cu", "scan.cu", "tc.cu", "diag.cu", "decode.cu", "gate.cu", "softmax.cu", "gate_vec.cu"]
+SOURCES = ["api.cu", "simt.cu", "scan.cu", "tc.cu", "diag.cu", "decode.cu", "gate.cu", "softmax.cu", "gate_vec.cu",
+           "pad.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
 

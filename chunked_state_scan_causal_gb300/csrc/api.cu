@@ -176,10 +176,40 @@ static BwdLayout bwd_layout(const Problem &p) {
   return w;
 }
 
+// bf16 with d = 64 runs on the tensor-core kernels through zero-padded d = 128
+// copies of its sequence tensors and states (pad.cu: the padded problem is the
+// same problem).  The padded copies sit after the d = 128 workspace, whose
+// status word stays at offset 0.  Per-chunk states of linattn_fwd keep the
+// CUDA-core path.
+static bool padded(const Problem &p) { return p.dtype == 0 && p.d == 64 && p.T > 0; }
+static Problem padded_problem(const Problem &p) {
+  Problem q = p;
+  q.d = 128;
+  q.st = 128;
+  q.sh = (int64_t)p.T * 128;
+  q.sb = (int64_t)p.H * q.sh;
+  return q;
+}
+static size_t pad_rows_bytes(const Problem &p) { return align256((size_t)p.B * p.H * p.T * 128 * 2); }
+static size_t pad_state_bytes(const Problem &p) { return align256((size_t)p.B * p.H * 128 * 128 * sizeof(float)); }
+
 // Checkpoint of the forward group states: [G][BH][d][d] fp32 (tensor-core path only).
 static size_t ckpt_bytes(const Problem &p) {
+  if (padded(p)) return ckpt_bytes(padded_problem(p));
   const FwdLayout w = fwd_layout(p);
   return w.G == 0 ? 0 : (size_t)w.G * p.B * p.H * p.d * p.d * sizeof(float);
+}
+// workspace of linattn_fwd / linattn_bwd: the d = 128 layout, then (padded) q, k, v, o
+// and two states, or q, k, v, dO, dq, dk, dv and three states
+static size_t fwd_ws_bytes(const Problem &p) {
+  if (!padded(p)) return fwd_layout(p).total;
+  const Problem q = padded_problem(p);
+  return align256(fwd_layout(q).total) + 4 * pad_rows_bytes(p) + 2 * pad_state_bytes(p);
+}
+static size_t bwd_ws_bytes(const Problem &p) {
+  if (!padded(p)) return bwd_layout(p).total;
+  const Problem q = padded_problem(p);
+  return align256(bwd_layout(q).total) + 7 * pad_rows_bytes(p) + 3 * pad_state_bytes(p);
 }
 
 // Gated layouts: the forward layout plus the gates' cumulative sums [BH][T],
@@ -261,9 +291,9 @@ int32_t linattn_workspace_size(const linattn_shape *shape, int32_t op, int32_t s
   int st = validate(shape, &p);
   if (st) return st;
   if (op == LINATTN_OP_FWD) {
-    *bytes = fwd_layout(p).total;
+    *bytes = fwd_ws_bytes(p);
   } else if (op == LINATTN_OP_BWD) {
-    *bytes = bwd_layout(p).total;
+    *bytes = bwd_ws_bytes(p);
   } else if (op == LINATTN_OP_CHUNK_STATES) {
     if (seg_len < 1) return LINATTN_ERR_INVALID;
     *bytes = kHeader;
@@ -291,8 +321,10 @@ static int32_t fwd_impl(const linattn_shape *shape, const void *q, const void *k
   if (st) return st;
   if (p.T > 0 && (st = check_ptrs({q, k, v, o}, {}))) return st;
   if ((st = check_ptrs({}, {init_state, final_state, chunk_states}))) return st;
-  const FwdLayout w = fwd_layout(p);
-  if ((st = check_ws(workspace, workspace_bytes, w.total))) return st;
+  const bool pad = padded(p) && !chunk_states;
+  const Problem pt = pad ? padded_problem(p) : p;  // the problem the kernels run
+  const FwdLayout w = fwd_layout(pt);
+  if ((st = check_ws(workspace, workspace_bytes, pad ? fwd_ws_bytes(p) : w.total))) return st;
   const size_t need_ckpt = want_ckpt ? ckpt_bytes(p) : 0;
   if (need_ckpt && (!ckpt || (reinterpret_cast<uintptr_t>(ckpt) & 255u) || ckpt_size < need_ckpt))
     return LINATTN_ERR_INVALID;
@@ -312,18 +344,39 @@ static int32_t fwd_impl(const linattn_shape *shape, const void *q, const void *k
     }
     return LINATTN_OK;
   }
-  if (!tc_supported(p))
+  if (!tc_supported(pt))
     return cuda_status(simt_fwd(p, q, k, v, o, init_state, final_state, chunk_states, s));
+  cudaError_t e = cudaSuccess;
+  const void *qk[3] = {q, k, v};
+  void *out = o;
+  const float *init = init_state;
+  float *fin = final_state;
+  if (pad) {
+    char *pb = ws + align256(w.total);
+    const size_t R = pad_rows_bytes(p), SB = pad_state_bytes(p);
+    for (int i = 0; i < 3 && e == cudaSuccess; ++i) {
+      e = pad_rows_d64(p, qk[i], pb + i * R, s);
+      qk[i] = pb + i * R;
+    }
+    out = pb + 3 * R;
+    if (init && e == cudaSuccess) {
+      e = pad_state_d64(init_state, reinterpret_cast<float *>(pb + 4 * R), BH, s);
+      init = reinterpret_cast<const float *>(pb + 4 * R);
+    }
+    if (fin) fin = reinterpret_cast<float *>(pb + 4 * R + SB);
+  }
   // tensor-core path: chunk-group aggregates -> exclusive scan of the group states
   // -> chunked forward of every group from its entering state
   float *agg = reinterpret_cast<float *>(ws + w.agg);
   float *states = need_ckpt ? ckpt : reinterpret_cast<float *>(ws + w.states);
-  cudaError_t e = tc_segment_states(p, w.gp, k, v, false, agg, status, s);
-  if (e == cudaSuccess) e = plan_scan(p, w.gp, false, agg, init_state, states, nullptr, ws + w.scan, status, s);
-  if (e == cudaSuccess) e = tc_main(p, w.gp, q, k, v, o, states, false, final_state, status, s);
+  if (e == cudaSuccess) e = tc_segment_states(pt, w.gp, qk[1], qk[2], false, agg, status, s);
+  if (e == cudaSuccess) e = plan_scan(pt, w.gp, false, agg, init, states, nullptr, ws + w.scan, status, s);
+  if (e == cudaSuccess) e = tc_main(pt, w.gp, qk[0], qk[1], qk[2], out, states, false, fin, status, s);
   // per-chunk (C = 64) exclusive states, when asked for: every group walked again
   // from its entering state, one state out per chunk
-  if (e == cudaSuccess && chunk_states) e = tc_chunk_states(p, w.gp, k, v, states, chunk_states, status, s);
+  if (e == cudaSuccess && chunk_states) e = tc_chunk_states(pt, w.gp, qk[1], qk[2], states, chunk_states, status, s);
+  if (pad && e == cudaSuccess) e = unpad_rows_d64(p, out, o, s);
+  if (pad && fin && e == cudaSuccess) e = unpad_state_d64(fin, final_state, BH, s);
   return cuda_status(e);
 }
 
@@ -350,8 +403,10 @@ static int32_t bwd_impl(const linattn_shape *shape, const void *q, const void *k
   if (st) return st;
   if (p.T > 0 && (st = check_ptrs({q, k, v, dO, dq, dk, dv}, {}))) return st;
   if ((st = check_ptrs({}, {init_state, d_final, d_init_state}))) return st;
-  const BwdLayout w = bwd_layout(p);
-  if ((st = check_ws(workspace, workspace_bytes, w.total))) return st;
+  const bool pad = padded(p);
+  const Problem pt = pad ? padded_problem(p) : p;  // the problem the kernels run
+  const BwdLayout w = bwd_layout(pt);
+  if ((st = check_ws(workspace, workspace_bytes, pad ? bwd_ws_bytes(p) : w.total))) return st;
   const size_t need_ckpt = use_ckpt ? ckpt_bytes(p) : 0;
   if (need_ckpt && (!ckpt || (reinterpret_cast<uintptr_t>(ckpt) & 255u) || ckpt_size < need_ckpt))
     return LINATTN_ERR_INVALID;
@@ -369,20 +424,45 @@ static int32_t bwd_impl(const linattn_shape *shape, const void *q, const void *k
                                  : cudaMemsetAsync(d_init_state, 0, state_bytes, s));
     return LINATTN_OK;
   }
-  if (!tc_supported(p))
+  if (!tc_supported(pt))
     return cuda_status(simt_bwd(p, q, k, v, dO, init_state, d_final, dq, dk, dv, d_init_state, s));
+  cudaError_t e = cudaSuccess;
+  void *const user_out[3] = {dq, dk, dv};
+  float *const user_dinit = d_init_state;
+  if (pad) {
+    char *pb = ws + align256(w.total);
+    const size_t R = pad_rows_bytes(p), SB = pad_state_bytes(p);
+    const void *in[4] = {q, k, v, dO};
+    for (int i = 0; i < 4 && e == cudaSuccess; ++i) e = pad_rows_d64(p, in[i], pb + i * R, s);
+    q = pb;
+    k = pb + R;
+    v = pb + 2 * R;
+    dO = pb + 3 * R;
+    dq = pb + 4 * R;
+    dk = pb + 5 * R;
+    dv = pb + 6 * R;
+    char *sp = pb + 7 * R;
+    if (init_state && e == cudaSuccess) {
+      e = pad_state_d64(init_state, reinterpret_cast<float *>(sp), BH, s);
+      init_state = reinterpret_cast<const float *>(sp);
+    }
+    if (d_final && e == cudaSuccess) {
+      e = pad_state_d64(d_final, reinterpret_cast<float *>(sp + SB), BH, s);
+      d_final = reinterpret_cast<const float *>(sp + SB);
+    }
+    if (d_init_state) d_init_state = reinterpret_cast<float *>(sp + 2 * SB);
+  }
   const GroupPlan &gp = w.f.gp;
   const int G = gp.G;
   float *agg = reinterpret_cast<float *>(ws + w.f.agg);
   float *wagg = reinterpret_cast<float *>(ws + w.wagg);
   float *rbar = reinterpret_cast<float *>(ws + w.rbar);
-  cudaError_t e = cudaSuccess;
   // forward group states: from the checkpoint, or recomputed from k, v and init_state
   const float *states = ckpt;
   if (!need_ckpt) {
     float *st = reinterpret_cast<float *>(ws + w.f.states);
-    e = tc_segment_states(p, gp, k, v, false, agg, status, s);
-    if (e == cudaSuccess) e = plan_scan(p, gp, false, agg, init_state, st, nullptr, ws + w.f.scan, status, s);
+    if (e == cudaSuccess) e = tc_segment_states(pt, gp, k, v, false, agg, status, s);
+    if (e == cudaSuccess) e = plan_scan(pt, gp, false, agg, init_state, st, nullptr, ws + w.f.scan, status, s);
     states = st;
   }
   // dq: the forward-time kernel with (q, k, v) := (dO, v, k), reading every
@@ -392,19 +472,24 @@ static int32_t bwd_impl(const linattn_shape *shape, const void *q, const void *k
   // q_t dO_t^T).  The dq pass accumulates those aggregates too, for every head
   // without a decay or with one of at least 0.8; the aggregate pass computes
   // them for the heads with smaller decays and passes over the others.
-  if (e == cudaSuccess) e = tc_main(p, gp, dO, v, k, dq, states, true, nullptr, status, s, q, wagg);
-  if (e == cudaSuccess && p.decay) e = tc_segment_states(p, gp, q, dO, true, wagg, status, s, true);
+  if (e == cudaSuccess) e = tc_main(pt, gp, dO, v, k, dq, states, true, nullptr, status, s, q, wagg);
+  if (e == cudaSuccess && p.decay) e = tc_segment_states(pt, gp, q, dO, true, wagg, status, s, true);
   // A gradient D arriving at the final state enters the reverse scan across the
   // last group, whose length may be short of L: fold lambda^{len} D into that
   // group's aggregate, scan from zero, and give the last group D itself.
-  const int64_t E = BH * p.d * p.d;
+  const int64_t E = BH * pt.d * pt.d;
   if (e == cudaSuccess && d_final)
-    e = fold_state(wagg + (int64_t)(G - 1) * E, d_final, p.decay, p.H, p.d * p.d, gp.len(G - 1, p.T), E, s);
-  if (e == cudaSuccess) e = plan_scan(p, gp, true, wagg, nullptr, rbar, d_init_state, ws + w.f.scan, status, s);
+    e = fold_state(wagg + (int64_t)(G - 1) * E, d_final, p.decay, p.H, pt.d * pt.d, gp.len(G - 1, p.T), E, s);
+  if (e == cudaSuccess) e = plan_scan(pt, gp, true, wagg, nullptr, rbar, d_init_state, ws + w.f.scan, status, s);
   if (e == cudaSuccess && d_final)
-    e = cudaMemcpyAsync(rbar + (int64_t)(G - 1) * E, d_final, state_bytes, cudaMemcpyDeviceToDevice, s);
+    e = cudaMemcpyAsync(rbar + (int64_t)(G - 1) * E, d_final, (size_t)E * sizeof(float), cudaMemcpyDeviceToDevice, s);
   // dv and dk in one reverse-time pass from the states Rbar
-  if (e == cudaSuccess) e = tc_dual(p, gp, q, k, v, dO, dk, dv, rbar, status, s);
+  if (e == cudaSuccess) e = tc_dual(pt, gp, q, k, v, dO, dk, dv, rbar, status, s);
+  if (pad) {
+    for (int i = 0; i < 3 && e == cudaSuccess; ++i)
+      e = unpad_rows_d64(p, i == 0 ? dq : (i == 1 ? dk : dv), user_out[i], s);
+    if (user_dinit && e == cudaSuccess) e = unpad_state_d64(d_init_state, user_dinit, BH, s);
+  }
   return cuda_status(e);
 }
 
@@ -753,7 +838,7 @@ const char *linattn_kernel_name(int32_t kind) {
                                        "tc_segment_aggregate", "tc_chunked_fwd",
                                        "diag_mma", "decode", "tc_dual_rev", "tc_chunked_fwd_agg",
                                        "gate_prep_and_grad", "tc_chunk_states", "softmax_segment",
-                                       "gated_vec_fwd", "gated_vec_bwd"};
+                                       "gated_vec_fwd", "gated_vec_bwd", "pad_d64"};
   return (kind >= 0 && kind < K_KINDS) ? names[kind] : "?";
 }
 

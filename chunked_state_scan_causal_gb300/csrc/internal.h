@@ -58,7 +58,7 @@ int device_ok();
 enum KernelKind {
   K_SIMT_FWD = 0, K_SIMT_BWD, K_SIMT_SEGMENT, K_SCAN, K_TC_AGG, K_TC_MAIN_FWD, K_DIAG,
   K_DECODE, K_TC_DUAL_REV, K_TC_MAIN_AGG, K_GATE, K_TC_CHUNK_STATES, K_SOFTMAX_SEGMENT, K_GATED_VEC_FWD,
-  K_GATED_VEC_BWD, K_KINDS
+  K_GATED_VEC_BWD, K_PAD_D64, K_KINDS
 };
 // Records timing events around one launch on `s` while timing is enabled.
 struct TimedLaunch {
@@ -179,6 +179,12 @@ struct SoftmaxProblem {
   float scale;
   int num_sms;
 };
+// Zero padding of bf16 d = 64 problems to d = 128 (pad.cu): sequence rows at the
+// request's strides <-> contiguous [B*H*T][128]; states [n][64][64] <-> [n][128][128].
+cudaError_t pad_rows_d64(const Problem &p, const void *src, void *dst, cudaStream_t s);
+cudaError_t unpad_rows_d64(const Problem &p, const void *src, void *dst, cudaStream_t s);
+cudaError_t pad_state_d64(const float *src, float *dst, int64_t n, cudaStream_t s);
+cudaError_t unpad_state_d64(const float *src, float *dst, int64_t n, cudaStream_t s);
 // Per-dimension gates (gate_vec.cu): one CTA per (batch, head) walks the sequence;
 // log_gate and d_log_gate are [B*H][T][d] fp32.
 cudaError_t gated_vec_fwd(const Problem &p, const void *q, const void *k, const void *v, const float *log_gate,

@@ -36,10 +36,14 @@
  *    initial state (or zeros) and d_init_state is zero.
  *  - States are fp32, row-major [.., d_k, d_v] (row index = key dimension).
  *  - Paths: bf16 with d = 128 runs on the tensor-core kernels (chunk groups
- *    processed in parallel, states joined by the scan).  fp32 inputs and
- *    d = 64 run on CUDA-core kernels that walk every sequence serially, one
- *    CTA per (batch, head): correct for any length but far slower on long
- *    sequences (meant for fp32 checks and small heads).
+ *    processed in parallel, states joined by the scan).  bf16 with d = 64
+ *    runs on the same kernels through zero-padded d = 128 copies of the
+ *    sequence tensors and states in the workspace (exact: the padded columns
+ *    stay zero), for linattn_fwd / _ckpt and linattn_bwd / _ckpt without
+ *    per-chunk states.  fp32 inputs, the other d = 64 requests and the gated
+ *    entry points at d = 64 run on CUDA-core kernels that walk every sequence
+ *    serially, one CTA per (batch, head): correct for any length but far
+ *    slower on long sequences (meant for fp32 checks and small heads).
  */
 #ifndef LINATTN_H
 #define LINATTN_H
@@ -340,7 +344,7 @@ int32_t linattn_device_status(const void *workspace, void *stream);
  * for every kernel kind k < max_kinds its launch count and summed device time
  * (ms), clears the record and returns the number of kinds
  * (LINATTN_KERNEL_KINDS), or a negative status. */
-#define LINATTN_KERNEL_KINDS 15
+#define LINATTN_KERNEL_KINDS 16
 int32_t linattn_timing_enable(int32_t on);
 int32_t linattn_timing_collect(int32_t max_kinds, int32_t *launches, float *total_ms);
 /* Name of kernel kind k (static string; "?" when out of range). */

@@ -313,7 +313,7 @@ def test_forward_backward_decay_forms_mixed_across_items():
             assert rel(got[:, sl], ref) < 1e-2, (h, float(lam[h]))
 
 
-@pytest.mark.parametrize("dtype,d", [(torch.bfloat16, 128), (torch.float32, 64)])
+@pytest.mark.parametrize("dtype,d", [(torch.bfloat16, 128), (torch.bfloat16, 64), (torch.float32, 64)])
 @pytest.mark.parametrize("T,dk", [(2048, None), (8192 + 64, "cfg"), (1000, 0.5)])
 def test_checkpointed_forward_backward(dtype, d, T, dk):
     """fwd_ckpt + bwd_ckpt give the oracle's outputs (the backward reads the stored group states)."""
@@ -373,3 +373,37 @@ def test_decode_steps(dtype, d, T, dk):
     ro, _, rfin = oracle.fwd_recurrent(c["q"], c["k"], c["v"], lam=lam, init=init.astype(np.float64))
     assert rel(o, ro) < TOL[dtype]
     assert rel(state, rfin) < 1e-5
+
+
+def test_bf16_d64_runs_on_the_tensor_core_kernels():
+    """bf16 with d = 64 goes through zero-padded d = 128 copies on the tensor-core
+    kernels: the recorded launches are the chunked kernels and the padding passes,
+    not the CUDA-core walk; many chunk groups, per-head decays, an initial state and a
+    final-state gradient, every head against the oracle."""
+    B, H, T, d = 1, 4, 16384 + 77, 64
+    c, dev = case(61, B, H, T, d, torch.bfloat16, sigma=1 / np.sqrt(64))
+    lam = np.array([1.0, 0.999, 0.9, 0.5], np.float32)
+    dec = torch.from_numpy(lam).cuda()
+    r = np.random.default_rng(62)
+    init = (r.standard_normal((B, H, d, d)) * 0.1).astype(np.float32)
+    D = (r.standard_normal((B, H, d, d)) * 0.1).astype(np.float32)
+    init_d, D_d = torch.from_numpy(init).cuda(), torch.from_numpy(D).cuda()
+    ck = la.checkpoint(dev["q"], dec)
+    wsf, wsb = la.workspace(dev["q"], la.OP_FWD, dec), la.workspace(dev["q"], la.OP_BWD, dec)
+    la.linattn_timing_enable(True)
+    la.linattn_timing_collect()
+    o, fin, _ = la.fwd(dev["q"], dev["k"], dev["v"], decay=dec, init_state=init_d, want_final=True, ws=wsf, ckpt=ck)
+    dq, dk_, dv, dinit = la.bwd(dev["q"], dev["k"], dev["v"], dev["dO"], decay=dec, init_state=init_d, d_final=D_d,
+                                want_dinit=True, ws=wsb, ckpt=ck)
+    torch.cuda.synchronize()
+    kinds = la.linattn_timing_collect()
+    la.linattn_timing_enable(False)
+    assert la.device_status(wsf) == la.OK and la.device_status(wsb) == la.OK
+    assert "tc_chunked_fwd" in kinds and "tc_dual_rev" in kinds and "pad_d64" in kinds, kinds
+    assert "simt_fwd" not in kinds and "simt_bwd" not in kinds, kinds
+    init64, D64 = init.astype(np.float64), D.astype(np.float64)
+    ro, _, rfin = oracle.fwd_recurrent(c["q"], c["k"], c["v"], lam=lam, init=init64)
+    rq, rk, rv, rinit = oracle.bwd_recurrent(c["q"], c["k"], c["v"], c["dO"], lam=lam, init=init64, d_final=D64)
+    for name, got, ref in (("o", o, ro), ("final", fin, rfin), ("dq", dq, rq), ("dk", dk_, rk), ("dv", dv, rv),
+                           ("d_init", dinit, rinit)):
+        assert rel(got, ref) < 1e-2, name

@@ -176,21 +176,20 @@ static BwdLayout bwd_layout(const Problem &p) {
   return w;
 }
 
-// bf16 with d = 64 runs on the tensor-core kernels through zero-padded d = 128
-// copies of its sequence tensors and states (pad.cu: the padded problem is the
-// same problem).  The padded copies sit after the d = 128 workspace, whose
-// status word stays at offset 0.  Per-chunk states of linattn_fwd keep the
-// CUDA-core path.
+// bf16 with d = 64 runs on the d = 128 tensor-core kernels as the zero-padded
+// problem, which is the same problem: the tiles' columns 64..127 of q, k, v load
+// as zeros (the tensor maps give the rows 64 columns), so every q . k and every
+// product with the state is unchanged, the state's rows and columns 64..127 stay
+// zero, and only the first 64 output columns are stored.  The states go through
+// zero-padded 128 x 128 copies (pad.cu), after the d = 128 workspace, whose status
+// word stays at offset 0.  Per-chunk states of linattn_fwd keep the CUDA-core path.
 static bool padded(const Problem &p) { return p.dtype == 0 && p.d == 64 && p.T > 0; }
 static Problem padded_problem(const Problem &p) {
   Problem q = p;
   q.d = 128;
-  q.st = 128;
-  q.sh = (int64_t)p.T * 128;
-  q.sb = (int64_t)p.H * q.sh;
+  q.dcols = 64;
   return q;
 }
-static size_t pad_rows_bytes(const Problem &p) { return align256((size_t)p.B * p.H * p.T * 128 * 2); }
 static size_t pad_state_bytes(const Problem &p) { return align256((size_t)p.B * p.H * 128 * 128 * sizeof(float)); }
 
 // Checkpoint of the forward group states: [G][BH][d][d] fp32 (tensor-core path only).
@@ -199,17 +198,15 @@ static size_t ckpt_bytes(const Problem &p) {
   const FwdLayout w = fwd_layout(p);
   return w.G == 0 ? 0 : (size_t)w.G * p.B * p.H * p.d * p.d * sizeof(float);
 }
-// workspace of linattn_fwd / linattn_bwd: the d = 128 layout, then (padded) q, k, v, o
-// and two states, or q, k, v, dO, dq, dk, dv and three states
+// workspace of linattn_fwd / linattn_bwd: the d = 128 layout, then the padded
+// states (initial and final; or initial, final-state gradient and d_init)
 static size_t fwd_ws_bytes(const Problem &p) {
   if (!padded(p)) return fwd_layout(p).total;
-  const Problem q = padded_problem(p);
-  return align256(fwd_layout(q).total) + 4 * pad_rows_bytes(p) + 2 * pad_state_bytes(p);
+  return align256(fwd_layout(padded_problem(p)).total) + 2 * pad_state_bytes(p);
 }
 static size_t bwd_ws_bytes(const Problem &p) {
   if (!padded(p)) return bwd_layout(p).total;
-  const Problem q = padded_problem(p);
-  return align256(bwd_layout(q).total) + 7 * pad_rows_bytes(p) + 3 * pad_state_bytes(p);
+  return align256(bwd_layout(padded_problem(p)).total) + 3 * pad_state_bytes(p);
 }
 
 // Gated layouts: the forward layout plus the gates' cumulative sums [BH][T],
@@ -353,17 +350,11 @@ static int32_t fwd_impl(const linattn_shape *shape, const void *q, const void *k
   float *fin = final_state;
   if (pad) {
     char *pb = ws + align256(w.total);
-    const size_t R = pad_rows_bytes(p), SB = pad_state_bytes(p);
-    for (int i = 0; i < 3 && e == cudaSuccess; ++i) {
-      e = pad_rows_d64(p, qk[i], pb + i * R, s);
-      qk[i] = pb + i * R;
+    if (init) {
+      e = pad_state_d64(init_state, reinterpret_cast<float *>(pb), BH, s);
+      init = reinterpret_cast<const float *>(pb);
     }
-    out = pb + 3 * R;
-    if (init && e == cudaSuccess) {
-      e = pad_state_d64(init_state, reinterpret_cast<float *>(pb + 4 * R), BH, s);
-      init = reinterpret_cast<const float *>(pb + 4 * R);
-    }
-    if (fin) fin = reinterpret_cast<float *>(pb + 4 * R + SB);
+    if (fin) fin = reinterpret_cast<float *>(pb + pad_state_bytes(p));
   }
   // tensor-core path: chunk-group aggregates -> exclusive scan of the group states
   // -> chunked forward of every group from its entering state
@@ -375,7 +366,6 @@ static int32_t fwd_impl(const linattn_shape *shape, const void *q, const void *k
   // per-chunk (C = 64) exclusive states, when asked for: every group walked again
   // from its entering state, one state out per chunk
   if (e == cudaSuccess && chunk_states) e = tc_chunk_states(pt, w.gp, qk[1], qk[2], states, chunk_states, status, s);
-  if (pad && e == cudaSuccess) e = unpad_rows_d64(p, out, o, s);
   if (pad && fin && e == cudaSuccess) e = unpad_state_d64(fin, final_state, BH, s);
   return cuda_status(e);
 }
@@ -427,22 +417,11 @@ static int32_t bwd_impl(const linattn_shape *shape, const void *q, const void *k
   if (!tc_supported(pt))
     return cuda_status(simt_bwd(p, q, k, v, dO, init_state, d_final, dq, dk, dv, d_init_state, s));
   cudaError_t e = cudaSuccess;
-  void *const user_out[3] = {dq, dk, dv};
   float *const user_dinit = d_init_state;
   if (pad) {
-    char *pb = ws + align256(w.total);
-    const size_t R = pad_rows_bytes(p), SB = pad_state_bytes(p);
-    const void *in[4] = {q, k, v, dO};
-    for (int i = 0; i < 4 && e == cudaSuccess; ++i) e = pad_rows_d64(p, in[i], pb + i * R, s);
-    q = pb;
-    k = pb + R;
-    v = pb + 2 * R;
-    dO = pb + 3 * R;
-    dq = pb + 4 * R;
-    dk = pb + 5 * R;
-    dv = pb + 6 * R;
-    char *sp = pb + 7 * R;
-    if (init_state && e == cudaSuccess) {
+    char *sp = ws + align256(w.total);
+    const size_t SB = pad_state_bytes(p);
+    if (init_state) {
       e = pad_state_d64(init_state, reinterpret_cast<float *>(sp), BH, s);
       init_state = reinterpret_cast<const float *>(sp);
     }
@@ -485,11 +464,7 @@ static int32_t bwd_impl(const linattn_shape *shape, const void *q, const void *k
     e = cudaMemcpyAsync(rbar + (int64_t)(G - 1) * E, d_final, (size_t)E * sizeof(float), cudaMemcpyDeviceToDevice, s);
   // dv and dk in one reverse-time pass from the states Rbar
   if (e == cudaSuccess) e = tc_dual(pt, gp, q, k, v, dO, dk, dv, rbar, status, s);
-  if (pad) {
-    for (int i = 0; i < 3 && e == cudaSuccess; ++i)
-      e = unpad_rows_d64(p, i == 0 ? dq : (i == 1 ? dk : dv), user_out[i], s);
-    if (user_dinit && e == cudaSuccess) e = unpad_state_d64(d_init_state, user_dinit, BH, s);
-  }
+  if (pad && user_dinit && e == cudaSuccess) e = unpad_state_d64(d_init_state, user_dinit, BH, s);
   return cuda_status(e);
 }
 

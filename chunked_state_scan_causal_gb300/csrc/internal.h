@@ -25,6 +25,10 @@ struct Problem {
   // which the dq pass fills with q_t . dq_t and the dk/dv pass reduces by k_t . dk_t
   const void *gq = nullptr, *gk = nullptr;
   float *gx = nullptr;
+  // bf16 d = 64 on the d = 128 tensor-core kernels: the sequence tensors have 64
+  // columns (their tensor maps say so: the tiles' columns 64..127 load as zeros,
+  // and only the first 64 output columns are stored); 0 means d
+  int dcols = 0;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -179,10 +183,8 @@ struct SoftmaxProblem {
   float scale;
   int num_sms;
 };
-// Zero padding of bf16 d = 64 problems to d = 128 (pad.cu): sequence rows at the
-// request's strides <-> contiguous [B*H*T][128]; states [n][64][64] <-> [n][128][128].
-cudaError_t pad_rows_d64(const Problem &p, const void *src, void *dst, cudaStream_t s);
-cudaError_t unpad_rows_d64(const Problem &p, const void *src, void *dst, cudaStream_t s);
+// States of bf16 d = 64 problems run at d = 128 (pad.cu): [n][64][64] <-> the
+// top-left block of [n][128][128], zeros elsewhere.
 cudaError_t pad_state_d64(const float *src, float *dst, int64_t n, cudaStream_t s);
 cudaError_t unpad_state_d64(const float *src, float *dst, int64_t n, cudaStream_t s);
 // Per-dimension gates (gate_vec.cu): one CTA per (batch, head) walks the sequence;

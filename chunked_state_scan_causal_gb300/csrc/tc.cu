@@ -591,6 +591,7 @@ struct MainParams {
   const int *gflag;    // GATE, forward: per item [G][BH], nonzero: the weighted-operand form applies
   const __nv_bfloat16 *gq;  // GATE, dq pass: the true q (strides sb, sh, st) for gx = q . dq
   float *gx;           // GATE, dq pass: [BH][T] fp32 q_t . dq_t from the unrounded dq, or null
+  int half_out;        // the output rows have 64 columns (d = 64 run at d = 128): one store box
   int64_t sb, sh, st;
 };
 
@@ -1068,7 +1069,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         named_bar_sync(1, 128);
         if (leader) {
           tma_store_4d_hint(&mo, smem + kOffPs, 0, t0, h, b, kPolicyEvictFirst);
-          tma_store_4d_hint(&mo, smem + kOffPs + kTileHalfBytes, 64, t0, h, b, kPolicyEvictFirst);
+          if (!P.half_out) tma_store_4d_hint(&mo, smem + kOffPs + kTileHalfBytes, 64, t0, h, b, kPolicyEvictFirst);
           bulk_commit();
         }
       }
@@ -1257,6 +1258,7 @@ struct DualParams {
   const __nv_bfloat16 *gk;  // GATE: k (strides sb, sh, st) for gx -= k . dk
   float *gx;           // GATE: [BH][T] fp32, q . dq from the dq pass; k . dk (unrounded dk) subtracted
   const int *gflag;    // GATE: per item [G][BH], nonzero: the weighted-operand form (as in the dq pass)
+  int half_out;        // dk, dv rows have 64 columns (d = 64 run at d = 128): chunks 0, 1 only
 };
 
 constexpr int kDualThreads = 512;
@@ -1594,7 +1596,7 @@ __global__ void __launch_bounds__(kDualThreads, 1)
             ld_chunk(tO1 + lb + c * 32, x);
 #pragma unroll
             for (int j = 0; j < 32; ++j) x[j] *= wrow;
-            if (valid) {
+            if (valid && (c < 2 || !P.half_out)) {
               if (P.wide)
                 st_global_chunk_bf16<true>(dst + c * 32, x);
               else
@@ -1823,7 +1825,7 @@ __global__ void __launch_bounds__(kDualThreads, 1)
               for (int j = 0; j < 32; ++j) x[j] *= wrow;
             }
             if (gx_row && !wtd) gxacc += dot32_bf16(x, krow + c * 32);  // k . dk before dk is rounded
-            if (valid) {
+            if (valid && (c < 2 || !P.half_out)) {
               if (P.wide)
                 st_global_chunk_bf16<true>(dst + c * 32, x);
               else
@@ -1844,7 +1846,9 @@ __global__ void __launch_bounds__(kDualThreads, 1)
 }
 
 bool seq_tmap(const Problem &p, const void *base, CUtensorMap *m) {
-  const uint64_t dims[4] = {(uint64_t)p.d, (uint64_t)p.T, (uint64_t)p.H, (uint64_t)p.B};
+  // with dcols = 64 the second 64-column box of every tile lies past the rows' end:
+  // its loads fill zeros
+  const uint64_t dims[4] = {(uint64_t)(p.dcols ? p.dcols : p.d), (uint64_t)p.T, (uint64_t)p.H, (uint64_t)p.B};
   const uint64_t strides[3] = {(uint64_t)p.st * 2, (uint64_t)p.sh * 2, (uint64_t)p.sb * 2};
   return make_tmap_bf16(m, base, dims, strides);
 }
@@ -1926,6 +1930,7 @@ cudaError_t tc_dual(const Problem &p, const GroupPlan &gp, const void *q, const 
   D.gk = static_cast<const __nv_bfloat16 *>(p.gk);
   D.gx = p.gx;
   D.gflag = p.gflag;
+  D.half_out = p.dcols == 64;
   const int grid = D.nitems < p.num_sms ? D.nitems : p.num_sms;
   cudaError_t e;
   TimedLaunch t(K_TC_DUAL_REV, s);
@@ -1960,6 +1965,7 @@ cudaError_t tc_main(const Problem &p, const GroupPlan &gp, const void *q, const 
   M.agg_out = agg_out;
   M.gC = p.gC;
   M.gflag = p.gflag;
+  M.half_out = p.dcols == 64;
   M.gq = static_cast<const __nv_bfloat16 *>(p.gq);
   M.gx = p.gx;
   M.sb = p.sb; M.sh = p.sh; M.st = p.st;

@@ -37,10 +37,10 @@
  *  - States are fp32, row-major [.., d_k, d_v] (row index = key dimension).
  *  - Paths: bf16 with d = 128 runs on the tensor-core kernels (chunk groups
  *    processed in parallel, states joined by the scan).  bf16 with d = 64
- *    runs on the same kernels through zero-padded d = 128 copies of the
- *    sequence tensors and states in the workspace (exact: the padded columns
- *    stay zero), for linattn_fwd / _ckpt and linattn_bwd / _ckpt without
- *    per-chunk states.  fp32 inputs, the other d = 64 requests and the gated
+ *    runs on the same kernels as the zero-padded d = 128 problem (exact: the
+ *    tiles' columns past 64 load as zeros and are not stored; the states go
+ *    through padded copies in the workspace), for linattn_fwd / _ckpt and
+ *    linattn_bwd / _ckpt without per-chunk states.  fp32 inputs, the other d = 64 requests and the gated
  *    entry points at d = 64 run on CUDA-core kernels that walk every sequence
  *    serially, one CTA per (batch, head): correct for any length but far
  *    slower on long sequences (meant for fp32 checks and small heads).

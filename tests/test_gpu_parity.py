@@ -376,10 +376,11 @@ def test_decode_steps(dtype, d, T, dk):
 
 
 def test_bf16_d64_runs_on_the_tensor_core_kernels():
-    """bf16 with d = 64 goes through zero-padded d = 128 copies on the tensor-core
-    kernels: the recorded launches are the chunked kernels and the padding passes,
-    not the CUDA-core walk; many chunk groups, per-head decays, an initial state and a
-    final-state gradient, every head against the oracle."""
+    """bf16 with d = 64 runs on the d = 128 tensor-core kernels as the zero-padded
+    problem (64-column tensor maps: the tiles' other columns load as zeros; the states
+    through padded copies): the recorded launches are the chunked kernels and the state
+    padding, not the CUDA-core walk; many chunk groups, per-head decays, an initial
+    state and a final-state gradient, every head against the oracle."""
     B, H, T, d = 1, 4, 16384 + 77, 64
     c, dev = case(61, B, H, T, d, torch.bfloat16, sigma=1 / np.sqrt(64))
     lam = np.array([1.0, 0.999, 0.9, 0.5], np.float32)

@@ -180,9 +180,9 @@ static BwdLayout bwd_layout(const Problem &p) {
 // problem, which is the same problem: the tiles' columns 64..127 of q, k, v load
 // as zeros (the tensor maps give the rows 64 columns), so every q . k and every
 // product with the state is unchanged, the state's rows and columns 64..127 stay
-// zero, and only the first 64 output columns are stored.  The states go through
-// zero-padded 128 x 128 copies (pad.cu), after the d = 128 workspace, whose status
-// word stays at offset 0.  Per-chunk states of linattn_fwd keep the CUDA-core path.
+// zero, and only the first 64 output columns are stored (per-chunk states: their
+// top-left 64 x 64 blocks).  The states go through zero-padded 128 x 128 copies
+// (pad.cu), after the d = 128 workspace, whose status word stays at offset 0.
 static bool padded(const Problem &p) { return p.dtype == 0 && p.d == 64 && p.T > 0; }
 static Problem padded_problem(const Problem &p) {
   Problem q = p;
@@ -318,7 +318,7 @@ static int32_t fwd_impl(const linattn_shape *shape, const void *q, const void *k
   if (st) return st;
   if (p.T > 0 && (st = check_ptrs({q, k, v, o}, {}))) return st;
   if ((st = check_ptrs({}, {init_state, final_state, chunk_states}))) return st;
-  const bool pad = padded(p) && !chunk_states;
+  const bool pad = padded(p);
   const Problem pt = pad ? padded_problem(p) : p;  // the problem the kernels run
   const FwdLayout w = fwd_layout(pt);
   if ((st = check_ws(workspace, workspace_bytes, pad ? fwd_ws_bytes(p) : w.total))) return st;
@@ -673,6 +673,9 @@ static int32_t chunk_states_impl(const linattn_shape *shape, int32_t seg_len, co
   if (cudaMemsetAsync(workspace, 0, kHeader, s) != cudaSuccess) return LINATTN_ERR_CUDA;
   if (tc_supported(p) && seg_len % 128 == 0)
     return cuda_status(tc_segment_states(p, GroupPlan::uniform(p.T, seg_len), x, y, reverse, out, status, s));
+  if (padded(p) && seg_len % 128 == 0)  // bf16 d = 64: the d = 128 kernel, 64 x 64 states stored
+    return cuda_status(tc_segment_states(padded_problem(p), GroupPlan::uniform(p.T, seg_len), x, y, reverse, out,
+                                         status, s, false, 64));
   return cuda_status(simt_segment_states(p, seg_len, x, y, reverse, out, s));
 }
 

@@ -146,8 +146,11 @@ GroupPlan tc_group_plan(const Problem &p, int max_len = 0);
 //   reverse == false: w_s = lambda^{end - s};  reverse == true: w_s = lambda^{s - start + 1}.
 // skip_weighted: leave out the groups of heads whose decay takes the weighted
 // form (lambda >= 0.8), whose aggregates the dq pass accumulates itself.
+// dout: rows and columns of the stored states (64: the top-left blocks, for d = 64
+// run at d = 128 and stored at d = 64).
 cudaError_t tc_segment_states(const Problem &p, const GroupPlan &gp, const void *X, const void *Y, bool reverse,
-                              float *out, int *status, cudaStream_t s, bool skip_weighted = false);
+                              float *out, int *status, cudaStream_t s, bool skip_weighted = false,
+                              int dout = 128);
 // Per-group causal chunked attention from the given group states
 // [G][BH][d][d] (read transposed when init_transposed): o_i = lambda^{i+1}
 // S^T q_i + intra-block terms, S the state entering the block.  final_state

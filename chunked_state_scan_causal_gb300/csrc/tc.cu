@@ -200,6 +200,7 @@ struct AggParams {
   int *counter;  // [2] item counter and finished CTAs (zero at launch)
   const float *gC, *gtot;  // gates: group-local log2 cumulative sums [BH][T], group totals [G][BH]
   int skip_weighted;       // pass over the items of heads with lambda >= kWeightedMin (the dq pass has them)
+  int dout;                // rows and columns of the stored states: 128, or 64 (top-left blocks)
 };
 
 // GATE (with DECAY): token weights from the gates' cumulative sums instead of
@@ -346,14 +347,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int a = ai & 1, ua = ai >> 1;
       if (!__all_sync(0xffffffffu, mbar_wait(&accf[a], ua & 1, &abort_flag, P.status, detail))) break;
       tc_fence_after();
-      float *dst = P.out + ((int64_t)g * BH + bh) * 16384 + row * 128;
+      const int dout = P.dout;
+      float *dst = P.out + ((int64_t)g * BH + bh) * dout * dout + (int64_t)row * dout;
 #pragma unroll 1
       for (uint32_t c = 0; c < 4; ++c) {
         float x[32];
         ld_chunk(tmem + a * 128 + ((quad * 32) << 16) + c * 32, x);
+        if ((int)row < dout && (int)c * 32 < dout) {
 #pragma unroll
-        for (int j = 0; j < 32; j += 4)
-          *reinterpret_cast<float4 *>(dst + c * 32 + j) = make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
+          for (int j = 0; j < 32; j += 4)
+            *reinterpret_cast<float4 *>(dst + c * 32 + j) = make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
+        }
       }
       tc_fence_before();
       mbar_arrive(&acce[a]);
@@ -378,9 +382,10 @@ struct ChunkParams {
   GroupPlan gp;
   const float *decay;
   const float *ginit;  // [G][BH][d][d] states entering the groups
-  float *out;          // [BH][nch][d][d]
+  float *out;          // [BH][nch][dout][dout]
   int *status;
   int *counter;        // [2] item counter and finished CTAs (zero at launch)
+  int dout;            // 128, or 64 for d = 64 run at d = 128 (the states' top-left blocks)
 };
 
 template <bool DECAY>
@@ -532,10 +537,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       range(item, s0, s1);
       const int nc = (s1 - s0 + 63) / 64;
       const float dec = DECAY ? exp2f(log2f(P.decay[bh % P.H]) * 64.f) : 1.f;
-      float *dst0 = P.out + ((int64_t)bh * P.nch + s0 / 64) * 16384 + row * 128;
+      const int dout = P.dout, osz = dout * dout;
+      const bool store_row = (int)row < dout;  // d = 64: rows 64..127 of the state are zero, not stored
+      float *dst0 = P.out + ((int64_t)bh * P.nch + s0 / 64) * osz + (int64_t)row * dout;
       const float *src = P.ginit + ((int64_t)g * BH + bh) * 16384 + row * 128;
       for (int c = 0; c < nc && ok; ++c, ++ck) {
-        float *dst = dst0 + (int64_t)c * 16384;
+        float *dst = dst0 + (int64_t)c * osz;
         if (c > 0) {
           // chunk c-1's product is done: its result is chunk c's entering state
           if (!(ok = __all_sync(0xffffffffu, mbar_wait(cmma, (ck - 1 - k) & 1, &abort_flag, P.status, detail))))
@@ -554,9 +561,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             ld_chunk(tS + lb + q * 32, x);
           }
+          if (store_row && q * 32 < dout) {
 #pragma unroll
-          for (int j = 0; j < 32; j += 4)
-            __stcs(reinterpret_cast<float4 *>(dst + q * 32 + j), make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]));
+            for (int j = 0; j < 32; j += 4)
+              __stcs(reinterpret_cast<float4 *>(dst + q * 32 + j), make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]));
+          }
           if ((c == 0 || DECAY) && c + 1 < nc) {
             // the state the chunk's product accumulates into: lambda^64 S
             uint32_t r[32];
@@ -1861,7 +1870,7 @@ cudaError_t set_smem(K kern, size_t bytes) {
 }  // namespace
 
 cudaError_t tc_segment_states(const Problem &p, const GroupPlan &gp, const void *X, const void *Y, bool reverse,
-                              float *out, int *status, cudaStream_t s, bool skip_weighted) {
+                              float *out, int *status, cudaStream_t s, bool skip_weighted, int dout) {
   alignas(64) CUtensorMap mx, my;
   if (!seq_tmap(p, X, &mx) || !seq_tmap(p, Y, &my)) return cudaErrorInvalidValue;
   AggParams A;
@@ -1872,6 +1881,7 @@ cudaError_t tc_segment_states(const Problem &p, const GroupPlan &gp, const void 
   A.decay = p.decay; A.out = out; A.status = status; A.counter = status + kCounterAgg;
   A.gC = p.gC; A.gtot = p.gtot;
   A.skip_weighted = skip_weighted ? 1 : 0;
+  A.dout = dout;
   const size_t smem = 3 * 2 * kTileBytes + 1024 + 256;
   const int grid = A.nitems < p.num_sms ? A.nitems : p.num_sms;
   cudaError_t e;
@@ -1898,6 +1908,7 @@ cudaError_t tc_chunk_states(const Problem &p, const GroupPlan &gp, const void *k
   C.nitems = gp.G * p.B * p.H;
   C.nch = (p.T + 63) / 64;
   C.decay = p.decay; C.ginit = group_init; C.out = out; C.status = status; C.counter = status + kCounterChunk;
+  C.dout = p.dcols == 64 ? 64 : 128;
   const size_t smem = 3 * 2 * kTileBytes + 1024 + 256;
   const int grid = C.nitems < p.num_sms ? C.nitems : p.num_sms;
   cudaError_t e;

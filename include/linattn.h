@@ -39,8 +39,9 @@
  *    processed in parallel, states joined by the scan).  bf16 with d = 64
  *    runs on the same kernels as the zero-padded d = 128 problem (exact: the
  *    tiles' columns past 64 load as zeros and are not stored; the states go
- *    through padded copies in the workspace), for linattn_fwd / _ckpt and
- *    linattn_bwd / _ckpt without per-chunk states.  fp32 inputs, the other d = 64 requests and the gated
+ *    through padded copies in the workspace), for linattn_fwd / _ckpt,
+ *    linattn_bwd / _ckpt and linattn_chunk_states(_rev) with segments of a
+ *    multiple of 128 tokens.  fp32 inputs, the other d = 64 requests and the gated
  *    entry points at d = 64 run on CUDA-core kernels that walk every sequence
  *    serially, one CTA per (batch, head): correct for any length but far
  *    slower on long sequences (meant for fp32 checks and small heads).

@@ -87,7 +87,8 @@ def test_state_scan(G, with_decay, with_init):
 
 # ------------------------------------------------------------------ chunk_states (segment-local states)
 @pytest.mark.parametrize("dtype,d,T,seg", [(torch.float32, 64, 512, 128), (torch.bfloat16, 128, 1024, 256),
-                                           (torch.bfloat16, 128, 768, 384), (torch.bfloat16, 64, 512, 64)])
+                                           (torch.bfloat16, 128, 768, 384), (torch.bfloat16, 64, 512, 64),
+                                           (torch.bfloat16, 64, 1280, 256)])
 @pytest.mark.parametrize("dk", [None, 0.5, "cfg"])
 def test_chunk_states(dtype, d, T, seg, dk):
     B, H = 2, 3

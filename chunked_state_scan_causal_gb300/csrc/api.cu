@@ -238,7 +238,19 @@ static GatedLayout gated_layout(const Problem &p) {
   w.bwd_total = w.gx + align256((size_t)BH * p.T * sizeof(float));
   return w;
 }
+static size_t ckpt_bytes_gated(const Problem &p);
+// gated workspaces; bf16 d = 64 adds its padded states (initial; or final-state
+// gradient and d_init) after the d = 128 layout
+static size_t gated_fwd_ws_bytes(const Problem &p) {
+  if (!padded(p)) return gated_layout(p).fwd_total;
+  return align256(gated_layout(padded_problem(p)).fwd_total) + pad_state_bytes(p);
+}
+static size_t gated_bwd_ws_bytes(const Problem &p) {
+  if (!padded(p)) return gated_layout(p).bwd_total;
+  return align256(gated_layout(padded_problem(p)).bwd_total) + 2 * pad_state_bytes(p);
+}
 static size_t ckpt_bytes_gated(const Problem &p) {
+  if (padded(p)) return ckpt_bytes_gated(padded_problem(p));
   const FwdLayout w = fwd_layout(p, kGatedMaxGroup);
   return w.G == 0 ? 0 : ((size_t)w.G + 1) * p.B * p.H * p.d * p.d * sizeof(float);
 }
@@ -297,9 +309,9 @@ int32_t linattn_workspace_size(const linattn_shape *shape, int32_t op, int32_t s
   } else if (op == LINATTN_OP_CHECKPOINT) {
     *bytes = ckpt_bytes(p);
   } else if (op == LINATTN_OP_FWD_GATED) {
-    *bytes = gated_layout(p).fwd_total;
+    *bytes = gated_fwd_ws_bytes(p);
   } else if (op == LINATTN_OP_BWD_GATED) {
-    *bytes = gated_layout(p).bwd_total;
+    *bytes = gated_bwd_ws_bytes(p);
   } else if (op == LINATTN_OP_CHECKPOINT_GATED) {
     *bytes = ckpt_bytes_gated(p);
   } else if (op == LINATTN_OP_SOFTMAX_SEGMENT) {
@@ -505,8 +517,10 @@ int32_t linattn_fwd_gated(const linattn_shape *shape, const void *q, const void 
   if (st) return st;
   if (p.T > 0 && (st = check_ptrs({q, k, v, o}, {}))) return st;
   if ((st = check_ptrs({}, {init_state, final_state}))) return st;
-  const GatedLayout w = gated_layout(p);
-  if ((st = check_ws(workspace, workspace_bytes, w.fwd_total))) return st;
+  const bool pad = padded(p);
+  Problem pt = pad ? padded_problem(p) : p;  // the problem the kernels run
+  const GatedLayout w = gated_layout(pt);
+  if ((st = check_ws(workspace, workspace_bytes, gated_fwd_ws_bytes(p)))) return st;
   if ((st = device_ok())) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char *ws = static_cast<char *>(workspace);
@@ -523,24 +537,31 @@ int32_t linattn_fwd_gated(const linattn_shape *shape, const void *q, const void 
     }
     return LINATTN_OK;
   }
-  // CUDA-core path (fp32 inputs, d = 64): one sequential walk, no checkpoint
-  if (!tc_supported(p)) return cuda_status(simt_fwd(p, q, k, v, o, init_state, final_state, nullptr, s, log_gate));
+  // CUDA-core path (fp32 inputs): one sequential walk, no checkpoint
+  if (!tc_supported(pt)) return cuda_status(simt_fwd(p, q, k, v, o, init_state, final_state, nullptr, s, log_gate));
   const GroupPlan &gp = w.f.gp;
   const int G = gp.G;
   float *C = reinterpret_cast<float *>(ws + w.C), *tot = reinterpret_cast<float *>(ws + w.tot);
   float *agg = reinterpret_cast<float *>(ws + w.f.agg);
   float *states = static_cast<float *>(checkpoint);
-  float *fin = states + (size_t)G * BH * p.d * p.d;  // the checkpoint's final state
+  float *fin = states + (size_t)G * BH * pt.d * pt.d;  // the checkpoint's final state
   int *wflag = reinterpret_cast<int *>(ws + w.wflag);
-  cudaError_t e = gate_prep(p, gp, log_gate, C, tot, wflag, s);
-  p.gC = C;
-  p.gtot = tot;
-  p.gflag = wflag;  // the chunked forward may weight its operands
-  if (e == cudaSuccess) e = tc_segment_states(p, gp, k, v, false, agg, status, s);
-  if (e == cudaSuccess) e = plan_scan(p, gp, false, agg, init_state, states, nullptr, ws + w.f.scan, status, s, tot);
-  if (e == cudaSuccess) e = tc_main(p, gp, q, k, v, o, states, false, fin, status, s);
+  cudaError_t e = gate_prep(pt, gp, log_gate, C, tot, wflag, s);
+  const float *init = init_state;
+  if (pad && init && e == cudaSuccess) {
+    float *ip = reinterpret_cast<float *>(ws + align256(w.fwd_total));
+    e = pad_state_d64(init_state, ip, BH, s);
+    init = ip;
+  }
+  pt.gC = C;
+  pt.gtot = tot;
+  pt.gflag = wflag;  // the chunked forward may weight its operands
+  if (e == cudaSuccess) e = tc_segment_states(pt, gp, k, v, false, agg, status, s);
+  if (e == cudaSuccess) e = plan_scan(pt, gp, false, agg, init, states, nullptr, ws + w.f.scan, status, s, tot);
+  if (e == cudaSuccess) e = tc_main(pt, gp, q, k, v, o, states, false, fin, status, s);
   if (e == cudaSuccess && final_state)
-    e = cudaMemcpyAsync(final_state, fin, state_bytes, cudaMemcpyDeviceToDevice, s);
+    e = pad ? unpad_state_d64(fin, final_state, BH, s)
+            : cudaMemcpyAsync(final_state, fin, state_bytes, cudaMemcpyDeviceToDevice, s);
   return cuda_status(e);
 }
 
@@ -554,26 +575,30 @@ int32_t linattn_bwd_gated(const linattn_shape *shape, const void *q, const void 
   if (st) return st;
   if (p.T > 0 && (st = check_ptrs({q, k, v, dO, dq, dk, dv, d_log_gate}, {}))) return st;
   if ((st = check_ptrs({}, {init_state, d_final_state, d_init_state}))) return st;
-  const GatedLayout w = gated_layout(p);
-  if ((st = check_ws(workspace, workspace_bytes, w.bwd_total))) return st;
+  const bool pad = padded(p);
+  Problem pt = pad ? padded_problem(p) : p;  // the problem the kernels run
+  const GatedLayout w = gated_layout(pt);
+  if ((st = check_ws(workspace, workspace_bytes, gated_bwd_ws_bytes(p)))) return st;
   if ((st = device_ok())) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char *ws = static_cast<char *>(workspace);
   int *status = reinterpret_cast<int *>(ws);
   if (cudaMemsetAsync(ws, 0, kHeader, s) != cudaSuccess) return LINATTN_ERR_CUDA;
-  const int64_t BH = (int64_t)p.B * p.H, E = BH * p.d * p.d;
-  const size_t state_bytes = (size_t)E * sizeof(float);
+  const int64_t BH = (int64_t)p.B * p.H;
+  const size_t user_state_bytes = (size_t)BH * p.d * p.d * sizeof(float);
   if (p.T == 0) {
     if (d_init_state)
-      return cuda_status(d_final_state ? cudaMemcpyAsync(d_init_state, d_final_state, state_bytes,
+      return cuda_status(d_final_state ? cudaMemcpyAsync(d_init_state, d_final_state, user_state_bytes,
                                                          cudaMemcpyDeviceToDevice, s)
-                                       : cudaMemsetAsync(d_init_state, 0, state_bytes, s));
+                                       : cudaMemsetAsync(d_init_state, 0, user_state_bytes, s));
     return LINATTN_OK;
   }
   // CUDA-core path: recomputes the forward states from init_state (the checkpoint is empty)
-  if (!tc_supported(p))
+  if (!tc_supported(pt))
     return cuda_status(simt_bwd(p, q, k, v, dO, init_state, d_final_state, dq, dk, dv, d_init_state, s, log_gate,
                                 d_log_gate));
+  const int64_t E = BH * pt.d * pt.d;
+  const size_t state_bytes = (size_t)E * sizeof(float);
   const GroupPlan &gp = w.f.gp;
   const int G = gp.G;
   float *C = reinterpret_cast<float *>(ws + w.C), *tot = reinterpret_cast<float *>(ws + w.tot);
@@ -582,25 +607,37 @@ int32_t linattn_bwd_gated(const linattn_shape *shape, const void *q, const void 
   const float *fin = states + (size_t)G * E;
   // per-item flags: the dq and dk/dv passes take the weighted-operand form together
   int *wflag = reinterpret_cast<int *>(ws + w.wflag);
-  cudaError_t e = gate_prep(p, gp, log_gate, C, tot, wflag, s);
-  p.gC = C;
-  p.gtot = tot;
-  p.gflag = wflag;
-  p.gq = q;
-  p.gk = k;
-  p.gx = reinterpret_cast<float *>(ws + w.gx);
+  cudaError_t e = gate_prep(pt, gp, log_gate, C, tot, wflag, s);
+  // bf16 d = 64: the final-state gradient in, d_init out through padded states
+  const float *dfin = d_final_state;
+  float *dinit = d_init_state;
+  if (pad) {
+    float *sp = reinterpret_cast<float *>(ws + align256(w.bwd_total));
+    if (dfin && e == cudaSuccess) {
+      e = pad_state_d64(d_final_state, sp, BH, s);
+      dfin = sp;
+    }
+    if (dinit) dinit = reinterpret_cast<float *>(ws + align256(w.bwd_total) + pad_state_bytes(p));
+  }
+  pt.gC = C;
+  pt.gtot = tot;
+  pt.gflag = wflag;
+  pt.gq = q;
+  pt.gk = k;
+  pt.gx = reinterpret_cast<float *>(ws + w.gx);
   // dq: forward-time kernel with (q, k, v) := (dO, v, k) from the group states (transposed)
-  if (e == cudaSuccess) e = tc_main(p, gp, dO, v, k, dq, states, true, nullptr, status, s);
+  if (e == cudaSuccess) e = tc_main(pt, gp, dO, v, k, dq, states, true, nullptr, status, s);
   // reverse group aggregates sum_s exp2(C_s) q_s dO_s^T, the final-state gradient folded
   // across the last group, and the reverse scan with every group's own multiplier
-  if (e == cudaSuccess) e = tc_segment_states(p, gp, q, dO, true, wagg, status, s);
-  if (e == cudaSuccess && d_final_state)
-    e = fold_state_log2(wagg + (int64_t)(G - 1) * E, d_final_state, tot + (int64_t)(G - 1) * BH, p.d * p.d, E, s);
-  if (e == cudaSuccess) e = plan_scan(p, gp, true, wagg, nullptr, rbar, d_init_state, ws + w.f.scan, status, s, tot);
-  if (e == cudaSuccess && d_final_state)
-    e = cudaMemcpyAsync(rbar + (int64_t)(G - 1) * E, d_final_state, state_bytes, cudaMemcpyDeviceToDevice, s);
-  if (e == cudaSuccess) e = tc_dual(p, gp, q, k, v, dO, dk, dv, rbar, status, s);
-  if (e == cudaSuccess) e = gate_grad(p, gp, p.gx, rbar, states, d_final_state, fin, d_log_gate, s);
+  if (e == cudaSuccess) e = tc_segment_states(pt, gp, q, dO, true, wagg, status, s);
+  if (e == cudaSuccess && dfin)
+    e = fold_state_log2(wagg + (int64_t)(G - 1) * E, dfin, tot + (int64_t)(G - 1) * BH, pt.d * pt.d, E, s);
+  if (e == cudaSuccess) e = plan_scan(pt, gp, true, wagg, nullptr, rbar, dinit, ws + w.f.scan, status, s, tot);
+  if (e == cudaSuccess && dfin)
+    e = cudaMemcpyAsync(rbar + (int64_t)(G - 1) * E, dfin, state_bytes, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess) e = tc_dual(pt, gp, q, k, v, dO, dk, dv, rbar, status, s);
+  if (e == cudaSuccess) e = gate_grad(pt, gp, pt.gx, rbar, states, dfin, fin, d_log_gate, s);
+  if (pad && d_init_state && e == cudaSuccess) e = unpad_state_d64(dinit, d_init_state, BH, s);
   return cuda_status(e);
 }
 

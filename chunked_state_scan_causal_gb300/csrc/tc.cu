@@ -999,10 +999,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const __nv_bfloat16 *qr = P.gq + (int64_t)b * P.sb + (int64_t)h * P.sh + (int64_t)(t0 + (int)row) * P.st;
           if (qreg) {
 #pragma unroll
-            for (int m = 0; m < 16; ++m) qv[m] = __ldg(reinterpret_cast<const uint4 *>(qr) + m);
+            for (int m = 0; m < 16; ++m)  // (rows of 64 columns: the first 8 pieces)
+              if (m < 8 || !P.half_out) qv[m] = __ldg(reinterpret_cast<const uint4 *>(qr) + m);
           } else {
             prefetch_l1(qr);
-            prefetch_l1(qr + 64);
+            if (!P.half_out) prefetch_l1(qr + 64);
           }
         }
         ok = group_all(mbar_wait(&bar[B_PFULL], blk & 1, &abort_flag, P.status, detail), 2, 128);
@@ -1047,7 +1048,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < 4; ++c) {
             float x[32];
             ld_chunk(tO + lb + c * 32, x);
-            if (qreg) gxacc += dot32_regs_w(x, qv, c, wq);
+            if (qreg && (c < 2 || !P.half_out)) gxacc += dot32_regs_w(x, qv, c, wq);
 #pragma unroll
             for (int j = 0; j < 32; ++j) x[j] *= wq;
             store_row_chunk_bf16(sPs, row, c, x);
@@ -1067,7 +1068,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int j = 0; j < 32; ++j) x[j] = fmaf(wq, y[j], x[j]);
           }
-          if (gx_row && !wtd) gxacc += dot32_bf16(x, qrow + c * 32);  // q . dq before dq is rounded
+          if (gx_row && !wtd && (c < 2 || !P.half_out))
+            gxacc += dot32_bf16(x, qrow + c * 32);  // q . dq before dq is rounded
           store_row_chunk_bf16(sPs, row, c, x);
         }
         }
@@ -1805,7 +1807,7 @@ __global__ void __launch_bounds__(kDualThreads, 1)
           // the k row for k . dk: two 128-byte lines into L1 while dv drains
           const __nv_bfloat16 *kr = P.gk + (int64_t)b * P.sb + (int64_t)h * P.sh + (int64_t)(t0 + (int)row) * P.st;
           prefetch_l1(kr);
-          prefetch_l1(kr + 64);
+          if (!P.half_out) prefetch_l1(kr + 64);
         }
         // (gated items in the weighted form: the dv rows are stored by the score warps)
         for (int half = (GATE && wtd) ? 1 : 0; half < 2 && ok; ++half) {
@@ -1828,12 +1830,13 @@ __global__ void __launch_bounds__(kDualThreads, 1)
             // pass's products saw it (bf16(k exp2(C_last - C_i))) with the accumulator
             // (dk / exp2(C_last - C_i)), so that the intra-block terms of q . dq and
             // k . dk are the same products
-            if (gx_row && wtd) gxacc += dot32_bf16_w(x, krow + c * 32, wrow);
+            if (gx_row && wtd && (c < 2 || !P.half_out)) gxacc += dot32_bf16_w(x, krow + c * 32, wrow);
             if (wtd) {
 #pragma unroll
               for (int j = 0; j < 32; ++j) x[j] *= wrow;
             }
-            if (gx_row && !wtd) gxacc += dot32_bf16(x, krow + c * 32);  // k . dk before dk is rounded
+            if (gx_row && !wtd && (c < 2 || !P.half_out))
+              gxacc += dot32_bf16(x, krow + c * 32);  // k . dk before dk is rounded
             if (valid && (c < 2 || !P.half_out)) {
               if (P.wide)
                 st_global_chunk_bf16<true>(dst + c * 32, x);

@@ -40,11 +40,12 @@
  *    runs on the same kernels as the zero-padded d = 128 problem (exact: the
  *    tiles' columns past 64 load as zeros and are not stored; the states go
  *    through padded copies in the workspace), for linattn_fwd / _ckpt,
- *    linattn_bwd / _ckpt and linattn_chunk_states(_rev) with segments of a
- *    multiple of 128 tokens.  fp32 inputs, the other d = 64 requests and the gated
- *    entry points at d = 64 run on CUDA-core kernels that walk every sequence
- *    serially, one CTA per (batch, head): correct for any length but far
- *    slower on long sequences (meant for fp32 checks and small heads).
+ *    linattn_bwd / _ckpt, linattn_fwd_gated / linattn_bwd_gated and
+ *    linattn_chunk_states(_rev) with segments of a multiple of 128 tokens.
+ *    fp32 inputs and segment states of other segment lengths run on CUDA-core
+ *    kernels that walk every sequence serially, one CTA per (batch, head):
+ *    correct for any length but far slower on long sequences (meant for fp32
+ *    checks).
  */
 #ifndef LINATTN_H
 #define LINATTN_H
@@ -165,8 +166,8 @@ int32_t linattn_bwd_ckpt(const linattn_shape *shape, const void *q, const void *
  *   S_t = alpha_t S_{t-1} + k_t v_t^T,   o_t = S_t^T q_t.
  * log_gate is [B,H,T] fp32, contiguous, 16-byte aligned (log of gates in
  * (0, 1]: values <= 0; positive values are taken as given but their weights may
- * overflow).  The shape's decay must be NULL.  bf16 with d = 128 runs on the
- * tensor-core kernels; fp32 inputs and d = 64 on the CUDA-core kernels.  The
+ * overflow).  The shape's decay must be NULL.  bf16 runs on the tensor-core
+ * kernels (d = 64 as the zero-padded problem); fp32 on the CUDA-core kernels.  The
  * checkpoint (size from LINATTN_OP_CHECKPOINT_GATED) keeps every chunk group's
  * entering state and the final state for linattn_bwd_gated; it is required
  * when that size is nonzero (the CUDA-core path has none: its backward

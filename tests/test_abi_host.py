@@ -133,11 +133,19 @@ def test_device_status_null(cdll):
 def test_gated_entry_points_check_their_arguments(cdll):
     s = _shape()
     ck = 1 << 30  # large enough for any checkpoint size check
-    # fp32 inputs and d = 64 take the CUDA-core path: no checkpoint, no workspace past the status header
-    for sh in (_shape(dtype=la.F32), _shape(dk=64, dv=64, stride_b=2 * 256 * 64, stride_h=256 * 64, stride_t=64)):
-        for op in (la.OP_FWD_GATED, la.OP_BWD_GATED):
-            assert la.linattn_workspace_size(sh, op) == (la.OK, 256)
-        assert la.linattn_workspace_size(sh, la.OP_CHECKPOINT_GATED) == (la.OK, 0)
+    # fp32 inputs take the CUDA-core path: no checkpoint, no workspace past the status header
+    sh = _shape(dtype=la.F32)
+    for op in (la.OP_FWD_GATED, la.OP_BWD_GATED):
+        assert la.linattn_workspace_size(sh, op) == (la.OK, 256)
+    assert la.linattn_workspace_size(sh, la.OP_CHECKPOINT_GATED) == (la.OK, 0)
+    # bf16 with d = 64 runs as the zero-padded d = 128 problem: its checkpoint holds d = 128
+    # states, and the workspace adds the padded copies of the states that cross the ABI
+    sh64 = _shape(dk=64, dv=64, stride_b=2 * 256 * 64, stride_h=256 * 64, stride_t=64)
+    assert la.linattn_workspace_size(sh64, la.OP_CHECKPOINT_GATED) == la.linattn_workspace_size(
+        s, la.OP_CHECKPOINT_GATED)
+    for op, extra in ((la.OP_FWD_GATED, 1), (la.OP_BWD_GATED, 2)):
+        st, n64 = la.linattn_workspace_size(sh64, op)
+        assert st == la.OK and n64 >= la.linattn_workspace_size(s, op)[1] + extra * 2 * 128 * 128 * 4
     # the per-head decay and gates exclude each other
     lam = (ctypes.c_float * 2)(0.9, 0.9)
     assert la.linattn_fwd_gated(_shape(decay=ctypes.cast(lam, ctypes.c_void_p)), FAKE, FAKE, FAKE,

@@ -5,8 +5,8 @@ Only the test-suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 shares no code with it.
 
 It also holds the causal softmax attention of a query segment over its
-gathered key/value prefix (``softmax_segment_fwd``: the standard-attention
-layers of the hybrid variant).
+gathered key/value prefix (``softmax_segment_fwd`` and its gradients
+``softmax_segment_bwd``: the standard-attention layers of the hybrid variant).
 
 Every linear-attention function takes numpy arrays shaped ``[B, H, T, d]`` (any float dtype; they
 are widened to float64) and per-head decays ``lam`` shaped ``[H]`` or
@@ -32,4 +32,4 @@ from .oracle import (  # noqa: F401
     state_scan,
     threads_used,
 )
-from .softmax_oracle import softmax_segment_fwd  # noqa: F401
+from .softmax_oracle import softmax_segment_bwd, softmax_segment_fwd  # noqa: F401

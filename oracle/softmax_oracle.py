@@ -17,6 +17,17 @@ are the last Tq positions of a prefix of Tk tokens (offset = Tk - Tq):
 
 written row by row with numpy as the library primitive (max subtraction only
 keeps exp in range; it cancels exactly in the ratio).
+
+The backward (``softmax_segment_bwd``: the gradients of q, k, v for an output
+gradient dO, which a hybrid model's training step needs of its softmax layers)
+is the chain rule through the same rows: with p_ij the row's softmax weights,
+
+    dv_j  = sum_i p_ij dO_i
+    dp_ij = dO_i . v_j,   delta_i = sum_j p_ij dp_ij,   ds_ij = p_ij (dp_ij - delta_i)
+    dq_i  = scale sum_j ds_ij k_j,      dk_j = scale sum_i ds_ij q_i
+
+(the softmax Jacobian diag(p) - p p^T applied to dp), summed over the visible
+pairs j <= offset + i only.
 """
 from __future__ import annotations
 
@@ -47,3 +58,29 @@ def softmax_segment_fwd(q, k, v, scale=None, rows=None):
         o[:, :, i] = np.einsum("bhj,bhje->bhe", p, v[:, :, :n]) / l[..., None]
         lse[:, :, i] = m[..., 0] + np.log(l)
     return o, lse
+
+
+def softmax_segment_bwd(q, k, v, dO, scale=None):
+    """(dq [B,H,Tq,d], dk [B,H,Tk,d], dv [B,H,Tk,dv]) in float64: the gradients of
+    <o, dO> for o = softmax_segment_fwd(q, k, v, scale)[0]; Tk >= Tq."""
+    q, k, v, dO = (np.asarray(x, dtype=np.float64) for x in (q, k, v, dO))
+    B, H, Tq, d = q.shape
+    Tk = k.shape[2]
+    assert k.shape[:2] == (B, H) and v.shape[:3] == (B, H, Tk) and Tk >= Tq and dO.shape == (B, H, Tq, v.shape[3])
+    off = Tk - Tq
+    sc = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for i in range(Tq):
+        n = off + i + 1                                         # keys 0 .. off + i
+        s = sc * np.einsum("bhjd,bhd->bhj", k[:, :, :n], q[:, :, i])
+        p = np.exp(s - s.max(axis=2, keepdims=True))
+        p /= p.sum(axis=2, keepdims=True)                       # the row's softmax weights
+        dv[:, :, :n] += p[..., None] * dO[:, :, i, None, :]
+        dp = np.einsum("bhje,bhe->bhj", v[:, :, :n], dO[:, :, i])
+        delta = np.sum(p * dp, axis=2, keepdims=True)
+        ds = p * (dp - delta)
+        dq[:, :, i] = sc * np.einsum("bhj,bhjd->bhd", ds, k[:, :, :n])
+        dk[:, :, :n] += sc * ds[..., None] * q[:, :, i, None, :]
+    return dq, dk, dv

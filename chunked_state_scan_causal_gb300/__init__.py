@@ -30,7 +30,7 @@ NOALLOC_MAX_TILES = 65536
 BF16, F32 = 0, 1
 OP_FWD, OP_BWD, OP_CHUNK_STATES, OP_CHECKPOINT = 1, 2, 3, 4
 OP_FWD_GATED, OP_BWD_GATED, OP_CHECKPOINT_GATED = 5, 6, 7
-OP_SOFTMAX_SEGMENT = 8
+OP_SOFTMAX_SEGMENT, OP_SOFTMAX_SEGMENT_BWD = 8, 9
 ABI_VERSION = 2
 
 
@@ -80,13 +80,15 @@ _SIGS = {
     "linattn_segment_decay": ([_vp, _i32, _i32, _i32, _vp, _vp], _i32),
     "linattn_softmax_segment_fwd": ([ctypes.POINTER(Shape), ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp,
                                      ctypes.c_float, _vp, _sz, _vp], _i32),
+    "linattn_softmax_segment_bwd": ([ctypes.POINTER(Shape), ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp,
+                                     _vp, _vp, _vp, ctypes.c_float, _vp, _sz, _vp], _i32),
     "linattn_diag_scan_withhold": ([_i32, _i32, _i32, _i32, _vp, _vp, _i32, ctypes.c_double, _vp, _sz, _vp],
                                    _i32),
     "linattn_timing_enable": ([_i32], _i32),
     "linattn_timing_collect": ([_i32, ctypes.POINTER(_i32), ctypes.POINTER(ctypes.c_float)], _i32),
     "linattn_kernel_name": ([_i32], ctypes.c_char_p),
 }
-KERNEL_KINDS = 16
+KERNEL_KINDS = 19
 
 
 def lib():
@@ -206,6 +208,12 @@ def linattn_device_status(ws, stream) -> int:
 def linattn_softmax_segment_fwd(q_shape, kv_shape, q, k, v, o, lse, softmax_scale, ws, ws_bytes, stream) -> int:
     return lib().linattn_softmax_segment_fwd(ctypes.byref(q_shape), ctypes.byref(kv_shape), q, k, v, o, lse,
                                              softmax_scale, ws, ws_bytes, stream)
+
+
+def linattn_softmax_segment_bwd(q_shape, kv_shape, q, k, v, o, dO, lse, dq, dk, dv, softmax_scale, ws, ws_bytes,
+                                stream) -> int:
+    return lib().linattn_softmax_segment_bwd(ctypes.byref(q_shape), ctypes.byref(kv_shape), q, k, v, o, dO, lse, dq,
+                                             dk, dv, softmax_scale, ws, ws_bytes, stream)
 
 
 def linattn_segment_decay(decay, B, H, seg_len, out, stream) -> int:
@@ -536,6 +544,31 @@ def softmax_segment_fwd(q, k, v, scale: float = 0.0, want_lse: bool = False, out
                                      _ptr(ws), ws.numel(), _stream(q.device, stream))
     _check(st, "linattn_softmax_segment_fwd")
     return o, lse
+
+
+def softmax_segment_bwd(q, k, v, o, dO, lse, scale: float = 0.0, outs=None, ws=None, stream=None):
+    """(dq, dk, dv): gradients of the causal softmax attention segment for the output
+    gradient dO, from the forward's o and lse (bf16 q, o, dO, dq with q's layout; k, v,
+    dk, dv with k's layout; scale 0 means 1/sqrt(128))."""
+    import torch
+    _same_layout(q, o)
+    _same_layout(q, dO)
+    _same_layout(k, v)
+    if outs is None:
+        outs = (torch.empty_strided(q.shape, q.stride(), dtype=q.dtype, device=q.device),
+                torch.empty_strided(k.shape, k.stride(), dtype=k.dtype, device=k.device),
+                torch.empty_strided(v.shape, v.stride(), dtype=v.dtype, device=v.device))
+    dq, dk, dv = outs
+    _same_layout(q, dq)
+    _same_layout(k, dk)
+    _same_layout(k, dv)
+    if ws is None:
+        ws = workspace(q, OP_SOFTMAX_SEGMENT_BWD)
+    st = linattn_softmax_segment_bwd(shape_of(q), shape_of(k), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO),
+                                     _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), scale, _ptr(ws), ws.numel(),
+                                     _stream(q.device, stream))
+    _check(st, "linattn_softmax_segment_bwd")
+    return dq, dk, dv
 
 
 def device_status(ws, stream=None) -> int:

@@ -316,6 +316,8 @@ int32_t linattn_workspace_size(const linattn_shape *shape, int32_t op, int32_t s
     *bytes = ckpt_bytes_gated(p);
   } else if (op == LINATTN_OP_SOFTMAX_SEGMENT) {
     *bytes = kHeader;
+  } else if (op == LINATTN_OP_SOFTMAX_SEGMENT_BWD) {
+    *bytes = kHeader + softmax_bwd_stats_bytes(p.B, p.H, p.T);
   } else {
     return LINATTN_ERR_INVALID;
   }
@@ -776,6 +778,35 @@ int32_t linattn_softmax_segment_fwd(const linattn_shape *q_shape, const linattn_
   return cuda_status(softmax_segment(sp, q, k, v, o, lse, static_cast<int *>(workspace), s));
 }
 
+int32_t linattn_softmax_segment_bwd(const linattn_shape *q_shape, const linattn_shape *kv_shape, const void *q,
+                                    const void *k, const void *v, const void *o, const void *dO, const float *lse,
+                                    void *dq, void *dk, void *dv, float softmax_scale, void *workspace,
+                                    size_t workspace_bytes, void *stream) {
+  Problem pq, pk;
+  int st = validate(q_shape, &pq);
+  if (st) return st;
+  if ((st = validate(kv_shape, &pk))) return st;
+  if (pq.B != pk.B || pq.H != pk.H || pq.d != pk.d || pq.dtype != pk.dtype || pk.T < pq.T) return LINATTN_ERR_INVALID;
+  if (pq.decay || pk.decay) return LINATTN_ERR_INVALID;
+  if (pq.dtype != 0 || pq.d != 128) return LINATTN_ERR_UNSUPPORTED;
+  if (!(softmax_scale > 0.f) && softmax_scale != 0.f) return LINATTN_ERR_INVALID;
+  if (pq.T > 0 && (st = check_ptrs({q, k, v, o, dO, lse, dq, dk, dv}, {}))) return st;
+  if (pq.T == 0 && pk.T > 0 && (st = check_ptrs({dk, dv}, {}))) return st;
+  if ((st = check_ws(workspace, workspace_bytes, kHeader + softmax_bwd_stats_bytes(pq.B, pq.H, pq.T)))) return st;
+  if ((st = device_ok())) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(workspace, 0, kHeader, s) != cudaSuccess) return LINATTN_ERR_CUDA;
+  SoftmaxProblem sp;
+  sp.B = pq.B; sp.H = pq.H; sp.Tq = pq.T; sp.Tk = pk.T;
+  sp.qsb = pq.sb; sp.qsh = pq.sh; sp.qst = pq.st;
+  sp.ksb = pk.sb; sp.ksh = pk.sh; sp.kst = pk.st;
+  sp.scale = softmax_scale > 0.f ? softmax_scale : 1.f / sqrtf((float)pq.d);
+  sp.num_sms = pq.num_sms;
+  char *ws = static_cast<char *>(workspace);
+  return cuda_status(softmax_segment_bwd(sp, q, k, v, o, dO, lse, dq, dk, dv, reinterpret_cast<float *>(ws + kHeader),
+                                         reinterpret_cast<int *>(ws), s));
+}
+
 int32_t linattn_segment_decay(const float *decay, int32_t B, int32_t H, int32_t seg_len, float *out,
                               void *stream) {
   if (B < 1 || H < 1 || seg_len < 0 || (int64_t)B * H > (1 << 30)) return LINATTN_ERR_INVALID;
@@ -853,7 +884,8 @@ const char *linattn_kernel_name(int32_t kind) {
                                        "tc_segment_aggregate", "tc_chunked_fwd",
                                        "diag_mma", "decode", "tc_dual_rev", "tc_chunked_fwd_agg",
                                        "gate_prep_and_grad", "tc_chunk_states", "softmax_segment",
-                                       "gated_vec_fwd", "gated_vec_bwd", "pad_d64"};
+                                       "gated_vec_fwd", "gated_vec_bwd", "pad_d64", "softmax_bwd_prep",
+                                       "softmax_bwd_dkdv", "softmax_bwd_dq"};
   return (kind >= 0 && kind < K_KINDS) ? names[kind] : "?";
 }
 

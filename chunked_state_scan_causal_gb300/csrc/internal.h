@@ -62,7 +62,7 @@ int device_ok();
 enum KernelKind {
   K_SIMT_FWD = 0, K_SIMT_BWD, K_SIMT_SEGMENT, K_SCAN, K_TC_AGG, K_TC_MAIN_FWD, K_DIAG,
   K_DECODE, K_TC_DUAL_REV, K_TC_MAIN_AGG, K_GATE, K_TC_CHUNK_STATES, K_SOFTMAX_SEGMENT, K_GATED_VEC_FWD,
-  K_GATED_VEC_BWD, K_PAD_D64, K_KINDS
+  K_GATED_VEC_BWD, K_PAD_D64, K_SOFTMAX_BWD_PREP, K_SOFTMAX_BWD_KV, K_SOFTMAX_BWD_Q, K_KINDS
 };
 // Records timing events around one launch on `s` while timing is enabled.
 struct TimedLaunch {
@@ -136,7 +136,8 @@ cudaError_t gate_grad(const Problem &p, const GroupPlan &gp, const float *gx, co
 // per-warp record of a wait that gave up, and each kernel kind keeps the two
 // counters of its dynamic item order at these offsets (each launch leaves them
 // zero again, so one call may launch a kind more than once).
-constexpr int kCounterAgg = 32, kCounterMain = 34, kCounterDual = 36, kCounterChunk = 38, kCounterSoftmax = 40;
+constexpr int kCounterAgg = 32, kCounterMain = 34, kCounterDual = 36, kCounterChunk = 38, kCounterSoftmax = 40,
+              kCounterSoftmaxKV = 42, kCounterSoftmaxQ = 44;
 bool tc_supported(const Problem &p);   // bf16, d = 128
 // The chunk groups of the tensor-core path (lengths multiples of 128, at most
 // 256 groups); max_len > 0 caps the lengths where possible.
@@ -199,6 +200,13 @@ cudaError_t gated_vec_bwd(const Problem &p, const void *q, const void *k, const 
                           void *dv, float *d_log_gate, float *d_init, cudaStream_t s);
 cudaError_t softmax_segment(const SoftmaxProblem &p, const void *q, const void *k, const void *v, void *o, float *lse,
                             int *status, cudaStream_t s);
+// The backward: dq (q strides), dk and dv (k strides) for the output gradient dO
+// (q strides), with the forward's o and lse; stats: softmax_bwd_stats_bytes of
+// device scratch for the per-query statistics.
+size_t softmax_bwd_stats_bytes(int B, int H, int Tq);
+cudaError_t softmax_segment_bwd(const SoftmaxProblem &p, const void *q, const void *k, const void *v, const void *o,
+                                const void *dO, const float *lse, void *dq, void *dk, void *dv, float *stats,
+                                int *status, cudaStream_t s);
 
 // ---------------------------------------------------------------- TMA descriptors (api.cu)
 // 4-D bf16 tiled tensor map, dims innermost first, strides in bytes for dims 1..3,

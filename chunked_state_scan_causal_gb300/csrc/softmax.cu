@@ -490,6 +490,369 @@ __global__ void __launch_bounds__(kSmThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
+// ============================================================================ backward
+// The gradients for an output gradient dO, with the forward's log-sum-exp per
+// query row (lse) and delta_i = dO_i . o_i (the softmax Jacobian's row term):
+//   p_ij  = exp(scale q_i . k_j - lse_i)         (the row's softmax weights, recomputed)
+//   ds_ij = p_ij (dO_i . v_j - delta_i)
+//   dv_j  = sum_i p_ij dO_i,  dk_j = scale sum_i ds_ij q_i,  dq_i = scale sum_j ds_ij k_j
+// over the visible pairs j <= offset + i, in two launches that share one kernel:
+//   dK/dV: an item is one 128-key tile (X = K, V); it streams the query tiles that
+//          see it (Y = Q, dO): S^T = K Q^T and dP^T = V dO^T into TMEM, the
+//          elementwise warps write p and ds back as bf16, then dV += P^T dO and
+//          dK += dS^T Q read them from TMEM as the A operand;
+//   dQ:    an item is one 128-query tile (X = Q, dO); it streams the key tiles up to
+//          its diagonal (Y = K, V): S = Q K^T, dP = dO V^T, then dQ += dS K.
+// No atomics: every output row is owned by one item.  Warp roles as in the
+// forward: warp 0 the TMA producer, warp 1 the MMA issuer, warps 2..5 and 6..9
+// the elementwise work on the score columns 0..63 and 64..127 of a tile (one
+// row per thread), and the epilogue.  The bf16 results of a column half go to
+// that half's own TMEM columns (64 g .. 64 g + 31), so neither half writes
+// columns that the other still reads.  Every wait is bounded.
+constexpr int kBwThreads = 320;
+constexpr int kBwSlots = 5;                                  // ring of Y tiles (32 KiB each)
+constexpr uint32_t kBwOffY = 2 * kTileBytes;                 // after the item's two X tiles
+constexpr uint32_t kBwOffBar = kBwOffY + kBwSlots * kTileBytes;
+constexpr size_t kBwSmem = kBwOffBar + 256 + 1024;
+static_assert(kBwSmem + 128 <= 232448, "tiles, barriers and static shared memory fit 227 KB");
+
+enum { B_XFULL = 0, B_XEMPTY, B_FULL, B_EMPTY = B_FULL + kBwSlots, B_SFULL = B_EMPTY + kBwSlots,
+       B_PREADY = B_SFULL + 1, B_AFULL = B_PREADY + 2, B_AEMPTY, B_COUNT };
+static_assert(B_COUNT * 8 + 4 <= 256, "backward barriers and the TMEM slot fit their 256 bytes");
+
+struct BwdParams {
+  int B, H, Tq, Tk, off, nqt, nkt, nitems;
+  float scale_log2;             // softmax scale times log2(e)
+  float scale;
+  const float *lse2, *delta;    // [B*H][nqt*128]: lse_i log2(e) and dO_i . o_i (+inf and 0 past Tq)
+  __nv_bfloat16 *out1, *out2;   // dK/dV: dv, dk;  dQ: dq
+  int64_t osb, osh, ost;        // element strides of the outputs
+  int wide;                     // every output row starts on a 32-byte boundary
+  int *status;
+  int *counter;                 // [2] item counter and finished CTAs (zero at launch)
+};
+
+// item -> (sequence, X tile, first Y tile, Y tiles), sequence-major (the items in
+// flight share their sequences' Y tiles in L2) and longest first inside a sequence:
+// dK/dV key tiles in ascending order (a key tile is seen by the query tiles from the
+// one holding position key - offset on), dQ query tiles in descending order (a query
+// tile sees the key tiles up to its diagonal).
+template <bool KV>
+__device__ __forceinline__ void bw_item(const BwdParams &P, int item, int &bh, int &xt, int &lo, int &ns) {
+  if (KV) {
+    bh = item / P.nkt;
+    xt = item % P.nkt;
+    lo = max(0, 128 * xt - P.off) / 128;
+    ns = P.nqt - lo;
+  } else {
+    bh = item / P.nqt;
+    xt = P.nqt - 1 - item % P.nqt;
+    lo = 0;
+    ns = min(P.nkt - 1, (P.off + 128 * xt + 127) / 128) + 1;
+  }
+}
+
+template <bool KV>
+__global__ void __launch_bounds__(kBwThreads, 1)
+    softmax_bwd_kernel(const __grid_constant__ CUtensorMap mx1, const __grid_constant__ CUtensorMap mx2,
+                       const __grid_constant__ CUtensorMap my1, const __grid_constant__ CUtensorMap my2, BwdParams P) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = align1024(smem_raw);
+  uint64_t *bar = reinterpret_cast<uint64_t *>(smem + kBwOffBar);
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + B_COUNT);
+  __shared__ int abort_flag;
+  __shared__ int ring_item[kRingS];
+  __shared__ uint64_t ring_bar[2 * kRingS];
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  int *const detail = P.status ? P.status + 1 + warp : nullptr;
+  uint64_t *ring_full = ring_bar, *ring_empty = ring_bar + kRingS;
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bar[B_XFULL], 1);
+    mbar_init(&bar[B_XEMPTY], 1);
+    for (int s = 0; s < kBwSlots; ++s) {
+      mbar_init(&bar[B_FULL + s], 1);
+      mbar_init(&bar[B_EMPTY + s], 1);
+    }
+    mbar_init(&bar[B_SFULL], 1);
+    mbar_init(&bar[B_PREADY], 128);
+    mbar_init(&bar[B_PREADY + 1], 128);
+    mbar_init(&bar[B_AFULL], 1);
+    mbar_init(&bar[B_AEMPTY], 256);
+    for (int i = 0; i < kRingS; ++i) {
+      mbar_init(&ring_full[i], 1);
+      mbar_init(&ring_empty[i], 32 + 256);  // readers: the MMA warp, the eight elementwise warps
+    }
+    fence_mbar_init();
+    prefetch_tensormap(&mx1);
+    prefetch_tensormap(&mx2);
+    prefetch_tensormap(&my1);
+    prefetch_tensormap(&my2);
+  }
+  if (warp == 1) {
+    tmem_alloc(tslot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  // TMEM: the two score tiles (X1 Y1^T, X2 Y2^T; their bf16 results in place), the accumulators
+  const uint32_t tS = tmem, tP = tmem + 128u, tA1 = tmem + 256u, tA2 = tmem + 384u;
+  auto sX = [&](int x) { return smem_u32(smem) + (uint32_t)x * kTileBytes; };
+  auto slot_addr = [&](int i) { return smem_u32(smem + kBwOffY) + (uint32_t)(i % kBwSlots) * kTileBytes; };
+  auto wait = [&](int idx, int parity) { return mbar_wait(&bar[idx], parity & 1, &abort_flag, P.status, detail); };
+  auto take = [&](int k, int &item) {
+    const int s = k % kRingS;
+    if (!mbar_wait(&ring_full[s], (k / kRingS) & 1, &abort_flag, P.status, detail)) return false;
+    item = *reinterpret_cast<volatile int *>(&ring_item[s]);
+    mbar_arrive(&ring_empty[s]);
+    return true;
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int li = 0, nx = 0;  // Y tiles and X tile pairs loaded
+      bool ok = true;
+      auto load = [&](const CUtensorMap *m, int row, int h, int b) {
+        const int s = li % kBwSlots, u = li / kBwSlots;
+        if (u > 0 && !(ok = wait(B_EMPTY + s, u - 1))) return;
+        uint8_t *dst = smem + kBwOffY + s * kTileBytes;
+        mbar_arrive_expect_tx(&bar[B_FULL + s], kTileBytes);
+        tma_load_4d(m, &bar[B_FULL + s], dst, 0, row, h, b, kPolicyEvictLast);
+        tma_load_4d(m, &bar[B_FULL + s], dst + kTileHalfBytes, 64, row, h, b, kPolicyEvictLast);
+        ++li;
+      };
+      for (int k = 0;; ++k) {
+        const int s = k % kRingS;
+        if (k >= kRingS && !(ok = mbar_wait(&ring_empty[s], (k / kRingS - 1) & 1, &abort_flag, P.status, detail)))
+          break;
+        const int x = atomicAdd(P.counter, 1), item = x < P.nitems ? x : -1;
+        *reinterpret_cast<volatile int *>(&ring_item[s]) = item;
+        mbar_arrive(&ring_full[s]);
+        if (item < 0) break;
+        int bh, xt, lo, ns;
+        bw_item<KV>(P, item, bh, xt, lo, ns);
+        const int b = bh / P.H, h = bh % P.H;
+        if (k > 0 && !(ok = wait(B_XEMPTY, k - 1))) break;  // the previous item's score products read X
+        mbar_arrive_expect_tx(&bar[B_XFULL], 2 * kTileBytes);
+        tma_load_4d(&mx1, &bar[B_XFULL], smem, 0, 128 * xt, h, b, kPolicyEvictFirst);
+        tma_load_4d(&mx1, &bar[B_XFULL], smem + kTileHalfBytes, 64, 128 * xt, h, b, kPolicyEvictFirst);
+        tma_load_4d(&mx2, &bar[B_XFULL], smem + kTileBytes, 0, 128 * xt, h, b, kPolicyEvictFirst);
+        tma_load_4d(&mx2, &bar[B_XFULL], smem + kTileBytes + kTileHalfBytes, 64, 128 * xt, h, b, kPolicyEvictFirst);
+        ++nx;
+        for (int n = 0; n < ns && ok; ++n) {
+          load(&my1, 128 * (lo + n), h, b);
+          if (ok) load(&my2, 128 * (lo + n), h, b);
+        }
+        if (!ok) break;
+      }
+      // time-bounded drain of the loads in flight (also after an abort)
+      volatile int no_abort = 0;
+      if (nx > 0) mbar_wait(&bar[B_XFULL], (nx - 1) & 1, &no_abort, P.status);
+      for (int s = 0; s < kBwSlots; ++s) {
+        const int uses = li > s ? (li - 1 - s) / kBwSlots + 1 : 0;
+        if (uses > 0) mbar_wait(&bar[B_FULL + s], (uses - 1) & 1, &no_abort, P.status);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (the whole warp)
+    const uint32_t id_ss = idesc_bf16(128, 128, false, false);  // X Y^T
+    const uint32_t id_ts = idesc_bf16(128, 128, false, true);   // (bf16 tile in TMEM) Y
+    int li = 0, u = 0;
+    bool ok = true;
+    auto wait_all = [&](int idx, int parity) { return __all_sync(0xffffffffu, wait(idx, parity)); };
+    for (int k = 0, item; ok; ++k) {
+      if (!(ok = __all_sync(0xffffffffu, take(k, item))) || item < 0) break;
+      int bh, xt, lo, ns;
+      bw_item<KV>(P, item, bh, xt, lo, ns);
+      if (!(ok = wait_all(B_XFULL, k))) break;
+      for (int n = 0; n < ns && ok; ++n, ++u, li += 2) {
+        const int i1 = li, i2 = li + 1;
+        if (!(ok = wait_all(B_FULL + i1 % kBwSlots, i1 / kBwSlots) && wait_all(B_FULL + i2 % kBwSlots, i2 / kBwSlots)))
+          break;
+        tc_fence_after();
+        const uint32_t Y1 = slot_addr(i1), Y2 = slot_addr(i2);
+        // the two score tiles (issued behind the previous step's accumulation, which
+        // reads the bf16 results these overwrite)
+#pragma unroll
+        for (uint32_t ks = 0; ks < 8; ++ks) mma_ss_warp(tS, desc_kmajor(sX(0), ks), desc_kmajor(Y1, ks), id_ss, ks > 0);
+#pragma unroll
+        for (uint32_t ks = 0; ks < 8; ++ks) mma_ss_warp(tP, desc_kmajor(sX(1), ks), desc_kmajor(Y2, ks), id_ss, ks > 0);
+        mma_commit_warp(&bar[B_SFULL]);
+        if (n + 1 == ns) mma_commit_warp(&bar[B_XEMPTY]);
+        // the accumulators are free once the previous item's epilogue has read them
+        if (n == 0 && k > 0 && !(ok = wait_all(B_AEMPTY, k - 1))) break;
+        // accumulate over the Y rows (the contraction) one column half at a time, as
+        // soon as that half's bf16 results are in TMEM
+        for (int g = 0; g < 2 && ok; ++g) {
+          if (!(ok = wait_all(B_PREADY + g, u))) break;
+          tc_fence_after();
+#pragma unroll
+          for (uint32_t kk = 0; kk < 4; ++kk) {
+            const uint32_t ks = 4u * g + kk, col = 64u * g + 8u * kk, acc = (n > 0 || ks > 0) ? 1u : 0u;
+            if (KV) {
+              mma_ts_warp(tA1, tS + col, desc_mnmajor(Y2, ks), id_ts, acc);  // dV += P^T dO
+              mma_ts_warp(tA2, tP + col, desc_mnmajor(Y1, ks), id_ts, acc);  // dK += dS^T Q
+            } else {
+              mma_ts_warp(tA1, tP + col, desc_mnmajor(Y1, ks), id_ts, acc);  // dQ += dS K
+            }
+          }
+        }
+        if (!ok) break;
+        mma_commit_warp(&bar[B_EMPTY + i1 % kBwSlots]);
+        mma_commit_warp(&bar[B_EMPTY + i2 % kBwSlots]);
+        if (n + 1 == ns) mma_commit_warp(&bar[B_AFULL]);
+      }
+    }
+  } else if (warp >= 2 && warp < 10) {
+    // ------------------------------------------------------------ p and ds for a column half, epilogue
+    const int g = (warp - 2) >> 2;
+    const uint32_t quad = warp & 3, row = quad * 32 + lane, lb = (quad * 32) << 16;
+    int u = 0;
+    bool ok = true;
+    for (int k = 0, item; ok; ++k) {
+      if (!(ok = __all_sync(0xffffffffu, take(k, item))) || item < 0) break;
+      int bh, xt, lo, ns;
+      bw_item<KV>(P, item, bh, xt, lo, ns);
+      const float *L2 = P.lse2 + (int64_t)bh * P.nqt * 128, *DL = P.delta + (int64_t)bh * P.nqt * 128;
+      // dQ: this row's query statistics
+      const float lrow = KV ? 0.f : L2[128 * xt + row], drow = KV ? 0.f : DL[128 * xt + row];
+      for (int n = 0; n < ns; ++n, ++u) {
+        const int yt = lo + n;
+        if (!(ok = __all_sync(0xffffffffu, wait(B_SFULL, u)))) break;
+        tc_fence_after();
+        // dK/dV: key 128 xt + row sees the query columns c >= lim;  dQ: query 128 xt + row
+        // sees the key columns c <= lim
+        const int lim = KV ? 128 * (xt - yt) + (int)row - P.off : P.off + 128 * (xt - yt) + (int)row;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int c0 = 64 * g + 32 * hh;
+          uint32_t sr[32], dr[32];
+          tmem_ld32(tS + lb + c0, sr);
+          tmem_ld32(tP + lb + c0, dr);
+          tmem_ld_wait();
+          uint32_t wp[16], wd[16];
+#pragma unroll
+          for (int j4 = 0; j4 < 8; ++j4) {
+            float lv[4], dl[4];
+            if (KV) {
+              const float4 l4 = *reinterpret_cast<const float4 *>(L2 + 128 * yt + c0 + 4 * j4);
+              const float4 d4 = *reinterpret_cast<const float4 *>(DL + 128 * yt + c0 + 4 * j4);
+              lv[0] = l4.x; lv[1] = l4.y; lv[2] = l4.z; lv[3] = l4.w;
+              dl[0] = d4.x; dl[1] = d4.y; dl[2] = d4.z; dl[3] = d4.w;
+            } else {
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                lv[e] = lrow;
+                dl[e] = drow;
+              }
+            }
+            float pe[4], de[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int j = 4 * j4 + e, c = c0 + j;
+              float p = ex2(fmaf(__uint_as_float(sr[j]), P.scale_log2, -lv[e]));
+              if (KV ? c < lim : c > lim) p = 0.f;
+              pe[e] = p;
+              de[e] = p * (__uint_as_float(dr[j]) - dl[e]);
+            }
+            wp[2 * j4] = pack_bf16(pe[0], pe[1]);
+            wp[2 * j4 + 1] = pack_bf16(pe[2], pe[3]);
+            wd[2 * j4] = pack_bf16(de[0], de[1]);
+            wd[2 * j4 + 1] = pack_bf16(de[2], de[3]);
+          }
+          if (KV) tmem_st16(tS + lb + 64 * g + 16 * hh, wp);
+          tmem_st16(tP + lb + 64 * g + 16 * hh, wd);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bar[B_PREADY + g]);
+      }
+      if (!ok) break;
+      // epilogue: dK/dV: the first half stores the dv row, the second the dk row (times the
+      // scale); dQ: each half stores its 64 columns of the dq row (times the scale)
+      if (!(ok = __all_sync(0xffffffffu, wait(B_AFULL, k)))) break;
+      tc_fence_after();
+      const int b = bh / P.H, h = bh % P.H, r = 128 * xt + (int)row;
+      const bool valid = r < (KV ? P.Tk : P.Tq);
+      __nv_bfloat16 *dst = (KV && g == 1 ? P.out2 : P.out1) + (int64_t)b * P.osb + (int64_t)h * P.osh +
+                           (int64_t)r * P.ost + (KV ? 0 : 64 * g);
+      const uint32_t src = (KV ? (g == 0 ? tA1 : tA2) : tA1 + 64u * g) + lb;
+      const float f = KV && g == 0 ? 1.f : P.scale;
+#pragma unroll 1
+      for (int c = 0; c < (KV ? 4 : 2); ++c) {
+        float y[32];
+        uint32_t o[32];
+        tmem_ld32(src + 32 * c, o);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) y[j] = __uint_as_float(o[j]) * f;
+        if (valid) st_row_chunk(dst + 32 * c, y, P.wide != 0);
+      }
+      tc_fence_before();
+      mbar_arrive(&bar[B_AEMPTY]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(P.counter + 1, 1) == (int)gridDim.x - 1) {
+      atomicExch(P.counter, 0);
+      atomicExch(P.counter + 1, 0);
+    }
+  }
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// The per-query statistics of the backward, one warp per padded query row:
+// lse2 = lse log2(e) and delta = dO . o (fp32 from the bf16 rows); past Tq +inf and 0.
+__global__ void __launch_bounds__(256) softmax_bwd_prep_kernel(const __nv_bfloat16 *o, const __nv_bfloat16 *dO,
+                                                               const float *lse, int H, int Tq, int rows_pad,
+                                                               int64_t sb, int64_t sh, int64_t st, int64_t nrows,
+                                                               float *lse2, float *delta) {
+  const int64_t r = ((int64_t)blockIdx.x * 256 + threadIdx.x) / 32;
+  const int lane = threadIdx.x % 32;
+  if (r >= nrows) return;
+  const int64_t bh = r / rows_pad;
+  const int i = (int)(r % rows_pad);
+  if (i >= Tq) {
+    if (lane == 0) {
+      lse2[r] = INFINITY;
+      delta[r] = 0.f;
+    }
+    return;
+  }
+  const int64_t off = (bh / H) * sb + (bh % H) * sh + (int64_t)i * st + 4 * lane;
+  const uint2 a = *reinterpret_cast<const uint2 *>(o + off), c = *reinterpret_cast<const uint2 *>(dO + off);
+  const __nv_bfloat162 *a2 = reinterpret_cast<const __nv_bfloat162 *>(&a), *c2 = reinterpret_cast<const __nv_bfloat162 *>(&c);
+  float acc = 0.f;
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    const float2 x = __bfloat1622float2(a2[e]), y = __bfloat1622float2(c2[e]);
+    acc = fmaf(x.x, y.x, acc);
+    acc = fmaf(x.y, y.y, acc);
+  }
+#pragma unroll
+  for (int m = 16; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+  if (lane == 0) {
+    lse2[r] = lse[bh * Tq + i] * 1.4426950408889634f;
+    delta[r] = acc;
+  }
+}
+
+// Zero rows of 128 bf16 (the key gradients when no query is given), one warp per row.
+__global__ void __launch_bounds__(256) zero_rows_kernel(__nv_bfloat16 *x, int H, int T, int64_t sb, int64_t sh,
+                                                        int64_t st, int64_t nrows) {
+  const int64_t r = ((int64_t)blockIdx.x * 256 + threadIdx.x) / 32;
+  if (r >= nrows) return;
+  const int64_t bh = r / T, i = r % T;
+  *reinterpret_cast<uint2 *>(x + (bh / H) * sb + (bh % H) * sh + i * st + 4 * (threadIdx.x % 32)) = make_uint2(0u, 0u);
+}
+
 bool tmap_seq(const void *base, int B, int H, int T, int64_t sb, int64_t sh, int64_t st, CUtensorMap *m) {
   const uint64_t dims[4] = {128, (uint64_t)T, (uint64_t)H, (uint64_t)B};
   const uint64_t strides[3] = {(uint64_t)st * 2, (uint64_t)sh * 2, (uint64_t)sb * 2};
@@ -522,6 +885,84 @@ cudaError_t softmax_segment(const SoftmaxProblem &p, const void *q, const void *
   if (e != cudaSuccess) return e;
   TimedLaunch t(K_SOFTMAX_SEGMENT, s);
   softmax_segment_kernel<<<grid, kSmThreads, kSmSmem, s>>>(mq, mk, mv, S);
+  return cudaGetLastError();
+}
+
+
+size_t softmax_bwd_stats_bytes(int B, int H, int Tq) {
+  return 2 * align256((size_t)B * H * ((Tq + 127) / 128) * 128 * sizeof(float));
+}
+
+cudaError_t softmax_segment_bwd(const SoftmaxProblem &p, const void *q, const void *k, const void *v, const void *o,
+                                const void *dO, const float *lse, void *dq, void *dk, void *dv, float *stats,
+                                int *status, cudaStream_t s) {
+  const int64_t BH = (int64_t)p.B * p.H;
+  if (!status) return cudaErrorInvalidValue;
+  if (p.Tq == 0) {
+    // no queries: every key gradient is zero
+    const int64_t nrows = BH * p.Tk;
+    if (nrows == 0) return cudaSuccess;
+    const unsigned blocks = (unsigned)((nrows * 32 + 255) / 256);
+    TimedLaunch t(K_SOFTMAX_BWD_PREP, s);
+    zero_rows_kernel<<<blocks, 256, 0, s>>>(static_cast<__nv_bfloat16 *>(dk), p.H, p.Tk, p.ksb, p.ksh, p.kst, nrows);
+    zero_rows_kernel<<<blocks, 256, 0, s>>>(static_cast<__nv_bfloat16 *>(dv), p.H, p.Tk, p.ksb, p.ksh, p.kst, nrows);
+    return cudaGetLastError();
+  }
+  alignas(64) CUtensorMap mq, mk, mv, mdo;
+  if (!tmap_seq(q, p.B, p.H, p.Tq, p.qsb, p.qsh, p.qst, &mq) || !tmap_seq(dO, p.B, p.H, p.Tq, p.qsb, p.qsh, p.qst, &mdo) ||
+      !tmap_seq(k, p.B, p.H, p.Tk, p.ksb, p.ksh, p.kst, &mk) || !tmap_seq(v, p.B, p.H, p.Tk, p.ksb, p.ksh, p.kst, &mv))
+    return cudaErrorInvalidValue;
+  BwdParams P;
+  P.B = p.B; P.H = p.H; P.Tq = p.Tq; P.Tk = p.Tk; P.off = p.Tk - p.Tq;
+  P.nqt = (p.Tq + 127) / 128;
+  P.nkt = (p.Tk + 127) / 128;
+  P.scale_log2 = p.scale * 1.4426950408889634f;
+  P.scale = p.scale;
+  const int64_t nrows = BH * P.nqt * 128;
+  float *lse2 = stats, *delta = stats + align256((size_t)nrows * sizeof(float)) / sizeof(float);
+  P.lse2 = lse2;
+  P.delta = delta;
+  P.status = status;
+  cudaError_t e;
+  {
+    TimedLaunch t(K_SOFTMAX_BWD_PREP, s);
+    softmax_bwd_prep_kernel<<<(unsigned)((nrows * 32 + 255) / 256), 256, 0, s>>>(
+        static_cast<const __nv_bfloat16 *>(o), static_cast<const __nv_bfloat16 *>(dO), lse, p.H, p.Tq, P.nqt * 128,
+        p.qsb, p.qsh, p.qst, nrows, lse2, delta);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  auto a32 = [](const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 31u) == 0; };
+  // dK, dV: items over the key tiles
+  {
+    BwdParams K = P;
+    K.nitems = (int)(P.nkt * BH);
+    K.out1 = static_cast<__nv_bfloat16 *>(dv);
+    K.out2 = static_cast<__nv_bfloat16 *>(dk);
+    K.osb = p.ksb; K.osh = p.ksh; K.ost = p.kst;
+    K.wide = a32(dk) && a32(dv) && (p.ksb * 2) % 32 == 0 && (p.ksh * 2) % 32 == 0 && (p.kst * 2) % 32 == 0;
+    K.counter = status + kCounterSoftmaxKV;
+    if ((e = cudaFuncSetAttribute(softmax_bwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)kBwSmem)) != cudaSuccess)
+      return e;
+    TimedLaunch t(K_SOFTMAX_BWD_KV, s);
+    softmax_bwd_kernel<true><<<K.nitems < p.num_sms ? K.nitems : p.num_sms, kBwThreads, kBwSmem, s>>>(mk, mv, mq, mdo,
+                                                                                                      K);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  // dQ: items over the query tiles
+  BwdParams Q = P;
+  Q.nitems = (int)(P.nqt * BH);
+  Q.out1 = static_cast<__nv_bfloat16 *>(dq);
+  Q.out2 = nullptr;
+  Q.osb = p.qsb; Q.osh = p.qsh; Q.ost = p.qst;
+  Q.wide = a32(dq) && (p.qsb * 2) % 32 == 0 && (p.qsh * 2) % 32 == 0 && (p.qst * 2) % 32 == 0;
+  Q.counter = status + kCounterSoftmaxQ;
+  if ((e = cudaFuncSetAttribute(softmax_bwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kBwSmem)) != cudaSuccess)
+    return e;
+  TimedLaunch t(K_SOFTMAX_BWD_Q, s);
+  softmax_bwd_kernel<false><<<Q.nitems < p.num_sms ? Q.nitems : p.num_sms, kBwThreads, kBwSmem, s>>>(mq, mdo, mk, mv,
+                                                                                                     Q);
   return cudaGetLastError();
 }
 

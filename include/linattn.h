@@ -78,7 +78,7 @@ enum { LINATTN_BF16 = 0, LINATTN_F32 = 1 };
 /* Workspace / checkpoint queries. */
 enum { LINATTN_OP_FWD = 1, LINATTN_OP_BWD = 2, LINATTN_OP_CHUNK_STATES = 3, LINATTN_OP_CHECKPOINT = 4,
        LINATTN_OP_FWD_GATED = 5, LINATTN_OP_BWD_GATED = 6, LINATTN_OP_CHECKPOINT_GATED = 7,
-       LINATTN_OP_SOFTMAX_SEGMENT = 8 };
+       LINATTN_OP_SOFTMAX_SEGMENT = 8, LINATTN_OP_SOFTMAX_SEGMENT_BWD = 9 };
 
 typedef struct {
   int32_t abi_version;  /* must be LINATTN_ABI_VERSION                              */
@@ -261,7 +261,7 @@ int32_t linattn_chunk_states_rev(const linattn_shape *shape, int32_t seg_len, co
  *   o_i   = sum_{j <= offset+i} softmax_j(scale q_i . k_j) v_j
  *   lse_i = log sum_{j <= offset+i} exp(scale q_i . k_j)
  * (blockwise with a running maximum and sum per row; the full row softmax is
- * never formed).  Forward only.
+ * never formed).  The gradients are linattn_softmax_segment_bwd.
  *   q_shape:  B, H, T = Tq and the element strides of q and o
  *   kv_shape: B, H, T = Tk and the element strides of k and v
  *   both: bf16, dk = dv = 128, chunk = 64, decay NULL (else INVALID/UNSUPPORTED)
@@ -272,6 +272,25 @@ int32_t linattn_chunk_states_rev(const linattn_shape *shape, int32_t seg_len, co
 int32_t linattn_softmax_segment_fwd(const linattn_shape *q_shape, const linattn_shape *kv_shape, const void *q,
                                     const void *k, const void *v, void *o, float *lse, float softmax_scale,
                                     void *workspace, size_t workspace_bytes, void *stream);
+
+/* Gradients of the softmax-attention segment (the training step of the hybrid's
+ * softmax layers): for an output gradient dO, with the forward's o and lse,
+ *   p_ij  = exp(scale q_i . k_j - lse_i),   delta_i = dO_i . o_i,
+ *   ds_ij = p_ij (dO_i . v_j - delta_i),
+ *   dv_j  = sum_i p_ij dO_i,  dk_j = scale sum_i ds_ij q_i,  dq_i = scale sum_j ds_ij k_j
+ * over the visible pairs j <= offset + i (offset = Tk - Tq).  p and ds enter the
+ * products as bf16 (fp32 accumulation); delta is taken from the bf16 o.
+ *   q_shape:  B, H, T = Tq and the element strides of q, o, dO and dq
+ *   kv_shape: B, H, T = Tk and the element strides of k, v, dk and dv
+ *   both: bf16, dk = dv = 128, decay NULL (else INVALID/UNSUPPORTED)
+ *   lse [B,H,Tq] fp32 contiguous (the forward's); softmax_scale as in the forward
+ *   workspace: LINATTN_OP_SOFTMAX_SEGMENT_BWD bytes for q_shape (status word, item
+ *   counters and two fp32 statistics per query row)
+ * Every output row is written (Tq = 0: dk and dv are zero).  Returns a status. */
+int32_t linattn_softmax_segment_bwd(const linattn_shape *q_shape, const linattn_shape *kv_shape, const void *q,
+                                    const void *k, const void *v, const void *o, const void *dO, const float *lse,
+                                    void *dq, void *dk, void *dv, float softmax_scale, void *workspace,
+                                    size_t workspace_bytes, void *stream);
 
 /* Workspace bytes for linattn_state_scan. */
 int32_t linattn_state_scan_workspace_size(int32_t G, int32_t BH, int32_t dk, int32_t dv,
@@ -346,7 +365,7 @@ int32_t linattn_device_status(const void *workspace, void *stream);
  * for every kernel kind k < max_kinds its launch count and summed device time
  * (ms), clears the record and returns the number of kinds
  * (LINATTN_KERNEL_KINDS), or a negative status. */
-#define LINATTN_KERNEL_KINDS 16
+#define LINATTN_KERNEL_KINDS 19
 int32_t linattn_timing_enable(int32_t on);
 int32_t linattn_timing_collect(int32_t max_kinds, int32_t *launches, float *total_ms);
 /* Name of kernel kind k (static string; "?" when out of range). */

@@ -756,31 +756,52 @@ def run_softmax_segment(args):
     v = torch.randn(B, H, Tk, d, generator=g).to(torch.bfloat16).to(dev)
     o = torch.empty_like(q)
     ws = la.workspace(q, la.OP_SOFTMAX_SEGMENT)
+    bwd = args.sm_bwd
+    if bwd:
+        # the backward alone, from the forward's o and lse
+        dO = torch.randn(B, H, Tq, d, generator=g).to(torch.bfloat16).to(dev)
+        _, lse = la.softmax_segment_fwd(q, k, v, out=o, want_lse=True, ws=ws)
+        wsb = la.workspace(q, la.OP_SOFTMAX_SEGMENT_BWD)
+        outs = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+        step = lambda: la.softmax_segment_bwd(q, k, v, o, dO, lse, outs=outs, ws=wsb)
+    else:
+        wsb = ws
+        step = lambda: la.softmax_segment_fwd(q, k, v, out=o, ws=ws)
     for _ in range(args.warmup):
-        la.softmax_segment_fwd(q, k, v, out=o, ws=ws)
+        step()
     torch.cuda.synchronize()
-    if la.device_status(ws) != la.OK:
+    if la.device_status(wsb) != la.OK:
         raise RuntimeError("device-side error during warm-up")
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(_gpu_uuid(dev), 0) as clk:
         torch.cuda.synchronize()
         e0.record()
         for _ in range(args.steps):
-            la.softmax_segment_fwd(q, k, v, out=o, ws=ws)
+            step()
         e1.record()
         torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / args.steps
+    # per-kernel times from a separate pass (the library's event timing stays off above)
+    la.linattn_timing_enable(True)
+    la.linattn_timing_collect()
+    for _ in range(min(args.steps, 10)):
+        step()
+    torch.cuda.synchronize()
+    kern = {name: round(t / n, 4) for name, (n, t) in la.linattn_timing_collect().items()}
+    la.linattn_timing_enable(False)
     off = Tk - Tq
     pairs = Tq * off + Tq * (Tq + 1) // 2
-    flops = 4 * d * pairs * B * H
-    bytes_ = (2 * Tq + 2 * Tk) * d * 2 * B * H  # q, o; k, v once
+    # forward: Q K^T and P V (4 d per visible pair); backward: the five products of the
+    # usual count, Q K^T (recomputed), dO V^T, P^T dO, dS^T Q, dS K (10 d per pair)
+    flops = (10 if bwd else 4) * d * pairs * B * H
+    bytes_ = ((4 * Tq + 4 * Tk) if bwd else (2 * Tq + 2 * Tk)) * d * 2 * B * H  # each tensor once
     p = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
         os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
     peak = float(p.get("bf16_tflops", 1900.0))
     src = "measured bf16_tflops (burst, of measured)" if "bf16_tflops" in p else "fallback 1900 TFLOP/s"
     tf = flops / (ms * 1e-3) / 1e12
     cpu = None
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and not bwd:
         import oracle
         rows = list(range(0, Tq, max(1, Tq // 16)))[:16]
         qn, kn, vn = (x[0:1, 0:4].double().cpu().numpy() for x in (q, k, v))
@@ -790,16 +811,32 @@ def run_softmax_segment(args):
         rp = sum(off + r + 1 for r in rows) * 4
         cpu = {"value": 4 * d * rp / sec / 1e12, "unit": "TFLOP/s", "cores": oracle.threads_used(), "kind": "oracle",
                "sample": f"heads 0..3, {len(rows)} query rows spread over the segment, fp64 numpy, {sec:.2f} s"}
+    if bwd and not args.no_cpu_baseline:
+        # the last 128 queries of head 0 over the whole prefix (the same positions as in the
+        # workload: its queries are the prefix's last Tq)
+        import oracle
+        n_s = min(128, Tq)
+        qs, dOs = (x[0:1, 0:1, Tq - n_s:].double().cpu().numpy() for x in (q, dO))
+        ks, vs = (x[0:1, 0:1].double().cpu().numpy() for x in (k, v))
+        t0 = time.perf_counter()
+        oracle.softmax_segment_bwd(qs, ks, vs, dOs)
+        sec = time.perf_counter() - t0
+        sp = n_s * (Tk - n_s) + n_s * (n_s + 1) // 2
+        cpu = {"value": 10 * d * sp / sec / 1e12, "unit": "TFLOP/s", "cores": oracle.threads_used(), "kind": "oracle",
+               "sample": f"head 0, the last {n_s} queries over the {Tk}-token prefix, fp64 numpy, {sec:.2f} s"}
     print(json.dumps({
-        "metric": "causal softmax-attention segment TFLOP/s (hybrid layers, prefix gathered)", "value": tf,
+        "metric": "causal softmax-attention segment " + ("backward " if bwd else "") +
+                  "TFLOP/s (hybrid layers, prefix gathered)", "value": tf,
         "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "dtype": "bf16", "data": "synthetic (seeded normal)",
         "config": {"workload": f"softmax-segment-B{B}H{H}-Tq{Tq}-Tk{Tk}-d{d}", "B": B, "H": H, "Tq": Tq, "Tk": Tk,
                    "d": d, "causal": True, "scale": "1/sqrt(d)"},
         "tokens_per_s": B * Tq / (ms * 1e-3), "algorithmic_gbs": bytes_ / (ms * 1e-3) / 1e9,
-        "roofline": {"kernel": "softmax_segment_kernel", "bound": "tensor", "achieved": tf, "peak": peak,
-                     "unit": "TFLOP/s", "frac": tf / peak, "traffic": None, "peak_source": src},
-        "gpu_launches": args.steps, "clocks": clk.summary(), "cpu_baseline": cpu}), flush=True)
+        "roofline": {"kernel": "softmax_bwd_kernel (dK/dV and dQ)" if bwd else "softmax_segment_kernel",
+                     "bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s", "frac": tf / peak,
+                     "traffic": None, "peak_source": src},
+        "kernels_ms": kern, "gpu_launches": args.steps * (3 if bwd else 1), "clocks": clk.summary(),
+        "cpu_baseline": cpu}), flush=True)
 
 
 # ---------------------------------------------------------------------------------- sequence split
@@ -891,6 +928,7 @@ def main():
     ap.add_argument("--softmax-segment", action="store_true", help="measure the softmax-attention segment instead")
     ap.add_argument("--sm-tq", type=int, default=16384, help="queries of the softmax segment")
     ap.add_argument("--sm-tk", type=int, default=65536, help="gathered prefix length of the softmax segment")
+    ap.add_argument("--sm-bwd", action="store_true", help="with --softmax-segment: time the backward")
     ap.add_argument("--traffic-from", default="", help="ncu CSV of whole steps (dram__bytes_read/write.sum): "
                     "store DRAM bytes per token-head in profiles/traffic.json and exit")
     ap.add_argument("--traffic-steps", type=int, default=1, help="steps the --traffic-from capture covers")

@@ -510,14 +510,17 @@ __global__ void __launch_bounds__(kSmThreads, 1)
 // that half's own TMEM columns (64 g .. 64 g + 31), so neither half writes
 // columns that the other still reads.  Every wait is bounded.
 constexpr int kBwThreads = 320;
-constexpr int kBwSlots = 5;                                  // ring of Y tiles (32 KiB each)
+constexpr int kBwSlots = 5;                                  // ring of Y tiles (32 KiB each), at most
+// the dK/dV kernel keeps one slot fewer: its column statistics take 2 KiB of static shared memory
+template <bool KV> constexpr int bw_slots() { return KV ? kBwSlots - 1 : kBwSlots; }
 constexpr uint32_t kBwOffY = 2 * kTileBytes;                 // after the item's two X tiles
-constexpr uint32_t kBwOffBar = kBwOffY + kBwSlots * kTileBytes;
-constexpr size_t kBwSmem = kBwOffBar + 256 + 1024;
-static_assert(kBwSmem + 128 <= 232448, "tiles, barriers and static shared memory fit 227 KB");
+template <bool KV> constexpr uint32_t bw_off_bar() { return kBwOffY + bw_slots<KV>() * kTileBytes; }
+template <bool KV> constexpr size_t bw_smem() { return bw_off_bar<KV>() + 256 + 1024; }
+static_assert(bw_smem<false>() + 128 <= 232448 && bw_smem<true>() + 2048 + 128 <= 232448,
+              "tiles, barriers and static shared memory fit 227 KB");
 
-enum { B_XFULL = 0, B_XEMPTY, B_FULL, B_EMPTY = B_FULL + kBwSlots, B_SFULL = B_EMPTY + kBwSlots,
-       B_PREADY = B_SFULL + 1, B_AFULL = B_PREADY + 2, B_AEMPTY, B_COUNT };
+enum { B_XFULL = 0, B_XEMPTY, B_FULL, B_EMPTY = B_FULL + kBwSlots, B_SFULL = B_EMPTY + kBwSlots, B_DPFULL,
+       B_PREADY, B_DSREADY = B_PREADY + 2, B_AFULL = B_DSREADY + 2, B_AEMPTY, B_STAT, B_COUNT = B_STAT + 2 };
 static_assert(B_COUNT * 8 + 4 <= 256, "backward barriers and the TMEM slot fit their 256 bytes");
 
 struct BwdParams {
@@ -556,9 +559,10 @@ template <bool KV>
 __global__ void __launch_bounds__(kBwThreads, 1)
     softmax_bwd_kernel(const __grid_constant__ CUtensorMap mx1, const __grid_constant__ CUtensorMap mx2,
                        const __grid_constant__ CUtensorMap my1, const __grid_constant__ CUtensorMap my2, BwdParams P) {
+  constexpr int kSlots = bw_slots<KV>();
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
-  uint64_t *bar = reinterpret_cast<uint64_t *>(smem + kBwOffBar);
+  uint64_t *bar = reinterpret_cast<uint64_t *>(smem + bw_off_bar<KV>());
   uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + B_COUNT);
   __shared__ int abort_flag;
   __shared__ int ring_item[kRingS];
@@ -571,13 +575,17 @@ __global__ void __launch_bounds__(kBwThreads, 1)
     abort_flag = 0;
     mbar_init(&bar[B_XFULL], 1);
     mbar_init(&bar[B_XEMPTY], 1);
-    for (int s = 0; s < kBwSlots; ++s) {
+    for (int s = 0; s < kSlots; ++s) {
       mbar_init(&bar[B_FULL + s], 1);
       mbar_init(&bar[B_EMPTY + s], 1);
     }
     mbar_init(&bar[B_SFULL], 1);
-    mbar_init(&bar[B_PREADY], 128);
-    mbar_init(&bar[B_PREADY + 1], 128);
+    mbar_init(&bar[B_DPFULL], 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&bar[B_PREADY + x], 128);
+      mbar_init(&bar[B_DSREADY + x], 128);
+      mbar_init(&bar[B_STAT + x], 128);
+    }
     mbar_init(&bar[B_AFULL], 1);
     mbar_init(&bar[B_AEMPTY], 256);
     for (int i = 0; i < kRingS; ++i) {
@@ -598,10 +606,14 @@ __global__ void __launch_bounds__(kBwThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
-  // TMEM: the two score tiles (X1 Y1^T, X2 Y2^T; their bf16 results in place), the accumulators
-  const uint32_t tS = tmem, tP = tmem + 128u, tA1 = tmem + 256u, tA2 = tmem + 384u;
+  // TMEM.  dK/dV: S^T (p in place as bf16), dP^T (ds in place), dV, dK.  dQ: two S buffers
+  // (the next tile's scores are formed while this tile's p are), dP (ds in place), dQ.
+  const uint32_t tP = tmem + (KV ? 128u : 256u), tA1 = tmem + (KV ? 256u : 384u), tA2 = tmem + 384u;
+  auto tS = [&](int u) { return tmem + (KV ? 0u : 128u * (uint32_t)(u & 1)); };
+  // dK/dV: the current step's column statistics (lse2, delta) per column half, two buffers
+  __shared__ float4 colstat[2][2][2][16];  // [step parity][half][lse2 | delta][16 x 4 columns]
   auto sX = [&](int x) { return smem_u32(smem) + (uint32_t)x * kTileBytes; };
-  auto slot_addr = [&](int i) { return smem_u32(smem + kBwOffY) + (uint32_t)(i % kBwSlots) * kTileBytes; };
+  auto slot_addr = [&](int i) { return smem_u32(smem + kBwOffY) + (uint32_t)(i % kSlots) * kTileBytes; };
   auto wait = [&](int idx, int parity) { return mbar_wait(&bar[idx], parity & 1, &abort_flag, P.status, detail); };
   auto take = [&](int k, int &item) {
     const int s = k % kRingS;
@@ -617,7 +629,7 @@ __global__ void __launch_bounds__(kBwThreads, 1)
       int li = 0, nx = 0;  // Y tiles and X tile pairs loaded
       bool ok = true;
       auto load = [&](const CUtensorMap *m, int row, int h, int b) {
-        const int s = li % kBwSlots, u = li / kBwSlots;
+        const int s = li % kSlots, u = li / kSlots;
         if (u > 0 && !(ok = wait(B_EMPTY + s, u - 1))) return;
         uint8_t *dst = smem + kBwOffY + s * kTileBytes;
         mbar_arrive_expect_tx(&bar[B_FULL + s], kTileBytes);
@@ -652,58 +664,83 @@ __global__ void __launch_bounds__(kBwThreads, 1)
       // time-bounded drain of the loads in flight (also after an abort)
       volatile int no_abort = 0;
       if (nx > 0) mbar_wait(&bar[B_XFULL], (nx - 1) & 1, &no_abort, P.status);
-      for (int s = 0; s < kBwSlots; ++s) {
-        const int uses = li > s ? (li - 1 - s) / kBwSlots + 1 : 0;
+      for (int s = 0; s < kSlots; ++s) {
+        const int uses = li > s ? (li - 1 - s) / kSlots + 1 : 0;
         if (uses > 0) mbar_wait(&bar[B_FULL + s], (uses - 1) & 1, &no_abort, P.status);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (the whole warp)
+    // Per step n (one Y tile pair):  dK/dV:  dP(n), dV(n), S(n+1), dK(n);  dQ:  dP(n), S(n+1),
+    // dQ(n).  The products of step n run while the elementwise warps form its p and ds, and
+    // the next tile's scores run while they form its ds; S(0) of an item opens its first step.
+    // The products read the bf16 p and ds from TMEM right where the elementwise warps
+    // wrote them, so every product that overwrites a score tile is issued after the one
+    // that reads it (the products of a CTA run in issue order).
     const uint32_t id_ss = idesc_bf16(128, 128, false, false);  // X Y^T
     const uint32_t id_ts = idesc_bf16(128, 128, false, true);   // (bf16 tile in TMEM) Y
     int li = 0, u = 0;
     bool ok = true;
     auto wait_all = [&](int idx, int parity) { return __all_sync(0xffffffffu, wait(idx, parity)); };
+    auto score = [&](uint32_t d, uint32_t x, uint32_t y) {
+#pragma unroll
+      for (uint32_t ks = 0; ks < 8; ++ks) mma_ss_warp(d, desc_kmajor(x, ks), desc_kmajor(y, ks), id_ss, ks > 0);
+    };
+    // the accumulation over the Y rows of one column half g (k-steps 4g .. 4g+3)
+    auto accum = [&](uint32_t d, uint32_t a, uint32_t y, int g, bool first) {
+#pragma unroll
+      for (uint32_t kk = 0; kk < 4; ++kk) {
+        const uint32_t ks = 4u * g + kk;
+        mma_ts_warp(d, a + 64u * g + 8u * kk, desc_mnmajor(y, ks), id_ts, (!first || ks > 0) ? 1u : 0u);
+      }
+    };
     for (int k = 0, item; ok; ++k) {
       if (!(ok = __all_sync(0xffffffffu, take(k, item))) || item < 0) break;
       int bh, xt, lo, ns;
       bw_item<KV>(P, item, bh, xt, lo, ns);
       if (!(ok = wait_all(B_XFULL, k))) break;
       for (int n = 0; n < ns && ok; ++n, ++u, li += 2) {
-        const int i1 = li, i2 = li + 1;
-        if (!(ok = wait_all(B_FULL + i1 % kBwSlots, i1 / kBwSlots) && wait_all(B_FULL + i2 % kBwSlots, i2 / kBwSlots)))
+        const int i1 = li, i2 = li + 1, i3 = li + 2;  // Y1, Y2 of this step, Y1 of the next
+        if (!(ok = wait_all(B_FULL + i1 % kSlots, i1 / kSlots) && wait_all(B_FULL + i2 % kSlots, i2 / kSlots)))
           break;
         tc_fence_after();
         const uint32_t Y1 = slot_addr(i1), Y2 = slot_addr(i2);
-        // the two score tiles (issued behind the previous step's accumulation, which
-        // reads the bf16 results these overwrite)
-#pragma unroll
-        for (uint32_t ks = 0; ks < 8; ++ks) mma_ss_warp(tS, desc_kmajor(sX(0), ks), desc_kmajor(Y1, ks), id_ss, ks > 0);
-#pragma unroll
-        for (uint32_t ks = 0; ks < 8; ++ks) mma_ss_warp(tP, desc_kmajor(sX(1), ks), desc_kmajor(Y2, ks), id_ss, ks > 0);
-        mma_commit_warp(&bar[B_SFULL]);
+        if (n == 0) {
+          score(tS(u), sX(0), Y1);
+          mma_commit_warp(&bar[B_SFULL]);
+        }
+        score(tP, sX(1), Y2);
+        mma_commit_warp(&bar[B_DPFULL]);
         if (n + 1 == ns) mma_commit_warp(&bar[B_XEMPTY]);
         // the accumulators are free once the previous item's epilogue has read them
         if (n == 0 && k > 0 && !(ok = wait_all(B_AEMPTY, k - 1))) break;
-        // accumulate over the Y rows (the contraction) one column half at a time, as
-        // soon as that half's bf16 results are in TMEM
-        for (int g = 0; g < 2 && ok; ++g) {
-          if (!(ok = wait_all(B_PREADY + g, u))) break;
-          tc_fence_after();
-#pragma unroll
-          for (uint32_t kk = 0; kk < 4; ++kk) {
-            const uint32_t ks = 4u * g + kk, col = 64u * g + 8u * kk, acc = (n > 0 || ks > 0) ? 1u : 0u;
-            if (KV) {
-              mma_ts_warp(tA1, tS + col, desc_mnmajor(Y2, ks), id_ts, acc);  // dV += P^T dO
-              mma_ts_warp(tA2, tP + col, desc_mnmajor(Y1, ks), id_ts, acc);  // dK += dS^T Q
-            } else {
-              mma_ts_warp(tA1, tP + col, desc_mnmajor(Y1, ks), id_ts, acc);  // dQ += dS K
-            }
+        if (KV) {
+          // dV += P^T dO, each column half as soon as its p are in TMEM
+          for (int g = 0; g < 2 && ok; ++g) {
+            if (!(ok = wait_all(B_PREADY + g, u))) break;
+            tc_fence_after();
+            accum(tA1, tS(u), Y2, g, n == 0);
           }
+          if (!ok) break;
+        }
+        if (n + 1 < ns) {
+          // the elementwise warps have read this step's scores (dK/dV: waited above) before
+          // the next ones complete: a barrier phase never runs two ahead of its waiters
+          if (!KV && !(ok = wait_all(B_PREADY, u) && wait_all(B_PREADY + 1, u))) break;
+          if (!(ok = wait_all(B_FULL + i3 % kSlots, i3 / kSlots))) break;
+          tc_fence_after();
+          score(tS(u + 1), sX(0), slot_addr(i3));
+          mma_commit_warp(&bar[B_SFULL]);
+        }
+        // dK += dS^T Q  or  dQ += dS K, each column half as soon as its ds are in TMEM
+        for (int g = 0; g < 2 && ok; ++g) {
+          if (!(ok = wait_all(B_DSREADY + g, u))) break;
+          tc_fence_after();
+          accum(KV ? tA2 : tA1, tP, Y1, g, n == 0);
         }
         if (!ok) break;
-        mma_commit_warp(&bar[B_EMPTY + i1 % kBwSlots]);
-        mma_commit_warp(&bar[B_EMPTY + i2 % kBwSlots]);
+        mma_commit_warp(&bar[B_EMPTY + i1 % kSlots]);
+        mma_commit_warp(&bar[B_EMPTY + i2 % kSlots]);
         if (n + 1 == ns) mma_commit_warp(&bar[B_AFULL]);
       }
     }
@@ -711,6 +748,7 @@ __global__ void __launch_bounds__(kBwThreads, 1)
     // ------------------------------------------------------------ p and ds for a column half, epilogue
     const int g = (warp - 2) >> 2;
     const uint32_t quad = warp & 3, row = quad * 32 + lane, lb = (quad * 32) << 16;
+    const int gt = threadIdx.x - 64 - 128 * g;  // 0..127 within the column half's warps
     int u = 0;
     bool ok = true;
     for (int k = 0, item; ok; ++k) {
@@ -722,54 +760,84 @@ __global__ void __launch_bounds__(kBwThreads, 1)
       const float lrow = KV ? 0.f : L2[128 * xt + row], drow = KV ? 0.f : DL[128 * xt + row];
       for (int n = 0; n < ns; ++n, ++u) {
         const int yt = lo + n;
-        if (!(ok = __all_sync(0xffffffffu, wait(B_SFULL, u)))) break;
+        float4 *cs = &colstat[u & 1][g][0][0];
+        if (KV) {
+          // this step's 64 column statistics of the half into shared memory: one value per
+          // thread, published through the half's mbarrier (a thread rewrites a buffer two
+          // steps later, after every thread of the half has arrived for the step between)
+          const int c = gt & 63, which = gt >> 6;
+          reinterpret_cast<float *>(cs)[64 * which + c] = (which ? DL : L2)[128 * yt + 64 * g + c];
+          mbar_arrive(&bar[B_STAT + g]);
+        }
+        if (!(ok = __all_sync(0xffffffffu, wait(B_SFULL, u) && (!KV || wait(B_STAT + g, u))))) break;
         tc_fence_after();
         // dK/dV: key 128 xt + row sees the query columns c >= lim;  dQ: query 128 xt + row
         // sees the key columns c <= lim
         const int lim = KV ? 128 * (xt - yt) + (int)row - P.off : P.off + 128 * (xt - yt) + (int)row;
+        // phase 1: p of the half's 64 columns (kept in registers; dK/dV: also into TMEM as bf16)
+        float p[64];
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           const int c0 = 64 * g + 32 * hh;
-          uint32_t sr[32], dr[32];
-          tmem_ld32(tS + lb + c0, sr);
-          tmem_ld32(tP + lb + c0, dr);
+          uint32_t sr[32];
+          tmem_ld32(tS(u) + lb + c0, sr);
           tmem_ld_wait();
-          uint32_t wp[16], wd[16];
 #pragma unroll
           for (int j4 = 0; j4 < 8; ++j4) {
-            float lv[4], dl[4];
+            float lv[4];
             if (KV) {
-              const float4 l4 = *reinterpret_cast<const float4 *>(L2 + 128 * yt + c0 + 4 * j4);
-              const float4 d4 = *reinterpret_cast<const float4 *>(DL + 128 * yt + c0 + 4 * j4);
+              const float4 l4 = cs[8 * hh + j4];
               lv[0] = l4.x; lv[1] = l4.y; lv[2] = l4.z; lv[3] = l4.w;
-              dl[0] = d4.x; dl[1] = d4.y; dl[2] = d4.z; dl[3] = d4.w;
             } else {
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                lv[e] = lrow;
-                dl[e] = drow;
-              }
+              lv[0] = lv[1] = lv[2] = lv[3] = lrow;
             }
-            float pe[4], de[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int j = 4 * j4 + e, c = c0 + j;
-              float p = ex2(fmaf(__uint_as_float(sr[j]), P.scale_log2, -lv[e]));
-              if (KV ? c < lim : c > lim) p = 0.f;
-              pe[e] = p;
-              de[e] = p * (__uint_as_float(dr[j]) - dl[e]);
+              const float x = ex2(fmaf(__uint_as_float(sr[j]), P.scale_log2, -lv[e]));
+              p[32 * hh + j] = (KV ? c < lim : c > lim) ? 0.f : x;
             }
-            wp[2 * j4] = pack_bf16(pe[0], pe[1]);
-            wp[2 * j4 + 1] = pack_bf16(pe[2], pe[3]);
-            wd[2 * j4] = pack_bf16(de[0], de[1]);
-            wd[2 * j4 + 1] = pack_bf16(de[2], de[3]);
           }
-          if (KV) tmem_st16(tS + lb + 64 * g + 16 * hh, wp);
+          if (KV) {
+            uint32_t wp[16];
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) wp[jj] = pack_bf16(p[32 * hh + 2 * jj], p[32 * hh + 2 * jj + 1]);
+            tmem_st16(tS(u) + lb + 64 * g + 16 * hh, wp);
+          }
+        }
+        // dK/dV: p is in TMEM for the dV product; dQ: the scores have been read
+        if (KV) tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bar[B_PREADY + g]);
+        // phase 2: ds = p (dp - delta) into the dP tile as bf16
+        if (!(ok = __all_sync(0xffffffffu, wait(B_DPFULL, u)))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int c0 = 64 * g + 32 * hh;
+          uint32_t dr[32], wd[16];
+          tmem_ld32(tP + lb + c0, dr);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j4 = 0; j4 < 8; ++j4) {
+            float dl[4];
+            if (KV) {
+              const float4 d4 = cs[16 + 8 * hh + j4];
+              dl[0] = d4.x; dl[1] = d4.y; dl[2] = d4.z; dl[3] = d4.w;
+            } else {
+              dl[0] = dl[1] = dl[2] = dl[3] = drow;
+            }
+            const int j = 4 * j4;
+            wd[2 * j4] = pack_bf16(p[32 * hh + j] * (__uint_as_float(dr[j]) - dl[0]),
+                                   p[32 * hh + j + 1] * (__uint_as_float(dr[j + 1]) - dl[1]));
+            wd[2 * j4 + 1] = pack_bf16(p[32 * hh + j + 2] * (__uint_as_float(dr[j + 2]) - dl[2]),
+                                       p[32 * hh + j + 3] * (__uint_as_float(dr[j + 3]) - dl[3]));
+          }
           tmem_st16(tP + lb + 64 * g + 16 * hh, wd);
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&bar[B_PREADY + g]);
+        mbar_arrive(&bar[B_DSREADY + g]);
       }
       if (!ok) break;
       // epilogue: dK/dV: the first half stores the dv row, the second the dk row (times the
@@ -942,11 +1010,11 @@ cudaError_t softmax_segment_bwd(const SoftmaxProblem &p, const void *q, const vo
     K.wide = a32(dk) && a32(dv) && (p.ksb * 2) % 32 == 0 && (p.ksh * 2) % 32 == 0 && (p.kst * 2) % 32 == 0;
     K.counter = status + kCounterSoftmaxKV;
     if ((e = cudaFuncSetAttribute(softmax_bwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)kBwSmem)) != cudaSuccess)
+                                  (int)bw_smem<true>())) != cudaSuccess)
       return e;
     TimedLaunch t(K_SOFTMAX_BWD_KV, s);
-    softmax_bwd_kernel<true><<<K.nitems < p.num_sms ? K.nitems : p.num_sms, kBwThreads, kBwSmem, s>>>(mk, mv, mq, mdo,
-                                                                                                      K);
+    softmax_bwd_kernel<true><<<K.nitems < p.num_sms ? K.nitems : p.num_sms, kBwThreads, bw_smem<true>(), s>>>(
+        mk, mv, mq, mdo, K);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   // dQ: items over the query tiles
@@ -958,11 +1026,11 @@ cudaError_t softmax_segment_bwd(const SoftmaxProblem &p, const void *q, const vo
   Q.wide = a32(dq) && (p.qsb * 2) % 32 == 0 && (p.qsh * 2) % 32 == 0 && (p.qst * 2) % 32 == 0;
   Q.counter = status + kCounterSoftmaxQ;
   if ((e = cudaFuncSetAttribute(softmax_bwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)kBwSmem)) != cudaSuccess)
+                                (int)bw_smem<false>())) != cudaSuccess)
     return e;
   TimedLaunch t(K_SOFTMAX_BWD_Q, s);
-  softmax_bwd_kernel<false><<<Q.nitems < p.num_sms ? Q.nitems : p.num_sms, kBwThreads, kBwSmem, s>>>(mq, mdo, mk, mv,
-                                                                                                     Q);
+  softmax_bwd_kernel<false><<<Q.nitems < p.num_sms ? Q.nitems : p.num_sms, kBwThreads, bw_smem<false>(), s>>>(
+      mq, mdo, mk, mv, Q);
   return cudaGetLastError();
 }
 

@@ -69,6 +69,12 @@ def test_softmax_segment_bwd_matches_oracle(B, H, Tq, Tk):
     check(*case(Tq * 7 + Tk + 1, B, H, Tq, Tk))
 
 
+def test_softmax_segment_bwd_several_items_per_cta():
+    """More items than SMs in both launches (2 x 40 sequences of 2 query and 4 key tiles),
+    so CTAs go from one item's last step to the next item's first."""
+    check(*case(21, 2, 40, 256, 512))
+
+
 def test_softmax_segment_bwd_large_scores():
     """Scores of a few tens: sharp rows, p close to one on a few keys."""
     check(*case(3, 1, 2, 256, 700, sigma=2.5))

@@ -774,66 +774,80 @@ __global__ void __launch_bounds__(kBwThreads, 1)
         // dK/dV: key 128 xt + row sees the query columns c >= lim;  dQ: query 128 xt + row
         // sees the key columns c <= lim
         const int lim = KV ? 128 * (xt - yt) + (int)row - P.off : P.off + 128 * (xt - yt) + (int)row;
+        // every row of the warp sees every column of the half: no masks
+        const bool full = __all_sync(0xffffffffu, KV ? lim <= 64 * g : lim >= 64 * g + 63);
+        // dQ: the scores are double-buffered, so the next ones may be formed as soon as this
+        // step's have been waited for (the barrier phases stay within one of each other)
+        if (!KV) mbar_arrive(&bar[B_PREADY + g]);
         // phase 1: p of the half's 64 columns (kept in registers; dK/dV: also into TMEM as bf16)
         float p[64];
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int c0 = 64 * g + 32 * hh;
-          uint32_t sr[32];
-          tmem_ld32(tS(u) + lb + c0, sr);
+        {
+          uint32_t sr[2][32];
+          tmem_ld32(tS(u) + lb + 64 * g, sr[0]);
+          tmem_ld32(tS(u) + lb + 64 * g + 32, sr[1]);
           tmem_ld_wait();
 #pragma unroll
-          for (int j4 = 0; j4 < 8; ++j4) {
+          for (int j4 = 0; j4 < 16; ++j4) {
             float lv[4];
             if (KV) {
-              const float4 l4 = cs[8 * hh + j4];
+              const float4 l4 = cs[j4];
               lv[0] = l4.x; lv[1] = l4.y; lv[2] = l4.z; lv[3] = l4.w;
             } else {
               lv[0] = lv[1] = lv[2] = lv[3] = lrow;
             }
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const int j = 4 * j4 + e, c = c0 + j;
-              const float x = ex2(fmaf(__uint_as_float(sr[j]), P.scale_log2, -lv[e]));
-              p[32 * hh + j] = (KV ? c < lim : c > lim) ? 0.f : x;
+              const int j = 4 * j4 + e;
+              p[j] = ex2(fmaf(__uint_as_float(sr[j >> 5][j & 31]), P.scale_log2, -lv[e]));
             }
           }
-          if (KV) {
+          if (!full) {
+#pragma unroll
+            for (int j = 0; j < 64; ++j)
+              if (KV ? 64 * g + j < lim : 64 * g + j > lim) p[j] = 0.f;
+          }
+        }
+        if (KV) {
+          // p into TMEM for the dV product
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
             uint32_t wp[16];
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) wp[jj] = pack_bf16(p[32 * hh + 2 * jj], p[32 * hh + 2 * jj + 1]);
             tmem_st16(tS(u) + lb + 64 * g + 16 * hh, wp);
           }
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(&bar[B_PREADY + g]);
         }
-        // dK/dV: p is in TMEM for the dV product; dQ: the scores have been read
-        if (KV) tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(&bar[B_PREADY + g]);
         // phase 2: ds = p (dp - delta) into the dP tile as bf16
         if (!(ok = __all_sync(0xffffffffu, wait(B_DPFULL, u)))) break;
         tc_fence_after();
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int c0 = 64 * g + 32 * hh;
-          uint32_t dr[32], wd[16];
-          tmem_ld32(tP + lb + c0, dr);
+        {
+          uint32_t dr[2][32];
+          tmem_ld32(tP + lb + 64 * g, dr[0]);
+          tmem_ld32(tP + lb + 64 * g + 32, dr[1]);
           tmem_ld_wait();
 #pragma unroll
-          for (int j4 = 0; j4 < 8; ++j4) {
-            float dl[4];
-            if (KV) {
-              const float4 d4 = cs[16 + 8 * hh + j4];
-              dl[0] = d4.x; dl[1] = d4.y; dl[2] = d4.z; dl[3] = d4.w;
-            } else {
-              dl[0] = dl[1] = dl[2] = dl[3] = drow;
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t wd[16];
+#pragma unroll
+            for (int j4 = 0; j4 < 8; ++j4) {
+              float dl[4];
+              if (KV) {
+                const float4 d4 = cs[16 + 8 * hh + j4];
+                dl[0] = d4.x; dl[1] = d4.y; dl[2] = d4.z; dl[3] = d4.w;
+              } else {
+                dl[0] = dl[1] = dl[2] = dl[3] = drow;
+              }
+              const int j = 4 * j4;
+              wd[2 * j4] = pack_bf16(p[32 * hh + j] * (__uint_as_float(dr[hh][j]) - dl[0]),
+                                     p[32 * hh + j + 1] * (__uint_as_float(dr[hh][j + 1]) - dl[1]));
+              wd[2 * j4 + 1] = pack_bf16(p[32 * hh + j + 2] * (__uint_as_float(dr[hh][j + 2]) - dl[2]),
+                                         p[32 * hh + j + 3] * (__uint_as_float(dr[hh][j + 3]) - dl[3]));
             }
-            const int j = 4 * j4;
-            wd[2 * j4] = pack_bf16(p[32 * hh + j] * (__uint_as_float(dr[j]) - dl[0]),
-                                   p[32 * hh + j + 1] * (__uint_as_float(dr[j + 1]) - dl[1]));
-            wd[2 * j4 + 1] = pack_bf16(p[32 * hh + j + 2] * (__uint_as_float(dr[j + 2]) - dl[2]),
-                                       p[32 * hh + j + 3] * (__uint_as_float(dr[j + 3]) - dl[3]));
+            tmem_st16(tP + lb + 64 * g + 16 * hh, wd);
           }
-          tmem_st16(tP + lb + 64 * g + 16 * hh, wd);
         }
         tmem_st_wait();
         tc_fence_before();

@@ -60,27 +60,45 @@ def softmax_segment_fwd(q, k, v, scale=None, rows=None):
     return o, lse
 
 
-def softmax_segment_bwd(q, k, v, dO, scale=None):
+def softmax_segment_bwd(q, k, v, dO, scale=None, rows=None, first_key=None):
     """(dq [B,H,Tq,d], dk [B,H,Tk,d], dv [B,H,Tk,dv]) in float64: the gradients of
-    <o, dO> for o = softmax_segment_fwd(q, k, v, scale)[0]; Tk >= Tq."""
+    <o, dO> for o = softmax_segment_fwd(q, k, v, scale)[0]; Tk >= Tq.
+
+    Sampling for long inputs: ``rows`` (a list of query indices) computes dq for those
+    rows only; ``first_key`` computes dk, dv for the keys first_key .. Tk-1 only (only the
+    queries that see one of them are visited, each over its whole key prefix).  The other
+    entries are NaN; with either argument, only the requested outputs are formed."""
     q, k, v, dO = (np.asarray(x, dtype=np.float64) for x in (q, k, v, dO))
     B, H, Tq, d = q.shape
     Tk = k.shape[2]
     assert k.shape[:2] == (B, H) and v.shape[:3] == (B, H, Tk) and Tk >= Tq and dO.shape == (B, H, Tq, v.shape[3])
     off = Tk - Tq
     sc = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    dq = np.zeros_like(q)
-    dk = np.zeros_like(k)
-    dv = np.zeros_like(v)
-    for i in range(Tq):
+    sampled = rows is not None or first_key is not None
+    dq = np.full_like(q, np.nan) if sampled else np.zeros_like(q)
+    dk = np.full_like(k, np.nan) if sampled else np.zeros_like(k)
+    dv = np.full_like(v, np.nan) if sampled else np.zeros_like(v)
+    if first_key is not None:
+        dk[:, :, first_key:] = 0.0
+        dv[:, :, first_key:] = 0.0
+    if sampled:
+        # query i sees key first_key once off + i >= first_key
+        visit = set(rows or []) | (set(range(max(0, first_key - off), Tq)) if first_key is not None else set())
+        row_list = sorted(visit)
+    else:
+        row_list = range(Tq)
+    for i in row_list:
         n = off + i + 1                                         # keys 0 .. off + i
         s = sc * np.einsum("bhjd,bhd->bhj", k[:, :, :n], q[:, :, i])
         p = np.exp(s - s.max(axis=2, keepdims=True))
         p /= p.sum(axis=2, keepdims=True)                       # the row's softmax weights
-        dv[:, :, :n] += p[..., None] * dO[:, :, i, None, :]
         dp = np.einsum("bhje,bhe->bhj", v[:, :, :n], dO[:, :, i])
         delta = np.sum(p * dp, axis=2, keepdims=True)
         ds = p * (dp - delta)
-        dq[:, :, i] = sc * np.einsum("bhj,bhjd->bhd", ds, k[:, :, :n])
-        dk[:, :, :n] += sc * ds[..., None] * q[:, :, i, None, :]
+        if not sampled or (rows is not None and i in rows):
+            dq[:, :, i] = sc * np.einsum("bhj,bhjd->bhd", ds, k[:, :, :n])
+        lo = 0 if not sampled else (first_key if first_key is not None else n)
+        if lo < n:
+            dv[:, :, lo:n] += p[:, :, lo:, None] * dO[:, :, i, None, :]
+            dk[:, :, lo:n] += sc * ds[:, :, lo:, None] * q[:, :, i, None, :]
     return dq, dk, dv

@@ -114,3 +114,22 @@ def test_softmax_segment_bwd_empty_queries():
     la.softmax_segment_bwd(q, k, k, q, q, lse, outs=(q.clone(), dk, dv))
     torch.cuda.synchronize()
     assert torch.count_nonzero(dk) == 0 and torch.count_nonzero(dv) == 0
+
+
+def test_softmax_segment_bwd_full_size_sampled():
+    """The benchmark's shape (B1 H16, Tq 16384 over Tk 65536), in the launch configuration
+    the bench times: dq of rows spread over the segment and dk, dv of the prefix's last 64
+    keys (seen by the last 64 queries only), on the first and last head, against the
+    oracle; every other output finite and the status clean."""
+    B, H, Tq, Tk = 1, 16, 16384, 65536
+    q, k, v, dO = case(77, B, H, Tq, Tk)
+    dq, dk, dv = run(q, k, v, dO)
+    assert all(bool(torch.isfinite(x).all()) for x in (dq, dk, dv))
+    rows = [0, 1, 127, 128, 5000, 8191, 16383]
+    heads = [0, H - 1]
+    n = lambda x: x[:, heads].double().numpy()
+    rq, rk, rv = oracle.softmax_segment_bwd(n(q), n(k), n(v), n(dO), rows=rows, first_key=Tk - 64)
+    got_q, got_k, got_v = (x[:, heads].double().cpu().numpy() for x in (dq, dk, dv))
+    for name, got, ref in (("dq", got_q[:, :, rows], rq[:, :, rows]), ("dk", got_k[:, :, -64:], rk[:, :, -64:]),
+                           ("dv", got_v[:, :, -64:], rv[:, :, -64:])):
+        assert rel(got, ref) < 1e-2, (name, rel(got, ref))

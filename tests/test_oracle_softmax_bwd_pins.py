@@ -74,3 +74,17 @@ def test_softmax_identities():
     o, lse = oracle.softmax_segment_fwd(q, k, v)
     p0 = np.exp(np.einsum("bhid,bhd->bhi", q, k[:, :, 0]) / math.sqrt(d) - lse)
     np.testing.assert_allclose(dv[:, :, 0], np.einsum("bhi,bhie->bhe", p0, dO), rtol=1e-12, atol=1e-12)
+
+
+def test_sampled_rows_and_last_keys_equal_the_full_computation():
+    """The sampling arguments (dq of chosen rows; dk, dv of the last keys) give the same
+    entries as the full computation, whose pins are above."""
+    B, H, Tq, Tk, d = 1, 2, 30, 80, 8
+    q, k, v, dO = _rand(8, B, H, Tq, Tk, d)
+    fq, fk, fv = oracle.softmax_segment_bwd(q, k, v, dO)
+    rows = [0, 7, 29]
+    sq, sk, sv = oracle.softmax_segment_bwd(q, k, v, dO, rows=rows, first_key=70)
+    np.testing.assert_allclose(sq[:, :, rows], fq[:, :, rows], rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(sk[:, :, 70:], fk[:, :, 70:], rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(sv[:, :, 70:], fv[:, :, 70:], rtol=1e-13, atol=1e-14)
+    assert np.isnan(sq[:, :, 1]).all() and np.isnan(sk[:, :, 69]).all()

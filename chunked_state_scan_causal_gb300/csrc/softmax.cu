@@ -890,6 +890,303 @@ __global__ void __launch_bounds__(kBwThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
+// dQ with two adjacent query tiles per CTA (A, B): each K and V tile serves both, and
+// while one tile's p or ds are formed the other tile's products run.  Per tile one
+// TMEM region holds S, then dP once p is in registers, then ds as bf16 (the A
+// operand of dQ += dS K), and a dQ accumulator (4 x 128 columns).  Per key tile t:
+//   S_x(t) -> p (elementwise) -> dP_x(t) -> ds -> dQ_x(t) -> S_x(t+1) ...
+// issued as dP_A, dP_B, dQ_A, S_A(t+1), dQ_B, S_B(t+1).  Shared memory: the item's
+// Q and dO tiles of A and B, K tiles alternating between two slots, V tiles in a third.
+constexpr uint32_t kQ2OffY = 4 * kTileBytes;
+constexpr uint32_t kQ2OffBar = kQ2OffY + 3 * kTileBytes;
+constexpr size_t kQ2Smem = kQ2OffBar + 256 + 1024;
+static_assert(kQ2Smem + 128 <= 232448, "tiles, barriers and static shared memory fit 227 KB");
+enum { Q2_XFULL = 0, Q2_XEMPTY, Q2_FULL, Q2_EMPTY = Q2_FULL + 3, Q2_SFULL = Q2_EMPTY + 3, Q2_SREAD = Q2_SFULL + 2,
+       Q2_DPFULL = Q2_SREAD + 2, Q2_DSREADY = Q2_DPFULL + 2, Q2_AFULL = Q2_DSREADY + 2, Q2_AEMPTY = Q2_AFULL + 2,
+       Q2_COUNT = Q2_AEMPTY + 2 };
+static_assert(Q2_COUNT * 8 + 4 <= 256, "dQ barriers and the TMEM slot fit their 256 bytes");
+
+// item -> (sequence, first query tile of the pair, key tiles up to the second tile's
+// diagonal), sequence-major and longest first inside a sequence (as the forward)
+__device__ __forceinline__ void q2_item(const BwdParams &P, int item, int &bh, int &qt, int &nt) {
+  const int npair = (P.nqt + 1) / 2;
+  qt = 2 * (npair - 1 - item % npair);
+  bh = item / npair;
+  nt = (min(P.Tk, P.off + 128 * qt + 256) + 127) / 128;
+}
+
+__global__ void __launch_bounds__(kBwThreads, 1)
+    softmax_bwd_dq2_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mdo,
+                           const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
+                           BwdParams P) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = align1024(smem_raw);
+  uint64_t *bar = reinterpret_cast<uint64_t *>(smem + kQ2OffBar);
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + Q2_COUNT);
+  __shared__ int abort_flag;
+  __shared__ int ring_item[kRingS];
+  __shared__ uint64_t ring_bar[2 * kRingS];
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  int *const detail = P.status ? P.status + 1 + warp : nullptr;
+  uint64_t *ring_full = ring_bar, *ring_empty = ring_bar + kRingS;
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bar[Q2_XFULL], 1);
+    mbar_init(&bar[Q2_XEMPTY], 1);
+    for (int s = 0; s < 3; ++s) {
+      mbar_init(&bar[Q2_FULL + s], 1);
+      mbar_init(&bar[Q2_EMPTY + s], 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&bar[Q2_SFULL + x], 1);
+      mbar_init(&bar[Q2_SREAD + x], 128);
+      mbar_init(&bar[Q2_DPFULL + x], 1);
+      mbar_init(&bar[Q2_DSREADY + x], 128);
+      mbar_init(&bar[Q2_AFULL + x], 1);
+      mbar_init(&bar[Q2_AEMPTY + x], 128);
+    }
+    for (int i = 0; i < kRingS; ++i) {
+      mbar_init(&ring_full[i], 1);
+      mbar_init(&ring_empty[i], 32 + 256);  // readers: the MMA warp, the eight elementwise warps
+    }
+    fence_mbar_init();
+    prefetch_tensormap(&mq);
+    prefetch_tensormap(&mdo);
+    prefetch_tensormap(&mk);
+    prefetch_tensormap(&mv);
+  }
+  if (warp == 1) {
+    tmem_alloc(tslot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  auto tR = [&](int x) { return tmem + 128u * (uint32_t)x; };         // S / dP / ds of tile x
+  auto tQ = [&](int x) { return tmem + 256u + 128u * (uint32_t)x; };  // dQ of tile x
+  // smem: Q_A, dO_A, Q_B, dO_B, then the K slots 0, 1 and the V slot 2
+  auto sXq = [&](int x) { return smem_u32(smem) + (uint32_t)(2 * x) * kTileBytes; };
+  auto sXo = [&](int x) { return smem_u32(smem) + (uint32_t)(2 * x + 1) * kTileBytes; };
+  auto sY = [&](int slot) { return smem_u32(smem + kQ2OffY) + (uint32_t)slot * kTileBytes; };
+  auto wait = [&](int idx, int parity) { return mbar_wait(&bar[idx], parity & 1, &abort_flag, P.status, detail); };
+  auto take = [&](int k, int &item) {
+    const int s = k % kRingS;
+    if (!mbar_wait(&ring_full[s], (k / kRingS) & 1, &abort_flag, P.status, detail)) return false;
+    item = *reinterpret_cast<volatile int *>(&ring_item[s]);
+    mbar_arrive(&ring_empty[s]);
+    return true;
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int nk = 0, nv = 0, nx = 0;  // K tiles, V tiles and X tile sets loaded
+      bool ok = true;
+      for (int k = 0;; ++k) {
+        const int s = k % kRingS;
+        if (k >= kRingS && !(ok = mbar_wait(&ring_empty[s], (k / kRingS - 1) & 1, &abort_flag, P.status, detail)))
+          break;
+        const int x = atomicAdd(P.counter, 1), item = x < P.nitems ? x : -1;
+        *reinterpret_cast<volatile int *>(&ring_item[s]) = item;
+        mbar_arrive(&ring_full[s]);
+        if (item < 0) break;
+        int bh, qt, nt;
+        q2_item(P, item, bh, qt, nt);
+        const int b = bh / P.H, h = bh % P.H;
+        if (k > 0 && !(ok = wait(Q2_XEMPTY, k - 1))) break;  // the previous item's products read X
+        mbar_arrive_expect_tx(&bar[Q2_XFULL], 4 * kTileBytes);
+        for (int x = 0; x < 2; ++x) {
+          uint8_t *dq = smem + (2 * x) * kTileBytes, *dd = smem + (2 * x + 1) * kTileBytes;
+          tma_load_4d(&mq, &bar[Q2_XFULL], dq, 0, 128 * (qt + x), h, b, kPolicyEvictFirst);
+          tma_load_4d(&mq, &bar[Q2_XFULL], dq + kTileHalfBytes, 64, 128 * (qt + x), h, b, kPolicyEvictFirst);
+          tma_load_4d(&mdo, &bar[Q2_XFULL], dd, 0, 128 * (qt + x), h, b, kPolicyEvictFirst);
+          tma_load_4d(&mdo, &bar[Q2_XFULL], dd + kTileHalfBytes, 64, 128 * (qt + x), h, b, kPolicyEvictFirst);
+        }
+        ++nx;
+        for (int t = 0; t < nt && ok; ++t) {
+          // K(t) into slot nk & 1 (its previous K released after that step's dQ products),
+          // V(t) into slot 2 (the previous V released after that step's dP products)
+          const int ks = nk & 1;
+          if (nk >= 2 && !(ok = wait(Q2_EMPTY + ks, (nk >> 1) - 1))) break;
+          mbar_arrive_expect_tx(&bar[Q2_FULL + ks], kTileBytes);
+          uint8_t *dk = smem + kQ2OffY + ks * kTileBytes;
+          tma_load_4d(&mk, &bar[Q2_FULL + ks], dk, 0, 128 * t, h, b, kPolicyEvictLast);
+          tma_load_4d(&mk, &bar[Q2_FULL + ks], dk + kTileHalfBytes, 64, 128 * t, h, b, kPolicyEvictLast);
+          ++nk;
+          if (nv >= 1 && !(ok = wait(Q2_EMPTY + 2, nv - 1))) break;
+          mbar_arrive_expect_tx(&bar[Q2_FULL + 2], kTileBytes);
+          uint8_t *dv = smem + kQ2OffY + 2 * kTileBytes;
+          tma_load_4d(&mv, &bar[Q2_FULL + 2], dv, 0, 128 * t, h, b, kPolicyEvictLast);
+          tma_load_4d(&mv, &bar[Q2_FULL + 2], dv + kTileHalfBytes, 64, 128 * t, h, b, kPolicyEvictLast);
+          ++nv;
+        }
+        if (!ok) break;
+      }
+      // time-bounded drain of the loads in flight (also after an abort)
+      volatile int no_abort = 0;
+      if (nx > 0) mbar_wait(&bar[Q2_XFULL], (nx - 1) & 1, &no_abort, P.status);
+      for (int s = 0; s < 2; ++s) {
+        const int uses = nk > s ? (nk - 1 - s) / 2 + 1 : 0;
+        if (uses > 0) mbar_wait(&bar[Q2_FULL + s], (uses - 1) & 1, &no_abort, P.status);
+      }
+      if (nv > 0) mbar_wait(&bar[Q2_FULL + 2], (nv - 1) & 1, &no_abort, P.status);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (the whole warp)
+    const uint32_t id_ss = idesc_bf16(128, 128, false, false);  // X Y^T
+    const uint32_t id_ts = idesc_bf16(128, 128, false, true);   // (ds in TMEM) K
+    int nk = 0, nv = 0, u = 0;
+    bool ok = true;
+    auto wait_all = [&](int idx, int parity) { return __all_sync(0xffffffffu, wait(idx, parity)); };
+    auto score = [&](uint32_t d, uint32_t x, uint32_t y) {
+#pragma unroll
+      for (uint32_t ks = 0; ks < 8; ++ks) mma_ss_warp(d, desc_kmajor(x, ks), desc_kmajor(y, ks), id_ss, ks > 0);
+    };
+    auto dq = [&](int x, uint32_t K, bool first) {
+#pragma unroll
+      for (uint32_t ks = 0; ks < 8; ++ks)
+        mma_ts_warp(tQ(x), tR(x) + 8u * ks, desc_mnmajor(K, ks), id_ts, (!first || ks > 0) ? 1u : 0u);
+    };
+    for (int k = 0, item; ok; ++k) {
+      if (!(ok = __all_sync(0xffffffffu, take(k, item))) || item < 0) break;
+      int bh, qt, nt;
+      q2_item(P, item, bh, qt, nt);
+      if (!(ok = wait_all(Q2_XFULL, k) && wait_all(Q2_FULL + (nk & 1), nk >> 1))) break;
+      tc_fence_after();
+      // the item's first scores
+      for (int x = 0; x < 2; ++x) {
+        score(tR(x), sXq(x), sY(nk & 1));
+        mma_commit_warp(&bar[Q2_SFULL + x]);
+      }
+      for (int t = 0; t < nt && ok; ++t, ++u, ++nk, ++nv) {
+        const uint32_t K = sY(nk & 1), V = sY(2);
+        if (!(ok = wait_all(Q2_FULL + 2, nv))) break;
+        // dP of both tiles once their p are in registers (the region is then free)
+        for (int x = 0; x < 2 && ok; ++x) {
+          if (!(ok = wait_all(Q2_SREAD + x, u))) break;
+          tc_fence_after();
+          score(tR(x), sXo(x), V);
+          mma_commit_warp(&bar[Q2_DPFULL + x]);
+        }
+        if (!ok) break;
+        mma_commit_warp(&bar[Q2_EMPTY + 2]);
+        if (t + 1 == nt) mma_commit_warp(&bar[Q2_XEMPTY]);
+        if (t == 0 && k > 0 && !(ok = wait_all(Q2_AEMPTY, k - 1) && wait_all(Q2_AEMPTY + 1, k - 1))) break;
+        // dQ of each tile once its ds are in TMEM, then that tile's next scores
+        const bool more = t + 1 < nt;
+        if (more && !(ok = wait_all(Q2_FULL + ((nk + 1) & 1), (nk + 1) >> 1))) break;
+        for (int x = 0; x < 2 && ok; ++x) {
+          if (!(ok = wait_all(Q2_DSREADY + x, u))) break;
+          tc_fence_after();
+          dq(x, K, t == 0);
+          if (x == 1) mma_commit_warp(&bar[Q2_EMPTY + (nk & 1)]);
+          if (t + 1 == nt) mma_commit_warp(&bar[Q2_AFULL + x]);
+          if (more) {
+            score(tR(x), sXq(x), sY((nk + 1) & 1));
+            mma_commit_warp(&bar[Q2_SFULL + x]);
+          }
+        }
+      }
+    }
+  } else if (warp >= 2 && warp < 10) {
+    // ------------------------------------------------------------ p, ds and the dq rows of tile x
+    const int x = (warp - 2) >> 2;
+    const uint32_t quad = warp & 3, row = quad * 32 + lane, lb = (quad * 32) << 16;
+    int u = 0;
+    bool ok = true;
+    for (int k = 0, item; ok; ++k) {
+      if (!(ok = __all_sync(0xffffffffu, take(k, item))) || item < 0) break;
+      int bh, qt, nt;
+      q2_item(P, item, bh, qt, nt);
+      const int qtile = qt + x, i = 128 * qtile + (int)row;
+      // this row's statistics (a second tile past the end has none: p = 0)
+      const bool in = qtile < P.nqt;
+      const float lrow = in ? P.lse2[(int64_t)bh * P.nqt * 128 + i] : INFINITY;
+      const float drow = in ? P.delta[(int64_t)bh * P.nqt * 128 + i] : 0.f;
+      for (int t = 0; t < nt; ++t, ++u) {
+        if (!(ok = __all_sync(0xffffffffu, wait(Q2_SFULL + x, u)))) break;
+        tc_fence_after();
+        // key column c of this tile is visible to the row when c <= lim
+        const int lim = P.off + i - 128 * t;
+        const bool full = __all_sync(0xffffffffu, lim >= 127);
+        // p as bf16 pairs (the registers of a thread hold at most 168 values here)
+        uint32_t pw[64];
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          uint32_t sr[2][32];
+          tmem_ld32(tR(x) + lb + 64 * cc, sr[0]);
+          tmem_ld32(tR(x) + lb + 64 * cc + 32, sr[1]);
+          tmem_ld_wait();
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) {
+            const int j = 64 * cc + 2 * jj;
+            float p0 = ex2(fmaf(__uint_as_float(sr[jj >> 4][(2 * jj) & 31]), P.scale_log2, -lrow));
+            float p1 = ex2(fmaf(__uint_as_float(sr[jj >> 4][(2 * jj + 1) & 31]), P.scale_log2, -lrow));
+            if (!full) {
+              p0 = j > lim ? 0.f : p0;
+              p1 = j + 1 > lim ? 0.f : p1;
+            }
+            pw[32 * cc + jj] = pack_bf16(p0, p1);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&bar[Q2_SREAD + x]);  // the scores are in registers: dP may overwrite them
+        if (!(ok = __all_sync(0xffffffffu, wait(Q2_DPFULL + x, u)))) break;
+        tc_fence_after();
+        // ds = p (dp - delta), chunk by chunk into the region's first 64 columns (chunk c's
+        // bf16 pairs overwrite dp columns that earlier chunks have already read)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t dr[32], wd[16];
+          tmem_ld32(tR(x) + lb + 32 * c, dr);
+          tmem_ld_wait();
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) {
+            const uint32_t pp = pw[16 * c + jj];
+            wd[jj] = pack_bf16(bf16lo(pp) * (__uint_as_float(dr[2 * jj]) - drow),
+                               bf16hi(pp) * (__uint_as_float(dr[2 * jj + 1]) - drow));
+          }
+          tmem_st16(tR(x) + lb + 16 * c, wd);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bar[Q2_DSREADY + x]);
+      }
+      if (!ok) break;
+      // the dq row (times the scale)
+      if (!(ok = __all_sync(0xffffffffu, wait(Q2_AFULL + x, k)))) break;
+      tc_fence_after();
+      const int b = bh / P.H, h = bh % P.H;
+      const bool valid = i < P.Tq;
+      __nv_bfloat16 *dst = P.out1 + (int64_t)b * P.osb + (int64_t)h * P.osh + (int64_t)i * P.ost;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        float y[32];
+        uint32_t o[32];
+        tmem_ld32(tQ(x) + lb + 32 * c, o);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) y[j] = __uint_as_float(o[j]) * P.scale;
+        if (valid) st_row_chunk(dst + 32 * c, y, P.wide != 0);
+      }
+      tc_fence_before();
+      mbar_arrive(&bar[Q2_AEMPTY + x]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(P.counter + 1, 1) == (int)gridDim.x - 1) {
+      atomicExch(P.counter, 0);
+      atomicExch(P.counter + 1, 0);
+    }
+  }
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
 // The per-query statistics of the backward, one warp per padded query row:
 // lse2 = lse log2(e) and delta = dO . o (fp32 from the bf16 rows); past Tq +inf and 0.
 __global__ void __launch_bounds__(256) softmax_bwd_prep_kernel(const __nv_bfloat16 *o, const __nv_bfloat16 *dO,
@@ -1031,20 +1328,20 @@ cudaError_t softmax_segment_bwd(const SoftmaxProblem &p, const void *q, const vo
         mk, mv, mq, mdo, K);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  // dQ: items over the query tiles
+  // dQ: items over pairs of query tiles
   BwdParams Q = P;
-  Q.nitems = (int)(P.nqt * BH);
+  Q.nitems = (int)((P.nqt + 1) / 2 * BH);
   Q.out1 = static_cast<__nv_bfloat16 *>(dq);
   Q.out2 = nullptr;
   Q.osb = p.qsb; Q.osh = p.qsh; Q.ost = p.qst;
   Q.wide = a32(dq) && (p.qsb * 2) % 32 == 0 && (p.qsh * 2) % 32 == 0 && (p.qst * 2) % 32 == 0;
   Q.counter = status + kCounterSoftmaxQ;
-  if ((e = cudaFuncSetAttribute(softmax_bwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)bw_smem<false>())) != cudaSuccess)
+  if ((e = cudaFuncSetAttribute(softmax_bwd_dq2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kQ2Smem)) != cudaSuccess)
     return e;
   TimedLaunch t(K_SOFTMAX_BWD_Q, s);
-  softmax_bwd_kernel<false><<<Q.nitems < p.num_sms ? Q.nitems : p.num_sms, kBwThreads, bw_smem<false>(), s>>>(
-      mq, mdo, mk, mv, Q);
+  softmax_bwd_dq2_kernel<<<Q.nitems < p.num_sms ? Q.nitems : p.num_sms, kBwThreads, kQ2Smem, s>>>(mq, mdo, mk, mv,
+                                                                                                 Q);
   return cudaGetLastError();
 }
 

@@ -496,28 +496,24 @@ __global__ void __launch_bounds__(kSmThreads, 1)
 //   p_ij  = exp(scale q_i . k_j - lse_i)         (the row's softmax weights, recomputed)
 //   ds_ij = p_ij (dO_i . v_j - delta_i)
 //   dv_j  = sum_i p_ij dO_i,  dk_j = scale sum_i ds_ij q_i,  dq_i = scale sum_j ds_ij k_j
-// over the visible pairs j <= offset + i, in two launches that share one kernel:
-//   dK/dV: an item is one 128-key tile (X = K, V); it streams the query tiles that
-//          see it (Y = Q, dO): S^T = K Q^T and dP^T = V dO^T into TMEM, the
-//          elementwise warps write p and ds back as bf16, then dV += P^T dO and
-//          dK += dS^T Q read them from TMEM as the A operand;
-//   dQ:    an item is one 128-query tile (X = Q, dO); it streams the key tiles up to
-//          its diagonal (Y = K, V): S = Q K^T, dP = dO V^T, then dQ += dS K.
-// No atomics: every output row is owned by one item.  Warp roles as in the
-// forward: warp 0 the TMA producer, warp 1 the MMA issuer, warps 2..5 and 6..9
-// the elementwise work on the score columns 0..63 and 64..127 of a tile (one
-// row per thread), and the epilogue.  The bf16 results of a column half go to
-// that half's own TMEM columns (64 g .. 64 g + 31), so neither half writes
-// columns that the other still reads.  Every wait is bounded.
+// over the visible pairs j <= offset + i, in two launches, so that every output row is
+// owned by one item and nothing is accumulated with atomics:
+//   dK/dV (softmax_bwd_kernel): an item is one 128-key tile (X = K, V); it streams
+//          the query tiles that see it (Y = Q, dO): S^T = K Q^T and dP^T = V dO^T into
+//          TMEM, the elementwise warps write p and ds back as bf16, then dV += P^T dO
+//          and dK += dS^T Q read them from TMEM as the A operand;
+//   dQ (softmax_bwd_dq2_kernel, below): an item is a pair of 128-query tiles.
+// Warp roles as in the forward: warp 0 the TMA producer, warp 1 the MMA issuer,
+// warps 2..5 and 6..9 the elementwise work on the score columns 0..63 and 64..127
+// of a tile (one row per thread), and the epilogue.  The bf16 results of a column
+// half go to that half's own TMEM columns (64 g .. 64 g + 31), so neither half
+// writes columns that the other still reads.  Every wait is bounded.
 constexpr int kBwThreads = 320;
-constexpr int kBwSlots = 5;                                  // ring of Y tiles (32 KiB each), at most
-// the dK/dV kernel keeps one slot fewer: its column statistics take 2 KiB of static shared memory
-template <bool KV> constexpr int bw_slots() { return KV ? kBwSlots - 1 : kBwSlots; }
+constexpr int kBwSlots = 4;                                  // ring of Y tiles (32 KiB each)
 constexpr uint32_t kBwOffY = 2 * kTileBytes;                 // after the item's two X tiles
-template <bool KV> constexpr uint32_t bw_off_bar() { return kBwOffY + bw_slots<KV>() * kTileBytes; }
-template <bool KV> constexpr size_t bw_smem() { return bw_off_bar<KV>() + 256 + 1024; }
-static_assert(bw_smem<false>() + 128 <= 232448 && bw_smem<true>() + 2048 + 128 <= 232448,
-              "tiles, barriers and static shared memory fit 227 KB");
+constexpr uint32_t kBwOffBar = kBwOffY + kBwSlots * kTileBytes;
+constexpr size_t kBwSmem = kBwOffBar + 256 + 1024;
+static_assert(kBwSmem + 2048 + 128 <= 232448, "tiles, barriers, column statistics and static shared memory fit");
 
 enum { B_XFULL = 0, B_XEMPTY, B_FULL, B_EMPTY = B_FULL + kBwSlots, B_SFULL = B_EMPTY + kBwSlots, B_DPFULL,
        B_PREADY, B_DSREADY = B_PREADY + 2, B_AFULL = B_DSREADY + 2, B_AEMPTY, B_STAT, B_COUNT = B_STAT + 2 };
@@ -528,41 +524,31 @@ struct BwdParams {
   float scale_log2;             // softmax scale times log2(e)
   float scale;
   const float *lse2, *delta;    // [B*H][nqt*128]: lse_i log2(e) and dO_i . o_i (+inf and 0 past Tq)
-  __nv_bfloat16 *out1, *out2;   // dK/dV: dv, dk;  dQ: dq
+  __nv_bfloat16 *out1, *out2;   // dK/dV launch: dv, dk;  dQ launch: dq
   int64_t osb, osh, ost;        // element strides of the outputs
   int wide;                     // every output row starts on a 32-byte boundary
   int *status;
   int *counter;                 // [2] item counter and finished CTAs (zero at launch)
 };
 
-// item -> (sequence, X tile, first Y tile, Y tiles), sequence-major (the items in
-// flight share their sequences' Y tiles in L2) and longest first inside a sequence:
-// dK/dV key tiles in ascending order (a key tile is seen by the query tiles from the
-// one holding position key - offset on), dQ query tiles in descending order (a query
-// tile sees the key tiles up to its diagonal).
-template <bool KV>
+// item -> (sequence, key tile, first query tile, query tiles), sequence-major (the
+// items in flight share their sequences' query tiles in L2) and longest first inside
+// a sequence: key tiles in ascending order (a key tile is seen by the query tiles
+// from the one holding position key - offset on)
 __device__ __forceinline__ void bw_item(const BwdParams &P, int item, int &bh, int &xt, int &lo, int &ns) {
-  if (KV) {
-    bh = item / P.nkt;
-    xt = item % P.nkt;
-    lo = max(0, 128 * xt - P.off) / 128;
-    ns = P.nqt - lo;
-  } else {
-    bh = item / P.nqt;
-    xt = P.nqt - 1 - item % P.nqt;
-    lo = 0;
-    ns = min(P.nkt - 1, (P.off + 128 * xt + 127) / 128) + 1;
-  }
+  bh = item / P.nkt;
+  xt = item % P.nkt;
+  lo = max(0, 128 * xt - P.off) / 128;
+  ns = P.nqt - lo;
 }
 
-template <bool KV>
 __global__ void __launch_bounds__(kBwThreads, 1)
     softmax_bwd_kernel(const __grid_constant__ CUtensorMap mx1, const __grid_constant__ CUtensorMap mx2,
                        const __grid_constant__ CUtensorMap my1, const __grid_constant__ CUtensorMap my2, BwdParams P) {
-  constexpr int kSlots = bw_slots<KV>();
+  constexpr int kSlots = kBwSlots;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
-  uint64_t *bar = reinterpret_cast<uint64_t *>(smem + bw_off_bar<KV>());
+  uint64_t *bar = reinterpret_cast<uint64_t *>(smem + kBwOffBar);
   uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + B_COUNT);
   __shared__ int abort_flag;
   __shared__ int ring_item[kRingS];
@@ -606,10 +592,8 @@ __global__ void __launch_bounds__(kBwThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
-  // TMEM.  dK/dV: S^T (p in place as bf16), dP^T (ds in place), dV, dK.  dQ: two S buffers
-  // (the next tile's scores are formed while this tile's p are), dP (ds in place), dQ.
-  const uint32_t tP = tmem + (KV ? 128u : 256u), tA1 = tmem + (KV ? 256u : 384u), tA2 = tmem + 384u;
-  auto tS = [&](int u) { return tmem + (KV ? 0u : 128u * (uint32_t)(u & 1)); };
+  // TMEM: S^T (p in place as bf16), dP^T (ds in place), dV, dK
+  const uint32_t tS = tmem, tP = tmem + 128u, tA1 = tmem + 256u, tA2 = tmem + 384u;
   // dK/dV: the current step's column statistics (lse2, delta) per column half, two buffers
   __shared__ float4 colstat[2][2][2][16];  // [step parity][half][lse2 | delta][16 x 4 columns]
   auto sX = [&](int x) { return smem_u32(smem) + (uint32_t)x * kTileBytes; };
@@ -646,7 +630,7 @@ __global__ void __launch_bounds__(kBwThreads, 1)
         mbar_arrive(&ring_full[s]);
         if (item < 0) break;
         int bh, xt, lo, ns;
-        bw_item<KV>(P, item, bh, xt, lo, ns);
+        bw_item(P, item, bh, xt, lo, ns);
         const int b = bh / P.H, h = bh % P.H;
         if (k > 0 && !(ok = wait(B_XEMPTY, k - 1))) break;  // the previous item's score products read X
         mbar_arrive_expect_tx(&bar[B_XFULL], 2 * kTileBytes);
@@ -697,7 +681,7 @@ __global__ void __launch_bounds__(kBwThreads, 1)
     for (int k = 0, item; ok; ++k) {
       if (!(ok = __all_sync(0xffffffffu, take(k, item))) || item < 0) break;
       int bh, xt, lo, ns;
-      bw_item<KV>(P, item, bh, xt, lo, ns);
+      bw_item(P, item, bh, xt, lo, ns);
       if (!(ok = wait_all(B_XFULL, k))) break;
       for (int n = 0; n < ns && ok; ++n, ++u, li += 2) {
         const int i1 = li, i2 = li + 1, i3 = li + 2;  // Y1, Y2 of this step, Y1 of the next
@@ -706,7 +690,7 @@ __global__ void __launch_bounds__(kBwThreads, 1)
         tc_fence_after();
         const uint32_t Y1 = slot_addr(i1), Y2 = slot_addr(i2);
         if (n == 0) {
-          score(tS(u), sX(0), Y1);
+          score(tS, sX(0), Y1);
           mma_commit_warp(&bar[B_SFULL]);
         }
         score(tP, sX(1), Y2);
@@ -714,29 +698,26 @@ __global__ void __launch_bounds__(kBwThreads, 1)
         if (n + 1 == ns) mma_commit_warp(&bar[B_XEMPTY]);
         // the accumulators are free once the previous item's epilogue has read them
         if (n == 0 && k > 0 && !(ok = wait_all(B_AEMPTY, k - 1))) break;
-        if (KV) {
-          // dV += P^T dO, each column half as soon as its p are in TMEM
-          for (int g = 0; g < 2 && ok; ++g) {
-            if (!(ok = wait_all(B_PREADY + g, u))) break;
-            tc_fence_after();
-            accum(tA1, tS(u), Y2, g, n == 0);
-          }
-          if (!ok) break;
+        // dV += P^T dO, each column half as soon as its p are in TMEM
+        for (int g = 0; g < 2 && ok; ++g) {
+          if (!(ok = wait_all(B_PREADY + g, u))) break;
+          tc_fence_after();
+          accum(tA1, tS, Y2, g, n == 0);
         }
+        if (!ok) break;
         if (n + 1 < ns) {
-          // the elementwise warps have read this step's scores (dK/dV: waited above) before
-          // the next ones complete: a barrier phase never runs two ahead of its waiters
-          if (!KV && !(ok = wait_all(B_PREADY, u) && wait_all(B_PREADY + 1, u))) break;
+          // (the elementwise warps have read this step's scores, waited above, before the
+          // next ones complete: a barrier phase never runs two ahead of its waiters)
           if (!(ok = wait_all(B_FULL + i3 % kSlots, i3 / kSlots))) break;
           tc_fence_after();
-          score(tS(u + 1), sX(0), slot_addr(i3));
+          score(tS, sX(0), slot_addr(i3));
           mma_commit_warp(&bar[B_SFULL]);
         }
-        // dK += dS^T Q  or  dQ += dS K, each column half as soon as its ds are in TMEM
+        // dK += dS^T Q, each column half as soon as its ds are in TMEM
         for (int g = 0; g < 2 && ok; ++g) {
           if (!(ok = wait_all(B_DSREADY + g, u))) break;
           tc_fence_after();
-          accum(KV ? tA2 : tA1, tP, Y1, g, n == 0);
+          accum(tA2, tP, Y1, g, n == 0);
         }
         if (!ok) break;
         mma_commit_warp(&bar[B_EMPTY + i1 % kSlots]);
@@ -754,14 +735,12 @@ __global__ void __launch_bounds__(kBwThreads, 1)
     for (int k = 0, item; ok; ++k) {
       if (!(ok = __all_sync(0xffffffffu, take(k, item))) || item < 0) break;
       int bh, xt, lo, ns;
-      bw_item<KV>(P, item, bh, xt, lo, ns);
+      bw_item(P, item, bh, xt, lo, ns);
       const float *L2 = P.lse2 + (int64_t)bh * P.nqt * 128, *DL = P.delta + (int64_t)bh * P.nqt * 128;
-      // dQ: this row's query statistics
-      const float lrow = KV ? 0.f : L2[128 * xt + row], drow = KV ? 0.f : DL[128 * xt + row];
       for (int n = 0; n < ns; ++n, ++u) {
         const int yt = lo + n;
         float4 *cs = &colstat[u & 1][g][0][0];
-        if (KV) {
+        {
           // this step's 64 column statistics of the half into shared memory: one value per
           // thread, published through the half's mbarrier (a thread rewrites a buffer two
           // steps later, after every thread of the half has arrived for the step between)
@@ -769,32 +748,23 @@ __global__ void __launch_bounds__(kBwThreads, 1)
           reinterpret_cast<float *>(cs)[64 * which + c] = (which ? DL : L2)[128 * yt + 64 * g + c];
           mbar_arrive(&bar[B_STAT + g]);
         }
-        if (!(ok = __all_sync(0xffffffffu, wait(B_SFULL, u) && (!KV || wait(B_STAT + g, u))))) break;
+        if (!(ok = __all_sync(0xffffffffu, wait(B_SFULL, u) && wait(B_STAT + g, u)))) break;
         tc_fence_after();
-        // dK/dV: key 128 xt + row sees the query columns c >= lim;  dQ: query 128 xt + row
-        // sees the key columns c <= lim
-        const int lim = KV ? 128 * (xt - yt) + (int)row - P.off : P.off + 128 * (xt - yt) + (int)row;
+        // key 128 xt + row sees the query columns c >= lim of this tile
+        const int lim = 128 * (xt - yt) + (int)row - P.off;
         // every row of the warp sees every column of the half: no masks
-        const bool full = __all_sync(0xffffffffu, KV ? lim <= 64 * g : lim >= 64 * g + 63);
-        // dQ: the scores are double-buffered, so the next ones may be formed as soon as this
-        // step's have been waited for (the barrier phases stay within one of each other)
-        if (!KV) mbar_arrive(&bar[B_PREADY + g]);
-        // phase 1: p of the half's 64 columns (kept in registers; dK/dV: also into TMEM as bf16)
+        const bool full = __all_sync(0xffffffffu, lim <= 64 * g);
+        // phase 1: p of the half's 64 columns (kept in registers, and into TMEM as bf16)
         float p[64];
         {
           uint32_t sr[2][32];
-          tmem_ld32(tS(u) + lb + 64 * g, sr[0]);
-          tmem_ld32(tS(u) + lb + 64 * g + 32, sr[1]);
+          tmem_ld32(tS + lb + 64 * g, sr[0]);
+          tmem_ld32(tS + lb + 64 * g + 32, sr[1]);
           tmem_ld_wait();
 #pragma unroll
           for (int j4 = 0; j4 < 16; ++j4) {
-            float lv[4];
-            if (KV) {
-              const float4 l4 = cs[j4];
-              lv[0] = l4.x; lv[1] = l4.y; lv[2] = l4.z; lv[3] = l4.w;
-            } else {
-              lv[0] = lv[1] = lv[2] = lv[3] = lrow;
-            }
+            const float4 l4 = cs[j4];
+            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int j = 4 * j4 + e;
@@ -804,22 +774,20 @@ __global__ void __launch_bounds__(kBwThreads, 1)
           if (!full) {
 #pragma unroll
             for (int j = 0; j < 64; ++j)
-              if (KV ? 64 * g + j < lim : 64 * g + j > lim) p[j] = 0.f;
+              if (64 * g + j < lim) p[j] = 0.f;
           }
         }
-        if (KV) {
-          // p into TMEM for the dV product
+        // p into TMEM for the dV product
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            uint32_t wp[16];
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t wp[16];
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) wp[jj] = pack_bf16(p[32 * hh + 2 * jj], p[32 * hh + 2 * jj + 1]);
-            tmem_st16(tS(u) + lb + 64 * g + 16 * hh, wp);
-          }
-          tmem_st_wait();
-          tc_fence_before();
-          mbar_arrive(&bar[B_PREADY + g]);
+          for (int jj = 0; jj < 16; ++jj) wp[jj] = pack_bf16(p[32 * hh + 2 * jj], p[32 * hh + 2 * jj + 1]);
+          tmem_st16(tS + lb + 64 * g + 16 * hh, wp);
         }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bar[B_PREADY + g]);
         // phase 2: ds = p (dp - delta) into the dP tile as bf16
         if (!(ok = __all_sync(0xffffffffu, wait(B_DPFULL, u)))) break;
         tc_fence_after();
@@ -833,13 +801,8 @@ __global__ void __launch_bounds__(kBwThreads, 1)
             uint32_t wd[16];
 #pragma unroll
             for (int j4 = 0; j4 < 8; ++j4) {
-              float dl[4];
-              if (KV) {
-                const float4 d4 = cs[16 + 8 * hh + j4];
-                dl[0] = d4.x; dl[1] = d4.y; dl[2] = d4.z; dl[3] = d4.w;
-              } else {
-                dl[0] = dl[1] = dl[2] = dl[3] = drow;
-              }
+              const float4 d4 = cs[16 + 8 * hh + j4];
+              const float dl[4] = {d4.x, d4.y, d4.z, d4.w};
               const int j = 4 * j4;
               wd[2 * j4] = pack_bf16(p[32 * hh + j] * (__uint_as_float(dr[hh][j]) - dl[0]),
                                      p[32 * hh + j + 1] * (__uint_as_float(dr[hh][j + 1]) - dl[1]));
@@ -854,18 +817,16 @@ __global__ void __launch_bounds__(kBwThreads, 1)
         mbar_arrive(&bar[B_DSREADY + g]);
       }
       if (!ok) break;
-      // epilogue: dK/dV: the first half stores the dv row, the second the dk row (times the
-      // scale); dQ: each half stores its 64 columns of the dq row (times the scale)
+      // epilogue: the first half stores the dv row, the second the dk row (times the scale)
       if (!(ok = __all_sync(0xffffffffu, wait(B_AFULL, k)))) break;
       tc_fence_after();
       const int b = bh / P.H, h = bh % P.H, r = 128 * xt + (int)row;
-      const bool valid = r < (KV ? P.Tk : P.Tq);
-      __nv_bfloat16 *dst = (KV && g == 1 ? P.out2 : P.out1) + (int64_t)b * P.osb + (int64_t)h * P.osh +
-                           (int64_t)r * P.ost + (KV ? 0 : 64 * g);
-      const uint32_t src = (KV ? (g == 0 ? tA1 : tA2) : tA1 + 64u * g) + lb;
-      const float f = KV && g == 0 ? 1.f : P.scale;
+      const bool valid = r < P.Tk;
+      __nv_bfloat16 *dst = (g == 1 ? P.out2 : P.out1) + (int64_t)b * P.osb + (int64_t)h * P.osh + (int64_t)r * P.ost;
+      const uint32_t src = (g == 0 ? tA1 : tA2) + lb;
+      const float f = g == 0 ? 1.f : P.scale;
 #pragma unroll 1
-      for (int c = 0; c < (KV ? 4 : 2); ++c) {
+      for (int c = 0; c < 4; ++c) {
         float y[32];
         uint32_t o[32];
         tmem_ld32(src + 32 * c, o);
@@ -1320,12 +1281,11 @@ cudaError_t softmax_segment_bwd(const SoftmaxProblem &p, const void *q, const vo
     K.osb = p.ksb; K.osh = p.ksh; K.ost = p.kst;
     K.wide = a32(dk) && a32(dv) && (p.ksb * 2) % 32 == 0 && (p.ksh * 2) % 32 == 0 && (p.kst * 2) % 32 == 0;
     K.counter = status + kCounterSoftmaxKV;
-    if ((e = cudaFuncSetAttribute(softmax_bwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)bw_smem<true>())) != cudaSuccess)
+    if ((e = cudaFuncSetAttribute(softmax_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)kBwSmem)) != cudaSuccess)
       return e;
     TimedLaunch t(K_SOFTMAX_BWD_KV, s);
-    softmax_bwd_kernel<true><<<K.nitems < p.num_sms ? K.nitems : p.num_sms, kBwThreads, bw_smem<true>(), s>>>(
-        mk, mv, mq, mdo, K);
+    softmax_bwd_kernel<<<K.nitems < p.num_sms ? K.nitems : p.num_sms, kBwThreads, kBwSmem, s>>>(mk, mv, mq, mdo, K);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   // dQ: items over pairs of query tiles

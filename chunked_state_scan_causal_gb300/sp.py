@@ -19,8 +19,17 @@ Backward (the same exchange run in reverse):
      total is the gradient of the initial state               (linattn_state_scan)
   4. each rank runs its backward with d_final_state = D_r     (linattn_bwd_ckpt)
 
+The standard-attention layers of the hybrid model (LASP-2H on the same page)
+split the same way with one gather of keys and values instead of states
+(``softmax_forward`` / ``softmax_backward``): every rank gathers the k, v of all
+segments, its queries attend causally over segments 0..rank
+(linattn_softmax_segment_fwd), and in the backward the gradients of the
+gathered k, v go back to their owners, summed over the ranks that used them,
+by one reduce-scatter (linattn_softmax_segment_bwd for the local gradients).
+
 The arithmetic runs in this package's kernels; this module only moves the
-states between ranks.  The exchange is pluggable: ``TorchDistExchange`` uses a
+states (and, for the softmax layers, keys, values and their gradients)
+between ranks.  The exchange is pluggable: ``TorchDistExchange`` uses a
 torch.distributed process group (NCCL between GPUs, gloo between CPU
 processes); ``ThreadExchange`` connects ranks that are threads of one process.
 Every wait is bounded: an exchange that does not complete in ``timeout``
@@ -66,6 +75,25 @@ class TorchDistExchange:
             raise SequenceParallelError(f"rank {self.rank}: state exchange timed out after {self.timeout} s")
         return out
 
+    def reduce_scatter(self, parts):
+        """The sum over ranks of parts[this rank], for parts [world, ...] on every rank
+        (NCCL's reduce-scatter; other backends reduce the whole stack and keep the row)."""
+        import torch
+        parts = parts.contiguous()
+        try:
+            if self.dist.get_backend(self.group) == "nccl":
+                out = torch.empty_like(parts[0])
+                work = self.dist.reduce_scatter_tensor(out, parts, group=self.group, async_op=True)
+            else:
+                out = parts.clone()
+                work = self.dist.all_reduce(out, group=self.group, async_op=True)
+            ok = work.wait(timeout=datetime.timedelta(seconds=self.timeout))
+        except Exception as e:  # peer gone, connection reset, backend timeout
+            raise SequenceParallelError(f"rank {self.rank}: gradient exchange failed: {e}") from e
+        if ok is False:
+            raise SequenceParallelError(f"rank {self.rank}: gradient exchange timed out after {self.timeout} s")
+        return out if out.dim() == parts.dim() - 1 else out[self.rank]
+
 
 class ThreadExchange:
     """Ranks that are threads of one process (a rendezvous per exchange).
@@ -106,6 +134,17 @@ class ThreadExchange:
         self._wait()  # every rank has read the slots before they are reused
         return torch.stack(rows[::-1] if reverse else rows)
 
+    def reduce_scatter(self, parts):
+        """The sum over ranks of parts[this rank] (in rank order)."""
+        self.group.slots[self.rank] = parts
+        self._wait()
+        rows = list(self.group.slots)
+        out = rows[0][self.rank].clone()
+        for x in rows[1:]:
+            out += x[self.rank]
+        self._wait()
+        return out
+
 
 # ----------------------------------------------------------------------------- local operations
 class KernelOps:
@@ -138,6 +177,12 @@ class KernelOps:
     def seg_decay(self, decay, B, seg_len):
         """Per-(b, h) multiplier lambda_h^seg_len for the scan, [B*H] fp32 (None for lambda = 1)."""
         return self.la.segment_decay(decay, B, seg_len)
+
+    def softmax_fwd(self, q, k, v, scale):
+        return self.la.softmax_segment_fwd(q, k, v, scale=scale, want_lse=True)
+
+    def softmax_bwd(self, q, k, v, o, dO, lse, scale):
+        return self.la.softmax_segment_bwd(q, k, v, o, dO, lse, scale=scale)
 
 
 @dataclass
@@ -185,3 +230,55 @@ def backward(q, k, v, dO, ctx: Context, exchange, decay=None, d_final=None, ops=
     d_fin = D[exchange.world - 1 - exchange.rank].contiguous()
     dq, dk, dv = ops.bwd(q, k, v, dO, decay, ctx.init_state, ctx.checkpoint, d_fin)
     return dq, dk, dv, d_init
+
+
+# ----------------------------------------------------------------------------- softmax layers (LASP-2H)
+@dataclass
+class SoftmaxContext:
+    """What a rank keeps from a softmax layer's forward for its backward."""
+    k_prefix: object   # [B, H, (rank + 1) L, d]: the gathered keys of segments 0..rank
+    v_prefix: object
+    o: object          # this rank's outputs
+    lse: object        # [B, H, L] fp32 log-sum-exp of this rank's rows
+    scale: float
+
+
+def softmax_forward(q, k, v, exchange, scale=0.0, ops=None):
+    """This rank's outputs of causal softmax attention and a SoftmaxContext.
+
+    One gather hands every rank the keys and values of all segments; the rank's
+    queries, the last L positions of the prefix that ends with its own segment,
+    attend over segments 0..rank.  ``scale`` 0 means 1/sqrt(d)."""
+    import torch
+    ops = ops or KernelOps()
+    _check_segment(q, exchange.world)
+    allK = exchange.all_gather(k.contiguous())                    # [N, B, H, L, d]
+    allV = exchange.all_gather(v.contiguous())
+    r = exchange.rank
+    kp = torch.cat(list(allK[:r + 1]), dim=2)                     # [B, H, (r + 1) L, d]
+    vp = torch.cat(list(allV[:r + 1]), dim=2)
+    o, lse = ops.softmax_fwd(q, kp, vp, scale)
+    return o, SoftmaxContext(kp, vp, o, lse, scale)
+
+
+def softmax_backward(q, dO, ctx: SoftmaxContext, exchange, ops=None):
+    """This rank's (dq, dk, dv).  The gradients of the gathered keys and values are
+    returned to their owners, summed over the ranks whose queries saw them (one
+    reduce-scatter)."""
+    import torch
+    ops = ops or KernelOps()
+    dq, dkp, dvp = ops.softmax_bwd(q, ctx.k_prefix, ctx.v_prefix, ctx.o, dO, ctx.lse, ctx.scale)
+    N, r = exchange.world, exchange.rank
+    B, H, L, d = q.shape
+
+    def spread(x):
+        # this rank's contribution to every segment's gradient: [N, B, H, L, d], zero past
+        # rank r, summed in fp32 (or the inputs' own type when that is wider)
+        acc = torch.float64 if x.dtype == torch.float64 else torch.float32
+        out = torch.zeros((N, B, H, L, x.shape[3]), dtype=acc, device=x.device)
+        out[:r + 1] = x.to(acc).reshape(B, H, r + 1, L, x.shape[3]).permute(2, 0, 1, 3, 4)
+        return out
+
+    dk = exchange.reduce_scatter(spread(dkp)).to(q.dtype)
+    dv = exchange.reduce_scatter(spread(dvp)).to(q.dtype)
+    return dq, dk, dv

@@ -41,3 +41,11 @@ class OracleOps:
 
     def seg_decay(self, decay, B, seg_len):
         return None if decay is None else (decay.double() ** seg_len).repeat(B)
+
+    def softmax_fwd(self, q, k, v, scale):
+        o, lse = oracle.softmax_segment_fwd(_np(q), _np(k), _np(v), scale=None if scale == 0.0 else scale)
+        return _t(o), _t(lse)
+
+    def softmax_bwd(self, q, k, v, o, dO, lse, scale):
+        dq, dk, dv = oracle.softmax_segment_bwd(_np(q), _np(k), _np(v), _np(dO), scale=None if scale == 0.0 else scale)
+        return _t(dq), _t(dk), _t(dv)

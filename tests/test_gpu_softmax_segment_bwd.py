@@ -133,3 +133,41 @@ def test_softmax_segment_bwd_full_size_sampled():
     for name, got, ref in (("dq", got_q[:, :, rows], rq[:, :, rows]), ("dk", got_k[:, :, -64:], rk[:, :, -64:]),
                            ("dv", got_v[:, :, -64:], rv[:, :, -64:])):
         assert rel(got, ref) < 1e-2, (name, rel(got, ref))
+
+
+def test_softmax_layer_split_across_thread_ranks():
+    """The hybrid's softmax layers split across 4 ranks (threads of this process, one
+    gather of k, v; the key and value gradients summed back to their owners), on the
+    kernels: the concatenated outputs and gradients equal whole-sequence causal softmax
+    attention (oracle)."""
+    import threading
+    from chunked_state_scan_causal_gb300 import sp
+    N, L, B, H = 4, 256, 1, 2
+    q, k, v, dO = case(31, B, H, N * L, N * L)
+    dev = [x.cuda() for x in (q, k, v, dO)]
+    group = sp.ThreadExchange.Group(N, timeout=60)
+    res, errs = [None] * N, []
+
+    def rank(r):
+        ex = group.rank(r)
+        try:
+            seg = [x[:, :, r * L:(r + 1) * L] for x in dev]
+            o, ctx = sp.softmax_forward(seg[0], seg[1], seg[2], ex)
+            res[r] = (o,) + sp.softmax_backward(seg[0], seg[3], ctx, ex)
+        except Exception as e:  # a failing rank releases its peers
+            errs.append(e)
+            ex.abort()
+
+    th = [threading.Thread(target=rank, args=(r,)) for r in range(N)]
+    for t in th:
+        t.start()
+    for t in th:
+        t.join(timeout=300)
+    torch.cuda.synchronize()
+    assert not errs, errs
+    n = lambda x: x.double().numpy()
+    ro, _ = oracle.softmax_segment_fwd(n(q), n(k), n(v))
+    rq, rk, rv = oracle.softmax_segment_bwd(n(q), n(k), n(v), n(dO))
+    for i, (name, ref) in enumerate((("o", ro), ("dq", rq), ("dk", rk), ("dv", rv))):
+        got = torch.cat([x[i] for x in res], dim=2)
+        assert rel(got, ref) < 1e-2, (name, rel(got, ref))

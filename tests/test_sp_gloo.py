@@ -1,8 +1,10 @@
 """The sequence-parallel exchange (chunked_state_scan_causal_gb300.sp) across CPU
 processes over gloo: ranks holding consecutive segments reproduce the
 whole-sequence forward and backward, and a rank that dies before the exchange
-makes its peers fail within the timeout instead of hanging.  The per-rank
-arithmetic is the fp64 oracle here; on GPUs it is the library's kernels."""
+makes its peers fail within the timeout instead of hanging; the softmax layers of
+the hybrid (one gather of k, v, the gradients summed back to their owners)
+reproduce whole-sequence causal softmax attention.  The per-rank arithmetic is
+the fp64 oracle here; on GPUs it is the library's kernels."""
 import datetime
 import os
 import socket
@@ -70,6 +72,50 @@ def test_ranks_reproduce_the_whole_sequence(world):
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
     procs = [ctx.Process(target=_rank_split, args=(r, world, port, 100 + world, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=180)
+        assert p.exitcode == 0
+    res = sorted(q.get(timeout=10) for _ in range(world))
+    assert [r for r, _ in res] == list(range(world))
+    for r, err in res:
+        assert err < 1e-10, (r, err)
+
+
+def _rank_softmax(rank, world, port, seed, out):
+    """LASP-2H: the rank's queries over the gathered keys and values of segments 0..rank."""
+    sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
+    from chunked_state_scan_causal_gb300 import sp
+    from sp_oracle_ops import OracleOps
+    import oracle
+    dist = _init(rank, world, port)
+    try:
+        q, k, v, dO, _, _, _ = _inputs(world, seed)
+        seg = slice(rank * L, (rank + 1) * L)
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a))
+        ex = sp.TorchDistExchange(timeout=20)
+        ops = OracleOps()
+        o, ctx = sp.softmax_forward(t(q[:, :, seg]), t(k[:, :, seg]), t(v[:, :, seg]), ex, scale=0.6, ops=ops)
+        dq, dk, dv = sp.softmax_backward(t(q[:, :, seg]), t(dO[:, :, seg]), ctx, ex, ops=ops)
+        ro, _ = oracle.softmax_segment_fwd(q, k, v, scale=0.6)
+        rq, rk, rv = oracle.softmax_segment_bwd(q, k, v, dO, scale=0.6)
+        err = max(float(np.abs(a.numpy() - b).max()) for a, b in (
+            (o, ro[:, :, seg]), (dq, rq[:, :, seg]), (dk, rk[:, :, seg]), (dv, rv[:, :, seg])))
+        out.put((rank, err))
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world", [2, 3])
+def test_softmax_layer_split_reproduces_the_whole_sequence(world):
+    """The softmax layers of the hybrid split across ranks (one gather of k, v; the key
+    and value gradients summed back to their owners) equal causal softmax attention over
+    the whole sequence, forward and backward."""
+    port = _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_rank_softmax, args=(r, world, port, 200 + world, q)) for r in range(world)]
     for p in procs:
         p.start()
     for p in procs:

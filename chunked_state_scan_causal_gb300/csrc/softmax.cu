@@ -737,16 +737,21 @@ __global__ void __launch_bounds__(kBwThreads, 1)
       int bh, xt, lo, ns;
       bw_item(P, item, bh, xt, lo, ns);
       const float *L2 = P.lse2 + (int64_t)bh * P.nqt * 128, *DL = P.delta + (int64_t)bh * P.nqt * 128;
+      // this thread's column statistic of a step (one value per thread: 64 columns x two
+      // arrays per half), loaded one step ahead so that its latency is not on the step's path
+      const int sc = gt & 63, which = gt >> 6;
+      const float *stat = (which ? DL : L2) + 64 * g + sc;
+      float sv = stat[128 * lo];
       for (int n = 0; n < ns; ++n, ++u) {
         const int yt = lo + n;
         float4 *cs = &colstat[u & 1][g][0][0];
         {
-          // this step's 64 column statistics of the half into shared memory: one value per
-          // thread, published through the half's mbarrier (a thread rewrites a buffer two
-          // steps later, after every thread of the half has arrived for the step between)
-          const int c = gt & 63, which = gt >> 6;
-          reinterpret_cast<float *>(cs)[64 * which + c] = (which ? DL : L2)[128 * yt + 64 * g + c];
+          // this step's 64 column statistics of the half into shared memory, published
+          // through the half's mbarrier (a thread rewrites a buffer two steps later, after
+          // every thread of the half has arrived for the step between)
+          reinterpret_cast<float *>(cs)[64 * which + sc] = sv;
           mbar_arrive(&bar[B_STAT + g]);
+          if (n + 1 < ns) sv = stat[128 * (yt + 1)];
         }
         if (!(ok = __all_sync(0xffffffffu, wait(B_SFULL, u) && wait(B_STAT + g, u)))) break;
         tc_fence_after();

@@ -627,11 +627,13 @@ int32_t linattn_bwd_gated(const linattn_shape *shape, const void *q, const void 
   pt.gq = q;
   pt.gk = k;
   pt.gx = reinterpret_cast<float *>(ws + w.gx);
-  // dq: forward-time kernel with (q, k, v) := (dO, v, k) from the group states (transposed)
-  if (e == cudaSuccess) e = tc_main(pt, gp, dO, v, k, dq, states, true, nullptr, status, s);
-  // reverse group aggregates sum_s exp2(C_s) q_s dO_s^T, the final-state gradient folded
-  // across the last group, and the reverse scan with every group's own multiplier
-  if (e == cudaSuccess) e = tc_segment_states(pt, gp, q, dO, true, wagg, status, s);
+  // dq: forward-time kernel with (q, k, v) := (dO, v, k) from the group states (transposed),
+  // which also accumulates the reverse group aggregates sum_s exp2(C_s) q_s dO_s^T of the
+  // items in the weighted form; the aggregate pass forms those of the other items
+  if (e == cudaSuccess) e = tc_main(pt, gp, dO, v, k, dq, states, true, nullptr, status, s, q, wagg);
+  if (e == cudaSuccess) e = tc_segment_states(pt, gp, q, dO, true, wagg, status, s, true);
+  // the final-state gradient folded across the last group, and the reverse scan with
+  // every group's own multiplier
   if (e == cudaSuccess && dfin)
     e = fold_state_log2(wagg + (int64_t)(G - 1) * E, dfin, tot + (int64_t)(G - 1) * BH, pt.d * pt.d, E, s);
   if (e == cudaSuccess) e = plan_scan(pt, gp, true, wagg, nullptr, rbar, dinit, ws + w.f.scan, status, s, tot);

@@ -199,7 +199,9 @@ struct AggParams {
   int *status;
   int *counter;  // [2] item counter and finished CTAs (zero at launch)
   const float *gC, *gtot;  // gates: group-local log2 cumulative sums [BH][T], group totals [G][BH]
-  int skip_weighted;       // pass over the items of heads with lambda >= kWeightedMin (the dq pass has them)
+  int skip_weighted;       // pass over the items of the weighted form (the dq pass has them): heads with
+                           // lambda >= kWeightedMin, or gated items flagged in gflag
+  const int *gflag;        // gates: per item [G][BH], nonzero for the weighted form
   int dout;                // rows and columns of the stored states: 128, or 64 (top-left blocks)
 };
 
@@ -255,7 +257,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       int it = 0;
       bool ok = true;
       for (int k = 0, item; ok; ++k) {
-        auto skip = [&](int x) { return DECAY && !GATE && P.skip_weighted && P.decay[(x % BH) % P.H] >= kWeightedMin; };
+        auto skip = [&](int x) {
+          if (!DECAY || !P.skip_weighted) return false;
+          return GATE ? (P.gflag && P.gflag[x] != 0) : P.decay[(x % BH) % P.H] >= kWeightedMin;
+        };
         if (!(ok = ring_post(ring, k, P.counter, P.nitems, item, &abort_flag, P.status, detail, skip)) || item < 0)
           break;
         const int g = item / BH, bh = item % BH, b = bh / P.H, h = bh % P.H;
@@ -774,7 +779,7 @@ __device__ __forceinline__ float dot32_bf16(const float (&x)[32], const __nv_bfl
 // written per group to agg_out: for the dq launch (q := dO, x := q) that is
 // the reverse group aggregate sum_s w_s q_s dO_s^T.  With a decay only the
 // items of the weighted form do so (the fourth region holds O_inter in the
-// others).  Tiles are loaded in the order q, x, k, v and released as their
+// others); gated items of that form weight the x rows by exp2(C_s).  Tiles are loaded in the order q, x, k, v and released as their
 // last product completes.
 // GATE (with DECAY) takes every weight from the gates' group-local cumulative
 // sums C: o_i = exp2(C_i - C_prev) (Q S)_i + (P V)_i, mask exp2(C_i - C_j), key
@@ -787,7 +792,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_main_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                    const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mo,
                    const __grid_constant__ CUtensorMap mx, MainParams P) {
-  static_assert(!AGG || !GATE, "group aggregates are fused for per-head decays only");
   static_assert(!GATE || DECAY, "gates use the weighted code paths");
   constexpr int NT = AGG ? 4 : 3;  // tiles per block
   extern __shared__ uint8_t smem_raw[];
@@ -1109,7 +1113,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (r >= nv) return 0.f;
         return GATE ? exp2f(gc[t0 + nv - 1] - gc[t0 + r]) : exp2f(l2 * (float)(nv - 1 - r));
       };
-      auto wx = [&](int n) { return (int)row < nvalid(n) ? exp2f(l2 * (float)(128 * n + (int)row + 1)) : 0.f; };
+      auto wx = [&](int n) {
+        if ((int)row >= nvalid(n)) return 0.f;
+        return GATE ? exp2f(gc[s0 + 128 * n + (int)row]) : exp2f(l2 * (float)(128 * n + (int)row + 1));
+      };
       // weigh this thread's row of tile role r (2 V, 3 X) of CTA block b once it
       // has landed, then arrive on the barrier bar_idx + block parity
       auto weigh = [&](int b, int r, float w, int bar_idx) {
@@ -1884,6 +1891,7 @@ cudaError_t tc_segment_states(const Problem &p, const GroupPlan &gp, const void 
   A.decay = p.decay; A.out = out; A.status = status; A.counter = status + kCounterAgg;
   A.gC = p.gC; A.gtot = p.gtot;
   A.skip_weighted = skip_weighted ? 1 : 0;
+  A.gflag = p.gflag;
   A.dout = dout;
   const size_t smem = 3 * 2 * kTileBytes + 1024 + 256;
   const int grid = A.nitems < p.num_sms ? A.nitems : p.num_sms;
@@ -1964,7 +1972,7 @@ cudaError_t tc_dual(const Problem &p, const GroupPlan &gp, const void *q, const 
 cudaError_t tc_main(const Problem &p, const GroupPlan &gp, const void *q, const void *k, const void *v, void *o,
                     const float *group_init, bool init_transposed, float *final_state, int *status,
                     cudaStream_t s, const void *x, float *agg_out) {
-  if (x && (p.gC || !agg_out)) return cudaErrorInvalidValue;
+  if (x && !agg_out) return cudaErrorInvalidValue;
   alignas(64) CUtensorMap mq, mk, mv, mo, mx;
   if (!seq_tmap(p, q, &mq) || !seq_tmap(p, k, &mk) || !seq_tmap(p, v, &mv) || !seq_tmap(p, o, &mo) ||
       !seq_tmap(p, x ? x : q, &mx))
@@ -1991,7 +1999,9 @@ cudaError_t tc_main(const Problem &p, const GroupPlan &gp, const void *q, const 
     if ((e = set_smem(tc_main_kernel<DEC, AGG, GATE>, kMainSmem)) != cudaSuccess) return e;   \
     tc_main_kernel<DEC, AGG, GATE><<<grid, kThreads, kMainSmem, s>>>(mq, mk, mv, mo, mx, M);  \
   } while (0)
-  if (x && p.decay)
+  if (x && p.gC)
+    LINATTN_LAUNCH_MAIN(true, true, true);
+  else if (x && p.decay)
     LINATTN_LAUNCH_MAIN(true, true, false);
   else if (x)
     LINATTN_LAUNCH_MAIN(false, true, false);

@@ -31,6 +31,7 @@ BF16, F32 = 0, 1
 OP_FWD, OP_BWD, OP_CHUNK_STATES, OP_CHECKPOINT = 1, 2, 3, 4
 OP_FWD_GATED, OP_BWD_GATED, OP_CHECKPOINT_GATED = 5, 6, 7
 OP_SOFTMAX_SEGMENT, OP_SOFTMAX_SEGMENT_BWD = 8, 9
+OP_FWD_GATED_VEC, OP_BWD_GATED_VEC = 10, 11
 ABI_VERSION = 2
 
 
@@ -68,9 +69,9 @@ _SIGS = {
     "linattn_fwd_gated": ([ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _sz, _vp], _i32),
     "linattn_bwd_gated": ([ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _vp, _vp, _vp,
                            _vp, _vp, _sz, _vp], _i32),
-    "linattn_fwd_gated_vec": ([ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp], _i32),
+    "linattn_fwd_gated_vec": ([ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "linattn_bwd_gated_vec": ([ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
-                               _vp], _i32),
+                               _vp, _sz, _vp], _i32),
     "linattn_decode": ([ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp], _i32),
     "linattn_state_scan_workspace_size": ([_i32, _i32, _i32, _i32, ctypes.POINTER(_sz)], _i32),
     "linattn_state_scan": ([_i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
@@ -171,14 +172,15 @@ def linattn_bwd_gated(shape, q, k, v, dO, log_gate, init_state, d_final, ckpt, c
                                    ckpt_bytes, dq, dk, dv, d_log_gate, d_init, ws, ws_bytes, stream)
 
 
-def linattn_fwd_gated_vec(shape, q, k, v, log_gate, o, init_state, final_state, stream) -> int:
-    return lib().linattn_fwd_gated_vec(ctypes.byref(shape), q, k, v, log_gate, o, init_state, final_state, stream)
+def linattn_fwd_gated_vec(shape, q, k, v, log_gate, o, init_state, final_state, ws, ws_bytes, stream) -> int:
+    return lib().linattn_fwd_gated_vec(ctypes.byref(shape), q, k, v, log_gate, o, init_state, final_state, ws,
+                                       ws_bytes, stream)
 
 
-def linattn_bwd_gated_vec(shape, q, k, v, dO, log_gate, init_state, d_final, dq, dk, dv, d_log_gate, d_init,
-                          stream) -> int:
+def linattn_bwd_gated_vec(shape, q, k, v, dO, log_gate, init_state, d_final, dq, dk, dv, d_log_gate, d_init, ws,
+                          ws_bytes, stream) -> int:
     return lib().linattn_bwd_gated_vec(ctypes.byref(shape), q, k, v, dO, log_gate, init_state, d_final, dq, dk, dv,
-                                       d_log_gate, d_init, stream)
+                                       d_log_gate, d_init, ws, ws_bytes, stream)
 
 
 def linattn_chunk_states_rev(shape, seg_len, q, dO, out, ws, ws_bytes, stream) -> int:
@@ -465,7 +467,7 @@ def _gate_tensor_vec(log_gate, q):
     return log_gate
 
 
-def fwd_gated_vec(q, k, v, log_gate, init_state=None, want_final=False, out=None, stream=None):
+def fwd_gated_vec(q, k, v, log_gate, init_state=None, want_final=False, out=None, ws=None, stream=None):
     """(o, final_state or None) with a gate per token and key dimension:
     S_t = diag(exp(log_gate_t)) S_{t-1} + k_t v_t^T (log_gate [B, H, T, d] fp32)."""
     import torch
@@ -474,13 +476,16 @@ def fwd_gated_vec(q, k, v, log_gate, init_state=None, want_final=False, out=None
     B, H, T, d = q.shape
     o = out if out is not None else torch.empty_strided(q.shape, q.stride(), dtype=q.dtype, device=q.device)
     fin = torch.empty((B, H, d, d), dtype=torch.float32, device=q.device) if want_final else None
+    if ws is None:
+        ws = workspace(q, OP_FWD_GATED_VEC)
     st = linattn_fwd_gated_vec(shape_of(q, None), _ptr(q), _ptr(k), _ptr(v), _ptr(log_gate), _ptr(o),
-                               _ptr(init_state), _ptr(fin), _stream(q.device, stream))
+                               _ptr(init_state), _ptr(fin), _ptr(ws), ws.numel(), _stream(q.device, stream))
     _check(st, "linattn_fwd_gated_vec")
     return o, fin
 
 
-def bwd_gated_vec(q, k, v, dO, log_gate, init_state=None, d_final=None, want_dinit=False, outs=None, stream=None):
+def bwd_gated_vec(q, k, v, dO, log_gate, init_state=None, d_final=None, want_dinit=False, outs=None, ws=None,
+                  stream=None):
     """(dq, dk, dv, d_log_gate [B, H, T, d], d_init or None) of fwd_gated_vec for the upstream gradient dO."""
     import torch
     _same_layout(q, k, v, dO)
@@ -491,9 +496,11 @@ def bwd_gated_vec(q, k, v, dO, log_gate, init_state=None, d_final=None, want_din
     dq, dk, dv = outs
     dlg = torch.empty((B, H, T, d), dtype=torch.float32, device=q.device)
     dinit = torch.empty((B, H, d, d), dtype=torch.float32, device=q.device) if want_dinit else None
+    if ws is None:
+        ws = workspace(q, OP_BWD_GATED_VEC)
     st = linattn_bwd_gated_vec(shape_of(q, None), _ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(log_gate),
                                _ptr(init_state), _ptr(d_final), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dlg), _ptr(dinit),
-                               _stream(q.device, stream))
+                               _ptr(ws), ws.numel(), _stream(q.device, stream))
     _check(st, "linattn_bwd_gated_vec")
     return dq, dk, dv, dlg, dinit
 

@@ -316,6 +316,8 @@ int32_t linattn_workspace_size(const linattn_shape *shape, int32_t op, int32_t s
     *bytes = ckpt_bytes_gated(p);
   } else if (op == LINATTN_OP_SOFTMAX_SEGMENT) {
     *bytes = kHeader;
+  } else if (op == LINATTN_OP_FWD_GATED_VEC || op == LINATTN_OP_BWD_GATED_VEC) {
+    *bytes = kHeader + gated_vec_ws_bytes(p, op == LINATTN_OP_BWD_GATED_VEC);
   } else if (op == LINATTN_OP_SOFTMAX_SEGMENT_BWD) {
     *bytes = kHeader + softmax_bwd_stats_bytes(p.B, p.H, p.T);
   } else {
@@ -647,12 +649,13 @@ int32_t linattn_bwd_gated(const linattn_shape *shape, const void *q, const void 
 
 int32_t linattn_fwd_gated_vec(const linattn_shape *shape, const void *q, const void *k, const void *v,
                               const float *log_gate, void *o, const float *init_state, float *final_state,
-                              void *stream) {
+                              void *workspace, size_t workspace_bytes, void *stream) {
   Problem p;
   int st = validate(shape, &p);
   if (st) return st;
   if (p.decay) return LINATTN_ERR_INVALID;  // the gates replace the per-head decay
   if ((st = check_ptrs({}, {init_state, final_state}))) return st;
+  if ((st = check_ws(workspace, workspace_bytes, kHeader + gated_vec_ws_bytes(p, false)))) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (p.T == 0) {
     if (!final_state) return LINATTN_OK;
@@ -662,18 +665,21 @@ int32_t linattn_fwd_gated_vec(const linattn_shape *shape, const void *q, const v
   }
   if ((st = check_ptrs({q, k, v, o, log_gate}, {}))) return st;
   if ((st = device_ok())) return st;
-  return cuda_status(gated_vec_fwd(p, q, k, v, log_gate, o, init_state, final_state, s));
+  if (cudaMemsetAsync(workspace, 0, kHeader, s) != cudaSuccess) return LINATTN_ERR_CUDA;
+  return cuda_status(gated_vec_fwd(p, q, k, v, log_gate, o, init_state, final_state,
+                                   static_cast<char *>(workspace) + kHeader, s));
 }
 
 int32_t linattn_bwd_gated_vec(const linattn_shape *shape, const void *q, const void *k, const void *v,
                               const void *dO, const float *log_gate, const float *init_state,
                               const float *d_final_state, void *dq, void *dk, void *dv, float *d_log_gate,
-                              float *d_init_state, void *stream) {
+                              float *d_init_state, void *workspace, size_t workspace_bytes, void *stream) {
   Problem p;
   int st = validate(shape, &p);
   if (st) return st;
   if (p.decay) return LINATTN_ERR_INVALID;
   if ((st = check_ptrs({}, {init_state, d_final_state, d_init_state}))) return st;
+  if ((st = check_ws(workspace, workspace_bytes, kHeader + gated_vec_ws_bytes(p, true)))) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (p.T == 0) {
     if (!d_init_state) return LINATTN_OK;
@@ -684,8 +690,9 @@ int32_t linattn_bwd_gated_vec(const linattn_shape *shape, const void *q, const v
   }
   if ((st = check_ptrs({q, k, v, dO, log_gate, dq, dk, dv, d_log_gate}, {}))) return st;
   if ((st = device_ok())) return st;
+  if (cudaMemsetAsync(workspace, 0, kHeader, s) != cudaSuccess) return LINATTN_ERR_CUDA;
   return cuda_status(gated_vec_bwd(p, q, k, v, dO, log_gate, init_state, d_final_state, dq, dk, dv, d_log_gate,
-                                   d_init_state, s));
+                                   d_init_state, static_cast<char *>(workspace) + kHeader, s));
 }
 
 int32_t linattn_decode(const linattn_shape *shape, const void *q, const void *k, const void *v, void *o,

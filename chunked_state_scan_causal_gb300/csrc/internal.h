@@ -191,13 +191,16 @@ struct SoftmaxProblem {
 // top-left block of [n][128][128], zeros elsewhere.
 cudaError_t pad_state_d64(const float *src, float *dst, int64_t n, cudaStream_t s);
 cudaError_t unpad_state_d64(const float *src, float *dst, int64_t n, cudaStream_t s);
-// Per-dimension gates (gate_vec.cu): one CTA per (batch, head) walks the sequence;
-// log_gate and d_log_gate are [B*H][T][d] fp32.
+// Per-dimension gates (gate_vec.cu): one CTA per (chunk group, batch, head) walks its
+// tokens, the groups joined by scans with per-row multipliers; log_gate and d_log_gate
+// are [B*H][T][d] fp32.  Workspace bytes of the group path (0 when one group covers
+// the sequence).
+size_t gated_vec_ws_bytes(const Problem &p, bool bwd);
 cudaError_t gated_vec_fwd(const Problem &p, const void *q, const void *k, const void *v, const float *log_gate,
-                          void *o, const float *init, float *final_state, cudaStream_t s);
+                          void *o, const float *init, float *final_state, void *ws, cudaStream_t s);
 cudaError_t gated_vec_bwd(const Problem &p, const void *q, const void *k, const void *v, const void *dO,
                           const float *log_gate, const float *init, const float *d_final, void *dq, void *dk,
-                          void *dv, float *d_log_gate, float *d_init, cudaStream_t s);
+                          void *dv, float *d_log_gate, float *d_init, void *ws, cudaStream_t s);
 cudaError_t softmax_segment(const SoftmaxProblem &p, const void *q, const void *k, const void *v, void *o, float *lse,
                             int *status, cudaStream_t s);
 // The backward: dq (q strides), dk and dv (k strides) for the output gradient dO

@@ -78,7 +78,8 @@ enum { LINATTN_BF16 = 0, LINATTN_F32 = 1 };
 /* Workspace / checkpoint queries. */
 enum { LINATTN_OP_FWD = 1, LINATTN_OP_BWD = 2, LINATTN_OP_CHUNK_STATES = 3, LINATTN_OP_CHECKPOINT = 4,
        LINATTN_OP_FWD_GATED = 5, LINATTN_OP_BWD_GATED = 6, LINATTN_OP_CHECKPOINT_GATED = 7,
-       LINATTN_OP_SOFTMAX_SEGMENT = 8, LINATTN_OP_SOFTMAX_SEGMENT_BWD = 9 };
+       LINATTN_OP_SOFTMAX_SEGMENT = 8, LINATTN_OP_SOFTMAX_SEGMENT_BWD = 9, LINATTN_OP_FWD_GATED_VEC = 10,
+       LINATTN_OP_BWD_GATED_VEC = 11 };
 
 typedef struct {
   int32_t abi_version;  /* must be LINATTN_ABI_VERSION                              */
@@ -198,24 +199,28 @@ int32_t linattn_bwd_gated(const linattn_shape *shape, const void *q, const void 
  *   S_t = diag(alpha_t) S_{t-1} + k_t v_t^T,   o_t = S_t^T q_t
  * (row i of the state decays by the gate of key dimension i).  log_gate is
  * [B,H,T,d] fp32, contiguous, 16-byte aligned; the shape's decay must be NULL.
- * Runs on CUDA-core kernels that walk every sequence token by token, one CTA
- * per (batch, head), fp32 state in shared memory: correct for any length,
- * meant for moderate T (the per-token gates above have the tensor-core path).
- * No workspace and no device-side waits.  Returns a status. */
+ * Runs on CUDA-core kernels (fp32 state in shared memory, no device-side
+ * waits): each sequence is cut into chunk groups, one CTA per (group, batch,
+ * head) walks its tokens, and the groups are joined by scans whose multipliers
+ * are per state row (the product of a group's gates of that key dimension);
+ * with few tokens, one CTA per (batch, head) walks the whole sequence.  The
+ * per-token gates above have the tensor-core path.  Workspace:
+ * LINATTN_OP_FWD_GATED_VEC bytes (the groups' states).  Returns a status. */
 int32_t linattn_fwd_gated_vec(const linattn_shape *shape, const void *q, const void *k, const void *v,
                               const float *log_gate, void *o, const float *init_state, float *final_state,
-                              void *stream);
+                              void *workspace, size_t workspace_bytes, void *stream);
 
 /* Backward of linattn_fwd_gated_vec for an upstream gradient dO and the
  * gradient d_final_state arriving at the final state (or NULL): dq, dk, dv,
  * d_init_state = diag(alpha_0) R_0 (R the state gradient), and the gradient of
  * every log-gate ([B,H,T,d] fp32, contiguous)
  *   d_log_gate[t][i] = sum_{u >= t} (q_u[i] dq_u[i] - k_u[i] dk_u[i]) + sum_j D[i][j] S_final[i][j].
- * The forward states are recomputed from init_state.  Returns a status. */
+ * The forward states are recomputed from init_state.  Workspace:
+ * LINATTN_OP_BWD_GATED_VEC bytes.  Returns a status. */
 int32_t linattn_bwd_gated_vec(const linattn_shape *shape, const void *q, const void *k, const void *v,
                               const void *dO, const float *log_gate, const float *init_state,
                               const float *d_final_state, void *dq, void *dk, void *dv, float *d_log_gate,
-                              float *d_init_state, void *stream);
+                              float *d_init_state, void *workspace, size_t workspace_bytes, void *stream);
 
 /* Recurrent decode of T new tokens per sequence (constant-memory inference:
  * LASP-2 page, abstract): for t = 0..T-1

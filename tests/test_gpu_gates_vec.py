@@ -6,7 +6,8 @@ Tolerances: fp32 inputs 1e-4 of max|ref| (one fp32 walk per sequence); bf16 inpu
 1e-2 (outputs rounded to bf16; the oracle sees the same bf16 inputs), the fp32
 log-gate gradient and states 1e-3.  Cases: d = 64 and 128, several heads, ragged
 lengths, an initial state and a final-state gradient, padded strides, shared gates
-(every dimension the token's gate) against the per-token gated entry points, T = 0.
+(every dimension the token's gate) against the per-token gated entry points, T = 0,
+and sequences long enough to be cut into chunk groups joined by per-row scans.
 """
 import numpy as np
 import pytest
@@ -115,3 +116,30 @@ def test_gated_vec_empty_sequence():
     torch.cuda.synchronize()
     assert o.numel() == 0
     assert torch.equal(fin, init) and torch.equal(dinit, D)
+
+
+@pytest.mark.parametrize("d,dtype,B,H,T,lo", [(128, torch.bfloat16, 1, 2, 3000, -0.2), (64, torch.float32, 2, 3, 2500, -0.5),
+                                              (128, torch.float32, 1, 1, 1025, -2.0), (64, torch.bfloat16, 1, 4, 4096, -0.05)])
+def test_gated_vec_chunk_groups(d, dtype, B, H, T, lo):
+    """Sequences long enough to be cut into chunk groups (one CTA per group and sequence,
+    the groups joined by scans with per-row multipliers), ragged last groups, an initial
+    state and a final-state gradient, against the oracle."""
+    q, k, v, dO, lg, init, D = case(T + d + 5, B, H, T, d, dtype, lo=lo)
+    cu = [x.cuda() for x in (q, k, v, dO, lg, init, D)]
+    la.linattn_timing_enable(True)
+    la.linattn_timing_collect()
+    o, fin = la.fwd_gated_vec(cu[0], cu[1], cu[2], cu[4], init_state=cu[5], want_final=True)
+    dq, dk, dv, dlg, dinit = la.bwd_gated_vec(cu[0], cu[1], cu[2], cu[3], cu[4], init_state=cu[5], d_final=cu[6],
+                                              want_dinit=True)
+    torch.cuda.synchronize()
+    kinds = la.linattn_timing_collect()
+    la.linattn_timing_enable(False)
+    assert kinds["gated_vec_fwd"][0] >= 3 + 2, kinds  # aggregates, scan, outputs (forward), aggregates, scan (backward)
+    n = lambda x: x.double().numpy()
+    ro, rfin = oracle.fwd_gated_vec(n(q), n(k), n(v), n(lg), init=n(init))
+    rq, rk, rv, rlg, rinit = oracle.bwd_gated_vec(n(q), n(k), n(v), n(dO), n(lg), init=n(init), d_final=n(D))
+    tol = 1e-4 if dtype == torch.float32 else 1e-2
+    stol = 1e-4 if dtype == torch.float32 else 1e-3
+    for name, got, ref, t in (("o", o, ro, tol), ("final", fin, rfin, stol), ("dq", dq, rq, tol), ("dk", dk, rk, tol),
+                              ("dv", dv, rv, tol), ("d_log_gate", dlg, rlg, stol), ("d_init", dinit, rinit, stol)):
+        assert rel(got, ref) < t, (name, rel(got, ref))

@@ -12,6 +12,8 @@ A "step" is one pass of the whole hot path over one batch of synthetic input:
       per-segment forward from those states; the single unsegmented forward of
       the same sequence is timed in the same run (`single_fwd`);
   workload 6: B=1 H=32 T=131072 with per-token gates, forward + backward.
+  workload 7: B=2 H=16 T=65536 d=64 bf16, forward + backward (the d = 128 kernels
+    as the zero-padded problem).
 
 Prints ONE JSON line.
 
@@ -269,15 +271,22 @@ def passes(cfg) -> str:
 
 
 def step_units(cfg):
-    """(algorithmic FLOP, algorithmic bytes) per token-head of one step of the workload."""
+    """(algorithmic FLOP, algorithmic bytes) per token-head of one step of the workload.
+
+    The constants above are for d = 128; bytes scale with d (bf16 rows of d), and
+    FLOPs are 4 C d (the masked intra-chunk products) + 4 d^2 (the state products)
+    per pass, the backward twice the forward."""
     gated = cfg.get("gates") is not None
     p = passes(cfg)
+    d = cfg["d"]
+    fs = (4 * 64 * d + 4 * d * d) / FLOP_FWD  # 1 at d = 128
+    bs = d / 128
     if p == "fwd":
-        return FLOP_FWD, BYTES_FWD
+        return FLOP_FWD * fs, BYTES_FWD * bs
     if p == "segments":
-        return FLOP_FWD, BYTES_SEGMENTS
+        return FLOP_FWD * fs, BYTES_SEGMENTS * bs
     # gates add a 4-byte log-gate read to each pass and the 4-byte gate gradient written
-    return FLOP_FWD + FLOP_BWD, BYTES_FWD + BYTES_BWD + (12 if gated else 0)
+    return (FLOP_FWD + FLOP_BWD) * fs, (BYTES_FWD + BYTES_BWD) * bs + (12 if gated else 0)
 
 
 def step_name(cfg) -> str:
@@ -569,8 +578,9 @@ def run_ours(args):
         e = {"launches_per_step": n / n_break, "ms_per_step": t / n_break}
         if k in KIND_IO_BYTES_PER_TOKEN_HEAD and t > 0 and k != "tc_segment_aggregate":
             # bytes the kernel's own sequence-tensor inputs and outputs take per token-head
-            e["io_bytes_per_token_head"] = KIND_IO_BYTES_PER_TOKEN_HEAD[k]
-            e["io_gbs"] = KIND_IO_BYTES_PER_TOKEN_HEAD[k] * tok_heads * n / (t * 1e-3) / 1e9
+            io = KIND_IO_BYTES_PER_TOKEN_HEAD[k] * d / 128
+            e["io_bytes_per_token_head"] = io
+            e["io_gbs"] = io * tok_heads * n / (t * 1e-3) / 1e9
         breakdown[k] = e
     ms_kernels = sum(t for _, t in kernels.values()) / n_break
     traffic = _traffic(cfg["name"]) if not (args.B or args.T) else None

@@ -39,6 +39,10 @@ WORKLOADS = {
     6: dict(name="fwdbwd-gated-B1H32T128K-d128", B=1, H=32, T=131072, d=128, dtype="bf16",
             decay=None, dist="normal", sigma=1.0 / math.sqrt(128), seed=5, passes="fwd+bwd",
             gates=(-1.0 / 16, 0.0)),
+    # the benchmark's shape with heads of 64 (bf16: the d = 128 tensor-core kernels as the
+    # zero-padded problem)
+    7: dict(name="fwdbwd-B2H16T64K-d64", B=2, H=16, T=65536, d=64, dtype="bf16", decay=None,
+            dist="normal", sigma=1.0 / math.sqrt(64), seed=6, passes="fwd+bwd"),
 }
 
 

@@ -655,9 +655,9 @@ __global__ void __launch_bounds__(kBwThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (the whole warp)
-    // Per step n (one Y tile pair):  dK/dV:  dP(n), dV(n), S(n+1), dK(n);  dQ:  dP(n), S(n+1),
-    // dQ(n).  The products of step n run while the elementwise warps form its p and ds, and
-    // the next tile's scores run while they form its ds; S(0) of an item opens its first step.
+    // Per step n (one query tile): dP(n), dV(n), S(n+1), dK(n).  The products of step n run
+    // while the elementwise warps form its p and ds, and the next tile's scores run while
+    // they form its ds; S(0) of an item opens its first step.
     // The products read the bf16 p and ds from TMEM right where the elementwise warps
     // wrote them, so every product that overwrites a score tile is issued after the one
     // that reads it (the products of a CTA run in issue order).

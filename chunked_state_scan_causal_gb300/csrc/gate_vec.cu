@@ -30,17 +30,84 @@
 namespace linattn {
 namespace {
 
-constexpr int kVecThreads = 256;
+constexpr int kVecThreads = 256, kVecWarps = kVecThreads / 32;
+constexpr int kVecChunk = 8;  // tokens staged in shared memory per step of a walk
 
-__device__ __forceinline__ float ld_val(const float *p) { return *p; }
-__device__ __forceinline__ float ld_val(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
 __device__ __forceinline__ void st_val(float *p, float x) { *p = x; }
 __device__ __forceinline__ void st_val(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
 
-// shared memory: the state [D][D+1], five vectors of D, two partial-sum buffers of kVecThreads
+// Two fp32 lanes per instruction (the packed f32x2 forms of sm_100 and later); each
+// lane rounds exactly as the scalar instruction does.
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 dup2(float x) { return make_float2(x, x); }
+__device__ __forceinline__ float2 ld2(const float *p) { return *reinterpret_cast<const float2 *>(p); }
+__device__ __forceinline__ void st2(float *p, float2 x) { *reinterpret_cast<float2 *>(p) = x; }
+
+// Two consecutive input elements, held raw between their global load and their
+// staging (the pointers and strides are 16-byte aligned and the index is even).
+template <typename T>
+struct PairOf;
+template <>
+struct PairOf<float> {
+  using type = float2;
+};
+template <>
+struct PairOf<__nv_bfloat16> {
+  using type = __nv_bfloat162;
+};
+__device__ __forceinline__ void ld_raw(float2 &r, const float *p) { r = *reinterpret_cast<const float2 *>(p); }
+__device__ __forceinline__ void ld_raw(__nv_bfloat162 &r, const __nv_bfloat16 *p) {
+  r = *reinterpret_cast<const __nv_bfloat162 *>(p);
+}
+__device__ __forceinline__ void zero_raw(float2 &r) { r = make_float2(0.f, 0.f); }
+__device__ __forceinline__ void zero_raw(__nv_bfloat162 &r) { r = __floats2bfloat162_rn(0.f, 0.f); }
+__device__ __forceinline__ float2 to_f2(float2 x) { return x; }
+__device__ __forceinline__ float2 to_f2(__nv_bfloat162 x) { return __bfloat1622float2(x); }
+
+// The sum of x[c] over the 32 lanes of a warp, scattered over the lanes: lane l returns
+// the total of value l >> (5 - log2 N), the lanes with equal high bits holding the same
+// total.  Each halving step sends half of the values still held to the partner lane.
+template <int N>
+__device__ __forceinline__ float lanes_reduce_scatter(float (&x)[N], int lane) {
+  static_assert(N >= 2 && N <= 32 && (N & (N - 1)) == 0, "a power of two up to 32 values");
+#pragma unroll
+  for (int half = N / 2, off = 16; half >= 1; half /= 2, off /= 2) {
+    const bool up = lane & off;
+#pragma unroll
+    for (int m = 0; m < half; ++m) {
+      const float send = up ? x[m] : x[m + half], keep = up ? x[m + half] : x[m];
+      x[m] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+    }
+  }
+  constexpr int kLog = N == 2 ? 1 : N == 4 ? 2 : N == 8 ? 3 : N == 16 ? 4 : 5;
+#pragma unroll
+  for (int off = 16 >> kLog; off >= 1; off /= 2) x[0] += __shfl_xor_sync(0xffffffffu, x[0], off);
+  return x[0];
+}
+
+// shared memory of a walk: `vectors` staged vectors of kVecChunk x D, the per-warp
+// partial sums [kVecChunk][kVecWarps][D] (when it reduces across warps) and kVecThreads pairs
 template <int D>
-constexpr size_t vec_smem() {
-  return sizeof(float) * ((size_t)D * (D + 1) + 5 * D + 2 * kVecThreads);
+constexpr size_t vec_smem(int vectors, bool partial) {
+  return sizeof(float) * ((size_t)vectors * kVecChunk * D + (partial ? (size_t)kVecChunk * kVecWarps * D : 0) +
+                          2 * kVecThreads);
 }
 
 // Chunk groups of L tokens (the last one shorter): CTA (bh, g) walks tokens [g L, min(T, (g+1) L)).
@@ -50,95 +117,212 @@ struct VecGroups {
   __device__ int end(int g, int T) const { return min(T, (g + 1) * L); }
 };
 
+// The staged inputs of a walk.  Every kVecChunk tokens the CTA writes the pairs its
+// threads fetched into shared memory as fp32 (the gates as alpha = exp(log_gate)),
+// then fetches the next kVecChunk tokens' pairs into registers while it walks these.
+// Thread tid holds pairs 2 (tid + kVecThreads m) of the chunk's kVecChunk x D
+// elements, always the same two key dimensions 2 tid mod D.
+template <int D, typename TIn, int NV>
+struct VecStage {
+  using Raw = typename PairOf<TIn>::type;
+  static constexpr int kPairs = kVecChunk * D / (2 * kVecThreads);
+  Raw x[NV][kPairs];
+  float2 lg[kPairs];
+  // the first NV of src; token tt of the chunk is time t = tb + dir * tt; its gate is
+  // the log-gate at time t + gshift (0 at or past t1); tokens outside [t0, t1) are zero
+  __device__ void fetch(const TIn *const *src, int64_t base, int64_t st, const float *g, int tb, int dir,
+                        int gshift, int t0, int t1) {
+#pragma unroll
+    for (int m = 0; m < kPairs; ++m) {
+      const int e = 2 * (threadIdx.x + kVecThreads * m), t = tb + dir * (e / D), i = e % D;
+      if (t >= t0 && t < t1) {
+        const int64_t row = base + (int64_t)t * st + i;
+#pragma unroll
+        for (int n = 0; n < NV; ++n) ld_raw(x[n][m], src[n] + row);
+        const int tg = t + gshift;
+        lg[m] = tg < t1 ? ld2(g + (int64_t)tg * D + i) : make_float2(0.f, 0.f);
+      } else {
+#pragma unroll
+        for (int n = 0; n < NV; ++n) zero_raw(x[n][m]);
+        lg[m] = make_float2(0.f, 0.f);
+      }
+    }
+  }
+  // the vectors to dst[n], alpha to alpha; returns this thread's sum of the log-gates
+  __device__ float2 store(float *const *dst, float *alpha) const {
+    float2 sum = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int m = 0; m < kPairs; ++m) {
+      const int e = 2 * (threadIdx.x + kVecThreads * m);
+#pragma unroll
+      for (int n = 0; n < NV; ++n) st2(dst[n] + e, to_f2(x[n][m]));
+      st2(alpha + e, make_float2(expf(lg[m].x), expf(lg[m].y)));
+      sum.x += lg[m].x;
+      sum.y += lg[m].y;
+    }
+    return sum;
+  }
+};
+
 // Forward walk of group g = blockIdx.y of sequence bh = blockIdx.x from its entering
-// state (init [G][BH][D][D], or zero), with the outputs o (or none), the group's last
-// state (fin [G][BH][D][D], or none) and the sums of its log-gates per key dimension
-// (gsum [G][BH][D], or none).
-template <int D, typename TIn>
-__global__ void __launch_bounds__(kVecThreads) vec_fwd_kernel(Problem p, VecGroups gr, const TIn *q, const TIn *k,
-                                                             const TIn *v, const float *lg, TIn *o,
-                                                             const float *init, float *fin, float *gsum) {
-  constexpr int kParts = kVecThreads / D, kSpan = D / kParts;  // row (or column) ranges per thread
+// state (init [G][BH][D][D], or zero), with the outputs o (OUT), the group's last state
+// (fin [G][BH][D][D], or none) and the sums of its log-gates per key dimension (gsum
+// [G][BH][D], or none).  The fp32 state lives in registers: warp w holds rows
+// [w D/8, (w+1) D/8), lane l columns [l D/32, (l+1) D/32), as pairs of adjacent rows;
+// o_t = S_t^T q_t sums each thread's rows and then the warps' partial sums.
+template <int D, typename TIn, bool OUT>
+__global__ void __launch_bounds__(kVecThreads, 2)
+    vec_fwd_kernel(Problem p, VecGroups gr, const TIn *q, const TIn *k, const TIn *v, const float *lg, TIn *o,
+                   const float *init, float *fin, float *gsum) {
+  constexpr int RW = D / kVecWarps, CL = D / 32, ND = kVecChunk * D, NV = OUT ? 3 : 2;
   extern __shared__ float sm[];
-  float *S = sm, *vq = S + D * (D + 1), *vk = vq + D, *va = vk + D, *vv = va + D, *part = vv + 2 * D;
-  const int tid = threadIdx.x, bh = blockIdx.x, gi = blockIdx.y, b = bh / p.H, h = bh % p.H;
+  float *sk = sm, *sv = sk + ND, *sq = sv + ND, *sa = sm + NV * ND, *part = sa + ND;
+  float *red = part + (OUT ? kVecWarps * ND : 0);
+  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, bh = blockIdx.x, gi = blockIdx.y;
+  const int b = bh / p.H, h = bh % p.H;
   const int64_t BH = (int64_t)p.B * p.H, slot = (int64_t)gi * BH + bh;
   const int64_t base = (int64_t)b * p.sb + (int64_t)h * p.sh;
   const float *g = lg + (int64_t)bh * p.T * D;
-  const int t0 = gr.start(gi), t1 = gr.end(gi, p.T);
-  for (int e = tid; e < D * D; e += kVecThreads)
-    S[(e / D) * (D + 1) + e % D] = init ? init[slot * D * D + e] : 0.f;
-  float gs = 0.f;  // this thread's key dimension: the group's sum of log-gates
-  const int c = tid % D, r0 = (tid / D) * kSpan;  // output column, first row of this thread's range
-  for (int t = t0; t < t1; ++t) {
-    const int64_t row = base + (int64_t)t * p.st;
-    if (tid < D) {
-      if (o) vq[tid] = ld_val(q + row + tid);
-      vk[tid] = ld_val(k + row + tid);
-      vv[tid] = ld_val(v + row + tid);
-      const float lgv = g[(int64_t)t * D + tid];
-      gs += lgv;
-      va[tid] = expf(lgv);
+  const int t0 = gr.start(gi), t1 = gr.end(gi, p.T), r0 = w * RW, c0 = lane * CL;
+
+  float2 s[RW / 2][CL];  // s[m][c] = (S[r0 + 2m][c0 + c], S[r0 + 2m + 1][c0 + c])
+#pragma unroll
+  for (int m = 0; m < RW / 2; ++m)
+#pragma unroll
+    for (int c = 0; c < CL; ++c) {
+      const float *src = init + slot * D * D + (int64_t)(r0 + 2 * m) * D + c0 + c;
+      s[m][c] = init ? make_float2(src[0], src[D]) : make_float2(0.f, 0.f);
     }
+
+  VecStage<D, TIn, NV> stage;
+  const TIn *const srcs[3] = {k, v, q};  // the first NV are staged
+  float *const dsts[3] = {sk, sv, sq};
+  float2 gs = make_float2(0.f, 0.f);  // the group's log-gate sums of this thread's two key dimensions
+  stage.fetch(srcs, base, p.st, g, t0, 1, 0, t0, t1);
+  for (int tc = t0; tc < t1; tc += kVecChunk) {
+    const int nt = min(kVecChunk, t1 - tc);
+    __syncthreads();  // the previous step is done with the staged vectors and the partial sums
+    const float2 add = stage.store(dsts, sa);
+    gs.x += add.x;
+    gs.y += add.y;
+    if (tc + kVecChunk < t1) stage.fetch(srcs, base, p.st, g, tc + kVecChunk, 1, 0, t0, t1);
     __syncthreads();
-    for (int e = tid; e < D * D; e += kVecThreads) {
-      const int i = e / D, j = e % D;
-      float &s = S[i * (D + 1) + j];
-      s = fmaf(va[i], s, vk[i] * vv[j]);
+    for (int tt = 0; tt < nt; ++tt) {
+      const float *ra = sa + tt * D + r0, *rk = sk + tt * D + r0, *rq = sq + tt * D + r0;
+      float2 vv[CL], acc[CL];
+#pragma unroll
+      for (int c = 0; c < CL; ++c) {
+        vv[c] = dup2(sv[tt * D + c0 + c]);
+        acc[c] = make_float2(0.f, 0.f);
+      }
+#pragma unroll
+      for (int m = 0; m < RW / 2; ++m) {
+        const float2 a = ld2(ra + 2 * m), kk = ld2(rk + 2 * m);
+#pragma unroll
+        for (int c = 0; c < CL; ++c) s[m][c] = fma2(a, s[m][c], mul2(kk, vv[c]));
+        if (OUT) {
+          const float2 qq = ld2(rq + 2 * m);
+#pragma unroll
+          for (int c = 0; c < CL; ++c) acc[c] = fma2(qq, s[m][c], acc[c]);
+        }
+      }
+      if (OUT) {
+#pragma unroll
+        for (int c = 0; c < CL; ++c) part[(tt * kVecWarps + w) * D + c0 + c] = acc[c].x + acc[c].y;
+      }
     }
-    __syncthreads();
-    if (o) {
-      float acc = 0.f;
-#pragma unroll 8
-      for (int i = r0; i < r0 + kSpan; ++i) acc = fmaf(S[i * (D + 1) + c], vq[i], acc);
-      part[tid] = acc;
+    if (OUT) {
       __syncthreads();
-      if (tid < D) {
+      for (int e = tid; e < nt * D; e += kVecThreads) {
+        const int tt = e / D, j = e % D;
         float x = 0.f;
 #pragma unroll
-        for (int m = 0; m < kParts; ++m) x += part[m * D + tid];
-        st_val(o + row + tid, x);
+        for (int u = 0; u < kVecWarps; ++u) x += part[(tt * kVecWarps + u) * D + j];
+        st_val(o + base + (int64_t)(tc + tt) * p.st + j, x);
       }
     }
   }
   if (fin) {
-    __syncthreads();
-    for (int e = tid; e < D * D; e += kVecThreads) fin[slot * D * D + e] = S[(e / D) * (D + 1) + e % D];
+#pragma unroll
+    for (int m = 0; m < RW / 2; ++m)
+#pragma unroll
+      for (int c = 0; c < CL; ++c) {
+        float *dst = fin + slot * D * D + (int64_t)(r0 + 2 * m) * D + c0 + c;
+        dst[0] = s[m][c].x;
+        dst[D] = s[m][c].y;
+      }
   }
-  if (gsum && tid < D) gsum[slot * D + tid] = gs;
+  if (gsum) {
+    // threads tid = u D/2 + n (u < 2 kVecThreads / D) hold key dimensions 2n and 2n + 1
+    reinterpret_cast<float2 *>(red)[tid] = gs;
+    __syncthreads();
+    if (tid < D / 2) {
+      float2 x = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int u = 0; u < 2 * kVecThreads / D; ++u) {
+        const float2 y = reinterpret_cast<const float2 *>(red)[tid + u * D / 2];
+        x.x += y.x;
+        x.y += y.y;
+      }
+      st2(gsum + slot * D + 2 * tid, x);
+    }
+  }
 }
 
 // The reverse aggregate of group g = blockIdx.y of sequence bh = blockIdx.x:
 //   W_g = sum_{t in g} diag(alpha_start .. alpha_t) q_t dO_t^T,
-// walked backward (A <- diag(alpha_t) (A + q_t dO_t^T)), into W [G][BH][D][D].
+// walked backward (A <- diag(alpha_t) (A + q_t dO_t^T)), into W [G][BH][D][D].  The
+// state lives in registers: warp w holds columns [w D/8, (w+1) D/8), lane l rows
+// [l D/32, (l+1) D/32), as pairs of adjacent columns.
 template <int D, typename TIn>
-__global__ void __launch_bounds__(kVecThreads) vec_ragg_kernel(Problem p, VecGroups gr, const TIn *q,
-                                                              const TIn *dO, const float *lg, float *W) {
+__global__ void __launch_bounds__(kVecThreads, 2)
+    vec_ragg_kernel(Problem p, VecGroups gr, const TIn *q, const TIn *dO, const float *lg, float *W) {
+  constexpr int CW = D / kVecWarps, RL = D / 32, ND = kVecChunk * D;
   extern __shared__ float sm[];
-  float *A = sm, *vq = A + D * (D + 1), *vg = vq + D, *va = vg + D;
-  const int tid = threadIdx.x, bh = blockIdx.x, gi = blockIdx.y, b = bh / p.H, h = bh % p.H;
+  float *sq = sm, *sg = sq + ND, *sa = sg + ND;
+  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, bh = blockIdx.x, gi = blockIdx.y;
+  const int b = bh / p.H, h = bh % p.H;
   const int64_t BH = (int64_t)p.B * p.H, slot = (int64_t)gi * BH + bh;
   const int64_t base = (int64_t)b * p.sb + (int64_t)h * p.sh;
   const float *g = lg + (int64_t)bh * p.T * D;
-  const int t0 = gr.start(gi), t1 = gr.end(gi, p.T);
-  for (int e = tid; e < D * D; e += kVecThreads) A[(e / D) * (D + 1) + e % D] = 0.f;
-  for (int t = t1 - 1; t >= t0; --t) {
-    const int64_t row = base + (int64_t)t * p.st;
-    __syncthreads();  // the previous token's update has read the vectors
-    if (tid < D) {
-      vq[tid] = ld_val(q + row + tid);
-      vg[tid] = ld_val(dO + row + tid);
-      va[tid] = expf(g[(int64_t)t * D + tid]);
-    }
+  const int t0 = gr.start(gi), t1 = gr.end(gi, p.T), r0 = lane * RL, c0 = w * CW;
+
+  float2 s[RL][CW / 2];  // s[r][n] = (A[r0 + r][c0 + 2n], A[r0 + r][c0 + 2n + 1])
+#pragma unroll
+  for (int r = 0; r < RL; ++r)
+#pragma unroll
+    for (int n = 0; n < CW / 2; ++n) s[r][n] = make_float2(0.f, 0.f);
+
+  VecStage<D, TIn, 2> stage;
+  const TIn *const srcs[2] = {q, dO};
+  float *const dsts[2] = {sq, sg};
+  // token tt of a step is time hi - 1 - tt
+  stage.fetch(srcs, base, p.st, g, t1 - 1, -1, 0, t0, t1);
+  for (int hi = t1; hi > t0; hi -= kVecChunk) {
+    const int nt = min(kVecChunk, hi - t0);
     __syncthreads();
-    for (int e = tid; e < D * D; e += kVecThreads) {
-      const int i = e / D, j = e % D;
-      float &a = A[i * (D + 1) + j];
-      a = va[i] * fmaf(vq[i], vg[j], a);
+    stage.store(dsts, sa);
+    if (hi - kVecChunk > t0) stage.fetch(srcs, base, p.st, g, hi - kVecChunk - 1, -1, 0, t0, t1);
+    __syncthreads();
+    for (int tt = 0; tt < nt; ++tt) {
+      float2 ad[RL], qd[RL];
+#pragma unroll
+      for (int r = 0; r < RL; ++r) {
+        ad[r] = dup2(sa[tt * D + r0 + r]);
+        qd[r] = dup2(sq[tt * D + r0 + r]);
+      }
+#pragma unroll
+      for (int n = 0; n < CW / 2; ++n) {
+        const float2 dp = ld2(sg + tt * D + c0 + 2 * n);
+#pragma unroll
+        for (int r = 0; r < RL; ++r) s[r][n] = mul2(ad[r], fma2(qd[r], dp, s[r][n]));
+      }
     }
   }
-  __syncthreads();
-  for (int e = tid; e < D * D; e += kVecThreads) W[slot * D * D + e] = A[(e / D) * (D + 1) + e % D];
+#pragma unroll
+  for (int r = 0; r < RL; ++r)
+#pragma unroll
+    for (int n = 0; n < CW / 2; ++n) st2(W + slot * D * D + (int64_t)(r0 + r) * D + c0 + 2 * n, s[r][n]);
 }
 
 // The scans across groups, one thread per (sequence, state element (i, j)), with the
@@ -164,125 +348,175 @@ __global__ void __launch_bounds__(256) vec_scan_kernel(int G, int64_t BH, int D,
 
 // Backward of group g = blockIdx.y of sequence bh = blockIdx.x from its entering state
 // (init [G][BH][D][D], or zero) and the gradient arriving at its last state (dfin
-// [G][BH][D][D], or zero); d_init from group 0.
+// [G][BH][D][D], or zero); d_init from group 0.  S and then R live in registers as in
+// the reverse aggregate (warp: columns, lane: rows).  dq_t = S_t dO_t and dk_t = R_t v_t
+// sum each thread's columns and then the warps' partial sums; dv_t = R_t^T k_t sums
+// each thread's rows and then the warp's lanes.
 template <int D, typename TIn>
-__global__ void __launch_bounds__(kVecThreads) vec_bwd_kernel(Problem p, VecGroups gr, const TIn *q, const TIn *k,
-                                                             const TIn *v, const TIn *dO, const float *lg,
-                                                             const float *init, const float *dfin, TIn *dq,
-                                                             TIn *dk, TIn *dv, float *dlg, float *dinit) {
-  constexpr int kParts = kVecThreads / D, kSpan = D / kParts;
+__global__ void __launch_bounds__(kVecThreads, 2)
+    vec_bwd_kernel(Problem p, VecGroups gr, const TIn *q, const TIn *k, const TIn *v, const TIn *dO,
+                   const float *lg, const float *init, const float *dfin, TIn *dq, TIn *dk, TIn *dv, float *dlg,
+                   float *dinit) {
+  constexpr int CW = D / kVecWarps, RL = D / 32, ND = kVecChunk * D;
   extern __shared__ float sm[];
-  float *S = sm, *vq = S + D * (D + 1), *vk = vq + D, *va = vk + D, *vv = va + D, *vg = vv + D;
-  float *partA = vg + D, *partB = partA + kVecThreads;
-  const int tid = threadIdx.x, bh = blockIdx.x, gi = blockIdx.y, b = bh / p.H, h = bh % p.H;
+  float *sq = sm, *sk = sq + ND, *sv = sk + ND, *sg = sv + ND, *sa = sg + ND, *part = sa + ND;
+  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, bh = blockIdx.x, gi = blockIdx.y;
+  const int b = bh / p.H, h = bh % p.H;
   const int64_t BH = (int64_t)p.B * p.H, slot = (int64_t)gi * BH + bh;
   const int64_t base = (int64_t)b * p.sb + (int64_t)h * p.sh;
   const float *g = lg + (int64_t)bh * p.T * D;
   float *dg = dlg + (int64_t)bh * p.T * D;
-  const int t0 = gr.start(gi), t1 = gr.end(gi, p.T);
-  const int c = tid % D, r0 = (tid / D) * kSpan;  // this thread's row / column and its range of the other index
+  const int t0 = gr.start(gi), t1 = gr.end(gi, p.T), r0 = lane * RL, c0 = w * CW;
+
+  float2 s[RL][CW / 2];  // s[r][n] = (S[r0 + r][c0 + 2n], S[r0 + r][c0 + 2n + 1])
+#pragma unroll
+  for (int r = 0; r < RL; ++r)
+#pragma unroll
+    for (int n = 0; n < CW / 2; ++n)
+      s[r][n] = init ? ld2(init + slot * D * D + (int64_t)(r0 + r) * D + c0 + 2 * n) : make_float2(0.f, 0.f);
+
+  VecStage<D, TIn, 4> stage;
+  const TIn *const srcs[4] = {q, k, v, dO};
+  float *const dsts[4] = {sq, sk, sv, sg};
 
   // forward sweep: S_t, dq_t = S_t dO_t, and q_t[i] dq_t[i] into d_log_gate
-  for (int e = tid; e < D * D; e += kVecThreads)
-    S[(e / D) * (D + 1) + e % D] = init ? init[slot * D * D + e] : 0.f;
-  for (int t = t0; t < t1; ++t) {
-    const int64_t row = base + (int64_t)t * p.st;
-    if (tid < D) {
-      vq[tid] = ld_val(q + row + tid);
-      vk[tid] = ld_val(k + row + tid);
-      vv[tid] = ld_val(v + row + tid);
-      vg[tid] = ld_val(dO + row + tid);
-      va[tid] = expf(g[(int64_t)t * D + tid]);
+  stage.fetch(srcs, base, p.st, g, t0, 1, 0, t0, t1);
+  for (int tc = t0; tc < t1; tc += kVecChunk) {
+    const int nt = min(kVecChunk, t1 - tc);
+    __syncthreads();
+    stage.store(dsts, sa);
+    if (tc + kVecChunk < t1) stage.fetch(srcs, base, p.st, g, tc + kVecChunk, 1, 0, t0, t1);
+    __syncthreads();
+    for (int tt = 0; tt < nt; ++tt) {
+      float2 ad[RL], kd[RL], acc[RL];
+#pragma unroll
+      for (int r = 0; r < RL; ++r) {
+        ad[r] = dup2(sa[tt * D + r0 + r]);
+        kd[r] = dup2(sk[tt * D + r0 + r]);
+        acc[r] = make_float2(0.f, 0.f);
+      }
+#pragma unroll
+      for (int n = 0; n < CW / 2; ++n) {
+        const float2 vp = ld2(sv + tt * D + c0 + 2 * n), dp = ld2(sg + tt * D + c0 + 2 * n);
+#pragma unroll
+        for (int r = 0; r < RL; ++r) {
+          s[r][n] = fma2(ad[r], s[r][n], mul2(kd[r], vp));
+          acc[r] = fma2(s[r][n], dp, acc[r]);
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < RL; ++r) part[(tt * kVecWarps + w) * D + r0 + r] = acc[r].x + acc[r].y;
     }
     __syncthreads();
-    for (int e = tid; e < D * D; e += kVecThreads) {
-      const int i = e / D, j = e % D;
-      float &s = S[i * (D + 1) + j];
-      s = fmaf(va[i], s, vk[i] * vv[j]);
-    }
-    __syncthreads();
-    float acc = 0.f;  // row c of S against dO over this thread's column range
-#pragma unroll 8
-    for (int j = r0; j < r0 + kSpan; ++j) acc = fmaf(S[c * (D + 1) + j], vg[j], acc);
-    partA[tid] = acc;
-    __syncthreads();
-    if (tid < D) {
+    for (int e = tid; e < nt * D; e += kVecThreads) {
+      const int tt = e / D, i = e % D;
       float x = 0.f;
 #pragma unroll
-      for (int m = 0; m < kParts; ++m) x += partA[m * D + tid];
-      st_val(dq + row + tid, x);
-      dg[(int64_t)t * D + tid] = vq[tid] * x;
+      for (int u = 0; u < kVecWarps; ++u) x += part[(tt * kVecWarps + u) * D + i];
+      st_val(dq + base + (int64_t)(tc + tt) * p.st + i, x);
+      dg[(int64_t)(tc + tt) * D + i] = sq[tt * D + i] * x;
     }
   }
-  __syncthreads();
-  // the group's last state's term of the log-gate gradient (row tid), then R from dfin
-  float gacc = 0.f;
-  if (tid < D && dfin) {
-    const float *Dr = dfin + slot * D * D + (int64_t)tid * D;
-    for (int j = 0; j < D; ++j) gacc = fmaf(Dr[j], S[tid * (D + 1) + j], gacc);
-  }
-  __syncthreads();
-  for (int e = tid; e < D * D; e += kVecThreads)
-    S[(e / D) * (D + 1) + e % D] = dfin ? dfin[slot * D * D + e] : 0.f;
 
-  // reverse sweep
-  for (int t = t1 - 1; t >= t0; --t) {
-    const int64_t row = base + (int64_t)t * p.st;
-    if (tid < D) {
-      vq[tid] = ld_val(q + row + tid);
-      vk[tid] = ld_val(k + row + tid);
-      vv[tid] = ld_val(v + row + tid);
-      vg[tid] = ld_val(dO + row + tid);
-      va[tid] = t == t1 - 1 ? 1.f : expf(g[(int64_t)(t + 1) * D + tid]);  // the carry alpha_{t+1}
-    }
-    __syncthreads();
-    for (int e = tid; e < D * D; e += kVecThreads) {
-      const int i = e / D, j = e % D;
-      float &s = S[i * (D + 1) + j];
-      s = fmaf(va[i], s, vq[i] * vg[j]);
-    }
-    __syncthreads();
-    float a = 0.f, bsum = 0.f;  // dk: row c against v; dv: column c against k
-#pragma unroll 8
-    for (int m = r0; m < r0 + kSpan; ++m) {
-      a = fmaf(S[c * (D + 1) + m], vv[m], a);
-      bsum = fmaf(S[m * (D + 1) + c], vk[m], bsum);
-    }
-    partA[tid] = a;
-    partB[tid] = bsum;
-    __syncthreads();
-    if (tid < D) {
-      float x = 0.f, y = 0.f;
+  // the group's last state's term of the log-gate gradient (row i: sum_j Dfin[i][j]
+  // S_end[i][j]), then R from Dfin
+  {
+    float2 acc[RL];
 #pragma unroll
-      for (int m = 0; m < kParts; ++m) {
-        x += partA[m * D + tid];
-        y += partB[m * D + tid];
+    for (int r = 0; r < RL; ++r) {
+      acc[r] = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int n = 0; n < CW / 2; ++n) {
+        const float2 df =
+            dfin ? ld2(dfin + slot * D * D + (int64_t)(r0 + r) * D + c0 + 2 * n) : make_float2(0.f, 0.f);
+        acc[r] = fma2(df, s[r][n], acc[r]);
+        s[r][n] = df;
       }
-      st_val(dk + row + tid, x);
-      st_val(dv + row + tid, y);
-      gacc += dg[(int64_t)t * D + tid] - vk[tid] * x;
-      dg[(int64_t)t * D + tid] = gacc;
+    }
+    __syncthreads();  // the last step's sums are read
+#pragma unroll
+    for (int r = 0; r < RL; ++r) part[w * D + r0 + r] = acc[r].x + acc[r].y;
+    __syncthreads();
+  }
+  float gacc = 0.f;  // key dimension tid's running log-gate gradient
+  if (tid < D) {
+#pragma unroll
+    for (int u = 0; u < kVecWarps; ++u) gacc += part[u * D + tid];
+  }
+
+  // reverse sweep, R_t = diag(alpha_{t+1}) R_{t+1} + q_t dO_t^T; token tt of a step is time hi - 1 - tt
+  constexpr int kLowBits = 5 - (CW == 8 ? 3 : 4);  // lanes sharing one column total of dv
+  stage.fetch(srcs, base, p.st, g, t1 - 1, -1, 1, t0, t1);
+  for (int hi = t1; hi > t0; hi -= kVecChunk) {
+    const int nt = min(kVecChunk, hi - t0);
+    __syncthreads();
+    stage.store(dsts, sa);
+    if (hi - kVecChunk > t0) stage.fetch(srcs, base, p.st, g, hi - kVecChunk - 1, -1, 1, t0, t1);
+    __syncthreads();
+    for (int tt = 0; tt < nt; ++tt) {
+      const int t = hi - 1 - tt;
+      float2 ad[RL], qd[RL], kd[RL], dka[RL];
+#pragma unroll
+      for (int r = 0; r < RL; ++r) {
+        ad[r] = dup2(sa[tt * D + r0 + r]);
+        qd[r] = dup2(sq[tt * D + r0 + r]);
+        kd[r] = dup2(sk[tt * D + r0 + r]);
+        dka[r] = make_float2(0.f, 0.f);
+      }
+      float dva[CW];
+#pragma unroll
+      for (int n = 0; n < CW / 2; ++n) {
+        const float2 vp = ld2(sv + tt * D + c0 + 2 * n), dp = ld2(sg + tt * D + c0 + 2 * n);
+        float2 col = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int r = 0; r < RL; ++r) {
+          s[r][n] = fma2(ad[r], s[r][n], mul2(qd[r], dp));
+          dka[r] = fma2(s[r][n], vp, dka[r]);
+          col = fma2(s[r][n], kd[r], col);
+        }
+        dva[2 * n] = col.x;
+        dva[2 * n + 1] = col.y;
+      }
+#pragma unroll
+      for (int r = 0; r < RL; ++r) part[(tt * kVecWarps + w) * D + r0 + r] = dka[r].x + dka[r].y;
+      const float x = lanes_reduce_scatter<CW>(dva, lane);
+      if ((lane & ((1 << kLowBits) - 1)) == 0)
+        st_val(dv + base + (int64_t)t * p.st + c0 + (lane >> kLowBits), x);
+    }
+    __syncthreads();
+    if (tid < D) {
+      for (int tt = 0; tt < nt; ++tt) {
+        const int t = hi - 1 - tt;
+        float x = 0.f;
+#pragma unroll
+        for (int u = 0; u < kVecWarps; ++u) x += part[(tt * kVecWarps + u) * D + tid];
+        st_val(dk + base + (int64_t)t * p.st + tid, x);
+        gacc += dg[(int64_t)t * D + tid] - sk[tt * D + tid] * x;
+        dg[(int64_t)t * D + tid] = gacc;
+      }
     }
   }
   if (dinit && gi == 0) {
-    __syncthreads();
-    for (int e = tid; e < D * D; e += kVecThreads) {
-      const int i = e / D;
-      const float a0 = t1 > t0 ? expf(g[(int64_t)t0 * D + i]) : 1.f;
-      dinit[(int64_t)bh * D * D + e] = a0 * S[i * (D + 1) + e % D];
+#pragma unroll
+    for (int r = 0; r < RL; ++r) {
+      const float a0 = t1 > t0 ? expf(g[(int64_t)t0 * D + r0 + r]) : 1.f;
+#pragma unroll
+      for (int n = 0; n < CW / 2; ++n)
+        st2(dinit + (int64_t)bh * D * D + (int64_t)(r0 + r) * D + c0 + 2 * n, mul2(dup2(a0), s[r][n]));
     }
   }
 }
 
-template <int D, typename TIn>
+template <int D, typename TIn, bool OUT>
 cudaError_t launch_vec_fwd(const Problem &p, VecGroups gr, const void *q, const void *k, const void *v,
                            const float *lg, void *o, const float *init, float *fin, float *gsum, cudaStream_t s) {
-  auto kern = vec_fwd_kernel<D, TIn>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)vec_smem<D>());
+  auto kern = vec_fwd_kernel<D, TIn, OUT>;
+  const size_t smem = vec_smem<D>(OUT ? 4 : 3, OUT);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   TimedLaunch t(K_GATED_VEC_FWD, s);
-  kern<<<dim3(p.B * p.H, gr.G), kVecThreads, vec_smem<D>(), s>>>(p, gr, (const TIn *)q, (const TIn *)k,
-                                                                 (const TIn *)v, lg, (TIn *)o, init, fin, gsum);
+  kern<<<dim3(p.B * p.H, gr.G), kVecThreads, smem, s>>>(p, gr, (const TIn *)q, (const TIn *)k, (const TIn *)v, lg,
+                                                        (TIn *)o, init, fin, gsum);
   return cudaGetLastError();
 }
 
@@ -290,10 +524,11 @@ template <int D, typename TIn>
 cudaError_t launch_vec_ragg(const Problem &p, VecGroups gr, const void *q, const void *dO, const float *lg, float *W,
                             cudaStream_t s) {
   auto kern = vec_ragg_kernel<D, TIn>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)vec_smem<D>());
+  const size_t smem = vec_smem<D>(3, false);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   TimedLaunch t(K_GATED_VEC_BWD, s);
-  kern<<<dim3(p.B * p.H, gr.G), kVecThreads, vec_smem<D>(), s>>>(p, gr, (const TIn *)q, (const TIn *)dO, lg, W);
+  kern<<<dim3(p.B * p.H, gr.G), kVecThreads, smem, s>>>(p, gr, (const TIn *)q, (const TIn *)dO, lg, W);
   return cudaGetLastError();
 }
 
@@ -302,12 +537,13 @@ cudaError_t launch_vec_bwd(const Problem &p, VecGroups gr, const void *q, const 
                            const void *dO, const float *lg, const float *init, const float *dfin, void *dq, void *dk,
                            void *dv, float *dlg, float *dinit, cudaStream_t s) {
   auto kern = vec_bwd_kernel<D, TIn>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)vec_smem<D>());
+  const size_t smem = vec_smem<D>(5, true);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   TimedLaunch t(K_GATED_VEC_BWD, s);
-  kern<<<dim3(p.B * p.H, gr.G), kVecThreads, vec_smem<D>(), s>>>(p, gr, (const TIn *)q, (const TIn *)k,
-                                                                 (const TIn *)v, (const TIn *)dO, lg, init, dfin,
-                                                                 (TIn *)dq, (TIn *)dk, (TIn *)dv, dlg, dinit);
+  kern<<<dim3(p.B * p.H, gr.G), kVecThreads, smem, s>>>(p, gr, (const TIn *)q, (const TIn *)k, (const TIn *)v,
+                                                        (const TIn *)dO, lg, init, dfin, (TIn *)dq, (TIn *)dk,
+                                                        (TIn *)dv, dlg, dinit);
   return cudaGetLastError();
 }
 
@@ -320,10 +556,11 @@ cudaError_t launch_vec_scan(const Problem &p, VecGroups gr, const float *X, cons
   return cudaGetLastError();
 }
 
-// Groups: enough (group, sequence) CTAs for about two per SM, of at least 256 tokens.
+// Groups: as many (group, sequence) CTAs as the SMs hold at once (two per SM), the
+// groups at least 256 tokens long.
 VecGroups vec_groups(const Problem &p) {
   const int64_t BH = (int64_t)p.B * p.H, sms = p.num_sms > 0 ? p.num_sms : 1;
-  int64_t G = (2 * sms + BH - 1) / BH;
+  int64_t G = 2 * sms / BH;
   G = std::max<int64_t>(1, std::min<int64_t>(G, (p.T + 255) / 256));
   VecGroups gr;
   gr.L = (int)((p.T + G - 1) / G);
@@ -350,14 +587,14 @@ template <int D, typename TIn>
 cudaError_t vec_fwd_path(const Problem &p, const void *q, const void *k, const void *v, const float *lg, void *o,
                          const float *init, float *final_state, char *ws, cudaStream_t s) {
   const VecGroups gr = vec_groups(p);
-  if (gr.G == 1) return launch_vec_fwd<D, TIn>(p, gr, q, k, v, lg, o, init, final_state, nullptr, s);
+  if (gr.G == 1) return launch_vec_fwd<D, TIn, true>(p, gr, q, k, v, lg, o, init, final_state, nullptr, s);
   const VecLayout w = vec_layout(p, false);
   float *states = reinterpret_cast<float *>(ws + w.states), *agg = reinterpret_cast<float *>(ws + w.agg);
   float *gsum = reinterpret_cast<float *>(ws + w.gsum);
   // the groups' own states from zero and their gate sums, the scan, the outputs
-  cudaError_t e = launch_vec_fwd<D, TIn>(p, gr, q, k, v, lg, nullptr, nullptr, agg, gsum, s);
+  cudaError_t e = launch_vec_fwd<D, TIn, false>(p, gr, q, k, v, lg, nullptr, nullptr, agg, gsum, s);
   if (e == cudaSuccess) e = launch_vec_scan(p, gr, agg, gsum, init, states, final_state, false, s);
-  if (e == cudaSuccess) e = launch_vec_fwd<D, TIn>(p, gr, q, k, v, lg, o, states, nullptr, nullptr, s);
+  if (e == cudaSuccess) e = launch_vec_fwd<D, TIn, true>(p, gr, q, k, v, lg, o, states, nullptr, nullptr, s);
   return e;
 }
 
@@ -372,7 +609,7 @@ cudaError_t vec_bwd_path(const Problem &p, const void *q, const void *k, const v
   float *gsum = reinterpret_cast<float *>(ws + w.gsum), *dfin = reinterpret_cast<float *>(ws + w.dfin);
   // forward states entering every group; reverse aggregates and the gradients arriving
   // at every group's last state; then every group's backward
-  cudaError_t e = launch_vec_fwd<D, TIn>(p, gr, q, k, v, lg, nullptr, nullptr, agg, gsum, s);
+  cudaError_t e = launch_vec_fwd<D, TIn, false>(p, gr, q, k, v, lg, nullptr, nullptr, agg, gsum, s);
   if (e == cudaSuccess) e = launch_vec_scan(p, gr, agg, gsum, init, states, nullptr, false, s);
   if (e == cudaSuccess) e = launch_vec_ragg<D, TIn>(p, gr, q, dO, lg, agg, s);
   if (e == cudaSuccess) e = launch_vec_scan(p, gr, agg, gsum, d_final, dfin, nullptr, true, s);

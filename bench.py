@@ -849,6 +849,90 @@ def run_softmax_segment(args):
         "cpu_baseline": cpu}), flush=True)
 
 
+# ---------------------------------------------------------------------------------- per-dimension gates
+def run_gated_vec(args):
+    """The per-dimension gated step (fwd_gated_vec + bwd_gated_vec) on workload 8
+    (B1 H32 T131072 d128 bf16, log-gates U(-1/16, 0) per token, head and key dimension).
+    CUDA-core kernels walking chunk groups: bound by the fp32 pipe.  Algorithmic FLOPs per
+    state element and token: the sequential recurrence's own arithmetic, forward 5 (the
+    update a s + k v, 3; the output's q s, 2) and backward 12 (the forward states again, 3,
+    with dq's S dO, 2; the reverse update, 3, with dk's R v and dv's R^T k, 2 each).  The
+    group scans' extra passes (the forward's group states, 3; the backward's group states
+    and reverse aggregates, 3 each) are work the split adds and are not credited."""
+    import torch
+    import chunked_state_scan_causal_gb300 as la
+    from chunked_state_scan_causal_gb300 import build, inputs
+    build.build()
+    dev = torch.device("cuda", 0)
+    cfg = dict(inputs.WORKLOADS[8])
+    B, H, T, d = cfg["B"], cfg["H"], cfg["T"], cfg["d"]
+    q, k, v, dO = (inputs.make(cfg, w).to(dev) for w in ("q", "k", "v", "dO"))
+    lg = inputs.make_gates(cfg, device=dev)
+    wsf, wsb = la.workspace(q, la.OP_FWD_GATED_VEC), la.workspace(q, la.OP_BWD_GATED_VEC)
+    o = torch.empty_like(q)
+    outs = [torch.empty_like(q) for _ in range(3)]
+
+    def step():
+        la.fwd_gated_vec(q, k, v, lg, out=o, ws=wsf)
+        la.bwd_gated_vec(q, k, v, dO, lg, outs=outs, ws=wsb)
+
+    steps = args.steps
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if la.device_status(wsf) != la.OK or la.device_status(wsb) != la.OK:
+        raise RuntimeError("device-side error during warm-up")
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(_gpu_uuid(dev), 0) as clk:
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(steps):
+            step()
+        e1.record()
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    la.linattn_timing_enable(True)
+    la.linattn_timing_collect()
+    for _ in range(min(steps, 5)):
+        step()
+    torch.cuda.synchronize()
+    timing = la.linattn_timing_collect()
+    la.linattn_timing_enable(False)
+    kern = {name: round(t / n, 4) for name, (n, t) in timing.items()}
+    launches = sum(n for n, _ in timing.values()) // min(steps, 5)
+    units = B * H * T
+    flops = 17 * d * d * units
+    executed = 26 * d * d * units
+    sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    mhz = 2070.0
+    peak = sm * 128 * 2 * mhz * 1e6 / 1e12  # FP32 FMA lanes x 2 FLOP x the maximum SM clock
+    tf = flops / (ms * 1e-3) / 1e12
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+        n_s = 1 << 17  # about 10 s
+        qs, ks, vs, ds = (x[0:1, 0:1, :n_s].double().cpu().numpy() for x in (q, k, v, dO))
+        gs = lg[0:1, 0:1, :n_s].double().cpu().numpy()
+        t0 = time.perf_counter()
+        oracle.fwd_gated_vec(qs, ks, vs, gs)
+        oracle.bwd_gated_vec(qs, ks, vs, ds, gs)
+        sec = time.perf_counter() - t0
+        cpu = {"value": 17 * d * d * n_s / sec / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+               "sample": f"batch row 0, head 0, the first {n_s} tokens, fp64 C recurrence, {sec:.2f} s"}
+    print(json.dumps({
+        "metric": "per-dimension gated fwd+bwd token-heads/s", "value": units / (ms * 1e-3),
+        "unit": "token-heads/s", "n_gpus": 1, "steps": steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "dtype": "bf16 (fp32 state)", "data": "synthetic (seeded normal; uniform log-gates)",
+        "config": {"workload": cfg["name"], "B": B, "H": H, "T": T, "d": d, "gates": "per token, head and key dim",
+                   "step": "linattn_fwd_gated_vec + linattn_bwd_gated_vec"},
+        "roofline": {"kernel": "gated_vec_fwd + gated_vec_bwd (whole step)", "bound": "alu", "achieved": tf,
+                     "peak": peak, "unit": "TFLOP/s", "frac": tf / peak, "traffic": None,
+                     "executed_tflops": executed / (ms * 1e-3) / 1e12,
+                     "peak_source": f"{sm} SMs x 128 fp32 lanes x 2 FLOP x {mhz:.0f} MHz (nominal unit counts)"},
+        "kernels_ms": kern, "gpu_launches": launches * steps, "clocks": clk.summary(), "cpu_baseline": cpu}),
+        flush=True)
+
+
 # ---------------------------------------------------------------------------------- sequence split
 def run_sp(args):
     """The sequence split across ranks (sp.forward + sp.backward) with N ranks as threads of
@@ -939,6 +1023,8 @@ def main():
     ap.add_argument("--sm-tq", type=int, default=16384, help="queries of the softmax segment")
     ap.add_argument("--sm-tk", type=int, default=65536, help="gathered prefix length of the softmax segment")
     ap.add_argument("--sm-bwd", action="store_true", help="with --softmax-segment: time the backward")
+    ap.add_argument("--gated-vec", action="store_true", help="measure the per-dimension gated step instead "
+                    "(workload 8; pass --steps 20)")
     ap.add_argument("--traffic-from", default="", help="ncu CSV of whole steps (dram__bytes_read/write.sum): "
                     "store DRAM bytes per token-head in profiles/traffic.json and exit")
     ap.add_argument("--traffic-steps", type=int, default=1, help="steps the --traffic-from capture covers")
@@ -956,6 +1042,8 @@ def main():
         run_decode(args)
     elif args.softmax_segment:
         run_softmax_segment(args)
+    elif args.gated_vec:
+        run_gated_vec(args)
     elif args.sp:
         run_sp(args)
     elif args.impl == "reference":

@@ -22,7 +22,7 @@ import torch
 
 TENSOR_ID = {"q": 0, "k": 1, "v": 2, "dO": 3}  # 4: the log-gates of a gated workload
 
-# The five workloads.  "sigma" is the std-dev of q, k, v; dO is always N(0, 1).
+# The workloads.  "sigma" is the std-dev of q, k, v; dO is always N(0, 1).
 WORKLOADS = {
     1: dict(name="tiny-fp32-fwd-B1H2T1K-d64", B=1, H=2, T=1024, d=64, dtype="f32",
             decay=None, dist="normal", sigma=0.125, seed=0, passes="fwd+chunk_states"),
@@ -43,6 +43,10 @@ WORKLOADS = {
     # zero-padded problem)
     7: dict(name="fwdbwd-B2H16T64K-d64", B=2, H=16, T=65536, d=64, dtype="bf16", decay=None,
             dist="normal", sigma=1.0 / math.sqrt(64), seed=6, passes="fwd+bwd"),
+    # per-dimension gates: log_gate ~ U(-1/16, 0) per token, head and key dimension
+    8: dict(name="fwdbwd-gatedvec-B1H32T128K-d128", B=1, H=32, T=131072, d=128, dtype="bf16",
+            decay=None, dist="normal", sigma=1.0 / math.sqrt(128), seed=7, passes="fwd+bwd",
+            gates=(-1.0 / 16, 0.0), gate_per_dim=True),
 }
 
 
@@ -53,17 +57,19 @@ def decay_per_head(H: int) -> np.ndarray:
 
 
 def gate_head(cfg: dict, b: int, h: int, T: int | None = None) -> np.ndarray:
-    """log-gates of one head, float32 [T] (uniform in cfg["gates"]), or None without gates."""
+    """log-gates of one head, float32 [T] (or [T, d] with a gate per key dimension; uniform
+    in cfg["gates"]), or None without gates."""
     if cfg.get("gates") is None:
         return None
     T = cfg["T"] if T is None else T
     lo, hi = cfg["gates"]
     ss = np.random.SeedSequence([cfg["seed"], 4, b, h])
-    return np.random.Generator(np.random.PCG64(ss)).uniform(lo, hi, T).astype(np.float32)
+    shape = (T, cfg["d"]) if cfg.get("gate_per_dim") else T
+    return np.random.Generator(np.random.PCG64(ss)).uniform(lo, hi, shape).astype(np.float32)
 
 
 def make_gates(cfg: dict, T: int | None = None, B: int | None = None, H: int | None = None, device=None):
-    """log-gates [B, H, T] float32 of a gated workload (None without gates)."""
+    """log-gates [B, H, T] (or [B, H, T, d]) float32 of a gated workload (None without gates)."""
     if cfg.get("gates") is None:
         return None
     B = cfg["B"] if B is None else B

@@ -865,9 +865,10 @@ def run_gated_vec(args):
     build.build()
     dev = torch.device("cuda", 0)
     cfg = dict(inputs.WORKLOADS[8])
-    B, H, T, d = cfg["B"], cfg["H"], cfg["T"], cfg["d"]
-    q, k, v, dO = (inputs.make(cfg, w).to(dev) for w in ("q", "k", "v", "dO"))
-    lg = inputs.make_gates(cfg, device=dev)
+    B, H, d = cfg["B"], cfg["H"], cfg["d"]
+    T = args.T or cfg["T"]  # --T: a shorter case of the same kernels (profiling)
+    q, k, v, dO = (inputs.make(cfg, w, T=T).to(dev) for w in ("q", "k", "v", "dO"))
+    lg = inputs.make_gates(cfg, T=T, device=dev)
     wsf, wsb = la.workspace(q, la.OP_FWD_GATED_VEC), la.workspace(q, la.OP_BWD_GATED_VEC)
     o = torch.empty_like(q)
     outs = [torch.empty_like(q) for _ in range(3)]
@@ -910,7 +911,7 @@ def run_gated_vec(args):
     cpu = None
     if not args.no_cpu_baseline:
         import oracle
-        n_s = 1 << 17  # about 10 s
+        n_s = min(T, 1 << 17)  # about 10 s
         qs, ks, vs, ds = (x[0:1, 0:1, :n_s].double().cpu().numpy() for x in (q, k, v, dO))
         gs = lg[0:1, 0:1, :n_s].double().cpu().numpy()
         t0 = time.perf_counter()
@@ -923,7 +924,8 @@ def run_gated_vec(args):
         "metric": "per-dimension gated fwd+bwd token-heads/s", "value": units / (ms * 1e-3),
         "unit": "token-heads/s", "n_gpus": 1, "steps": steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "dtype": "bf16 (fp32 state)", "data": "synthetic (seeded normal; uniform log-gates)",
-        "config": {"workload": cfg["name"], "B": B, "H": H, "T": T, "d": d, "gates": "per token, head and key dim",
+        "config": {"workload": cfg["name"] if T == cfg["T"] else f"{cfg['name']} at T={T}", "B": B, "H": H, "T": T,
+                   "d": d, "gates": "per token, head and key dim",
                    "step": "linattn_fwd_gated_vec + linattn_bwd_gated_vec"},
         "roofline": {"kernel": "gated_vec_fwd + gated_vec_bwd (whole step)", "bound": "alu", "achieved": tf,
                      "peak": peak, "unit": "TFLOP/s", "frac": tf / peak, "traffic": None,

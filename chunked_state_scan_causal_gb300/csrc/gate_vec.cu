@@ -484,15 +484,32 @@ __global__ void __launch_bounds__(kVecThreads, 2)
         st_val(dv + base + (int64_t)t * p.st + c0 + (lane >> kLowBits), x);
     }
     __syncthreads();
-    if (tid < D) {
-      for (int tt = 0; tt < nt; ++tt) {
-        const int t = hi - 1 - tt;
+    // dk, and each token's own log-gate term q_t[i] dq_t[i] - k_t[i] dk_t[i] (into the
+    // staged gates' place, free until the next step) ...
+    constexpr int kPer = kVecChunk * D / kVecThreads;
+    float own[kPer];  // q_t[i] dq_t[i] from the forward sweep, all loads in flight at once
+#pragma unroll
+    for (int m = 0; m < kPer; ++m) {
+      const int e = tid + m * kVecThreads, tt = e / D;
+      own[m] = tt < nt ? dg[(int64_t)(hi - 1 - tt) * D + e % D] : 0.f;
+    }
+#pragma unroll
+    for (int m = 0; m < kPer; ++m) {
+      const int e = tid + m * kVecThreads, tt = e / D, i = e % D;
+      if (tt < nt) {
         float x = 0.f;
 #pragma unroll
-        for (int u = 0; u < kVecWarps; ++u) x += part[(tt * kVecWarps + u) * D + tid];
-        st_val(dk + base + (int64_t)t * p.st + tid, x);
-        gacc += dg[(int64_t)t * D + tid] - sk[tt * D + tid] * x;
-        dg[(int64_t)t * D + tid] = gacc;
+        for (int u = 0; u < kVecWarps; ++u) x += part[(tt * kVecWarps + u) * D + i];
+        st_val(dk + base + (int64_t)(hi - 1 - tt) * p.st + i, x);
+        sa[tt * D + i] = own[m] - sk[tt * D + i] * x;
+      }
+    }
+    __syncthreads();
+    // ... then their running sums down the step's tokens
+    if (tid < D) {
+      for (int tt = 0; tt < nt; ++tt) {
+        gacc += sa[tt * D + tid];
+        dg[(int64_t)(hi - 1 - tt) * D + tid] = gacc;
       }
     }
   }

@@ -7,7 +7,8 @@ Tolerances: fp32 inputs 1e-4 of max|ref| (one fp32 walk per sequence); bf16 inpu
 log-gate gradient and states 1e-3.  Cases: d = 64 and 128, several heads, ragged
 lengths, an initial state and a final-state gradient, padded strides, shared gates
 (every dimension the token's gate) against the per-token gated entry points, T = 0,
-and sequences long enough to be cut into chunk groups joined by per-row scans.
+sequences long enough to be cut into chunk groups joined by per-row scans, and two
+whole heads of the full-size per-dimension gated workload.
 """
 import numpy as np
 import pytest
@@ -143,3 +144,24 @@ def test_gated_vec_chunk_groups(d, dtype, B, H, T, lo):
     for name, got, ref, t in (("o", o, ro, tol), ("final", fin, rfin, stol), ("dq", dq, rq, tol), ("dk", dk, rk, tol),
                               ("dv", dv, rv, tol), ("d_log_gate", dlg, rlg, stol), ("d_init", dinit, rinit, stol)):
         assert rel(got, ref) < t, (name, rel(got, ref))
+
+
+def test_gated_vec_full_size_sampled_heads():
+    """The per-dimension gated workload at its full size (B1 H32 T131072 d128 bf16, nine
+    chunk groups per sequence, the launch configuration the benchmark times): every
+    output of two whole heads, the first and the last, against the oracle."""
+    from chunked_state_scan_causal_gb300 import inputs
+    cfg = dict(inputs.WORKLOADS[8])
+    dev = torch.device("cuda", 0)
+    q, k, v, dO = (inputs.make(cfg, w).to(dev) for w in ("q", "k", "v", "dO"))
+    lg = inputs.make_gates(cfg, device=dev)
+    o, _ = la.fwd_gated_vec(q, k, v, lg)
+    dq, dk, dv, dlg, _ = la.bwd_gated_vec(q, k, v, dO, lg)
+    torch.cuda.synchronize()
+    for h in (0, cfg["H"] - 1):
+        n = lambda x: x[:, h:h + 1].double().cpu().numpy()
+        ro, _ = oracle.fwd_gated_vec(n(q), n(k), n(v), n(lg))
+        rq, rk, rv, rlg, _ = oracle.bwd_gated_vec(n(q), n(k), n(v), n(dO), n(lg))
+        for name, got, ref, t in (("o", o, ro, 1e-2), ("dq", dq, rq, 1e-2), ("dk", dk, rk, 1e-2),
+                                  ("dv", dv, rv, 1e-2), ("d_log_gate", dlg, rlg, 1e-3)):
+            assert rel(got[:, h:h + 1], ref) < t, (h, name, rel(got[:, h:h + 1], ref))

@@ -851,14 +851,15 @@ def run_softmax_segment(args):
 
 # ---------------------------------------------------------------------------------- per-dimension gates
 def run_gated_vec(args):
-    """The per-dimension gated step (fwd_gated_vec + bwd_gated_vec) on workload 8
-    (B1 H32 T131072 d128 bf16, log-gates U(-1/16, 0) per token, head and key dimension).
-    CUDA-core kernels walking chunk groups: bound by the fp32 pipe.  Algorithmic FLOPs per
-    state element and token: the sequential recurrence's own arithmetic, forward 5 (the
-    update a s + k v, 3; the output's q s, 2) and backward 12 (the forward states again, 3,
-    with dq's S dO, 2; the reverse update, 3, with dk's R v and dv's R^T k, 2 each).  The
-    group scans' extra passes (the forward's group states, 3; the backward's group states
-    and reverse aggregates, 3 each) are work the split adds and are not credited."""
+    """The per-dimension gated step (fwd_gated_vec + bwd_gated_vec, the backward taking
+    the forward's group states from its checkpoint) on workload 8 (B1 H32 T131072 d128
+    bf16, log-gates U(-1/16, 0) per token, head and key dimension).  CUDA-core kernels
+    walking chunk groups: bound by the fp32 pipe.  Algorithmic FLOPs per state element and
+    token: the sequential recurrence's own arithmetic, forward 5 (the update a s + k v, 3;
+    the output's q s, 2) and backward 12 (the forward states again, 3, with dq's S dO, 2;
+    the reverse update, 3, with dk's R v and dv's R^T k, 2 each).  The group split's extra
+    passes (the forward's group states from zero, 3; the backward's reverse aggregates, 3)
+    are executed but not credited."""
     import torch
     import chunked_state_scan_causal_gb300 as la
     from chunked_state_scan_causal_gb300 import build, inputs
@@ -870,12 +871,13 @@ def run_gated_vec(args):
     q, k, v, dO = (inputs.make(cfg, w, T=T).to(dev) for w in ("q", "k", "v", "dO"))
     lg = inputs.make_gates(cfg, T=T, device=dev)
     wsf, wsb = la.workspace(q, la.OP_FWD_GATED_VEC), la.workspace(q, la.OP_BWD_GATED_VEC)
+    ck = la.checkpoint_gated_vec(q)
     o = torch.empty_like(q)
     outs = [torch.empty_like(q) for _ in range(3)]
 
     def step():
-        la.fwd_gated_vec(q, k, v, lg, out=o, ws=wsf)
-        la.bwd_gated_vec(q, k, v, dO, lg, outs=outs, ws=wsb)
+        la.fwd_gated_vec(q, k, v, lg, out=o, ws=wsf, ckpt=ck)
+        la.bwd_gated_vec(q, k, v, dO, lg, outs=outs, ws=wsb, ckpt=ck)
 
     steps = args.steps
     for _ in range(args.warmup):
@@ -903,7 +905,7 @@ def run_gated_vec(args):
     launches = sum(n for n, _ in timing.values()) // min(steps, 5)
     units = B * H * T
     flops = 17 * d * d * units
-    executed = 26 * d * d * units
+    executed = 23 * d * d * units  # with the split's two extra passes
     sm = torch.cuda.get_device_properties(dev).multi_processor_count
     mhz = 2070.0
     peak = sm * 128 * 2 * mhz * 1e6 / 1e12  # FP32 FMA lanes x 2 FLOP x the maximum SM clock
@@ -926,7 +928,7 @@ def run_gated_vec(args):
         "higher_is_better": True, "dtype": "bf16 (fp32 state)", "data": "synthetic (seeded normal; uniform log-gates)",
         "config": {"workload": cfg["name"] if T == cfg["T"] else f"{cfg['name']} at T={T}", "B": B, "H": H, "T": T,
                    "d": d, "gates": "per token, head and key dim",
-                   "step": "linattn_fwd_gated_vec + linattn_bwd_gated_vec"},
+                   "step": "linattn_fwd_gated_vec_ckpt + linattn_bwd_gated_vec_ckpt"},
         "roofline": {"kernel": "gated_vec_fwd + gated_vec_bwd (whole step)", "bound": "alu", "achieved": tf,
                      "peak": peak, "unit": "TFLOP/s", "frac": tf / peak, "traffic": None,
                      "executed_tflops": executed / (ms * 1e-3) / 1e12,

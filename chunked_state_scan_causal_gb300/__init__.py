@@ -31,7 +31,7 @@ BF16, F32 = 0, 1
 OP_FWD, OP_BWD, OP_CHUNK_STATES, OP_CHECKPOINT = 1, 2, 3, 4
 OP_FWD_GATED, OP_BWD_GATED, OP_CHECKPOINT_GATED = 5, 6, 7
 OP_SOFTMAX_SEGMENT, OP_SOFTMAX_SEGMENT_BWD = 8, 9
-OP_FWD_GATED_VEC, OP_BWD_GATED_VEC = 10, 11
+OP_FWD_GATED_VEC, OP_BWD_GATED_VEC, OP_CHECKPOINT_GATED_VEC = 10, 11, 12
 ABI_VERSION = 2
 
 
@@ -72,6 +72,10 @@ _SIGS = {
     "linattn_fwd_gated_vec": ([ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "linattn_bwd_gated_vec": ([ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                _vp, _sz, _vp], _i32),
+    "linattn_fwd_gated_vec_ckpt": ([ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _sz,
+                                    _vp], _i32),
+    "linattn_bwd_gated_vec_ckpt": ([ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _vp,
+                                    _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "linattn_decode": ([ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp], _i32),
     "linattn_state_scan_workspace_size": ([_i32, _i32, _i32, _i32, ctypes.POINTER(_sz)], _i32),
     "linattn_state_scan": ([_i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
@@ -181,6 +185,18 @@ def linattn_bwd_gated_vec(shape, q, k, v, dO, log_gate, init_state, d_final, dq,
                           ws_bytes, stream) -> int:
     return lib().linattn_bwd_gated_vec(ctypes.byref(shape), q, k, v, dO, log_gate, init_state, d_final, dq, dk, dv,
                                        d_log_gate, d_init, ws, ws_bytes, stream)
+
+
+def linattn_fwd_gated_vec_ckpt(shape, q, k, v, log_gate, o, init_state, final_state, ckpt, ckpt_bytes, ws, ws_bytes,
+                               stream) -> int:
+    return lib().linattn_fwd_gated_vec_ckpt(ctypes.byref(shape), q, k, v, log_gate, o, init_state, final_state, ckpt,
+                                            ckpt_bytes, ws, ws_bytes, stream)
+
+
+def linattn_bwd_gated_vec_ckpt(shape, q, k, v, dO, log_gate, init_state, d_final, ckpt, ckpt_bytes, dq, dk, dv,
+                               d_log_gate, d_init, ws, ws_bytes, stream) -> int:
+    return lib().linattn_bwd_gated_vec_ckpt(ctypes.byref(shape), q, k, v, dO, log_gate, init_state, d_final, ckpt,
+                                            ckpt_bytes, dq, dk, dv, d_log_gate, d_init, ws, ws_bytes, stream)
 
 
 def linattn_chunk_states_rev(shape, seg_len, q, dO, out, ws, ws_bytes, stream) -> int:
@@ -467,9 +483,19 @@ def _gate_tensor_vec(log_gate, q):
     return log_gate
 
 
-def fwd_gated_vec(q, k, v, log_gate, init_state=None, want_final=False, out=None, ws=None, stream=None):
+def checkpoint_gated_vec(q):
+    """Checkpoint buffer of fwd_gated_vec(..., ckpt=) for bwd_gated_vec(..., ckpt=) (the chunk
+    groups' entering states and log-gate sums)."""
+    import torch
+    st, n = linattn_workspace_size(shape_of(q, None), OP_CHECKPOINT_GATED_VEC)
+    _check(st, "linattn_workspace_size")
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=q.device)
+
+
+def fwd_gated_vec(q, k, v, log_gate, init_state=None, want_final=False, out=None, ws=None, stream=None, ckpt=None):
     """(o, final_state or None) with a gate per token and key dimension:
-    S_t = diag(exp(log_gate_t)) S_{t-1} + k_t v_t^T (log_gate [B, H, T, d] fp32)."""
+    S_t = diag(exp(log_gate_t)) S_{t-1} + k_t v_t^T (log_gate [B, H, T, d] fp32).  With ``ckpt``
+    (from checkpoint_gated_vec) the groups' states are also kept for bwd_gated_vec(..., ckpt=)."""
     import torch
     _same_layout(q, k, v, out)
     _gate_tensor_vec(log_gate, q)
@@ -478,6 +504,12 @@ def fwd_gated_vec(q, k, v, log_gate, init_state=None, want_final=False, out=None
     fin = torch.empty((B, H, d, d), dtype=torch.float32, device=q.device) if want_final else None
     if ws is None:
         ws = workspace(q, OP_FWD_GATED_VEC)
+    if ckpt is not None:
+        st = linattn_fwd_gated_vec_ckpt(shape_of(q, None), _ptr(q), _ptr(k), _ptr(v), _ptr(log_gate), _ptr(o),
+                                        _ptr(init_state), _ptr(fin), _ptr(ckpt), ckpt.numel(), _ptr(ws), ws.numel(),
+                                        _stream(q.device, stream))
+        _check(st, "linattn_fwd_gated_vec_ckpt")
+        return o, fin
     st = linattn_fwd_gated_vec(shape_of(q, None), _ptr(q), _ptr(k), _ptr(v), _ptr(log_gate), _ptr(o),
                                _ptr(init_state), _ptr(fin), _ptr(ws), ws.numel(), _stream(q.device, stream))
     _check(st, "linattn_fwd_gated_vec")
@@ -485,8 +517,9 @@ def fwd_gated_vec(q, k, v, log_gate, init_state=None, want_final=False, out=None
 
 
 def bwd_gated_vec(q, k, v, dO, log_gate, init_state=None, d_final=None, want_dinit=False, outs=None, ws=None,
-                  stream=None):
-    """(dq, dk, dv, d_log_gate [B, H, T, d], d_init or None) of fwd_gated_vec for the upstream gradient dO."""
+                  stream=None, ckpt=None):
+    """(dq, dk, dv, d_log_gate [B, H, T, d], d_init or None) of fwd_gated_vec for the upstream gradient dO
+    (the forward's group states from ``ckpt`` if given)."""
     import torch
     _same_layout(q, k, v, dO)
     _gate_tensor_vec(log_gate, q)
@@ -498,6 +531,13 @@ def bwd_gated_vec(q, k, v, dO, log_gate, init_state=None, d_final=None, want_din
     dinit = torch.empty((B, H, d, d), dtype=torch.float32, device=q.device) if want_dinit else None
     if ws is None:
         ws = workspace(q, OP_BWD_GATED_VEC)
+    if ckpt is not None:
+        st = linattn_bwd_gated_vec_ckpt(shape_of(q, None), _ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(log_gate),
+                                        _ptr(init_state), _ptr(d_final), _ptr(ckpt), ckpt.numel(), _ptr(dq), _ptr(dk),
+                                        _ptr(dv), _ptr(dlg), _ptr(dinit), _ptr(ws), ws.numel(),
+                                        _stream(q.device, stream))
+        _check(st, "linattn_bwd_gated_vec_ckpt")
+        return dq, dk, dv, dlg, dinit
     st = linattn_bwd_gated_vec(shape_of(q, None), _ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(log_gate),
                                _ptr(init_state), _ptr(d_final), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dlg), _ptr(dinit),
                                _ptr(ws), ws.numel(), _stream(q.device, stream))

@@ -318,6 +318,8 @@ int32_t linattn_workspace_size(const linattn_shape *shape, int32_t op, int32_t s
     *bytes = kHeader;
   } else if (op == LINATTN_OP_FWD_GATED_VEC || op == LINATTN_OP_BWD_GATED_VEC) {
     *bytes = kHeader + gated_vec_ws_bytes(p, op == LINATTN_OP_BWD_GATED_VEC);
+  } else if (op == LINATTN_OP_CHECKPOINT_GATED_VEC) {
+    *bytes = gated_vec_ckpt_bytes(p);
   } else if (op == LINATTN_OP_SOFTMAX_SEGMENT_BWD) {
     *bytes = kHeader + softmax_bwd_stats_bytes(p.B, p.H, p.T);
   } else {
@@ -647,15 +649,23 @@ int32_t linattn_bwd_gated(const linattn_shape *shape, const void *q, const void 
   return cuda_status(e);
 }
 
-int32_t linattn_fwd_gated_vec(const linattn_shape *shape, const void *q, const void *k, const void *v,
-                              const float *log_gate, void *o, const float *init_state, float *final_state,
-                              void *workspace, size_t workspace_bytes, void *stream) {
+static int check_vec_ckpt(const Problem &p, const void *ckpt, size_t ckpt_size, bool use_ckpt) {
+  const size_t need = use_ckpt ? gated_vec_ckpt_bytes(p) : 0;
+  if (need && (!ckpt || (reinterpret_cast<uintptr_t>(ckpt) & 255u) || ckpt_size < need)) return LINATTN_ERR_INVALID;
+  return LINATTN_OK;
+}
+
+static int32_t fwd_gated_vec_impl(const linattn_shape *shape, const void *q, const void *k, const void *v,
+                                  const float *log_gate, void *o, const float *init_state, float *final_state,
+                                  void *ckpt, size_t ckpt_size, bool use_ckpt, void *workspace,
+                                  size_t workspace_bytes, void *stream) {
   Problem p;
   int st = validate(shape, &p);
   if (st) return st;
   if (p.decay) return LINATTN_ERR_INVALID;  // the gates replace the per-head decay
   if ((st = check_ptrs({}, {init_state, final_state}))) return st;
   if ((st = check_ws(workspace, workspace_bytes, kHeader + gated_vec_ws_bytes(p, false)))) return st;
+  if ((st = check_vec_ckpt(p, ckpt, ckpt_size, use_ckpt))) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (p.T == 0) {
     if (!final_state) return LINATTN_OK;
@@ -667,19 +677,37 @@ int32_t linattn_fwd_gated_vec(const linattn_shape *shape, const void *q, const v
   if ((st = device_ok())) return st;
   if (cudaMemsetAsync(workspace, 0, kHeader, s) != cudaSuccess) return LINATTN_ERR_CUDA;
   return cuda_status(gated_vec_fwd(p, q, k, v, log_gate, o, init_state, final_state,
-                                   static_cast<char *>(workspace) + kHeader, s));
+                                   static_cast<char *>(workspace) + kHeader,
+                                   use_ckpt && gated_vec_ckpt_bytes(p) ? ckpt : nullptr, s));
 }
 
-int32_t linattn_bwd_gated_vec(const linattn_shape *shape, const void *q, const void *k, const void *v,
-                              const void *dO, const float *log_gate, const float *init_state,
-                              const float *d_final_state, void *dq, void *dk, void *dv, float *d_log_gate,
-                              float *d_init_state, void *workspace, size_t workspace_bytes, void *stream) {
+int32_t linattn_fwd_gated_vec(const linattn_shape *shape, const void *q, const void *k, const void *v,
+                              const float *log_gate, void *o, const float *init_state, float *final_state,
+                              void *workspace, size_t workspace_bytes, void *stream) {
+  return fwd_gated_vec_impl(shape, q, k, v, log_gate, o, init_state, final_state, nullptr, 0, false, workspace,
+                            workspace_bytes, stream);
+}
+
+int32_t linattn_fwd_gated_vec_ckpt(const linattn_shape *shape, const void *q, const void *k, const void *v,
+                                   const float *log_gate, void *o, const float *init_state, float *final_state,
+                                   void *checkpoint, size_t checkpoint_bytes, void *workspace,
+                                   size_t workspace_bytes, void *stream) {
+  return fwd_gated_vec_impl(shape, q, k, v, log_gate, o, init_state, final_state, checkpoint, checkpoint_bytes,
+                            true, workspace, workspace_bytes, stream);
+}
+
+static int32_t bwd_gated_vec_impl(const linattn_shape *shape, const void *q, const void *k, const void *v,
+                                  const void *dO, const float *log_gate, const float *init_state,
+                                  const float *d_final_state, const void *ckpt, size_t ckpt_size, bool use_ckpt,
+                                  void *dq, void *dk, void *dv, float *d_log_gate, float *d_init_state,
+                                  void *workspace, size_t workspace_bytes, void *stream) {
   Problem p;
   int st = validate(shape, &p);
   if (st) return st;
   if (p.decay) return LINATTN_ERR_INVALID;
   if ((st = check_ptrs({}, {init_state, d_final_state, d_init_state}))) return st;
   if ((st = check_ws(workspace, workspace_bytes, kHeader + gated_vec_ws_bytes(p, true)))) return st;
+  if ((st = check_vec_ckpt(p, ckpt, ckpt_size, use_ckpt))) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (p.T == 0) {
     if (!d_init_state) return LINATTN_OK;
@@ -692,7 +720,25 @@ int32_t linattn_bwd_gated_vec(const linattn_shape *shape, const void *q, const v
   if ((st = device_ok())) return st;
   if (cudaMemsetAsync(workspace, 0, kHeader, s) != cudaSuccess) return LINATTN_ERR_CUDA;
   return cuda_status(gated_vec_bwd(p, q, k, v, dO, log_gate, init_state, d_final_state, dq, dk, dv, d_log_gate,
-                                   d_init_state, static_cast<char *>(workspace) + kHeader, s));
+                                   d_init_state, static_cast<char *>(workspace) + kHeader,
+                                   use_ckpt && gated_vec_ckpt_bytes(p) ? ckpt : nullptr, s));
+}
+
+int32_t linattn_bwd_gated_vec(const linattn_shape *shape, const void *q, const void *k, const void *v,
+                              const void *dO, const float *log_gate, const float *init_state,
+                              const float *d_final_state, void *dq, void *dk, void *dv, float *d_log_gate,
+                              float *d_init_state, void *workspace, size_t workspace_bytes, void *stream) {
+  return bwd_gated_vec_impl(shape, q, k, v, dO, log_gate, init_state, d_final_state, nullptr, 0, false, dq, dk, dv,
+                            d_log_gate, d_init_state, workspace, workspace_bytes, stream);
+}
+
+int32_t linattn_bwd_gated_vec_ckpt(const linattn_shape *shape, const void *q, const void *k, const void *v,
+                                   const void *dO, const float *log_gate, const float *init_state,
+                                   const float *d_final_state, const void *checkpoint, size_t checkpoint_bytes,
+                                   void *dq, void *dk, void *dv, float *d_log_gate, float *d_init_state,
+                                   void *workspace, size_t workspace_bytes, void *stream) {
+  return bwd_gated_vec_impl(shape, q, k, v, dO, log_gate, init_state, d_final_state, checkpoint, checkpoint_bytes,
+                            true, dq, dk, dv, d_log_gate, d_init_state, workspace, workspace_bytes, stream);
 }
 
 int32_t linattn_decode(const linattn_shape *shape, const void *q, const void *k, const void *v, void *o,

@@ -600,14 +600,29 @@ VecLayout vec_layout(const Problem &p, bool bwd) {
   return w;
 }
 
+// The checkpoint of a chunk-group split: every group's entering state [G][BH][D][D]
+// and its log-gate sums [G][BH][D].
+struct VecCkpt {
+  size_t states = 0, gsum = 0, total = 0;
+};
+VecCkpt vec_ckpt_layout(const Problem &p) {
+  VecCkpt c;
+  const VecGroups gr = vec_groups(p);
+  c.gsum = align256((size_t)gr.G * p.B * p.H * p.d * p.d * sizeof(float));
+  c.total = c.gsum + align256((size_t)gr.G * p.B * p.H * p.d * sizeof(float));
+  return c;
+}
+
 template <int D, typename TIn>
 cudaError_t vec_fwd_path(const Problem &p, const void *q, const void *k, const void *v, const float *lg, void *o,
-                         const float *init, float *final_state, char *ws, cudaStream_t s) {
+                         const float *init, float *final_state, char *ws, char *ckpt, cudaStream_t s) {
   const VecGroups gr = vec_groups(p);
   if (gr.G == 1) return launch_vec_fwd<D, TIn, true>(p, gr, q, k, v, lg, o, init, final_state, nullptr, s);
   const VecLayout w = vec_layout(p, false);
-  float *states = reinterpret_cast<float *>(ws + w.states), *agg = reinterpret_cast<float *>(ws + w.agg);
-  float *gsum = reinterpret_cast<float *>(ws + w.gsum);
+  const VecCkpt c = vec_ckpt_layout(p);
+  float *agg = reinterpret_cast<float *>(ws + w.agg);
+  float *states = reinterpret_cast<float *>(ckpt ? ckpt + c.states : ws + w.states);
+  float *gsum = reinterpret_cast<float *>(ckpt ? ckpt + c.gsum : ws + w.gsum);
   // the groups' own states from zero and their gate sums, the scan, the outputs
   cudaError_t e = launch_vec_fwd<D, TIn, false>(p, gr, q, k, v, lg, nullptr, nullptr, agg, gsum, s);
   if (e == cudaSuccess) e = launch_vec_scan(p, gr, agg, gsum, init, states, final_state, false, s);
@@ -618,16 +633,27 @@ cudaError_t vec_fwd_path(const Problem &p, const void *q, const void *k, const v
 template <int D, typename TIn>
 cudaError_t vec_bwd_path(const Problem &p, const void *q, const void *k, const void *v, const void *dO,
                          const float *lg, const float *init, const float *d_final, void *dq, void *dk, void *dv,
-                         float *dlg, float *dinit, char *ws, cudaStream_t s) {
+                         float *dlg, float *dinit, char *ws, const char *ckpt, cudaStream_t s) {
   const VecGroups gr = vec_groups(p);
   if (gr.G == 1) return launch_vec_bwd<D, TIn>(p, gr, q, k, v, dO, lg, init, d_final, dq, dk, dv, dlg, dinit, s);
   const VecLayout w = vec_layout(p, true);
-  float *states = reinterpret_cast<float *>(ws + w.states), *agg = reinterpret_cast<float *>(ws + w.agg);
-  float *gsum = reinterpret_cast<float *>(ws + w.gsum), *dfin = reinterpret_cast<float *>(ws + w.dfin);
-  // forward states entering every group; reverse aggregates and the gradients arriving
-  // at every group's last state; then every group's backward
-  cudaError_t e = launch_vec_fwd<D, TIn, false>(p, gr, q, k, v, lg, nullptr, nullptr, agg, gsum, s);
-  if (e == cudaSuccess) e = launch_vec_scan(p, gr, agg, gsum, init, states, nullptr, false, s);
+  const VecCkpt c = vec_ckpt_layout(p);
+  float *agg = reinterpret_cast<float *>(ws + w.agg), *dfin = reinterpret_cast<float *>(ws + w.dfin);
+  cudaError_t e = cudaSuccess;
+  const float *states, *gsum;
+  if (ckpt) {
+    // the forward states entering every group, kept by the forward
+    states = reinterpret_cast<const float *>(ckpt + c.states);
+    gsum = reinterpret_cast<const float *>(ckpt + c.gsum);
+  } else {
+    float *st = reinterpret_cast<float *>(ws + w.states), *gs = reinterpret_cast<float *>(ws + w.gsum);
+    e = launch_vec_fwd<D, TIn, false>(p, gr, q, k, v, lg, nullptr, nullptr, agg, gs, s);
+    if (e == cudaSuccess) e = launch_vec_scan(p, gr, agg, gs, init, st, nullptr, false, s);
+    states = st;
+    gsum = gs;
+  }
+  // reverse aggregates and the gradients arriving at every group's last state; then
+  // every group's backward
   if (e == cudaSuccess) e = launch_vec_ragg<D, TIn>(p, gr, q, dO, lg, agg, s);
   if (e == cudaSuccess) e = launch_vec_scan(p, gr, agg, gsum, d_final, dfin, nullptr, true, s);
   if (e == cudaSuccess) e = launch_vec_bwd<D, TIn>(p, gr, q, k, v, dO, lg, states, dfin, dq, dk, dv, dlg, dinit, s);
@@ -641,29 +667,35 @@ size_t gated_vec_ws_bytes(const Problem &p, bool bwd) {
   return vec_layout(p, bwd).total;
 }
 
+size_t gated_vec_ckpt_bytes(const Problem &p) {
+  if (p.T == 0 || vec_groups(p).G == 1) return 0;
+  return vec_ckpt_layout(p).total;
+}
+
 cudaError_t gated_vec_fwd(const Problem &p, const void *q, const void *k, const void *v, const float *log_gate,
-                          void *o, const float *init, float *final_state, void *ws, cudaStream_t s) {
-  char *w = static_cast<char *>(ws);
+                          void *o, const float *init, float *final_state, void *ws, void *ckpt, cudaStream_t s) {
+  char *w = static_cast<char *>(ws), *c = static_cast<char *>(ckpt);
   if (p.d == 64)
-    return p.dtype == 1 ? vec_fwd_path<64, float>(p, q, k, v, log_gate, o, init, final_state, w, s)
-                        : vec_fwd_path<64, __nv_bfloat16>(p, q, k, v, log_gate, o, init, final_state, w, s);
-  return p.dtype == 1 ? vec_fwd_path<128, float>(p, q, k, v, log_gate, o, init, final_state, w, s)
-                      : vec_fwd_path<128, __nv_bfloat16>(p, q, k, v, log_gate, o, init, final_state, w, s);
+    return p.dtype == 1 ? vec_fwd_path<64, float>(p, q, k, v, log_gate, o, init, final_state, w, c, s)
+                        : vec_fwd_path<64, __nv_bfloat16>(p, q, k, v, log_gate, o, init, final_state, w, c, s);
+  return p.dtype == 1 ? vec_fwd_path<128, float>(p, q, k, v, log_gate, o, init, final_state, w, c, s)
+                      : vec_fwd_path<128, __nv_bfloat16>(p, q, k, v, log_gate, o, init, final_state, w, c, s);
 }
 
 cudaError_t gated_vec_bwd(const Problem &p, const void *q, const void *k, const void *v, const void *dO,
                           const float *log_gate, const float *init, const float *d_final, void *dq, void *dk,
-                          void *dv, float *d_log_gate, float *d_init, void *ws, cudaStream_t s) {
+                          void *dv, float *d_log_gate, float *d_init, void *ws, const void *ckpt, cudaStream_t s) {
   char *w = static_cast<char *>(ws);
+  const char *c = static_cast<const char *>(ckpt);
   if (p.d == 64)
     return p.dtype == 1 ? vec_bwd_path<64, float>(p, q, k, v, dO, log_gate, init, d_final, dq, dk, dv, d_log_gate,
-                                                  d_init, w, s)
+                                                  d_init, w, c, s)
                         : vec_bwd_path<64, __nv_bfloat16>(p, q, k, v, dO, log_gate, init, d_final, dq, dk, dv,
-                                                          d_log_gate, d_init, w, s);
+                                                          d_log_gate, d_init, w, c, s);
   return p.dtype == 1 ? vec_bwd_path<128, float>(p, q, k, v, dO, log_gate, init, d_final, dq, dk, dv, d_log_gate,
-                                                 d_init, w, s)
+                                                 d_init, w, c, s)
                       : vec_bwd_path<128, __nv_bfloat16>(p, q, k, v, dO, log_gate, init, d_final, dq, dk, dv,
-                                                         d_log_gate, d_init, w, s);
+                                                         d_log_gate, d_init, w, c, s);
 }
 
 }  // namespace linattn

@@ -196,11 +196,16 @@ cudaError_t unpad_state_d64(const float *src, float *dst, int64_t n, cudaStream_
 // are [B*H][T][d] fp32.  Workspace bytes of the group path (0 when one group covers
 // the sequence).
 size_t gated_vec_ws_bytes(const Problem &p, bool bwd);
+// bytes of the per-dimension checkpoint (the groups' entering states and log-gate
+// sums; 0 with one group per sequence)
+size_t gated_vec_ckpt_bytes(const Problem &p);
+// ckpt: NULL, or gated_vec_ckpt_bytes of device memory the forward fills and the
+// backward then reads instead of recomputing the groups' states
 cudaError_t gated_vec_fwd(const Problem &p, const void *q, const void *k, const void *v, const float *log_gate,
-                          void *o, const float *init, float *final_state, void *ws, cudaStream_t s);
+                          void *o, const float *init, float *final_state, void *ws, void *ckpt, cudaStream_t s);
 cudaError_t gated_vec_bwd(const Problem &p, const void *q, const void *k, const void *v, const void *dO,
                           const float *log_gate, const float *init, const float *d_final, void *dq, void *dk,
-                          void *dv, float *d_log_gate, float *d_init, void *ws, cudaStream_t s);
+                          void *dv, float *d_log_gate, float *d_init, void *ws, const void *ckpt, cudaStream_t s);
 cudaError_t softmax_segment(const SoftmaxProblem &p, const void *q, const void *k, const void *v, void *o, float *lse,
                             int *status, cudaStream_t s);
 // The backward: dq (q strides), dk and dv (k strides) for the output gradient dO

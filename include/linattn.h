@@ -79,7 +79,7 @@ enum { LINATTN_BF16 = 0, LINATTN_F32 = 1 };
 enum { LINATTN_OP_FWD = 1, LINATTN_OP_BWD = 2, LINATTN_OP_CHUNK_STATES = 3, LINATTN_OP_CHECKPOINT = 4,
        LINATTN_OP_FWD_GATED = 5, LINATTN_OP_BWD_GATED = 6, LINATTN_OP_CHECKPOINT_GATED = 7,
        LINATTN_OP_SOFTMAX_SEGMENT = 8, LINATTN_OP_SOFTMAX_SEGMENT_BWD = 9, LINATTN_OP_FWD_GATED_VEC = 10,
-       LINATTN_OP_BWD_GATED_VEC = 11 };
+       LINATTN_OP_BWD_GATED_VEC = 11, LINATTN_OP_CHECKPOINT_GATED_VEC = 12 };
 
 typedef struct {
   int32_t abi_version;  /* must be LINATTN_ABI_VERSION                              */
@@ -199,11 +199,11 @@ int32_t linattn_bwd_gated(const linattn_shape *shape, const void *q, const void 
  *   S_t = diag(alpha_t) S_{t-1} + k_t v_t^T,   o_t = S_t^T q_t
  * (row i of the state decays by the gate of key dimension i).  log_gate is
  * [B,H,T,d] fp32, contiguous, 16-byte aligned; the shape's decay must be NULL.
- * Runs on CUDA-core kernels (fp32 state in shared memory, no device-side
- * waits): each sequence is cut into chunk groups, one CTA per (group, batch,
- * head) walks its tokens, and the groups are joined by scans whose multipliers
- * are per state row (the product of a group's gates of that key dimension);
- * with few tokens, one CTA per (batch, head) walks the whole sequence.  The
+ * Runs on CUDA-core kernels (fp32 state in registers, no device-side waits):
+ * each sequence is cut into chunk groups, one CTA per (group, batch, head)
+ * walks its tokens, and the groups are joined by scans whose multipliers are
+ * per state row (the product of a group's gates of that key dimension); with
+ * few tokens, one CTA per (batch, head) walks the whole sequence.  The
  * per-token gates above have the tensor-core path.  Workspace:
  * LINATTN_OP_FWD_GATED_VEC bytes (the groups' states).  Returns a status. */
 int32_t linattn_fwd_gated_vec(const linattn_shape *shape, const void *q, const void *k, const void *v,
@@ -221,6 +221,30 @@ int32_t linattn_bwd_gated_vec(const linattn_shape *shape, const void *q, const v
                               const void *dO, const float *log_gate, const float *init_state,
                               const float *d_final_state, void *dq, void *dk, void *dv, float *d_log_gate,
                               float *d_init_state, void *workspace, size_t workspace_bytes, void *stream);
+
+/* linattn_fwd_gated_vec that also keeps a checkpoint for
+ * linattn_bwd_gated_vec_ckpt: every chunk group's entering state and the sums
+ * of its log-gates per key dimension (size from linattn_workspace_size(..,
+ * LINATTN_OP_CHECKPOINT_GATED_VEC, ..); 0 when every sequence is one group, in
+ * which case checkpoint may be NULL).  `checkpoint` is caller-owned device
+ * memory, 256-byte aligned.  Same outputs as linattn_fwd_gated_vec.  Returns a
+ * status (LINATTN_ERR_INVALID for a missing, misaligned or short checkpoint). */
+int32_t linattn_fwd_gated_vec_ckpt(const linattn_shape *shape, const void *q, const void *k, const void *v,
+                                   const float *log_gate, void *o, const float *init_state, float *final_state,
+                                   void *checkpoint, size_t checkpoint_bytes, void *workspace,
+                                   size_t workspace_bytes, void *stream);
+
+/* linattn_bwd_gated_vec that takes the forward's group states from a checkpoint
+ * written by linattn_fwd_gated_vec_ckpt for the same shape, k, v, log_gate and
+ * init_state, instead of recomputing them (one pass over k, v and the gates
+ * less).  init_state is the one given to the forward (read only when every
+ * sequence is one group).  Same outputs as linattn_bwd_gated_vec.  Returns a
+ * status. */
+int32_t linattn_bwd_gated_vec_ckpt(const linattn_shape *shape, const void *q, const void *k, const void *v,
+                                   const void *dO, const float *log_gate, const float *init_state,
+                                   const float *d_final_state, const void *checkpoint, size_t checkpoint_bytes,
+                                   void *dq, void *dk, void *dv, float *d_log_gate, float *d_init_state,
+                                   void *workspace, size_t workspace_bytes, void *stream);
 
 /* Recurrent decode of T new tokens per sequence (constant-memory inference:
  * LASP-2 page, abstract): for t = 0..T-1

@@ -160,3 +160,20 @@ def test_gated_entry_points_check_their_arguments(cdll):
     for op in (la.OP_FWD_GATED, la.OP_BWD_GATED, la.OP_CHECKPOINT_GATED):
         st, n = la.linattn_workspace_size(s, op)
         assert st == la.OK and n >= 256
+
+
+def test_gated_vec_checkpoint_checks(cdll):
+    """The per-dimension checkpoint: empty with one chunk group per sequence, otherwise
+    required by the _ckpt entry points (NULL, short or misaligned: ERR_INVALID before any
+    device work).  The group count follows the SM count, so the case takes one sequence
+    long enough for two groups on any device (the host without a GPU counts one SM)."""
+    one = _shape(H=1, T=200, stride_b=200 * 128, stride_h=200 * 128)
+    assert la.linattn_workspace_size(one, la.OP_CHECKPOINT_GATED_VEC) == (la.OK, 0)
+    s = _shape(H=1, T=4096, stride_b=4096 * 128, stride_h=4096 * 128)
+    st, n = la.linattn_workspace_size(s, la.OP_CHECKPOINT_GATED_VEC)
+    assert st == la.OK and n > 0 and n % 256 == 0
+    for ck, nb in ((None, n), (FAKE, n - 256), (FAKE + 16, n)):
+        assert la.linattn_fwd_gated_vec_ckpt(s, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, ck, nb, FAKE, 1 << 30,
+                                             None) == la.ERR_INVALID
+        assert la.linattn_bwd_gated_vec_ckpt(s, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, ck, nb, FAKE, FAKE, FAKE,
+                                             FAKE, None, FAKE, 1 << 30, None) == la.ERR_INVALID

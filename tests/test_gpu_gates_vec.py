@@ -165,3 +165,21 @@ def test_gated_vec_full_size_sampled_heads():
         for name, got, ref, t in (("o", o, ro, 1e-2), ("dq", dq, rq, 1e-2), ("dk", dk, rk, 1e-2),
                                   ("dv", dv, rv, 1e-2), ("d_log_gate", dlg, rlg, 1e-3)):
             assert rel(got[:, h:h + 1], ref) < t, (h, name, rel(got[:, h:h + 1], ref))
+
+
+@pytest.mark.parametrize("d,dtype,B,H,T", [(128, torch.bfloat16, 1, 2, 3000), (64, torch.float32, 2, 1, 2600),
+                                           (128, torch.float32, 1, 1, 100)])
+def test_gated_vec_checkpoint_equals_recompute(d, dtype, B, H, T):
+    """fwd_gated_vec(ckpt=) + bwd_gated_vec(ckpt=) take the groups' entering states from the
+    forward instead of recomputing them with the same kernels: every output is bitwise
+    the same (T = 100: one group per sequence, the checkpoint is empty)."""
+    q, k, v, dO, lg, init, D = (x.cuda() for x in case(T + 3 * d, B, H, T, d, dtype))
+    ck = la.checkpoint_gated_vec(q)
+    o1, f1 = la.fwd_gated_vec(q, k, v, lg, init_state=init, want_final=True)
+    g1 = la.bwd_gated_vec(q, k, v, dO, lg, init_state=init, d_final=D, want_dinit=True)
+    o2, f2 = la.fwd_gated_vec(q, k, v, lg, init_state=init, want_final=True, ckpt=ck)
+    g2 = la.bwd_gated_vec(q, k, v, dO, lg, init_state=init, d_final=D, want_dinit=True, ckpt=ck)
+    torch.cuda.synchronize()
+    for name, a, b in zip(("o", "final", "dq", "dk", "dv", "d_log_gate", "d_init"), (o1, f1) + tuple(g1),
+                          (o2, f2) + tuple(g2)):
+        assert torch.equal(a, b), name

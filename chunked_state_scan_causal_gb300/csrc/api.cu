@@ -347,7 +347,7 @@ static int32_t fwd_impl(const linattn_shape *shape, const void *q, const void *k
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char *ws = static_cast<char *>(workspace);
   int *status = reinterpret_cast<int *>(ws);
-  if (cudaMemsetAsync(ws, 0, kHeader, s) != cudaSuccess) return LINATTN_ERR_CUDA;
+  if (clear_header(ws, kHeader, s) != cudaSuccess) return LINATTN_ERR_CUDA;
   const int64_t BH = (int64_t)p.B * p.H;
   const size_t state_bytes = (size_t)BH * p.d * p.d * sizeof(float);
   if (p.T == 0) {
@@ -422,7 +422,7 @@ static int32_t bwd_impl(const linattn_shape *shape, const void *q, const void *k
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char *ws = static_cast<char *>(workspace);
   int *status = reinterpret_cast<int *>(ws);
-  if (cudaMemsetAsync(ws, 0, kHeader, s) != cudaSuccess) return LINATTN_ERR_CUDA;
+  if (clear_header(ws, kHeader, s) != cudaSuccess) return LINATTN_ERR_CUDA;
   const int64_t BH = (int64_t)p.B * p.H;
   const size_t state_bytes = (size_t)BH * p.d * p.d * sizeof(float);
   if (p.T == 0) {
@@ -531,7 +531,7 @@ int32_t linattn_fwd_gated(const linattn_shape *shape, const void *q, const void 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char *ws = static_cast<char *>(workspace);
   int *status = reinterpret_cast<int *>(ws);
-  if (cudaMemsetAsync(ws, 0, kHeader, s) != cudaSuccess) return LINATTN_ERR_CUDA;
+  if (clear_header(ws, kHeader, s) != cudaSuccess) return LINATTN_ERR_CUDA;
   const int64_t BH = (int64_t)p.B * p.H;
   const size_t state_bytes = (size_t)BH * p.d * p.d * sizeof(float);
   if (p.T == 0) {
@@ -589,7 +589,7 @@ int32_t linattn_bwd_gated(const linattn_shape *shape, const void *q, const void 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char *ws = static_cast<char *>(workspace);
   int *status = reinterpret_cast<int *>(ws);
-  if (cudaMemsetAsync(ws, 0, kHeader, s) != cudaSuccess) return LINATTN_ERR_CUDA;
+  if (clear_header(ws, kHeader, s) != cudaSuccess) return LINATTN_ERR_CUDA;
   const int64_t BH = (int64_t)p.B * p.H;
   const size_t user_state_bytes = (size_t)BH * p.d * p.d * sizeof(float);
   if (p.T == 0) {
@@ -675,7 +675,7 @@ static int32_t fwd_gated_vec_impl(const linattn_shape *shape, const void *q, con
   }
   if ((st = check_ptrs({q, k, v, o, log_gate}, {}))) return st;
   if ((st = device_ok())) return st;
-  if (cudaMemsetAsync(workspace, 0, kHeader, s) != cudaSuccess) return LINATTN_ERR_CUDA;
+  if (clear_header(workspace, kHeader, s) != cudaSuccess) return LINATTN_ERR_CUDA;
   return cuda_status(gated_vec_fwd(p, q, k, v, log_gate, o, init_state, final_state,
                                    static_cast<char *>(workspace) + kHeader,
                                    use_ckpt && gated_vec_ckpt_bytes(p) ? ckpt : nullptr, s));
@@ -718,7 +718,7 @@ static int32_t bwd_gated_vec_impl(const linattn_shape *shape, const void *q, con
   }
   if ((st = check_ptrs({q, k, v, dO, log_gate, dq, dk, dv, d_log_gate}, {}))) return st;
   if ((st = device_ok())) return st;
-  if (cudaMemsetAsync(workspace, 0, kHeader, s) != cudaSuccess) return LINATTN_ERR_CUDA;
+  if (clear_header(workspace, kHeader, s) != cudaSuccess) return LINATTN_ERR_CUDA;
   return cuda_status(gated_vec_bwd(p, q, k, v, dO, log_gate, init_state, d_final_state, dq, dk, dv, d_log_gate,
                                    d_init_state, static_cast<char *>(workspace) + kHeader,
                                    use_ckpt && gated_vec_ckpt_bytes(p) ? ckpt : nullptr, s));
@@ -764,7 +764,7 @@ static int32_t chunk_states_impl(const linattn_shape *shape, int32_t seg_len, co
   if ((st = device_ok())) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int *status = reinterpret_cast<int *>(workspace);
-  if (cudaMemsetAsync(workspace, 0, kHeader, s) != cudaSuccess) return LINATTN_ERR_CUDA;
+  if (clear_header(workspace, kHeader, s) != cudaSuccess) return LINATTN_ERR_CUDA;
   if (tc_supported(p) && seg_len % 128 == 0)
     return cuda_status(tc_segment_states(p, GroupPlan::uniform(p.T, seg_len), x, y, reverse, out, status, s));
   if (padded(p) && seg_len % 128 == 0)  // bf16 d = 64: the d = 128 kernel, 64 x 64 states stored
@@ -802,7 +802,7 @@ int32_t linattn_state_scan(int32_t G, int32_t BH, int32_t dk, int32_t dv, const 
   if ((st = device_ok())) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char *ws = static_cast<char *>(workspace);
-  if (cudaMemsetAsync(ws, 0, kHeader, s) != cudaSuccess) return LINATTN_ERR_CUDA;
+  if (clear_header(ws, kHeader, s) != cudaSuccess) return LINATTN_ERR_CUDA;
   return cuda_status(state_scan(G, BH, dk * dv, seg_decay, nullptr, 1, 1, false, local_states, init,
                                 init_states, total, ws + kHeader, reinterpret_cast<int *>(ws), s));
 }
@@ -822,7 +822,7 @@ int32_t linattn_softmax_segment_fwd(const linattn_shape *q_shape, const linattn_
   if ((st = check_ws(workspace, workspace_bytes, kHeader))) return st;
   if ((st = device_ok())) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(workspace, 0, kHeader, s) != cudaSuccess) return LINATTN_ERR_CUDA;
+  if (clear_header(workspace, kHeader, s) != cudaSuccess) return LINATTN_ERR_CUDA;
   if (pq.T == 0) return LINATTN_OK;
   SoftmaxProblem sp;
   sp.B = pq.B; sp.H = pq.H; sp.Tq = pq.T; sp.Tk = pk.T;
@@ -850,7 +850,7 @@ int32_t linattn_softmax_segment_bwd(const linattn_shape *q_shape, const linattn_
   if ((st = check_ws(workspace, workspace_bytes, kHeader + softmax_bwd_stats_bytes(pq.B, pq.H, pq.T)))) return st;
   if ((st = device_ok())) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(workspace, 0, kHeader, s) != cudaSuccess) return LINATTN_ERR_CUDA;
+  if (clear_header(workspace, kHeader, s) != cudaSuccess) return LINATTN_ERR_CUDA;
   SoftmaxProblem sp;
   sp.B = pq.B; sp.H = pq.H; sp.Tq = pq.T; sp.Tk = pk.T;
   sp.qsb = pq.sb; sp.qsh = pq.sh; sp.qst = pq.st;
@@ -885,7 +885,7 @@ int32_t linattn_diag_scan_withhold(int32_t G, int32_t BH, int32_t dk, int32_t dv
   if ((st = device_ok())) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char *ws = static_cast<char *>(workspace);
-  if (cudaMemsetAsync(ws, 0, kHeader, s) != cudaSuccess) return LINATTN_ERR_CUDA;
+  if (clear_header(ws, kHeader, s) != cudaSuccess) return LINATTN_ERR_CUDA;
   return cuda_status(state_scan(G, BH, dk * dv, nullptr, nullptr, 1, 1, false, local_states, nullptr, init_states,
                                 nullptr, ws + kHeader, reinterpret_cast<int *>(ws), s, nullptr, 1 << 30, 0,
                                 (uint64_t)(wait_limit_ms * 1e6), withhold_tile));
@@ -940,7 +940,7 @@ const char *linattn_kernel_name(int32_t kind) {
                                        "diag_mma", "decode", "tc_dual_rev", "tc_chunked_fwd_agg",
                                        "gate_prep_and_grad", "tc_chunk_states", "softmax_segment",
                                        "gated_vec_fwd", "gated_vec_bwd", "pad_d64", "softmax_bwd_prep",
-                                       "softmax_bwd_dkdv", "softmax_bwd_dq"};
+                                       "softmax_bwd_dkdv", "softmax_bwd_dq", "clear_status"};
   return (kind >= 0 && kind < K_KINDS) ? names[kind] : "?";
 }
 

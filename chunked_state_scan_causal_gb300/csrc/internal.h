@@ -6,6 +6,26 @@
 
 namespace linattn {
 
+// Launches with programmatic stream serialization: the kernel may start (up to its
+// griddep_wait, which every kernel launched this way calls before its first global
+// memory access) while the kernel before it on the stream finishes, so that its
+// prologue overlaps that kernel's tail.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_overlapped(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
+}
+
 // A validated request.  Sequence tensors are [B, H, T, d] with element strides
 // (sb, sh, st); states are [B*H, d, d] fp32.
 struct Problem {
@@ -62,7 +82,7 @@ int device_ok();
 enum KernelKind {
   K_SIMT_FWD = 0, K_SIMT_BWD, K_SIMT_SEGMENT, K_SCAN, K_TC_AGG, K_TC_MAIN_FWD, K_DIAG,
   K_DECODE, K_TC_DUAL_REV, K_TC_MAIN_AGG, K_GATE, K_TC_CHUNK_STATES, K_SOFTMAX_SEGMENT, K_GATED_VEC_FWD,
-  K_GATED_VEC_BWD, K_PAD_D64, K_SOFTMAX_BWD_PREP, K_SOFTMAX_BWD_KV, K_SOFTMAX_BWD_Q, K_KINDS
+  K_GATED_VEC_BWD, K_PAD_D64, K_SOFTMAX_BWD_PREP, K_SOFTMAX_BWD_KV, K_SOFTMAX_BWD_Q, K_CLEAR_STATUS, K_KINDS
 };
 // Records timing events around one launch on `s` while timing is enabled.
 struct TimedLaunch {
@@ -71,6 +91,12 @@ struct TimedLaunch {
   int kind, slot;
   cudaStream_t stream;
 };
+
+// Zeroes `bytes` (a multiple of 4, at most 1024) at the start of a workspace (its
+// status word and item counters) on the stream.  A kernel rather than a memset, so
+// that it takes part in the overlapped launches: it waits for the kernel before it,
+// and the next kernel may start its prologue meanwhile.
+cudaError_t clear_header(void *ws, size_t bytes, cudaStream_t s);
 
 // ---------------------------------------------------------------- SIMT path (simt.cu)
 // log_gate ([BH][T] fp32, natural log of the per-token gates) replaces the per-head

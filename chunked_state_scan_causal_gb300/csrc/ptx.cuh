@@ -200,6 +200,18 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// ----------------------------------------------------------------------------- programmatic dependent launch
+// A kernel launched with programmatic stream serialization may start while the
+// kernel before it on the stream still runs.  griddep_wait() blocks until that
+// kernel has completed and its memory operations are visible (at once when the
+// launch carries no such dependency); every global access of the kernel must come
+// after it.  griddep_launch_dependents() lets the next such kernel start its own
+// prologue once every CTA of this grid has issued it.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ----------------------------------------------------------------------------- tcgen05 / TMEM
 __device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(

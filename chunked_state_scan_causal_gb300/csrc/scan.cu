@@ -215,6 +215,8 @@ constexpr int kColumnMaxG = 256;
 constexpr int kColumnDepth = 4;  // loads in flight per thread
 
 __global__ void __launch_bounds__(256) scan_columns_kernel(ScanArgs A) {
+  griddep_wait();  // the states come from the kernel before on the stream
+  griddep_launch_dependents();
   const int64_t E = (int64_t)A.BH * A.DD, n4 = E / 4;
   for (int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c < n4; c += (int64_t)gridDim.x * blockDim.x) {
     const int64_t e0 = c * 4;
@@ -319,8 +321,7 @@ cudaError_t state_scan(int G, int BH, int DD, const float *seg_decay, const floa
   if (G <= kColumnMaxG && withhold < 0) {
     const int64_t n4 = E / 4, want = (n4 + 255) / 256, cap = (int64_t)sms * 8;
     TimedLaunch t(K_SCAN, s);
-    scan_columns_kernel<<<(int)(want < cap ? want : cap), 256, 0, s>>>(A);
-    return cudaGetLastError();
+    return launch_overlapped(scan_columns_kernel, dim3((unsigned)(want < cap ? want : cap)), dim3(256), 0, s, A);
   }
   const int64_t nt = (int64_t)A.ntg * A.ncg;
   char *w = static_cast<char *>(ws);
@@ -375,6 +376,20 @@ cudaError_t noalloc_scratch(void **ptr) {
   return cudaSuccess;
 }
 }  // namespace
+namespace {
+__global__ void clear_header_kernel(int *hdr, int n) {
+  griddep_launch_dependents();  // the next kernel waits for this one before its first access
+  griddep_wait();               // the header may still be in use by the kernel before
+  for (int i = threadIdx.x; i < n; i += blockDim.x) hdr[i] = 0;
+}
+}  // namespace
+
+cudaError_t clear_header(void *ws, size_t bytes, cudaStream_t s) {
+  if (!ws || bytes % 4 || bytes > 1024) return cudaErrorInvalidValue;
+  TimedLaunch t(K_CLEAR_STATUS, s);
+  return launch_overlapped(clear_header_kernel, dim3(1), dim3(64), 0, s, static_cast<int *>(ws), (int)(bytes / 4));
+}
+
 }  // namespace linattn
 
 extern "C" int32_t linattn_state_scan_noalloc(int32_t G, int32_t BH, int32_t dk, int32_t dv,

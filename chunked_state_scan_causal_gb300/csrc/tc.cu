@@ -251,6 +251,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
+  // barriers, ring, TMEM and tensor maps are set up: wait for the kernel before on
+  // the stream (its outputs are this kernel's inputs), then let the next one start
+  griddep_wait();
+  griddep_launch_dependents();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -840,6 +844,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
+  // barriers, ring, TMEM and tensor maps are set up: wait for the kernel before on
+  // the stream (its outputs are this kernel's inputs), then let the next one start
+  griddep_wait();
+  griddep_launch_dependents();
   const uint32_t tS = tmem, tP = tmem + 128, tO = tmem + 256;
   const uint32_t tW = tmem + 384, tOi = tmem + 384;  // AGG: aggregate; DECAY: inter-block term
   const uint32_t sbase = smem_u32(smem);
@@ -1404,6 +1412,10 @@ __global__ void __launch_bounds__(kDualThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
+  // barriers, ring, TMEM and tensor maps are set up: wait for the kernel before on
+  // the stream (its outputs are this kernel's inputs), then let the next one start
+  griddep_wait();
+  griddep_launch_dependents();
   const uint32_t tR = tmem, tP = tmem + 128, tO1 = tmem + 256, tO2 = tmem + 384;
   const uint32_t sbase = smem_u32(smem);
   const uint32_t sSh = sbase + kDualOffSh;
@@ -1899,15 +1911,15 @@ cudaError_t tc_segment_states(const Problem &p, const GroupPlan &gp, const void 
   TimedLaunch t(K_TC_AGG, s);
   if (p.gC) {
     if ((e = set_smem(tc_agg_kernel<true, true>, smem)) != cudaSuccess) return e;
-    tc_agg_kernel<true, true><<<grid, kThreads, smem, s>>>(mx, my, A);
+    e = launch_overlapped(tc_agg_kernel<true, true>, grid, kThreads, smem, s, mx, my, A);
   } else if (p.decay) {
     if ((e = set_smem(tc_agg_kernel<true>, smem)) != cudaSuccess) return e;
-    tc_agg_kernel<true><<<grid, kThreads, smem, s>>>(mx, my, A);
+    e = launch_overlapped(tc_agg_kernel<true>, grid, kThreads, smem, s, mx, my, A);
   } else {
     if ((e = set_smem(tc_agg_kernel<false>, smem)) != cudaSuccess) return e;
-    tc_agg_kernel<false><<<grid, kThreads, smem, s>>>(mx, my, A);
+    e = launch_overlapped(tc_agg_kernel<false>, grid, kThreads, smem, s, mx, my, A);
   }
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t tc_chunk_states(const Problem &p, const GroupPlan &gp, const void *k, const void *v,
@@ -1958,15 +1970,15 @@ cudaError_t tc_dual(const Problem &p, const GroupPlan &gp, const void *q, const 
   TimedLaunch t(K_TC_DUAL_REV, s);
   if (p.gC) {
     if ((e = set_smem(tc_dual_kernel<true, true>, kDualSmem)) != cudaSuccess) return e;
-    tc_dual_kernel<true, true><<<grid, kDualThreads, kDualSmem, s>>>(mk, mq, mv, mdo, D);
+    e = launch_overlapped(tc_dual_kernel<true, true>, grid, kDualThreads, kDualSmem, s, mk, mq, mv, mdo, D);
   } else if (p.decay) {
     if ((e = set_smem(tc_dual_kernel<true>, kDualSmem)) != cudaSuccess) return e;
-    tc_dual_kernel<true><<<grid, kDualThreads, kDualSmem, s>>>(mk, mq, mv, mdo, D);
+    e = launch_overlapped(tc_dual_kernel<true>, grid, kDualThreads, kDualSmem, s, mk, mq, mv, mdo, D);
   } else {
     if ((e = set_smem(tc_dual_kernel<false>, kDualSmem)) != cudaSuccess) return e;
-    tc_dual_kernel<false><<<grid, kDualThreads, kDualSmem, s>>>(mk, mq, mv, mdo, D);
+    e = launch_overlapped(tc_dual_kernel<false>, grid, kDualThreads, kDualSmem, s, mk, mq, mv, mdo, D);
   }
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t tc_main(const Problem &p, const GroupPlan &gp, const void *q, const void *k, const void *v, void *o,
@@ -1997,7 +2009,7 @@ cudaError_t tc_main(const Problem &p, const GroupPlan &gp, const void *q, const 
 #define LINATTN_LAUNCH_MAIN(DEC, AGG, GATE)                                                    \
   do {                                                                                        \
     if ((e = set_smem(tc_main_kernel<DEC, AGG, GATE>, kMainSmem)) != cudaSuccess) return e;   \
-    tc_main_kernel<DEC, AGG, GATE><<<grid, kThreads, kMainSmem, s>>>(mq, mk, mv, mo, mx, M);  \
+    e = launch_overlapped(tc_main_kernel<DEC, AGG, GATE>, grid, kThreads, kMainSmem, s, mq, mk, mv, mo, mx, M); \
   } while (0)
   if (x && p.gC)
     LINATTN_LAUNCH_MAIN(true, true, true);
@@ -2012,7 +2024,7 @@ cudaError_t tc_main(const Problem &p, const GroupPlan &gp, const void *q, const 
   else
     LINATTN_LAUNCH_MAIN(false, false, false);
 #undef LINATTN_LAUNCH_MAIN
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace linattn

@@ -394,7 +394,7 @@ int32_t linattn_device_status(const void *workspace, void *stream);
  * for every kernel kind k < max_kinds its launch count and summed device time
  * (ms), clears the record and returns the number of kinds
  * (LINATTN_KERNEL_KINDS), or a negative status. */
-#define LINATTN_KERNEL_KINDS 19
+#define LINATTN_KERNEL_KINDS 20
 int32_t linattn_timing_enable(int32_t on);
 int32_t linattn_timing_collect(int32_t max_kinds, int32_t *launches, float *total_ms);
 /* Name of kernel kind k (static string; "?" when out of range). */

@@ -39,29 +39,40 @@ __global__ void __launch_bounds__(256) gate_prep_kernel(const float *lg, int T, 
   float *dst = C + (int64_t)bh * T;
   float carry = 0.f;
   float bmin = 0.f, bmax = 0.f, span = 0.f;  // the current block's range (from the sum before it)
-  for (int t = s0; t < s1; t += 32) {
-    const int tt = t + lane;
-    float x = tt < s1 ? src[tt] * kLog2e : 0.f;
+  constexpr int kTiles = 8;                   // tiles of 32 tokens whose loads are in flight together
+  for (int t0 = s0; t0 < s1; t0 += 32 * kTiles) {
+    float xs[kTiles];
 #pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const float y = __shfl_up_sync(0xffffffffu, x, d);
-      if (lane >= d) x += y;
+    for (int j = 0; j < kTiles; ++j) {
+      const int tt = t0 + 32 * j + lane;
+      xs[j] = tt < s1 ? src[tt] * kLog2e : 0.f;
     }
-    x += carry;
-    if (tt < s1) dst[tt] = x;
-    // lanes past the end hold the last sum, so all 32 lanes take part
-    float mn = x, mx = x;
 #pragma unroll
-    for (int d = 16; d > 0; d >>= 1) {
-      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, d));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, d));
-    }
-    bmin = fminf(bmin, mn);
-    bmax = fmaxf(bmax, mx);
-    carry = __shfl_sync(0xffffffffu, x, 31);
-    if (((t - s0) & 127) == 96 || t + 32 >= s1) {  // a block ends (groups start on 128-token boundaries)
-      span = fmaxf(span, bmax - bmin);
-      bmin = bmax = carry;
+    for (int j = 0; j < kTiles; ++j) {
+      const int t = t0 + 32 * j, tt = t + lane;
+      if (t >= s1) break;  // warp-uniform
+      float x = xs[j];
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, x, d);
+        if (lane >= d) x += y;
+      }
+      x += carry;
+      if (tt < s1) dst[tt] = x;
+      // lanes past the end hold the last sum, so all 32 lanes take part
+      float mn = x, mx = x;
+#pragma unroll
+      for (int d = 16; d > 0; d >>= 1) {
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, d));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, d));
+      }
+      bmin = fminf(bmin, mn);
+      bmax = fmaxf(bmax, mx);
+      carry = __shfl_sync(0xffffffffu, x, 31);
+      if (((t - s0) & 127) == 96 || t + 32 >= s1) {  // a block ends (groups start on 128-token boundaries)
+        span = fmaxf(span, bmax - bmin);
+        bmin = bmax = carry;
+      }
     }
   }
   if (lane == 0) {
@@ -113,25 +124,36 @@ __global__ void __launch_bounds__(256) dgate_kernel(int T, GroupPlan gp, int BH,
   for (int w2 = 0; w2 < 8; ++w2) carry += wsum[w2];
   __syncthreads();
   const int s0 = gp.start(g), s1 = min(T, gp.start(g + 1));
-  for (int te = s1; te > s0; te -= 256) {
-    const int ts = max(s0, te - 256), n = te - ts;
-    float v = (int)threadIdx.x < n ? gx[(int64_t)bh * T + ts + threadIdx.x] : 0.f;
-    // reverse inclusive scan: thread i owns token ts + i
+  constexpr int kTiles = 4;  // tiles of 256 tokens whose loads are in flight together
+  for (int tb = s1; tb > s0; tb -= 256 * kTiles) {
+    float vs[kTiles];
 #pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const float y = __shfl_down_sync(0xffffffffu, v, d);
-      if (lane + d < 32) v += y;
+    for (int j = 0; j < kTiles; ++j) {
+      const int te = tb - 256 * j, ts = max(s0, te - 256);
+      vs[j] = te > s0 && (int)threadIdx.x < te - ts ? gx[(int64_t)bh * T + ts + threadIdx.x] : 0.f;
     }
-    if (lane == 0) wsum[warp] = v;  // lane 0 holds its warp's total
-    __syncthreads();
-    float later = 0.f, tile = 0.f;  // sums of the later warps of the tile, of the whole tile
-    for (int w2 = 0; w2 < 8; ++w2) {
-      tile += wsum[w2];
-      if (w2 > warp) later += wsum[w2];
+#pragma unroll
+    for (int j = 0; j < kTiles; ++j) {
+      const int te = tb - 256 * j, ts = max(s0, te - 256), n = te - ts;
+      if (te <= s0) break;  // block-uniform
+      float v = vs[j];
+      // reverse inclusive scan: thread i owns token ts + i
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const float y = __shfl_down_sync(0xffffffffu, v, d);
+        if (lane + d < 32) v += y;
+      }
+      if (lane == 0) wsum[warp] = v;  // lane 0 holds its warp's total
+      __syncthreads();
+      float later = 0.f, tile = 0.f;  // sums of the later warps of the tile, of the whole tile
+      for (int w2 = 0; w2 < 8; ++w2) {
+        tile += wsum[w2];
+        if (w2 > warp) later += wsum[w2];
+      }
+      if ((int)threadIdx.x < n) dlg[(int64_t)bh * T + ts + threadIdx.x] = v + later + carry;
+      carry += tile;
+      __syncthreads();  // wsum is rewritten by the next tile
     }
-    if ((int)threadIdx.x < n) dlg[(int64_t)bh * T + ts + threadIdx.x] = v + later + carry;
-    carry += tile;
-    __syncthreads();  // wsum is rewritten by the next tile
   }
 }
 

@@ -573,14 +573,27 @@ cudaError_t launch_vec_scan(const Problem &p, VecGroups gr, const float *X, cons
   return cudaGetLastError();
 }
 
-// Groups: as many (group, sequence) CTAs as the SMs hold at once (two per SM), the
-// groups at least 256 tokens long.
+// Groups: the count that minimises waves x (group length + a fixed cost of about 128
+// tokens per group: its state in and out, its share of the scans) x the walks a token
+// takes, with two CTAs per SM and groups of at least 256 tokens; the fewest groups
+// among equals.  One group per sequence walks each token 10 state-updates' worth
+// (forward 3, backward 7 in FMA-pipe operations per state element); a split adds
+// the forward's pass for the groups' own states and the backward's reverse
+// aggregates (14 with the checkpoint).
 VecGroups vec_groups(const Problem &p) {
-  const int64_t BH = (int64_t)p.B * p.H, sms = p.num_sms > 0 ? p.num_sms : 1;
-  int64_t G = 2 * sms / BH;
-  G = std::max<int64_t>(1, std::min<int64_t>(G, (p.T + 255) / 256));
+  const int64_t BH = (int64_t)p.B * p.H, slots = 2 * (int64_t)(p.num_sms > 0 ? p.num_sms : 1);
+  const int64_t gmax = std::max<int64_t>(1, std::min<int64_t>(p.T / 256, 8 * slots / BH + 1));
+  int64_t best = 1, best_cost = -1;
+  for (int64_t G = 1; G <= gmax; ++G) {
+    const int64_t L = (p.T + G - 1) / G, waves = (G * BH + slots - 1) / slots;
+    const int64_t cost = waves * (L + 128) * (G > 1 ? 14 : 10);
+    if (best_cost < 0 || cost < best_cost) {
+      best = G;
+      best_cost = cost;
+    }
+  }
   VecGroups gr;
-  gr.L = (int)((p.T + G - 1) / G);
+  gr.L = (int)((p.T + best - 1) / best);
   gr.G = gr.L > 0 ? (int)((p.T + gr.L - 1) / gr.L) : 1;
   return gr;
 }

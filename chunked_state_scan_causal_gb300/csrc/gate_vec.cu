@@ -165,19 +165,17 @@ struct VecStage {
 };
 
 // Forward walk of group g = blockIdx.y of sequence bh = blockIdx.x from its entering
-// state (init [G][BH][D][D], or zero), with the outputs o (OUT), the group's last state
-// (fin [G][BH][D][D], or none) and the sums of its log-gates per key dimension (gsum
-// [G][BH][D], or none).  The fp32 state lives in registers: warp w holds rows
+// state (init [G][BH][D][D], or zero), with the outputs o and the group's last state
+// (fin [G][BH][D][D], or none).  The fp32 state lives in registers: warp w holds rows
 // [w D/8, (w+1) D/8), lane l columns [l D/32, (l+1) D/32), as pairs of adjacent rows;
 // o_t = S_t^T q_t sums each thread's rows and then the warps' partial sums.
-template <int D, typename TIn, bool OUT>
+template <int D, typename TIn>
 __global__ void __launch_bounds__(kVecThreads, 2)
     vec_fwd_kernel(Problem p, VecGroups gr, const TIn *q, const TIn *k, const TIn *v, const float *lg, TIn *o,
-                   const float *init, float *fin, float *gsum) {
-  constexpr int RW = D / kVecWarps, CL = D / 32, ND = kVecChunk * D, NV = OUT ? 3 : 2;
+                   const float *init, float *fin) {
+  constexpr int RW = D / kVecWarps, CL = D / 32, ND = kVecChunk * D, NV = 3;
   extern __shared__ float sm[];
   float *sk = sm, *sv = sk + ND, *sq = sv + ND, *sa = sm + NV * ND, *part = sa + ND;
-  float *red = part + (OUT ? kVecWarps * ND : 0);
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, bh = blockIdx.x, gi = blockIdx.y;
   const int b = bh / p.H, h = bh % p.H;
   const int64_t BH = (int64_t)p.B * p.H, slot = (int64_t)gi * BH + bh;
@@ -195,16 +193,13 @@ __global__ void __launch_bounds__(kVecThreads, 2)
     }
 
   VecStage<D, TIn, NV> stage;
-  const TIn *const srcs[3] = {k, v, q};  // the first NV are staged
+  const TIn *const srcs[3] = {k, v, q};
   float *const dsts[3] = {sk, sv, sq};
-  float2 gs = make_float2(0.f, 0.f);  // the group's log-gate sums of this thread's two key dimensions
   stage.fetch(srcs, base, p.st, g, t0, 1, 0, t0, t1);
   for (int tc = t0; tc < t1; tc += kVecChunk) {
     const int nt = min(kVecChunk, t1 - tc);
     __syncthreads();  // the previous step is done with the staged vectors and the partial sums
-    const float2 add = stage.store(dsts, sa);
-    gs.x += add.x;
-    gs.y += add.y;
+    stage.store(dsts, sa);
     if (tc + kVecChunk < t1) stage.fetch(srcs, base, p.st, g, tc + kVecChunk, 1, 0, t0, t1);
     __syncthreads();
     for (int tt = 0; tt < nt; ++tt) {
@@ -220,26 +215,20 @@ __global__ void __launch_bounds__(kVecThreads, 2)
         const float2 a = ld2(ra + 2 * m), kk = ld2(rk + 2 * m);
 #pragma unroll
         for (int c = 0; c < CL; ++c) s[m][c] = fma2(a, s[m][c], mul2(kk, vv[c]));
-        if (OUT) {
-          const float2 qq = ld2(rq + 2 * m);
+        const float2 qq = ld2(rq + 2 * m);
 #pragma unroll
-          for (int c = 0; c < CL; ++c) acc[c] = fma2(qq, s[m][c], acc[c]);
-        }
+        for (int c = 0; c < CL; ++c) acc[c] = fma2(qq, s[m][c], acc[c]);
       }
-      if (OUT) {
 #pragma unroll
-        for (int c = 0; c < CL; ++c) part[(tt * kVecWarps + w) * D + c0 + c] = acc[c].x + acc[c].y;
-      }
+      for (int c = 0; c < CL; ++c) part[(tt * kVecWarps + w) * D + c0 + c] = acc[c].x + acc[c].y;
     }
-    if (OUT) {
-      __syncthreads();
-      for (int e = tid; e < nt * D; e += kVecThreads) {
-        const int tt = e / D, j = e % D;
-        float x = 0.f;
+    __syncthreads();
+    for (int e = tid; e < nt * D; e += kVecThreads) {
+      const int tt = e / D, j = e % D;
+      float x = 0.f;
 #pragma unroll
-        for (int u = 0; u < kVecWarps; ++u) x += part[(tt * kVecWarps + u) * D + j];
-        st_val(o + base + (int64_t)(tc + tt) * p.st + j, x);
-      }
+      for (int u = 0; u < kVecWarps; ++u) x += part[(tt * kVecWarps + u) * D + j];
+      st_val(o + base + (int64_t)(tc + tt) * p.st + j, x);
     }
   }
   if (fin) {
@@ -252,34 +241,28 @@ __global__ void __launch_bounds__(kVecThreads, 2)
         dst[D] = s[m][c].y;
       }
   }
-  if (gsum) {
-    // threads tid = u D/2 + n (u < 2 kVecThreads / D) hold key dimensions 2n and 2n + 1
-    reinterpret_cast<float2 *>(red)[tid] = gs;
-    __syncthreads();
-    if (tid < D / 2) {
-      float2 x = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int u = 0; u < 2 * kVecThreads / D; ++u) {
-        const float2 y = reinterpret_cast<const float2 *>(red)[tid + u * D / 2];
-        x.x += y.x;
-        x.y += y.y;
-      }
-      st2(gsum + slot * D + 2 * tid, x);
-    }
-  }
 }
 
-// The reverse aggregate of group g = blockIdx.y of sequence bh = blockIdx.x:
-//   W_g = sum_{t in g} diag(alpha_start .. alpha_t) q_t dO_t^T,
-// walked backward (A <- diag(alpha_t) (A + q_t dO_t^T)), into W [G][BH][D][D].  The
-// state lives in registers: warp w holds columns [w D/8, (w+1) D/8), lane l rows
-// [l D/32, (l+1) D/32), as pairs of adjacent columns.
-template <int D, typename TIn>
+// The state a group builds from zero, group g = blockIdx.y of sequence bh = blockIdx.x:
+//   forward (REV = false): S <- diag(alpha_t) S + k_t v_t^T over the group's tokens in
+//     order, i.e. U_g into out [G][BH][D][D], and the group's log-gate sums per key
+//     dimension into gsum [G][BH][D] (or none);
+//   reverse (REV = true): A <- diag(alpha_t) (A + q_t dO_t^T) from the group's last token
+//     back, i.e. W_g = sum_{t in g} diag(alpha_start .. alpha_t) q_t dO_t^T into out.
+// Both are S <- diag(a) S + x y^T (x = k, or alpha q), and two tokens u then w of the
+// walk fold into one update, S <- diag(a_u a_w) S + (a_w x_u) y_u^T + x_w y_w^T: three
+// packed operations per pair of state elements for two tokens instead of four.  Every
+// step walks all kVecChunk staged tokens; those outside the group are staged as x = y
+// = 0 and alpha = 1, which leave S exactly as it is.  The state lives in registers:
+// warp w holds columns [w D/8, (w+1) D/8), lane l rows [l D/32, (l+1) D/32), as pairs
+// of adjacent columns, so a row's products serve 16 (or 8) columns.
+template <int D, typename TIn, bool REV>
 __global__ void __launch_bounds__(kVecThreads, 2)
-    vec_ragg_kernel(Problem p, VecGroups gr, const TIn *q, const TIn *dO, const float *lg, float *W) {
+    vec_agg_kernel(Problem p, VecGroups gr, const TIn *x, const TIn *y, const float *lg, float *out, float *gsum) {
+  static_assert(kVecChunk % 2 == 0, "tokens are folded in pairs");
   constexpr int CW = D / kVecWarps, RL = D / 32, ND = kVecChunk * D;
   extern __shared__ float sm[];
-  float *sq = sm, *sg = sq + ND, *sa = sg + ND;
+  float *sx = sm, *sy = sx + ND, *sa = sy + ND, *red = sa + ND;
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, bh = blockIdx.x, gi = blockIdx.y;
   const int b = bh / p.H, h = bh % p.H;
   const int64_t BH = (int64_t)p.B * p.H, slot = (int64_t)gi * BH + bh;
@@ -287,42 +270,67 @@ __global__ void __launch_bounds__(kVecThreads, 2)
   const float *g = lg + (int64_t)bh * p.T * D;
   const int t0 = gr.start(gi), t1 = gr.end(gi, p.T), r0 = lane * RL, c0 = w * CW;
 
-  float2 s[RL][CW / 2];  // s[r][n] = (A[r0 + r][c0 + 2n], A[r0 + r][c0 + 2n + 1])
+  float2 s[RL][CW / 2];  // s[r][n] = (S[r0 + r][c0 + 2n], S[r0 + r][c0 + 2n + 1])
 #pragma unroll
   for (int r = 0; r < RL; ++r)
 #pragma unroll
     for (int n = 0; n < CW / 2; ++n) s[r][n] = make_float2(0.f, 0.f);
 
   VecStage<D, TIn, 2> stage;
-  const TIn *const srcs[2] = {q, dO};
-  float *const dsts[2] = {sq, sg};
-  // token tt of a step is time hi - 1 - tt
-  stage.fetch(srcs, base, p.st, g, t1 - 1, -1, 0, t0, t1);
-  for (int hi = t1; hi > t0; hi -= kVecChunk) {
-    const int nt = min(kVecChunk, hi - t0);
+  const TIn *const srcs[2] = {x, y};
+  float *const dsts[2] = {sx, sy};
+  float2 gs = make_float2(0.f, 0.f);  // this thread's two key dimensions' log-gate sums
+  // token tt of a step is time tb + tt (forward) or hi - 1 - tt (reverse)
+  const int nsteps = (t1 - t0 + kVecChunk - 1) / kVecChunk;
+  stage.fetch(srcs, base, p.st, g, REV ? t1 - 1 : t0, REV ? -1 : 1, 0, t0, t1);
+  for (int k = 0; k < nsteps; ++k) {
+    __syncthreads();  // the previous step is done with the staged vectors
+    const float2 add = stage.store(dsts, sa);
+    gs.x += add.x;
+    gs.y += add.y;
+    if (k + 1 < nsteps)
+      stage.fetch(srcs, base, p.st, g, REV ? t1 - 1 - (k + 1) * kVecChunk : t0 + (k + 1) * kVecChunk, REV ? -1 : 1, 0,
+                  t0, t1);
     __syncthreads();
-    stage.store(dsts, sa);
-    if (hi - kVecChunk > t0) stage.fetch(srcs, base, p.st, g, hi - kVecChunk - 1, -1, 0, t0, t1);
-    __syncthreads();
-    for (int tt = 0; tt < nt; ++tt) {
-      float2 ad[RL], qd[RL];
+#pragma unroll 1
+    for (int tt = 0; tt < kVecChunk; tt += 2) {
+      const float *au = sa + tt * D + r0, *aw = au + D, *xu = sx + tt * D + r0, *xw = xu + D;
+      float2 A[RL], Xu[RL], Xw[RL];
 #pragma unroll
       for (int r = 0; r < RL; ++r) {
-        ad[r] = dup2(sa[tt * D + r0 + r]);
-        qd[r] = dup2(sq[tt * D + r0 + r]);
+        const float a1 = au[r], a2 = aw[r];
+        const float x1 = REV ? a1 * xu[r] : xu[r], x2 = REV ? a2 * xw[r] : xw[r];
+        A[r] = dup2(a1 * a2);
+        Xu[r] = dup2(a2 * x1);
+        Xw[r] = dup2(x2);
       }
 #pragma unroll
       for (int n = 0; n < CW / 2; ++n) {
-        const float2 dp = ld2(sg + tt * D + c0 + 2 * n);
+        const float2 yu = ld2(sy + tt * D + c0 + 2 * n), yw = ld2(sy + (tt + 1) * D + c0 + 2 * n);
 #pragma unroll
-        for (int r = 0; r < RL; ++r) s[r][n] = mul2(ad[r], fma2(qd[r], dp, s[r][n]));
+        for (int r = 0; r < RL; ++r) s[r][n] = fma2(A[r], s[r][n], fma2(Xu[r], yu, mul2(Xw[r], yw)));
       }
     }
   }
 #pragma unroll
   for (int r = 0; r < RL; ++r)
 #pragma unroll
-    for (int n = 0; n < CW / 2; ++n) st2(W + slot * D * D + (int64_t)(r0 + r) * D + c0 + 2 * n, s[r][n]);
+    for (int n = 0; n < CW / 2; ++n) st2(out + slot * D * D + (int64_t)(r0 + r) * D + c0 + 2 * n, s[r][n]);
+  if (gsum) {
+    // threads tid = u D/2 + n (u < 2 kVecThreads / D) hold key dimensions 2n and 2n + 1
+    reinterpret_cast<float2 *>(red)[tid] = gs;
+    __syncthreads();
+    if (tid < D / 2) {
+      float2 z = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int u = 0; u < 2 * kVecThreads / D; ++u) {
+        const float2 v = reinterpret_cast<const float2 *>(red)[tid + u * D / 2];
+        z.x += v.x;
+        z.y += v.y;
+      }
+      st2(gsum + slot * D + 2 * tid, z);
+    }
+  }
 }
 
 // The scans across groups, one thread per (sequence, state element (i, j)), with the
@@ -524,28 +532,30 @@ __global__ void __launch_bounds__(kVecThreads, 2)
   }
 }
 
-template <int D, typename TIn, bool OUT>
+template <int D, typename TIn>
 cudaError_t launch_vec_fwd(const Problem &p, VecGroups gr, const void *q, const void *k, const void *v,
-                           const float *lg, void *o, const float *init, float *fin, float *gsum, cudaStream_t s) {
-  auto kern = vec_fwd_kernel<D, TIn, OUT>;
-  const size_t smem = vec_smem<D>(OUT ? 4 : 3, OUT);
+                           const float *lg, void *o, const float *init, float *fin, cudaStream_t s) {
+  auto kern = vec_fwd_kernel<D, TIn>;
+  const size_t smem = vec_smem<D>(4, true);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   TimedLaunch t(K_GATED_VEC_FWD, s);
   kern<<<dim3(p.B * p.H, gr.G), kVecThreads, smem, s>>>(p, gr, (const TIn *)q, (const TIn *)k, (const TIn *)v, lg,
-                                                        (TIn *)o, init, fin, gsum);
+                                                        (TIn *)o, init, fin);
   return cudaGetLastError();
 }
 
-template <int D, typename TIn>
-cudaError_t launch_vec_ragg(const Problem &p, VecGroups gr, const void *q, const void *dO, const float *lg, float *W,
-                            cudaStream_t s) {
-  auto kern = vec_ragg_kernel<D, TIn>;
+// The groups' own states from zero (forward: x = k, y = v, with the log-gate sums) or
+// their reverse aggregates (x = q, y = dO).
+template <int D, typename TIn, bool REV>
+cudaError_t launch_vec_agg(const Problem &p, VecGroups gr, const void *x, const void *y, const float *lg, float *out,
+                           float *gsum, cudaStream_t s) {
+  auto kern = vec_agg_kernel<D, TIn, REV>;
   const size_t smem = vec_smem<D>(3, false);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  TimedLaunch t(K_GATED_VEC_BWD, s);
-  kern<<<dim3(p.B * p.H, gr.G), kVecThreads, smem, s>>>(p, gr, (const TIn *)q, (const TIn *)dO, lg, W);
+  TimedLaunch t(REV ? K_GATED_VEC_BWD : K_GATED_VEC_FWD, s);
+  kern<<<dim3(p.B * p.H, gr.G), kVecThreads, smem, s>>>(p, gr, (const TIn *)x, (const TIn *)y, lg, out, gsum);
   return cudaGetLastError();
 }
 
@@ -630,16 +640,16 @@ template <int D, typename TIn>
 cudaError_t vec_fwd_path(const Problem &p, const void *q, const void *k, const void *v, const float *lg, void *o,
                          const float *init, float *final_state, char *ws, char *ckpt, cudaStream_t s) {
   const VecGroups gr = vec_groups(p);
-  if (gr.G == 1) return launch_vec_fwd<D, TIn, true>(p, gr, q, k, v, lg, o, init, final_state, nullptr, s);
+  if (gr.G == 1) return launch_vec_fwd<D, TIn>(p, gr, q, k, v, lg, o, init, final_state, s);
   const VecLayout w = vec_layout(p, false);
   const VecCkpt c = vec_ckpt_layout(p);
   float *agg = reinterpret_cast<float *>(ws + w.agg);
   float *states = reinterpret_cast<float *>(ckpt ? ckpt + c.states : ws + w.states);
   float *gsum = reinterpret_cast<float *>(ckpt ? ckpt + c.gsum : ws + w.gsum);
   // the groups' own states from zero and their gate sums, the scan, the outputs
-  cudaError_t e = launch_vec_fwd<D, TIn, false>(p, gr, q, k, v, lg, nullptr, nullptr, agg, gsum, s);
+  cudaError_t e = launch_vec_agg<D, TIn, false>(p, gr, k, v, lg, agg, gsum, s);
   if (e == cudaSuccess) e = launch_vec_scan(p, gr, agg, gsum, init, states, final_state, false, s);
-  if (e == cudaSuccess) e = launch_vec_fwd<D, TIn, true>(p, gr, q, k, v, lg, o, states, nullptr, nullptr, s);
+  if (e == cudaSuccess) e = launch_vec_fwd<D, TIn>(p, gr, q, k, v, lg, o, states, nullptr, s);
   return e;
 }
 
@@ -660,14 +670,14 @@ cudaError_t vec_bwd_path(const Problem &p, const void *q, const void *k, const v
     gsum = reinterpret_cast<const float *>(ckpt + c.gsum);
   } else {
     float *st = reinterpret_cast<float *>(ws + w.states), *gs = reinterpret_cast<float *>(ws + w.gsum);
-    e = launch_vec_fwd<D, TIn, false>(p, gr, q, k, v, lg, nullptr, nullptr, agg, gs, s);
+    e = launch_vec_agg<D, TIn, false>(p, gr, k, v, lg, agg, gs, s);
     if (e == cudaSuccess) e = launch_vec_scan(p, gr, agg, gs, init, st, nullptr, false, s);
     states = st;
     gsum = gs;
   }
   // reverse aggregates and the gradients arriving at every group's last state; then
   // every group's backward
-  if (e == cudaSuccess) e = launch_vec_ragg<D, TIn>(p, gr, q, dO, lg, agg, s);
+  if (e == cudaSuccess) e = launch_vec_agg<D, TIn, true>(p, gr, q, dO, lg, agg, nullptr, s);
   if (e == cudaSuccess) e = launch_vec_scan(p, gr, agg, gsum, d_final, dfin, nullptr, true, s);
   if (e == cudaSuccess) e = launch_vec_bwd<D, TIn>(p, gr, q, k, v, dO, lg, states, dfin, dq, dk, dv, dlg, dinit, s);
   return e;

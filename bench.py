@@ -858,8 +858,8 @@ def run_gated_vec(args):
     token: the sequential recurrence's own arithmetic, forward 5 (the update a s + k v, 3;
     the output's q s, 2) and backward 12 (the forward states again, 3, with dq's S dO, 2;
     the reverse update, 3, with dk's R v and dv's R^T k, 2 each).  The group split's extra
-    passes (the forward's group states from zero, 3; the backward's reverse aggregates, 3)
-    are executed but not credited."""
+    passes (the forward's group states from zero and the backward's reverse aggregates,
+    2.5 each: two tokens folded into one update of 5 FLOP) are executed but not credited."""
     import torch
     import chunked_state_scan_causal_gb300 as la
     from chunked_state_scan_causal_gb300 import build, inputs
@@ -905,7 +905,7 @@ def run_gated_vec(args):
     launches = sum(n for n, _ in timing.values()) // min(steps, 5)
     units = B * H * T
     flops = 17 * d * d * units
-    executed = 23 * d * d * units  # with the split's two extra passes
+    executed = 22 * d * d * units  # with the split's two extra passes
     sm = torch.cuda.get_device_properties(dev).multi_processor_count
     mhz = 2070.0
     peak = sm * 128 * 2 * mhz * 1e6 / 1e12  # FP32 FMA lanes x 2 FLOP x the maximum SM clock

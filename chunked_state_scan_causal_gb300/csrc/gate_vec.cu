@@ -2,10 +2,10 @@
 // dimension (the vector form of the data-dependent gate; "Gated Linear
 // Attention ..." on the LASP-2 page's related list),
 //   S_t = diag(alpha_t) S_{t-1} + k_t v_t^T,   o_t = S_t^T q_t,   alpha_t = exp(log_gate_t).
-// A CTA walks one chunk group of one (batch, head) sequence token by token with
-// the fp32 state in shared memory (row stride d + 1: row walks and column walks
-// are free of bank conflicts).  Row i of the state only ever sees key dimension
-// i's gates, so the groups are joined by scans whose multipliers are per row:
+// A CTA walks one chunk group of one (batch, head) sequence with the fp32 state in
+// registers (each of its 256 threads holds a tile of it), staging the tokens'
+// vectors in shared memory eight at a time.  Row i of the state only ever sees key
+// dimension i's gates, so the groups are joined by scans whose multipliers are per row:
 //   forward:  S_{g+1} = diag(A_g) S_g + U_g,   A_g[i] = prod of group g's gates of dimension i,
 //             U_g the group's state walked from zero;
 //   backward: Dfin_{g-1} = W_g + diag(A_g) Dfin_g, Dfin_{G-1} = the gradient at the final state,

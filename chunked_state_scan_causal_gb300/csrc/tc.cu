@@ -897,6 +897,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t id_qs = idesc_bf16(128, 128, false, true);   // Q S,  P V
       const uint32_t id_kv = idesc_bf16(128, 128, true, true);    // K^T V
       const uint32_t id_xq = idesc_bf16(128, 128, true, true);    // X^T Q
+      // steps of 16 over the head dimension: with d = 64 (run zero-padded) the last
+      // four multiply zero columns only, so they are skipped
+      const uint32_t nkd = P.half_out ? 4u : 8u;
       int blk = 0, ia = 0;  // ia: items that accumulated their group aggregate (phases of B_WEMPTY)
       bool ok = true;
       for (int k = 0, item; ok; ++k) {
@@ -919,7 +922,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
-          for (uint32_t ks = 0; ks < 8; ++ks) mma_ss_warp(tP, desc_kmajor(Q, ks), desc_kmajor(K, ks), id_qk, ks > 0);
+          for (uint32_t ks = 0; ks < 8; ++ks)
+            if (ks < nkd) mma_ss_warp(tP, desc_kmajor(Q, ks), desc_kmajor(K, ks), id_qk, ks > 0);
           mma_commit_warp(&bar[B_PFULL]);
           // inter-block term: O = Q S (its own accumulator with a decay, unless weighted)
           ok = mbar_wait_w(&bar[B_PRE], blk & 1, &abort_flag, P.status, detail) &&
@@ -928,7 +932,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
 #pragma unroll
           for (uint32_t ks = 0; ks < 8; ++ks)
-            mma_ss_warp((DECAY && !wtd) ? tOi : tO, desc_kmajor(Q, ks), desc_mnmajor(sSh, ks), id_qs, ks > 0);
+            if (ks < nkd)
+              mma_ss_warp((DECAY && !wtd) ? tOi : tO, desc_kmajor(Q, ks), desc_mnmajor(sSh, ks), id_qs, ks > 0);
           if (aggw) {
             // group aggregate: W += X'^T Q (the previous group's W must have been read out;
             // with a decay X' has its rows weighted by lambda^{s - start + 1})
@@ -1457,6 +1462,9 @@ __global__ void __launch_bounds__(kDualThreads, 1)
       const uint32_t id_kk = idesc_bf16(128, 128, false, false);  // A K-major, B K-major
       const uint32_t id_km = idesc_bf16(128, 128, false, true);   // A K-major (or TMEM), B MN-major
       const uint32_t id_mm = idesc_bf16(128, 128, true, true);    // A MN-major, B MN-major
+      // steps of 16 over the head dimension (d = 64 runs zero-padded: the last four
+      // multiply zero columns only and are skipped)
+      const uint32_t nkd = P.half_out ? 4u : 8u;
       int blk = 0;
       bool ok = true;
       auto wait = [&](int idx, int parity) {
@@ -1495,14 +1503,16 @@ __global__ void __launch_bounds__(kDualThreads, 1)
           if (!(ok = full(0) && (wq ? wait(D_DS + wb, wp) : full(1)))) break;
           tc_fence_after();
 #pragma unroll
-          for (uint32_t ks = 0; ks < 8; ++ks) mma_ss_warp(tP, desc_kmajor(K, ks), desc_kmajor(Q, ks), id_kk, ks > 0);
+          for (uint32_t ks = 0; ks < 8; ++ks)
+            if (ks < nkd) mma_ss_warp(tP, desc_kmajor(K, ks), desc_kmajor(Q, ks), id_kk, ks > 0);
           mma_commit_warp(&bar[D_PFULL]);
           // dv = K' R   (R from the bf16 state tile, MN-major)
           ok = (!DECAY || wtd || wait(D_KS + wb, wp)) && wait(D_PRE, blk) && (blk == 0 || wait(D_O1EMPTY, blk - 1));
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
-          for (uint32_t ks = 0; ks < 8; ++ks) mma_ss_warp(tO1, desc_kmajor(K, ks), desc_mnmajor(sSh, ks), id_km, ks > 0);
+          for (uint32_t ks = 0; ks < 8; ++ks)
+            if (ks < nkd) mma_ss_warp(tO1, desc_kmajor(K, ks), desc_mnmajor(sSh, ks), id_km, ks > 0);
           release(0);
           if (early_r) {
             // R += Q^T dO' (the state tile is rewritten only after SFULL, below)
@@ -1521,7 +1531,8 @@ __global__ void __launch_bounds__(kDualThreads, 1)
           if (!(ok = full(3))) break;
           tc_fence_after();
 #pragma unroll
-          for (uint32_t ks = 0; ks < 8; ++ks) mma_ss_warp(tP, desc_kmajor(V, ks), desc_kmajor(DO, ks), id_kk, ks > 0);
+          for (uint32_t ks = 0; ks < 8; ++ks)
+            if (ks < nkd) mma_ss_warp(tP, desc_kmajor(V, ks), desc_kmajor(DO, ks), id_kk, ks > 0);
           mma_commit_warp(&bar[D_PFULL]);
           if (early_r) release(2);
           // dk = V' R^T  (the state tile read K-major)
@@ -1529,7 +1540,8 @@ __global__ void __launch_bounds__(kDualThreads, 1)
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
-          for (uint32_t ks = 0; ks < 8; ++ks) mma_ss_warp(tO2, desc_kmajor(V, ks), desc_kmajor(sSh, ks), id_kk, ks > 0);
+          for (uint32_t ks = 0; ks < 8; ++ks)
+            if (ks < nkd) mma_ss_warp(tO2, desc_kmajor(V, ks), desc_kmajor(sSh, ks), id_kk, ks > 0);
           release(3);
           if (!early_r) {
             // R += Q^T dO'  (dO rows weighted together with V's)

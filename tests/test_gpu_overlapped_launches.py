@@ -70,3 +70,23 @@ def test_back_to_back_steps_equal_an_isolated_step(workload, T):
         assert la.device_status(b["wsf"]) == la.OK and la.device_status(b["wsb"]) == la.OK
         for got, want in zip(_outs(b), _outs(ref)):
             assert torch.equal(got, want)
+
+
+def test_many_steps_at_full_size():
+    """500 benchmark steps (B2 H16 T65536) back to back on one stream: the bounded waits
+    never give up under the overlapped launches, and the last step's outputs are bitwise
+    those of a step run alone."""
+    cfg = dict(inputs.WORKLOADS[3])
+    dev = torch.device("cuda", 0)
+    x = {w: inputs.make(cfg, w).to(dev) for w in ("q", "k", "v", "dO")}
+    s = torch.cuda.current_stream(dev)
+    ref = _buffers(x, None, False)
+    _step(x, ref, None, False, s)
+    torch.cuda.synchronize()
+    b = _buffers(x, None, False)
+    for _ in range(500):
+        _step(x, b, None, False, s)
+    torch.cuda.synchronize()
+    assert la.device_status(b["wsf"]) == la.OK and la.device_status(b["wsb"]) == la.OK
+    for got, want in zip(_outs(b), _outs(ref)):
+        assert torch.equal(got, want)

@@ -7,6 +7,7 @@ Tolerances: fp32 inputs 1e-4 of max|ref| (one fp32 walk per sequence); bf16 inpu
 log-gate gradient and states 1e-3.  Cases: d = 64 and 128, several heads, ragged
 lengths, an initial state and a final-state gradient, padded strides, shared gates
 (every dimension the token's gate) against the per-token gated entry points, T = 0,
+lengths 1 to 16 at the edges of the 8-token staging and the two-token updates,
 sequences long enough to be cut into chunk groups joined by per-row scans, and two
 whole heads of the full-size per-dimension gated workload.
 """
@@ -183,3 +184,25 @@ def test_gated_vec_checkpoint_equals_recompute(d, dtype, B, H, T):
     for name, a, b in zip(("o", "final", "dq", "dk", "dv", "d_log_gate", "d_init"), (o1, f1) + tuple(g1),
                           (o2, f2) + tuple(g2)):
         assert torch.equal(a, b), name
+
+
+@pytest.mark.parametrize("T", [1, 2, 3, 7, 8, 9, 15, 16])
+@pytest.mark.parametrize("d,dtype", [(128, torch.bfloat16), (64, torch.float32)])
+def test_gated_vec_short_sequences(T, d, dtype):
+    """Lengths at the edges of the 8-token staging and of the two-token updates (one
+    group per sequence), with an initial state and a final-state gradient."""
+    B, H = 2, 2
+    q, k, v, dO, lg, init, D = case(100 + T + d, B, H, T, d, dtype, lo=-0.5)
+    cu = [x.cuda() for x in (q, k, v, dO, lg, init, D)]
+    o, fin = la.fwd_gated_vec(cu[0], cu[1], cu[2], cu[4], init_state=cu[5], want_final=True)
+    dq, dk, dv, dlg, dinit = la.bwd_gated_vec(cu[0], cu[1], cu[2], cu[3], cu[4], init_state=cu[5], d_final=cu[6],
+                                              want_dinit=True)
+    torch.cuda.synchronize()
+    n = lambda x: x.double().numpy()
+    ro, rfin = oracle.fwd_gated_vec(n(q), n(k), n(v), n(lg), init=n(init))
+    rq, rk, rv, rlg, rinit = oracle.bwd_gated_vec(n(q), n(k), n(v), n(dO), n(lg), init=n(init), d_final=n(D))
+    tol = 1e-4 if dtype == torch.float32 else 1e-2
+    stol = 1e-4 if dtype == torch.float32 else 1e-3
+    for name, got, ref, t in (("o", o, ro, tol), ("final", fin, rfin, stol), ("dq", dq, rq, tol), ("dk", dk, rk, tol),
+                              ("dv", dv, rv, tol), ("d_log_gate", dlg, rlg, stol), ("d_init", dinit, rinit, stol)):
+        assert rel(got, ref) < t, (name, rel(got, ref))

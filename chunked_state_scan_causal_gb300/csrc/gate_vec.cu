@@ -102,6 +102,37 @@ __device__ __forceinline__ float lanes_reduce_scatter(float (&x)[N], int lane) {
   return x[0];
 }
 
+// lanes_reduce_scatter for values held in a lane-dependent order of 4-value blocks:
+// slot block b of lane l holds column block b ^ ((l >> (5 - log2 NB)) & (NB - 1)), NB = N / 4.
+// In that order the half a lane keeps in each of the first log2 NB halving steps is
+// always its first half (the partner, whose block mask differs in that step's bit,
+// holds the same columns in its second half), so those steps need no selects; the
+// last two steps split a block as lanes_reduce_scatter does.  Same result, same
+// column per lane: l >> (5 - log2 N).
+template <int N>
+__device__ __forceinline__ float lanes_reduce_scatter_blocked(float (&x)[N], int lane) {
+  static_assert(N == 8 || N == 16, "two or four blocks of four values");
+  constexpr int kBlockSteps = N == 16 ? 2 : 1;
+#pragma unroll
+  for (int st = 0, half = N / 2, off = 16; st < kBlockSteps; ++st, half /= 2, off /= 2) {
+#pragma unroll
+    for (int m = 0; m < half; ++m) x[m] += __shfl_xor_sync(0xffffffffu, x[m + half], off);
+  }
+  constexpr int kOff = 16 >> kBlockSteps;  // then 4 values left, as in the plain form
+#pragma unroll
+  for (int half = 2, off = kOff; half >= 1; half /= 2, off /= 2) {
+    const bool up = lane & off;
+#pragma unroll
+    for (int m = 0; m < half; ++m) {
+      const float send = up ? x[m] : x[m + half], keep = up ? x[m + half] : x[m];
+      x[m] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+    }
+  }
+#pragma unroll
+  for (int off = kOff / 4; off >= 1; off /= 2) x[0] += __shfl_xor_sync(0xffffffffu, x[0], off);
+  return x[0];
+}
+
 // shared memory of a walk: `vectors` staged vectors of kVecChunk x D, the per-warp
 // partial sums [kVecChunk][kVecWarps][D] (when it reduces across warps) and kVecThreads pairs
 template <int D>
@@ -375,13 +406,18 @@ __global__ void __launch_bounds__(kVecThreads, 2)
   const float *g = lg + (int64_t)bh * p.T * D;
   float *dg = dlg + (int64_t)bh * p.T * D;
   const int t0 = gr.start(gi), t1 = gr.end(gi, p.T), r0 = lane * RL, c0 = w * CW;
+  // this lane's order of its columns: pair n of the slots is column pair pc(n), the
+  // 4-column blocks permuted by the lane's bits the dv reduction splits first
+  constexpr int NB = CW / 4, kLogNB = NB == 4 ? 2 : 1;
+  const int mb = (lane >> (5 - kLogNB)) & (NB - 1);
+  auto pc = [&](int n) { return 2 * ((n >> 1) ^ mb) + (n & 1); };
 
-  float2 s[RL][CW / 2];  // s[r][n] = (S[r0 + r][c0 + 2n], S[r0 + r][c0 + 2n + 1])
+  float2 s[RL][CW / 2];  // s[r][n] = (S[r0 + r][c0 + 2 pc(n)], S[r0 + r][c0 + 2 pc(n) + 1])
 #pragma unroll
   for (int r = 0; r < RL; ++r)
 #pragma unroll
     for (int n = 0; n < CW / 2; ++n)
-      s[r][n] = init ? ld2(init + slot * D * D + (int64_t)(r0 + r) * D + c0 + 2 * n) : make_float2(0.f, 0.f);
+      s[r][n] = init ? ld2(init + slot * D * D + (int64_t)(r0 + r) * D + c0 + 2 * pc(n)) : make_float2(0.f, 0.f);
 
   VecStage<D, TIn, 4> stage;
   const TIn *const srcs[4] = {q, k, v, dO};
@@ -405,7 +441,7 @@ __global__ void __launch_bounds__(kVecThreads, 2)
       }
 #pragma unroll
       for (int n = 0; n < CW / 2; ++n) {
-        const float2 vp = ld2(sv + tt * D + c0 + 2 * n), dp = ld2(sg + tt * D + c0 + 2 * n);
+        const float2 vp = ld2(sv + tt * D + c0 + 2 * pc(n)), dp = ld2(sg + tt * D + c0 + 2 * pc(n));
 #pragma unroll
         for (int r = 0; r < RL; ++r) {
           s[r][n] = fma2(ad[r], s[r][n], mul2(kd[r], vp));
@@ -436,7 +472,7 @@ __global__ void __launch_bounds__(kVecThreads, 2)
 #pragma unroll
       for (int n = 0; n < CW / 2; ++n) {
         const float2 df =
-            dfin ? ld2(dfin + slot * D * D + (int64_t)(r0 + r) * D + c0 + 2 * n) : make_float2(0.f, 0.f);
+            dfin ? ld2(dfin + slot * D * D + (int64_t)(r0 + r) * D + c0 + 2 * pc(n)) : make_float2(0.f, 0.f);
         acc[r] = fma2(df, s[r][n], acc[r]);
         s[r][n] = df;
       }
@@ -474,7 +510,7 @@ __global__ void __launch_bounds__(kVecThreads, 2)
       float dva[CW];
 #pragma unroll
       for (int n = 0; n < CW / 2; ++n) {
-        const float2 vp = ld2(sv + tt * D + c0 + 2 * n), dp = ld2(sg + tt * D + c0 + 2 * n);
+        const float2 vp = ld2(sv + tt * D + c0 + 2 * pc(n)), dp = ld2(sg + tt * D + c0 + 2 * pc(n));
         float2 col = make_float2(0.f, 0.f);
 #pragma unroll
         for (int r = 0; r < RL; ++r) {
@@ -487,7 +523,7 @@ __global__ void __launch_bounds__(kVecThreads, 2)
       }
 #pragma unroll
       for (int r = 0; r < RL; ++r) part[(tt * kVecWarps + w) * D + r0 + r] = dka[r].x + dka[r].y;
-      const float x = lanes_reduce_scatter<CW>(dva, lane);
+      const float x = lanes_reduce_scatter_blocked<CW>(dva, lane);
       if ((lane & ((1 << kLowBits) - 1)) == 0)
         st_val(dv + base + (int64_t)t * p.st + c0 + (lane >> kLowBits), x);
     }
@@ -527,7 +563,7 @@ __global__ void __launch_bounds__(kVecThreads, 2)
       const float a0 = t1 > t0 ? expf(g[(int64_t)t0 * D + r0 + r]) : 1.f;
 #pragma unroll
       for (int n = 0; n < CW / 2; ++n)
-        st2(dinit + (int64_t)bh * D * D + (int64_t)(r0 + r) * D + c0 + 2 * n, mul2(dup2(a0), s[r][n]));
+        st2(dinit + (int64_t)bh * D * D + (int64_t)(r0 + r) * D + c0 + 2 * pc(n), mul2(dup2(a0), s[r][n]));
     }
   }
 }
